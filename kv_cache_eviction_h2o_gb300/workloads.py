@@ -1,0 +1,197 @@
+"""Seeded synthetic workloads for the budgeted-KV decode path.
+
+This module is the one piece shared by the CUDA path's callers and the CPU
+oracle's callers: it draws the inputs and nothing else.  It holds none of the
+method's arithmetic (no attention, no scores, no eviction, no hashing).
+
+Every array is drawn per (batch*head) unit from ``numpy.random.PCG64`` keyed by
+``SeedSequence([seed, tag, unit])``, so any subset of units can be generated
+alone and agrees bit for bit with the full tensor.  Half-precision workloads
+are rounded to bfloat16 (round to nearest even) here, so the device path and
+the oracle read identical values.
+
+Workload shapes follow the model shapes the H2O review page evaluates on
+(OPT-6.7B / OPT-30B at a ~20% KV budget, 主な発見 / 提案手法 sections; LLaMA for
+long context) with synthetic data in place of model activations.
+"""
+from dataclasses import dataclass, field
+from typing import Optional, Sequence
+
+import numpy as np
+
+TAG_PROMPT = 1
+TAG_DECODE = 2
+TAG_SHARED = 3
+TAG_LSH = 4
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    batch: int
+    heads: int
+    head_dim: int
+    prompt: int
+    steps: int
+    budget: int
+    heavy: int
+    recent: int
+    dtype: str            # "f32" or "bf16"
+    seed: int
+    structure: tuple = field(default=())
+    lsh: bool = False
+    lsh_seed: int = 4
+
+    @property
+    def units(self) -> int:
+        return self.batch * self.heads
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / float(np.sqrt(self.head_dim))
+
+    @property
+    def elem_bytes(self) -> int:
+        return 2 if self.dtype == "bf16" else 4
+
+
+WORKLOADS = {
+    # fp32, 1 x 4 heads, d 64, prompt 128, 64 steps, budget 32 = 16 heavy + 16 recent,
+    # rank-2 shared key component of scale 2.
+    "tiny": Workload("tiny", 1, 4, 64, 128, 64, 32, 16, 16, "f32", 0, ("rank", 2, 2.0)),
+    # OPT-6.7B-shaped layer: 8 x 32 heads, d 128, prompt 2048, 256 steps,
+    # budget 410 = 205 heavy + 205 recent, rank-4 shared key component of scale 2.
+    "opt-6.7b": Workload("opt-6.7b", 8, 32, 128, 2048, 256, 410, 205, 205, "bf16", 1,
+                         ("rank", 4, 2.0)),
+    # OPT-30B-shaped layer: 64 x 56 heads, prompt 512, 1024 steps, budget 308 = 154 + 154;
+    # 1% of key positions scaled 4x along one shared unit direction.
+    "opt-30b": Workload("opt-30b", 64, 56, 128, 512, 1024, 308, 154, 154, "bf16", 2,
+                        ("outlier_dir", 0.01, 4.0)),
+    # Llama-7B-shaped long context: 1 x 32 heads, prompt 32768, 128 steps,
+    # budget 4096 = 2048 + 2048; positions 0..3 and 0.5% of positions get key norm x6.
+    "llama-7b-32k": Workload("llama-7b-32k", 1, 32, 128, 32768, 128, 4096, 2048, 2048, "bf16", 3,
+                             ("sink_norm", 4, 0.005, 6.0)),
+    # HashEvict on the OPT-6.7B shapes and inputs: 32-bit sign projections through a
+    # seeded N(0,1) 128 x 32 matrix, recent window 205.
+    "hashevict-opt-6.7b": Workload("hashevict-opt-6.7b", 8, 32, 128, 2048, 256, 410, 205, 205,
+                                   "bf16", 1, ("rank", 4, 2.0), lsh=True, lsh_seed=4),
+}
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bfloat16 (ties to even); the result
+    is float32 holding exactly representable bfloat16 values."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    bias = ((u >> 16) & 1) + 0x7FFF
+    r = ((u + bias) & 0xFFFF0000).astype(np.uint32)
+    return r.view(np.float32)
+
+
+def _rng(seed: int, tag: int, index: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tag, index])))
+
+
+def _shared_direction(w: Workload) -> np.ndarray:
+    g = _rng(w.seed, TAG_SHARED, 0)
+    u = g.standard_normal(w.head_dim)
+    return u / np.linalg.norm(u)
+
+
+def _unit_basis(w: Workload, unit: int, rank: int) -> np.ndarray:
+    g = _rng(w.seed, TAG_SHARED, 1 + unit)
+    a = g.standard_normal((w.head_dim, rank))
+    qm, _ = np.linalg.qr(a)
+    return qm.T.copy()          # [rank, d] orthonormal rows
+
+
+def _structure_keys(w: Workload, unit: int, K: np.ndarray, g: np.random.Generator,
+                    first_pos: int) -> np.ndarray:
+    """Apply the workload's key structure to K [n, d] (float64) in place."""
+    if not w.structure:
+        return K
+    kind = w.structure[0]
+    n = K.shape[0]
+    if kind == "rank":
+        rank, amp = int(w.structure[1]), float(w.structure[2])
+        basis = _unit_basis(w, unit, rank)
+        coef = g.standard_normal((n, rank))
+        K += amp * (coef @ basis)
+    elif kind == "outlier_dir":
+        frac, factor = float(w.structure[1]), float(w.structure[2])
+        u = _shared_direction(w)
+        mask = g.random(n) < frac
+        proj = K[mask] @ u
+        K[mask] += (factor - 1.0) * proj[:, None] * u[None, :]
+    elif kind == "sink_norm":
+        nsink, frac, factor = int(w.structure[1]), float(w.structure[2]), float(w.structure[3])
+        mask = g.random(n) < frac
+        posn = first_pos + np.arange(n)
+        mask |= posn < nsink
+        K[mask] *= factor
+    else:
+        raise ValueError(kind)
+    return K
+
+
+def _finish(w: Workload, x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    return round_bf16(x) if w.dtype == "bf16" else x
+
+
+def prompt_unit(w: Workload, unit: int, prompt: Optional[int] = None):
+    """Prompt Q, K, V of one unit, each [T, d] float32."""
+    T = w.prompt if prompt is None else prompt
+    g = _rng(w.seed, TAG_PROMPT, unit)
+    d = w.head_dim
+    Q = g.standard_normal((T, d), dtype=np.float32).astype(np.float64)
+    K = g.standard_normal((T, d), dtype=np.float32).astype(np.float64)
+    V = g.standard_normal((T, d), dtype=np.float32).astype(np.float64)
+    K = _structure_keys(w, unit, K, g, 0)
+    return _finish(w, Q), _finish(w, K), _finish(w, V)
+
+
+def decode_unit(w: Workload, unit: int, steps: Optional[int] = None,
+                prompt: Optional[int] = None):
+    """Decode-step q, k, v of one unit, each [S, d] float32; the new keys get
+    the same structure as the prompt keys."""
+    S = w.steps if steps is None else steps
+    T = w.prompt if prompt is None else prompt
+    g = _rng(w.seed, TAG_DECODE, unit)
+    d = w.head_dim
+    q = g.standard_normal((S, d), dtype=np.float32).astype(np.float64)
+    k = g.standard_normal((S, d), dtype=np.float32).astype(np.float64)
+    v = g.standard_normal((S, d), dtype=np.float32).astype(np.float64)
+    k = _structure_keys(w, unit, k, g, T)
+    return _finish(w, q), _finish(w, k), _finish(w, v)
+
+
+def lsh_matrix(w: Workload) -> np.ndarray:
+    """HashEvict projection matrix W [d, 32] float32, N(0, 1)."""
+    g = _rng(w.lsh_seed, TAG_LSH, 0)
+    return g.standard_normal((w.head_dim, 32), dtype=np.float32)
+
+
+def generate(w: Workload, units: Optional[Sequence[int]] = None,
+             steps: Optional[int] = None, prompt: Optional[int] = None):
+    """Inputs for the listed units (default all): dict with Q, K, V
+    [U, T, d] and q, k, v [S, U, d] (float32) plus W for LSH workloads."""
+    if units is None:
+        units = range(w.units)
+    units = list(units)
+    S = w.steps if steps is None else steps
+    T = w.prompt if prompt is None else prompt
+    d = w.head_dim
+    U = len(units)
+    out = {
+        "Q": np.empty((U, T, d), np.float32), "K": np.empty((U, T, d), np.float32),
+        "V": np.empty((U, T, d), np.float32), "q": np.empty((S, U, d), np.float32),
+        "k": np.empty((S, U, d), np.float32), "v": np.empty((S, U, d), np.float32),
+    }
+    for i, u in enumerate(units):
+        out["Q"][i], out["K"][i], out["V"][i] = prompt_unit(w, u, T)
+        if S > 0:
+            out["q"][:, i], out["k"][:, i], out["v"][:, i] = decode_unit(w, u, S, T)
+    if w.lsh:
+        out["W"] = lsh_matrix(w)
+    return out

@@ -1,0 +1,205 @@
+"""CPU oracle for budgeted-KV decode attention with H2O heavy-hitter eviction
+and the HashEvict LSH variant.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, the package smoke check and
+the benchmark's CPU-baseline leg, never by the product path.  The arithmetic
+lives in ``oracle.c`` (plain C, fp64); this module only marshals numpy arrays
+through ctypes.  Every array is C-contiguous; floating inputs are float64
+holding the exact values the device path reads (bf16/fp32 upcast), the LSH
+projection matrix is float32.
+
+Shapes use U = batch*heads independent units:
+  prompt Q, K, V  [U, T, d]      decode q, k, v  [U, d]
+  cache K, V      [U, B, d]      score [U, B]  pos [U, B]  occ [U]
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+_f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+_f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+_i32p = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
+_u32p = np.ctypeslib.ndpointer(dtype=np.uint32, flags="C_CONTIGUOUS")
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_d = ctypes.c_double
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        # ORACLE_LIB lets the mutation tests load a deliberately broken copy
+        path = os.environ.get("ORACLE_LIB") or _build.build()
+        L = ctypes.CDLL(path)
+        L.oracle_set_threads.argtypes = [_i]
+        L.oracle_get_threads.restype = _i
+        L.oracle_prefill_scores.argtypes = [_i, _i, _i, _d, _f64p, _f64p, _f64p, _f64p, _f64p]
+        L.oracle_select.argtypes = [_i, _i, _i, _i, _f64p, _i32p, _vp]
+        L.oracle_select.restype = _i
+        L.oracle_build_cache.argtypes = [_i, _i, _i, _i, _i32p, _i32p, _f64p, _f64p, _f64p,
+                                         _f64p, _f64p, _f64p, _i32p, _i32p]
+        L.oracle_h2o_prefill.argtypes = [_i, _i, _i, _i, _i, _i, _d, _f64p, _f64p, _f64p,
+                                         _f64p, _f64p, _f64p, _i32p, _i32p, _vp, _vp, _vp]
+        L.oracle_h2o_decode_step.argtypes = [_i, _i, _i, _i, _d, _i, _f64p, _f64p, _f64p,
+                                             _i32p, _i32p, _f64p, _f64p, _f64p, _f64p,
+                                             _vp, _vp, _vp, _vp]
+        L.oracle_lsh_code.argtypes = [_i, _f64p, _f32p]
+        L.oracle_lsh_code.restype = ctypes.c_uint32
+        L.oracle_lsh_codes.argtypes = [_i, _i, _f64p, _f32p, _u32p]
+        L.oracle_lsh_prefill.argtypes = [_i, _i, _i, _i, _i, _f64p, _f64p, _f64p, _f32p,
+                                         _f64p, _f64p, _u32p, _i32p, _i32p]
+        L.oracle_lsh_decode_step.argtypes = [_i, _i, _i, _i, _d, _i, _f64p, _f64p, _u32p,
+                                             _i32p, _i32p, _f64p, _f64p, _f64p, _f32p,
+                                             _f64p, _vp]
+        _lib = L
+    return _lib
+
+
+def _c64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def set_threads(n: int) -> None:
+    lib().oracle_set_threads(int(n))
+
+
+def get_threads() -> int:
+    return int(lib().oracle_get_threads())
+
+
+def prefill_scores(Q, K, scale):
+    """Row max m, row normaliser l and column sums c of the causal prompt
+    softmax, each [U, T] float64."""
+    Q = _c64(Q); K = _c64(K)
+    U, T, d = Q.shape
+    m = np.empty((U, T)); l = np.empty((U, T)); c = np.empty((U, T))
+    lib().oracle_prefill_scores(U, T, d, float(scale), Q, K, m, l, c)
+    return m, l, c
+
+
+def select(c, B, H, r):
+    """Kept prompt positions (ascending) for one unit and the relative
+    score gap at the heavy-hitter cut (inf when no choice was made)."""
+    c = _c64(c)
+    T = c.shape[0]
+    kept = np.empty(max(T, 1), dtype=np.int32)
+    margin = np.empty(1)
+    n = lib().oracle_select(T, B, H, r, c, kept, _ptr(margin))
+    return kept[:n].copy(), float(margin[0])
+
+
+class H2OState:
+    """Oracle H2O cache for U units (all arrays float64 / int32)."""
+
+    def __init__(self, U, B, d):
+        self.U, self.B, self.d = U, B, d
+        self.K = np.zeros((U, B, d))
+        self.V = np.zeros((U, B, d))
+        self.score = np.zeros((U, B))
+        self.pos = np.full((U, B), -1, dtype=np.int32)
+        self.occ = np.zeros(U, dtype=np.int32)
+
+    def copy(self):
+        s = H2OState(self.U, self.B, self.d)
+        for name in ("K", "V", "score", "pos", "occ"):
+            setattr(s, name, getattr(self, name).copy())
+        return s
+
+
+def h2o_prefill(Q, K, V, B, H, r, scale):
+    """Prompt phase: returns (state, c [U,T], kept [U,B] (-1 padded),
+    margin [U])."""
+    Q = _c64(Q); K = _c64(K); V = _c64(V)
+    U, T, d = Q.shape
+    st = H2OState(U, B, d)
+    c = np.empty((U, T))
+    kept = np.empty((U, B), dtype=np.int32)
+    margin = np.empty(U)
+    lib().oracle_h2o_prefill(U, T, d, B, H, r, float(scale), Q, K, V,
+                             st.K, st.V, st.score, st.pos, st.occ,
+                             _ptr(c), _ptr(kept), _ptr(margin))
+    return st, c, kept, margin
+
+
+def build_cache(K, V, c, kept, B):
+    """Cache built from explicit kept lists ([U, B], -1 padded, ascending)."""
+    K = _c64(K); V = _c64(V); c = _c64(c)
+    U, T, d = K.shape
+    kept = np.ascontiguousarray(kept, dtype=np.int32)
+    nkept = np.ascontiguousarray((kept >= 0).sum(axis=1), dtype=np.int32)
+    st = H2OState(U, B, d)
+    lib().oracle_build_cache(U, T, d, B, kept, nkept, c, K, V,
+                             st.K, st.V, st.score, st.pos, st.occ)
+    return st
+
+
+def h2o_decode_step(st, q, k, v, p, r, scale, forced=None):
+    """One decode step in place on ``st``.  Returns (out [U,d], victim [U],
+    margin [U], evicted [U])."""
+    q = _c64(q); k = _c64(k); v = _c64(v)
+    U, d = q.shape
+    out = np.empty((U, d))
+    victim = np.empty(U, dtype=np.int32)
+    margin = np.empty(U)
+    evicted = np.empty(U)
+    f = None if forced is None else np.ascontiguousarray(forced, dtype=np.int32)
+    lib().oracle_h2o_decode_step(U, d, st.B, r, float(scale), int(p), st.K, st.V,
+                                 st.score, st.pos, st.occ, q, k, v, out,
+                                 _ptr(victim), _ptr(margin), _ptr(evicted), _ptr(f))
+    return out, victim, margin, evicted
+
+
+def lsh_code(x, W):
+    x = _c64(x)
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    return int(lib().oracle_lsh_code(x.shape[0], x, W))
+
+
+def lsh_codes(X, W):
+    """Codes of every row of X [..., d] -> uint32 [...]."""
+    X = _c64(X)
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    flat = X.reshape(-1, X.shape[-1])
+    out = np.empty(flat.shape[0], dtype=np.uint32)
+    lib().oracle_lsh_codes(flat.shape[0], flat.shape[1], flat, W, out)
+    return out.reshape(X.shape[:-1])
+
+
+class LSHState:
+    def __init__(self, U, B, d):
+        self.U, self.B, self.d = U, B, d
+        self.K = np.zeros((U, B, d))
+        self.V = np.zeros((U, B, d))
+        self.code = np.zeros((U, B), dtype=np.uint32)
+        self.pos = np.full((U, B), -1, dtype=np.int32)
+        self.occ = np.zeros(U, dtype=np.int32)
+
+
+def lsh_prefill(Q, K, V, W, B, r):
+    Q = _c64(Q); K = _c64(K); V = _c64(V)
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    U, T, d = Q.shape
+    st = LSHState(U, B, d)
+    lib().oracle_lsh_prefill(U, T, d, B, r, Q, K, V, W, st.K, st.V, st.code, st.pos, st.occ)
+    return st
+
+
+def lsh_decode_step(st, q, k, v, W, p, r, scale):
+    """One HashEvict step in place on ``st``.  Returns (out [U,d], victim [U])."""
+    q = _c64(q); k = _c64(k); v = _c64(v)
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    U, d = q.shape
+    out = np.empty((U, d))
+    victim = np.empty(U, dtype=np.int32)
+    lib().oracle_lsh_decode_step(U, d, st.B, r, float(scale), int(p), st.K, st.V,
+                                 st.code, st.pos, st.occ, q, k, v, W, out, _ptr(victim))
+    return out, victim

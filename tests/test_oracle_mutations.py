@@ -1,0 +1,61 @@
+"""The pins must be strong enough to catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of oracle.c (on the CPU), builds it,
+and runs the pin suite against it through ORACLE_LIB; the suite has to fail.
+"""
+import os
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+MUTATIONS = {
+    "causal_drops_diagonal": ("for (int j = 0; j <= i; ++j) {\n                z[j]",
+                              "for (int j = 0; j < i; ++j) {\n                z[j]"),
+    "unnormalised_rows": ("cu[j] += exp(z[j] - mi) / li;", "cu[j] += exp(z[j] - mi);"),
+    "scale_dropped": ("z[j] = scale * dot(Qu", "z[j] = dot(Qu"),
+    "q_k_transposed": ("dot(Qu + (size_t)i * d, Ku + (size_t)j * d, d)",
+                       "dot(Qu + (size_t)j * d, Ku + (size_t)i * d, d)"),
+    "topk_ties_to_higher": ("return (x->j < y->j) ? -1 : (x->j > y->j);",
+                            "return (x->j > y->j) ? -1 : (x->j < y->j);"),
+    "recent_window_short": ("for (int j = ncand; j < T; ++j) keep[j] = 1;",
+                            "for (int j = ncand + 1; j < T; ++j) keep[j] = 1;"),
+    "new_token_not_attended": ("for (int s = 0; s <= n; ++s) lsum += exp(z[s] - mx);\n        for (int e = 0; e < d; ++e) ou[e] = 0.0;\n        for (int s = 0; s <= n; ++s) {",
+                               "for (int s = 0; s < n; ++s) lsum += exp(z[s] - mx);\n        for (int e = 0; e < d; ++e) ou[e] = 0.0;\n        for (int s = 0; s < n; ++s) {"),
+    "window_boundary_off_by_one": ("if (ncand > 0 && !(pu[s] <= p - r)) continue;\n                if (best",
+                                   "if (ncand > 0 && !(pu[s] < p - r)) continue;\n                if (best"),
+    "evict_max_score": ("if (best < 0 || su[s] < su[best])", "if (best < 0 || su[s] > su[best])"),
+    "no_accumulate": ("for (int s = 0; s < n; ++s) su[s] += exp(z[s] - mx) / lsum;",
+                      "for (int s = 0; s < n; ++s) su[s] += 0.0;"),
+    "new_score_zero": ("su[slot] = P_new;", "su[slot] = 0.0;"),
+    "evict_ties_to_higher": ("if (best < 0 || su[s] < su[best])", "if (best < 0 || su[s] <= su[best])"),
+    "lsh_zero_sets_bit": ("if (acc > 0.0f) code", "if (acc >= 0.0f) code"),
+    "lsh_min_distance": ("if (dist > bestd) { bestd = dist; best = s; }",
+                         "if (bestd < 0 || dist < bestd) { bestd = dist; best = s; }"),
+    "lsh_ties_to_higher": ("if (dist > bestd) { bestd = dist; best = s; }",
+                           "if (dist >= bestd) { bestd = dist; best = s; }"),
+    "lsh_window_ignored": ("if (ncand > 0 && !(pos[s] <= p - r)) continue;", ""),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name):
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, "mutation anchor not found: " + name
+    mutated = src.replace(old, new)
+    with tempfile.TemporaryDirectory() as tmp:
+        c = os.path.join(tmp, "oracle_mut.c")
+        so = os.path.join(tmp, "liboracle_mut.so")
+        open(c, "w").write(mutated)
+        subprocess.run(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-fopenmp",
+                        "-ffp-contract=off", c, "-o", so, "-lm"], check=True)
+        env = dict(os.environ, ORACLE_LIB=so)
+        r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                            os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                           env=env, cwd=ROOT, capture_output=True, text=True, timeout=300)
+        assert r.returncode != 0, "planted mistake %s passed every pin:\n%s" % (name, r.stdout[-2000:])

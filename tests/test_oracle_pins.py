@@ -1,0 +1,402 @@
+"""Pins for the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: values
+worked by hand (tests/golden/), closed forms, invariants the method must keep,
+special cases that reduce to textbook attention, and brute force on tiny
+inputs.  None of them needs a GPU.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- prefill ---
+
+def test_prefill_hand_worked_three_tokens():
+    g = _golden("prefill_three_tokens.json")
+    a = np.array(g["a"], float)
+    w = np.array(g["w"], float)
+    Q = np.zeros((1, 3, 2)); K = np.zeros((1, 3, 2))
+    Q[0, :, 0] = 2.0 * w
+    K[0, :, 0] = np.log(a)
+    K[0, :, 1] = g["key_pad"]
+    m, l, c = oracle.prefill_scores(Q, K, g["scale"])
+    want_c = np.array(g["c_num"], float) / g["c_den"]
+    np.testing.assert_allclose(c[0], want_c, rtol=0, atol=g["tol"])
+    np.testing.assert_allclose(m[0], [0.0, math.log(2), 2 * math.log(3)], rtol=0, atol=g["tol"])
+    np.testing.assert_allclose(l[0], g["l"], rtol=0, atol=g["tol"])
+
+
+def test_prefill_equal_keys_harmonic_closed_form():
+    # identical keys: every row is uniform, c_j = H_T - H_j
+    rng = np.random.default_rng(11)
+    T, d = 50, 16
+    Q = rng.standard_normal((2, T, d))
+    K = np.tile(rng.standard_normal((1, 1, d)), (2, T, 1))
+    _, l, c = oracle.prefill_scores(Q, K, 0.25)
+    H = np.concatenate([[0.0], np.cumsum(1.0 / np.arange(1, T + 1))])
+    want = H[T] - H[:T]
+    np.testing.assert_allclose(c[0], want, rtol=1e-13)
+    np.testing.assert_allclose(c[1], want, rtol=1e-13)
+    np.testing.assert_allclose(l[0], np.arange(1, T + 1), rtol=1e-13)
+
+
+def test_prefill_mass_is_prompt_length():
+    # every causal row is a distribution, so the column sums add up to T
+    rng = np.random.default_rng(12)
+    for T in (1, 2, 77):
+        Q = rng.standard_normal((3, T, 8)) * 2
+        K = rng.standard_normal((3, T, 8)) * 2
+        _, _, c = oracle.prefill_scores(Q, K, 0.7)
+        np.testing.assert_allclose(c.sum(axis=1), T, rtol=1e-12)
+        assert (c >= 0).all()
+
+
+def test_prefill_single_token():
+    Q = np.array([[[0.3, -1.0]]]); K = np.array([[[2.0, 5.0]]])
+    m, l, c = oracle.prefill_scores(Q, K, 1.0)
+    assert c[0, 0] == 1.0 and l[0, 0] == 1.0
+    assert m[0, 0] == pytest.approx(0.3 * 2.0 - 5.0, abs=1e-15)
+
+
+def test_prefill_brute_force_small():
+    # dense masked softmax over the whole prompt, column-summed
+    rng = np.random.default_rng(13)
+    for T in range(1, 13):
+        Q = rng.standard_normal((1, T, 4)); K = rng.standard_normal((1, T, 4))
+        scale = 0.6
+        m, l, c = oracle.prefill_scores(Q, K, scale)
+        Z = scale * Q[0] @ K[0].T
+        Z[np.triu_indices(T, 1)] = -np.inf
+        E = np.exp(Z - Z.max(axis=1, keepdims=True))
+        P = E / E.sum(axis=1, keepdims=True)
+        np.testing.assert_allclose(c[0], P.sum(axis=0), rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(m[0], Z.max(axis=1), rtol=1e-13)
+
+
+def test_prefill_one_dominant_key():
+    # a key that every later query strongly prefers collects (almost) every row
+    T, d = 20, 4
+    Q = np.zeros((1, T, d)); K = np.zeros((1, T, d))
+    Q[0, :, 0] = 1.0
+    K[0, 5, 0] = 60.0          # exp(60) dwarfs the other weights (all exp(0))
+    _, _, c = oracle.prefill_scores(Q, K, 1.0)
+    assert c[0, 5] == pytest.approx(T - 5, rel=1e-12)
+    for j in range(6, T):
+        assert c[0, j] < 1e-20
+
+
+# -------------------------------------------------------------- selection ---
+
+def _brute_select(c, T, B, H, r):
+    if T <= B:
+        return list(range(T))
+    nc = T - r
+    heavy = [j for j in range(nc)
+             if sum(1 for k in range(nc) if c[k] > c[j] or (c[k] == c[j] and k < j)) < H]
+    return sorted(set(heavy) | set(range(nc, T)))
+
+
+def test_select_hand_worked_tie():
+    g = _golden("select_ties.json")
+    kept, margin = oracle.select(np.array(g["c"]), g["B"], g["H"], g["r"])
+    assert kept.tolist() == g["kept"]
+    assert margin == g["margin"]
+
+
+def test_select_brute_force_with_ties():
+    rng = np.random.default_rng(14)
+    for _ in range(400):
+        T = int(rng.integers(1, 13))
+        B = int(rng.integers(1, 13))
+        r = int(rng.integers(0, B + 1))
+        H = B - r
+        c = rng.integers(0, 4, size=T).astype(float)   # many ties
+        kept, _ = oracle.select(c, B, H, r)
+        assert kept.tolist() == _brute_select(c, T, B, H, r)
+        assert len(kept) == min(T, B)
+        if T > B:
+            assert set(range(T - r, T)) <= set(kept.tolist())
+
+
+# ---------------------------------------------------------------- decode ---
+
+def _run_h2o(Q, K, V, q, k, v, B, H, r, scale):
+    st, c, kept, _ = oracle.h2o_prefill(Q, K, V, B, H, r, scale)
+    T = Q.shape[1]
+    outs, victims, evs, states = [], [], [], []
+    for t in range(q.shape[0]):
+        out, vic, mg, ev = oracle.h2o_decode_step(st, q[t], k[t], v[t], T + t, r, scale)
+        outs.append(out); victims.append(vic); evs.append(ev)
+        states.append(st.copy())
+    return st, c, kept, outs, victims, evs, states
+
+
+def _full_causal_attention(Qall, Kall, Vall, scale, i):
+    z = scale * Kall[: i + 1] @ Qall[i]
+    e = np.exp(z - z.max())
+    return (e / e.sum()) @ Vall[: i + 1]
+
+
+def test_decode_equals_full_attention_when_budget_covers_sequence():
+    rng = np.random.default_rng(15)
+    U, T, S, d = 3, 9, 7, 8
+    Q = rng.standard_normal((U, T, d)); K = rng.standard_normal((U, T, d))
+    V = rng.standard_normal((U, T, d))
+    q = rng.standard_normal((S, U, d)); k = rng.standard_normal((S, U, d))
+    v = rng.standard_normal((S, U, d))
+    B = T + S
+    _, _, _, outs, victims, _, _ = _run_h2o(Q, K, V, q, k, v, B, 4, B - 4, 0.4)
+    for u in range(U):
+        Kall = np.concatenate([K[u], k[:, u]]); Vall = np.concatenate([V[u], v[:, u]])
+        Qall = np.concatenate([Q[u], q[:, u]])
+        for t in range(S):
+            want = _full_causal_attention(Qall, Kall, Vall, 0.4, T + t)
+            np.testing.assert_allclose(outs[t][u], want, rtol=0, atol=1e-12)
+            assert victims[t][u] == -1
+
+
+def test_decode_attention_rows_sum_to_one():
+    # one-hot values: out equals the attention row itself
+    rng = np.random.default_rng(16)
+    T, S, B, d = 10, 12, 6, 32
+    Q = rng.standard_normal((1, T, d)); K = rng.standard_normal((1, T, d))
+    V = np.zeros((1, T, d)); V[0, np.arange(T), np.arange(T)] = 1.0
+    q = rng.standard_normal((S, 1, d)); k = rng.standard_normal((S, 1, d))
+    v = np.zeros((S, 1, d)); v[np.arange(S), 0, T + np.arange(S) - 0] = 1.0  # positions 10..21
+    st, _, _, _ = oracle.h2o_prefill(Q, K, V, B, 3, 3, 0.3)
+    for t in range(S):
+        out, _, _, _ = oracle.h2o_decode_step(st, q[t], k[t], v[t], T + t, 3, 0.3)
+        assert abs(out[0].sum() - 1.0) < 1e-12
+        assert (out[0] >= 0).all()
+        # the weight lands only on cached positions and the new one
+        assert out[0][T + t] > 0
+
+
+def test_decode_hand_worked_equal_keys():
+    g = _golden("h2o_equal_keys.json")
+    T, B, H, r = g["T"], g["B"], g["H"], g["r"]
+    d = 4
+    rng = np.random.default_rng(17)
+    key = rng.standard_normal(d)
+    Q = rng.standard_normal((1, T, d)); K = np.tile(key, (1, T, 1))
+    V = rng.standard_normal((1, T, d))
+    st, c, _, _ = oracle.h2o_prefill(Q, K, V, B, H, r, 0.5)
+    assert st.pos[0].tolist() == g["prefill_pos"]
+    np.testing.assert_allclose(st.score[0] * 12, g["prefill_score_12ths"], atol=g["tol"])
+    vals = {j: V[0, j] for j in range(T)}
+    for s in g["steps"]:
+        qn = rng.standard_normal((1, d)); vn = rng.standard_normal((1, d))
+        cached = [vals[p] for p in st.pos[0]]
+        out, vic, mg, ev = oracle.h2o_decode_step(st, qn, key[None, :], vn, s["p"], r, 0.5)
+        np.testing.assert_allclose(out[0], (sum(cached) + vn[0]) / 4, atol=1e-13)
+        assert vic[0] == s["victim"]
+        assert st.pos[0].tolist() == s["pos"]
+        np.testing.assert_allclose(st.score[0] * 12, s["score_12ths"], atol=g["tol"])
+        np.testing.assert_allclose(ev[0] * 12, s["evicted_12ths"], atol=g["tol"])
+        assert mg[0] == pytest.approx(s["margin"], rel=1e-12)
+        vals[s["p"]] = vn[0]
+
+
+@pytest.mark.parametrize("B,H,r", [(6, 3, 3), (6, 0, 6), (6, 6, 0), (5, 4, 1), (1, 0, 1)])
+def test_decode_invariants(B, H, r):
+    # occupancy, recent window, mass conservation, sliding window when H = 0
+    rng = np.random.default_rng(18 + B + 7 * H)
+    U, T, S, d = 4, 11, 25, 6
+    Q = rng.standard_normal((U, T, d)) * 1.5; K = rng.standard_normal((U, T, d)) * 1.5
+    V = rng.standard_normal((U, T, d))
+    q = rng.standard_normal((S, U, d)) * 1.5; k = rng.standard_normal((S, U, d)) * 1.5
+    v = rng.standard_normal((S, U, d))
+    st, c, kept, _ = oracle.h2o_prefill(Q, K, V, B, H, r, 0.5)
+    dropped = np.array([c[u].sum() - st.score[u][st.pos[u] >= 0].sum() for u in range(U)])
+    ev_total = dropped.copy()
+    for t in range(S):
+        p = T + t
+        _, vic, _, ev = oracle.h2o_decode_step(st, q[t], k[t], v[t], p, r, 0.5)
+        ev_total += ev
+        assert (st.occ == min(B, T + t + 1)).all()
+        live = st.score[:, :].sum(axis=1)
+        np.testing.assert_allclose(live + ev_total, T + t + 1, rtol=1e-12)
+        for u in range(U):
+            held = set(st.pos[u][st.pos[u] >= 0].tolist())
+            assert set(range(max(0, p - r + 1), p + 1)) <= held
+            assert len(held) == st.occ[u]
+            if H == 0:
+                assert held == set(range(p - B + 1, p + 1))
+        assert (st.score >= 0).all()
+
+
+def test_decode_victim_brute_force():
+    # the victim is the lowest-index minimum over slots outside the window
+    rng = np.random.default_rng(19)
+    U, T, S, d, B, H, r = 6, 12, 20, 5, 7, 3, 4
+    Q = rng.standard_normal((U, T, d)); K = rng.standard_normal((U, T, d))
+    V = rng.standard_normal((U, T, d))
+    st, _, _, _ = oracle.h2o_prefill(Q, K, V, B, H, r, 0.5)
+    for t in range(S):
+        p = T + t
+        before = st.copy()
+        qn = rng.standard_normal((U, d)); kn = rng.standard_normal((U, d))
+        vn = rng.standard_normal((U, d))
+        _, vic, _, _ = oracle.h2o_decode_step(st, qn, kn, vn, p, r, 0.5)
+        for u in range(U):
+            # recompute this step's probabilities independently
+            keys = np.concatenate([before.K[u], kn[u][None]])
+            z = 0.5 * keys @ qn[u]
+            P = np.exp(z - z.max()); P /= P.sum()
+            sc = before.score[u] + P[:B]
+            cands = [s for s in range(B) if before.pos[u][s] <= p - r]
+            best = min(cands, key=lambda s: (sc[s], s))
+            assert vic[u] == best
+            assert st.pos[u][best] == p
+            assert st.score[u][best] == pytest.approx(P[B], rel=1e-13)
+
+
+def test_forced_victim_is_honoured():
+    rng = np.random.default_rng(20)
+    Q = rng.standard_normal((1, 8, 4)); K = rng.standard_normal((1, 8, 4))
+    V = rng.standard_normal((1, 8, 4))
+    st, _, _, _ = oracle.h2o_prefill(Q, K, V, 4, 2, 2, 0.5)
+    cand = [s for s in range(4) if st.pos[0][s] <= 8 - 2]
+    forced = np.array([cand[-1]], np.int32)
+    _, vic, _, _ = oracle.h2o_decode_step(st, Q[:, 0], K[:, 0], V[:, 0], 8, 2, 0.5, forced)
+    assert vic[0] == cand[-1] and st.pos[0][cand[-1]] == 8
+
+
+# ------------------------------------------------------------------- LSH ---
+
+def _bits_vec(bits, d, neg):
+    x = np.full(d, neg, float)
+    x[list(bits)] = 1.0
+    return x
+
+
+def test_lsh_identity_projection_codes():
+    d = 32
+    W = np.eye(d, dtype=np.float32)
+    rng = np.random.default_rng(21)
+    for _ in range(50):
+        x = rng.integers(-1, 2, size=d).astype(float)   # -1, 0, +1
+        want = sum(1 << j for j in range(d) if x[j] > 0)
+        assert oracle.lsh_code(x, W) == want
+    assert oracle.lsh_code(np.zeros(d), W) == 0
+
+
+def test_lsh_sign_matches_exact_projection():
+    # the fp32 fma chain can only disagree with the exact sign inside its
+    # rounding bound, d * 2^-24 * sum |x_i w_ij|
+    rng = np.random.default_rng(22)
+    W = rng.standard_normal((128, 32)).astype(np.float32)
+    X = rng.standard_normal((300, 128)).astype(np.float32).astype(np.float64)
+    codes = oracle.lsh_codes(X, W)
+    Wd = W.astype(np.float64)
+    exact = X @ Wd
+    bound = 128 * 2.0 ** -24 * (np.abs(X) @ np.abs(Wd))
+    checked = 0
+    for t in range(X.shape[0]):
+        for j in range(32):
+            if abs(exact[t, j]) > bound[t, j]:
+                assert ((int(codes[t]) >> j) & 1) == int(exact[t, j] > 0)
+                checked += 1
+    assert checked > 0.99 * 300 * 32
+    # x and -x give complementary codes where no projection is exactly zero
+    c1 = oracle.lsh_code(X[0], W); c2 = oracle.lsh_code(-X[0], W)
+    assert c1 ^ c2 == 0xFFFFFFFF
+
+
+def test_lsh_hand_worked_identity_projection():
+    g = _golden("lsh_identity_projection.json")
+    d, B, r = g["d"], g["B"], g["r"]
+    W = np.eye(d, dtype=np.float32)
+    T = len(g["key_bits"])
+    K = np.stack([_bits_vec(b, d, -1.0) for b in g["key_bits"]])[None]
+    Q = np.stack([_bits_vec(b, d, 0.0) for b in g["query_bits"]])[None]
+    V = np.arange(T * d, dtype=float).reshape(1, T, d)
+    assert [oracle.lsh_code(K[0, t], W) for t in range(T)] == g["key_codes"]
+    st = oracle.lsh_prefill(Q, K, V, W, B, r)
+    assert st.pos[0].tolist() == g["after_prefill_pos"]
+    assert st.code[0].tolist() == g["after_prefill_code"]
+    dec = g["decode"]
+    qn = _bits_vec(dec["q_bits"], d, 0.0)[None]; kn = _bits_vec(dec["k_bits"], d, -1.0)[None]
+    vn = np.ones((1, d))
+    out, vic = oracle.lsh_decode_step(st, qn, kn, vn, W, dec["p"], r, 0.25)
+    assert vic[0] == dec["victim"]
+    assert st.pos[0].tolist() == dec["pos"] and st.code[0].tolist() == dec["code"]
+
+
+def test_lsh_equals_full_attention_when_budget_covers_sequence():
+    rng = np.random.default_rng(23)
+    U, T, S, d = 2, 6, 5, 16
+    W = rng.standard_normal((d, 32)).astype(np.float32)
+    Q = rng.standard_normal((U, T, d)); K = rng.standard_normal((U, T, d))
+    V = rng.standard_normal((U, T, d))
+    st = oracle.lsh_prefill(Q, K, V, W, T + S, 3)
+    for t in range(S):
+        q = rng.standard_normal((U, d)); k = rng.standard_normal((U, d))
+        v = rng.standard_normal((U, d))
+        out, vic = oracle.lsh_decode_step(st, q, k, v, W, T + t, 3, 0.3)
+        for u in range(U):
+            assert vic[u] == -1
+            n = T + t + 1
+            Kall = st.K[u, :n]; Vall = st.V[u, :n]
+            z = 0.3 * Kall @ q[u]
+            e = np.exp(z - z.max())
+            np.testing.assert_allclose(out[u], (e / e.sum()) @ Vall, atol=1e-12)
+            assert st.pos[u, :n].tolist() == list(range(n))
+
+
+def test_lsh_decode_brute_force_and_invariants():
+    rng = np.random.default_rng(24)
+    U, T, S, d, B, r = 5, 15, 30, 8, 6, 2
+    W = rng.standard_normal((d, 32)).astype(np.float32)
+    Q = rng.standard_normal((U, T, d)); K = rng.standard_normal((U, T, d))
+    V = rng.standard_normal((U, T, d))
+    st = oracle.lsh_prefill(Q, K, V, W, B, r)
+    for t in range(S):
+        p = T + t
+        before_pos = st.pos.copy(); before_code = st.code.copy()
+        q = rng.standard_normal((U, d)); k = rng.standard_normal((U, d))
+        v = rng.standard_normal((U, d))
+        out, vic = oracle.lsh_decode_step(st, q, k, v, W, p, r, 0.3)
+        for u in range(U):
+            cq = oracle.lsh_code(q[u], W)
+            dist = [bin(cq ^ int(before_code[u, s])).count("1") for s in range(B)]
+            cands = [s for s in range(B) if before_pos[u, s] <= p - r]
+            best = min(cands, key=lambda s: (-dist[s], s))
+            assert vic[u] == best
+            held = set(st.pos[u].tolist())
+            assert set(range(p - r + 1, p + 1)) <= held and len(held) == B
+            assert st.code[u, best] == oracle.lsh_code(k[u], W)
+            # attention after the replacement, over the budget
+            z = 0.3 * st.K[u] @ q[u]
+            e = np.exp(z - z.max())
+            np.testing.assert_allclose(out[u], (e / e.sum()) @ st.V[u], atol=1e-12)
+
+
+def test_decode_exact_tie_goes_to_lowest_slot():
+    # equal keys add the same probability to every slot, so equal prompt
+    # scores stay exactly equal and the victim must be the lower slot
+    d, T, B, r = 4, 6, 4, 2
+    key = np.array([0.5, -1.0, 2.0, 0.25])
+    K = np.tile(key, (1, T, 1)); V = np.arange(T * d, dtype=float).reshape(1, T, d)
+    c = np.array([[1.0, 0.5, 3.0, 0.5, 0.25, 0.25]])
+    kept = np.array([[1, 2, 3, 5]], np.int32)          # scores 0.5, 3.0, 0.5, 0.25
+    st = oracle.build_cache(K, V, c, kept, B)
+    # p = 6, r = 2: candidates are positions <= 4 (slots 0, 1, 2); slots 0
+    # and 2 tie at 0.5 + 1/5 and the lower one goes
+    _, vic, mg, ev = oracle.h2o_decode_step(st, np.ones((1, d)), key[None], np.ones((1, d)), 6, r, 0.5)
+    assert vic[0] == 0 and mg[0] == 0.0
+    assert ev[0] == pytest.approx(0.7, rel=1e-15)
+    assert st.pos[0].tolist() == [6, 2, 3, 5]

@@ -1,0 +1,57 @@
+"""The seeded input generator: deterministic, per-unit addressable, and
+rounded to the declared precision."""
+import numpy as np
+
+from kv_cache_eviction_h2o_gb300 import workloads as wl
+
+
+def test_round_bf16_is_nearest_even():
+    x = np.array([1.0, 1.00390625, 1.005859375, 1.0078125, -3.14159, 0.0], np.float32)
+    r = wl.round_bf16(x)
+    # bf16 keeps 8 significant bits: 1 + k/128 in [1, 2)
+    assert r[0] == 1.0
+    assert r[1] == 1.0                       # exactly half way to 1 + 1/128 -> even (1.0)
+    assert r[2] == np.float32(1.0078125)     # above half way -> up
+    assert r[3] == np.float32(1.0078125)
+    assert (r.view(np.uint32) & 0xFFFF == 0).all()
+    assert abs(r[4] - x[4]) <= abs(x[4]) * 2 ** -8
+
+
+def test_subset_matches_full_and_is_deterministic():
+    w = wl.WORKLOADS["tiny"]
+    full = wl.generate(w)
+    part = wl.generate(w, units=[2, 0])
+    np.testing.assert_array_equal(part["K"][0], full["K"][2])
+    np.testing.assert_array_equal(part["q"][:, 1], full["q"][:, 0])
+    again = wl.generate(w)
+    for name in ("Q", "K", "V", "q", "k", "v"):
+        np.testing.assert_array_equal(full[name], again[name])
+
+
+def test_shapes_and_precision():
+    w = wl.WORKLOADS["opt-6.7b"]
+    g = wl.generate(w, units=[5], steps=3, prompt=64)
+    assert g["Q"].shape == (1, 64, 128) and g["q"].shape == (3, 1, 128)
+    assert (g["K"].view(np.uint32) & 0xFFFF == 0).all()
+    h = wl.WORKLOADS["hashevict-opt-6.7b"]
+    assert wl.lsh_matrix(h).shape == (128, 32)
+    assert wl.lsh_matrix(h).dtype == np.float32
+
+
+def test_structures_present():
+    # rank component: keys carry extra energy in a low-rank subspace
+    w = wl.WORKLOADS["tiny"]
+    Q, K, V = wl.prompt_unit(w, 0)
+    s = np.linalg.svd(K.astype(np.float64), compute_uv=False)
+    assert s[0] > 1.5 * s[3]
+    # sink/outlier keys: the first four positions have ~6x the norm
+    w3 = wl.WORKLOADS["llama-7b-32k"]
+    Q, K, V = wl.prompt_unit(w3, 1, prompt=4096)
+    n = np.linalg.norm(K, axis=1)
+    assert (n[:4] > 4 * np.median(n)).all()
+    frac = (n > 4 * np.median(n)).mean()
+    assert 0.002 < frac < 0.01
+    # shared-direction outliers: about 1% of keys get 4x along one direction
+    w2 = wl.WORKLOADS["opt-30b"]
+    Q, K, V = wl.prompt_unit(w2, 3)
+    assert K.shape == (512, 128)
