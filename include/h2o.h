@@ -1,0 +1,197 @@
+/*
+ * h2o.h -- C ABI of libh2o_gb300.so: budgeted-KV-cache decode attention with
+ * heavy-hitter (H2O) eviction and the HashEvict LSH variant, on one GB300
+ * (sm_103a).
+ *
+ * The operations follow these pages (cited by title and section):
+ *  [H2O] "H2O: Heavy-Hitter Oracle for Efficient Generative Inference of Large
+ *        Language Models" (review page), 提案手法 (method) and 研究の動機と目的
+ *        (motivation) sections: heavy hitters are the tokens that accumulate
+ *        the most attention; a greedy per-decode-step rule driven by local
+ *        attention statistics evicts, balancing recency against relevance.
+ *  [FG]  "Model Tells You What to Discard: Adaptive KV Cache Compression for
+ *        LLMs" (review page), Figure 2 caption: the fixed "Frequency + Local"
+ *        cache, i.e. heavy hitters plus a recent window.
+ *  [SH]  "Scissorhands: Exploiting the Persistence of Importance Hypothesis
+ *        for LLM KV Cache Compression at Test Time", abstract: the cache is
+ *        held at a fixed budget.
+ *  [HE]  "HashEvict: A Pre-Attention KV Cache Eviction Strategy using
+ *        Locality-Sensitive Hashing", abstract: Hamming distance between
+ *        binarised Gaussian projections of the query and the cached keys,
+ *        decided before attention; the new token replaces the cached token
+ *        expected to receive the least attention; a compact binary structure
+ *        is kept in GPU memory.
+ *
+ * Conventions shared by every call
+ *  - U = batch * heads independent (batch, head) units; the unit index is
+ *    b * heads + h.  d = head_dim (64 or 128).  Element type is fp32
+ *    (H2O_F32) or bf16 (H2O_BF16) for every Q/K/V/q/k/v buffer of a handle.
+ *  - Pointers named "device" must point to device memory of the current
+ *    device, C-contiguous, 16-byte aligned.  The caller owns them.
+ *  - The library owns the cache (K, V [U][B][d]), the scores (fp64
+ *    [U][B]), the slot positions (int32 [U][B], -1 = empty), the LSH codes
+ *    (uint32 [U][B]), the per-unit occupancy and next position, and the
+ *    prompt scratch.  The cache is allocated by *_init; the prompt scratch
+ *    by the first *_prefill with a given or larger prompt length (so that
+ *    call must not be inside a CUDA stream capture).
+ *  - Calls enqueue work on the handle's stream and return without waiting.
+ *    Argument and state errors are returned synchronously; a device-side
+ *    error (a bounded wait that ran out) is reported by h2o_sync.
+ *  - Every int-returning call returns H2O_OK (0) or a negative h2o_status;
+ *    h2o_last_error() then describes the failure (thread-local).
+ *  - Positions are 0-based.  After a prompt of T tokens the next decoded
+ *    token has position T, then T+1, ...
+ */
+#ifndef H2O_GB300_H
+#define H2O_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct h2o_ctx* h2o_handle;
+
+typedef enum {
+    H2O_OK = 0,
+    H2O_ERR_ARG = -1,             /* bad argument (null, size, alignment)      */
+    H2O_ERR_STATE = -2,           /* wrong call order or wrong handle kind     */
+    H2O_ERR_ALLOC = -3,           /* device allocation failed                  */
+    H2O_ERR_CUDA = -4,            /* a CUDA runtime call failed                */
+    H2O_ERR_DEVICE_TIMEOUT = -5,  /* a kernel's bounded wait ran out           */
+    H2O_ERR_UNSUPPORTED = -6      /* not supported on this device / dtype      */
+} h2o_status;
+
+enum { H2O_F32 = 0, H2O_BF16 = 1 };
+
+/*
+ * h2o_init -- create an H2O cache handle [H2O 提案手法; FG Figure 2; SH].
+ *   budget = B slots per unit (>= 1), heavy = H heavy-hitter slots,
+ *   recent = r recent-window slots; heavy + recent must equal budget.
+ *   batch, heads >= 1; head_dim in {64, 128}; dtype H2O_F32 or H2O_BF16;
+ *   scale > 0 is the softmax scale (usually 1/sqrt(head_dim)).
+ *   cuda_stream: the cudaStream_t to enqueue on (NULL = legacy stream).
+ * On success *out holds the handle; destroy it with h2o_destroy.
+ */
+int h2o_init(h2o_handle* out, int budget, int heavy, int recent, int batch, int heads,
+             int head_dim, int dtype, double scale, void* cuda_stream);
+
+/*
+ * h2o_prefill -- build the initial cache from a prompt of T >= 1 tokens
+ * [H2O 提案手法]: the accumulated attention of prompt token j is
+ *   c_j = sum_{i>=j} exp(z_ij - m_i) / l_i,  z_ij = scale q_i.k_j,
+ *   m_i = max_{j<=i} z_ij,  l_i = sum_{j<=i} exp(z_ij - m_i);
+ * if T <= B every token is kept, otherwise the recent window T-r..T-1 and
+ * the H largest c_j among j < T-r (ties to the lower j).  Kept tokens fill
+ * slots 0..n-1 in ascending position; each slot's score starts at c_j.
+ *   Q, K, V: device [U][T][d] of the handle's dtype.
+ * Resets the handle's decode position to T.  Allocates the prompt scratch
+ * (16 bytes per unit per token) when T exceeds the largest T seen so far.
+ */
+int h2o_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T);
+
+/*
+ * h2o_decode_step -- one decode step for all U units [H2O 提案手法]:
+ *   attend:     out = softmax(scale q.K) V over the live slots and the new
+ *               token itself;
+ *   accumulate: every live slot's score += its probability this step;
+ *   evict:      if the cache is full, the victim is the slot with the
+ *               smallest score among slots whose position is <= p - r
+ *               (p = this token's position), lowest slot on ties;
+ *               otherwise the next empty slot;
+ *   insert:     the victim slot takes (k, v), score = the new token's own
+ *               probability, position p.
+ *   q, k, v: device [U][d] of the handle's dtype; out: device fp32 [U][d];
+ *   victim_out: device int32 [U] or NULL, receives the evicted slot or -1
+ *   when the token was appended.
+ * Requires a prior h2o_prefill (or h2o_set_state) on an H2O handle.
+ */
+int h2o_decode_step(h2o_handle h, const void* q, const void* k, const void* v,
+                    float* out, int* victim_out);
+
+/*
+ * lsh_init -- create a HashEvict cache handle [HE abstract].
+ *   budget = B slots, recent = r slots never evicted (0 <= r <= B);
+ *   W: device fp32 [d][32], the Gaussian projection matrix, copied at init.
+ *   Other arguments as h2o_init.
+ * Code of a vector x: bit j is 1 iff the fp32 fused multiply-add chain
+ *   acc = fmaf(x_i, W[i][j], acc), i = 0..d-1, from acc = 0, ends > 0.
+ */
+int lsh_init(h2o_handle* out, int budget, int recent, int batch, int heads, int head_dim,
+             int dtype, double scale, const float* W, void* cuda_stream);
+
+/*
+ * lsh_prefill -- build the initial HashEvict cache from a prompt of T >= 1
+ * tokens by replaying the decode replacement rule token by token: tokens
+ * enter empty slots while there are any; afterwards token t replaces the
+ * slot with the largest Hamming distance between code(q_t) and the slot's
+ * key code among slots with position <= t - r (lowest slot on ties).
+ *   Q, K, V: device [U][T][d].  Scratch: 8 bytes per unit per token.
+ */
+int lsh_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T);
+
+/*
+ * lsh_decode_step -- one HashEvict step [HE abstract]: the victim is chosen
+ * before attention (largest Hamming distance between code(q) and the
+ * cached key codes among slots with position <= p - r, lowest slot on ties;
+ * the next empty slot while the cache is not full), the new (k, v, code(k),
+ * p) is written into it, and out = softmax(scale q.K) V over the live slots,
+ * which now hold the new token and no longer the victim.
+ *   Arguments as h2o_decode_step.  Requires lsh_prefill on an LSH handle.
+ */
+int lsh_decode_step(h2o_handle h, const void* q, const void* k, const void* v,
+                    float* out, int* victim_out);
+
+/*
+ * h2o_get_state -- copy the cache to HOST buffers (any pointer may be NULL):
+ *   K, V [U][B][d] of the handle's dtype; score fp64 [U][B] (H2O handles;
+ *   zeros for LSH); pos int32 [U][B]; code uint32 [U][B] (LSH handles;
+ *   zeros for H2O); occupancy int32 [U]; next_pos int32 [U].
+ * Waits for the handle's stream.
+ */
+int h2o_get_state(h2o_handle h, void* K, void* V, double* score, int* pos, unsigned* code,
+                  int* occupancy, int* next_pos);
+
+/*
+ * h2o_set_state -- overwrite the cache from HOST buffers laid out as in
+ * h2o_get_state (NULL leaves that part unchanged).  Marks the handle ready
+ * for decode.  Waits for the handle's stream.
+ */
+int h2o_set_state(h2o_handle h, const void* K, const void* V, const double* score,
+                  const int* pos, const unsigned* code, const int* occupancy,
+                  const int* next_pos);
+
+/*
+ * h2o_get_prefill_stats -- copy the last h2o_prefill's prompt statistics to
+ * HOST buffers [U][T] (any may be NULL): m (row max of z, natural-log
+ * units), l (row normaliser) and c (column sums, fp64).  Waits.
+ */
+int h2o_get_prefill_stats(h2o_handle h, float* m, float* l, double* c);
+
+/* Replace the stream later calls enqueue on. */
+int h2o_set_stream(h2o_handle h, void* cuda_stream);
+
+/*
+ * h2o_set_decode_split -- CTAs (1..16) that share one unit's slots in the
+ * decode kernels (a thread-block cluster); 0 restores the automatic choice.
+ * Affects performance only, never results.
+ */
+int h2o_set_decode_split(h2o_handle h, int ctas_per_unit);
+
+/*
+ * h2o_sync -- wait for the handle's stream; returns H2O_ERR_DEVICE_TIMEOUT
+ * if a kernel reported a bounded wait that ran out (the error word is then
+ * cleared), H2O_ERR_CUDA on a CUDA error.
+ */
+int h2o_sync(h2o_handle h);
+
+/* Free every library-owned buffer of the handle; NULL is a no-op. */
+void h2o_destroy(h2o_handle h);
+
+/* Thread-local description of the last failure in this thread ("" if none). */
+const char* h2o_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* H2O_GB300_H */

@@ -1,0 +1,195 @@
+// common.cuh -- device helpers shared by the library's kernels: element
+// loads, mbarrier / bulk-copy (TMA) wrappers with bounded waits, cluster
+// barriers, and the launch-side structures.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace h2o {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// bit flags OR-ed into a handle's device error word
+enum DeviceError : int {
+    kErrNone = 0,
+    kErrWaitTimeout = 1,   // an mbarrier wait ran out of its bound
+};
+
+// ----------------------------------------------------------------- elements
+
+template <typename T> struct Elem;
+
+template <> struct Elem<float> {
+    __device__ __forceinline__ static float to_f(float x) { return x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    __device__ __forceinline__ static float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+};
+
+// Load E consecutive elements starting at p (E * sizeof(T) bytes, naturally
+// aligned) and widen them to fp32.
+template <typename T, int E>
+__device__ __forceinline__ void load_vec(const T* p, float* out)
+{
+    if constexpr (sizeof(T) == 2) {
+        static_assert(E == 2 || E == 4 || E == 8, "bf16 vector width");
+        if constexpr (E == 2) {
+            uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+            out[0] = __uint_as_float(w << 16);
+            out[1] = __uint_as_float(w & 0xffff0000u);
+        } else if constexpr (E == 4) {
+            uint2 w = *reinterpret_cast<const uint2*>(p);
+            out[0] = __uint_as_float(w.x << 16); out[1] = __uint_as_float(w.x & 0xffff0000u);
+            out[2] = __uint_as_float(w.y << 16); out[3] = __uint_as_float(w.y & 0xffff0000u);
+        } else {
+            uint4 w = *reinterpret_cast<const uint4*>(p);
+            out[0] = __uint_as_float(w.x << 16); out[1] = __uint_as_float(w.x & 0xffff0000u);
+            out[2] = __uint_as_float(w.y << 16); out[3] = __uint_as_float(w.y & 0xffff0000u);
+            out[4] = __uint_as_float(w.z << 16); out[5] = __uint_as_float(w.z & 0xffff0000u);
+            out[6] = __uint_as_float(w.w << 16); out[7] = __uint_as_float(w.w & 0xffff0000u);
+        }
+    } else {
+        static_assert(E == 2 || E == 4, "fp32 vector width");
+        if constexpr (E == 2) {
+            float2 w = *reinterpret_cast<const float2*>(p);
+            out[0] = w.x; out[1] = w.y;
+        } else {
+            float4 w = *reinterpret_cast<const float4*>(p);
+            out[0] = w.x; out[1] = w.y; out[2] = w.z; out[3] = w.w;
+        }
+    }
+}
+
+// ------------------------------------------------------- shared-memory PTX
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+// make mbarrier initialisation visible to the async (bulk-copy) proxy and
+// to the rest of the cluster
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase: gives up after ~2^31 SM clocks (about
+// a second) or 2^24 polls, whichever comes first, and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (int it = 0; it < (1 << 24); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (clock64() - t0 > (1LL << 31)) break;
+    }
+    return false;
+}
+
+// --------------------------------------------------------- cluster barrier
+
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+// address of the same shared-memory variable in CTA `rank` of this cluster
+__device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_f64(uint32_t addr, double v)
+{
+    asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(addr), "d"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v)
+{
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// ------------------------------------------------------------- reductions
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+}  // namespace h2o

@@ -1,0 +1,442 @@
+// h2o_api.cu -- the C ABI declared in include/h2o.h: argument checks, device
+// buffers owned by a handle, and the launch sequence of each call.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "h2o.h"
+#include "kernels.h"
+
+using namespace h2o;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where)
+{
+    return fail(H2O_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+// Host-side fault injection for the failure-path tests: H2O_FAULT=alloc makes
+// the next device allocation fail, H2O_FAULT=launch the next launch.
+bool inject(const char* what)
+{
+    const char* f = getenv("H2O_FAULT");
+    return f && strcmp(f, what) == 0;
+}
+
+enum Kind { kH2O = 0, kLSH = 1 };
+
+}  // namespace
+
+struct h2o_ctx {
+    int kind;
+    int B, H, r, batch, heads, D, dtype, U;
+    double scale;
+    cudaStream_t stream;
+    int device;
+    int num_sms;
+    int split;                 // 0 = automatic
+    // cache
+    void* K;
+    void* V;
+    double* score;
+    int* pos;
+    uint32_t* code;
+    int2* ustate;
+    int* err;
+    float* W;
+    // prompt scratch
+    int T_cap;
+    float* m2;
+    float* l;
+    double* c;
+    uint32_t* cq;
+    uint32_t* ck;
+    int last_T;
+    int ready;                 // 1 once a prompt or a state was loaded
+};
+
+namespace {
+
+size_t elem_size(int dtype) { return dtype == H2O_BF16 ? 2 : 4; }
+
+int dev_alloc(void** p, size_t bytes, const char* what)
+{
+    *p = nullptr;
+    if (inject("alloc")) return fail(H2O_ERR_ALLOC, "allocation of %s failed (injected)", what);
+    if (bytes == 0) bytes = 16;
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e != cudaSuccess) {
+        *p = nullptr;
+        cudaGetLastError();
+        return fail(H2O_ERR_ALLOC, "cudaMalloc(%zu) for %s: %s", bytes, what, cudaGetErrorString(e));
+    }
+    return H2O_OK;
+}
+
+void free_prompt(h2o_ctx* h)
+{
+    cudaFree(h->m2); cudaFree(h->l); cudaFree(h->c); cudaFree(h->cq); cudaFree(h->ck);
+    h->m2 = nullptr; h->l = nullptr; h->c = nullptr; h->cq = nullptr; h->ck = nullptr;
+    h->T_cap = 0;
+}
+
+void free_all(h2o_ctx* h)
+{
+    free_prompt(h);
+    cudaFree(h->K); cudaFree(h->V); cudaFree(h->score); cudaFree(h->pos); cudaFree(h->code);
+    cudaFree(h->ustate); cudaFree(h->err); cudaFree(h->W);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+CacheView view(const h2o_ctx* h)
+{
+    CacheView v;
+    v.K = h->K; v.V = h->V; v.score = h->score; v.pos = h->pos; v.code = h->code;
+    v.ustate = h->ustate; v.err = h->err;
+    v.U = h->U; v.B = h->B; v.D = h->D; v.dtype = h->dtype; v.r = h->r;
+    v.qscale = (float)(h->scale * 1.4426950408889634);
+    return v;
+}
+
+int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int batch, int heads,
+           int head_dim, int dtype, double scale, const float* W, void* stream)
+{
+    if (!out) return fail(H2O_ERR_ARG, "out handle pointer is NULL");
+    *out = nullptr;
+    if (budget < 1) return fail(H2O_ERR_ARG, "budget must be >= 1 (got %d)", budget);
+    if (recent < 0 || recent > budget) return fail(H2O_ERR_ARG, "recent must be in [0, budget] (got %d)", recent);
+    if (kind == kH2O && (heavy < 0 || heavy + recent != budget))
+        return fail(H2O_ERR_ARG, "heavy + recent must equal budget (%d + %d != %d)", heavy, recent, budget);
+    if (batch < 1 || heads < 1) return fail(H2O_ERR_ARG, "batch and heads must be >= 1");
+    if ((long long)batch * heads > (1LL << 24)) return fail(H2O_ERR_ARG, "batch * heads too large");
+    if (head_dim != 64 && head_dim != 128) return fail(H2O_ERR_ARG, "head_dim must be 64 or 128 (got %d)", head_dim);
+    if (dtype != H2O_F32 && dtype != H2O_BF16) return fail(H2O_ERR_ARG, "dtype must be H2O_F32 or H2O_BF16");
+    if (!(scale > 0.0) || !std::isfinite(scale)) return fail(H2O_ERR_ARG, "scale must be finite and > 0");
+    if ((long long)budget > (1LL << 20)) return fail(H2O_ERR_ARG, "budget too large");
+    if (kind == kLSH && !W) return fail(H2O_ERR_ARG, "W is NULL");
+    if (kind == kLSH && !aligned16(W)) return fail(H2O_ERR_ARG, "W must be 16-byte aligned");
+
+    h2o_ctx* h = new (std::nothrow) h2o_ctx();
+    if (!h) return fail(H2O_ERR_ALLOC, "host allocation failed");
+    memset(h, 0, sizeof(*h));
+    h->kind = kind; h->B = budget; h->H = heavy; h->r = recent; h->batch = batch; h->heads = heads;
+    h->D = head_dim; h->dtype = dtype; h->U = batch * heads; h->scale = scale;
+    h->stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e != cudaSuccess) { delete h; cudaGetLastError(); return cuda_fail(e, "cudaGetDevice"); }
+    e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+    if (e != cudaSuccess) { delete h; cudaGetLastError(); return cuda_fail(e, "cudaDeviceGetAttribute"); }
+    int major = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, h->device);
+    if (major < 10) { delete h; return fail(H2O_ERR_UNSUPPORTED, "device compute capability %d.x is not sm_103", major); }
+
+    const size_t U = (size_t)h->U, B = (size_t)h->B, row = (size_t)h->D * elem_size(dtype);
+    int rc = H2O_OK;
+    if ((rc = dev_alloc(&h->K, U * B * row, "cache K")) ||
+        (rc = dev_alloc(&h->V, U * B * row, "cache V")) ||
+        (rc = dev_alloc((void**)&h->pos, U * B * sizeof(int), "positions")) ||
+        (rc = dev_alloc((void**)&h->ustate, U * sizeof(int2), "unit state")) ||
+        (rc = dev_alloc((void**)&h->err, sizeof(int), "error word"))) {
+        free_all(h); delete h; return rc;
+    }
+    if (kind == kH2O) {
+        if ((rc = dev_alloc((void**)&h->score, U * B * sizeof(double), "scores"))) { free_all(h); delete h; return rc; }
+    } else {
+        if ((rc = dev_alloc((void**)&h->code, U * B * sizeof(uint32_t), "codes")) ||
+            (rc = dev_alloc((void**)&h->W, (size_t)head_dim * 32 * sizeof(float), "projection"))) {
+            free_all(h); delete h; return rc;
+        }
+        e = cudaMemcpyAsync(h->W, W, (size_t)head_dim * 32 * sizeof(float), cudaMemcpyDeviceToDevice, h->stream);
+        if (e != cudaSuccess) { free_all(h); delete h; return cuda_fail(e, "copy W"); }
+    }
+    e = cudaMemsetAsync(h->err, 0, sizeof(int), h->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->ustate, 0, U * sizeof(int2), h->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->pos, 0xff, U * B * sizeof(int), h->stream);
+    if (e != cudaSuccess) { free_all(h); delete h; return cuda_fail(e, "initialise state"); }
+    *out = h;
+    return H2O_OK;
+}
+
+int ensure_prompt_scratch(h2o_ctx* h, int T)
+{
+    if (T <= h->T_cap) return H2O_OK;
+    // the old buffers may still be read by queued work
+    cudaError_t e = cudaStreamSynchronize(h->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    free_prompt(h);
+    const size_t n = (size_t)h->U * (size_t)T;
+    int rc;
+    if (h->kind == kH2O) {
+        if ((rc = dev_alloc((void**)&h->m2, n * sizeof(float), "row max")) ||
+            (rc = dev_alloc((void**)&h->l, n * sizeof(float), "row normaliser")) ||
+            (rc = dev_alloc((void**)&h->c, n * sizeof(double), "column sums"))) {
+            free_prompt(h); return rc;
+        }
+    } else {
+        if ((rc = dev_alloc((void**)&h->cq, n * sizeof(uint32_t), "query codes")) ||
+            (rc = dev_alloc((void**)&h->ck, n * sizeof(uint32_t), "key codes"))) {
+            free_prompt(h); return rc;
+        }
+    }
+    h->T_cap = T;
+    return H2O_OK;
+}
+
+int check_prompt(h2o_ctx* h, int kind, const void* Q, const void* K, const void* V, int T)
+{
+    if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
+    if (h->kind != kind) return fail(H2O_ERR_STATE, "%s called on a %s handle", kind == kH2O ? "h2o_prefill" : "lsh_prefill", h->kind == kH2O ? "H2O" : "LSH");
+    if (!Q || !K || !V) return fail(H2O_ERR_ARG, "Q, K and V must be non-NULL");
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V)) return fail(H2O_ERR_ARG, "Q, K, V must be 16-byte aligned");
+    if (T < 1) return fail(H2O_ERR_ARG, "prompt length must be >= 1 (got %d)", T);
+    if ((long long)T * h->U > (1LL << 31) / 4) return fail(H2O_ERR_ARG, "prompt too long for this batch");
+    if (kind == kH2O && T >= (1 << 24)) return fail(H2O_ERR_ARG, "prompt too long");
+    return H2O_OK;
+}
+
+int check_step(h2o_ctx* h, int kind, const void* q, const void* k, const void* v, const float* out)
+{
+    if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
+    if (h->kind != kind) return fail(H2O_ERR_STATE, "%s called on a %s handle", kind == kH2O ? "h2o_decode_step" : "lsh_decode_step", h->kind == kH2O ? "H2O" : "LSH");
+    if (!h->ready) return fail(H2O_ERR_STATE, "decode before prefill");
+    if (!q || !k || !v || !out) return fail(H2O_ERR_ARG, "q, k, v and out must be non-NULL");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return fail(H2O_ERR_ARG, "q, k, v, out must be 16-byte aligned");
+    return H2O_OK;
+}
+
+int decode_split(const h2o_ctx* h)
+{
+    int s = h->split > 0 ? h->split : auto_decode_split(h->U, h->B, h->num_sms);
+    const int lo = (h->B + 1023) / 1024;
+    if (s < lo) s = lo;
+    if (s > max_decode_split()) s = max_decode_split();
+    return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+int h2o_init(h2o_handle* out, int budget, int heavy, int recent, int batch, int heads, int head_dim,
+             int dtype, double scale, void* cuda_stream)
+{
+    return create(out, kH2O, budget, heavy, recent, batch, heads, head_dim, dtype, scale, nullptr, cuda_stream);
+}
+
+int lsh_init(h2o_handle* out, int budget, int recent, int batch, int heads, int head_dim, int dtype,
+             double scale, const float* W, void* cuda_stream)
+{
+    return create(out, kLSH, budget, budget - recent, recent, batch, heads, head_dim, dtype, scale, W,
+                  cuda_stream);
+}
+
+int h2o_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T)
+{
+    int rc = check_prompt(h, kH2O, Q, K, V, T);
+    if (rc) return rc;
+    if ((rc = ensure_prompt_scratch(h, T))) return rc;
+    if (inject("launch")) return fail(H2O_ERR_CUDA, "kernel launch failed (injected)");
+    CacheView cv = view(h);
+    PromptArgs pa = {};
+    pa.Q = Q; pa.K = K; pa.V = V; pa.T = T; pa.H = h->H;
+    pa.m2 = h->m2; pa.l = h->l; pa.c = h->c;
+    cudaError_t e = launch_prompt_stats(cv, pa, h->stream);
+    if (e == cudaSuccess) e = launch_select(cv, pa, h->stream);
+    if (e == cudaSuccess) e = launch_gather(cv, pa, false, h->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "h2o_prefill launch");
+    h->last_T = T;
+    h->ready = 1;
+    return H2O_OK;
+}
+
+int lsh_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T)
+{
+    int rc = check_prompt(h, kLSH, Q, K, V, T);
+    if (rc) return rc;
+    if ((rc = ensure_prompt_scratch(h, T))) return rc;
+    if (inject("launch")) return fail(H2O_ERR_CUDA, "kernel launch failed (injected)");
+    CacheView cv = view(h);
+    PromptArgs pa = {};
+    pa.Q = Q; pa.K = K; pa.V = V; pa.T = T;
+    pa.cq = h->cq; pa.ck = h->ck;
+    cudaError_t e = launch_lsh_prompt(cv, pa, h->W, h->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "lsh_prefill launch");
+    h->last_T = T;
+    h->ready = 1;
+    return H2O_OK;
+}
+
+int h2o_decode_step(h2o_handle h, const void* q, const void* k, const void* v, float* out, int* victim_out)
+{
+    int rc = check_step(h, kH2O, q, k, v, out);
+    if (rc) return rc;
+    if (inject("launch")) return fail(H2O_ERR_CUDA, "kernel launch failed (injected)");
+    DecodeArgs a = {};
+    a.c = view(h); a.q = q; a.k = k; a.v = v; a.out = out; a.victim_out = victim_out;
+    cudaError_t e = launch_h2o_decode(a, decode_split(h), h->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "h2o_decode_step launch");
+    return H2O_OK;
+}
+
+int lsh_decode_step(h2o_handle h, const void* q, const void* k, const void* v, float* out, int* victim_out)
+{
+    int rc = check_step(h, kLSH, q, k, v, out);
+    if (rc) return rc;
+    if (inject("launch")) return fail(H2O_ERR_CUDA, "kernel launch failed (injected)");
+    DecodeArgs a = {};
+    a.c = view(h); a.q = q; a.k = k; a.v = v; a.out = out; a.victim_out = victim_out; a.W = h->W;
+    cudaError_t e = launch_lsh_decode(a, decode_split(h), h->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "lsh_decode_step launch");
+    return H2O_OK;
+}
+
+int h2o_get_state(h2o_handle h, void* K, void* V, double* score, int* pos, unsigned* code, int* occupancy,
+                  int* next_pos)
+{
+    if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
+    const size_t UB = (size_t)h->U * h->B, row = (size_t)h->D * elem_size(h->dtype);
+    cudaError_t e = cudaSuccess;
+    if (K && e == cudaSuccess) e = cudaMemcpyAsync(K, h->K, UB * row, cudaMemcpyDeviceToHost, h->stream);
+    if (V && e == cudaSuccess) e = cudaMemcpyAsync(V, h->V, UB * row, cudaMemcpyDeviceToHost, h->stream);
+    if (pos && e == cudaSuccess) e = cudaMemcpyAsync(pos, h->pos, UB * sizeof(int), cudaMemcpyDeviceToHost, h->stream);
+    if (score && e == cudaSuccess) {
+        if (h->score) e = cudaMemcpyAsync(score, h->score, UB * sizeof(double), cudaMemcpyDeviceToHost, h->stream);
+        else memset(score, 0, UB * sizeof(double));
+    }
+    if (code && e == cudaSuccess) {
+        if (h->code) e = cudaMemcpyAsync(code, h->code, UB * sizeof(uint32_t), cudaMemcpyDeviceToHost, h->stream);
+        else memset(code, 0, UB * sizeof(uint32_t));
+    }
+    int2* us = nullptr;
+    if ((occupancy || next_pos) && e == cudaSuccess) {
+        us = static_cast<int2*>(malloc((size_t)h->U * sizeof(int2)));
+        if (!us) return fail(H2O_ERR_ALLOC, "host allocation failed");
+        e = cudaMemcpyAsync(us, h->ustate, (size_t)h->U * sizeof(int2), cudaMemcpyDeviceToHost, h->stream);
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+    if (e == cudaSuccess && us) {
+        for (int u = 0; u < h->U; ++u) {
+            if (occupancy) occupancy[u] = us[u].x;
+            if (next_pos) next_pos[u] = us[u].y;
+        }
+    }
+    free(us);
+    if (e != cudaSuccess) return cuda_fail(e, "h2o_get_state");
+    return H2O_OK;
+}
+
+int h2o_set_state(h2o_handle h, const void* K, const void* V, const double* score, const int* pos,
+                  const unsigned* code, const int* occupancy, const int* next_pos)
+{
+    if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
+    const size_t UB = (size_t)h->U * h->B, row = (size_t)h->D * elem_size(h->dtype);
+    if (occupancy)
+        for (int u = 0; u < h->U; ++u)
+            if (occupancy[u] < 0 || occupancy[u] > h->B) return fail(H2O_ERR_ARG, "occupancy out of range");
+    cudaError_t e = cudaStreamSynchronize(h->stream);
+    if (K && e == cudaSuccess) e = cudaMemcpyAsync(h->K, K, UB * row, cudaMemcpyHostToDevice, h->stream);
+    if (V && e == cudaSuccess) e = cudaMemcpyAsync(h->V, V, UB * row, cudaMemcpyHostToDevice, h->stream);
+    if (pos && e == cudaSuccess) e = cudaMemcpyAsync(h->pos, pos, UB * sizeof(int), cudaMemcpyHostToDevice, h->stream);
+    if (score && h->score && e == cudaSuccess)
+        e = cudaMemcpyAsync(h->score, score, UB * sizeof(double), cudaMemcpyHostToDevice, h->stream);
+    if (code && h->code && e == cudaSuccess)
+        e = cudaMemcpyAsync(h->code, code, UB * sizeof(uint32_t), cudaMemcpyHostToDevice, h->stream);
+    int2* us = nullptr;
+    if ((occupancy || next_pos) && e == cudaSuccess) {
+        us = static_cast<int2*>(malloc((size_t)h->U * sizeof(int2)));
+        if (!us) return fail(H2O_ERR_ALLOC, "host allocation failed");
+        e = cudaMemcpyAsync(us, h->ustate, (size_t)h->U * sizeof(int2), cudaMemcpyDeviceToHost, h->stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+        if (e == cudaSuccess) {
+            for (int u = 0; u < h->U; ++u) {
+                if (occupancy) us[u].x = occupancy[u];
+                if (next_pos) us[u].y = next_pos[u];
+            }
+            e = cudaMemcpyAsync(h->ustate, us, (size_t)h->U * sizeof(int2), cudaMemcpyHostToDevice, h->stream);
+        }
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+    free(us);
+    if (e != cudaSuccess) return cuda_fail(e, "h2o_set_state");
+    h->ready = 1;
+    return H2O_OK;
+}
+
+int h2o_get_prefill_stats(h2o_handle h, float* m, float* l, double* c)
+{
+    if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
+    if (h->kind != kH2O) return fail(H2O_ERR_STATE, "prompt statistics exist only on H2O handles");
+    if (!h->last_T) return fail(H2O_ERR_STATE, "no prompt has been processed");
+    const size_t n = (size_t)h->U * h->last_T;
+    cudaError_t e = cudaSuccess;
+    if (m) e = cudaMemcpyAsync(m, h->m2, n * sizeof(float), cudaMemcpyDeviceToHost, h->stream);
+    if (l && e == cudaSuccess) e = cudaMemcpyAsync(l, h->l, n * sizeof(float), cudaMemcpyDeviceToHost, h->stream);
+    if (c && e == cudaSuccess) e = cudaMemcpyAsync(c, h->c, n * sizeof(double), cudaMemcpyDeviceToHost, h->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "h2o_get_prefill_stats");
+    if (m)
+        for (size_t i = 0; i < n; ++i) m[i] = (float)((double)m[i] * 0.6931471805599453);
+    return H2O_OK;
+}
+
+int h2o_set_stream(h2o_handle h, void* cuda_stream)
+{
+    if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
+    h->stream = reinterpret_cast<cudaStream_t>(cuda_stream);
+    return H2O_OK;
+}
+
+int h2o_set_decode_split(h2o_handle h, int ctas_per_unit)
+{
+    if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
+    if (ctas_per_unit < 0 || ctas_per_unit > max_decode_split())
+        return fail(H2O_ERR_ARG, "ctas_per_unit must be in [0, %d]", max_decode_split());
+    if (ctas_per_unit > 0 && ctas_per_unit < (h->B + 1023) / 1024)
+        return fail(H2O_ERR_ARG, "ctas_per_unit must be >= %d for budget %d", (h->B + 1023) / 1024, h->B);
+    h->split = ctas_per_unit;
+    return H2O_OK;
+}
+
+int h2o_sync(h2o_handle h)
+{
+    if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
+    cudaError_t e = cudaStreamSynchronize(h->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "h2o_sync");
+    int word = 0;
+    e = cudaMemcpy(&word, h->err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "h2o_sync read error word");
+    if (word) {
+        cudaMemset(h->err, 0, sizeof(int));
+        return fail(H2O_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out (error word 0x%x)", word);
+    }
+    return H2O_OK;
+}
+
+void h2o_destroy(h2o_handle h)
+{
+    if (!h) return;
+    cudaStreamSynchronize(h->stream);
+    free_all(h);
+    delete h;
+}
+
+const char* h2o_last_error(void) { return g_err; }
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// kernels.h -- launchers between the C ABI (h2o_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace h2o {
+
+// One handle's device-resident cache.
+struct CacheView {
+    void* K;            // [U][B][D] element type per dtype
+    void* V;            // [U][B][D]
+    double* score;      // [U][B] accumulated attention (H2O)
+    int* pos;           // [U][B] token position per slot, -1 = empty
+    uint32_t* code;     // [U][B] key codes (LSH)
+    int2* ustate;       // [U] {occupancy, position of the next token}
+    int* err;           // device error word (DeviceError bits)
+    int U, B, D, dtype, r;
+    float qscale;       // softmax scale * log2(e): logits are kept in base 2
+};
+
+struct DecodeArgs {
+    CacheView c;
+    const void* q;      // [U][D]
+    const void* k;      // [U][D]
+    const void* v;      // [U][D]
+    float* out;         // [U][D]
+    int* victim_out;    // [U] or nullptr
+    const float* W;     // [D][32] (LSH)
+};
+
+struct PromptArgs {
+    const void* Q;      // [U][T][D]
+    const void* K;
+    const void* V;
+    int T;
+    int H;              // heavy-hitter slots (H2O)
+    float* m2;          // [U][T] row max, base-2 logit units
+    float* l;           // [U][T] row normaliser
+    double* c;          // [U][T] column sums
+    uint32_t* cq;       // [U][T] query codes (LSH)
+    uint32_t* ck;       // [U][T] key codes (LSH)
+};
+
+cudaError_t launch_h2o_decode(const DecodeArgs& a, int split, cudaStream_t st);
+cudaError_t launch_lsh_decode(const DecodeArgs& a, int split, cudaStream_t st);
+int auto_decode_split(int U, int B, int num_sms);
+int max_decode_split();
+
+cudaError_t launch_prompt_stats(const CacheView& c, const PromptArgs& p, cudaStream_t st);
+cudaError_t launch_select(const CacheView& c, const PromptArgs& p, cudaStream_t st);
+cudaError_t launch_gather(const CacheView& c, const PromptArgs& p, bool with_codes, cudaStream_t st);
+cudaError_t launch_lsh_prompt(const CacheView& c, const PromptArgs& p, const float* W,
+                              cudaStream_t st);
+
+}  // namespace h2o

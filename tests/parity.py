@@ -1,0 +1,183 @@
+"""Helpers for the GPU parity tests: drive the CUDA library through its C ABI
+(via the ctypes binding) and the CPU oracle on the same seeded inputs, and
+compare them with the rules the tests state:
+
+* slot positions, eviction victims, LSH codes: bit-exact;
+* an H2O decision may differ only where the oracle's relative score margin
+  is below 1e-6; such near-ties are counted and the oracle is then forced to
+  the device's choice so both trajectories stay aligned;
+* outputs within 2e-3 absolute + 1e-2 relative; accumulated scores within
+  1e-4 relative (+1e-12 absolute floor).
+"""
+import numpy as np
+import torch
+
+import oracle
+from kv_cache_eviction_h2o_gb300 import binding as L
+
+NEAR_TIE = 1e-6
+OUT_ATOL, OUT_RTOL = 2e-3, 1e-2
+SCORE_RTOL, SCORE_ATOL = 1e-4, 1e-12
+
+
+def tdtype(dtype):
+    return torch.bfloat16 if dtype == "bf16" else torch.float32
+
+
+def cdtype(dtype):
+    return L.H2O_BF16 if dtype == "bf16" else L.H2O_F32
+
+
+def to_dev(x, dtype):
+    """float32 numpy holding exactly representable values -> device tensor."""
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to("cuda").to(tdtype(dtype)).contiguous()
+
+
+def host_elems(dtype, shape):
+    return np.empty(shape, np.uint16 if dtype == "bf16" else np.float32)
+
+
+def widen(a, dtype):
+    if dtype == "bf16":
+        return (a.astype(np.uint32) << 16).view(np.float32)
+    return a
+
+
+class Dev:
+    """One device handle (H2O or LSH) for U units with its own stream."""
+
+    def __init__(self, kind, U, d, B, H, r, dtype, scale, W=None, split=0):
+        self.kind, self.U, self.d, self.B, self.dtype = kind, U, d, B, dtype
+        self.stream = torch.cuda.current_stream()
+        if kind == "h2o":
+            self.h = L.h2o_init(B, H, r, 1, U, d, cdtype(dtype), scale, self.stream)
+        else:
+            self.Wd = torch.from_numpy(np.ascontiguousarray(W, np.float32)).cuda()
+            self.h = L.lsh_init(B, r, 1, U, d, cdtype(dtype), scale, self.Wd, self.stream)
+        if split:
+            L.h2o_set_decode_split(self.h, split)
+        self.out = torch.empty((U, d), dtype=torch.float32, device="cuda")
+        self.victim = torch.empty((U,), dtype=torch.int32, device="cuda")
+
+    def prefill(self, Q, K, V):
+        self.Qd, self.Kd, self.Vd = (to_dev(x, self.dtype) for x in (Q, K, V))
+        T = Q.shape[1]
+        if self.kind == "h2o":
+            L.h2o_prefill(self.h, self.Qd, self.Kd, self.Vd, T)
+        else:
+            L.lsh_prefill(self.h, self.Qd, self.Kd, self.Vd, T)
+        L.h2o_sync(self.h)
+
+    def step(self, q, k, v):
+        qd, kd, vd = (to_dev(x, self.dtype) for x in (q, k, v))
+        if self.kind == "h2o":
+            L.h2o_decode_step(self.h, qd, kd, vd, self.out, self.victim)
+        else:
+            L.lsh_decode_step(self.h, qd, kd, vd, self.out, self.victim)
+        L.h2o_sync(self.h)
+        return self.out.cpu().numpy().astype(np.float64), self.victim.cpu().numpy()
+
+    def state(self):
+        U, B, d = self.U, self.B, self.d
+        K = host_elems(self.dtype, (U, B, d)); V = host_elems(self.dtype, (U, B, d))
+        score = np.empty((U, B)); pos = np.empty((U, B), np.int32)
+        code = np.empty((U, B), np.uint32); occ = np.empty(U, np.int32); npos = np.empty(U, np.int32)
+        L.h2o_get_state(self.h, K, V, score, pos, code, occ, npos)
+        return dict(K=widen(K, self.dtype), V=widen(V, self.dtype), score=score, pos=pos, code=code,
+                    occ=occ, npos=npos)
+
+    def stats(self, T):
+        m = np.empty((self.U, T), np.float32); l = np.empty((self.U, T), np.float32)
+        c = np.empty((self.U, T))
+        L.h2o_get_prefill_stats(self.h, m, l, c)
+        return m, l, c
+
+    def close(self):
+        L.h2o_destroy(self.h)
+
+
+def check_scores(g, o, what):
+    bad = np.abs(g - o) > SCORE_RTOL * np.abs(o) + SCORE_ATOL
+    assert not bad.any(), "%s: %d mismatches, worst |d|=%g at %s (dev %r, oracle %r)" % (
+        what, bad.sum(), np.abs(g - o).max(), np.argwhere(bad)[0], g[bad][0], o[bad][0])
+
+
+def check_out(g, o, what):
+    bad = np.abs(g - o) > OUT_ATOL + OUT_RTOL * np.abs(o)
+    assert not bad.any(), "%s: %d mismatches, worst |d|=%g" % (what, bad.sum(), np.abs(g - o).max())
+
+
+def kept_lists(pos, B):
+    """Ascending kept positions per unit, -1 padded to B."""
+    out = np.full((pos.shape[0], B), -1, np.int32)
+    for u in range(pos.shape[0]):
+        p = np.sort(pos[u][pos[u] >= 0])
+        out[u, :len(p)] = p
+    return out
+
+
+def align_prefill(dev_state, Q, K, V, B, H, r, scale):
+    """Oracle prompt phase compared with the device's; returns (oracle state,
+    oracle column sums, near-tie count).  Fails on any other disagreement."""
+    st, c, kept_o, margin = oracle.h2o_prefill(Q, K, V, B, H, r, scale)
+    kept_g = kept_lists(dev_state["pos"], B)
+    near = 0
+    U, T = c.shape
+    for u in range(U):
+        if (kept_g[u] == kept_o[u]).all():
+            continue
+        assert margin[u] < NEAR_TIE, "unit %d: kept set differs with margin %g" % (u, margin[u])
+        # the device's choice must be a valid top-H up to the near tie
+        go = set(kept_g[u][kept_g[u] >= 0].tolist()); oo = set(kept_o[u][kept_o[u] >= 0].tolist())
+        cut = min(c[u][j] for j in oo if j < T - r)
+        for j in go ^ oo:
+            assert abs(c[u][j] - cut) <= NEAR_TIE * abs(cut) + 1e-300, "unit %d: position %d off the cut" % (u, j)
+        near += 1
+    if near:
+        st = oracle.build_cache(K, V, c, kept_g, B)
+    return st, c, near
+
+
+def h2o_lockstep(dev, st, q, k, v, T, r, scale, check_every=1):
+    """Run the device and the oracle step by step; returns near-tie count."""
+    near = 0
+    S = q.shape[0]
+    for t in range(S):
+        p = T + t
+        out_g, vic_g = dev.step(q[t], k[t], v[t])
+        before = st.copy()
+        out_o, vic_o, mg, _ = oracle.h2o_decode_step(st, q[t], k[t], v[t], p, r, scale)
+        mism = vic_g != vic_o
+        if mism.any():
+            hard = mism & ~(mg < NEAR_TIE)
+            assert not hard.any(), "step %d: victims differ at units %s (margins %s)" % (
+                t, np.nonzero(hard)[0][:8], mg[hard][:8])
+            near += int(mism.sum())
+            st = before
+            forced = np.where(mism, vic_g, -1).astype(np.int32)
+            out_o, vic_o, mg, _ = oracle.h2o_decode_step(st, q[t], k[t], v[t], p, r, scale, forced)
+        check_out(out_g, out_o, "step %d out" % t)
+        if (t % check_every == 0) or t == S - 1:
+            g = dev.state()
+            assert (g["pos"] == st.pos).all(), "step %d: positions differ" % t
+            assert (g["occ"] == st.occ).all() and (g["npos"] == p + 1).all()
+            assert (g["K"] == st.K).all() and (g["V"] == st.V).all(), "step %d: cache rows differ" % t
+            check_scores(g["score"], st.score, "step %d scores" % t)
+    return near, st
+
+
+def lsh_lockstep(dev, st, q, k, v, W, T, r, scale, check_every=1):
+    S = q.shape[0]
+    for t in range(S):
+        p = T + t
+        out_g, vic_g = dev.step(q[t], k[t], v[t])
+        out_o, vic_o = oracle.lsh_decode_step(st, q[t], k[t], v[t], W, p, r, scale)
+        assert (vic_g == vic_o).all(), "step %d: LSH victims differ at %s" % (t, np.nonzero(vic_g != vic_o)[0][:8])
+        check_out(out_g, out_o, "LSH step %d out" % t)
+        if (t % check_every == 0) or t == S - 1:
+            g = dev.state()
+            assert (g["pos"] == st.pos).all(), "LSH step %d: positions differ" % t
+            assert (g["code"] == st.code).all(), "LSH step %d: codes differ" % t
+            assert (g["occ"] == st.occ).all()
+            assert (g["K"] == st.K).all() and (g["V"] == st.V).all(), "LSH step %d: cache rows differ" % t
+    return st

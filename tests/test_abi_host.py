@@ -1,0 +1,89 @@
+"""Host-only checks of the C ABI: the library loads, exports every symbol
+include/h2o.h declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "h2o.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b((?:h2o|lsh)_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from kv_cache_eviction_h2o_gb300 import build as b
+    b.build()
+    from kv_cache_eviction_h2o_gb300 import binding
+    return binding
+
+
+def test_header_declares_the_api():
+    names = _declared()
+    for must in ("h2o_init", "h2o_prefill", "h2o_decode_step", "lsh_decode_step", "lsh_init",
+                 "lsh_prefill", "h2o_get_state", "h2o_set_state", "h2o_sync", "h2o_destroy",
+                 "h2o_last_error"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    lib = L.lib()
+    for name in _declared():
+        assert hasattr(lib, name), name
+    # the binding wraps exactly the declared set
+    assert set(L.SIGNATURES) == set(_declared())
+    out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T ((?:h2o|lsh)_\w+)$", out, flags=re.M))
+    assert set(_declared()) <= exported
+
+
+def test_library_has_sm103a_code(L):
+    # the fat binary is tagged with the architecture it was built for
+    out = subprocess.run(["strings", L.LIB_PATH], capture_output=True, text=True).stdout
+    assert "sm_103a" in out
+
+
+@pytest.mark.parametrize("args,frag", [
+    ((0, 0, 0, 1, 1, 128, 1, 0.1), "budget"),
+    ((10, 5, 6, 1, 1, 128, 1, 0.1), "heavy + recent"),
+    ((10, 5, 5, 1, 1, 96, 1, 0.1), "head_dim"),
+    ((10, 5, 5, 1, 1, 128, 7, 0.1), "dtype"),
+    ((10, 5, 5, 0, 1, 128, 1, 0.1), "batch"),
+    ((10, 5, 5, 1, 1, 128, 1, -1.0), "scale"),
+    ((10, 5, 11, 1, 1, 128, 1, 0.1), "recent"),
+])
+def test_init_rejects_bad_arguments(L, args, frag):
+    with pytest.raises(L.H2OError) as e:
+        L.h2o_init(*args)
+    assert e.value.code == L.H2O_ERR_ARG
+    assert frag in str(e.value)
+
+
+def test_lsh_init_requires_projection(L):
+    with pytest.raises(L.H2OError) as e:
+        L.lsh_init(10, 5, 1, 1, 128, 1, 0.1, None)
+    assert e.value.code == L.H2O_ERR_ARG
+
+
+def test_null_handle_is_rejected(L):
+    lib = L.lib()
+    assert lib.h2o_prefill(None, None, None, None, 4) == L.H2O_ERR_ARG
+    assert lib.h2o_decode_step(None, None, None, None, None, None) == L.H2O_ERR_ARG
+    assert lib.lsh_decode_step(None, None, None, None, None, None) == L.H2O_ERR_ARG
+    assert lib.h2o_sync(None) == L.H2O_ERR_ARG
+    assert lib.h2o_get_state(None, None, None, None, None, None, None, None) == L.H2O_ERR_ARG
+    assert lib.h2o_set_decode_split(None, 2) == L.H2O_ERR_ARG
+    lib.h2o_destroy(None)          # no-op
+    assert "NULL" in L.h2o_last_error()
+
+
+def test_out_pointer_is_required(L):
+    lib = L.lib()
+    assert lib.h2o_init(None, 10, 5, 5, 1, 1, 128, 1, 0.1, None) == L.H2O_ERR_ARG

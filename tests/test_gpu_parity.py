@@ -1,0 +1,179 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs, at sizes the oracle finishes in seconds that still span
+several tiles, several bulk-copy groups and ragged tails."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+import oracle                                              # noqa: E402
+from kv_cache_eviction_h2o_gb300 import workloads as wl    # noqa: E402
+from parity import (Dev, align_prefill, check_out, check_scores, h2o_lockstep,  # noqa: E402
+                    kept_lists, lsh_lockstep)
+
+pytestmark = pytest.mark.gpu
+
+
+def _rand(seed, U, T, S, d, dtype, key_scale=1.0):
+    g = np.random.default_rng(seed)
+    f = (lambda x: wl.round_bf16(x)) if dtype == "bf16" else (lambda x: x.astype(np.float32))
+    Q = f(g.standard_normal((U, T, d), dtype=np.float32))
+    K = f(g.standard_normal((U, T, d), dtype=np.float32) * key_scale)
+    V = f(g.standard_normal((U, T, d), dtype=np.float32))
+    q = f(g.standard_normal((S, U, d), dtype=np.float32))
+    k = f(g.standard_normal((S, U, d), dtype=np.float32) * key_scale)
+    v = f(g.standard_normal((S, U, d), dtype=np.float32))
+    return Q, K, V, q, k, v
+
+
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 130, 257])
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
+def test_prefill_statistics(T, dtype, d):
+    U = 3
+    Q, K, V, *_ = _rand(100 + T, U, T, 0, d, dtype, key_scale=2.0)
+    scale = 1.0 / np.sqrt(d)
+    dev = Dev("h2o", U, d, 16, 8, 8, dtype, scale)
+    dev.prefill(Q, K, V)
+    m, l, c = dev.stats(T)
+    mo, lo, co = oracle.prefill_scores(Q, K, scale)
+    np.testing.assert_allclose(m, mo, rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(l, lo, rtol=1e-4)
+    check_scores(c, co, "column sums")
+    np.testing.assert_allclose(c.sum(axis=1), T, rtol=1e-5)
+    dev.close()
+
+
+def test_tiny_workload_h2o():
+    w = wl.WORKLOADS["tiny"]
+    g = wl.generate(w)
+    dev = Dev("h2o", w.units, w.head_dim, w.budget, w.heavy, w.recent, w.dtype, w.scale)
+    dev.prefill(g["Q"], g["K"], g["V"])
+    st, c, near0 = align_prefill(dev.state(), g["Q"], g["K"], g["V"], w.budget, w.heavy, w.recent, w.scale)
+    s = dev.state()
+    assert (s["pos"] == st.pos).all()
+    check_scores(s["score"], st.score, "prefill scores")
+    near, _ = h2o_lockstep(dev, st, g["q"], g["k"], g["v"], w.prompt, w.recent, w.scale)
+    print("tiny: near ties prefill %d decode %d" % (near0, near))
+    dev.close()
+
+
+@pytest.mark.parametrize("split", [1, 2, 3, 4, 8, 16])
+def test_opt67b_units_h2o(split):
+    w = wl.WORKLOADS["opt-6.7b"]
+    units = list(range(12))
+    g = wl.generate(w, units=units, steps=24)
+    U = len(units)
+    dev = Dev("h2o", U, w.head_dim, w.budget, w.heavy, w.recent, w.dtype, w.scale, split=split)
+    dev.prefill(g["Q"], g["K"], g["V"])
+    st, c, near0 = align_prefill(dev.state(), g["Q"], g["K"], g["V"], w.budget, w.heavy, w.recent, w.scale)
+    s = dev.state()
+    assert (s["pos"] == st.pos).all()
+    assert (s["K"] == st.K).all()
+    check_scores(s["score"], st.score, "prefill scores")
+    near, _ = h2o_lockstep(dev, st, g["q"], g["k"], g["v"], w.prompt, w.recent, w.scale, check_every=4)
+    print("opt-6.7b split %d: near ties prefill %d decode %d" % (split, near0, near))
+    dev.close()
+
+
+@pytest.mark.parametrize("split", [1, 3, 16])
+def test_hashevict_units(split):
+    w = wl.WORKLOADS["hashevict-opt-6.7b"]
+    units = list(range(10))
+    g = wl.generate(w, units=units, steps=24)
+    W = g["W"]
+    U = len(units)
+    dev = Dev("lsh", U, w.head_dim, w.budget, 0, w.recent, w.dtype, w.scale, W=W, split=split)
+    dev.prefill(g["Q"], g["K"], g["V"])
+    st = oracle.lsh_prefill(g["Q"], g["K"], g["V"], W, w.budget, w.recent)
+    s = dev.state()
+    assert (s["pos"] == st.pos).all()
+    assert (s["code"] == st.code).all()
+    assert (s["K"] == st.K).all() and (s["V"] == st.V).all()
+    lsh_lockstep(dev, st, g["q"], g["k"], g["v"], W, w.prompt, w.recent, w.scale, check_every=4)
+    dev.close()
+
+
+@pytest.mark.parametrize("T,B,H,r", [
+    (5, 8, 4, 4),        # prompt shorter than the budget: append phase
+    (1, 8, 4, 4),        # single-token prompt
+    (40, 8, 0, 8),       # no heavy hitters: sliding window
+    (40, 8, 8, 0),       # no recent window
+    (40, 1, 0, 1),       # one slot
+    (40, 1, 1, 0),
+    (70, 33, 17, 16),    # ragged groups and tiles
+    (130, 129, 64, 65),
+])
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
+def test_edge_cases_h2o(T, B, H, r, dtype, d):
+    U, S = 3, 12
+    Q, K, V, q, k, v = _rand(7 * T + B, U, T, S, d, dtype, key_scale=1.5)
+    scale = 1.0 / np.sqrt(d)
+    dev = Dev("h2o", U, d, B, H, r, dtype, scale)
+    dev.prefill(Q, K, V)
+    st, c, _ = align_prefill(dev.state(), Q, K, V, B, H, r, scale)
+    h2o_lockstep(dev, st, q, k, v, T, r, scale)
+    dev.close()
+
+
+@pytest.mark.parametrize("T,B,r", [(5, 8, 4), (1, 8, 4), (40, 8, 8), (40, 8, 0), (40, 1, 1), (70, 33, 16)])
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
+def test_edge_cases_lsh(T, B, r, dtype, d):
+    U, S = 3, 12
+    Q, K, V, q, k, v = _rand(11 * T + B, U, T, S, d, dtype)
+    W = np.random.default_rng(5).standard_normal((d, 32), dtype=np.float32)
+    scale = 1.0 / np.sqrt(d)
+    dev = Dev("lsh", U, d, B, 0, r, dtype, scale, W=W)
+    dev.prefill(Q, K, V)
+    st = oracle.lsh_prefill(Q, K, V, W, B, r)
+    s = dev.state()
+    assert (s["pos"] == st.pos).all() and (s["code"] == st.code).all()
+    lsh_lockstep(dev, st, q, k, v, W, T, r, scale)
+    dev.close()
+
+
+def test_full_attention_when_budget_covers_sequence():
+    # budget >= prompt + steps: nothing is evicted and every output is full
+    # causal attention over all tokens so far
+    U, T, S, d = 2, 50, 20, 128
+    Q, K, V, q, k, v = _rand(3, U, T, S, d, "bf16")
+    scale = 1.0 / np.sqrt(d)
+    dev = Dev("h2o", U, d, T + S, 30, T + S - 30, "bf16", scale)
+    dev.prefill(Q, K, V)
+    for t in range(S):
+        out, vic = dev.step(q[t], k[t], v[t])
+        assert (vic == -1).all()
+        for u in range(U):
+            Ka = np.concatenate([K[u], k[: t + 1, u]]).astype(np.float64)
+            Va = np.concatenate([V[u], v[: t + 1, u]]).astype(np.float64)
+            z = scale * Ka @ q[t, u].astype(np.float64)
+            e = np.exp(z - z.max())
+            check_out(out[u:u + 1], ((e / e.sum()) @ Va)[None], "full attention")
+    dev.close()
+
+
+def test_state_roundtrip_and_errors():
+    from kv_cache_eviction_h2o_gb300 import binding as L
+    U, T, d = 2, 30, 64
+    Q, K, V, q, k, v = _rand(9, U, T, 3, d, "f32")
+    dev = Dev("h2o", U, d, 10, 5, 5, "f32", 0.125)
+    # decode before prefill is a state error
+    qd = torch.zeros((U, d), device="cuda")
+    with pytest.raises(L.H2OError) as e:
+        L.h2o_decode_step(dev.h, qd, qd, qd, dev.out, None)
+    assert e.value.code == L.H2O_ERR_STATE
+    # lsh call on an H2O handle
+    dev.prefill(Q, K, V)
+    with pytest.raises(L.H2OError) as e:
+        L.lsh_decode_step(dev.h, qd, qd, qd, dev.out, None)
+    assert e.value.code == L.H2O_ERR_STATE
+    s = dev.state()
+    dev2 = Dev("h2o", U, d, 10, 5, 5, "f32", 0.125)
+    Kh = s["K"].astype(np.float32); Vh = s["V"].astype(np.float32)
+    L.h2o_set_state(dev2.h, Kh, Vh, s["score"], s["pos"], None, s["occ"], s["npos"])
+    o1, v1 = dev.step(q[0], k[0], v[0])
+    o2, v2 = dev2.step(q[0], k[0], v[0])
+    assert (v1 == v2).all()
+    np.testing.assert_array_equal(o1, o2)
+    dev.close(); dev2.close()
