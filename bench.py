@@ -1,0 +1,499 @@
+#!/usr/bin/env python3
+"""Whole-job throughput of the budgeted-KV decode path on GB300.
+
+One bench step is one pass of the whole hot path over one batch of synthetic
+input shaped like an OPT-6.7B attention layer (8 x 32 heads, head_dim 128,
+prompt 2048, 256 decode steps, budget 410 = 205 heavy + 205 recent, bf16):
+
+  for each of L layer caches: H2O prompt phase (scores, top-k, gather) and
+  HashEvict prompt phase (codes, replay, gather) on the same prompt;
+  then 256 H2O decode steps and 256 HashEvict decode steps, token-major over
+  the L layers, as a model decodes.
+
+L layers (default 8, ~890 MB of caches plus 3.2 GB of prompts) keep every
+cache out of L2 between its uses.  The device-timed value replays the step
+from CUDA graphs with inputs already in HBM; the e2e value drives the same
+job through the public API with pinned host inputs copied in and outputs
+copied out inside the timed region.  The CPU oracle is timed on a bounded
+sample of the same job.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "H2O decode steps/s (batch×heads) at 1 GB300; achieved HBM GB/s vs peak"
+UNIT = "steps/s"
+WORKLOAD = "opt-6.7b"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--layers", type=int, default=8)
+    p.add_argument("--decode-steps", type=int, default=None)
+    p.add_argument("--split", type=int, default=0, help="CTAs per unit in decode (0 = automatic)")
+    p.add_argument("--oracle-units", type=int, default=32)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def file_digest(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "kv_cache_eviction_h2o_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """Per-launch DRAM bytes from the committed ncu capture, if it was taken
+    on the current kernel source; None otherwise."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        e = d[kernel]
+        if e["source_digest"] != file_digest(*e["sources"]):
+            return None
+        return float(e["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class Clocks:
+    """nvidia-smi sampler for the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu):
+        self.gpu = gpu
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.gpu)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        rows = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), float(f[3]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        loaded = [r for r in rows if r[2] > 0.25 * max(x[2] for x in rows)] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(r[2] for r in rows)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------ algorithmic
+
+def decode_bytes(U, B, d, eb, lsh):
+    """Algorithmic HBM bytes of one full-cache decode launch over U units:
+    per live slot K and V rows, plus score read+write (fp64) and position
+    read (H2O) or code and position read (HashEvict); per unit q, k, v in,
+    fp32 out, one K/V row written, victim score/code and position written,
+    unit state read and written; plus the projection matrix once."""
+    row = d * eb
+    if lsh:
+        per_slot = 2 * row + 4 + 4
+        fixed = 3 * row + 4 * d + 2 * row + 4 + 4 + 16
+        return U * (B * per_slot + fixed) + d * 32 * 4
+    per_slot = 2 * row + 8 + 8 + 4
+    fixed = 3 * row + 4 * d + 2 * row + 8 + 4 + 16
+    return U * (B * per_slot + fixed)
+
+
+def prefill_flops(U, T, d):
+    """Both score passes of the H2O prompt phase: 2 x (2 d flops per causal
+    (i, j) pair, T (T + 1) / 2 pairs per unit)."""
+    return 2 * 2 * U * d * T * (T + 1) // 2
+
+
+# ------------------------------------------------------------------ oracle
+
+def oracle_job(w, wl_lsh, units, S):
+    """The CPU oracle on a sample of units: H2O prompt + S steps and
+    HashEvict prompt + S steps.  Returns (seconds, threads)."""
+    import numpy as np
+
+    import oracle
+    from kv_cache_eviction_h2o_gb300 import workloads as wl
+    g = wl.generate(w, units=units, steps=S)
+    W = wl.lsh_matrix(wl_lsh)
+    T = w.prompt
+    t0 = time.perf_counter()
+    st, _, _, _ = oracle.h2o_prefill(g["Q"], g["K"], g["V"], w.budget, w.heavy, w.recent, w.scale)
+    for t in range(S):
+        oracle.h2o_decode_step(st, g["q"][t], g["k"][t], g["v"][t], T + t, w.recent, w.scale)
+    ls = oracle.lsh_prefill(g["Q"], g["K"], g["V"], W, wl_lsh.budget, wl_lsh.recent)
+    for t in range(S):
+        oracle.lsh_decode_step(ls, g["q"][t], g["k"][t], g["v"][t], W, T + t, wl_lsh.recent, w.scale)
+    return time.perf_counter() - t0, oracle.get_threads()
+
+
+def oracle_rate(w, seconds, n_units, S):
+    """Oracle time on n_units scaled to the metric: decode steps (all units of
+    one layer cache advancing one token, both variants) per second."""
+    per_layer_job = seconds * w.units / n_units
+    return 2 * S / per_layer_job
+
+
+# -------------------------------------------------------------- reference
+
+def run_reference(args):
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return
+    from kv_cache_eviction_h2o_gb300 import workloads as wl
+    w = wl.WORKLOADS[WORKLOAD]
+    wl_lsh = wl.WORKLOADS["hashevict-" + WORKLOAD]
+    S = args.decode_steps or w.steps
+    n = max(1, args.oracle_units // 4)
+    units = list(range(n))
+    for _ in range(args.warmup):
+        oracle_job(w, wl_lsh, units, S)
+    times = []
+    threads = 1
+    for _ in range(args.steps):
+        t, threads = oracle_job(w, wl_lsh, units, S)
+        times.append(t)
+    total = sum(times)
+    value = oracle_rate(w, total / len(times), n, S)
+    sample = "%d of %d units of one %s layer per step (prompt %d, %d decode steps, H2O + HashEvict)" % (
+        n, w.units, WORKLOAD, w.prompt, S)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * total / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "%s-shaped layer: H2O + HashEvict, prompt %d -> %d decode steps, budget %d"
+                               % (WORKLOAD, w.prompt, S, w.budget)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# -------------------------------------------------------------------- ours
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from kv_cache_eviction_h2o_gb300 import binding as L
+    from kv_cache_eviction_h2o_gb300 import build as lib_build
+    from kv_cache_eviction_h2o_gb300 import workloads as wl
+
+    world, rank, local = dist_setup(args)
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(local)
+    lib_build.build()
+    L.lib()
+    w = wl.WORKLOADS[WORKLOAD]
+    wl_lsh = wl.WORKLOADS["hashevict-" + WORKLOAD]
+    S = args.decode_steps or w.steps
+    NL = args.layers
+    U, T, d, B = w.units, w.prompt, w.head_dim, w.budget
+    dt = L.H2O_BF16
+    stream = torch.cuda.Stream()
+
+    # ---- inputs resident in HBM, one set per layer cache
+    layers = []
+    with torch.cuda.stream(stream):
+        for li in range(NL):
+            g = wl.generate_device(w, seed_offset=li + 1000 * rank, steps=S)
+            layers.append(g)
+        W = torch.from_numpy(wl.lsh_matrix(wl_lsh)).cuda()
+    torch.cuda.synchronize()
+    h2o = [L.h2o_init(B, w.heavy, w.recent, w.batch, w.heads, d, dt, w.scale, stream) for _ in range(NL)]
+    lsh = [L.lsh_init(B, wl_lsh.recent, w.batch, w.heads, d, dt, w.scale, W, stream) for _ in range(NL)]
+    if args.split:
+        for h in h2o + lsh:
+            L.h2o_set_decode_split(h, args.split)
+    out_h = [torch.empty((S, U, d), dtype=torch.float32, device="cuda") for _ in range(NL)]
+    out_l = [torch.empty((S, U, d), dtype=torch.float32, device="cuda") for _ in range(NL)]
+    vic_h = [torch.empty((S, U), dtype=torch.int32, device="cuda") for _ in range(NL)]
+    vic_l = [torch.empty((S, U), dtype=torch.int32, device="cuda") for _ in range(NL)]
+
+    def pre_h2o():
+        for li in range(NL):
+            g = layers[li]
+            L.h2o_prefill(h2o[li], g["Q"], g["K"], g["V"], T)
+
+    def pre_lsh():
+        for li in range(NL):
+            g = layers[li]
+            L.lsh_prefill(lsh[li], g["Q"], g["K"], g["V"], T)
+
+    def dec_h2o():
+        for t in range(S):
+            for li in range(NL):
+                g = layers[li]
+                L.h2o_decode_step(h2o[li], g["q"][t], g["k"][t], g["v"][t], out_h[li][t], vic_h[li][t])
+
+    def dec_lsh():
+        for t in range(S):
+            for li in range(NL):
+                g = layers[li]
+                L.lsh_decode_step(lsh[li], g["q"][t], g["k"][t], g["v"][t], out_l[li][t], vic_l[li][t])
+
+    phases = [("h2o_prefill", pre_h2o), ("lsh_prefill", pre_lsh), ("h2o_decode", dec_h2o), ("lsh_decode", dec_lsh)]
+    # eager pass: allocates prompt scratch, sets kernel attributes, checks errors
+    with torch.cuda.stream(stream):
+        for _, f in phases:
+            f()
+    for h in h2o + lsh:
+        L.h2o_sync(h)
+
+    graphs = []
+    with torch.cuda.stream(stream):
+        for name, f in phases:
+            gr = torch.cuda.CUDAGraph()
+            gr.capture_begin()
+            f()
+            gr.capture_end()
+            graphs.append((name, gr))
+    torch.cuda.synchronize()
+
+    def one_step(evs=None):
+        with torch.cuda.stream(stream):
+            for i, (name, gr) in enumerate(graphs):
+                gr.replay()
+                if evs is not None:
+                    evs[i].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    for h in h2o + lsh:
+        L.h2o_sync(h)
+
+    # ---- timed region
+    clocks = Clocks(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    step_events = [[torch.cuda.Event(enable_timing=True) for _ in graphs] for _ in range(args.steps)]
+    start.record(stream)
+    for i in range(args.steps):
+        one_step(step_events[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    elapsed_ms = start.elapsed_time(end)
+    phase_ms = {name: 0.0 for name, _ in graphs}
+    for i in range(args.steps):
+        prev = start if i == 0 else step_events[i - 1][-1]
+        for j, (name, _) in enumerate(graphs):
+            phase_ms[name] += prev.elapsed_time(step_events[i][j])
+            prev = step_events[i][j]
+    for h in h2o + lsh:
+        L.h2o_sync(h)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    K = args.steps
+    ms_per_step = elapsed_ms / K
+    decode_steps_per_bench_step = 2 * S * NL
+    value = world * decode_steps_per_bench_step / (ms_per_step / 1000.0)
+    hbm, tf_burst, tf_sus, peak_src = load_peaks()
+
+    # ---- rooflines from the phase times (per-launch averages)
+    eb = 2
+    rl = []
+    n_dec = S * NL * K
+    for name, lsh_flag, src in (("h2o_decode", False, ["decode.cu", "common.cuh"]),
+                                ("lsh_decode", True, ["decode.cu", "common.cuh"])):
+        t_launch = phase_ms[name] / n_dec / 1000.0
+        by = decode_bytes(U, B, d, eb, lsh_flag)
+        ach = by / t_launch / 1e9
+        rl.append({"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                   "frac": ach / hbm, "traffic": ncu_traffic(name), "algorithmic_bytes": by,
+                   "launch_us": t_launch * 1e6, "peak_source": peak_src, "share": phase_ms[name] / elapsed_ms})
+    t_pre = phase_ms["h2o_prefill"] / (NL * K) / 1000.0
+    fl = prefill_flops(U, T, d)
+    ach = fl / t_pre / 1e12
+    rl.append({"kernel": "h2o_prefill", "bound": "tensor", "achieved": ach, "peak": tf_sus, "unit": "TFLOP/s",
+               "frac": ach / tf_sus, "traffic": None, "algorithmic_flops": fl, "launch_us": t_pre * 1e6,
+               "peak_source": peak_src, "share": phase_ms["h2o_prefill"] / elapsed_ms})
+    t_lp = phase_ms["lsh_prefill"] / (NL * K) / 1000.0
+    rl.append({"kernel": "lsh_prefill", "bound": "latency", "launch_us": t_lp * 1e6,
+               "share": phase_ms["lsh_prefill"] / elapsed_ms})
+    dominant = max(rl, key=lambda r: r["share"])
+    main_rl = {k: dominant[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic") if k in dominant}
+    main_rl["kernel"] = dominant["kernel"]
+    main_rl["peak_source"] = peak_src
+    if "achieved" not in main_rl:
+        main_rl = {k: rl[0][k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+        main_rl["kernel"] = rl[0]["kernel"]
+
+    # ---- end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, L, torch, layers, h2o, lsh, out_h, out_l, vic_h, vic_l, W, S, NL, T, stream, world)
+
+    # ---- CPU oracle on a bounded sample (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        n = args.oracle_units
+        secs, threads = oracle_job(w, wl_lsh, list(range(n)), S)
+        cpu = {"value": oracle_rate(w, secs, n, S), "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": "%d of %d units of one layer (prompt %d, %d decode steps, H2O + HashEvict), %.1f s"
+                         % (n, U, T, S, secs)}
+
+    launches_per_step = NL * (4 + 3) + 2 * S * NL
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "%s-shaped layer x%d: H2O + HashEvict, prompt %d -> %d decode steps, budget %d "
+                               "(%d heavy + %d recent)" % (WORKLOAD, NL, T, S, B, w.heavy, w.recent),
+                   "batch": w.batch, "heads": w.heads, "head_dim": d, "prompt": T, "decode_steps": S,
+                   "budget": B, "layers": NL, "global_batch": w.batch * world,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2: %d layer caches (%.0f MB) + prompts (%.0f MB); a cache is reused "
+                         "only after %d others" % (NL, 2 * NL * decode_bytes(U, B, d, eb, False) / 1e6,
+                                                   NL * 3 * U * T * d * eb / 1e6, NL - 1),
+                   "step": "one decode step = all %d (batch x head) units of one layer cache advance one token; "
+                           "both eviction variants counted; prompt phases inside the timed step" % U},
+        "roofline": main_rl,
+        "rooflines": rl,
+        "phases_ms_per_step": {k: v / K for k, v in phase_ms.items()},
+        "head_steps_per_s": value * U,
+        "cpu_baseline": cpu,
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+    }
+    for h in h2o + lsh:
+        L.h2o_destroy(h)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, L, torch, layers, h2o, lsh, out_h, out_l, vic_h, vic_l, W, S, NL, T, stream, world):
+    """Same job through the public API, eager, with every input copied in from
+    pinned host memory and every output copied out inside the timed region."""
+    host_in = []
+    for g in layers:
+        host_in.append({k: g[k].cpu().pin_memory() for k in ("Q", "K", "V", "q", "k", "v")})
+    host_out = [(torch.empty(o.shape, dtype=o.dtype).pin_memory(), torch.empty(o2.shape, dtype=o2.dtype).pin_memory(),
+                 torch.empty(v.shape, dtype=v.dtype).pin_memory(), torch.empty(v2.shape, dtype=v2.dtype).pin_memory())
+                for o, o2, v, v2 in zip(out_h, out_l, vic_h, vic_l)]
+    h2d = sum(x.numel() * x.element_size() for hi in host_in for x in hi.values())
+    d2h = sum(x.numel() * x.element_size() for ho in host_out for x in ho)
+
+    def step():
+        with torch.cuda.stream(stream):
+            for li in range(NL):
+                for k in ("Q", "K", "V", "q", "k", "v"):
+                    layers[li][k].copy_(host_in[li][k], non_blocking=True)
+            for li in range(NL):
+                g = layers[li]
+                L.h2o_prefill(h2o[li], g["Q"], g["K"], g["V"], T)
+                L.lsh_prefill(lsh[li], g["Q"], g["K"], g["V"], T)
+            for t in range(S):
+                for li in range(NL):
+                    g = layers[li]
+                    L.h2o_decode_step(h2o[li], g["q"][t], g["k"][t], g["v"][t], out_h[li][t], vic_h[li][t])
+            for t in range(S):
+                for li in range(NL):
+                    g = layers[li]
+                    L.lsh_decode_step(lsh[li], g["q"][t], g["k"][t], g["v"][t], out_l[li][t], vic_l[li][t])
+            for li in range(NL):
+                ho = host_out[li]
+                ho[0].copy_(out_h[li], non_blocking=True)
+                ho[1].copy_(out_l[li], non_blocking=True)
+                ho[2].copy_(vic_h[li], non_blocking=True)
+                ho[3].copy_(vic_l[li], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, 3))
+    t0 = time.perf_counter()
+    for _ in range(n):
+        step()
+    torch.cuda.synchronize()
+    secs = (time.perf_counter() - t0) / n
+    value = world * 2 * S * NL / secs
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": secs * 1000.0, "steps": n}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -461,10 +461,18 @@ cudaError_t stats_t(const CacheView& c, const PromptArgs& p, cudaStream_t st)
     const int nb = (p.T + kTile - 1) / kTile;
     dim3 grid((unsigned)nb, (unsigned)c.U);
     const size_t smem = 2 * (size_t)D * (kTile + kPad) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(rowstats_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(colsum_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(rowstats_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(colsum_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
     rowstats_kernel<T, D><<<grid, 256, smem, st>>>(reinterpret_cast<const T*>(p.Q),
                                                  reinterpret_cast<const T*>(p.K), p.T, c.qscale, p.m2, p.l);
     e = cudaGetLastError();
@@ -495,8 +503,16 @@ cudaError_t lsh_t(const CacheView& c, const PromptArgs& p, const float* W, cudaS
     if (e != cudaSuccess) return e;
     const size_t smem = (size_t)c.B * 8;
     if (smem > 48 * 1024) {
-        e = cudaFuncSetAttribute(lsh_replay_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        static size_t configured[64] = {0};
+        int dev = 0;
+        e = cudaGetDevice(&dev);
         if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (configured[dev] < smem) {
+            e = cudaFuncSetAttribute(lsh_replay_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            configured[dev] = smem;
+        }
     }
     lsh_replay_kernel<<<(unsigned)c.U, kReplayThreads, smem, st>>>(c, p);
     e = cudaGetLastError();

@@ -195,3 +195,66 @@ def generate(w: Workload, units: Optional[Sequence[int]] = None,
     if w.lsh:
         out["W"] = lsh_matrix(w)
     return out
+
+
+def generate_device(w: Workload, seed_offset: int = 0, prompt: Optional[int] = None,
+                    steps: Optional[int] = None, device: str = "cuda"):
+    """The same recipe drawn with torch's device generator, for full-size
+    benchmark pools (values differ from ``generate``; distributions and
+    structure match).  Returns device tensors Q, K, V [U, T, d] and q, k, v
+    [S, U, d] in the workload's element type, plus W [d, 32] for LSH."""
+    import torch
+
+    T = w.prompt if prompt is None else prompt
+    S = w.steps if steps is None else steps
+    U, d = w.units, w.head_dim
+    g = torch.Generator(device=device)
+    g.manual_seed(1_000_003 * (w.seed + 1) + seed_offset)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def normal(*shape):
+        return torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
+
+    basis = None
+    if w.structure and w.structure[0] == "rank":
+        rank = int(w.structure[1])
+        basis = torch.linalg.qr(normal(U, d, rank))[0].transpose(1, 2).contiguous()   # [U, rank, d]
+    u_dir = None
+    if w.structure and w.structure[0] == "outlier_dir":
+        u_dir = normal(d)
+        u_dir = u_dir / u_dir.norm()
+
+    def keys(Kx, first_pos):
+        # Kx: [U, n, d] (prompt) or [n, U, d] transposed by the caller
+        if not w.structure:
+            return Kx
+        kind = w.structure[0]
+        n = Kx.shape[1]
+        if kind == "rank":
+            coef = normal(U, n, basis.shape[1])
+            return Kx + float(w.structure[2]) * torch.bmm(coef, basis)
+        if kind == "outlier_dir":
+            frac, factor = float(w.structure[1]), float(w.structure[2])
+            mask = (torch.rand(U, n, generator=g, device=device) < frac).unsqueeze(-1)
+            proj = (Kx @ u_dir).unsqueeze(-1) * u_dir
+            return torch.where(mask, Kx + (factor - 1.0) * proj, Kx)
+        if kind == "sink_norm":
+            nsink, frac, factor = int(w.structure[1]), float(w.structure[2]), float(w.structure[3])
+            mask = torch.rand(U, n, generator=g, device=device) < frac
+            posn = first_pos + torch.arange(n, device=device)
+            mask |= (posn < nsink).unsqueeze(0)
+            return torch.where(mask.unsqueeze(-1), Kx * factor, Kx)
+        raise ValueError(kind)
+
+    out = {
+        "Q": normal(U, T, d).to(dt).contiguous(),
+        "K": keys(normal(U, T, d), 0).to(dt).contiguous(),
+        "V": normal(U, T, d).to(dt).contiguous(),
+    }
+    if S > 0:
+        out["q"] = normal(S, U, d).to(dt).contiguous()
+        out["k"] = keys(normal(U, S, d), T).transpose(0, 1).to(dt).contiguous()
+        out["v"] = normal(S, U, d).to(dt).contiguous()
+    if w.lsh:
+        out["W"] = torch.from_numpy(lsh_matrix(w)).to(device)
+    return out
