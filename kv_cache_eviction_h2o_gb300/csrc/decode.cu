@@ -25,6 +25,7 @@
 // handle's error word.
 #include <cfloat>
 #include <climits>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -33,13 +34,19 @@ namespace h2o {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kGroup = 8;                  // slots per bulk-copy group
 constexpr int kMaxSplit = 16;              // CTAs per cluster (non-portable above 8)
-constexpr int kSlotsPerThread = 4;
-constexpr int kMaxChunk = kThreads * kSlotsPerThread;  // slots per CTA
+constexpr int kMaxChunk = 1024;            // slots per CTA
 constexpr unsigned kFull = 0xffffffffu;
+
+// Tile shape of the decode kernels: NW warps per CTA, each streaming groups of
+// G slots through a private ring of NBUF shared-memory buffers.
+template <int NW_, int G_, int NBUF_>
+struct Tile {
+    static constexpr int NW = NW_, NT = 32 * NW_, G = G_, NBUF = NBUF_;
+    static constexpr int SPT = kMaxChunk / NT;            // slots per thread in the score pass
+    static constexpr int LOG2G = G_ == 8 ? 3 : (G_ == 4 ? 2 : 1);
+    static_assert(G_ == 2 || G_ == 4 || G_ == 8, "group size");
+};
 
 template <int D>
 struct Exchange {                 // every CTA has one; rank 0's is the meeting point
@@ -52,51 +59,58 @@ struct Exchange {                 // every CTA has one; rank 0's is the meeting 
     float o[kMaxSplit][D];        // per-CTA unnormalised output
 };
 
-template <typename T, int D, int NBUF>
+template <typename T, int D, class TL>
 struct DecodeSmem {
-    T buf[kWarps][NBUF][2][kGroup * D];   // per-warp ring: [K rows | V rows]
-    uint64_t bar[kWarps][NBUF];
+    T buf[TL::NW][TL::NBUF][2][TL::G * D];   // per-warp ring: [K rows | V rows]
+    uint64_t bar[TL::NW][TL::NBUF];
     Exchange<D> x;
     float z[kMaxChunk];                   // base-2 logits of this CTA's slots
-    float wo[kWarps][D];
-    alignas(16) float e[kWarps][kGroup];
-    float wm[kWarps];
-    float wl[kWarps];
+    float wo[TL::NW][D];
+    alignas(16) float e[TL::NW][TL::G < 4 ? 4 : TL::G];
+    float wm[TL::NW];
+    float wl[TL::NW];
     float qf[D];
     float kf[D];
-    double rd[2][kWarps];
-    int ri[2][kWarps];
-    unsigned long long ru[2][kWarps];
+    double rd[2][TL::NW];
+    int ri[2][TL::NW];
+    unsigned long long ru[2][TL::NW];
     float M, invL, z_new, P_new;
     int victim;
     unsigned code_q, code_k;
 };
 
-// Sum 8 per-lane partials over the warp; lane l receives the total of
-// partial j = (l >> 2) & 7 (9 shuffles instead of 40).
-__device__ __forceinline__ float reduce8_transposed(const float (&v)[8], int lane)
+// Sum G per-lane partials over the warp: each exchange level keeps half of
+// the live partials and sends the other half, so lane l ends up with the
+// total of partial j, j read from lane bits 4, 3, ... (most significant
+// first); log2(G) + (5 - log2(G)) = 5 shuffle levels, G - 1 + 5 - log2(G)
+// shuffles instead of 5 G.
+template <int G>
+__device__ __forceinline__ float reduce_transposed(float (&v)[G], int lane)
 {
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-    float a[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float keep = b4 ? v[i + 4] : v[i];
-        const float send = b4 ? v[i] : v[i + 4];
-        a[i] = keep + __shfl_xor_sync(kFull, send, 16);
-    }
-    float b[2];
+    for (int k = 0; (G >> k) > 1; ++k) {
+        const int half = (G >> k) / 2;
+        const bool up = (lane >> (4 - k)) & 1;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float keep = b3 ? a[i + 2] : a[i];
-        const float send = b3 ? a[i] : a[i + 2];
-        b[i] = keep + __shfl_xor_sync(kFull, send, 8);
+        for (int i = 0; i < half; ++i) {
+            const float keep = up ? v[i + half] : v[i];
+            const float send = up ? v[i] : v[i + half];
+            v[i] = keep + __shfl_xor_sync(kFull, send, 16 >> k);
+        }
     }
-    const float keep = b2 ? b[1] : b[0];
-    const float send = b2 ? b[0] : b[1];
-    float c = keep + __shfl_xor_sync(kFull, send, 4);
-    c += __shfl_xor_sync(kFull, c, 2);
-    c += __shfl_xor_sync(kFull, c, 1);
+    float c = v[0];
+    constexpr int lg = G == 8 ? 3 : (G == 4 ? 2 : 1);
+#pragma unroll
+    for (int o = 16 >> lg; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
     return c;
+}
+
+// slot (within a group of G) whose total lane `lane` holds after the reduction
+template <int G>
+__device__ __forceinline__ int owned_slot(int lane)
+{
+    constexpr int lg = G == 8 ? 3 : (G == 4 ? 2 : 1);
+    return (lane >> (5 - lg)) & (G - 1);
 }
 
 __device__ __forceinline__ float safe_exp2_diff(float a, float m)
@@ -107,19 +121,21 @@ __device__ __forceinline__ float safe_exp2_diff(float a, float m)
 // Per-warp streaming online softmax over this CTA's chunk [c0, c1) of live
 // slots.  `skip` (absolute slot) is left out of the softmax.  When keep_z,
 // logits are stored in S.z[slot - c0].  Returns through (m_run, l_run, o).
-template <typename T, int D, int NBUF>
-__device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, NBUF>& S, const T* Kc, const T* Vc,
+template <typename T, int D, class TL>
+__device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL>& S, const T* Kc, const T* Vc,
                                              int c0, int c1, int skip, bool keep_z,
                                              const float (&qr)[D / 32], float& m_run,
                                              float& l_run, float (&o)[D / 32], int* err)
 {
     constexpr int EPL = D / 32;
+    constexpr int G = TL::G, NW = TL::NW, NBUF = TL::NBUF;
+    constexpr int OWN = (1 << (5 - TL::LOG2G)) - 1;     // lanes sharing one slot's total
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int len = c1 - c0;
-    const int ngroups = (len + kGroup - 1) / kGroup;
+    const int ngroups = (len + G - 1) / G;
     bool timed_out = false;
     int it = 0;
-    for (int g = warp; g < ngroups; g += kWarps, ++it) {
+    for (int g = warp; g < ngroups; g += NW, ++it) {
         const int b = it % NBUF;
         const uint32_t parity = (uint32_t)(it / NBUF) & 1u;
         if (!mbar_wait(&S.bar[warp][b], parity)) {
@@ -128,12 +144,12 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, NBUF>& S, const T*
         }
         const T* kb = S.buf[warp][b][0];
         const T* vb = S.buf[warp][b][1];
-        const int s0 = g * kGroup;                // chunk-relative first slot
-        const int gl = min(kGroup, len - s0);
+        const int s0 = g * G;                     // chunk-relative first slot
+        const int gl = min(G, len - s0);
 
-        float part[kGroup];
+        float part[G];
 #pragma unroll
-        for (int j = 0; j < kGroup; ++j) {
+        for (int j = 0; j < G; ++j) {
             float kr[EPL];
             load_vec<T, EPL>(kb + j * D + lane * EPL, kr);
             float acc = 0.f;
@@ -141,26 +157,35 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, NBUF>& S, const T*
             for (int e = 0; e < EPL; ++e) acc = fmaf(qr[e], kr[e], acc);
             part[j] = acc;
         }
-        float zj = reduce8_transposed(part, lane);
-        const int jl = (lane >> 2) & 7;
+        float zj = reduce_transposed<G>(part, lane);
+        const int jl = owned_slot<G>(lane);
         if (jl >= gl || c0 + s0 + jl == skip) zj = -INFINITY;
-        float gm = fmaxf(zj, __shfl_xor_sync(kFull, zj, 4));
-        gm = fmaxf(gm, __shfl_xor_sync(kFull, gm, 8));
-        gm = fmaxf(gm, __shfl_xor_sync(kFull, gm, 16));
+        float gm = zj;
+#pragma unroll
+        for (int o = 16; o > OWN; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(kFull, gm, o));
         const float m_new = fmaxf(m_run, gm);
         const float alpha = safe_exp2_diff(m_run, m_new);
         const float ej = safe_exp2_diff(zj, m_new);
-        if ((lane & 3) == 0) {
+        if ((lane & OWN) == 0) {
             S.e[warp][jl] = ej;
             if (keep_z && jl < gl) S.z[s0 + jl] = zj;
         }
         __syncwarp();
-        const float4 e0 = *reinterpret_cast<const float4*>(&S.e[warp][0]);
-        const float4 e1 = *reinterpret_cast<const float4*>(&S.e[warp][4]);
-        const float ev[kGroup] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+        float ev[G];
+#pragma unroll
+        for (int j = 0; j < G; j += 4) {
+            if (j + 4 <= G) {
+                const float4 e4 = *reinterpret_cast<const float4*>(&S.e[warp][j]);
+                ev[j] = e4.x; ev[j + 1] = e4.y; ev[j + 2] = e4.z; ev[j + 3] = e4.w;
+            }
+        }
+        if (G < 4) {
+#pragma unroll
+            for (int j = 0; j < G; ++j) ev[j] = S.e[warp][j];
+        }
         float esum = 0.f;
 #pragma unroll
-        for (int j = 0; j < kGroup; ++j) esum += ev[j];
+        for (int j = 0; j < G; ++j) esum += ev[j];
         if (m_new != -INFINITY) {
             l_run = l_run * alpha + esum;
 #pragma unroll
@@ -168,7 +193,7 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, NBUF>& S, const T*
             m_run = m_new;
         }
 #pragma unroll
-        for (int j = 0; j < kGroup; ++j) {
+        for (int j = 0; j < G; ++j) {
             if (j < gl) {
                 float vr[EPL];
                 load_vec<T, EPL>(vb + j * D + lane * EPL, vr);
@@ -179,10 +204,10 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, NBUF>& S, const T*
         __syncwarp();
         // refill this buffer with the warp's group NBUF rounds ahead
         if (lane == 0) {
-            const int gn = g + kWarps * NBUF;
+            const int gn = g + NW * NBUF;
             if (gn < ngroups) {
-                const int s = c0 + gn * kGroup;
-                const uint32_t bytes = (uint32_t)(min(kGroup, c1 - s) * D * sizeof(T));
+                const int s = c0 + gn * G;
+                const uint32_t bytes = (uint32_t)(min(G, c1 - s) * D * sizeof(T));
                 mbar_arrive_expect_tx(&S.bar[warp][b], 2 * bytes);
                 bulk_g2s(S.buf[warp][b][0], Kc + (size_t)s * D, bytes, &S.bar[warp][b]);
                 bulk_g2s(S.buf[warp][b][1], Vc + (size_t)s * D, bytes, &S.bar[warp][b]);
@@ -193,18 +218,18 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, NBUF>& S, const T*
 
 // Kick off the first NBUF groups of each warp (called by lane 0 of every warp
 // after its barriers are initialised).
-template <typename T, int D, int NBUF>
-__device__ __forceinline__ void prime_ring(DecodeSmem<T, D, NBUF>& S, const T* Kc, const T* Vc,
+template <typename T, int D, class TL>
+__device__ __forceinline__ void prime_ring(DecodeSmem<T, D, TL>& S, const T* Kc, const T* Vc,
                                            int c0, int c1)
 {
     const int warp = threadIdx.x >> 5;
-    const int ngroups = (c1 - c0 + kGroup - 1) / kGroup;
+    const int ngroups = (c1 - c0 + TL::G - 1) / TL::G;
 #pragma unroll
-    for (int b = 0; b < NBUF; ++b) {
-        const int g = warp + kWarps * b;
+    for (int b = 0; b < TL::NBUF; ++b) {
+        const int g = warp + TL::NW * b;
         if (g < ngroups) {
-            const int s = c0 + g * kGroup;
-            const uint32_t bytes = (uint32_t)(min(kGroup, c1 - s) * D * sizeof(T));
+            const int s = c0 + g * TL::G;
+            const uint32_t bytes = (uint32_t)(min(TL::G, c1 - s) * D * sizeof(T));
             mbar_arrive_expect_tx(&S.bar[warp][b], 2 * bytes);
             bulk_g2s(S.buf[warp][b][0], Kc + (size_t)s * D, bytes, &S.bar[warp][b]);
             bulk_g2s(S.buf[warp][b][1], Vc + (size_t)s * D, bytes, &S.bar[warp][b]);
@@ -213,8 +238,8 @@ __device__ __forceinline__ void prime_ring(DecodeSmem<T, D, NBUF>& S, const T* K
 }
 
 // Merge the warps' softmax states; threads < D get their output column.
-template <typename T, int D, int NBUF>
-__device__ __forceinline__ void merge_warps(DecodeSmem<T, D, NBUF>& S, float m_run, float l_run,
+template <typename T, int D, class TL>
+__device__ __forceinline__ void merge_warps(DecodeSmem<T, D, TL>& S, float m_run, float l_run,
                                             const float (&o)[D / 32], float& Mc, float& Lc,
                                             float& Oc)
 {
@@ -226,11 +251,11 @@ __device__ __forceinline__ void merge_warps(DecodeSmem<T, D, NBUF>& S, float m_r
     __syncthreads();
     Mc = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) Mc = fmaxf(Mc, S.wm[w]);
+    for (int w = 0; w < TL::NW; ++w) Mc = fmaxf(Mc, S.wm[w]);
     Lc = 0.f;
     Oc = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < TL::NW; ++w) {
         const float f = safe_exp2_diff(S.wm[w], Mc);
         Lc += S.wl[w] * f;
         if (tid < D) Oc += S.wo[w][tid] * f;
@@ -246,11 +271,11 @@ __device__ __forceinline__ void copy_row(T* dst, const T* src, int t)
 
 // ------------------------------------------------------------------ H2O
 
-template <typename T, int D, int NBUF>
-__global__ void __launch_bounds__(kThreads) h2o_decode_kernel(const DecodeArgs a)
+template <typename T, int D, class TL>
+__global__ void __launch_bounds__(TL::NT) h2o_decode_kernel(const DecodeArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    auto& S = *reinterpret_cast<DecodeSmem<T, D, NBUF>*>(smem_raw);
+    auto& S = *reinterpret_cast<DecodeSmem<T, D, TL>*>(smem_raw);
     constexpr int EPL = D / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const CacheView& c = a.c;
@@ -264,7 +289,7 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_kernel(const DecodeArgs a
     const int n = us.x, p = us.y;
     const bool full = (n >= B);
     int cs = (n + C - 1) / C;
-    cs = (cs + kGroup - 1) / kGroup * kGroup;
+    cs = (cs + TL::G - 1) / TL::G * TL::G;
     const int c0 = min(n, rank * cs), c1 = min(n, c0 + cs);
     const size_t ub = (size_t)unit * B;
     T* Kc = reinterpret_cast<T*>(c.K) + ub * D;
@@ -272,17 +297,17 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_kernel(const DecodeArgs a
 
     if (lane == 0) {
 #pragma unroll
-        for (int b = 0; b < NBUF; ++b) mbar_init(&S.bar[warp][b], 1);
+        for (int b = 0; b < TL::NBUF; ++b) mbar_init(&S.bar[warp][b], 1);
         fence_mbar_init();
-        prime_ring<T, D, NBUF>(S, Kc, Vc, c0, c1);
+        prime_ring<T, D, TL>(S, Kc, Vc, c0, c1);
     }
 
     // scores and positions of this thread's slots, consumed after the merge
-    double sc_old[kSlotsPerThread];
-    int ps[kSlotsPerThread];
+    double sc_old[TL::SPT];
+    int ps[TL::SPT];
 #pragma unroll
-    for (int i = 0; i < kSlotsPerThread; ++i) {
-        const int s = c0 + tid + i * kThreads;
+    for (int i = 0; i < TL::SPT; ++i) {
+        const int s = c0 + tid + i * TL::NT;
         sc_old[i] = 0.0;
         ps[i] = 0;
         if (s < c1) { sc_old[i] = c.score[ub + s]; ps[i] = c.pos[ub + s]; }
@@ -312,10 +337,10 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_kernel(const DecodeArgs a
     }
     __syncwarp();
 
-    attend_chunk<T, D, NBUF>(S, Kc, Vc, c0, c1, -1, true, qr, m_run, l_run, o, c.err);
+    attend_chunk<T, D, TL>(S, Kc, Vc, c0, c1, -1, true, qr, m_run, l_run, o, c.err);
 
     float Mc, Lc, Oc;
-    merge_warps<T, D, NBUF>(S, m_run, l_run, o, Mc, Lc, Oc);
+    merge_warps<T, D, TL>(S, m_run, l_run, o, Mc, Lc, Oc);
 
     // exchange 1: (max, normaliser, output) of every CTA into rank 0
     cluster_wait();
@@ -344,8 +369,8 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_kernel(const DecodeArgs a
     double best = DBL_MAX, best_all = DBL_MAX;
     int bslot = INT_MAX, bslot_all = INT_MAX;
 #pragma unroll
-    for (int i = 0; i < kSlotsPerThread; ++i) {
-        const int s = c0 + tid + i * kThreads;
+    for (int i = 0; i < TL::SPT; ++i) {
+        const int s = c0 + tid + i * TL::NT;
         if (s < c1) {
             const float P = exp2f(S.z[s - c0] - M) * invL;
             const double ns = sc_old[i] + (double)P;
@@ -379,7 +404,7 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_kernel(const DecodeArgs a
     if (rank == 0 && tid == 0) S.P_new = exp2f(S.z_new - M) * invL;
     __syncthreads();
     if (full && tid == 0) {
-        for (int w = 1; w < kWarps; ++w) {
+        for (int w = 1; w < TL::NW; ++w) {
             if (S.rd[0][w] < best || (S.rd[0][w] == best && S.ri[0][w] < bslot)) { best = S.rd[0][w]; bslot = S.ri[0][w]; }
             if (S.rd[1][w] < best_all || (S.rd[1][w] == best_all && S.ri[1][w] < bslot_all)) {
                 best_all = S.rd[1][w]; bslot_all = S.ri[1][w];
@@ -429,11 +454,11 @@ __global__ void __launch_bounds__(kThreads) h2o_decode_kernel(const DecodeArgs a
 
 // ------------------------------------------------------------------ LSH
 
-template <typename T, int D, int NBUF>
-__global__ void __launch_bounds__(kThreads) lsh_decode_kernel(const DecodeArgs a)
+template <typename T, int D, class TL>
+__global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    auto& S = *reinterpret_cast<DecodeSmem<T, D, NBUF>*>(smem_raw);
+    auto& S = *reinterpret_cast<DecodeSmem<T, D, TL>*>(smem_raw);
     constexpr int EPL = D / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const CacheView& c = a.c;
@@ -447,7 +472,7 @@ __global__ void __launch_bounds__(kThreads) lsh_decode_kernel(const DecodeArgs a
     const int n = us.x, p = us.y;
     const bool full = (n >= B);
     int cs = (n + C - 1) / C;
-    cs = (cs + kGroup - 1) / kGroup * kGroup;
+    cs = (cs + TL::G - 1) / TL::G * TL::G;
     const int c0 = min(n, rank * cs), c1 = min(n, c0 + cs);
     const size_t ub = (size_t)unit * B;
     T* Kc = reinterpret_cast<T*>(c.K) + ub * D;
@@ -455,9 +480,9 @@ __global__ void __launch_bounds__(kThreads) lsh_decode_kernel(const DecodeArgs a
 
     if (lane == 0) {
 #pragma unroll
-        for (int b = 0; b < NBUF; ++b) mbar_init(&S.bar[warp][b], 1);
+        for (int b = 0; b < TL::NBUF; ++b) mbar_init(&S.bar[warp][b], 1);
         fence_mbar_init();
-        prime_ring<T, D, NBUF>(S, Kc, Vc, c0, c1);
+        prime_ring<T, D, TL>(S, Kc, Vc, c0, c1);
     }
 
     const T* qg = reinterpret_cast<const T*>(a.q) + (size_t)unit * D;
@@ -484,7 +509,7 @@ __global__ void __launch_bounds__(kThreads) lsh_decode_kernel(const DecodeArgs a
     if (full) {
         const unsigned cq = S.code_q;
         unsigned long long bk = 0ull, bka = 0ull;    // (distance << 32) | ~slot, max wins
-        for (int s = tid; s < n; s += kThreads) {
+        for (int s = tid; s < n; s += TL::NT) {
             const unsigned long long key =
                 ((unsigned long long)__popc(cq ^ c.code[ub + s]) << 32) | (unsigned)(0xffffffffu - (unsigned)s);
             if (c.pos[ub + s] <= p - c.r && key > bk) bk = key;
@@ -500,7 +525,7 @@ __global__ void __launch_bounds__(kThreads) lsh_decode_kernel(const DecodeArgs a
         if (lane == 0) { S.ru[0][warp] = bk; S.ru[1][warp] = bka; }
         __syncthreads();
         if (tid == 0) {
-            for (int w = 1; w < kWarps; ++w) {
+            for (int w = 1; w < TL::NW; ++w) {
                 bk = S.ru[0][w] > bk ? S.ru[0][w] : bk;
                 bka = S.ru[1][w] > bka ? S.ru[1][w] : bka;
             }
@@ -533,11 +558,11 @@ __global__ void __launch_bounds__(kThreads) lsh_decode_kernel(const DecodeArgs a
     }
     __syncwarp();
 
-    attend_chunk<T, D, NBUF>(S, Kc, Vc, c0, c1, full ? victim : -1, false, qr, m_run, l_run, o,
+    attend_chunk<T, D, TL>(S, Kc, Vc, c0, c1, full ? victim : -1, false, qr, m_run, l_run, o,
                              c.err);
 
     float Mc, Lc, Oc;
-    merge_warps<T, D, NBUF>(S, m_run, l_run, o, Mc, Lc, Oc);
+    merge_warps<T, D, TL>(S, m_run, l_run, o, Mc, Lc, Oc);
 
     cluster_wait();
     const uint32_t x0 = map_to_rank(&S.x, 0);
@@ -578,38 +603,29 @@ __global__ void __launch_bounds__(kThreads) lsh_decode_kernel(const DecodeArgs a
 
 // ------------------------------------------------------------- launching
 
-constexpr int kNbuf = 2;
+using TileDefault = Tile<8, 8, 2>;
 
-template <typename T, int D, bool LSH>
-cudaError_t launch_t(const DecodeArgs& a, int split)
+template <typename T, int D, bool LSH, class TL>
+cudaError_t launch_decode_t(const DecodeArgs& a, int split, cudaStream_t st)
 {
-    using Smem = DecodeSmem<T, D, kNbuf>;
-    auto kern = LSH ? lsh_decode_kernel<T, D, kNbuf> : h2o_decode_kernel<T, D, kNbuf>;
-    const size_t smem = sizeof(Smem);
+    auto kern = LSH ? lsh_decode_kernel<T, D, TL> : h2o_decode_kernel<T, D, TL>;
+    const size_t smem = sizeof(DecodeSmem<T, D, TL>);
     static bool configured[64] = {false};
     int dev = 0;
-    cudaGetDevice(&dev);
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    return cudaSuccess;
-}
-
-template <typename T, int D, bool LSH>
-cudaError_t launch_decode_t(const DecodeArgs& a, int split, cudaStream_t st)
-{
-    cudaError_t e = launch_t<T, D, LSH>(a, split);
-    if (e != cudaSuccess) return e;
-    auto kern = LSH ? lsh_decode_kernel<T, D, kNbuf> : h2o_decode_kernel<T, D, kNbuf>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a.c.U * split), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = sizeof(DecodeSmem<T, D, kNbuf>);
+    cfg.blockDim = dim3(TL::NT, 1, 1);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -621,16 +637,37 @@ cudaError_t launch_decode_t(const DecodeArgs& a, int split, cudaStream_t st)
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
+// Tile variants for bf16 / head_dim 128, selectable with H2O_DECODE_TILE for
+// tuning; every variant computes the same result.
+int tile_variant()
+{
+    static int v = -1;
+    if (v < 0) {
+        const char* e = getenv("H2O_DECODE_TILE");
+        v = e ? atoi(e) : 0;
+    }
+    return v;
+}
+
 template <bool LSH>
 cudaError_t dispatch(const DecodeArgs& a, int split, cudaStream_t st)
 {
     const bool bf = a.c.dtype == 1;
-    if (a.c.D == 128)
-        return bf ? launch_decode_t<__nv_bfloat16, 128, LSH>(a, split, st)
-                  : launch_decode_t<float, 128, LSH>(a, split, st);
+    if (a.c.D == 128 && bf) {
+        switch (tile_variant()) {
+        case 1: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<16, 8, 1>>(a, split, st);
+        case 2: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<16, 4, 2>>(a, split, st);
+        case 3: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<8, 4, 4>>(a, split, st);
+        case 4: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<16, 8, 2>>(a, split, st);
+        case 5: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<8, 8, 3>>(a, split, st);
+        case 6: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<4, 8, 4>>(a, split, st);
+        default: return launch_decode_t<__nv_bfloat16, 128, LSH, TileDefault>(a, split, st);
+        }
+    }
+    if (a.c.D == 128) return launch_decode_t<float, 128, LSH, TileDefault>(a, split, st);
     if (a.c.D == 64)
-        return bf ? launch_decode_t<__nv_bfloat16, 64, LSH>(a, split, st)
-                  : launch_decode_t<float, 64, LSH>(a, split, st);
+        return bf ? launch_decode_t<__nv_bfloat16, 64, LSH, TileDefault>(a, split, st)
+                  : launch_decode_t<float, 64, LSH, TileDefault>(a, split, st);
     return cudaErrorInvalidValue;
 }
 
@@ -638,14 +675,14 @@ cudaError_t dispatch(const DecodeArgs& a, int split, cudaStream_t st)
 
 int max_decode_split() { return kMaxSplit; }
 
-// Enough CTAs to keep several resident per SM, never more slots per CTA
-// than the per-thread register budget covers.
+// One CTA per unit whenever the units alone cover the SMs: the cluster
+// exchange costs more than it saves.  Otherwise enough CTAs per unit to give
+// every SM one, never more slots per CTA than the registers cover.
 int auto_decode_split(int U, int B, int num_sms)
 {
-    int lo = (B + kMaxChunk - 1) / kMaxChunk;
-    int want = (4 * num_sms + U - 1) / U;
-    int hi = (B + 31) / 32;
-    int s = want;
+    int s = (num_sms + U - 1) / U;
+    const int lo = (B + kMaxChunk - 1) / kMaxChunk;
+    const int hi = (B + 63) / 64;
     if (s > hi) s = hi;
     if (s < lo) s = lo;
     if (s < 1) s = 1;

@@ -218,7 +218,9 @@ def generate_device(w: Workload, seed_offset: int = 0, prompt: Optional[int] = N
     basis = None
     if w.structure and w.structure[0] == "rank":
         rank = int(w.structure[1])
-        basis = torch.linalg.qr(normal(U, d, rank))[0].transpose(1, 2).contiguous()   # [U, rank, d]
+        gb = _rng(w.seed, TAG_SHARED, 1_000_000 + seed_offset)
+        qb = np.linalg.qr(gb.standard_normal((U, d, rank)))[0]           # [U, d, rank]
+        basis = torch.from_numpy(np.ascontiguousarray(qb.transpose(0, 2, 1), np.float32)).to(device)
     u_dir = None
     if w.structure and w.structure[0] == "outlier_dir":
         u_dir = normal(d)
