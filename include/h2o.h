@@ -187,6 +187,34 @@ int h2o_sync(h2o_handle h);
 /* Free every library-owned buffer of the handle; NULL is a no-op. */
 void h2o_destroy(h2o_handle h);
 
+/*
+ * h2o_prompt_scores_noalloc -- the prompt column sums c [U][T] (fp64) that
+ * h2o_prefill ranks prompt tokens by, computed without allocating device
+ * memory.  The pages have no counterpart: this is a variant of the prompt
+ * scorer for callers that cannot call cudaMalloc, such as code running
+ * while a stream is captured into a CUDA graph, or serving runtimes that
+ * reserve all device memory at start-up and forbid allocations afterwards.
+ *
+ * The scorer's scratch (row max and normaliser, 8 bytes per unit per token)
+ * is a fixed device array inside the library of H2O_NOALLOC_MAX_TOKENS
+ * unit-tokens (8 MiB), present on every device that loads the library until
+ * the process exits.  The call allocates nothing.
+ *   Q, K:  device [batch*heads][T][head_dim] of dtype, 16-byte aligned;
+ *   c:     device fp64 [batch*heads][T], written in full;
+ *   batch, heads, T >= 1 with batch*heads*T <= H2O_NOALLOC_MAX_TOKENS,
+ *   otherwise H2O_ERR_ARG; head_dim in {64, 128}; scale > 0;
+ *   cuda_stream: the stream to enqueue on (NULL = legacy stream).
+ * The first call on each device looks up the array's device address (a
+ * set-up step, not an allocation); make that first call before any stream
+ * capture.  All calls share the one array and nothing in it carries over
+ * between calls, but calls whose work overlaps on the GPU (other streams,
+ * other host threads) race on it: the caller must serialise them.
+ */
+#define H2O_NOALLOC_MAX_TOKENS (1 << 20)
+int h2o_prompt_scores_noalloc(const void* Q, const void* K, int batch, int heads, int T,
+                              int head_dim, int dtype, double scale, double* c,
+                              void* cuda_stream);
+
 /* Thread-local description of the last failure in this thread ("" if none). */
 const char* h2o_last_error(void);
 

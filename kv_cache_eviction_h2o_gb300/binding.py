@@ -45,7 +45,10 @@ SIGNATURES = {
     "h2o_sync": (_i, [_vp]),
     "h2o_destroy": (None, [_vp]),
     "h2o_last_error": (ctypes.c_char_p, []),
+    "h2o_prompt_scores_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _d, _vp, _vp]),
 }
+
+H2O_NOALLOC_MAX_TOKENS = 1 << 20
 
 _lib = None
 
@@ -161,3 +164,10 @@ def h2o_sync(h):
 
 def h2o_destroy(h):
     lib().h2o_destroy(h)
+
+
+def h2o_prompt_scores_noalloc(Q, K, batch, heads, T, head_dim, dtype, scale, c, stream=None):
+    """Prompt column sums into ``c`` without any device allocation (scratch
+    is a fixed array inside the library); see include/h2o.h."""
+    _check(lib().h2o_prompt_scores_noalloc(_ptr(Q), _ptr(K), batch, heads, int(T), head_dim, dtype,
+                                           float(scale), _ptr(c), _stream(stream)))

@@ -162,7 +162,7 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL>& S, const T* K
         if (jl >= gl || c0 + s0 + jl == skip) zj = -INFINITY;
         float gm = zj;
 #pragma unroll
-        for (int o = 16; o > OWN; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(kFull, gm, o));
+        for (int sh = 16; sh > OWN; sh >>= 1) gm = fmaxf(gm, __shfl_xor_sync(kFull, gm, sh));
         const float m_new = fmaxf(m_run, gm);
         const float alpha = safe_exp2_diff(m_run, m_new);
         const float ej = safe_exp2_diff(zj, m_new);

@@ -16,6 +16,19 @@ namespace {
 
 thread_local char g_err[512] = "";
 
+}  // namespace
+
+int h2o::set_last_error(int code, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+namespace {
+
 int fail(int code, const char* fmt, ...)
 {
     va_list ap;

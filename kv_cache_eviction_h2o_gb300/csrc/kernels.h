@@ -50,6 +50,9 @@ int max_decode_split();
 cudaError_t launch_prompt_stats(const CacheView& c, const PromptArgs& p, cudaStream_t st);
 cudaError_t launch_select(const CacheView& c, const PromptArgs& p, cudaStream_t st);
 cudaError_t launch_gather(const CacheView& c, const PromptArgs& p, bool with_codes, cudaStream_t st);
+// Record a failure for h2o_last_error() and return `code`.
+int set_last_error(int code, const char* fmt, ...);
+
 cudaError_t launch_lsh_prompt(const CacheView& c, const PromptArgs& p, const float* W,
                               cudaStream_t st);
 
