@@ -177,7 +177,57 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr)
     return v;
 }
 
+// ------------------------------------------------------- fp32 pair scores
+//
+// Accumulated scores are held as an unevaluated pair hi + lo of fp32 values
+// with |lo| <= ulp(hi) / 2 (about 48 significant bits), so the per-step
+// accumulate and the eviction comparisons stay on the fp32 and integer
+// pipes; GB300's fp64 pipe is far too narrow for the decode epilogue.
+
+// (hi, lo) + x, exactly up to the final rounding of lo (TwoSum, then a
+// renormalising Fast2Sum).
+__device__ __forceinline__ float2 pair_add(float2 a, float x)
+{
+    const float s = a.x + x;
+    const float bp = s - a.x;
+    const float err = (a.x - (s - bp)) + (x - bp);
+    const float t = a.y + err;
+    const float hi = s + t;
+    const float lo = t - (hi - s);
+    return make_float2(hi, lo);
+}
+
+// Order-preserving map of an fp32 value to an unsigned key.
+__device__ __forceinline__ unsigned ord_key(float x)
+{
+    const unsigned b = __float_as_uint(x);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// ---------------------------------------------- programmatic dependent launch
+
+// Block until the grid this one depends on (the previous kernel in the
+// stream) has completed and its memory is visible; a no-op when the grid was
+// launched without a programmatic dependency.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Let the next grid in the stream be scheduled; it still waits for this
+// grid's completion in grid_dependency_wait before touching memory.
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------- reductions
+
+// Cheapest proxy fence that makes mbarrier initialisation visible to the
+// bulk-copy engine of this CTA.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 __device__ __forceinline__ float warp_max(float v)
 {

@@ -36,81 +36,77 @@ namespace {
 
 constexpr int kMaxSplit = 16;              // CTAs per cluster (non-portable above 8)
 constexpr int kMaxChunk = 1024;            // slots per CTA
+constexpr int kStage = 16;                 // slots per warp stage
 constexpr unsigned kFull = 0xffffffffu;
 
-// Tile shape of the decode kernels: NW warps per CTA, each streaming groups of
-// G slots through a private ring of NBUF shared-memory buffers.
-template <int NW_, int G_, int NBUF_>
+// NW warps per CTA, each streaming 16-slot stages through a private ring of
+// NBUF shared-memory buffers.
+template <int NW_, int NBUF_>
 struct Tile {
-    static constexpr int NW = NW_, NT = 32 * NW_, G = G_, NBUF = NBUF_;
+    static constexpr int NW = NW_, NT = 32 * NW_, NBUF = NBUF_;
     static constexpr int SPT = kMaxChunk / NT;            // slots per thread in the score pass
-    static constexpr int LOG2G = G_ == 8 ? 3 : (G_ == 4 ? 2 : 1);
-    static_assert(G_ == 2 || G_ == 4 || G_ == 8, "group size");
+};
+
+// Row geometry.  For the logits a stage's 16 rows are split between the two
+// half-warps: lane (r = lane & 15, h = lane >> 4) computes the dot of row r's
+// half h with the matching half of q.  Rows are read as 16-byte chunks in
+// the order c ^ (r & XM): eight consecutive lanes then touch eight distinct
+// chunk positions, so the row-major stage is read without bank conflicts;
+// each lane holds its half of q already permuted into that order.
+template <typename T, int D>
+struct Rows {
+    static constexpr int VE = 16 / (int)sizeof(T);        // elements per 16-byte chunk
+    static constexpr int HALF = D / 2;                    // elements per half row
+    static constexpr int HCH = HALF / VE;                 // chunks per half row
+    static constexpr int XM = HCH >= 8 ? 7 : HCH - 1;     // chunk rotation mask
+    static constexpr int EPL = D / 32;                    // value elements per lane
 };
 
 template <int D>
 struct Exchange {                 // every CTA has one; rank 0's is the meeting point
     float m[kMaxSplit];           // per-CTA running max (base 2)
     float l[kMaxSplit];           // per-CTA normaliser at that max
-    double cand_score[kMaxSplit]; // per-CTA arg-min over eviction candidates
-    double all_score[kMaxSplit];  // per-CTA arg-min over every live slot
-    int cand_slot[kMaxSplit];
-    int all_slot[kMaxSplit];
+    unsigned am[2][3][kMaxSplit]; // per-CTA arg-min keys (hi, lo, slot): [0] candidates, [1] every live slot
     float o[kMaxSplit][D];        // per-CTA unnormalised output
 };
 
 template <typename T, int D, class TL>
-struct DecodeSmem {
-    T buf[TL::NW][TL::NBUF][2][TL::G * D];   // per-warp ring: [K rows | V rows]
-    uint64_t bar[TL::NW][TL::NBUF];
+struct Ring {
+    T kbuf[TL::NW][TL::NBUF][kStage * D];   // per-warp ring of K rows
+    T vbuf[TL::NW][TL::NBUF][kStage * D];   // per-warp ring of V rows
+};
+
+template <int D, class TL>
+struct Epilogue {
     Exchange<D> x;
-    float z[kMaxChunk];                   // base-2 logits of this CTA's slots
     float wo[TL::NW][D];
-    alignas(16) float e[TL::NW][TL::G < 4 ? 4 : TL::G];
+};
+
+template <typename T, int D, class TL>
+struct DecodeSmem {
+    // the epilogue buffers reuse the ring once every copy has landed and
+    // been consumed (after the barrier that opens merge_warps)
+    union {
+        Ring<T, D, TL> ring;
+        Epilogue<D, TL> epi;
+    } u;
+    uint64_t bar[TL::NW][TL::NBUF];
+    float z[kMaxChunk];                     // base-2 logits of this CTA's slots
+    alignas(16) float e[TL::NW][kStage];
     float wm[TL::NW];
     float wl[TL::NW];
     float qf[D];
     float kf[D];
-    double rd[2][TL::NW];
-    int ri[2][TL::NW];
+    unsigned am[2][3][TL::NW];              // per-warp arg-min keys
     unsigned long long ru[2][TL::NW];
     float M, invL, z_new, P_new;
     int victim;
     unsigned code_q, code_k;
 };
 
-// Sum G per-lane partials over the warp: each exchange level keeps half of
-// the live partials and sends the other half, so lane l ends up with the
-// total of partial j, j read from lane bits 4, 3, ... (most significant
-// first); log2(G) + (5 - log2(G)) = 5 shuffle levels, G - 1 + 5 - log2(G)
-// shuffles instead of 5 G.
-template <int G>
-__device__ __forceinline__ float reduce_transposed(float (&v)[G], int lane)
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
 {
-#pragma unroll
-    for (int k = 0; (G >> k) > 1; ++k) {
-        const int half = (G >> k) / 2;
-        const bool up = (lane >> (4 - k)) & 1;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-            const float keep = up ? v[i + half] : v[i];
-            const float send = up ? v[i] : v[i + half];
-            v[i] = keep + __shfl_xor_sync(kFull, send, 16 >> k);
-        }
-    }
-    float c = v[0];
-    constexpr int lg = G == 8 ? 3 : (G == 4 ? 2 : 1);
-#pragma unroll
-    for (int o = 16 >> lg; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
-    return c;
-}
-
-// slot (within a group of G) whose total lane `lane` holds after the reduction
-template <int G>
-__device__ __forceinline__ int owned_slot(int lane)
-{
-    constexpr int lg = G == 8 ? 3 : (G == 4 ? 2 : 1);
-    return (lane >> (5 - lg)) & (G - 1);
+    return __ffma2_rn(a, b, c);
 }
 
 __device__ __forceinline__ float safe_exp2_diff(float a, float m)
@@ -118,121 +114,176 @@ __device__ __forceinline__ float safe_exp2_diff(float a, float m)
     return (a == -INFINITY) ? 0.f : exp2f(a - m);
 }
 
-// Per-warp streaming online softmax over this CTA's chunk [c0, c1) of live
-// slots.  `skip` (absolute slot) is left out of the softmax.  When keep_z,
-// logits are stored in S.z[slot - c0].  Returns through (m_run, l_run, o).
+// Lexicographic arg-min over (score hi, score lo, slot), each an unsigned
+// key; all-ones means "no slot".
+struct ArgMin {
+    unsigned hi, lo, slot;
+};
+
+__device__ __forceinline__ ArgMin argmin_none() { return ArgMin{0xffffffffu, 0xffffffffu, 0xffffffffu}; }
+
+__device__ __forceinline__ void argmin_take(ArgMin& a, const ArgMin& b)
+{
+    if (b.hi < a.hi || (b.hi == a.hi && (b.lo < a.lo || (b.lo == a.lo && b.slot < a.slot)))) a = b;
+}
+
+__device__ __forceinline__ ArgMin warp_argmin(const ArgMin& a)
+{
+    const unsigned mh = __reduce_min_sync(kFull, a.hi);
+    const unsigned ml = __reduce_min_sync(kFull, a.hi == mh ? a.lo : 0xffffffffu);
+    const unsigned ms = __reduce_min_sync(kFull, (a.hi == mh && a.lo == ml) ? a.slot : 0xffffffffu);
+    return ArgMin{mh, ml, ms};
+}
+
+// This lane's half of q (scaled to base-2 logits) in its rotated chunk order.
+template <typename T, int D>
+__device__ __forceinline__ void load_q_rotated(const T* q, float scale, int lane,
+                                               float (&qp)[D / 2])
+{
+    using R = Rows<T, D>;
+    const int r = lane & 15, h = lane >> 4;
+#pragma unroll
+    for (int c = 0; c < R::HCH; ++c) {
+        load_vec<T, R::VE>(q + h * R::HALF + (c ^ (r & R::XM)) * R::VE, &qp[c * R::VE]);
+#pragma unroll
+        for (int e = 0; e < R::VE; ++e) qp[c * R::VE + e] *= scale;
+    }
+}
+
+// Half-row dot product of row `row` (global or shared, elements of type T or
+// float) with the rotated q half; every lane returns the full dot of its
+// row after one exchange between the half-warps.
+template <typename T, int D, typename E>
+__device__ __forceinline__ float row_dot(const E* row, const float (&qp)[D / 2], int lane)
+{
+    using R = Rows<T, D>;
+    const int r = lane & 15, h = lane >> 4;
+    const E* half = row + h * R::HALF;
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < R::HCH; ++c) {
+        float kf[R::VE];
+        if constexpr (sizeof(E) == sizeof(float) && sizeof(T) == 2) {
+            // a float copy of a bf16 row (kept in shared memory)
+#pragma unroll
+            for (int e = 0; e < R::VE; ++e) kf[e] = half[(c ^ (r & R::XM)) * R::VE + e];
+        } else {
+            load_vec<T, R::VE>(reinterpret_cast<const T*>(half) + (c ^ (r & R::XM)) * R::VE, kf);
+        }
+#pragma unroll
+        for (int e = 0; e < R::VE; e += 4) {
+            acc0 = fma2(make_float2(qp[c * R::VE + e], qp[c * R::VE + e + 1]), make_float2(kf[e], kf[e + 1]), acc0);
+            acc1 = fma2(make_float2(qp[c * R::VE + e + 2], qp[c * R::VE + e + 3]), make_float2(kf[e + 2], kf[e + 3]), acc1);
+        }
+    }
+    const float zh = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+    return zh + __shfl_xor_sync(kFull, zh, 16);
+}
+
+// Per-warp streaming softmax over the rows this CTA fetched, [f0, f1); only
+// slots < n are live and `skip` (absolute slot) is left out.  When keep_z,
+// logits go to S.z[slot - f0].  The warp keeps one reference max m_ref and
+// rescales only when a logit exceeds it by more than 8 (weights stay below
+// 2^8), so most stages need no cross-lane max.  l_lane is this lane's share
+// of the normaliser (lanes 0..15 count their slot once); o holds the lane's
+// EPL output columns lane*EPL.. of the unnormalised sum, relative to m_ref.
 template <typename T, int D, class TL>
 __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL>& S, const T* Kc, const T* Vc,
-                                             int c0, int c1, int skip, bool keep_z,
-                                             const float (&qr)[D / 32], float& m_run,
-                                             float& l_run, float (&o)[D / 32], int* err)
+                                             int f0, int f1, int n, int skip, bool keep_z,
+                                             const float (&qp)[D / 2], float& m_ref,
+                                             float& l_lane, float (&o)[D / 32], int* err)
 {
-    constexpr int EPL = D / 32;
-    constexpr int G = TL::G, NW = TL::NW, NBUF = TL::NBUF;
-    constexpr int OWN = (1 << (5 - TL::LOG2G)) - 1;     // lanes sharing one slot's total
+    using R = Rows<T, D>;
+    constexpr int EPL = R::EPL, NW = TL::NW, NBUF = TL::NBUF;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int len = c1 - c0;
-    const int ngroups = (len + G - 1) / G;
+    const int r = lane & 15, h = lane >> 4;
+    const int nst = (f1 - f0 + kStage - 1) / kStage;
     bool timed_out = false;
     int it = 0;
-    for (int g = warp; g < ngroups; g += NW, ++it) {
+    for (int g = warp; g < nst; g += NW, ++it) {
         const int b = it % NBUF;
         const uint32_t parity = (uint32_t)(it / NBUF) & 1u;
         if (!mbar_wait(&S.bar[warp][b], parity)) {
             if (!timed_out && lane == 0) atomicOr(err, kErrWaitTimeout);
             timed_out = true;
         }
-        const T* kb = S.buf[warp][b][0];
-        const T* vb = S.buf[warp][b][1];
-        const int s0 = g * G;                     // chunk-relative first slot
-        const int gl = min(G, len - s0);
-
-        float part[G];
+        const int s0 = g * kStage;                 // fetch-relative first slot
+        const int gl = max(0, min(kStage, n - (f0 + s0)));   // live rows of this stage
+        if (gl > 0) {
+            const T* kst = S.u.ring.kbuf[warp][b];
+            const T* vst = S.u.ring.vbuf[warp][b];
+            float z = row_dot<T, D, T>(kst + r * D, qp, lane);
+            if (r >= gl || f0 + s0 + r == skip) z = -INFINITY;
+            if (__any_sync(kFull, z > m_ref + 8.f)) {
+                float zm = z;
 #pragma unroll
-        for (int j = 0; j < G; ++j) {
-            float kr[EPL];
-            load_vec<T, EPL>(kb + j * D + lane * EPL, kr);
-            float acc = 0.f;
+                for (int sh = 1; sh < 16; sh <<= 1) zm = fmaxf(zm, __shfl_xor_sync(kFull, zm, sh));
+                const float alpha = safe_exp2_diff(m_ref, zm);
+                l_lane *= alpha;
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) acc = fmaf(qr[e], kr[e], acc);
-            part[j] = acc;
-        }
-        float zj = reduce_transposed<G>(part, lane);
-        const int jl = owned_slot<G>(lane);
-        if (jl >= gl || c0 + s0 + jl == skip) zj = -INFINITY;
-        float gm = zj;
+                for (int e = 0; e < EPL; ++e) o[e] *= alpha;
+                m_ref = zm;
+            }
+            const float er = safe_exp2_diff(z, m_ref);
+            if (h == 0) {
+                l_lane += er;
+                S.e[warp][r] = er;
+                if (keep_z && r < gl) S.z[s0 + r] = z;
+            }
+            __syncwarp();
+            float ev[kStage];
 #pragma unroll
-        for (int sh = 16; sh > OWN; sh >>= 1) gm = fmaxf(gm, __shfl_xor_sync(kFull, gm, sh));
-        const float m_new = fmaxf(m_run, gm);
-        const float alpha = safe_exp2_diff(m_run, m_new);
-        const float ej = safe_exp2_diff(zj, m_new);
-        if ((lane & OWN) == 0) {
-            S.e[warp][jl] = ej;
-            if (keep_z && jl < gl) S.z[s0 + jl] = zj;
-        }
-        __syncwarp();
-        float ev[G];
-#pragma unroll
-        for (int j = 0; j < G; j += 4) {
-            if (j + 4 <= G) {
+            for (int j = 0; j < kStage; j += 4) {
                 const float4 e4 = *reinterpret_cast<const float4*>(&S.e[warp][j]);
                 ev[j] = e4.x; ev[j + 1] = e4.y; ev[j + 2] = e4.z; ev[j + 3] = e4.w;
             }
-        }
-        if (G < 4) {
 #pragma unroll
-            for (int j = 0; j < G; ++j) ev[j] = S.e[warp][j];
-        }
-        float esum = 0.f;
+            for (int j = 0; j < kStage; ++j) {
+                if (j < gl) {
+                    float vr[EPL];
+                    load_vec<T, EPL>(vst + j * D + lane * EPL, vr);
+                    const float2 pj = make_float2(ev[j], ev[j]);
 #pragma unroll
-        for (int j = 0; j < G; ++j) esum += ev[j];
-        if (m_new != -INFINITY) {
-            l_run = l_run * alpha + esum;
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) o[e] *= alpha;
-            m_run = m_new;
-        }
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-            if (j < gl) {
-                float vr[EPL];
-                load_vec<T, EPL>(vb + j * D + lane * EPL, vr);
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) o[e] = fmaf(ev[j], vr[e], o[e]);
+                    for (int e = 0; e < EPL; e += 2) {
+                        const float2 acc = fma2(pj, make_float2(vr[e], vr[e + 1]), make_float2(o[e], o[e + 1]));
+                        o[e] = acc.x;
+                        o[e + 1] = acc.y;
+                    }
+                }
             }
+            __syncwarp();
         }
-        __syncwarp();
-        // refill this buffer with the warp's group NBUF rounds ahead
+        // refill this buffer with the warp's stage NBUF rounds ahead
         if (lane == 0) {
             const int gn = g + NW * NBUF;
-            if (gn < ngroups) {
-                const int s = c0 + gn * G;
-                const uint32_t bytes = (uint32_t)(min(G, c1 - s) * D * sizeof(T));
+            if (gn < nst) {
+                const int s = f0 + gn * kStage;
+                const uint32_t bytes = (uint32_t)(min(kStage, f1 - s) * D * sizeof(T));
                 mbar_arrive_expect_tx(&S.bar[warp][b], 2 * bytes);
-                bulk_g2s(S.buf[warp][b][0], Kc + (size_t)s * D, bytes, &S.bar[warp][b]);
-                bulk_g2s(S.buf[warp][b][1], Vc + (size_t)s * D, bytes, &S.bar[warp][b]);
+                bulk_g2s(S.u.ring.kbuf[warp][b], Kc + (size_t)s * D, bytes, &S.bar[warp][b]);
+                bulk_g2s(S.u.ring.vbuf[warp][b], Vc + (size_t)s * D, bytes, &S.bar[warp][b]);
             }
         }
     }
 }
 
-// Kick off the first NBUF groups of each warp (called by lane 0 of every warp
+// Kick off the first NBUF stages of each warp (called by lane 0 of every warp
 // after its barriers are initialised).
 template <typename T, int D, class TL>
 __device__ __forceinline__ void prime_ring(DecodeSmem<T, D, TL>& S, const T* Kc, const T* Vc,
                                            int c0, int c1)
 {
     const int warp = threadIdx.x >> 5;
-    const int ngroups = (c1 - c0 + TL::G - 1) / TL::G;
+    const int nst = (c1 - c0 + kStage - 1) / kStage;
 #pragma unroll
     for (int b = 0; b < TL::NBUF; ++b) {
         const int g = warp + TL::NW * b;
-        if (g < ngroups) {
-            const int s = c0 + g * TL::G;
-            const uint32_t bytes = (uint32_t)(min(TL::G, c1 - s) * D * sizeof(T));
+        if (g < nst) {
+            const int s = c0 + g * kStage;
+            const uint32_t bytes = (uint32_t)(min(kStage, c1 - s) * D * sizeof(T));
             mbar_arrive_expect_tx(&S.bar[warp][b], 2 * bytes);
-            bulk_g2s(S.buf[warp][b][0], Kc + (size_t)s * D, bytes, &S.bar[warp][b]);
-            bulk_g2s(S.buf[warp][b][1], Vc + (size_t)s * D, bytes, &S.bar[warp][b]);
+            bulk_g2s(S.u.ring.kbuf[warp][b], Kc + (size_t)s * D, bytes, &S.bar[warp][b]);
+            bulk_g2s(S.u.ring.vbuf[warp][b], Vc + (size_t)s * D, bytes, &S.bar[warp][b]);
         }
     }
 }
@@ -245,9 +296,11 @@ __device__ __forceinline__ void merge_warps(DecodeSmem<T, D, TL>& S, float m_run
 {
     constexpr int EPL = D / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (lane == 0) { S.wm[warp] = m_run; S.wl[warp] = l_run; }
+    const float l_warp = warp_sum(l_run);
+    __syncthreads();                         // every warp is past the ring it overlays
+    if (lane == 0) { S.wm[warp] = m_run; S.wl[warp] = l_warp; }
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) S.wo[warp][lane * EPL + e] = o[e];
+    for (int e = 0; e < EPL; ++e) S.u.epi.wo[warp][lane * EPL + e] = o[e];
     __syncthreads();
     Mc = -INFINITY;
 #pragma unroll
@@ -258,15 +311,30 @@ __device__ __forceinline__ void merge_warps(DecodeSmem<T, D, TL>& S, float m_run
     for (int w = 0; w < TL::NW; ++w) {
         const float f = safe_exp2_diff(S.wm[w], Mc);
         Lc += S.wl[w] * f;
-        if (tid < D) Oc += S.wo[w][tid] * f;
+        if (tid < D) Oc += S.u.epi.wo[w][tid] * f;
     }
 }
 
-template <typename T, int D>
-__device__ __forceinline__ void copy_row(T* dst, const T* src, int t)
+// Cluster-wide barrier; a single-CTA cluster only needs the CTA barrier.
+__device__ __forceinline__ void cta_group_sync(int C)
 {
-    constexpr int NV = D * (int)sizeof(T) / 16;
-    if (t < NV) reinterpret_cast<uint4*>(dst)[t] = reinterpret_cast<const uint4*>(src)[t];
+    if (C > 1) {
+        cluster_arrive();
+        cluster_wait();
+    } else {
+        __syncthreads();
+    }
+}
+
+// Fetch range of this CTA: its share of all B slots, rounded to stages.  The
+// range does not depend on the occupancy, so the bulk copies can start
+// before the unit's state is read.
+__device__ __forceinline__ void fetch_range(int B, int C, int rank, int& f0, int& f1)
+{
+    int cs = (B + C - 1) / C;
+    cs = (cs + kStage - 1) / kStage * kStage;
+    f0 = min(B, rank * cs);
+    f1 = min(B, f0 + cs);
 }
 
 // ------------------------------------------------------------------ H2O
@@ -277,179 +345,180 @@ __global__ void __launch_bounds__(TL::NT) h2o_decode_kernel(const DecodeArgs a)
     extern __shared__ __align__(128) unsigned char smem_raw[];
     auto& S = *reinterpret_cast<DecodeSmem<T, D, TL>*>(smem_raw);
     constexpr int EPL = D / 32;
+    constexpr int NV = D * (int)sizeof(T) / 16;          // 16-byte vectors per row
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const CacheView& c = a.c;
     const int C = (int)cluster_nctarank();
     const int rank = (int)cluster_ctarank();
     const int unit = blockIdx.x / C;
-    cluster_arrive_relaxed();     // paired with the wait before the first remote store
 
     const int B = c.B;
-    const int2 us = c.ustate[unit];
-    const int n = us.x, p = us.y;
-    const bool full = (n >= B);
-    int cs = (n + C - 1) / C;
-    cs = (cs + TL::G - 1) / TL::G * TL::G;
-    const int c0 = min(n, rank * cs), c1 = min(n, c0 + cs);
     const size_t ub = (size_t)unit * B;
     T* Kc = reinterpret_cast<T*>(c.K) + ub * D;
     T* Vc = reinterpret_cast<T*>(c.V) + ub * D;
-
+    int f0, f1;
+    fetch_range(B, C, rank, f0, f1);
     if (lane == 0) {
 #pragma unroll
         for (int b = 0; b < TL::NBUF; ++b) mbar_init(&S.bar[warp][b], 1);
-        fence_mbar_init();
-        prime_ring<T, D, TL>(S, Kc, Vc, c0, c1);
+        if (C > 1) fence_mbar_init(); else fence_proxy_async_smem();
     }
+    // everything below reads memory the previous kernel in the stream may
+    // have written (this unit's cache, or the inputs)
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (lane == 0) prime_ring<T, D, TL>(S, Kc, Vc, f0, f1);
+    const T* kg = reinterpret_cast<const T*>(a.k) + (size_t)unit * D;
+    const T* vg = reinterpret_cast<const T*>(a.v) + (size_t)unit * D;
+    // the new token's row, written into the victim slot at the end
+    uint4 newrow = make_uint4(0u, 0u, 0u, 0u);
+    if (rank == 0 && tid < 2 * NV)
+        newrow = tid < NV ? reinterpret_cast<const uint4*>(kg)[tid] : reinterpret_cast<const uint4*>(vg)[tid - NV];
+
+    float qp[D / 2];
+    load_q_rotated<T, D>(reinterpret_cast<const T*>(a.q) + (size_t)unit * D, c.qscale, lane, qp);
+    const int2 us = c.ustate[unit];
+    const int n = us.x, p = us.y;
+    const bool full = (n >= B);
+    const int c0 = f0, c1 = min(n, f1);     // live slots of this CTA
 
     // scores and positions of this thread's slots, consumed after the merge
-    double sc_old[TL::SPT];
+    float2 sc_old[TL::SPT];
     int ps[TL::SPT];
 #pragma unroll
     for (int i = 0; i < TL::SPT; ++i) {
         const int s = c0 + tid + i * TL::NT;
-        sc_old[i] = 0.0;
+        sc_old[i] = make_float2(0.f, 0.f);
         ps[i] = 0;
         if (s < c1) { sc_old[i] = c.score[ub + s]; ps[i] = c.pos[ub + s]; }
     }
-
-    float qr[EPL];
-    load_vec<T, EPL>(reinterpret_cast<const T*>(a.q) + (size_t)unit * D + lane * EPL, qr);
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) qr[e] *= c.qscale;
 
     float m_run = -INFINITY, l_run = 0.f, o[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] = 0.f;
     if (rank == 0 && warp == 0) {          // the new token attends to itself
-        float kr[EPL], vr[EPL];
-        load_vec<T, EPL>(reinterpret_cast<const T*>(a.k) + (size_t)unit * D + lane * EPL, kr);
-        load_vec<T, EPL>(reinterpret_cast<const T*>(a.v) + (size_t)unit * D + lane * EPL, vr);
-        float acc = 0.f;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) acc = fmaf(qr[e], kr[e], acc);
-        const float zn = warp_sum(acc);
+        float vr[EPL];
+        const float zn = row_dot<T, D, T>(kg, qp, lane);
+        load_vec<T, EPL>(vg + lane * EPL, vr);
         m_run = zn;
-        l_run = 1.f;
+        l_run = lane == 0 ? 1.f : 0.f;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) o[e] = vr[e];
         if (lane == 0) S.z_new = zn;
     }
     __syncwarp();
 
-    attend_chunk<T, D, TL>(S, Kc, Vc, c0, c1, -1, true, qr, m_run, l_run, o, c.err);
+    attend_chunk<T, D, TL>(S, Kc, Vc, f0, f1, n, -1, true, qp, m_run, l_run, o, c.err);
 
     float Mc, Lc, Oc;
     merge_warps<T, D, TL>(S, m_run, l_run, o, Mc, Lc, Oc);
 
-    // exchange 1: (max, normaliser, output) of every CTA into rank 0
-    cluster_wait();
-    const uint32_t x0 = map_to_rank(&S.x, 0);
-    const uint32_t off_m = (uint32_t)offsetof(Exchange<D>, m), off_l = (uint32_t)offsetof(Exchange<D>, l);
-    const uint32_t off_o = (uint32_t)offsetof(Exchange<D>, o);
-    if (tid < D) st_cluster_f32(x0 + off_o + (uint32_t)((rank * D + tid) * 4), Oc);
-    if (tid == 0) {
-        st_cluster_f32(x0 + off_m + rank * 4, Mc);
-        st_cluster_f32(x0 + off_l + rank * 4, Lc);
+    // exchange 1: (max, normaliser, output) of every CTA into rank 0; a
+    // single-CTA unit already has them
+    const uint32_t x0 = map_to_rank(&S.u.epi.x, 0);
+    float M, invL;
+    if (C > 1) {
+        cluster_arrive();                    // every CTA of the cluster is past its ring
+        cluster_wait();
+        const uint32_t off_m = (uint32_t)offsetof(Exchange<D>, m), off_l = (uint32_t)offsetof(Exchange<D>, l);
+        const uint32_t off_o = (uint32_t)offsetof(Exchange<D>, o);
+        if (tid < D) st_cluster_f32(x0 + off_o + (uint32_t)((rank * D + tid) * 4), Oc);
+        if (tid == 0) {
+            st_cluster_f32(x0 + off_m + rank * 4, Mc);
+            st_cluster_f32(x0 + off_l + rank * 4, Lc);
+        }
+        cluster_arrive();
+        cluster_wait();
+        if (warp == 0) {
+            const float mj = lane < C ? ld_cluster_f32(x0 + off_m + lane * 4) : -INFINITY;
+            const float lj = lane < C ? ld_cluster_f32(x0 + off_l + lane * 4) : 0.f;
+            const float Mx = warp_max(mj);
+            const float Lx = warp_sum(lane < C ? lj * safe_exp2_diff(mj, Mx) : 0.f);
+            if (lane == 0) { S.M = Mx; S.invL = 1.f / Lx; }
+        }
+        __syncthreads();
+        M = S.M;
+        invL = S.invL;
+    } else {
+        M = Mc;
+        invL = 1.f / Lc;
     }
-    cluster_arrive();
-    cluster_wait();
-
-    if (warp == 0) {
-        const float mj = lane < C ? ld_cluster_f32(x0 + off_m + lane * 4) : -INFINITY;
-        const float lj = lane < C ? ld_cluster_f32(x0 + off_l + lane * 4) : 0.f;
-        const float M = warp_max(mj);
-        const float L = warp_sum(lane < C ? lj * safe_exp2_diff(mj, M) : 0.f);
-        if (lane == 0) { S.M = M; S.invL = 1.f / L; }
-    }
-    __syncthreads();
-    const float M = S.M, invL = S.invL;
 
     // accumulate this step's probabilities; arg-min over candidates
-    double best = DBL_MAX, best_all = DBL_MAX;
-    int bslot = INT_MAX, bslot_all = INT_MAX;
+    ArgMin best = argmin_none(), best_all = argmin_none();
 #pragma unroll
     for (int i = 0; i < TL::SPT; ++i) {
         const int s = c0 + tid + i * TL::NT;
         if (s < c1) {
             const float P = exp2f(S.z[s - c0] - M) * invL;
-            const double ns = sc_old[i] + (double)P;
+            const float2 ns = pair_add(sc_old[i], P);
             c.score[ub + s] = ns;
             if (full) {
-                if (ps[i] <= p - c.r && (ns < best || (ns == best && s < bslot))) { best = ns; bslot = s; }
-                if (ns < best_all || (ns == best_all && s < bslot_all)) { best_all = ns; bslot_all = s; }
+                const ArgMin k = ArgMin{ord_key(ns.x), ord_key(ns.y), (unsigned)s};
+                if (ps[i] <= p - c.r) argmin_take(best, k);
+                argmin_take(best_all, k);
             }
         }
     }
     if (full) {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const double ob = __shfl_xor_sync(kFull, best, off);
-            const int os = __shfl_xor_sync(kFull, bslot, off);
-            if (ob < best || (ob == best && os < bslot)) { best = ob; bslot = os; }
-            const double oa = __shfl_xor_sync(kFull, best_all, off);
-            const int osa = __shfl_xor_sync(kFull, bslot_all, off);
-            if (oa < best_all || (oa == best_all && osa < bslot_all)) { best_all = oa; bslot_all = osa; }
-        }
+        best = warp_argmin(best);
+        best_all = warp_argmin(best_all);
         if (lane == 0) {
-            S.rd[0][warp] = best; S.ri[0][warp] = bslot;
-            S.rd[1][warp] = best_all; S.ri[1][warp] = bslot_all;
+            S.am[0][0][warp] = best.hi; S.am[0][1][warp] = best.lo; S.am[0][2][warp] = best.slot;
+            S.am[1][0][warp] = best_all.hi; S.am[1][1][warp] = best_all.lo; S.am[1][2][warp] = best_all.slot;
         }
     }
     if (rank == 0 && tid < D) {
-        float acc = 0.f;
-        for (int j = 0; j < C; ++j) acc += S.x.o[j][tid] * safe_exp2_diff(S.x.m[j], M);
+        float acc = Oc;
+        if (C > 1) {
+            acc = 0.f;
+            for (int j = 0; j < C; ++j) acc += S.u.epi.x.o[j][tid] * safe_exp2_diff(S.u.epi.x.m[j], M);
+        }
         a.out[(size_t)unit * D + tid] = acc * invL;
     }
     if (rank == 0 && tid == 0) S.P_new = exp2f(S.z_new - M) * invL;
     __syncthreads();
-    if (full && tid == 0) {
-        for (int w = 1; w < TL::NW; ++w) {
-            if (S.rd[0][w] < best || (S.rd[0][w] == best && S.ri[0][w] < bslot)) { best = S.rd[0][w]; bslot = S.ri[0][w]; }
-            if (S.rd[1][w] < best_all || (S.rd[1][w] == best_all && S.ri[1][w] < bslot_all)) {
-                best_all = S.rd[1][w]; bslot_all = S.ri[1][w];
+    if (full && warp == 0) {
+        // this CTA's arg-min over its warps, pushed into rank 0's exchange
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            ArgMin w = lane < TL::NW ? ArgMin{S.am[k][0][lane], S.am[k][1][lane], S.am[k][2][lane]} : argmin_none();
+            w = warp_argmin(w);
+            if (lane == 0) {
+                const uint32_t base = x0 + (uint32_t)offsetof(Exchange<D>, am) + (uint32_t)(k * 3 * kMaxSplit * 4);
+                st_cluster_s32(base + rank * 4, (int)w.hi);
+                st_cluster_s32(base + (kMaxSplit + rank) * 4, (int)w.lo);
+                st_cluster_s32(base + (2 * kMaxSplit + rank) * 4, (int)w.slot);
             }
         }
-        const uint32_t base = x0;
-        st_cluster_f64(base + (uint32_t)offsetof(Exchange<D>, cand_score) + rank * 8, best);
-        st_cluster_s32(base + (uint32_t)offsetof(Exchange<D>, cand_slot) + rank * 4, bslot);
-        st_cluster_f64(base + (uint32_t)offsetof(Exchange<D>, all_score) + rank * 8, best_all);
-        st_cluster_s32(base + (uint32_t)offsetof(Exchange<D>, all_slot) + rank * 4, bslot_all);
     }
     // exchange 2: arg-min of every CTA into rank 0
-    cluster_arrive();
-    cluster_wait();
+    cta_group_sync(C);
     if (rank != 0) return;
 
     if (tid == 0) {
         int victim = n;
         if (full) {
-            double vb = DBL_MAX, va = DBL_MAX;
-            int vs = INT_MAX, vsa = INT_MAX;
+            ArgMin vc = argmin_none(), va = argmin_none();
             for (int j = 0; j < C; ++j) {
-                const double sj = S.x.cand_score[j];
-                const int ij = S.x.cand_slot[j];
-                if (ij != INT_MAX && (sj < vb || (sj == vb && ij < vs))) { vb = sj; vs = ij; }
-                const double sa = S.x.all_score[j];
-                const int ia = S.x.all_slot[j];
-                if (ia != INT_MAX && (sa < va || (sa == va && ia < vsa))) { va = sa; vsa = ia; }
+                argmin_take(vc, ArgMin{S.u.epi.x.am[0][0][j], S.u.epi.x.am[0][1][j], S.u.epi.x.am[0][2][j]});
+                argmin_take(va, ArgMin{S.u.epi.x.am[1][0][j], S.u.epi.x.am[1][1][j], S.u.epi.x.am[1][2][j]});
             }
-            victim = (vs != INT_MAX) ? vs : vsa;
+            victim = (int)(vc.slot != 0xffffffffu ? vc.slot : va.slot);
         }
         if (victim < 0 || victim >= B) victim = 0;   // n == 0 with B == 0 cannot happen
         S.victim = victim;
-        c.score[ub + victim] = (double)S.P_new;
+        c.score[ub + victim] = make_float2(S.P_new, 0.f);
         c.pos[ub + victim] = p;
         c.ustate[unit] = make_int2(min(n + 1, B), p + 1);
         if (a.victim_out) a.victim_out[unit] = full ? victim : -1;
     }
     __syncthreads();
     const int victim = S.victim;
-    constexpr int NV = D * (int)sizeof(T) / 16;
     if (tid < NV)
-        copy_row<T, D>(Kc + (size_t)victim * D, reinterpret_cast<const T*>(a.k) + (size_t)unit * D, tid);
+        reinterpret_cast<uint4*>(Kc + (size_t)victim * D)[tid] = newrow;
     else if (tid < 2 * NV)
-        copy_row<T, D>(Vc + (size_t)victim * D, reinterpret_cast<const T*>(a.v) + (size_t)unit * D, tid - NV);
+        reinterpret_cast<uint4*>(Vc + (size_t)victim * D)[tid - NV] = newrow;
 }
 
 // ------------------------------------------------------------------ LSH
@@ -460,33 +529,42 @@ __global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
     extern __shared__ __align__(128) unsigned char smem_raw[];
     auto& S = *reinterpret_cast<DecodeSmem<T, D, TL>*>(smem_raw);
     constexpr int EPL = D / 32;
+    constexpr int NV = D * (int)sizeof(T) / 16;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const CacheView& c = a.c;
     const int C = (int)cluster_nctarank();
     const int rank = (int)cluster_ctarank();
     const int unit = blockIdx.x / C;
-    cluster_arrive_relaxed();
 
     const int B = c.B;
-    const int2 us = c.ustate[unit];
-    const int n = us.x, p = us.y;
-    const bool full = (n >= B);
-    int cs = (n + C - 1) / C;
-    cs = (cs + TL::G - 1) / TL::G * TL::G;
-    const int c0 = min(n, rank * cs), c1 = min(n, c0 + cs);
     const size_t ub = (size_t)unit * B;
     T* Kc = reinterpret_cast<T*>(c.K) + ub * D;
     T* Vc = reinterpret_cast<T*>(c.V) + ub * D;
-
+    int f0, f1;
+    fetch_range(B, C, rank, f0, f1);
     if (lane == 0) {
 #pragma unroll
         for (int b = 0; b < TL::NBUF; ++b) mbar_init(&S.bar[warp][b], 1);
-        fence_mbar_init();
-        prime_ring<T, D, TL>(S, Kc, Vc, c0, c1);
+        if (C > 1) fence_mbar_init(); else fence_proxy_async_smem();
     }
-
+    // everything below reads memory the previous kernel in the stream may
+    // have written (this unit's cache, or the inputs)
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (lane == 0) prime_ring<T, D, TL>(S, Kc, Vc, f0, f1);
     const T* qg = reinterpret_cast<const T*>(a.q) + (size_t)unit * D;
     const T* kg = reinterpret_cast<const T*>(a.k) + (size_t)unit * D;
+    const T* vg = reinterpret_cast<const T*>(a.v) + (size_t)unit * D;
+    uint4 newrow = make_uint4(0u, 0u, 0u, 0u);
+    if (rank == 0 && tid < 2 * NV)
+        newrow = tid < NV ? reinterpret_cast<const uint4*>(kg)[tid] : reinterpret_cast<const uint4*>(vg)[tid - NV];
+
+    float qp[D / 2];
+    load_q_rotated<T, D>(qg, c.qscale, lane, qp);
+    const int2 us = c.ustate[unit];
+    const int n = us.x, p = us.y;
+    const bool full = (n >= B);
+
     if (tid < D) {
         S.qf[tid] = Elem<T>::to_f(qg[tid]);
         S.kf[tid] = Elem<T>::to_f(kg[tid]);
@@ -538,55 +616,53 @@ __global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
     __syncthreads();
     const int victim = S.victim;
 
-    float qr[EPL];
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) qr[e] = S.qf[lane * EPL + e] * c.qscale;
     float m_run = -INFINITY, l_run = 0.f, o[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] = 0.f;
     if (rank == 0 && warp == 0) {          // the new token, now in the victim slot
-        float acc = 0.f;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) acc = fmaf(qr[e], S.kf[lane * EPL + e], acc);
-        const float zn = warp_sum(acc);
+        const float zn = row_dot<T, D, T>(kg, qp, lane);
         float vr[EPL];
-        load_vec<T, EPL>(reinterpret_cast<const T*>(a.v) + (size_t)unit * D + lane * EPL, vr);
+        load_vec<T, EPL>(vg + lane * EPL, vr);
         m_run = zn;
-        l_run = 1.f;
+        l_run = lane == 0 ? 1.f : 0.f;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) o[e] = vr[e];
     }
     __syncwarp();
 
-    attend_chunk<T, D, TL>(S, Kc, Vc, c0, c1, full ? victim : -1, false, qr, m_run, l_run, o,
-                             c.err);
+    attend_chunk<T, D, TL>(S, Kc, Vc, f0, f1, n, full ? victim : -1, false, qp, m_run, l_run, o,
+                           c.err);
 
     float Mc, Lc, Oc;
     merge_warps<T, D, TL>(S, m_run, l_run, o, Mc, Lc, Oc);
 
-    cluster_wait();
-    const uint32_t x0 = map_to_rank(&S.x, 0);
-    const uint32_t off_m = (uint32_t)offsetof(Exchange<D>, m), off_l = (uint32_t)offsetof(Exchange<D>, l);
-    const uint32_t off_o = (uint32_t)offsetof(Exchange<D>, o);
-    if (tid < D) st_cluster_f32(x0 + off_o + (uint32_t)((rank * D + tid) * 4), Oc);
-    if (tid == 0) {
-        st_cluster_f32(x0 + off_m + rank * 4, Mc);
-        st_cluster_f32(x0 + off_l + rank * 4, Lc);
-    }
-    cluster_arrive();
-    cluster_wait();
-    if (rank != 0) return;
-
-    if (tid < D) {
-        float M = -INFINITY;
-        for (int j = 0; j < C; ++j) M = fmaxf(M, S.x.m[j]);
-        float L = 0.f, acc = 0.f;
-        for (int j = 0; j < C; ++j) {
-            const float f = safe_exp2_diff(S.x.m[j], M);
-            L += S.x.l[j] * f;
-            acc += S.x.o[j][tid] * f;
+    if (C > 1) {
+        cluster_arrive();                    // every CTA of the cluster is past its ring
+        cluster_wait();
+        const uint32_t x0 = map_to_rank(&S.u.epi.x, 0);
+        const uint32_t off_m = (uint32_t)offsetof(Exchange<D>, m), off_l = (uint32_t)offsetof(Exchange<D>, l);
+        const uint32_t off_o = (uint32_t)offsetof(Exchange<D>, o);
+        if (tid < D) st_cluster_f32(x0 + off_o + (uint32_t)((rank * D + tid) * 4), Oc);
+        if (tid == 0) {
+            st_cluster_f32(x0 + off_m + rank * 4, Mc);
+            st_cluster_f32(x0 + off_l + rank * 4, Lc);
         }
-        a.out[(size_t)unit * D + tid] = acc / L;
+        cluster_arrive();
+        cluster_wait();
+        if (rank != 0) return;
+        if (tid < D) {
+            float Mx = -INFINITY;
+            for (int j = 0; j < C; ++j) Mx = fmaxf(Mx, S.u.epi.x.m[j]);
+            float L = 0.f, acc = 0.f;
+            for (int j = 0; j < C; ++j) {
+                const float f = safe_exp2_diff(S.u.epi.x.m[j], Mx);
+                L += S.u.epi.x.l[j] * f;
+                acc += S.u.epi.x.o[j][tid] * f;
+            }
+            a.out[(size_t)unit * D + tid] = acc / L;
+        }
+    } else if (tid < D) {
+        a.out[(size_t)unit * D + tid] = Oc / Lc;
     }
     if (tid == 0) {
         c.code[ub + victim] = S.code_k;
@@ -594,16 +670,38 @@ __global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
         c.ustate[unit] = make_int2(min(n + 1, B), p + 1);
         if (a.victim_out) a.victim_out[unit] = full ? victim : -1;
     }
-    constexpr int NV = D * (int)sizeof(T) / 16;
     if (tid < NV)
-        copy_row<T, D>(Kc + (size_t)victim * D, kg, tid);
+        reinterpret_cast<uint4*>(Kc + (size_t)victim * D)[tid] = newrow;
     else if (tid < 2 * NV)
-        copy_row<T, D>(Vc + (size_t)victim * D, reinterpret_cast<const T*>(a.v) + (size_t)unit * D, tid - NV);
+        reinterpret_cast<uint4*>(Vc + (size_t)victim * D)[tid - NV] = newrow;
 }
 
 // ------------------------------------------------------------- launching
 
-using TileDefault = Tile<8, 8, 2>;
+using TileDefault = Tile<6, 2>;
+
+// Programmatic dependent launch is on unless H2O_PDL=0 (for comparisons).
+bool pdl_enabled()
+{
+    static int v = -1;
+    if (v < 0) {
+        const char* e = getenv("H2O_PDL");
+        v = (e && e[0] == '0') ? 0 : 1;
+    }
+    return v == 1;
+}
+
+// Tile variants for bf16 / head_dim 128, selectable with H2O_DECODE_TILE for
+// tuning; every variant computes the same result.
+int tile_variant()
+{
+    static int v = -1;
+    if (v < 0) {
+        const char* e = getenv("H2O_DECODE_TILE");
+        v = e ? atoi(e) : 0;
+    }
+    return v;
+}
 
 template <typename T, int D, bool LSH, class TL>
 cudaError_t launch_decode_t(const DecodeArgs& a, int split, cudaStream_t st)
@@ -627,26 +725,22 @@ cudaError_t launch_decode_t(const DecodeArgs& a, int split, cudaStream_t st)
     cfg.blockDim = dim3(TL::NT, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)split;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
-}
-
-// Tile variants for bf16 / head_dim 128, selectable with H2O_DECODE_TILE for
-// tuning; every variant computes the same result.
-int tile_variant()
-{
-    static int v = -1;
-    if (v < 0) {
-        const char* e = getenv("H2O_DECODE_TILE");
-        v = e ? atoi(e) : 0;
+    // programmatic dependent launch: this grid may be scheduled while the
+    // previous one drains; the kernel waits for it before reading memory
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    int na = 1;
+    if (split > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)split;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        na = 2;
     }
-    return v;
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 template <bool LSH>
@@ -655,12 +749,12 @@ cudaError_t dispatch(const DecodeArgs& a, int split, cudaStream_t st)
     const bool bf = a.c.dtype == 1;
     if (a.c.D == 128 && bf) {
         switch (tile_variant()) {
-        case 1: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<16, 8, 1>>(a, split, st);
-        case 2: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<16, 4, 2>>(a, split, st);
-        case 3: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<8, 4, 4>>(a, split, st);
-        case 4: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<16, 8, 2>>(a, split, st);
-        case 5: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<8, 8, 3>>(a, split, st);
-        case 6: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<4, 8, 4>>(a, split, st);
+        case 1: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<4, 2>>(a, split, st);
+        case 2: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<6, 2>>(a, split, st);
+        case 3: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<4, 3>>(a, split, st);
+        case 4: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<12, 1>>(a, split, st);
+        case 5: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<13, 1>>(a, split, st);
+        case 6: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<8, 2>>(a, split, st);
         default: return launch_decode_t<__nv_bfloat16, 128, LSH, TileDefault>(a, split, st);
         }
     }

@@ -66,7 +66,7 @@ struct h2o_ctx {
     // cache
     void* K;
     void* V;
-    double* score;
+    float2* score;             // hi + lo fp32 pairs
     int* pos;
     uint32_t* code;
     int2* ustate;
@@ -169,7 +169,7 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
         free_all(h); delete h; return rc;
     }
     if (kind == kH2O) {
-        if ((rc = dev_alloc((void**)&h->score, U * B * sizeof(double), "scores"))) { free_all(h); delete h; return rc; }
+        if ((rc = dev_alloc((void**)&h->score, U * B * sizeof(float2), "scores"))) { free_all(h); delete h; return rc; }
     } else {
         if ((rc = dev_alloc((void**)&h->code, U * B * sizeof(uint32_t), "codes")) ||
             (rc = dev_alloc((void**)&h->W, (size_t)head_dim * 32 * sizeof(float), "projection"))) {
@@ -329,9 +329,15 @@ int h2o_get_state(h2o_handle h, void* K, void* V, double* score, int* pos, unsig
     if (K && e == cudaSuccess) e = cudaMemcpyAsync(K, h->K, UB * row, cudaMemcpyDeviceToHost, h->stream);
     if (V && e == cudaSuccess) e = cudaMemcpyAsync(V, h->V, UB * row, cudaMemcpyDeviceToHost, h->stream);
     if (pos && e == cudaSuccess) e = cudaMemcpyAsync(pos, h->pos, UB * sizeof(int), cudaMemcpyDeviceToHost, h->stream);
+    float2* pairs = nullptr;
     if (score && e == cudaSuccess) {
-        if (h->score) e = cudaMemcpyAsync(score, h->score, UB * sizeof(double), cudaMemcpyDeviceToHost, h->stream);
-        else memset(score, 0, UB * sizeof(double));
+        if (h->score) {
+            pairs = static_cast<float2*>(malloc(UB * sizeof(float2)));
+            if (!pairs) return fail(H2O_ERR_ALLOC, "host allocation failed");
+            e = cudaMemcpyAsync(pairs, h->score, UB * sizeof(float2), cudaMemcpyDeviceToHost, h->stream);
+        } else {
+            memset(score, 0, UB * sizeof(double));
+        }
     }
     if (code && e == cudaSuccess) {
         if (h->code) e = cudaMemcpyAsync(code, h->code, UB * sizeof(uint32_t), cudaMemcpyDeviceToHost, h->stream);
@@ -350,7 +356,10 @@ int h2o_get_state(h2o_handle h, void* K, void* V, double* score, int* pos, unsig
             if (next_pos) next_pos[u] = us[u].y;
         }
     }
+    if (e == cudaSuccess && pairs)
+        for (size_t i = 0; i < UB; ++i) score[i] = (double)pairs[i].x + (double)pairs[i].y;
     free(us);
+    free(pairs);
     if (e != cudaSuccess) return cuda_fail(e, "h2o_get_state");
     return H2O_OK;
 }
@@ -367,8 +376,16 @@ int h2o_set_state(h2o_handle h, const void* K, const void* V, const double* scor
     if (K && e == cudaSuccess) e = cudaMemcpyAsync(h->K, K, UB * row, cudaMemcpyHostToDevice, h->stream);
     if (V && e == cudaSuccess) e = cudaMemcpyAsync(h->V, V, UB * row, cudaMemcpyHostToDevice, h->stream);
     if (pos && e == cudaSuccess) e = cudaMemcpyAsync(h->pos, pos, UB * sizeof(int), cudaMemcpyHostToDevice, h->stream);
-    if (score && h->score && e == cudaSuccess)
-        e = cudaMemcpyAsync(h->score, score, UB * sizeof(double), cudaMemcpyHostToDevice, h->stream);
+    float2* pairs = nullptr;
+    if (score && h->score && e == cudaSuccess) {
+        pairs = static_cast<float2*>(malloc(UB * sizeof(float2)));
+        if (!pairs) return fail(H2O_ERR_ALLOC, "host allocation failed");
+        for (size_t i = 0; i < UB; ++i) {
+            const float hi = (float)score[i];
+            pairs[i] = make_float2(hi, (float)(score[i] - (double)hi));
+        }
+        e = cudaMemcpyAsync(h->score, pairs, UB * sizeof(float2), cudaMemcpyHostToDevice, h->stream);
+    }
     if (code && h->code && e == cudaSuccess)
         e = cudaMemcpyAsync(h->code, code, UB * sizeof(uint32_t), cudaMemcpyHostToDevice, h->stream);
     int2* us = nullptr;
@@ -387,6 +404,7 @@ int h2o_set_state(h2o_handle h, const void* K, const void* V, const double* scor
     }
     if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
     free(us);
+    free(pairs);
     if (e != cudaSuccess) return cuda_fail(e, "h2o_set_state");
     h->ready = 1;
     return H2O_OK;

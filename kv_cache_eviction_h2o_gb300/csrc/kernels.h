@@ -10,7 +10,7 @@ namespace h2o {
 struct CacheView {
     void* K;            // [U][B][D] element type per dtype
     void* V;            // [U][B][D]
-    double* score;      // [U][B] accumulated attention (H2O)
+    float2* score;      // [U][B] accumulated attention (H2O) as an unevaluated fp32 pair hi + lo
     int* pos;           // [U][B] token position per slot, -1 = empty
     uint32_t* code;     // [U][B] key codes (LSH)
     int2* ustate;       // [U] {occupancy, position of the next token}

@@ -334,14 +334,17 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(CacheView cv, Promp
             }
             if (k) {
                 cv.pos[ub + slot] = j;
-                if (cv.score) cv.score[ub + slot] = cu[j];
+                if (cv.score) {
+                    const float hi = __double2float_rn(cu[j]);
+                    cv.score[ub + slot] = make_float2(hi, __double2float_rn(cu[j] - (double)hi));
+                }
                 ++slot;
             }
         }
     }
     for (int s = nkept + tid; s < B; s += kSelThreads) {
         cv.pos[ub + s] = -1;
-        if (cv.score) cv.score[ub + s] = 0.0;
+        if (cv.score) cv.score[ub + s] = make_float2(0.f, 0.f);
     }
     if (tid == 0) cv.ustate[unit] = make_int2(nkept, T_);
 }
