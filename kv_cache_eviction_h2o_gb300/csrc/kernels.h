@@ -48,6 +48,9 @@ int auto_decode_split(int U, int B, int num_sms);
 int max_decode_split();
 
 cudaError_t launch_prompt_stats(const CacheView& c, const PromptArgs& p, cudaStream_t st);
+// tensor-core prompt scorer (bf16, head_dim 128)
+bool prompt_tc_supported(const CacheView& c);
+cudaError_t launch_prompt_stats_tc(const CacheView& c, const PromptArgs& p, cudaStream_t st);
 cudaError_t launch_select(const CacheView& c, const PromptArgs& p, cudaStream_t st);
 cudaError_t launch_gather(const CacheView& c, const PromptArgs& p, bool with_codes, cudaStream_t st);
 // Record a failure for h2o_last_error() and return `code`.

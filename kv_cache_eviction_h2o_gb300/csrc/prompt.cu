@@ -15,6 +15,7 @@
 // sums; logits are kept in base 2 (q is pre-multiplied by scale * log2 e).
 #include <cfloat>
 #include <climits>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -26,6 +27,14 @@ namespace {
 constexpr int kTile = 64;          // rows / columns per score tile
 constexpr int kPad = 4;
 constexpr unsigned kFull = 0xffffffffu;
+
+// H2O_PROMPT_CUDA_CORES=1 selects the CUDA-core scorer for bf16 / d 128 too
+// (used to compare the two implementations)
+bool getenv_flag(const char* name)
+{
+    const char* e = getenv(name);
+    return e && e[0] == '1';
+}
 
 // Load rows [r0, r0 + 64) of X [T][D] into Xs[D][64 + pad] transposed and
 // scaled; rows past T are zero.  Thread t handles row t % 64.
@@ -527,6 +536,8 @@ cudaError_t lsh_t(const CacheView& c, const PromptArgs& p, const float* W, cudaS
 
 cudaError_t launch_prompt_stats(const CacheView& c, const PromptArgs& p, cudaStream_t st)
 {
+    if (prompt_tc_supported(c) && !getenv_flag("H2O_PROMPT_CUDA_CORES"))
+        return launch_prompt_stats_tc(c, p, st);
     const bool bf = c.dtype == 1;
     if (c.D == 128) return bf ? stats_t<__nv_bfloat16, 128>(c, p, st) : stats_t<float, 128>(c, p, st);
     if (c.D == 64) return bf ? stats_t<__nv_bfloat16, 64>(c, p, st) : stats_t<float, 64>(c, p, st);

@@ -1,0 +1,497 @@
+// prompt_tc.cu -- the H2O prompt scorer on the 5th-generation tensor cores.
+//
+// [H2O review page, 提案手法: the accumulated attention of prompt token j,
+//  c_j = sum_{i >= j} exp(z_ij - m_i) / l_i, ranks the heavy hitters.]
+//
+// Two passes over the causal 128 x 128 score tiles of each (batch, head)
+// unit, bf16 inputs, head_dim 128:
+//   pass 1  S = Q_blk K_blk^T        -> per row i: m2_i (base-2 max), l_i
+//   pass 2  S^T = K_blk Q_blk^T      -> per key j: c_j = sum_i 2^(s_ij - m2_i) / l_i
+// Pass 2 computes the transposed tile so that TMEM lane = key: each epilogue
+// thread owns one key and sums its 128 query columns in registers; no
+// cross-thread reduction is needed for the column sums.
+//
+// Per CTA (192 threads): warp 0 issues TMA loads (128-byte swizzled boxes
+// of 128 rows x 64 columns) into a ring of stages; lane 0 of warp 1 issues
+// tcgen05.mma (M = N = 128, K = 16 per instruction, fp32 accumulate) into
+// one of two TMEM accumulators and commits to mbarriers; warps 2..5 drain
+// the accumulators with tcgen05.ld (thread = TMEM lane = tile row).  The
+// MMA of tile t+1 overlaps the exponentials of tile t.  Every wait is
+// bounded: a wait that runs out sets the handle's error word and the CTA
+// abandons its loop, waits (bounded) for its copies in flight, frees its
+// TMEM and returns.
+#include <cuda.h>
+#include <cfloat>
+#include <cstddef>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace h2o {
+
+namespace {
+
+constexpr int kT = 128;                          // tile rows / columns
+constexpr int kD = 128;                          // head dim handled here
+constexpr int kStages = 2;                       // B-operand ring depth
+constexpr uint32_t kBox = kT * 64 * 2;           // one 128 x 64 bf16 box: 16 KB
+constexpr uint32_t kTile = 2 * kBox;             // 128 x 128 bf16: 32 KB
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 2 * kT;           // two fp32 accumulators
+
+// instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits
+// 4-5 = 1), bf16 A and B (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 =
+// 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kT >> 3) << 17) |
+                            ((uint32_t)(kT >> 4) << 24);
+
+// ----------------------------------------------------------------- PTX
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* holder, uint32_t cols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(holder)),
+                 "r"(cols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+// arrive on `bar` once every tcgen05 operation issued so far has completed
+__device__ __forceinline__ void tc_commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzled layout TMA writes: start address >> 4 (bits 0-13), leading
+// offset 1 (unused for this layout), stride between 8-row groups 1024 B
+// (bits 32-45, >> 4), descriptor version 1 (bits 46-47), swizzle mode
+// 128 B (value 2 at bits 61-63).
+__device__ __forceinline__ uint64_t sw128_desc(const void* p)
+{
+    const uint32_t a = smem_u32(p);
+    return (uint64_t)((a & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Issue the 8 MMAs of one 128 x 128 x 128 tile: K slice k (16 elements,
+// 32 bytes) sits in box k / 4 at byte offset 32 (k % 4) of each 128-byte
+// swizzled row.
+__device__ __forceinline__ void tile_mma(uint32_t d_tmem, const uint8_t* a, const uint8_t* b)
+{
+#pragma unroll
+    for (int k = 0; k < kD / 16; ++k) {
+        const uint32_t off = (uint32_t)(k / 4) * kBox + (uint32_t)(k % 4) * 32u;
+        tc_mma(d_tmem, sw128_desc(a + off), sw128_desc(b + off), k > 0 ? 1u : 0u);
+    }
+}
+
+struct alignas(1024) TcSmem {
+    uint8_t a[kTile];                 // the tile's own block (Q in pass 1, K in pass 2)
+    uint8_t b[kStages][kTile];        // ring of the swept blocks
+    alignas(16) float colstat[2][2][kT];   // pass 2: per accumulator, m2 and 1/l of the 128 queries (read as float4)
+    uint64_t a_full;
+    uint64_t b_full[kStages];
+    uint64_t b_empty[kStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(offsetof(TcSmem, colstat) % 16 == 0, "colstat is read as float4");
+static_assert(offsetof(TcSmem, b) % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+
+__device__ __forceinline__ TcSmem& tc_smem(unsigned char* raw)
+{
+    const uintptr_t p = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~(uintptr_t)1023;
+    return *reinterpret_cast<TcSmem*>(p);
+}
+
+// bounded wait that also watches the CTA's abort flag
+__device__ __forceinline__ bool tc_wait(TcSmem& S, uint64_t* bar, uint32_t parity, int* err)
+{
+    if (mbar_wait(bar, parity)) return true;
+    if (err) atomicOr(err, kErrWaitTimeout);
+    *(volatile int*)&S.abort = 1;
+    return false;
+}
+
+__device__ __forceinline__ bool aborted(TcSmem& S) { return *(volatile int*)&S.abort != 0; }
+
+// OR of `pred` over the 128 epilogue threads (named barrier 1); also orders
+// their earlier shared-memory writes before the later reads
+__device__ __forceinline__ bool epilogue_any(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "barrier.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void tc_setup(TcSmem& S, int warp)
+{
+    if (threadIdx.x == 0) {
+        mbar_init(&S.a_full, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&S.b_full[s], 1);
+            mbar_init(&S.b_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&S.acc_full[b], 1);
+            mbar_init(&S.acc_empty[b], 4);        // one arrival per epilogue warp
+        }
+        S.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&S.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
+__device__ __forceinline__ void tc_teardown(TcSmem& S, int warp, int n_b_loads)
+{
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (aborted(S) && threadIdx.x == 0) {
+        // copies may still be in flight: wait (bounded) for every stage's
+        // last load before the CTA's shared memory is released
+        for (int t = (n_b_loads > kStages ? n_b_loads - kStages : 0); t < n_b_loads; ++t)
+            mbar_wait(&S.b_full[t % kStages], (uint32_t)(t / kStages) & 1u);
+        mbar_wait(&S.a_full, 0);
+    }
+    if (warp == 1) tmem_dealloc(S.tmem_base, kTmemCols);
+}
+
+// Producer: the CTA's own block once, then the swept blocks `first..last`
+// (inclusive) through the ring.  In pass 2 it also stages nothing else.
+__device__ __forceinline__ void tc_producer(TcSmem& S, const CUtensorMap* map_a, const CUtensorMap* map_b,
+                                            int row_a, int row0_b, int first, int last, int* err)
+{
+    mbar_arrive_expect_tx(&S.a_full, kTile);
+    tma_load_2d(S.a, map_a, 0, row_a, &S.a_full);
+    tma_load_2d(S.a + kBox, map_a, 64, row_a, &S.a_full);
+    for (int t = 0; first + t <= last; ++t) {
+        const int s = t % kStages;
+        if (t >= kStages && !tc_wait(S, &S.b_empty[s], ((uint32_t)(t / kStages) & 1u) ^ 1u, err)) return;
+        if (aborted(S)) return;
+        mbar_arrive_expect_tx(&S.b_full[s], kTile);
+        tma_load_2d(S.b[s], map_b, 0, row0_b + (first + t) * kT, &S.b_full[s]);
+        tma_load_2d(S.b[s] + kBox, map_b, 64, row0_b + (first + t) * kT, &S.b_full[s]);
+    }
+}
+
+// MMA issuer (one thread): tile t of the sweep into accumulator t & 1.
+__device__ __forceinline__ void tc_mma_loop(TcSmem& S, uint32_t tbase, int ntiles, int* err)
+{
+    if (!tc_wait(S, &S.a_full, 0, err)) return;
+    for (int t = 0; t < ntiles; ++t) {
+        const int s = t % kStages, b = t & 1;
+        if (!tc_wait(S, &S.b_full[s], (uint32_t)(t / kStages) & 1u, err)) return;
+        if (t >= 2 && !tc_wait(S, &S.acc_empty[b], ((uint32_t)(t >> 1) & 1u) ^ 1u, err)) return;
+        if (aborted(S)) return;
+        tc_fence_after();
+        tile_mma(tbase + (uint32_t)b * kT, S.a, S.b[s]);
+        tc_commit(&S.b_empty[s]);       // the stage is free once these MMAs have read it
+        tc_commit(&S.acc_full[b]);      // and the accumulator is ready for the epilogue
+    }
+}
+
+// ------------------------------------------------------------- pass 1
+
+// grid: U * nb CTAs; CTA x handles row block ib = nb - 1 - x / U of unit
+// x % U (heaviest blocks first)
+__global__ void __launch_bounds__(kThreads, 1)
+    rowstats_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK, int U,
+                       int T, int nb, float c2, float* __restrict__ m2, float* __restrict__ lout, int* err)
+{
+    extern __shared__ unsigned char smem_raw[];
+    TcSmem& S = tc_smem(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int u = blockIdx.x % U;
+    const int ib = nb - 1 - (int)(blockIdx.x / U);
+    const int row0 = u * T;
+    const int ntiles = ib + 1;
+    tc_setup(S, warp);
+    const uint32_t tbase = S.tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) tc_producer(S, &mapQ, &mapK, row0 + ib * kT, row0, 0, ib, err);
+    } else if (warp == 1) {
+        if (lane == 0) tc_mma_loop(S, tbase, ntiles, err);
+        __syncwarp();
+    } else {
+        const int q = warp & 3;                   // TMEM lane quarter of this warp
+        const int i = ib * kT + 32 * q + lane;    // query row within the unit
+        float m = -INFINITY, l = 0.f, lc = 0.f;   // running base-2 max, Kahan-summed normaliser
+        for (int t = 0; t < ntiles; ++t) {
+            const int b = t & 1;
+            const bool ok = tc_wait(S, &S.acc_full[b], (uint32_t)(t >> 1) & 1u, err);
+            if (__any_sync(0xffffffffu, !ok || aborted(S))) break;
+            tc_fence_after();
+            const bool diag = (t == ib);
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+                float v[32];
+                tc_ld32(tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * kT + ch * 32), v);
+                const int j0 = t * kT + ch * 32;
+                float cm = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    if (diag && j0 + e > i) v[e] = -INFINITY;
+                    cm = fmaxf(cm, v[e]);
+                }
+                if (cm != -INFINITY) {
+                    cm *= c2;
+                    if (cm > m) {
+                        const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - cm);
+                        l *= alpha;
+                        lc *= alpha;
+                        m = cm;
+                    }
+                    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        s0 += exp2f(fmaf(v[e], c2, -m));
+                        s1 += exp2f(fmaf(v[e + 1], c2, -m));
+                    }
+                    // Kahan step
+                    const float y = (s0 + s1) - lc;
+                    const float tsum = l + y;
+                    lc = (tsum - l) - y;
+                    l = tsum;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.acc_empty[b]);
+        }
+        if (i < T && !aborted(S)) {
+            m2[(size_t)u * T + i] = m;
+            lout[(size_t)u * T + i] = l - lc;
+        }
+    }
+    tc_teardown(S, warp, ntiles);
+}
+
+// ------------------------------------------------------------- pass 2
+
+// grid: U * nb CTAs; CTA x handles key block jb = x / U of unit x % U
+// (heaviest blocks, small jb, first) and sweeps query blocks jb..nb-1
+__global__ void __launch_bounds__(kThreads, 1)
+    colsum_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK, int U,
+                     int T, int nb, float c2, const float* __restrict__ m2, const float* __restrict__ lin,
+                     double* __restrict__ cout, int* err)
+{
+    extern __shared__ unsigned char smem_raw[];
+    TcSmem& S = tc_smem(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int u = blockIdx.x % U;
+    const int jb = (int)(blockIdx.x / U);
+    const int row0 = u * T;
+    const int ntiles = nb - jb;
+    const float* m2u = m2 + (size_t)u * T;
+    const float* lu = lin + (size_t)u * T;
+    tc_setup(S, warp);
+    const uint32_t tbase = S.tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) tc_producer(S, &mapK, &mapQ, row0 + jb * kT, row0, jb, nb - 1, err);
+    } else if (warp == 1) {
+        if (lane == 0) tc_mma_loop(S, tbase, ntiles, err);
+        __syncwarp();
+    } else {
+        const int et = threadIdx.x - 64;          // epilogue thread 0..127
+        const int q = warp & 3;
+        const int j = jb * kT + 32 * q + lane;    // key within the unit
+        // stage the query statistics of tile 0 (m2 and 1/l; zero weight past T)
+        {
+            const int i = jb * kT + et;
+            S.colstat[0][0][et] = i < T ? m2u[i] : 0.f;
+            S.colstat[0][1][et] = i < T ? 1.f / lu[i] : 0.f;
+        }
+        float cs = 0.f, cc = 0.f;                 // Kahan-summed column sum
+        for (int t = 0; t < ntiles; ++t) {
+            const int b = t & 1;
+            const int ib = jb + t;
+            // the next tile's statistics, stored after this tile
+            float nm = 0.f, nl = 0.f;
+            const int inext = (ib + 1) * kT + et;
+            if (t + 1 < ntiles && inext < T) {
+                nm = m2u[inext];
+                nl = lu[inext];
+            }
+            const bool ok = tc_wait(S, &S.acc_full[b], (uint32_t)(t >> 1) & 1u, err);
+            // agreed by all epilogue threads; also publishes last iteration's statistics
+            if (epilogue_any(!ok || aborted(S))) break;
+            tc_fence_after();
+            const bool edge = (t == 0) || ((ib + 1) * kT > T);
+            const float* ms = S.colstat[b][0];
+            const float* is = S.colstat[b][1];
+            float part = 0.f;
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+                float v[32];
+                tc_ld32(tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * kT + ch * 32), v);
+                const int i0 = ib * kT + ch * 32;
+                float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 m4 = *reinterpret_cast<const float4*>(ms + ch * 32 + e);
+                    const float4 i4 = *reinterpret_cast<const float4*>(is + ch * 32 + e);
+                    float w0 = exp2f(fmaf(v[e], c2, -m4.x)) * i4.x;
+                    float w1 = exp2f(fmaf(v[e + 1], c2, -m4.y)) * i4.y;
+                    float w2 = exp2f(fmaf(v[e + 2], c2, -m4.z)) * i4.z;
+                    float w3 = exp2f(fmaf(v[e + 3], c2, -m4.w)) * i4.w;
+                    if (edge) {
+                        if (i0 + e < j || i0 + e >= T) w0 = 0.f;
+                        if (i0 + e + 1 < j || i0 + e + 1 >= T) w1 = 0.f;
+                        if (i0 + e + 2 < j || i0 + e + 2 >= T) w2 = 0.f;
+                        if (i0 + e + 3 < j || i0 + e + 3 >= T) w3 = 0.f;
+                    }
+                    p0 += w0 + w2;
+                    p1 += w1 + w3;
+                }
+                part += p0 + p1;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.acc_empty[b]);
+            const float y = part - cc;
+            const float tsum = cs + y;
+            cc = (tsum - cs) - y;
+            cs = tsum;
+            // publish the next tile's statistics into the other buffer
+            if (t + 1 < ntiles) {
+                S.colstat[b ^ 1][0][et] = nm;
+                S.colstat[b ^ 1][1][et] = inext < T ? 1.f / nl : 0.f;
+            }
+        }
+        if (j < T && !aborted(S)) cout[(size_t)u * T + j] = (double)cs - (double)cc;
+    }
+    tc_teardown(S, warp, ntiles);
+}
+
+// ------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// [rows][128] bf16 row-major, boxes of 128 rows x 64 columns, 128-byte swizzle
+bool make_map(CUtensorMap* m, const void* base, long long rows)
+{
+    EncodeTiledFn enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)kT};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool prompt_tc_supported(const CacheView& c) { return c.dtype == 1 && c.D == kD; }
+
+cudaError_t launch_prompt_stats_tc(const CacheView& c, const PromptArgs& p, cudaStream_t st)
+{
+    CUtensorMap mq, mk;
+    const long long rows = (long long)c.U * p.T;
+    if (!make_map(&mq, p.Q, rows) || !make_map(&mk, p.K, rows)) return cudaErrorInvalidValue;
+    const size_t smem = sizeof(TcSmem) + 1024;
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(rowstats_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(colsum_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    const int nb = (p.T + kT - 1) / kT;
+    const unsigned grid = (unsigned)(c.U * nb);
+    rowstats_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, c.U, p.T, nb, c.qscale, p.m2, p.l, c.err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    colsum_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, c.U, p.T, nb, c.qscale, p.m2, p.l, p.c, c.err);
+    return cudaGetLastError();
+}
+
+}  // namespace h2o
