@@ -98,7 +98,7 @@ struct DecodeSmem {
     float qf[D];
     float kf[D];
     unsigned am[2][3][TL::NW];              // per-warp arg-min keys
-    unsigned long long ru[2][TL::NW];
+    unsigned ru[2][TL::NW];                  // per-warp HashEvict arg-max keys
     float M, invL, z_new, P_new;
     int victim;
     unsigned code_q, code_k;
@@ -559,6 +559,18 @@ __global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
     if (rank == 0 && tid < 2 * NV)
         newrow = tid < NV ? reinterpret_cast<const uint4*>(kg)[tid] : reinterpret_cast<const uint4*>(vg)[tid - NV];
 
+    // codes and positions of the slots this thread scans, fetched for all B
+    // slots before the occupancy is known
+    constexpr int PF = 4;
+    unsigned pcode[PF];
+    int ppos[PF];
+#pragma unroll
+    for (int i = 0; i < PF; ++i) {
+        const int s = tid + i * TL::NT;
+        pcode[i] = 0u;
+        ppos[i] = 0;
+        if (s < B) { pcode[i] = c.code[ub + s]; ppos[i] = c.pos[ub + s]; }
+    }
     float qp[D / 2];
     load_q_rotated<T, D>(qg, c.qscale, lane, qp);
     const int2 us = c.ustate[unit];
@@ -575,6 +587,7 @@ __global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
     if (warp < 2) {
         const float* x = warp == 0 ? S.qf : S.kf;
         float acc = 0.f;
+#pragma unroll 16
         for (int i = 0; i < D; ++i) acc = __fmaf_rn(x[i], __ldg(a.W + i * 32 + lane), acc);
         const unsigned code = __ballot_sync(kFull, acc > 0.f);
         if (lane == 0) {
@@ -583,32 +596,36 @@ __global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
     }
     __syncthreads();
 
-    // victim: every CTA of the cluster decides it redundantly from the codes
+    // victim: the largest Hamming distance, lowest slot on ties, packed as
+    // (distance << 20) | (2^20 - 1 - slot) so one unsigned max decides;
+    // every CTA of the cluster decides it redundantly
     if (full) {
         const unsigned cq = S.code_q;
-        unsigned long long bk = 0ull, bka = 0ull;    // (distance << 32) | ~slot, max wins
-        for (int s = tid; s < n; s += TL::NT) {
-            const unsigned long long key =
-                ((unsigned long long)__popc(cq ^ c.code[ub + s]) << 32) | (unsigned)(0xffffffffu - (unsigned)s);
-            if (c.pos[ub + s] <= p - c.r && key > bk) bk = key;
-            if (key > bka) bka = key;
-        }
+        unsigned bk = 0u, bka = 0u;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const unsigned long long o1 = __shfl_xor_sync(kFull, bk, off);
-            const unsigned long long o2 = __shfl_xor_sync(kFull, bka, off);
-            bk = o1 > bk ? o1 : bk;
-            bka = o2 > bka ? o2 : bka;
+        for (int i = 0; i < PF; ++i) {
+            const int s = tid + i * TL::NT;
+            if (s < n) {
+                const unsigned key = ((unsigned)__popc(cq ^ pcode[i]) << 20) | (0xFFFFFu - (unsigned)s);
+                if (ppos[i] <= p - c.r) bk = max(bk, key);
+                bka = max(bka, key);
+            }
         }
+        for (int s = tid + PF * TL::NT; s < n; s += TL::NT) {
+            const unsigned key = ((unsigned)__popc(cq ^ c.code[ub + s]) << 20) | (0xFFFFFu - (unsigned)s);
+            if (c.pos[ub + s] <= p - c.r) bk = max(bk, key);
+            bka = max(bka, key);
+        }
+        bk = __reduce_max_sync(kFull, bk);
+        bka = __reduce_max_sync(kFull, bka);
         if (lane == 0) { S.ru[0][warp] = bk; S.ru[1][warp] = bka; }
         __syncthreads();
-        if (tid == 0) {
-            for (int w = 1; w < TL::NW; ++w) {
-                bk = S.ru[0][w] > bk ? S.ru[0][w] : bk;
-                bka = S.ru[1][w] > bka ? S.ru[1][w] : bka;
-            }
-            const unsigned long long pick = bk ? bk : bka;
-            S.victim = (int)(0xffffffffu - (unsigned)(pick & 0xffffffffull));
+        if (warp == 0) {
+            unsigned k0 = lane < TL::NW ? S.ru[0][lane] : 0u;
+            unsigned k1 = lane < TL::NW ? S.ru[1][lane] : 0u;
+            k0 = __reduce_max_sync(kFull, k0);
+            k1 = __reduce_max_sync(kFull, k1);
+            if (lane == 0) S.victim = (int)(0xFFFFFu - ((k0 ? k0 : k1) & 0xFFFFFu));
         }
     } else if (tid == 0) {
         S.victim = n;

@@ -141,7 +141,9 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
     if (head_dim != 64 && head_dim != 128) return fail(H2O_ERR_ARG, "head_dim must be 64 or 128 (got %d)", head_dim);
     if (dtype != H2O_F32 && dtype != H2O_BF16) return fail(H2O_ERR_ARG, "dtype must be H2O_F32 or H2O_BF16");
     if (!(scale > 0.0) || !std::isfinite(scale)) return fail(H2O_ERR_ARG, "scale must be finite and > 0");
-    if ((long long)budget > (1LL << 20)) return fail(H2O_ERR_ARG, "budget too large");
+    if ((long long)budget >= (1LL << 20)) return fail(H2O_ERR_ARG, "budget must be below 2^20");
+    if (kind == kLSH && budget > 28 * 1024)
+        return fail(H2O_ERR_ARG, "HashEvict budget must be <= %d (its prompt replay keeps the slots in shared memory)", 28 * 1024);
     if (kind == kLSH && !W) return fail(H2O_ERR_ARG, "W is NULL");
     if (kind == kLSH && !aligned16(W)) return fail(H2O_ERR_ARG, "W must be 16-byte aligned");
 

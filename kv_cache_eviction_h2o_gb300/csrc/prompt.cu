@@ -383,88 +383,189 @@ __global__ void __launch_bounds__(256) gather_kernel(CacheView cv, PromptArgs pa
     }
 }
 
-// Sign codes of every prompt query and key: one warp per token, lane j owns
-// bit j; fp32 fused multiply-add chain in index order.
+// Sign codes of every prompt query and key.  Lane j of a warp keeps column j
+// of W in registers and owns bit j.  The warp hashes kCodeTok tokens per
+// pass (2 * kCodeTok independent fp32 fused multiply-add chains, each in
+// index order from 0); the next pass's rows are fetched into registers
+// while the current chains run, then staged in shared memory.
+constexpr int kCodeWarps = 8;
+constexpr int kCodeTok = 4;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(256) lsh_codes_kernel(const T* __restrict__ Q, const T* __restrict__ K,
-                                                       const float* __restrict__ W, long long ntok,
-                                                       uint32_t* __restrict__ cq, uint32_t* __restrict__ ck)
+__global__ void __launch_bounds__(32 * kCodeWarps) lsh_codes_kernel(const T* __restrict__ Q, const T* __restrict__ K,
+                                                                    const float* __restrict__ W, long long ntok,
+                                                                    uint32_t* __restrict__ cq,
+                                                                    uint32_t* __restrict__ ck)
 {
-    __shared__ float xs[8][2][D];
+    constexpr int EPL = D / 32;                       // elements of a row per lane
+    __shared__ __align__(16) float xs[kCodeWarps][2 * kCodeTok][D];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const long long tok = (long long)blockIdx.x * 8 + warp;
-    if (tok >= ntok) return;
-    for (int i = lane; i < D; i += 32) {
-        xs[warp][0][i] = Elem<T>::to_f(Q[tok * D + i]);
-        xs[warp][1][i] = Elem<T>::to_f(K[tok * D + i]);
+    float w[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) w[i] = __ldg(W + i * 32 + lane);
+    const long long step = (long long)gridDim.x * kCodeWarps * kCodeTok;
+    long long tok0 = ((long long)blockIdx.x * kCodeWarps + warp) * kCodeTok;
+    float pre[2 * kCodeTok][EPL];
+    auto fetch = [&](long long t0) {
+#pragma unroll
+        for (int k = 0; k < kCodeTok; ++k) {
+            const long long t = t0 + k;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                pre[2 * k][e] = t < ntok ? Elem<T>::to_f(Q[t * D + lane * EPL + e]) : 0.f;
+                pre[2 * k + 1][e] = t < ntok ? Elem<T>::to_f(K[t * D + lane * EPL + e]) : 0.f;
+            }
+        }
+    };
+    fetch(tok0);
+    for (; tok0 < ntok; tok0 += step) {
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 2 * kCodeTok; ++r)
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) xs[warp][r][lane * EPL + e] = pre[r][e];
+        __syncwarp();
+        fetch(tok0 + step);
+        float acc[2 * kCodeTok];
+#pragma unroll
+        for (int r = 0; r < 2 * kCodeTok; ++r) acc[r] = 0.f;
+#pragma unroll
+        for (int i = 0; i < D; i += 4) {
+#pragma unroll
+            for (int r = 0; r < 2 * kCodeTok; ++r) {
+                const float4 x4 = *reinterpret_cast<const float4*>(&xs[warp][r][i]);
+                acc[r] = __fmaf_rn(x4.x, w[i], acc[r]);
+                acc[r] = __fmaf_rn(x4.y, w[i + 1], acc[r]);
+                acc[r] = __fmaf_rn(x4.z, w[i + 2], acc[r]);
+                acc[r] = __fmaf_rn(x4.w, w[i + 3], acc[r]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kCodeTok; ++k) {
+            const unsigned bq = __ballot_sync(kFull, acc[2 * k] > 0.f);
+            const unsigned bk = __ballot_sync(kFull, acc[2 * k + 1] > 0.f);
+            if (lane == 0 && tok0 + k < ntok) { cq[tok0 + k] = bq; ck[tok0 + k] = bk; }
+        }
     }
-    __syncwarp();
-    float aq = 0.f, ak = 0.f;
-    for (int i = 0; i < D; ++i) {
-        const float w = __ldg(W + i * 32 + lane);
-        aq = __fmaf_rn(xs[warp][0][i], w, aq);
-        ak = __fmaf_rn(xs[warp][1][i], w, ak);
-    }
-    const unsigned bq = __ballot_sync(kFull, aq > 0.f);
-    const unsigned bk = __ballot_sync(kFull, ak > 0.f);
-    if (lane == 0) { cq[tok] = bq; ck[tok] = bk; }
 }
 
-// Replay the HashEvict replacement rule over the prompt, one CTA per unit:
-// the first B tokens fill the slots; token t >= B replaces the slot with the
-// largest Hamming distance to code(q_t) among slots with position <= t - r
-// (lowest slot on ties; every slot if none qualifies).
-constexpr int kReplayThreads = 256;
+// The same replay with each lane's slots (s = lane + 32 i) held in registers,
+// for budgets up to 32 * kRegSlots: no shared-memory round trip per step.
+constexpr int kRegSlots = 16;
 
-__global__ void __launch_bounds__(kReplayThreads) lsh_replay_kernel(CacheView cv, PromptArgs pa)
+__global__ void __launch_bounds__(64) lsh_replay_reg_kernel(CacheView cv, PromptArgs pa)
 {
-    extern __shared__ __align__(16) unsigned char sm[];
     const int B = cv.B, T_ = pa.T, r = cv.r;
-    uint32_t* code = reinterpret_cast<uint32_t*>(sm);
-    int* pos = reinterpret_cast<int*>(code + B);
-    __shared__ unsigned long long red[2][kReplayThreads / 32];
-    const int unit = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x & 31;
+    const int unit = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (unit >= cv.U) return;
     const uint32_t* cq = pa.cq + (size_t)unit * T_;
     const uint32_t* ck = pa.ck + (size_t)unit * T_;
     const int n0 = min(T_, B);
-    for (int s = tid; s < B; s += kReplayThreads) {
+    uint32_t code[kRegSlots];
+    int pos[kRegSlots];
+#pragma unroll
+    for (int i = 0; i < kRegSlots; ++i) {
+        const int s = lane + 32 * i;
+        pos[i] = s < n0 ? s : -1;
+        code[i] = s < n0 ? ck[s] : 0u;
+    }
+    uint32_t qb = 0u, kb = 0u;
+    for (int t = B; t < T_; ++t) {
+        const int o = (t - B) & 31;
+        if (o == 0) {
+            const int tt = t + lane;
+            qb = tt < T_ ? cq[tt] : 0u;
+            kb = tt < T_ ? ck[tt] : 0u;
+        }
+        const uint32_t q = __shfl_sync(kFull, qb, o);
+        const uint32_t knew = __shfl_sync(kFull, kb, o);
+        unsigned b0 = 0u, b1 = 0u;           // two chains over even / odd register slots
+#pragma unroll
+        for (int i = 0; i < kRegSlots; ++i) {
+            const int s = lane + 32 * i;
+            const unsigned key = ((unsigned)__popc(q ^ code[i]) << 20) | (0xFFFFFu - (unsigned)s);
+            if (s < B && pos[i] <= t - r) {
+                if (i & 1) b1 = max(b1, key); else b0 = max(b0, key);
+            }
+        }
+        unsigned best = __reduce_max_sync(kFull, max(b0, b1));
+        if (best == 0u) {                    // no slot outside the window: every slot competes
+#pragma unroll
+            for (int i = 0; i < kRegSlots; ++i) {
+                const int s = lane + 32 * i;
+                if (s < B) best = max(best, ((unsigned)__popc(q ^ code[i]) << 20) | (0xFFFFFu - (unsigned)s));
+            }
+            best = __reduce_max_sync(kFull, best);
+        }
+        const int v = (int)(0xFFFFFu - (best & 0xFFFFFu));
+        if ((v & 31) == lane) {
+            const int iv = v >> 5;
+#pragma unroll
+            for (int i = 0; i < kRegSlots; ++i)
+                if (i == iv) { code[i] = knew; pos[i] = t; }
+        }
+    }
+    const size_t ub = (size_t)unit * B;
+#pragma unroll
+    for (int i = 0; i < kRegSlots; ++i) {
+        const int s = lane + 32 * i;
+        if (s < B) cv.pos[ub + s] = pos[i];
+    }
+    if (lane == 0) cv.ustate[unit] = make_int2(n0, T_);
+}
+
+// Replay the HashEvict replacement rule over the prompt, one warp per unit:
+// the first B tokens fill the slots; token t >= B replaces the slot with the
+// largest Hamming distance to code(q_t) among slots with position <= t - r
+// (lowest slot on ties; every slot if none qualifies).  The slots' codes and
+// positions live in shared memory; the arg-max is one unsigned max of
+// (distance << 20) | (2^20 - 1 - slot).
+__global__ void lsh_replay_kernel(CacheView cv, PromptArgs pa, int warps_per_cta)
+{
+    extern __shared__ __align__(16) unsigned char sm[];
+    const int B = cv.B, T_ = pa.T, r = cv.r;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int unit = blockIdx.x * warps_per_cta + warp;
+    if (unit >= cv.U) return;
+    uint32_t* code = reinterpret_cast<uint32_t*>(sm) + (size_t)warp * 2 * B;
+    int* pos = reinterpret_cast<int*>(code + B);
+    const uint32_t* cq = pa.cq + (size_t)unit * T_;
+    const uint32_t* ck = pa.ck + (size_t)unit * T_;
+    const int n0 = min(T_, B);
+    for (int s = lane; s < B; s += 32) {
         pos[s] = s < n0 ? s : -1;
         code[s] = s < n0 ? ck[s] : 0u;
     }
-    __syncthreads();
+    __syncwarp();
+    uint32_t qb = 0u, kb = 0u;      // this lane's entry of the current 32-token batch
     for (int t = B; t < T_; ++t) {
-        const uint32_t q = cq[t];
-        unsigned long long bk = 0ull, bka = 0ull;
-        for (int s = tid; s < B; s += kReplayThreads) {
-            const unsigned long long key =
-                ((unsigned long long)__popc(q ^ code[s]) << 32) | (unsigned)(0xffffffffu - (unsigned)s);
-            if (pos[s] <= t - r && key > bk) bk = key;
-            if (key > bka) bka = key;
+        const int o = (t - B) & 31;
+        if (o == 0) {
+            const int tt = t + lane;
+            qb = tt < T_ ? cq[tt] : 0u;
+            kb = tt < T_ ? ck[tt] : 0u;
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const unsigned long long x1 = __shfl_xor_sync(kFull, bk, o);
-            const unsigned long long x2 = __shfl_xor_sync(kFull, bka, o);
-            bk = x1 > bk ? x1 : bk;
-            bka = x2 > bka ? x2 : bka;
+        const uint32_t q = __shfl_sync(kFull, qb, o);
+        const uint32_t knew = __shfl_sync(kFull, kb, o);
+        unsigned best = 0u, best_all = 0u;
+        for (int s = lane; s < B; s += 32) {
+            const unsigned key = ((unsigned)__popc(q ^ code[s]) << 20) | (0xFFFFFu - (unsigned)s);
+            if (pos[s] <= t - r) best = max(best, key);
+            best_all = max(best_all, key);
         }
-        if (lane == 0) { red[0][warp] = bk; red[1][warp] = bka; }
-        __syncthreads();
-        if (tid == 0) {
-            for (int w = 1; w < kReplayThreads / 32; ++w) {
-                bk = red[0][w] > bk ? red[0][w] : bk;
-                bka = red[1][w] > bka ? red[1][w] : bka;
-            }
-            const unsigned long long pick = bk ? bk : bka;
-            const int v = (int)(0xffffffffu - (unsigned)(pick & 0xffffffffull));
-            code[v] = ck[t];
+        best = __reduce_max_sync(kFull, best);
+        best_all = __reduce_max_sync(kFull, best_all);
+        const int v = (int)(0xFFFFFu - ((best ? best : best_all) & 0xFFFFFu));
+        if (lane == 0) {
+            code[v] = knew;
             pos[v] = t;
         }
-        __syncthreads();
+        __syncwarp();
     }
     const size_t ub = (size_t)unit * B;
-    for (int s = tid; s < B; s += kReplayThreads) cv.pos[ub + s] = pos[s];
-    if (tid == 0) cv.ustate[unit] = make_int2(n0, T_);
+    for (int s = lane; s < B; s += 32) cv.pos[ub + s] = pos[s];
+    if (lane == 0) cv.ustate[unit] = make_int2(n0, T_);
 }
 
 template <typename T, int D>
@@ -505,28 +606,52 @@ cudaError_t gather_t(const CacheView& c, const PromptArgs& p, bool with_codes, c
     return cudaGetLastError();
 }
 
+// warps per CTA of the replay: how many units' slot state fits the shared
+// memory chosen (H2O_REPLAY_WARPS overrides, for tuning)
+int replay_warps(int B)
+{
+    const char* e = getenv("H2O_REPLAY_WARPS");
+    int w = e ? atoi(e) : 2;
+    const int fit = (int)((48 * 1024) / ((size_t)B * 8));
+    if (w > fit) w = fit;
+    if (w < 1) w = 1;
+    return w;
+}
+
 template <typename T, int D>
 cudaError_t lsh_t(const CacheView& c, const PromptArgs& p, const float* W, cudaStream_t st)
 {
     const long long ntok = (long long)c.U * p.T;
-    lsh_codes_kernel<T, D><<<(unsigned)((ntok + 7) / 8), 256, 0, st>>>(
-        reinterpret_cast<const T*>(p.Q), reinterpret_cast<const T*>(p.K), W, ntok, p.cq, p.ck);
-    cudaError_t e = cudaGetLastError();
+    int sms = 0, dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const size_t smem = (size_t)c.B * 8;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    long long blocks = (ntok + kCodeWarps * kCodeTok - 1) / (kCodeWarps * kCodeTok);
+    if (blocks > 4LL * sms) blocks = 4LL * sms;
+    lsh_codes_kernel<T, D><<<(unsigned)blocks, 32 * kCodeWarps, 0, st>>>(
+        reinterpret_cast<const T*>(p.Q), reinterpret_cast<const T*>(p.K), W, ntok, p.cq, p.ck);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (c.B <= 32 * kRegSlots) {
+        lsh_replay_reg_kernel<<<(unsigned)((c.U + 1) / 2), 64, 0, st>>>(c, p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return gather_t<T, D>(c, p, true, st);
+    }
+    const size_t per_unit = (size_t)c.B * 8;
+    const int wpc = replay_warps(c.B);
+    const size_t smem = per_unit * wpc;
     if (smem > 48 * 1024) {
         static size_t configured[64] = {0};
-        int dev = 0;
-        e = cudaGetDevice(&dev);
-        if (e != cudaSuccess) return e;
-        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
         if (configured[dev] < smem) {
             e = cudaFuncSetAttribute(lsh_replay_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
             configured[dev] = smem;
         }
     }
-    lsh_replay_kernel<<<(unsigned)c.U, kReplayThreads, smem, st>>>(c, p);
+    lsh_replay_kernel<<<(unsigned)((c.U + wpc - 1) / wpc), 32 * wpc, smem, st>>>(c, p, wpc);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return gather_t<T, D>(c, p, true, st);
