@@ -143,7 +143,7 @@ def dist_setup(args):
 
 def decode_bytes(U, B, d, eb, lsh):
     """Algorithmic HBM bytes of one full-cache decode launch over U units:
-    per live slot K and V rows, plus score read+write (fp64) and position
+    per live slot K and V rows, plus score read+write (8-byte fp32 pair) and position
     read (H2O) or code and position read (HashEvict); per unit q, k, v in,
     fp32 out, one K/V row written, victim score/code and position written,
     unit state read and written; plus the projection matrix once."""
