@@ -181,3 +181,103 @@ def lsh_lockstep(dev, st, q, k, v, W, T, r, scale, check_every=1):
             assert (g["occ"] == st.occ).all()
             assert (g["K"] == st.K).all() and (g["V"] == st.V).all(), "LSH step %d: cache rows differ" % t
     return st
+
+
+def run_full_config(name, sample, check_every=64):
+    """The whole workload on the device (every unit, full prompt, every
+    decode step, automatic launch configuration as the benchmark uses), with
+    the units in `sample` drawn from the seeded numpy recipe and replayed by
+    the oracle in lockstep from the device's recorded outputs and victims.
+    Every unit is also checked against size-independent invariants."""
+    from kv_cache_eviction_h2o_gb300 import workloads as wl
+    w = wl.WORKLOADS[name]
+    U, T, d, B, S = w.units, w.prompt, w.head_dim, w.budget, w.steps
+    g = wl.generate_device(w)
+    gs = wl.generate(w, units=sample)
+    idx = torch.tensor(sample, device="cuda")
+    for key in ("Q", "K", "V"):
+        g[key][idx] = to_dev(gs[key], w.dtype)
+    for key in ("q", "k", "v"):
+        g[key][:, idx] = to_dev(gs[key], w.dtype)
+    stream = torch.cuda.current_stream()
+    dt = cdtype(w.dtype)
+    if w.lsh:
+        W = gs["W"]
+        Wd = torch.from_numpy(W).cuda()
+        h = L.lsh_init(B, w.recent, w.batch, w.heads, d, dt, w.scale, Wd, stream)
+        L.lsh_prefill(h, g["Q"], g["K"], g["V"], T)
+    else:
+        h = L.h2o_init(B, w.heavy, w.recent, w.batch, w.heads, d, dt, w.scale, stream)
+        L.h2o_prefill(h, g["Q"], g["K"], g["V"], T)
+    L.h2o_sync(h)
+    st0 = _state_all(h, U, B, d, w.dtype)
+    st0 = {k: (v[sample] if getattr(v, "ndim", 0) >= 1 else v) for k, v in st0.items()}
+    out = torch.empty((U, d), dtype=torch.float32, device="cuda")
+    vic = torch.empty((U,), dtype=torch.int32, device="cuda")
+    outs, vics = [], []
+    for t in range(S):
+        if w.lsh:
+            L.lsh_decode_step(h, g["q"][t], g["k"][t], g["v"][t], out, vic)
+        else:
+            L.h2o_decode_step(h, g["q"][t], g["k"][t], g["v"][t], out, vic)
+        outs.append(out[idx].cpu().numpy().astype(np.float64))
+        vics.append(vic[idx].cpu().numpy())
+    L.h2o_sync(h)
+    st_all = _state_all(h, U, B, d, w.dtype)
+    L.h2o_destroy(h)
+
+    # invariants on every unit: full occupancy, unique positions, the recent
+    # window present, next position T + S, finite non-negative scores
+    pF = T + S - 1
+    assert (st_all["occ"] == min(B, T + S)).all()
+    assert (st_all["npos"] == T + S).all()
+    pos = st_all["pos"]
+    srt = np.sort(pos, axis=1)
+    assert (np.diff(srt, axis=1) > 0).all(), "duplicate positions"
+    lo = max(0, pF - w.recent + 1)
+    if pF - lo + 1 > 0:
+        recent = np.arange(lo, pF + 1)
+        assert all(np.isin(recent, pos[u]).all() for u in range(U)), "recent window missing"
+    if not w.lsh:
+        assert np.isfinite(st_all["score"]).all() and (st_all["score"] >= 0).all()
+
+    # the sampled units against the oracle, step by step
+    sub = {k: v[sample] if k in ("K", "V", "score", "pos", "code", "occ", "npos") else v for k, v in st_all.items()}
+    near = 0
+    if w.lsh:
+        st = oracle.lsh_prefill(gs["Q"], gs["K"], gs["V"], W, B, w.recent)
+        for t in range(S):
+            o_ref, v_ref = oracle.lsh_decode_step(st, gs["q"][t], gs["k"][t], gs["v"][t], W, T + t, w.recent, w.scale)
+            assert (vics[t] == v_ref).all(), "step %d: LSH victims differ" % t
+            check_out(outs[t], o_ref, "step %d out" % t)
+        assert (sub["code"] == st.code).all()
+    else:
+        # prompt phase: the device's kept set against the oracle's (near ties counted)
+        st, c, near = align_prefill(st0, gs["Q"], gs["K"], gs["V"], B, w.heavy, w.recent, w.scale)
+        assert (st0["pos"] == st.pos).all(), "prompt positions differ"
+        check_scores(st0["score"], st.score, "prompt scores")
+        for t in range(S):
+            before = st.copy()
+            o_ref, v_ref, mg, _ = oracle.h2o_decode_step(st, gs["q"][t], gs["k"][t], gs["v"][t], T + t, w.recent,
+                                                         w.scale)
+            mism = vics[t] != v_ref
+            if mism.any():
+                assert (mg[mism] < NEAR_TIE).all(), "step %d: victims differ outside a near tie" % t
+                near += int(mism.sum())
+                st = before
+                forced = np.where(mism, vics[t], -1).astype(np.int32)
+                o_ref, _, _, _ = oracle.h2o_decode_step(st, gs["q"][t], gs["k"][t], gs["v"][t], T + t, w.recent,
+                                                        w.scale, forced)
+            check_out(outs[t], o_ref, "step %d out" % t)
+        check_scores(sub["score"], st.score, "final scores")
+    assert (sub["pos"] == st.pos).all(), "final positions differ"
+    assert (sub["K"] == st.K).all() and (sub["V"] == st.V).all(), "final cache rows differ"
+    return near
+
+
+def _state_all(h, U, B, d, dtype):
+    K = host_elems(dtype, (U, B, d)); V = host_elems(dtype, (U, B, d))
+    score = np.empty((U, B)); pos = np.empty((U, B), np.int32)
+    code = np.empty((U, B), np.uint32); occ = np.empty(U, np.int32); npos = np.empty(U, np.int32)
+    L.h2o_get_state(h, K, V, score, pos, code, occ, npos)
+    return dict(K=widen(K, dtype), V=widen(V, dtype), score=score, pos=pos, code=code, occ=occ, npos=npos)
