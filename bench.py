@@ -132,6 +132,18 @@ class Clocks:
                 "reasons": reasons, "samples": len(rows), "power_w_max": max(r[2] for r in rows)}
 
 
+def max_over_ranks(x, world, device="cpu"):
+    """Largest value of x over all ranks (the timing rule: the slowest rank
+    sets the job time); x itself when world == 1."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -352,10 +364,7 @@ def run_ours(args):
             prev = step_events[i][j]
     for h in h2o + lsh:
         L.h2o_sync(h)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, device="cuda")
 
     K = args.steps
     ms_per_step = elapsed_ms / K

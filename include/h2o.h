@@ -215,6 +215,17 @@ int h2o_prompt_scores_noalloc(const void* Q, const void* K, int batch, int heads
                               int head_dim, int dtype, double scale, double* c,
                               void* cuda_stream);
 
+/*
+ * h2o_selftest_wait_timeout -- enqueue one small kernel that waits, through
+ * the same bounded mbarrier wait every kernel of this library uses, on a
+ * barrier nothing ever completes.  The wait gives up after about a second
+ * of GPU clock, sets the handle's device error word and the kernel returns;
+ * the next h2o_sync then reports H2O_ERR_DEVICE_TIMEOUT and clears the word,
+ * and the handle stays usable.  The pages have no counterpart: this checks
+ * the failure-detection path without faulting or hanging the GPU.
+ */
+int h2o_selftest_wait_timeout(h2o_handle h);
+
 /* Thread-local description of the last failure in this thread ("" if none). */
 const char* h2o_last_error(void);
 

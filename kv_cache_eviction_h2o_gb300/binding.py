@@ -46,6 +46,7 @@ SIGNATURES = {
     "h2o_destroy": (None, [_vp]),
     "h2o_last_error": (ctypes.c_char_p, []),
     "h2o_prompt_scores_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _d, _vp, _vp]),
+    "h2o_selftest_wait_timeout": (_i, [_vp]),
 }
 
 H2O_NOALLOC_MAX_TOKENS = 1 << 20
@@ -164,6 +165,10 @@ def h2o_sync(h):
 
 def h2o_destroy(h):
     lib().h2o_destroy(h)
+
+
+def h2o_selftest_wait_timeout(h):
+    _check(lib().h2o_selftest_wait_timeout(h))
 
 
 def h2o_prompt_scores_noalloc(Q, K, batch, heads, T, head_dim, dtype, scale, c, stream=None):

@@ -222,6 +222,11 @@ __device__ __forceinline__ void grid_launch_dependents()
 
 // ------------------------------------------------------------- reductions
 
+__device__ __forceinline__ void prefetch_l1(const void* p)
+{
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // Cheapest proxy fence that makes mbarrier initialisation visible to the
 // bulk-copy engine of this CTA.
 __device__ __forceinline__ void fence_proxy_async_smem()

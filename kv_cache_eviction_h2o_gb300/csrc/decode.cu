@@ -549,6 +549,9 @@ __global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
     }
     // everything below reads memory the previous kernel in the stream may
     // have written (this unit's cache, or the inputs)
+    // the projection matrix is written once at lsh_init, never by the
+    // previous kernel: pull its 128 rows of 128 bytes into L1 now
+    if (tid < 128 && tid < D) prefetch_l1(a.W + tid * 32);
     grid_dependency_wait();
     grid_launch_dependents();
     if (lane == 0) prime_ring<T, D, TL>(S, Kc, Vc, f0, f1);
@@ -783,6 +786,27 @@ cudaError_t dispatch(const DecodeArgs& a, int split, cudaStream_t st)
 }
 
 }  // namespace
+
+namespace {
+
+// The bounded wait on a barrier that expects one arrival which never comes.
+__global__ void wait_selftest_kernel(int* err)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_proxy_async_smem();
+        if (!mbar_wait(&bar, 0)) atomicOr(err, kErrWaitTimeout);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(int* err, cudaStream_t st)
+{
+    wait_selftest_kernel<<<1, 32, 0, st>>>(err);
+    return cudaGetLastError();
+}
 
 int max_decode_split() { return kMaxSplit; }
 

@@ -462,6 +462,14 @@ int h2o_sync(h2o_handle h)
     return H2O_OK;
 }
 
+int h2o_selftest_wait_timeout(h2o_handle h)
+{
+    if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
+    cudaError_t e = launch_wait_selftest(h->err, h->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "h2o_selftest_wait_timeout launch");
+    return H2O_OK;
+}
+
 void h2o_destroy(h2o_handle h)
 {
     if (!h) return;

@@ -53,6 +53,10 @@ bool prompt_tc_supported(const CacheView& c);
 cudaError_t launch_prompt_stats_tc(const CacheView& c, const PromptArgs& p, cudaStream_t st);
 cudaError_t launch_select(const CacheView& c, const PromptArgs& p, cudaStream_t st);
 cudaError_t launch_gather(const CacheView& c, const PromptArgs& p, bool with_codes, cudaStream_t st);
+// One CTA whose bounded wait on a barrier nobody completes must run out and
+// set *err.
+cudaError_t launch_wait_selftest(int* err, cudaStream_t st);
+
 // Record a failure for h2o_last_error() and return `code`.
 int set_last_error(int code, const char* fmt, ...);
 
