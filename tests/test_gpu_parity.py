@@ -104,6 +104,7 @@ def test_hashevict_units(split):
     (40, 1, 1, 0),
     (70, 33, 17, 16),    # ragged groups and tiles
     (130, 129, 64, 65),
+    (1500, 1100, 600, 500),  # budget above one CTA's chunk: split across a cluster
 ])
 @pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
 def test_edge_cases_h2o(T, B, H, r, dtype, d):
@@ -117,7 +118,8 @@ def test_edge_cases_h2o(T, B, H, r, dtype, d):
     dev.close()
 
 
-@pytest.mark.parametrize("T,B,r", [(5, 8, 4), (1, 8, 4), (40, 8, 8), (40, 8, 0), (40, 1, 1), (70, 33, 16)])
+@pytest.mark.parametrize("T,B,r", [(5, 8, 4), (1, 8, 4), (40, 8, 8), (40, 8, 0), (40, 1, 1), (70, 33, 16),
+                                   (1500, 1100, 100)])
 @pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
 def test_edge_cases_lsh(T, B, r, dtype, d):
     U, S = 3, 12
