@@ -47,7 +47,7 @@ def parse():
     p.add_argument("--layers", type=int, default=8)
     p.add_argument("--decode-steps", type=int, default=None)
     p.add_argument("--split", type=int, default=0, help="CTAs per unit in decode (0 = automatic)")
-    p.add_argument("--oracle-units", type=int, default=32)
+    p.add_argument("--oracle-units", type=int, default=64)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     return p.parse_args()
@@ -459,23 +459,41 @@ def run_e2e(args, L, torch, layers, h2o, lsh, out_h, out_l, vic_h, vic_l, W, S, 
     h2d = sum(x.numel() * x.element_size() for hi in host_in for x in hi.values())
     d2h = sum(x.numel() * x.element_size() for ho in host_out for x in ho)
 
+    copy_stream = torch.cuda.Stream()
+    ready = [torch.cuda.Event() for _ in range(NL)]
+    # raw device addresses of every per-step argument, computed once (the
+    # binding takes plain integers; no tensor views per call)
+    def rows(x):
+        base, stride = x.data_ptr(), x.stride(0) * x.element_size()
+        return [base + t * stride for t in range(x.shape[0])]
+    ptr = [{k: rows(layers[li][k]) for k in ("q", "k", "v")} for li in range(NL)]
+    optr = [(rows(out_h[li]), rows(out_l[li]), rows(vic_h[li]), rows(vic_l[li])) for li in range(NL)]
+    hh = [int(h) for h in h2o]
+    hl = [int(h) for h in lsh]
+
     def step():
-        with torch.cuda.stream(stream):
+        # inputs stream in layer by layer on a copy stream; each layer's
+        # prompt phase waits only for its own inputs
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_stream(stream)
             for li in range(NL):
                 for k in ("Q", "K", "V", "q", "k", "v"):
                     layers[li][k].copy_(host_in[li][k], non_blocking=True)
+                ready[li].record(copy_stream)
+        with torch.cuda.stream(stream):
             for li in range(NL):
+                stream.wait_event(ready[li])
                 g = layers[li]
                 L.h2o_prefill(h2o[li], g["Q"], g["K"], g["V"], T)
                 L.lsh_prefill(lsh[li], g["Q"], g["K"], g["V"], T)
             for t in range(S):
                 for li in range(NL):
-                    g = layers[li]
-                    L.h2o_decode_step(h2o[li], g["q"][t], g["k"][t], g["v"][t], out_h[li][t], vic_h[li][t])
+                    pp, op = ptr[li], optr[li]
+                    L.h2o_decode_step(hh[li], pp["q"][t], pp["k"][t], pp["v"][t], op[0][t], op[2][t])
             for t in range(S):
                 for li in range(NL):
-                    g = layers[li]
-                    L.lsh_decode_step(lsh[li], g["q"][t], g["k"][t], g["v"][t], out_l[li][t], vic_l[li][t])
+                    pp, op = ptr[li], optr[li]
+                    L.lsh_decode_step(hl[li], pp["q"][t], pp["k"][t], pp["v"][t], op[1][t], op[3][t])
             for li in range(NL):
                 ho = host_out[li]
                 ho[0].copy_(out_h[li], non_blocking=True)
