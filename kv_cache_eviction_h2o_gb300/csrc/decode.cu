@@ -102,6 +102,7 @@ struct DecodeSmem {
     float M, invL, z_new, P_new;
     int victim;
     unsigned code_q, code_k;
+    float hacc[2][32];                      // HashEvict projection partial sums
 };
 
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
@@ -135,18 +136,41 @@ __device__ __forceinline__ ArgMin warp_argmin(const ArgMin& a)
     return ArgMin{mh, ml, ms};
 }
 
-// This lane's half of q (scaled to base-2 logits) in its rotated chunk order.
+// This lane's half of q as raw 16-byte chunks in its rotated chunk order.
+// Loading and widening are separate so that nothing consumes the load
+// before the ring's bulk copies are issued.
 template <typename T, int D>
-__device__ __forceinline__ void load_q_rotated(const T* q, float scale, int lane,
-                                               float (&qp)[D / 2])
+struct QRaw {
+    uint4 w[Rows<T, D>::HCH];
+};
+
+template <typename T, int D>
+__device__ __forceinline__ void load_q_raw(const T* q, int lane, QRaw<T, D>& raw)
 {
     using R = Rows<T, D>;
     const int r = lane & 15, h = lane >> 4;
 #pragma unroll
-    for (int c = 0; c < R::HCH; ++c) {
-        load_vec<T, R::VE>(q + h * R::HALF + (c ^ (r & R::XM)) * R::VE, &qp[c * R::VE]);
+    for (int c = 0; c < R::HCH; ++c)
+        raw.w[c] = *reinterpret_cast<const uint4*>(q + h * R::HALF + (c ^ (r & R::XM)) * R::VE);
+}
+
+// Widen the raw chunks to fp32 and scale them to base-2 logits.
+template <typename T, int D>
+__device__ __forceinline__ void widen_q(const QRaw<T, D>& raw, float scale, float (&qp)[D / 2])
+{
+    using R = Rows<T, D>;
 #pragma unroll
-        for (int e = 0; e < R::VE; ++e) qp[c * R::VE + e] *= scale;
+    for (int c = 0; c < R::HCH; ++c) {
+        const uint32_t u[4] = {raw.w[c].x, raw.w[c].y, raw.w[c].z, raw.w[c].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if constexpr (sizeof(T) == 2) {
+                qp[c * R::VE + 2 * k] = __uint_as_float(u[k] << 16) * scale;
+                qp[c * R::VE + 2 * k + 1] = __uint_as_float(u[k] & 0xffff0000u) * scale;
+            } else {
+                qp[c * R::VE + k] = __uint_as_float(u[k]) * scale;
+            }
+        }
     }
 }
 
@@ -367,31 +391,34 @@ __global__ void __launch_bounds__(TL::NT) h2o_decode_kernel(const DecodeArgs a)
     // have written (this unit's cache, or the inputs)
     grid_dependency_wait();
     grid_launch_dependents();
-    if (lane == 0) prime_ring<T, D, TL>(S, Kc, Vc, f0, f1);
+    // The small, latency-critical loads go out before the bulk copies: issued
+    // after them they would queue behind every CTA's ring in HBM.
     const T* kg = reinterpret_cast<const T*>(a.k) + (size_t)unit * D;
     const T* vg = reinterpret_cast<const T*>(a.v) + (size_t)unit * D;
     // the new token's row, written into the victim slot at the end
     uint4 newrow = make_uint4(0u, 0u, 0u, 0u);
     if (rank == 0 && tid < 2 * NV)
         newrow = tid < NV ? reinterpret_cast<const uint4*>(kg)[tid] : reinterpret_cast<const uint4*>(vg)[tid - NV];
-
-    float qp[D / 2];
-    load_q_rotated<T, D>(reinterpret_cast<const T*>(a.q) + (size_t)unit * D, c.qscale, lane, qp);
+    QRaw<T, D> qraw;
+    load_q_raw<T, D>(reinterpret_cast<const T*>(a.q) + (size_t)unit * D, lane, qraw);
     const int2 us = c.ustate[unit];
-    const int n = us.x, p = us.y;
-    const bool full = (n >= B);
-    const int c0 = f0, c1 = min(n, f1);     // live slots of this CTA
-
-    // scores and positions of this thread's slots, consumed after the merge
+    // scores and positions of this thread's fetched slots, consumed after the merge
     float2 sc_old[TL::SPT];
     int ps[TL::SPT];
 #pragma unroll
     for (int i = 0; i < TL::SPT; ++i) {
-        const int s = c0 + tid + i * TL::NT;
+        const int s = f0 + tid + i * TL::NT;
         sc_old[i] = make_float2(0.f, 0.f);
         ps[i] = 0;
-        if (s < c1) { sc_old[i] = c.score[ub + s]; ps[i] = c.pos[ub + s]; }
+        if (s < f1) { sc_old[i] = c.score[ub + s]; ps[i] = c.pos[ub + s]; }
     }
+    if (lane == 0) prime_ring<T, D, TL>(S, Kc, Vc, f0, f1);
+    float qp[D / 2];
+    widen_q<T, D>(qraw, c.qscale, qp);
+
+    const int n = us.x, p = us.y;
+    const bool full = (n >= B);
+    const int c0 = f0, c1 = min(n, f1);     // live slots of this CTA
 
     float m_run = -INFINITY, l_run = 0.f, o[EPL];
 #pragma unroll
@@ -547,14 +574,21 @@ __global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
         for (int b = 0; b < TL::NBUF; ++b) mbar_init(&S.bar[warp][b], 1);
         if (C > 1) fence_mbar_init(); else fence_proxy_async_smem();
     }
+    // The projection matrix is written once when the cache is created, never
+    // by a previous kernel in the stream, so it is read before the wait:
+    // warp w holds rows [w*RPW, w*RPW + RPW) of W, lane j the column of bit j.
+    constexpr int RPW = (D + TL::NW - 1) / TL::NW;
+    float wreg[RPW];
+#pragma unroll
+    for (int t = 0; t < RPW; ++t) {
+        const int row = warp * RPW + t;
+        wreg[t] = row < D ? __ldg(a.W + row * 32 + lane) : 0.f;
+    }
     // everything below reads memory the previous kernel in the stream may
     // have written (this unit's cache, or the inputs)
-    // the projection matrix is written once at lsh_init, never by the
-    // previous kernel: pull its 128 rows of 128 bytes into L1 now
-    if (tid < 128 && tid < D) prefetch_l1(a.W + tid * 32);
     grid_dependency_wait();
     grid_launch_dependents();
-    if (lane == 0) prime_ring<T, D, TL>(S, Kc, Vc, f0, f1);
+    // every small load goes out before the bulk copies (see the H2O kernel)
     const T* qg = reinterpret_cast<const T*>(a.q) + (size_t)unit * D;
     const T* kg = reinterpret_cast<const T*>(a.k) + (size_t)unit * D;
     const T* vg = reinterpret_cast<const T*>(a.v) + (size_t)unit * D;
@@ -574,30 +608,50 @@ __global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
         ppos[i] = 0;
         if (s < B) { pcode[i] = c.code[ub + s]; ppos[i] = c.pos[ub + s]; }
     }
-    float qp[D / 2];
-    load_q_rotated<T, D>(qg, c.qscale, lane, qp);
+    QRaw<T, D> qraw;
+    load_q_raw<T, D>(qg, lane, qraw);
     const int2 us = c.ustate[unit];
+    T xq = T(), xk = T();
+    if (tid < D) {
+        xq = qg[tid];
+        xk = kg[tid];
+    }
+    if (lane == 0) prime_ring<T, D, TL>(S, Kc, Vc, f0, f1);
     const int n = us.x, p = us.y;
     const bool full = (n >= B);
 
     if (tid < D) {
-        S.qf[tid] = Elem<T>::to_f(qg[tid]);
-        S.kf[tid] = Elem<T>::to_f(kg[tid]);
+        S.qf[tid] = Elem<T>::to_f(xq);
+        S.kf[tid] = Elem<T>::to_f(xk);
     }
     __syncthreads();
-    // sign codes: lane j of warp 0 (query) / warp 1 (key) owns bit j; the
-    // projection is an fp32 fused multiply-add chain in index order
-    if (warp < 2) {
-        const float* x = warp == 0 ? S.qf : S.kf;
-        float acc = 0.f;
-#pragma unroll 16
-        for (int i = 0; i < D; ++i) acc = __fmaf_rn(x[i], __ldg(a.W + i * 32 + lane), acc);
-        const unsigned code = __ballot_sync(kFull, acc > 0.f);
-        if (lane == 0) {
-            if (warp == 0) S.code_q = code; else S.code_k = code;
+    // sign codes: bit j is the sign of an fp32 fused multiply-add chain over
+    // x[i] * W[i][j] in index order; the chain runs through the warps in turn
+    // (lane j carries bit j's partial sums for query and key in S.hacc)
+#pragma unroll 1
+    for (int w = 0; w < TL::NW; ++w) {
+        if (warp == w) {
+            float aq = w == 0 ? 0.f : S.hacc[0][lane];
+            float ak = w == 0 ? 0.f : S.hacc[1][lane];
+#pragma unroll
+            for (int t = 0; t < RPW; ++t) {
+                const int row = w * RPW + t;
+                if (row < D) {
+                    aq = __fmaf_rn(S.qf[row], wreg[t], aq);
+                    ak = __fmaf_rn(S.kf[row], wreg[t], ak);
+                }
+            }
+            if (w + 1 < TL::NW) {
+                S.hacc[0][lane] = aq;
+                S.hacc[1][lane] = ak;
+            } else {
+                const unsigned cq = __ballot_sync(kFull, aq > 0.f);
+                const unsigned ck = __ballot_sync(kFull, ak > 0.f);
+                if (lane == 0) { S.code_q = cq; S.code_k = ck; }
+            }
         }
+        __syncthreads();
     }
-    __syncthreads();
 
     // victim: the largest Hamming distance, lowest slot on ties, packed as
     // (distance << 20) | (2^20 - 1 - slot) so one unsigned max decides;
@@ -635,6 +689,8 @@ __global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
     }
     __syncthreads();
     const int victim = S.victim;
+    float qp[D / 2];
+    widen_q<T, D>(qraw, c.qscale, qp);
 
     float m_run = -INFINITY, l_run = 0.f, o[EPL];
 #pragma unroll
