@@ -391,8 +391,8 @@ __global__ void __launch_bounds__(TL::NT) h2o_decode_kernel(const DecodeArgs a)
     // have written (this unit's cache, or the inputs)
     grid_dependency_wait();
     grid_launch_dependents();
-    // The small, latency-critical loads go out before the bulk copies: issued
-    // after them they would queue behind every CTA's ring in HBM.
+    // the attention starts on the ring, so its bulk copies go out first
+    if (lane == 0) prime_ring<T, D, TL>(S, Kc, Vc, f0, f1);
     const T* kg = reinterpret_cast<const T*>(a.k) + (size_t)unit * D;
     const T* vg = reinterpret_cast<const T*>(a.v) + (size_t)unit * D;
     // the new token's row, written into the victim slot at the end
@@ -412,7 +412,6 @@ __global__ void __launch_bounds__(TL::NT) h2o_decode_kernel(const DecodeArgs a)
         ps[i] = 0;
         if (s < f1) { sc_old[i] = c.score[ub + s]; ps[i] = c.pos[ub + s]; }
     }
-    if (lane == 0) prime_ring<T, D, TL>(S, Kc, Vc, f0, f1);
     float qp[D / 2];
     widen_q<T, D>(qraw, c.qscale, qp);
 
@@ -588,7 +587,8 @@ __global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
     // have written (this unit's cache, or the inputs)
     grid_dependency_wait();
     grid_launch_dependents();
-    // every small load goes out before the bulk copies (see the H2O kernel)
+    // the victim (which gates the attention) depends only on small loads:
+    // they go out before the bulk copies, which would otherwise delay them
     const T* qg = reinterpret_cast<const T*>(a.q) + (size_t)unit * D;
     const T* kg = reinterpret_cast<const T*>(a.k) + (size_t)unit * D;
     const T* vg = reinterpret_cast<const T*>(a.v) + (size_t)unit * D;
@@ -627,7 +627,16 @@ __global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
     __syncthreads();
     // sign codes: bit j is the sign of an fp32 fused multiply-add chain over
     // x[i] * W[i][j] in index order; the chain runs through the warps in turn
-    // (lane j carries bit j's partial sums for query and key in S.hacc)
+    // (lane j carries bit j's partial sums for query and key in S.hacc).
+    // Every warp first pulls its rows of q and k into registers, so a turn
+    // is a chain of register FMAs only.
+    float xqr[RPW], xkr[RPW];
+#pragma unroll
+    for (int t = 0; t < RPW; ++t) {
+        const int row = warp * RPW + t;
+        xqr[t] = row < D ? S.qf[row] : 0.f;
+        xkr[t] = row < D ? S.kf[row] : 0.f;
+    }
 #pragma unroll 1
     for (int w = 0; w < TL::NW; ++w) {
         if (warp == w) {
@@ -635,10 +644,9 @@ __global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
             float ak = w == 0 ? 0.f : S.hacc[1][lane];
 #pragma unroll
             for (int t = 0; t < RPW; ++t) {
-                const int row = w * RPW + t;
-                if (row < D) {
-                    aq = __fmaf_rn(S.qf[row], wreg[t], aq);
-                    ak = __fmaf_rn(S.kf[row], wreg[t], ak);
+                if (w * RPW + t < D) {
+                    aq = __fmaf_rn(xqr[t], wreg[t], aq);
+                    ak = __fmaf_rn(xkr[t], wreg[t], ak);
                 }
             }
             if (w + 1 < TL::NW) {
