@@ -229,6 +229,66 @@ __device__ __forceinline__ void prefetch_l1(const void* p)
 
 // Cheapest proxy fence that makes mbarrier initialisation visible to the
 // bulk-copy engine of this CTA.
+// Named CTA barriers (ids 1..15; id 0 is __syncthreads).  Memory
+// accesses made before the arrive are visible to the threads that pass the
+// sync.  The id is an immediate in the instruction (a register id makes the
+// compiler reserve all sixteen barriers).
+template <int ID>
+__device__ __forceinline__ void bar_sync_imm(int nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(nthreads) : "memory");
+}
+
+template <int ID>
+__device__ __forceinline__ void bar_arrive_imm(int nthreads)
+{
+    asm volatile("bar.arrive %0, %1;" ::"n"(ID), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads)
+{
+    switch (id) {
+    case 1: bar_sync_imm<1>(nthreads); break;
+    case 2: bar_sync_imm<2>(nthreads); break;
+    case 3: bar_sync_imm<3>(nthreads); break;
+    case 4: bar_sync_imm<4>(nthreads); break;
+    case 5: bar_sync_imm<5>(nthreads); break;
+    case 6: bar_sync_imm<6>(nthreads); break;
+    case 7: bar_sync_imm<7>(nthreads); break;
+    case 8: bar_sync_imm<8>(nthreads); break;
+    case 9: bar_sync_imm<9>(nthreads); break;
+    case 10: bar_sync_imm<10>(nthreads); break;
+    case 11: bar_sync_imm<11>(nthreads); break;
+    case 12: bar_sync_imm<12>(nthreads); break;
+    case 13: bar_sync_imm<13>(nthreads); break;
+    case 14: bar_sync_imm<14>(nthreads); break;
+    case 15: bar_sync_imm<15>(nthreads); break;
+    default: break;
+    }
+}
+
+__device__ __forceinline__ void named_barrier_arrive(int id, int nthreads)
+{
+    switch (id) {
+    case 1: bar_arrive_imm<1>(nthreads); break;
+    case 2: bar_arrive_imm<2>(nthreads); break;
+    case 3: bar_arrive_imm<3>(nthreads); break;
+    case 4: bar_arrive_imm<4>(nthreads); break;
+    case 5: bar_arrive_imm<5>(nthreads); break;
+    case 6: bar_arrive_imm<6>(nthreads); break;
+    case 7: bar_arrive_imm<7>(nthreads); break;
+    case 8: bar_arrive_imm<8>(nthreads); break;
+    case 9: bar_arrive_imm<9>(nthreads); break;
+    case 10: bar_arrive_imm<10>(nthreads); break;
+    case 11: bar_arrive_imm<11>(nthreads); break;
+    case 12: bar_arrive_imm<12>(nthreads); break;
+    case 13: bar_arrive_imm<13>(nthreads); break;
+    case 14: bar_arrive_imm<14>(nthreads); break;
+    case 15: bar_arrive_imm<15>(nthreads); break;
+    default: break;
+    }
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

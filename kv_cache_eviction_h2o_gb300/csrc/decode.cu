@@ -45,6 +45,7 @@ template <int NW_, int NBUF_>
 struct Tile {
     static constexpr int NW = NW_, NT = 32 * NW_, NBUF = NBUF_;
     static constexpr int SPT = kMaxChunk / NT;            // slots per thread in the score pass
+    static constexpr int MINB = NT <= 192 ? 2 : 1;        // CTAs per SM the registers must allow
 };
 
 // Row geometry.  For the logits a stage's 16 rows are split between the two
@@ -177,30 +178,76 @@ __device__ __forceinline__ void widen_q(const QRaw<T, D>& raw, float scale, floa
 // Half-row dot product of row `row` (global or shared, elements of type T or
 // float) with the rotated q half; every lane returns the full dot of its
 // row after one exchange between the half-warps.
+// Raw 32-bit words of a vector of E elements of T, and their fp32 values.
+template <int BYTES> struct RawT;
+template <> struct RawT<4> { using type = uint32_t; };
+template <> struct RawT<8> { using type = uint2; };
+template <> struct RawT<16> { using type = uint4; };
+
+__device__ __forceinline__ void raw_words(uint32_t w, uint32_t* u) { u[0] = w; }
+__device__ __forceinline__ void raw_words(uint2 w, uint32_t* u) { u[0] = w.x; u[1] = w.y; }
+__device__ __forceinline__ void raw_words(uint4 w, uint32_t* u) { u[0] = w.x; u[1] = w.y; u[2] = w.z; u[3] = w.w; }
+
+template <typename T, int E>
+__device__ __forceinline__ void widen_raw(const typename RawT<E * sizeof(T)>::type& w, float* out)
+{
+    constexpr int NWD = E * (int)sizeof(T) / 4;
+    uint32_t u[NWD];
+    raw_words(w, u);
+#pragma unroll
+    for (int k = 0; k < NWD; ++k) {
+        if constexpr (sizeof(T) == 2) {
+            out[2 * k] = __uint_as_float(u[k] << 16);
+            out[2 * k + 1] = __uint_as_float(u[k] & 0xffff0000u);
+        } else {
+            out[k] = __uint_as_float(u[k]);
+        }
+    }
+}
+
+// Half-row dot product of row `row` (global or shared, elements of type T or
+// float) with the rotated q half; every lane returns the full dot of its
+// row after one exchange between the half-warps.  For rows of T all chunks
+// are loaded before the first multiply, and four accumulator pairs keep the
+// dependent chains short.
 template <typename T, int D, typename E>
 __device__ __forceinline__ float row_dot(const E* row, const float (&qp)[D / 2], int lane)
 {
     using R = Rows<T, D>;
     const int r = lane & 15, h = lane >> 4;
     const E* half = row + h * R::HALF;
-    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                     make_float2(0.f, 0.f)};
+    if constexpr (sizeof(E) == sizeof(float) && sizeof(T) == 2) {
+        // a float copy of a bf16 row (kept in shared memory)
 #pragma unroll
-    for (int c = 0; c < R::HCH; ++c) {
-        float kf[R::VE];
-        if constexpr (sizeof(E) == sizeof(float) && sizeof(T) == 2) {
-            // a float copy of a bf16 row (kept in shared memory)
+        for (int c = 0; c < R::HCH; ++c) {
+            float kf[R::VE];
 #pragma unroll
             for (int e = 0; e < R::VE; ++e) kf[e] = half[(c ^ (r & R::XM)) * R::VE + e];
-        } else {
-            load_vec<T, R::VE>(reinterpret_cast<const T*>(half) + (c ^ (r & R::XM)) * R::VE, kf);
-        }
 #pragma unroll
-        for (int e = 0; e < R::VE; e += 4) {
-            acc0 = fma2(make_float2(qp[c * R::VE + e], qp[c * R::VE + e + 1]), make_float2(kf[e], kf[e + 1]), acc0);
-            acc1 = fma2(make_float2(qp[c * R::VE + e + 2], qp[c * R::VE + e + 3]), make_float2(kf[e + 2], kf[e + 3]), acc1);
+            for (int e = 0; e < R::VE; e += 2)
+                acc[(e / 2) & 3] = fma2(make_float2(qp[c * R::VE + e], qp[c * R::VE + e + 1]),
+                                        make_float2(kf[e], kf[e + 1]), acc[(e / 2) & 3]);
+        }
+    } else {
+        uint4 raw[R::HCH];
+#pragma unroll
+        for (int c = 0; c < R::HCH; ++c)
+            raw[c] = *reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(half) + (c ^ (r & R::XM)) * R::VE);
+#pragma unroll
+        for (int c = 0; c < R::HCH; ++c) {
+            float kf[R::VE];
+            widen_raw<T, R::VE>(raw[c], kf);
+#pragma unroll
+            for (int e = 0; e < R::VE; e += 2) {
+                const int a = (c * (R::VE / 2) + e / 2) & 3;
+                acc[a] = fma2(make_float2(qp[c * R::VE + e], qp[c * R::VE + e + 1]), make_float2(kf[e], kf[e + 1]),
+                              acc[a]);
+            }
         }
     }
-    const float zh = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+    const float zh = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
     return zh + __shfl_xor_sync(kFull, zh, 16);
 }
 
@@ -261,17 +308,43 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL>& S, const T* K
                 const float4 e4 = *reinterpret_cast<const float4*>(&S.e[warp][j]);
                 ev[j] = e4.x; ev[j + 1] = e4.y; ev[j + 2] = e4.z; ev[j + 3] = e4.w;
             }
+            using RV = typename RawT<EPL * sizeof(T)>::type;
+            if (gl == kStage) {
+                // a full stage: each half's value fragments are loaded before
+                // the first multiply (rows past gl of a partial stage may hold
+                // stale data and are never read)
 #pragma unroll
-            for (int j = 0; j < kStage; ++j) {
-                if (j < gl) {
-                    float vr[EPL];
-                    load_vec<T, EPL>(vst + j * D + lane * EPL, vr);
-                    const float2 pj = make_float2(ev[j], ev[j]);
+                for (int j0 = 0; j0 < kStage; j0 += kStage / 2) {
+                    RV vraw[kStage / 2];
 #pragma unroll
-                    for (int e = 0; e < EPL; e += 2) {
-                        const float2 acc = fma2(pj, make_float2(vr[e], vr[e + 1]), make_float2(o[e], o[e + 1]));
-                        o[e] = acc.x;
-                        o[e + 1] = acc.y;
+                    for (int j = 0; j < kStage / 2; ++j)
+                        vraw[j] = *reinterpret_cast<const RV*>(vst + (j0 + j) * D + lane * EPL);
+#pragma unroll
+                    for (int j = 0; j < kStage / 2; ++j) {
+                        float vr[EPL];
+                        widen_raw<T, EPL>(vraw[j], vr);
+                        const float2 pj = make_float2(ev[j0 + j], ev[j0 + j]);
+#pragma unroll
+                        for (int e = 0; e < EPL; e += 2) {
+                            const float2 acc = fma2(pj, make_float2(vr[e], vr[e + 1]), make_float2(o[e], o[e + 1]));
+                            o[e] = acc.x;
+                            o[e + 1] = acc.y;
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < kStage; ++j) {
+                    if (j < gl) {
+                        float vr[EPL];
+                        load_vec<T, EPL>(vst + j * D + lane * EPL, vr);
+                        const float2 pj = make_float2(ev[j], ev[j]);
+#pragma unroll
+                        for (int e = 0; e < EPL; e += 2) {
+                            const float2 acc = fma2(pj, make_float2(vr[e], vr[e + 1]), make_float2(o[e], o[e + 1]));
+                            o[e] = acc.x;
+                            o[e + 1] = acc.y;
+                        }
                     }
                 }
             }
@@ -291,16 +364,18 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL>& S, const T* K
     }
 }
 
-// Kick off the first NBUF stages of each warp (called by lane 0 of every warp
-// after its barriers are initialised).
+// Kick off ring buffers [b_lo, b_hi) of each warp -- by default all NBUF --
+// with their first stages (called by lane 0 of every warp after its barriers
+// are initialised).
 template <typename T, int D, class TL>
 __device__ __forceinline__ void prime_ring(DecodeSmem<T, D, TL>& S, const T* Kc, const T* Vc,
-                                           int c0, int c1)
+                                           int c0, int c1, int b_lo = 0, int b_hi = TL::NBUF)
 {
     const int warp = threadIdx.x >> 5;
     const int nst = (c1 - c0 + kStage - 1) / kStage;
 #pragma unroll
     for (int b = 0; b < TL::NBUF; ++b) {
+        if (b < b_lo || b >= b_hi) continue;
         const int g = warp + TL::NW * b;
         if (g < nst) {
             const int s = c0 + g * kStage;
@@ -364,7 +439,7 @@ __device__ __forceinline__ void fetch_range(int B, int C, int rank, int& f0, int
 // ------------------------------------------------------------------ H2O
 
 template <typename T, int D, class TL>
-__global__ void __launch_bounds__(TL::NT) h2o_decode_kernel(const DecodeArgs a)
+__global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const DecodeArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     auto& S = *reinterpret_cast<DecodeSmem<T, D, TL>*>(smem_raw);
@@ -387,31 +462,48 @@ __global__ void __launch_bounds__(TL::NT) h2o_decode_kernel(const DecodeArgs a)
         for (int b = 0; b < TL::NBUF; ++b) mbar_init(&S.bar[warp][b], 1);
         if (C > 1) fence_mbar_init(); else fence_proxy_async_smem();
     }
-    // everything below reads memory the previous kernel in the stream may
-    // have written (this unit's cache, or the inputs)
+    // This unit's cache: the ring's first stages (the attention starts on
+    // them, so their bulk copies go out first), the occupancy, and the scores
+    // and positions of this thread's fetched slots (consumed after the merge).
+    // When the previous kernel in the stream cannot have written the cache
+    // this happens before the dependency wait, overlapping that kernel's end.
+    int2 us = make_int2(0, 0);
+    float2 sc_old[TL::SPT];
+    int ps[TL::SPT];
+    auto read_cache = [&]() {
+        us = c.ustate[unit];
+#pragma unroll
+        for (int i = 0; i < TL::SPT; ++i) {
+            const int s = f0 + tid + i * TL::NT;
+            sc_old[i] = make_float2(0.f, 0.f);
+            ps[i] = 0;
+            if (s < f1) { sc_old[i] = c.score[ub + s]; ps[i] = c.pos[ub + s]; }
+        }
+    };
+    // Early, only each warp's first buffer is filled before the wait: the
+    // query row, requested right after the wait, then queues behind less
+    // traffic, and the remaining buffers keep HBM busy while it is in flight.
+    if (a.early) {
+        if (lane == 0) prime_ring<T, D, TL>(S, Kc, Vc, f0, f1, 0, 1);
+        read_cache();
+    }
+    // everything below may read memory the previous kernel in the stream
+    // has written (the inputs, and the cache unless read above)
     grid_dependency_wait();
     grid_launch_dependents();
-    // the attention starts on the ring, so its bulk copies go out first
-    if (lane == 0) prime_ring<T, D, TL>(S, Kc, Vc, f0, f1);
+    if (!a.early) {
+        if (lane == 0) prime_ring<T, D, TL>(S, Kc, Vc, f0, f1);
+        read_cache();
+    }
+    QRaw<T, D> qraw;
+    load_q_raw<T, D>(reinterpret_cast<const T*>(a.q) + (size_t)unit * D, lane, qraw);
+    if (a.early && lane == 0) prime_ring<T, D, TL>(S, Kc, Vc, f0, f1, 1, TL::NBUF);
     const T* kg = reinterpret_cast<const T*>(a.k) + (size_t)unit * D;
     const T* vg = reinterpret_cast<const T*>(a.v) + (size_t)unit * D;
     // the new token's row, written into the victim slot at the end
     uint4 newrow = make_uint4(0u, 0u, 0u, 0u);
     if (rank == 0 && tid < 2 * NV)
         newrow = tid < NV ? reinterpret_cast<const uint4*>(kg)[tid] : reinterpret_cast<const uint4*>(vg)[tid - NV];
-    QRaw<T, D> qraw;
-    load_q_raw<T, D>(reinterpret_cast<const T*>(a.q) + (size_t)unit * D, lane, qraw);
-    const int2 us = c.ustate[unit];
-    // scores and positions of this thread's fetched slots, consumed after the merge
-    float2 sc_old[TL::SPT];
-    int ps[TL::SPT];
-#pragma unroll
-    for (int i = 0; i < TL::SPT; ++i) {
-        const int s = f0 + tid + i * TL::NT;
-        sc_old[i] = make_float2(0.f, 0.f);
-        ps[i] = 0;
-        if (s < f1) { sc_old[i] = c.score[ub + s]; ps[i] = c.pos[ub + s]; }
-    }
     float qp[D / 2];
     widen_q<T, D>(qraw, c.qscale, qp);
 
@@ -550,7 +642,7 @@ __global__ void __launch_bounds__(TL::NT) h2o_decode_kernel(const DecodeArgs a)
 // ------------------------------------------------------------------ LSH
 
 template <typename T, int D, class TL>
-__global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
+__global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const DecodeArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     auto& S = *reinterpret_cast<DecodeSmem<T, D, TL>*>(smem_raw);
@@ -576,15 +668,40 @@ __global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
     // The projection matrix is written once when the cache is created, never
     // by a previous kernel in the stream, so it is read before the wait:
     // warp w holds rows [w*RPW, w*RPW + RPW) of W, lane j the column of bit j.
+    // Rows past D hold zeros (in x as well), which leave the sign of every
+    // partial sum above zero unchanged.
     constexpr int RPW = (D + TL::NW - 1) / TL::NW;
+    static_assert(TL::NW <= 16, "one named barrier (1..15) per hand-off");
     float wreg[RPW];
 #pragma unroll
     for (int t = 0; t < RPW; ++t) {
         const int row = warp * RPW + t;
         wreg[t] = row < D ? __ldg(a.W + row * 32 + lane) : 0.f;
     }
-    // everything below reads memory the previous kernel in the stream may
-    // have written (this unit's cache, or the inputs)
+    // This unit's occupancy, and the codes and positions of the slots this
+    // thread scans (fetched for all B slots before the occupancy is known).
+    // When the previous kernel in the stream cannot have written the cache,
+    // these are read before the dependency wait.
+    constexpr int PF = 4;
+    int2 us = make_int2(0, 0);
+    unsigned pcode[PF];
+    int ppos[PF];
+    auto read_state = [&]() {
+        us = c.ustate[unit];
+#pragma unroll
+        for (int i = 0; i < PF; ++i) {
+            const int s = tid + i * TL::NT;
+            pcode[i] = 0u;
+            ppos[i] = 0;
+            if (s < B) { pcode[i] = c.code[ub + s]; ppos[i] = c.pos[ub + s]; }
+        }
+    };
+    // (The ring is always primed after the wait: primed before it, its data
+    // would land while the victim is still being decided and HBM would then
+    // idle until the attention starts.)
+    if (a.early) read_state();
+    // everything below may read memory the previous kernel in the stream
+    // has written (the inputs, and the cache unless read above)
     grid_dependency_wait();
     grid_launch_dependents();
     // the victim (which gates the attention) depends only on small loads:
@@ -595,22 +712,9 @@ __global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
     uint4 newrow = make_uint4(0u, 0u, 0u, 0u);
     if (rank == 0 && tid < 2 * NV)
         newrow = tid < NV ? reinterpret_cast<const uint4*>(kg)[tid] : reinterpret_cast<const uint4*>(vg)[tid - NV];
-
-    // codes and positions of the slots this thread scans, fetched for all B
-    // slots before the occupancy is known
-    constexpr int PF = 4;
-    unsigned pcode[PF];
-    int ppos[PF];
-#pragma unroll
-    for (int i = 0; i < PF; ++i) {
-        const int s = tid + i * TL::NT;
-        pcode[i] = 0u;
-        ppos[i] = 0;
-        if (s < B) { pcode[i] = c.code[ub + s]; ppos[i] = c.pos[ub + s]; }
-    }
+    if (!a.early) read_state();
     QRaw<T, D> qraw;
     load_q_raw<T, D>(qg, lane, qraw);
-    const int2 us = c.ustate[unit];
     T xq = T(), xk = T();
     if (tid < D) {
         xq = qg[tid];
@@ -637,29 +741,31 @@ __global__ void __launch_bounds__(TL::NT) lsh_decode_kernel(const DecodeArgs a)
         xqr[t] = row < D ? S.qf[row] : 0.f;
         xkr[t] = row < D ? S.kf[row] : 0.f;
     }
-#pragma unroll 1
-    for (int w = 0; w < TL::NW; ++w) {
-        if (warp == w) {
-            float aq = w == 0 ? 0.f : S.hacc[0][lane];
-            float ak = w == 0 ? 0.f : S.hacc[1][lane];
-#pragma unroll
-            for (int t = 0; t < RPW; ++t) {
-                if (w * RPW + t < D) {
-                    aq = __fmaf_rn(xqr[t], wreg[t], aq);
-                    ak = __fmaf_rn(xkr[t], wreg[t], ak);
-                }
-            }
-            if (w + 1 < TL::NW) {
-                S.hacc[0][lane] = aq;
-                S.hacc[1][lane] = ak;
-            } else {
-                const unsigned cq = __ballot_sync(kFull, aq > 0.f);
-                const unsigned ck = __ballot_sync(kFull, ak > 0.f);
-                if (lane == 0) { S.code_q = cq; S.code_k = ck; }
-            }
+    // Warp w takes the partial sums from warp w-1 through named barrier w
+    // (64 threads: w-1 arrives, w waits), so a hand-off involves two warps.
+    {
+        float aq = 0.f, ak = 0.f;
+        if (warp > 0) {
+            named_barrier_sync(warp, 64);
+            aq = S.hacc[0][lane];
+            ak = S.hacc[1][lane];
         }
-        __syncthreads();
+#pragma unroll
+        for (int t = 0; t < RPW; ++t) {
+            aq = __fmaf_rn(xqr[t], wreg[t], aq);
+            ak = __fmaf_rn(xkr[t], wreg[t], ak);
+        }
+        if (warp + 1 < TL::NW) {
+            S.hacc[0][lane] = aq;
+            S.hacc[1][lane] = ak;
+            named_barrier_arrive(warp + 1, 64);
+        } else {
+            const unsigned cq = __ballot_sync(kFull, aq > 0.f);
+            const unsigned ck = __ballot_sync(kFull, ak > 0.f);
+            if (lane == 0) { S.code_q = cq; S.code_k = ck; }
+        }
     }
+    __syncthreads();
 
     // victim: the largest Hamming distance, lowest slot on ties, packed as
     // (distance << 20) | (2^20 - 1 - slot) so one unsigned max decides;

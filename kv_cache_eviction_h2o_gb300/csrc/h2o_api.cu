@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "h2o.h"
@@ -52,6 +53,50 @@ bool inject(const char* what)
 }
 
 enum Kind { kH2O = 0, kLSH = 1 };
+
+// The handle whose cache the library last wrote on each (device, stream).
+// A decode kernel may read its own cache before its programmatic-launch
+// dependency wait only when the work queued just before it on the stream
+// did not write that cache.  That holds when the last cache this library
+// wrote on the stream belongs to another handle: every kernel of the library
+// launched with programmatic serialisation waits for its predecessor before
+// it lets its own dependents start, so everything queued before that other
+// handle's work has completed by the time this kernel starts, and kernels
+// of the caller never write a cache (it is private to the handle).  A stream
+// with no record is treated as unsafe.
+struct LastWrite {
+    int device;
+    cudaStream_t stream;
+    const void* h;
+};
+constexpr int kLastWrites = 64;
+std::mutex g_lw_mu;
+LastWrite g_lw[kLastWrites];
+int g_lw_n = 0, g_lw_next = 0;
+
+// Record that `h` writes its cache on (device, stream); return true when the
+// previous record for that stream names another handle.
+bool note_cache_write(int device, cudaStream_t stream, const void* h)
+{
+    std::lock_guard<std::mutex> lock(g_lw_mu);
+    for (int i = 0; i < g_lw_n; ++i) {
+        if (g_lw[i].device == device && g_lw[i].stream == stream) {
+            const bool other = g_lw[i].h != h;
+            g_lw[i].h = h;
+            return other;
+        }
+    }
+    const int i = g_lw_n < kLastWrites ? g_lw_n++ : (g_lw_next++ % kLastWrites);
+    g_lw[i] = LastWrite{device, stream, h};
+    return false;
+}
+
+void forget_cache_writes(const void* h)
+{
+    std::lock_guard<std::mutex> lock(g_lw_mu);
+    for (int i = 0; i < g_lw_n; ++i)
+        if (g_lw[i].h == h) g_lw[i].h = nullptr;
+}
 
 }  // namespace
 
@@ -184,6 +229,7 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
     if (e == cudaSuccess) e = cudaMemsetAsync(h->ustate, 0, U * sizeof(int2), h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->pos, 0xff, U * B * sizeof(int), h->stream);
     if (e != cudaSuccess) { free_all(h); delete h; return cuda_fail(e, "initialise state"); }
+    note_cache_write(h->device, h->stream, h);
     *out = h;
     return H2O_OK;
 }
@@ -272,6 +318,7 @@ int h2o_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T
     PromptArgs pa = {};
     pa.Q = Q; pa.K = K; pa.V = V; pa.T = T; pa.H = h->H;
     pa.m2 = h->m2; pa.l = h->l; pa.c = h->c;
+    note_cache_write(h->device, h->stream, h);
     cudaError_t e = launch_prompt_stats(cv, pa, h->stream);
     if (e == cudaSuccess) e = launch_select(cv, pa, h->stream);
     if (e == cudaSuccess) e = launch_gather(cv, pa, false, h->stream);
@@ -291,6 +338,7 @@ int lsh_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T
     PromptArgs pa = {};
     pa.Q = Q; pa.K = K; pa.V = V; pa.T = T;
     pa.cq = h->cq; pa.ck = h->ck;
+    note_cache_write(h->device, h->stream, h);
     cudaError_t e = launch_lsh_prompt(cv, pa, h->W, h->stream);
     if (e != cudaSuccess) return cuda_fail(e, "lsh_prefill launch");
     h->last_T = T;
@@ -305,6 +353,7 @@ int h2o_decode_step(h2o_handle h, const void* q, const void* k, const void* v, f
     if (inject("launch")) return fail(H2O_ERR_CUDA, "kernel launch failed (injected)");
     DecodeArgs a = {};
     a.c = view(h); a.q = q; a.k = k; a.v = v; a.out = out; a.victim_out = victim_out;
+    a.early = note_cache_write(h->device, h->stream, h) ? 1 : 0;
     cudaError_t e = launch_h2o_decode(a, decode_split(h), h->stream);
     if (e != cudaSuccess) return cuda_fail(e, "h2o_decode_step launch");
     return H2O_OK;
@@ -317,6 +366,7 @@ int lsh_decode_step(h2o_handle h, const void* q, const void* k, const void* v, f
     if (inject("launch")) return fail(H2O_ERR_CUDA, "kernel launch failed (injected)");
     DecodeArgs a = {};
     a.c = view(h); a.q = q; a.k = k; a.v = v; a.out = out; a.victim_out = victim_out; a.W = h->W;
+    a.early = note_cache_write(h->device, h->stream, h) ? 1 : 0;
     cudaError_t e = launch_lsh_decode(a, decode_split(h), h->stream);
     if (e != cudaSuccess) return cuda_fail(e, "lsh_decode_step launch");
     return H2O_OK;
@@ -375,6 +425,7 @@ int h2o_set_state(h2o_handle h, const void* K, const void* V, const double* scor
         for (int u = 0; u < h->U; ++u)
             if (occupancy[u] < 0 || occupancy[u] > h->B) return fail(H2O_ERR_ARG, "occupancy out of range");
     cudaError_t e = cudaStreamSynchronize(h->stream);
+    note_cache_write(h->device, h->stream, h);
     if (K && e == cudaSuccess) e = cudaMemcpyAsync(h->K, K, UB * row, cudaMemcpyHostToDevice, h->stream);
     if (V && e == cudaSuccess) e = cudaMemcpyAsync(h->V, V, UB * row, cudaMemcpyHostToDevice, h->stream);
     if (pos && e == cudaSuccess) e = cudaMemcpyAsync(h->pos, pos, UB * sizeof(int), cudaMemcpyHostToDevice, h->stream);
@@ -465,6 +516,7 @@ int h2o_sync(h2o_handle h)
 int h2o_selftest_wait_timeout(h2o_handle h)
 {
     if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
+    note_cache_write(h->device, h->stream, h);
     cudaError_t e = launch_wait_selftest(h->err, h->stream);
     if (e != cudaSuccess) return cuda_fail(e, "h2o_selftest_wait_timeout launch");
     return H2O_OK;
@@ -474,6 +526,7 @@ void h2o_destroy(h2o_handle h)
 {
     if (!h) return;
     cudaStreamSynchronize(h->stream);
+    forget_cache_writes(h);
     free_all(h);
     delete h;
 }

@@ -27,6 +27,8 @@ struct DecodeArgs {
     float* out;         // [U][D]
     int* victim_out;    // [U] or nullptr
     const float* W;     // [D][32] (LSH)
+    int early;          // 1: the previous kernel in the stream does not write this
+                        // cache, so the cache may be read before the dependency wait
 };
 
 struct PromptArgs {

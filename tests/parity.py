@@ -246,33 +246,48 @@ def run_full_config(name, sample, check_every=64):
     near = 0
     if w.lsh:
         st = oracle.lsh_prefill(gs["Q"], gs["K"], gs["V"], W, B, w.recent)
-        for t in range(S):
-            o_ref, v_ref = oracle.lsh_decode_step(st, gs["q"][t], gs["k"][t], gs["v"][t], W, T + t, w.recent, w.scale)
-            assert (vics[t] == v_ref).all(), "step %d: LSH victims differ" % t
-            check_out(outs[t], o_ref, "step %d out" % t)
+        replay_lsh(st, gs, W, T, w.recent, w.scale, outs, vics)
         assert (sub["code"] == st.code).all()
     else:
         # prompt phase: the device's kept set against the oracle's (near ties counted)
         st, c, near = align_prefill(st0, gs["Q"], gs["K"], gs["V"], B, w.heavy, w.recent, w.scale)
         assert (st0["pos"] == st.pos).all(), "prompt positions differ"
         check_scores(st0["score"], st.score, "prompt scores")
-        for t in range(S):
-            before = st.copy()
-            o_ref, v_ref, mg, _ = oracle.h2o_decode_step(st, gs["q"][t], gs["k"][t], gs["v"][t], T + t, w.recent,
-                                                         w.scale)
-            mism = vics[t] != v_ref
-            if mism.any():
-                assert (mg[mism] < NEAR_TIE).all(), "step %d: victims differ outside a near tie" % t
-                near += int(mism.sum())
-                st = before
-                forced = np.where(mism, vics[t], -1).astype(np.int32)
-                o_ref, _, _, _ = oracle.h2o_decode_step(st, gs["q"][t], gs["k"][t], gs["v"][t], T + t, w.recent,
-                                                        w.scale, forced)
-            check_out(outs[t], o_ref, "step %d out" % t)
+        n2, st = replay_h2o(st, gs, T, w.recent, w.scale, outs, vics)
+        near += n2
         check_scores(sub["score"], st.score, "final scores")
     assert (sub["pos"] == st.pos).all(), "final positions differ"
     assert (sub["K"] == st.K).all() and (sub["V"] == st.V).all(), "final cache rows differ"
     return near
+
+
+def replay_h2o(st, g, T, r, scale, outs, vics):
+    """Replay the oracle's H2O decode steps over the device's recorded
+    outputs and victims (near ties counted and followed); returns
+    (near-tie count, final oracle state)."""
+    near = 0
+    for t in range(len(outs)):
+        before = st.copy()
+        o_ref, v_ref, mg, _ = oracle.h2o_decode_step(st, g["q"][t], g["k"][t], g["v"][t], T + t, r, scale)
+        mism = vics[t] != v_ref
+        if mism.any():
+            assert (mg[mism] < NEAR_TIE).all(), "step %d: victims differ outside a near tie" % t
+            near += int(mism.sum())
+            st = before
+            forced = np.where(mism, vics[t], -1).astype(np.int32)
+            o_ref, _, _, _ = oracle.h2o_decode_step(st, g["q"][t], g["k"][t], g["v"][t], T + t, r, scale, forced)
+        check_out(outs[t], o_ref, "step %d out" % t)
+    return near, st
+
+
+def replay_lsh(st, g, W, T, r, scale, outs, vics):
+    """Replay the oracle's HashEvict decode steps against the device's
+    recorded outputs and victims (victims bit-exact)."""
+    for t in range(len(outs)):
+        o_ref, v_ref = oracle.lsh_decode_step(st, g["q"][t], g["k"][t], g["v"][t], W, T + t, r, scale)
+        assert (vics[t] == v_ref).all(), "step %d: LSH victims differ" % t
+        check_out(outs[t], o_ref, "step %d out" % t)
+    return st
 
 
 def _state_all(h, U, B, d, dtype):

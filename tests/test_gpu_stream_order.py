@@ -1,0 +1,91 @@
+"""Decode steps of several caches queued back to back on one stream.
+
+No host synchronisation separates the steps, so consecutive decode kernels
+overlap through programmatic dependent launch.  A step that follows another
+cache's step reads its own cache before its dependency wait; a step that
+follows a step of the same cache waits first.  A seeded random interleaving
+exercises both, and every output and victim is compared with the oracle
+(H2O: Heavy-Hitter Oracle, the decode-phase eviction rule; HashEvict: the
+Hamming-distance eviction rule)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kv_cache_eviction_h2o_gb300 import binding as L
+from kv_cache_eviction_h2o_gb300 import workloads as wl
+from parity import (Dev, align_prefill, check_scores, replay_h2o, replay_lsh, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+def _order(counts, seed, repeat_p=0.35):
+    """A seeded interleaving of the handles' steps: each entry names the
+    handle that advances; a handle repeats with probability repeat_p."""
+    rng = np.random.default_rng(seed)
+    left = list(counts)
+    order, last = [], None
+    while sum(left):
+        live = [i for i in range(len(left)) if left[i]]
+        if last is not None and left[last] and rng.random() < repeat_p:
+            i = last
+        else:
+            i = int(rng.choice(live))
+        order.append(i)
+        left[i] -= 1
+        last = i
+    return order
+
+
+def test_interleaved_caches_back_to_back():
+    S = 20
+    wa = wl.WORKLOADS["opt-6.7b"]
+    wc = wl.WORKLOADS["hashevict-opt-6.7b"]
+    ga = wl.generate(wa, units=range(0, 12), steps=S)
+    gb = wl.generate(wa, units=range(12, 24), steps=S)
+    gc = wl.generate(wc, units=range(0, 10), steps=S)
+    W = gc["W"]
+    devs = [Dev("h2o", 12, wa.head_dim, wa.budget, wa.heavy, wa.recent, wa.dtype, wa.scale),
+            Dev("h2o", 12, wa.head_dim, wa.budget, wa.heavy, wa.recent, wa.dtype, wa.scale),
+            Dev("lsh", 10, wc.head_dim, wc.budget, 0, wc.recent, wc.dtype, wc.scale, W=W)]
+    gens = [ga, gb, gc]
+    for dev, g in zip(devs, gens):
+        dev.prefill(g["Q"], g["K"], g["V"])
+    st0 = [dev.state() for dev in devs]
+
+    # every step's inputs and outputs live on the device before the first launch
+    ins = [{key: to_dev(g[key], dev.dtype) for key in ("q", "k", "v")} for dev, g in zip(devs, gens)]
+    outs = [torch.empty((S, dev.U, dev.d), dtype=torch.float32, device="cuda") for dev in devs]
+    vics = [torch.empty((S, dev.U), dtype=torch.int32, device="cuda") for dev in devs]
+    order = _order([S, S, S], seed=7)
+    pairs = list(zip(order[:-1], order[1:]))
+    assert any(a == b for a, b in pairs) and any(a != b for a, b in pairs)
+    t_of = [0, 0, 0]
+    for i in order:
+        dev, t = devs[i], t_of[i]
+        fn = L.h2o_decode_step if dev.kind == "h2o" else L.lsh_decode_step
+        fn(dev.h, ins[i]["q"][t], ins[i]["k"][t], ins[i]["v"][t], outs[i][t], vics[i][t])
+        t_of[i] += 1
+    torch.cuda.synchronize()
+    for dev in devs:
+        L.h2o_sync(dev.h)
+
+    T = wa.prompt
+    for i, (dev, g) in enumerate(zip(devs, gens)):
+        o = [x.astype(np.float64) for x in outs[i].cpu().numpy()]
+        v = list(vics[i].cpu().numpy())
+        fin = dev.state()
+        if dev.kind == "h2o":
+            st, _, _ = align_prefill(st0[i], g["Q"], g["K"], g["V"], wa.budget, wa.heavy, wa.recent, wa.scale)
+            assert (st0[i]["pos"] == st.pos).all()
+            near, st = replay_h2o(st, g, T, wa.recent, wa.scale, o, v)
+            check_scores(fin["score"], st.score, "cache %d final scores" % i)
+        else:
+            st = oracle.lsh_prefill(g["Q"], g["K"], g["V"], W, wc.budget, wc.recent)
+            replay_lsh(st, g, W, T, wc.recent, wc.scale, o, v)
+            assert (fin["code"] == st.code).all()
+        assert (fin["pos"] == st.pos).all(), "cache %d: final positions differ" % i
+        assert (fin["K"] == st.K).all() and (fin["V"] == st.V).all(), "cache %d: final rows differ" % i
+        assert (fin["npos"] == T + S).all()
+    for dev in devs:
+        dev.close()
