@@ -562,7 +562,8 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
         invL = 1.f / Lc;
     }
 
-    // accumulate this step's probabilities; arg-min over candidates
+    // accumulate this step's probabilities; arg-min over candidates (slots
+    // whose position is at most p - r)
     ArgMin best = argmin_none(), best_all = argmin_none();
 #pragma unroll
     for (int i = 0; i < TL::SPT; ++i) {
@@ -574,13 +575,13 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
             if (full) {
                 const ArgMin k = ArgMin{ord_key(ns.x), ord_key(ns.y), (unsigned)s};
                 if (ps[i] <= p - c.r) argmin_take(best, k);
-                argmin_take(best_all, k);
+                if (C > 1) argmin_take(best_all, k);
             }
         }
     }
     if (full) {
         best = warp_argmin(best);
-        best_all = warp_argmin(best_all);
+        if (C > 1) best_all = warp_argmin(best_all);
         if (lane == 0) {
             S.am[0][0][warp] = best.hi; S.am[0][1][warp] = best.lo; S.am[0][2][warp] = best.slot;
             S.am[1][0][warp] = best_all.hi; S.am[1][1][warp] = best_all.lo; S.am[1][2][warp] = best_all.slot;
@@ -596,6 +597,52 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     }
     if (rank == 0 && tid == 0) S.P_new = exp2f(S.z_new - M) * invL;
     __syncthreads();
+
+    // Write the new token into the victim slot (slot n while the cache is
+    // not full).  `write_row` runs in the threads holding `newrow`.
+    auto finish = [&](int victim) {
+        if (victim < 0 || victim >= B) victim = 0;   // n == 0 with B == 0 cannot happen
+        if (tid == 0) {
+            c.score[ub + victim] = make_float2(S.P_new, 0.f);
+            c.pos[ub + victim] = p;
+            c.ustate[unit] = make_int2(min(n + 1, B), p + 1);
+            if (a.victim_out) a.victim_out[unit] = full ? victim : -1;
+        }
+        if (tid < NV)
+            reinterpret_cast<uint4*>(Kc + (size_t)victim * D)[tid] = newrow;
+        else if (tid < 2 * NV)
+            reinterpret_cast<uint4*>(Vc + (size_t)victim * D)[tid - NV] = newrow;
+    };
+
+    if (C == 1) {
+        // one CTA holds the unit: warp 0 reduces the warps' candidates; with
+        // no candidate at all (possible only for loaded states) every live
+        // slot competes, its new score re-read from global memory (written
+        // above by this CTA)
+        int victim = n;
+        if (warp == 0 && full) {
+            ArgMin w = lane < TL::NW ? ArgMin{S.am[0][0][lane], S.am[0][1][lane], S.am[0][2][lane]} : argmin_none();
+            w = warp_argmin(w);
+            if (w.slot == 0xffffffffu) {
+                ArgMin al = argmin_none();
+                for (int s = lane; s < n; s += 32) {
+                    const float2 sc = c.score[ub + s];
+                    argmin_take(al, ArgMin{ord_key(sc.x), ord_key(sc.y), (unsigned)s});
+                }
+                w = warp_argmin(al);
+            }
+            victim = (int)w.slot;
+        }
+        if constexpr (2 * NV <= 32) {
+            if (warp == 0) finish(victim);
+        } else {
+            if (tid == 0) S.victim = victim;
+            __syncthreads();
+            finish(S.victim);
+        }
+        return;
+    }
+
     if (full && warp == 0) {
         // this CTA's arg-min over its warps, pushed into rank 0's exchange
 #pragma unroll
@@ -624,19 +671,10 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
             }
             victim = (int)(vc.slot != 0xffffffffu ? vc.slot : va.slot);
         }
-        if (victim < 0 || victim >= B) victim = 0;   // n == 0 with B == 0 cannot happen
         S.victim = victim;
-        c.score[ub + victim] = make_float2(S.P_new, 0.f);
-        c.pos[ub + victim] = p;
-        c.ustate[unit] = make_int2(min(n + 1, B), p + 1);
-        if (a.victim_out) a.victim_out[unit] = full ? victim : -1;
     }
     __syncthreads();
-    const int victim = S.victim;
-    if (tid < NV)
-        reinterpret_cast<uint4*>(Kc + (size_t)victim * D)[tid] = newrow;
-    else if (tid < 2 * NV)
-        reinterpret_cast<uint4*>(Vc + (size_t)victim * D)[tid - NV] = newrow;
+    finish(S.victim);
 }
 
 // ------------------------------------------------------------------ LSH
