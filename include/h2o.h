@@ -37,6 +37,11 @@
  *  - Calls enqueue work on the handle's stream and return without waiting.
  *    Argument and state errors are returned synchronously; a device-side
  *    error (a bounded wait that ran out) is reported by h2o_sync.
+ *  - Decode steps use programmatic dependent launch: a step may start while
+ *    the previous kernel in its stream drains.  It reads q, k, v only after
+ *    that kernel has completed; it reads its own cache earlier only when the
+ *    last cache this library wrote on the stream belongs to another handle.
+ *    So nothing but this API may write a handle's cache (it is private).
  *  - Every int-returning call returns H2O_OK (0) or a negative h2o_status;
  *    h2o_last_error() then describes the failure (thread-local).
  *  - Positions are 0-based.  After a prompt of T tokens the next decoded
