@@ -117,6 +117,7 @@ struct h2o_ctx {
     int2* ustate;
     int* err;
     float* W;
+    float* W_host;             // host copy of W (launch parameter of the prompt codes)
     // prompt scratch
     int T_cap;
     float* m2;
@@ -158,6 +159,8 @@ void free_all(h2o_ctx* h)
     free_prompt(h);
     cudaFree(h->K); cudaFree(h->V); cudaFree(h->score); cudaFree(h->pos); cudaFree(h->code);
     cudaFree(h->ustate); cudaFree(h->err); cudaFree(h->W);
+    free(h->W_host);
+    h->W_host = nullptr;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -224,6 +227,11 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
         }
         e = cudaMemcpyAsync(h->W, W, (size_t)head_dim * 32 * sizeof(float), cudaMemcpyDeviceToDevice, h->stream);
         if (e != cudaSuccess) { free_all(h); delete h; return cuda_fail(e, "copy W"); }
+        h->W_host = static_cast<float*>(malloc((size_t)head_dim * 32 * sizeof(float)));
+        if (!h->W_host) { free_all(h); delete h; return fail(H2O_ERR_ALLOC, "host allocation failed"); }
+        e = cudaMemcpyAsync(h->W_host, W, (size_t)head_dim * 32 * sizeof(float), cudaMemcpyDeviceToHost, h->stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+        if (e != cudaSuccess) { free_all(h); delete h; return cuda_fail(e, "copy W to the host"); }
     }
     e = cudaMemsetAsync(h->err, 0, sizeof(int), h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->ustate, 0, U * sizeof(int2), h->stream);
@@ -339,7 +347,7 @@ int lsh_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T
     pa.Q = Q; pa.K = K; pa.V = V; pa.T = T;
     pa.cq = h->cq; pa.ck = h->ck;
     note_cache_write(h->device, h->stream, h);
-    cudaError_t e = launch_lsh_prompt(cv, pa, h->W, h->stream);
+    cudaError_t e = launch_lsh_prompt(cv, pa, h->W, h->W_host, h->stream);
     if (e != cudaSuccess) return cuda_fail(e, "lsh_prefill launch");
     h->last_T = T;
     h->ready = 1;

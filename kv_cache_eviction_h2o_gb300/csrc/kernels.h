@@ -62,7 +62,9 @@ cudaError_t launch_wait_selftest(int* err, cudaStream_t st);
 // Record a failure for h2o_last_error() and return `code`.
 int set_last_error(int code, const char* fmt, ...);
 
+// W: the projection [D][32] on the device; W_host: the same values in host
+// memory (the sign-code kernel takes them as a launch parameter).
 cudaError_t launch_lsh_prompt(const CacheView& c, const PromptArgs& p, const float* W,
-                              cudaStream_t st);
+                              const float* W_host, cudaStream_t st);
 
 }  // namespace h2o

@@ -16,6 +16,7 @@
 #include <cfloat>
 #include <climits>
 #include <cstdlib>
+#include <cstring>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -383,69 +384,75 @@ __global__ void __launch_bounds__(256) gather_kernel(CacheView cv, PromptArgs pa
     }
 }
 
-// Sign codes of every prompt query and key.  Lane j of a warp keeps column j
-// of W in registers and owns bit j.  The warp hashes kCodeTok tokens per
-// pass (2 * kCodeTok independent fp32 fused multiply-add chains, each in
-// index order from 0); the next pass's rows are fetched into registers
-// while the current chains run, then staged in shared memory.
-constexpr int kCodeWarps = 8;
-constexpr int kCodeTok = 4;
+// Sign codes of every prompt query and key, one row (a query or a key) per
+// thread: bit j is the sign of the fp32 fused multiply-add chain
+// x[0] W[0][j] + ... + x[D-1] W[D-1][j] taken in index order from 0.  A
+// thread runs its row's 32 chains side by side.  W is a launch parameter, so
+// every multiply-add reads its W value from the constant bank, broadcast to
+// the warp, instead of through shared memory (where delivering one value to
+// 32 lanes costs a shared-memory cycle, a quarter of the SM's FMA rate).
+constexpr int kCodeThreads = 256;
+
+template <int D>
+struct WParam {
+    float w[D * 32];
+};
+
+// The fp32 values of one 16-byte chunk of T.
+template <typename T>
+__device__ __forceinline__ void chunk_to_f32(const uint4& w, float* out)
+{
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if constexpr (sizeof(T) == 2) {
+            out[2 * k] = __uint_as_float(u[k] << 16);
+            out[2 * k + 1] = __uint_as_float(u[k] & 0xffff0000u);
+        } else {
+            out[k] = __uint_as_float(u[k]);
+        }
+    }
+}
 
 template <typename T, int D>
-__global__ void __launch_bounds__(32 * kCodeWarps) lsh_codes_kernel(const T* __restrict__ Q, const T* __restrict__ K,
-                                                                    const float* __restrict__ W, long long ntok,
-                                                                    uint32_t* __restrict__ cq,
-                                                                    uint32_t* __restrict__ ck)
+__global__ void __launch_bounds__(kCodeThreads) lsh_codes_kernel(const T* __restrict__ Q, const T* __restrict__ K,
+                                                                 const __grid_constant__ WParam<D> wp,
+                                                                 long long ntok, uint32_t* __restrict__ cq,
+                                                                 uint32_t* __restrict__ ck)
 {
-    constexpr int EPL = D / 32;                       // elements of a row per lane
-    __shared__ __align__(16) float xs[kCodeWarps][2 * kCodeTok][D];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float w[D];
+    constexpr int VE = 16 / (int)sizeof(T);           // elements per 16-byte chunk
+    constexpr int NCH = D / VE;                       // chunks per row
+    constexpr int G = NCH < 8 ? NCH : 8;              // chunks loaded ahead
+    const long long rows = 2 * ntok;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < rows; g += stride) {
+        const bool is_q = g < ntok;
+        const long long t = is_q ? g : g - ntok;
+        const uint4* row = reinterpret_cast<const uint4*>((is_q ? Q : K) + t * D);
+        float acc[32];
 #pragma unroll
-    for (int i = 0; i < D; ++i) w[i] = __ldg(W + i * 32 + lane);
-    const long long step = (long long)gridDim.x * kCodeWarps * kCodeTok;
-    long long tok0 = ((long long)blockIdx.x * kCodeWarps + warp) * kCodeTok;
-    float pre[2 * kCodeTok][EPL];
-    auto fetch = [&](long long t0) {
+        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
 #pragma unroll
-        for (int k = 0; k < kCodeTok; ++k) {
-            const long long t = t0 + k;
+        for (int c0 = 0; c0 < NCH; c0 += G) {
+            uint4 ch[G];
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) {
-                pre[2 * k][e] = t < ntok ? Elem<T>::to_f(Q[t * D + lane * EPL + e]) : 0.f;
-                pre[2 * k + 1][e] = t < ntok ? Elem<T>::to_f(K[t * D + lane * EPL + e]) : 0.f;
+            for (int c = 0; c < G; ++c) ch[c] = __ldg(row + c0 + c);
+#pragma unroll
+            for (int c = 0; c < G; ++c) {
+                float xv[VE];
+                chunk_to_f32<T>(ch[c], xv);
+#pragma unroll
+                for (int e = 0; e < VE; ++e) {
+                    const int i = (c0 + c) * VE + e;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[j] = __fmaf_rn(xv[e], wp.w[i * 32 + j], acc[j]);
+                }
             }
         }
-    };
-    fetch(tok0);
-    for (; tok0 < ntok; tok0 += step) {
-        __syncwarp();
+        uint32_t code = 0u;
 #pragma unroll
-        for (int r = 0; r < 2 * kCodeTok; ++r)
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) xs[warp][r][lane * EPL + e] = pre[r][e];
-        __syncwarp();
-        fetch(tok0 + step);
-        float acc[2 * kCodeTok];
-#pragma unroll
-        for (int r = 0; r < 2 * kCodeTok; ++r) acc[r] = 0.f;
-#pragma unroll
-        for (int i = 0; i < D; i += 4) {
-#pragma unroll
-            for (int r = 0; r < 2 * kCodeTok; ++r) {
-                const float4 x4 = *reinterpret_cast<const float4*>(&xs[warp][r][i]);
-                acc[r] = __fmaf_rn(x4.x, w[i], acc[r]);
-                acc[r] = __fmaf_rn(x4.y, w[i + 1], acc[r]);
-                acc[r] = __fmaf_rn(x4.z, w[i + 2], acc[r]);
-                acc[r] = __fmaf_rn(x4.w, w[i + 3], acc[r]);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < kCodeTok; ++k) {
-            const unsigned bq = __ballot_sync(kFull, acc[2 * k] > 0.f);
-            const unsigned bk = __ballot_sync(kFull, acc[2 * k + 1] > 0.f);
-            if (lane == 0 && tok0 + k < ntok) { cq[tok0 + k] = bq; ck[tok0 + k] = bk; }
-        }
+        for (int j = 0; j < 32; ++j) code |= (acc[j] > 0.f ? 1u : 0u) << j;
+        (is_q ? cq : ck)[t] = code;
     }
 }
 
@@ -511,6 +518,108 @@ __global__ void __launch_bounds__(64) lsh_replay_reg_kernel(CacheView cv, Prompt
     for (int i = 0; i < kRegSlots; ++i) {
         const int s = lane + 32 * i;
         if (s < B) cv.pos[ub + s] = pos[i];
+    }
+    if (lane == 0) cv.ustate[unit] = make_int2(n0, T_);
+}
+
+// The same replay, software-pipelined, for a recent window r >= 2 and
+// budgets up to 32 * NR.  A slot replaced at step t holds position t, which
+// is no candidate at step t + 1 (t > t + 1 - r), so step t + 1's scan can run
+// on registers that do not yet hold step t's replacement: each lane keeps its
+// two largest candidate keys, and once step t's victim is known (its
+// warp-wide max was reduced while the scan ran) a lane whose largest key
+// names that slot falls back to its second.  The victim's registers are then
+// updated.  Positions are 0..t-1 and distinct during the replay and B >= r,
+// so some slot is always a candidate; the every-slot rule is kept anyway.
+template <int NR>
+__global__ void __launch_bounds__(64) lsh_replay_pipe_kernel(CacheView cv, PromptArgs pa)
+{
+    const int B = cv.B, T_ = pa.T, r = cv.r;
+    const int lane = threadIdx.x & 31;
+    const int unit = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (unit >= cv.U) return;
+    const uint32_t* cq = pa.cq + (size_t)unit * T_;
+    const uint32_t* ck = pa.ck + (size_t)unit * T_;
+    const int n0 = min(T_, B);
+    uint32_t code[NR];
+    int pos[NR];
+    unsigned vmask = 0u;                        // bit i: slot lane + 32 i exists
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+        const int s = lane + 32 * i;
+        const bool ok = s < n0;
+        vmask |= ok ? (1u << i) : 0u;
+        pos[i] = ok ? s : INT_MAX;
+        code[i] = ok ? ck[s] : 0u;
+    }
+    // key of register slot i: (distance << 20) | (2^20 - 1 - slot)
+    auto slot_key = [&](uint32_t q, int i) -> unsigned {
+        return ((unsigned)__popc(q ^ code[i]) << 20) | (0xFFFFFu - (unsigned)(lane + 32 * i));
+    };
+    auto every_slot_best = [&](uint32_t q) -> unsigned {
+        unsigned b = 0u;
+#pragma unroll
+        for (int i = 0; i < NR; ++i)
+            if (vmask >> i & 1u) b = max(b, slot_key(q, i));
+        return __reduce_max_sync(kFull, b);
+    };
+    // put (kcode, p) into the slot that `key` names (selects, no branch: an
+    // indexed jump per step cost more than the selects)
+    auto replace = [&](unsigned key, uint32_t kcode, int p) {
+        const int v = (int)(0xFFFFFu - (key & 0xFFFFFu));
+        const int vl = v & 31, iv = v >> 5;
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            const bool hit = (lane == vl) && (i == iv);
+            code[i] = hit ? kcode : code[i];
+            pos[i] = hit ? p : pos[i];
+        }
+    };
+    // this lane's entry of the current and of the next 32-token batch
+    uint32_t qb = 0u, kb = 0u, qn = 0u, kn = 0u;
+    {
+        const int t0 = B + lane, t1 = B + 32 + lane;
+        if (t0 < T_) { qb = cq[t0]; kb = ck[t0]; }
+        if (t1 < T_) { qn = cq[t1]; kn = ck[t1]; }
+    }
+    unsigned prev = 0u;                         // last step's largest candidate key
+    uint32_t qprev = 0u, kprev = 0u;
+    for (int t = B; t < T_; ++t) {
+        const int o = (t - B) & 31;
+        if (o == 0 && t > B) {
+            qb = qn; kb = kn;
+            const int tt = t + 32 + lane;
+            qn = tt < T_ ? cq[tt] : 0u;
+            kn = tt < T_ ? ck[tt] : 0u;
+        }
+        const uint32_t q = __shfl_sync(kFull, qb, o);
+        const uint32_t knew = __shfl_sync(kFull, kb, o);
+        const int tr = t - r;
+        unsigned b1 = 0u, b2 = 0u;
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            const unsigned k = pos[i] <= tr ? slot_key(q, i) : 0u;
+            b2 = max(b2, min(b1, k));
+            b1 = max(b1, k);
+        }
+        if (t > B) {
+            if (prev == 0u) prev = every_slot_best(qprev);
+            if ((b1 & 0xFFFFFu) == (prev & 0xFFFFFu)) b1 = b2;
+            replace(prev, kprev, t - 1);
+        }
+        prev = __reduce_max_sync(kFull, b1);
+        qprev = q;
+        kprev = knew;
+    }
+    if (T_ > B) {
+        if (prev == 0u) prev = every_slot_best(qprev);
+        replace(prev, kprev, T_ - 1);
+    }
+    const size_t ub = (size_t)unit * B;
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+        const int s = lane + 32 * i;
+        if (s < B) cv.pos[ub + s] = (vmask >> i & 1u) ? pos[i] : -1;
     }
     if (lane == 0) cv.ustate[unit] = make_int2(n0, T_);
 }
@@ -619,7 +728,7 @@ int replay_warps(int B)
 }
 
 template <typename T, int D>
-cudaError_t lsh_t(const CacheView& c, const PromptArgs& p, const float* W, cudaStream_t st)
+cudaError_t lsh_t(const CacheView& c, const PromptArgs& p, const float* W_host, cudaStream_t st)
 {
     const long long ntok = (long long)c.U * p.T;
     int sms = 0, dev = 0;
@@ -628,12 +737,27 @@ cudaError_t lsh_t(const CacheView& c, const PromptArgs& p, const float* W, cudaS
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    long long blocks = (ntok + kCodeWarps * kCodeTok - 1) / (kCodeWarps * kCodeTok);
-    if (blocks > 4LL * sms) blocks = 4LL * sms;
-    lsh_codes_kernel<T, D><<<(unsigned)blocks, 32 * kCodeWarps, 0, st>>>(
-        reinterpret_cast<const T*>(p.Q), reinterpret_cast<const T*>(p.K), W, ntok, p.cq, p.ck);
+    long long blocks = (2 * ntok + kCodeThreads - 1) / kCodeThreads;
+    if (blocks > 8LL * sms) blocks = 8LL * sms;
+    WParam<D> wp;
+    memcpy(wp.w, W_host, sizeof(wp.w));
+    lsh_codes_kernel<T, D><<<(unsigned)blocks, kCodeThreads, 0, st>>>(
+        reinterpret_cast<const T*>(p.Q), reinterpret_cast<const T*>(p.K), wp, ntok, p.cq, p.ck);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (c.r >= 2 && c.B <= 32 * 16) {
+        const unsigned blocks = (unsigned)((c.U + 1) / 2);
+        const int nr = (c.B + 31) / 32;
+        if (nr <= 1) lsh_replay_pipe_kernel<1><<<blocks, 64, 0, st>>>(c, p);
+        else if (nr <= 2) lsh_replay_pipe_kernel<2><<<blocks, 64, 0, st>>>(c, p);
+        else if (nr <= 4) lsh_replay_pipe_kernel<4><<<blocks, 64, 0, st>>>(c, p);
+        else if (nr <= 8) lsh_replay_pipe_kernel<8><<<blocks, 64, 0, st>>>(c, p);
+        else if (nr <= 13) lsh_replay_pipe_kernel<13><<<blocks, 64, 0, st>>>(c, p);
+        else lsh_replay_pipe_kernel<16><<<blocks, 64, 0, st>>>(c, p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return gather_t<T, D>(c, p, true, st);
+    }
     if (c.B <= 32 * kRegSlots) {
         lsh_replay_reg_kernel<<<(unsigned)((c.U + 1) / 2), 64, 0, st>>>(c, p);
         e = cudaGetLastError();
@@ -685,11 +809,14 @@ cudaError_t launch_gather(const CacheView& c, const PromptArgs& p, bool with_cod
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_lsh_prompt(const CacheView& c, const PromptArgs& p, const float* W, cudaStream_t st)
+cudaError_t launch_lsh_prompt(const CacheView& c, const PromptArgs& p, const float* W, const float* W_host,
+                              cudaStream_t st)
 {
+    (void)W;
+    if (!W_host) return cudaErrorInvalidValue;
     const bool bf = c.dtype == 1;
-    if (c.D == 128) return bf ? lsh_t<__nv_bfloat16, 128>(c, p, W, st) : lsh_t<float, 128>(c, p, W, st);
-    if (c.D == 64) return bf ? lsh_t<__nv_bfloat16, 64>(c, p, W, st) : lsh_t<float, 64>(c, p, W, st);
+    if (c.D == 128) return bf ? lsh_t<__nv_bfloat16, 128>(c, p, W_host, st) : lsh_t<float, 128>(c, p, W_host, st);
+    if (c.D == 64) return bf ? lsh_t<__nv_bfloat16, 64>(c, p, W_host, st) : lsh_t<float, 64>(c, p, W_host, st);
     return cudaErrorInvalidValue;
 }
 

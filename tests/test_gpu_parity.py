@@ -119,6 +119,9 @@ def test_edge_cases_h2o(T, B, H, r, dtype, d):
 
 
 @pytest.mark.parametrize("T,B,r", [(5, 8, 4), (1, 8, 4), (40, 8, 8), (40, 8, 0), (40, 1, 1), (70, 33, 16),
+                                   (300, 100, 2),      # smallest window of the pipelined prompt replay
+                                   (400, 250, 60), (700, 500, 250),
+                                   (600, 480, 480),    # window = budget: one candidate per step
                                    (1500, 1100, 100)])
 @pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
 def test_edge_cases_lsh(T, B, r, dtype, d):
