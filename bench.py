@@ -461,6 +461,9 @@ def run_e2e(args, L, torch, layers, h2o, lsh, out_h, out_l, vic_h, vic_l, W, S, 
 
     copy_stream = torch.cuda.Stream()
     ready = [torch.cuda.Event() for _ in range(NL)]
+    ready_dec = torch.cuda.Event()
+    h2o_done = torch.cuda.Event()
+    out_h_home = torch.cuda.Event()
     # raw device addresses of every per-step argument, computed once (the
     # binding takes plain integers; no tensor views per call)
     def rows(x):
@@ -472,34 +475,47 @@ def run_e2e(args, L, torch, layers, h2o, lsh, out_h, out_l, vic_h, vic_l, W, S, 
     hl = [int(h) for h in lsh]
 
     def step():
-        # inputs stream in layer by layer on a copy stream; each layer's
-        # prompt phase waits only for its own inputs
+        # inputs stream in on a copy stream: every layer's prompt rows first
+        # (each layer's prompt phase waits only for its own), the decode
+        # steps' rows last; the H2O outputs go home while the HashEvict
+        # steps run
         with torch.cuda.stream(copy_stream):
             copy_stream.wait_stream(stream)
             for li in range(NL):
-                for k in ("Q", "K", "V", "q", "k", "v"):
+                for k in ("Q", "K", "V"):
                     layers[li][k].copy_(host_in[li][k], non_blocking=True)
                 ready[li].record(copy_stream)
+            for li in range(NL):
+                for k in ("q", "k", "v"):
+                    layers[li][k].copy_(host_in[li][k], non_blocking=True)
+            ready_dec.record(copy_stream)
         with torch.cuda.stream(stream):
             for li in range(NL):
                 stream.wait_event(ready[li])
                 g = layers[li]
                 L.h2o_prefill(h2o[li], g["Q"], g["K"], g["V"], T)
                 L.lsh_prefill(lsh[li], g["Q"], g["K"], g["V"], T)
+            stream.wait_event(ready_dec)
             for t in range(S):
                 for li in range(NL):
                     pp, op = ptr[li], optr[li]
                     L.h2o_decode_step(hh[li], pp["q"][t], pp["k"][t], pp["v"][t], op[0][t], op[2][t])
+            h2o_done.record(stream)
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(h2o_done)
+            for li in range(NL):
+                host_out[li][0].copy_(out_h[li], non_blocking=True)
+                host_out[li][2].copy_(vic_h[li], non_blocking=True)
+            out_h_home.record(copy_stream)
+        with torch.cuda.stream(stream):
             for t in range(S):
                 for li in range(NL):
                     pp, op = ptr[li], optr[li]
                     L.lsh_decode_step(hl[li], pp["q"][t], pp["k"][t], pp["v"][t], op[1][t], op[3][t])
             for li in range(NL):
-                ho = host_out[li]
-                ho[0].copy_(out_h[li], non_blocking=True)
-                ho[1].copy_(out_l[li], non_blocking=True)
-                ho[2].copy_(vic_h[li], non_blocking=True)
-                ho[3].copy_(vic_l[li], non_blocking=True)
+                host_out[li][1].copy_(out_l[li], non_blocking=True)
+                host_out[li][3].copy_(vic_l[li], non_blocking=True)
+            stream.wait_event(out_h_home)
 
     step()
     torch.cuda.synchronize()
