@@ -48,6 +48,7 @@ def lib():
         L.oracle_h2o_decode_step.argtypes = [_i, _i, _i, _i, _d, _i, _f64p, _f64p, _f64p,
                                              _i32p, _i32p, _f64p, _f64p, _f64p, _f64p,
                                              _vp, _vp, _vp, _vp]
+        L.oracle_quantize_rows.argtypes = [_i, _i, _f64p, _vp, _f32p]
         L.oracle_lsh_code.argtypes = [_i, _f64p, _f32p]
         L.oracle_lsh_code.restype = ctypes.c_uint32
         L.oracle_lsh_codes.argtypes = [_i, _i, _f64p, _f32p, _u32p]
@@ -110,8 +111,9 @@ class H2OState:
 
     def copy(self):
         s = H2OState(self.U, self.B, self.d)
-        for name in ("K", "V", "score", "pos", "occ"):
-            setattr(s, name, getattr(self, name).copy())
+        for name in ("K", "V", "score", "pos", "occ", "kq", "ks", "vq", "vs"):
+            if hasattr(self, name):
+                setattr(s, name, getattr(self, name).copy())
         return s
 
 
@@ -155,7 +157,53 @@ def h2o_decode_step(st, q, k, v, p, r, scale, forced=None):
     lib().oracle_h2o_decode_step(U, d, st.B, r, float(scale), int(p), st.K, st.V,
                                  st.score, st.pos, st.occ, q, k, v, out,
                                  _ptr(victim), _ptr(margin), _ptr(evicted), _ptr(f))
+    if hasattr(st, "kq"):
+        # int8 cache: the step attended to the new token at full precision;
+        # the slot it now occupies stores the quantised row
+        _kv8_written(st, _written_slots(victim, st.occ))
     return out, victim, margin, evicted
+
+
+def quantize_rows(X):
+    """int8 codes [..., d] and fp32 scales [...] of every row of X (values
+    exactly representable in fp32)."""
+    X = _c64(X)
+    flat = X.reshape(-1, X.shape[-1])
+    code = np.empty(flat.shape, dtype=np.int8)
+    scale = np.empty(flat.shape[0], dtype=np.float32)
+    lib().oracle_quantize_rows(flat.shape[0], flat.shape[1], flat, code.ctypes.data_as(ctypes.c_void_p), scale)
+    return code.reshape(X.shape), scale.reshape(X.shape[:-1])
+
+
+def dequantize(code, scale):
+    """code * scale, exactly, as float64."""
+    return code.astype(np.float64) * scale.astype(np.float64)[..., None]
+
+
+def kv8(st):
+    """Turn a freshly built cache (exact rows) into an int8 cache: every
+    row is quantised, its codes and scales kept on the state, and the rows
+    the arithmetic reads become the dequantised values."""
+    st.kq, st.ks = quantize_rows(st.K)
+    st.vq, st.vs = quantize_rows(st.V)
+    st.K = dequantize(st.kq, st.ks)
+    st.V = dequantize(st.vq, st.vs)
+    return st
+
+
+def _kv8_written(st, slots):
+    """Quantise the row each unit's step wrote (slots[u], exact values)."""
+    for u, s in enumerate(slots):
+        kq, ks = quantize_rows(st.K[u, s][None])
+        vq, vs = quantize_rows(st.V[u, s][None])
+        st.kq[u, s], st.ks[u, s] = kq[0], ks[0]
+        st.vq[u, s], st.vs[u, s] = vq[0], vs[0]
+        st.K[u, s] = dequantize(kq, ks)[0]
+        st.V[u, s] = dequantize(vq, vs)[0]
+
+
+def _written_slots(victim, occ_after):
+    return [int(v) if v >= 0 else int(o) - 1 for v, o in zip(victim, occ_after)]
 
 
 def lsh_code(x, W):
@@ -202,4 +250,6 @@ def lsh_decode_step(st, q, k, v, W, p, r, scale):
     victim = np.empty(U, dtype=np.int32)
     lib().oracle_lsh_decode_step(U, d, st.B, r, float(scale), int(p), st.K, st.V,
                                  st.code, st.pos, st.occ, q, k, v, W, out, _ptr(victim))
+    if hasattr(st, "kq"):
+        _kv8_written(st, _written_slots(victim, st.occ))
     return out, victim

@@ -52,7 +52,12 @@
  *    replacement rule token by token; the LSH step evicts and inserts
  *    first and then attends over the budget (the victim is not attended);
  *  - if no slot is an eviction candidate (possible only for a state that
- *    breaks the recent-window invariant), every live slot is a candidate.
+ *    breaks the recent-window invariant), every live slot is a candidate;
+ *  - int8 cache slots (an optional mode): each stored K or V row keeps int8
+ *    codes and one fp32 scale, amax/127, with codes rint(x * (127/amax))
+ *    in fp32, half to even; a step attends to its own new token at full
+ *    precision and stores it quantised (the quantiser is below; the mode's
+ *    bookkeeping is in the Python wrapper).
  *
  * parity unpinned: the readings above that have no printed example on the
  * pages (self-attention of the new token, accumulate-before-evict order,
@@ -338,6 +343,45 @@ void oracle_h2o_decode_step(int U, int d, int B, int r, double scale, int p,
         su[slot] = P_new;
         pu[slot] = p;
         free(z);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* int8 cache slots with one fp32 scale per row [SH abstract: a        */
+/* budgeted cache combines with 4-bit quantisation of its entries; the  */
+/* int8 form and its rounding are readings, listed in the design notes]:*/
+/*   amax = max_e |x_e|                                  (exact, fp32)   */
+/*   amax == 0:  scale = 0 and every code is 0                           */
+/*   otherwise:  inv = 127 / amax                     (fp32, rounded)   */
+/*               code_e = rint(x_e * inv), clamped to [-127, 127]        */
+/*                        (fp32 product; rint rounds half to even)       */
+/*               scale = amax / 127                    (fp32, rounded)   */
+/* A stored row reads back as code_e * scale.  X holds n rows of d      */
+/* values, each exactly representable in fp32.                          */
+/* ------------------------------------------------------------------ */
+void oracle_quantize_rows(int n, int d, const double* X, signed char* code, float* scale)
+{
+    for (int t = 0; t < n; ++t) {
+        const double* x = X + (size_t)t * d;
+        signed char* c = code + (size_t)t * d;
+        float amax = 0.0f;
+        for (int e = 0; e < d; ++e) {
+            float a = fabsf((float)x[e]);
+            if (a > amax) amax = a;
+        }
+        if (amax == 0.0f) {
+            for (int e = 0; e < d; ++e) c[e] = 0;
+            scale[t] = 0.0f;
+            continue;
+        }
+        float inv = 127.0f / amax;
+        for (int e = 0; e < d; ++e) {
+            float y = rintf((float)x[e] * inv);
+            if (y > 127.0f) y = 127.0f;
+            if (y < -127.0f) y = -127.0f;
+            c[e] = (signed char)y;
+        }
+        scale[t] = amax / 127.0f;
     }
 }
 

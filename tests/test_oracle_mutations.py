@@ -39,6 +39,9 @@ MUTATIONS = {
     "lsh_ties_to_higher": ("if (dist > bestd) { bestd = dist; best = s; }",
                            "if (dist >= bestd) { bestd = dist; best = s; }"),
     "lsh_window_ignored": ("if (ncand > 0 && !(pos[s] <= p - r)) continue;", ""),
+    "kv8_ties_away_from_zero": ("float y = rintf((float)x[e] * inv);", "float y = roundf((float)x[e] * inv);"),
+    "kv8_scale_over_128": ("scale[t] = amax / 127.0f;", "scale[t] = amax / 128.0f;"),
+    "kv8_inverse_from_128": ("float inv = 127.0f / amax;", "float inv = 128.0f / amax;"),
 }
 
 

@@ -400,3 +400,80 @@ def test_decode_exact_tie_goes_to_lowest_slot():
     assert vic[0] == 0 and mg[0] == 0.0
     assert ev[0] == pytest.approx(0.7, rel=1e-15)
     assert st.pos[0].tolist() == [6, 2, 3, 5]
+
+
+# ------------------------------------------------------------ int8 slots ---
+
+def test_quantize_hand_worked():
+    g = _golden("quantize_rows.json")
+    code, scale = oracle.quantize_rows(np.array(g["x"], float))
+    assert code.tolist() == g["code"]
+    want = [np.float32(n) / np.float32(g["scale_den"]) for n in g["scale_num"]]
+    assert scale.tolist() == [float(w) for w in want]
+
+
+def test_quantize_round_trip_bound_and_symmetry():
+    rng = np.random.default_rng(41)
+    X = (rng.standard_normal((200, 128)) * rng.uniform(0.01, 50, (200, 1))).astype(np.float32).astype(float)
+    code, scale = oracle.quantize_rows(X)
+    err = np.abs(X - oracle.dequantize(code, scale))
+    s = scale.astype(float)[:, None]
+    # half a step, plus the rounding of the fp32 inverse and scale
+    assert (err <= 0.5 * s * (1 + 1e-5) + 1e-30).all()
+    # the largest magnitude of each row maps to +-127
+    top = np.abs(X).argmax(axis=1)
+    assert (np.abs(code[np.arange(200), top]) == 127).all()
+    assert (np.abs(code) <= 127).all()
+    code_n, scale_n = oracle.quantize_rows(-X)
+    assert (code_n == -code).all() and (scale_n == scale).all()
+
+
+def _exact_rows(rng, shape):
+    """Integer rows in [-127, 127] whose largest magnitude is 127: the int8
+    form stores them exactly (scale 1)."""
+    x = rng.integers(-126, 127, size=shape).astype(float)
+    x[..., 0] = np.where(rng.random(shape[:-1]) < 0.5, 127.0, -127.0)
+    return x
+
+
+def test_kv8_exact_rows_reproduce_full_precision():
+    rng = np.random.default_rng(42)
+    U, T, S, d, B, H, r, scale = 3, 24, 10, 8, 8, 4, 4, 1e-3
+    Q, K, V = (_exact_rows(rng, (U, T, d)) for _ in range(3))
+    q, k, v = (_exact_rows(rng, (S, U, d)) for _ in range(3))
+    st, _, _, _ = oracle.h2o_prefill(Q, K, V, B, H, r, scale)
+    st8 = oracle.kv8(st.copy())
+    assert (st8.ks[st8.pos >= 0] == 1.0).all()
+    for t in range(S):
+        o, vic, _, _ = oracle.h2o_decode_step(st, q[t], k[t], v[t], T + t, r, scale)
+        o8, vic8, _, _ = oracle.h2o_decode_step(st8, q[t], k[t], v[t], T + t, r, scale)
+        assert (vic == vic8).all() and (o == o8).all()
+        assert (st.K == st8.K).all() and (st.score == st8.score).all()
+    W = rng.standard_normal((d, 32)).astype(np.float32)
+    ls = oracle.lsh_prefill(Q, K, V, W, B, r)
+    ls8 = oracle.kv8(oracle.lsh_prefill(Q, K, V, W, B, r))
+    for t in range(S):
+        o, vic = oracle.lsh_decode_step(ls, q[t], k[t], v[t], W, T + t, r, scale)
+        o8, vic8 = oracle.lsh_decode_step(ls8, q[t], k[t], v[t], W, T + t, r, scale)
+        assert (vic == vic8).all() and (o == o8).all() and (ls.V == ls8.V).all()
+
+
+def test_kv8_step_attends_new_token_exactly_and_stores_it_quantised():
+    rng = np.random.default_rng(43)
+    U, T, d, B, H, r, scale = 2, 30, 16, 10, 5, 5, 0.3
+    Q, K, V = (rng.standard_normal((U, T, d)).astype(np.float32).astype(float) for _ in range(3))
+    q, k, v = (rng.standard_normal((U, d)).astype(np.float32).astype(float) for _ in range(3))
+    st = oracle.kv8(oracle.h2o_prefill(Q, K, V, B, H, r, scale)[0])
+    Kc, Vc = st.K.copy(), st.V.copy()                     # dequantised rows
+    assert np.array_equal(Kc, st.kq.astype(float) * st.ks.astype(float)[..., None])
+    out, vic, _, _ = oracle.h2o_decode_step(st, q, k, v, T, r, scale)
+    for u in range(U):
+        keys = np.concatenate([Kc[u], k[u][None]]); vals = np.concatenate([Vc[u], v[u][None]])
+        z = scale * keys @ q[u]
+        e = np.exp(z - z.max())
+        np.testing.assert_allclose(out[u], (e / e.sum()) @ vals, rtol=0, atol=1e-12)
+        s = vic[u]
+        kq, ks = oracle.quantize_rows(k[u][None])
+        assert (st.kq[u, s] == kq[0]).all() and st.ks[u, s] == ks[0]
+        others = [x for x in range(B) if x != s]
+        assert (st.K[u, others] == Kc[u, others]).all()
