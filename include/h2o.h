@@ -69,10 +69,25 @@ typedef enum {
 enum { H2O_F32 = 0, H2O_BF16 = 1 };
 
 /*
+ * H2O_KV8 -- OR into dtype (H2O_BF16 | H2O_KV8, H2O_F32 | H2O_KV8) to store
+ * the cache's K and V rows as int8 codes with one fp32 scale per row
+ * [SH abstract: a budgeted cache combines with quantisation of its
+ * entries; the int8 form is this library's reading].  Inputs keep their
+ * type.  A row x is stored as amax = max|x_e|, scale = amax / 127 and
+ * code_e = rint(x_e * (127 / amax)) (fp32 arithmetic, half to even, within
+ * +-127; all zero when amax = 0), and reads back as code_e * scale.  A
+ * decode step attends to its own new token at full precision and then
+ * stores it quantised.  Eviction, scores and codes follow the same rules
+ * as without the flag.  The paper has no counterpart for the flag itself.
+ */
+enum { H2O_KV8 = 2 };
+
+/*
  * h2o_init -- create an H2O cache handle [H2O 提案手法; FG Figure 2; SH].
  *   budget = B slots per unit (>= 1), heavy = H heavy-hitter slots,
  *   recent = r recent-window slots; heavy + recent must equal budget.
- *   batch, heads >= 1; head_dim in {64, 128}; dtype H2O_F32 or H2O_BF16;
+ *   batch, heads >= 1; head_dim in {64, 128}; dtype H2O_F32 or H2O_BF16,
+ *   optionally | H2O_KV8;
  *   scale > 0 is the softmax scale (usually 1/sqrt(head_dim)).
  *   cuda_stream: the cudaStream_t to enqueue on (NULL = legacy stream).
  * On success *out holds the handle; destroy it with h2o_destroy.
@@ -148,7 +163,8 @@ int lsh_decode_step(h2o_handle h, const void* q, const void* k, const void* v,
 
 /*
  * h2o_get_state -- copy the cache to HOST buffers (any pointer may be NULL):
- *   K, V [U][B][d] of the handle's dtype; score fp64 [U][B] (H2O handles;
+ *   K, V [U][B][d] of the handle's dtype (int8 codes for H2O_KV8 handles,
+ *   whose scales h2o_get_kv_scales returns); score fp64 [U][B] (H2O handles;
  *   zeros for LSH); pos int32 [U][B]; code uint32 [U][B] (LSH handles;
  *   zeros for H2O); occupancy int32 [U]; next_pos int32 [U].
  * Waits for the handle's stream.
@@ -164,6 +180,16 @@ int h2o_get_state(h2o_handle h, void* K, void* V, double* score, int* pos, unsig
 int h2o_set_state(h2o_handle h, const void* K, const void* V, const double* score,
                   const int* pos, const unsigned* code, const int* occupancy,
                   const int* next_pos);
+
+/*
+ * h2o_get_kv_scales / h2o_set_kv_scales -- the fp32 K and V row scales
+ * [U][B] of an H2O_KV8 handle, to / from HOST buffers (get: either may be
+ * NULL; set: both required).  H2O_ERR_STATE on a handle without H2O_KV8.
+ * Both wait for the handle's stream.  The int8 cache is this library's
+ * reading of the quantised budgeted cache (see H2O_KV8).
+ */
+int h2o_get_kv_scales(h2o_handle h, float* kscale, float* vscale);
+int h2o_set_kv_scales(h2o_handle h, const float* kscale, const float* vscale);
 
 /*
  * h2o_get_prefill_stats -- copy the last h2o_prefill's prompt statistics to

@@ -25,6 +25,7 @@ H2O_ERR_DEVICE_TIMEOUT = -5
 H2O_ERR_UNSUPPORTED = -6
 H2O_F32 = 0
 H2O_BF16 = 1
+H2O_KV8 = 2
 
 # every symbol include/h2o.h declares, with (restype, argtypes)
 _vp = ctypes.c_void_p
@@ -40,6 +41,8 @@ SIGNATURES = {
     "h2o_get_state": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "h2o_set_state": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "h2o_get_prefill_stats": (_i, [_vp, _vp, _vp, _vp]),
+    "h2o_get_kv_scales": (_i, [_vp, _vp, _vp]),
+    "h2o_set_kv_scales": (_i, [_vp, _vp, _vp]),
     "h2o_set_stream": (_i, [_vp, _vp]),
     "h2o_set_decode_split": (_i, [_vp, _i]),
     "h2o_sync": (_i, [_vp]),
@@ -149,6 +152,14 @@ def h2o_set_state(h, K=None, V=None, score=None, pos=None, code=None, occupancy=
 
 def h2o_get_prefill_stats(h, m=None, l=None, c=None):
     _check(lib().h2o_get_prefill_stats(h, _ptr(m), _ptr(l), _ptr(c)))
+
+
+def h2o_get_kv_scales(h, kscale=None, vscale=None):
+    _check(lib().h2o_get_kv_scales(h, _ptr(kscale), _ptr(vscale)))
+
+
+def h2o_set_kv_scales(h, kscale, vscale):
+    _check(lib().h2o_set_kv_scales(h, _ptr(kscale), _ptr(vscale)))
 
 
 def h2o_set_stream(h, stream):

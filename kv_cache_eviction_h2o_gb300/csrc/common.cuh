@@ -229,6 +229,38 @@ __device__ __forceinline__ void prefetch_l1(const void* p)
 
 // Cheapest proxy fence that makes mbarrier initialisation visible to the
 // bulk-copy engine of this CTA.
+// ------------------------------------------------------------ int8 rows
+// A cache row x is stored as int8 codes with one fp32 scale: amax = max|x|,
+// inv = 127 / amax (0 when amax = 0), code = rint(x * inv) within +-127
+// (fp32 product, half to even), scale = amax / 127.  IEEE division and a
+// separate product keep the codes identical on every correct fp32 path.
+__device__ __forceinline__ float q8_inv(float amax) { return amax > 0.f ? __fdiv_rn(127.f, amax) : 0.f; }
+__device__ __forceinline__ float q8_scale(float amax) { return __fdiv_rn(amax, 127.f); }
+
+__device__ __forceinline__ uint32_t q8_code(float x, float inv)
+{
+    int c = __float2int_rn(__fmul_rn(x, inv));
+    c = max(-127, min(127, c));
+    return (uint32_t)c & 0xffu;
+}
+
+// Four fp32 values -> four int8 codes packed little-endian.
+__device__ __forceinline__ uint32_t q8_pack4(const float* x, float inv)
+{
+    return q8_code(x[0], inv) | (q8_code(x[1], inv) << 8) | (q8_code(x[2], inv) << 16) | (q8_code(x[3], inv) << 24);
+}
+
+// Four int8 codes (little-endian in w) -> fp32, exactly: each biased byte
+// becomes the low mantissa byte of 2^23, and the bias is subtracted.
+__device__ __forceinline__ void q8_unpack4(uint32_t w, float* f)
+{
+    const uint32_t x = w ^ 0x80808080u;
+    f[0] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540)) - 8388736.f;
+    f[1] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7541)) - 8388736.f;
+    f[2] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7542)) - 8388736.f;
+    f[3] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7543)) - 8388736.f;
+}
+
 // Named CTA barriers (ids 1..15; id 0 is __syncthreads).  Memory
 // accesses made before the arrive are visible to the threads that pass the
 // sync.  The id is an immediate in the instruction (a register id makes the

@@ -26,6 +26,7 @@
 #include <cfloat>
 #include <climits>
 #include <cstdlib>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -71,10 +72,14 @@ struct Exchange {                 // every CTA has one; rank 0's is the meeting 
     float o[kMaxSplit][D];        // per-CTA unnormalised output
 };
 
-template <typename T, int D, class TL>
+// Element a cache row is stored in: the input type, or int8 codes (Q8).
+template <typename T, bool Q8>
+using CacheElem = typename std::conditional<Q8, int8_t, T>::type;
+
+template <typename T, int D, class TL, bool Q8>
 struct Ring {
-    T kbuf[TL::NW][TL::NBUF][kStage * D];   // per-warp ring of K rows
-    T vbuf[TL::NW][TL::NBUF][kStage * D];   // per-warp ring of V rows
+    CacheElem<T, Q8> kbuf[TL::NW][TL::NBUF][kStage * D];   // per-warp ring of K rows
+    CacheElem<T, Q8> vbuf[TL::NW][TL::NBUF][kStage * D];   // per-warp ring of V rows
 };
 
 template <int D, class TL>
@@ -83,14 +88,16 @@ struct Epilogue {
     float wo[TL::NW][D];
 };
 
-template <typename T, int D, class TL>
+template <typename T, int D, class TL, bool Q8>
 struct DecodeSmem {
     // the epilogue buffers reuse the ring once every copy has landed and
     // been consumed (after the barrier that opens merge_warps)
     union {
-        Ring<T, D, TL> ring;
+        Ring<T, D, TL, Q8> ring;
         Epilogue<D, TL> epi;
     } u;
+    // Q8: {K scale, V scale} of every slot of a ring stage
+    alignas(16) float2 sbuf[Q8 ? TL::NW : 1][TL::NBUF][kStage];
     uint64_t bar[TL::NW][TL::NBUF];
     float z[kMaxChunk];                     // base-2 logits of this CTA's slots
     alignas(16) float e[TL::NW][kStage];
@@ -251,6 +258,140 @@ __device__ __forceinline__ float row_dot(const E* row, const float (&qp)[D / 2],
     return zh + __shfl_xor_sync(kFull, zh, 16);
 }
 
+// int8 rows (Q8): a row of D codes is D / 16 chunks of 16.  Lane (r, h)
+// takes half hh = h ^ ((r / HCH) & 1) of row r -- the halves swap every HCH
+// rows -- and at step c reads chunk HCH * hh + (c ^ (r % HCH)), so the 8
+// lanes of one 16-byte shared-memory phase hit 8 different bank groups
+// although every 128-byte row starts in the same one.  q is held in the
+// same order, scaled to base-2 logits.
+template <int D>
+__device__ __forceinline__ int q8_chunk(int lane, int c)
+{
+    constexpr int HCH = D / 32;
+    const int r = lane & 15, h = lane >> 4;
+    const int hh = h ^ ((r / HCH) & 1);
+    return HCH * hh + (c ^ (r % HCH));
+}
+
+template <typename T, int D>
+__device__ __forceinline__ void load_q_q8(const T* q, float scale, int lane, float (&qp)[D / 2])
+{
+    constexpr int HCH = D / 32, VE = 16 / (int)sizeof(T);
+#pragma unroll
+    for (int c = 0; c < HCH; ++c) {
+        const T* src = q + q8_chunk<D>(lane, c) * 16;
+#pragma unroll
+        for (int v = 0; v < 16; v += VE) load_vec<T, VE>(src + v, &qp[c * 16 + v]);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) qp[c * 16 + e] *= scale;
+    }
+}
+
+// Dot of an int8 row (codes, unscaled) with the lane's half of q; every
+// lane returns the full dot of its row.
+template <int D>
+__device__ __forceinline__ float row_dot_q8(const int8_t* row, const float (&qp)[D / 2], int lane)
+{
+    constexpr int HCH = D / 32;
+    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                     make_float2(0.f, 0.f)};
+    uint4 raw[HCH];
+#pragma unroll
+    for (int c = 0; c < HCH; ++c) raw[c] = *reinterpret_cast<const uint4*>(row + q8_chunk<D>(lane, c) * 16);
+#pragma unroll
+    for (int c = 0; c < HCH; ++c) {
+        const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float f[4];
+            q8_unpack4(u[i], f);
+            const int e = c * 16 + 4 * i;
+            acc[(2 * i) & 3] = fma2(make_float2(qp[e], qp[e + 1]), make_float2(f[0], f[1]), acc[(2 * i) & 3]);
+            acc[(2 * i + 1) & 3] = fma2(make_float2(qp[e + 2], qp[e + 3]), make_float2(f[2], f[3]), acc[(2 * i + 1) & 3]);
+        }
+    }
+    const float zh = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+    return zh + __shfl_xor_sync(kFull, zh, 16);
+}
+
+// Dot of a row of T (the new token's key, in global memory) with q held in
+// the int8 order.
+template <typename T, int D>
+__device__ __forceinline__ float row_dot_q8order(const T* row, const float (&qp)[D / 2], int lane)
+{
+    constexpr int HCH = D / 32, VE = 16 / (int)sizeof(T);
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < HCH; ++c) {
+        const T* src = row + q8_chunk<D>(lane, c) * 16;
+#pragma unroll
+        for (int v = 0; v < 16; v += VE) {
+            float x[VE];
+            load_vec<T, VE>(src + v, x);
+#pragma unroll
+            for (int e = 0; e < VE; ++e) acc = __fmaf_rn(qp[c * 16 + v + e], x[e], acc);
+        }
+    }
+    return acc + __shfl_xor_sync(kFull, acc, 16);
+}
+
+// The new token's row, held as 16 bytes of T by threads tid < 2 * NV (K rows
+// first, then V), stored quantised into slot `victim`: the NV threads of a
+// row form an aligned lane group, which reduces the row's max magnitude.
+// Every lane of the calling warps must take part (shuffles).
+template <typename T, int D>
+__device__ __forceinline__ void store_row_q8(uint4 newrow, int tid, int8_t* Kc8, int8_t* Vc8, float2* slot_scales,
+                                             int victim)
+{
+    constexpr int NV = D * (int)sizeof(T) / 16, VE = 16 / (int)sizeof(T);
+    static_assert(NV <= 32, "a row's threads must fit one warp");
+    float x[VE];
+    const uint32_t u[4] = {newrow.x, newrow.y, newrow.z, newrow.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (sizeof(T) == 2) {
+            x[2 * i] = __uint_as_float(u[i] << 16);
+            x[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+        } else {
+            x[i] = __uint_as_float(u[i]);
+        }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < VE; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+    for (int o = NV / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+    const float inv = q8_inv(amax);
+    if (tid < 2 * NV) {
+        const bool isv = tid >= NV;
+        const int v = isv ? tid - NV : tid;
+        int8_t* dst = (isv ? Vc8 : Kc8) + (size_t)victim * D + v * VE;
+        if constexpr (VE == 8)
+            *reinterpret_cast<uint2*>(dst) = make_uint2(q8_pack4(&x[0], inv), q8_pack4(&x[4], inv));
+        else
+            *reinterpret_cast<uint32_t*>(dst) = q8_pack4(&x[0], inv);
+        if (v == 0) reinterpret_cast<float*>(slot_scales + victim)[isv ? 1 : 0] = q8_scale(amax);
+    }
+}
+
+// Bulk copies of one stage (slots s .. min(s + 16, f1) - 1) into this warp's
+// ring buffer b: K and V rows and, for int8 rows, the slots' scale pairs
+// (an even count, so the copy stays a multiple of 16 bytes; the scale rows
+// are padded to an even length).
+template <typename T, int D, class TL, bool Q8>
+__device__ __forceinline__ void issue_stage(DecodeSmem<T, D, TL, Q8>& S, const CacheElem<T, Q8>* Kc,
+                                            const CacheElem<T, Q8>* Vc, const float2* Sc, int s, int f1, int b)
+{
+    const int warp = threadIdx.x >> 5;
+    const int rows = min(kStage, f1 - s);
+    const uint32_t bytes = (uint32_t)(rows * D * sizeof(CacheElem<T, Q8>));
+    const uint32_t sbytes = Q8 ? (uint32_t)(((rows + 1) & ~1) * sizeof(float2)) : 0u;
+    mbar_arrive_expect_tx(&S.bar[warp][b], 2 * bytes + sbytes);
+    bulk_g2s(S.u.ring.kbuf[warp][b], Kc + (size_t)s * D, bytes, &S.bar[warp][b]);
+    bulk_g2s(S.u.ring.vbuf[warp][b], Vc + (size_t)s * D, bytes, &S.bar[warp][b]);
+    if constexpr (Q8) bulk_g2s(S.sbuf[warp][b], Sc + s, sbytes, &S.bar[warp][b]);
+}
+
 // Per-warp streaming softmax over the rows this CTA fetched, [f0, f1); only
 // slots < n are live and `skip` (absolute slot) is left out.  When keep_z,
 // logits go to S.z[slot - f0].  The warp keeps one reference max m_ref and
@@ -258,8 +399,9 @@ __device__ __forceinline__ float row_dot(const E* row, const float (&qp)[D / 2],
 // 2^8), so most stages need no cross-lane max.  l_lane is this lane's share
 // of the normaliser (lanes 0..15 count their slot once); o holds the lane's
 // EPL output columns lane*EPL.. of the unnormalised sum, relative to m_ref.
-template <typename T, int D, class TL>
-__device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL>& S, const T* Kc, const T* Vc,
+template <typename T, int D, class TL, bool Q8>
+__device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, Q8>& S, const CacheElem<T, Q8>* Kc,
+                                             const CacheElem<T, Q8>* Vc, const float2* Sc,
                                              int f0, int f1, int n, int skip, bool keep_z,
                                              const float (&qp)[D / 2], float& m_ref,
                                              float& l_lane, float (&o)[D / 32], int* err)
@@ -281,9 +423,11 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL>& S, const T* K
         const int s0 = g * kStage;                 // fetch-relative first slot
         const int gl = max(0, min(kStage, n - (f0 + s0)));   // live rows of this stage
         if (gl > 0) {
-            const T* kst = S.u.ring.kbuf[warp][b];
-            const T* vst = S.u.ring.vbuf[warp][b];
-            float z = row_dot<T, D, T>(kst + r * D, qp, lane);
+            const auto* kst = S.u.ring.kbuf[warp][b];
+            const auto* vst = S.u.ring.vbuf[warp][b];
+            float z;
+            if constexpr (Q8) z = row_dot_q8<D>(kst + r * D, qp, lane) * S.sbuf[warp][b][r].x;
+            else z = row_dot<T, D, T>(kst + r * D, qp, lane);
             if (r >= gl || f0 + s0 + r == skip) z = -INFINITY;
             if (__any_sync(kFull, z > m_ref + 8.f)) {
                 float zm = z;
@@ -308,6 +452,27 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL>& S, const T* K
                 const float4 e4 = *reinterpret_cast<const float4*>(&S.e[warp][j]);
                 ev[j] = e4.x; ev[j + 1] = e4.y; ev[j + 2] = e4.z; ev[j + 3] = e4.w;
             }
+            if constexpr (Q8) {
+                // int8 values: the slot's V scale folds into its weight
+                for (int j = 0; j < kStage; ++j) {
+                    if (j < gl) {
+                        float vr[4];
+                        if constexpr (EPL == 4) {
+                            q8_unpack4(*reinterpret_cast<const uint32_t*>(vst + j * D + lane * EPL), vr);
+                        } else {
+                            q8_unpack4((uint32_t)*reinterpret_cast<const uint16_t*>(vst + j * D + lane * EPL), vr);
+                        }
+                        const float w = ev[j] * S.sbuf[warp][b][j].y;
+                        const float2 pj = make_float2(w, w);
+#pragma unroll
+                        for (int e = 0; e < EPL; e += 2) {
+                            const float2 acc = fma2(pj, make_float2(vr[e], vr[e + 1]), make_float2(o[e], o[e + 1]));
+                            o[e] = acc.x;
+                            o[e + 1] = acc.y;
+                        }
+                    }
+                }
+            } else {
             using RV = typename RawT<EPL * sizeof(T)>::type;
             if (gl == kStage) {
                 // a full stage: each half's value fragments are loaded before
@@ -348,18 +513,13 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL>& S, const T* K
                     }
                 }
             }
+            }
             __syncwarp();
         }
         // refill this buffer with the warp's stage NBUF rounds ahead
         if (lane == 0) {
             const int gn = g + NW * NBUF;
-            if (gn < nst) {
-                const int s = f0 + gn * kStage;
-                const uint32_t bytes = (uint32_t)(min(kStage, f1 - s) * D * sizeof(T));
-                mbar_arrive_expect_tx(&S.bar[warp][b], 2 * bytes);
-                bulk_g2s(S.u.ring.kbuf[warp][b], Kc + (size_t)s * D, bytes, &S.bar[warp][b]);
-                bulk_g2s(S.u.ring.vbuf[warp][b], Vc + (size_t)s * D, bytes, &S.bar[warp][b]);
-            }
+            if (gn < nst) issue_stage<T, D, TL, Q8>(S, Kc, Vc, Sc, f0 + gn * kStage, f1, b);
         }
     }
 }
@@ -367,8 +527,9 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL>& S, const T* K
 // Kick off ring buffers [b_lo, b_hi) of each warp -- by default all NBUF --
 // with their first stages (called by lane 0 of every warp after its barriers
 // are initialised).
-template <typename T, int D, class TL>
-__device__ __forceinline__ void prime_ring(DecodeSmem<T, D, TL>& S, const T* Kc, const T* Vc,
+template <typename T, int D, class TL, bool Q8>
+__device__ __forceinline__ void prime_ring(DecodeSmem<T, D, TL, Q8>& S, const CacheElem<T, Q8>* Kc,
+                                           const CacheElem<T, Q8>* Vc, const float2* Sc,
                                            int c0, int c1, int b_lo = 0, int b_hi = TL::NBUF)
 {
     const int warp = threadIdx.x >> 5;
@@ -377,19 +538,13 @@ __device__ __forceinline__ void prime_ring(DecodeSmem<T, D, TL>& S, const T* Kc,
     for (int b = 0; b < TL::NBUF; ++b) {
         if (b < b_lo || b >= b_hi) continue;
         const int g = warp + TL::NW * b;
-        if (g < nst) {
-            const int s = c0 + g * kStage;
-            const uint32_t bytes = (uint32_t)(min(kStage, c1 - s) * D * sizeof(T));
-            mbar_arrive_expect_tx(&S.bar[warp][b], 2 * bytes);
-            bulk_g2s(S.u.ring.kbuf[warp][b], Kc + (size_t)s * D, bytes, &S.bar[warp][b]);
-            bulk_g2s(S.u.ring.vbuf[warp][b], Vc + (size_t)s * D, bytes, &S.bar[warp][b]);
-        }
+        if (g < nst) issue_stage<T, D, TL, Q8>(S, Kc, Vc, Sc, c0 + g * kStage, c1, b);
     }
 }
 
 // Merge the warps' softmax states; threads < D get their output column.
-template <typename T, int D, class TL>
-__device__ __forceinline__ void merge_warps(DecodeSmem<T, D, TL>& S, float m_run, float l_run,
+template <typename T, int D, class TL, bool Q8>
+__device__ __forceinline__ void merge_warps(DecodeSmem<T, D, TL, Q8>& S, float m_run, float l_run,
                                             const float (&o)[D / 32], float& Mc, float& Lc,
                                             float& Oc)
 {
@@ -438,11 +593,11 @@ __device__ __forceinline__ void fetch_range(int B, int C, int rank, int& f0, int
 
 // ------------------------------------------------------------------ H2O
 
-template <typename T, int D, class TL>
+template <typename T, int D, class TL, bool Q8>
 __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const DecodeArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    auto& S = *reinterpret_cast<DecodeSmem<T, D, TL>*>(smem_raw);
+    auto& S = *reinterpret_cast<DecodeSmem<T, D, TL, Q8>*>(smem_raw);
     constexpr int EPL = D / 32;
     constexpr int NV = D * (int)sizeof(T) / 16;          // 16-byte vectors per row
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -453,8 +608,10 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
 
     const int B = c.B;
     const size_t ub = (size_t)unit * B;
-    T* Kc = reinterpret_cast<T*>(c.K) + ub * D;
-    T* Vc = reinterpret_cast<T*>(c.V) + ub * D;
+    using CE = CacheElem<T, Q8>;
+    CE* Kc = reinterpret_cast<CE*>(c.K) + ub * D;
+    CE* Vc = reinterpret_cast<CE*>(c.V) + ub * D;
+    float2* Sc = Q8 ? c.kvs + (size_t)unit * c.Bp : nullptr;   // slot scale pairs
     int f0, f1;
     fetch_range(B, C, rank, f0, f1);
     if (lane == 0) {
@@ -484,7 +641,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     // query row, requested right after the wait, then queues behind less
     // traffic, and the remaining buffers keep HBM busy while it is in flight.
     if (a.early) {
-        if (lane == 0) prime_ring<T, D, TL>(S, Kc, Vc, f0, f1, 0, 1);
+        if (lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, 0, 1);
         read_cache();
     }
     // everything below may read memory the previous kernel in the stream
@@ -492,20 +649,21 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     grid_dependency_wait();
     grid_launch_dependents();
     if (!a.early) {
-        if (lane == 0) prime_ring<T, D, TL>(S, Kc, Vc, f0, f1);
+        if (lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1);
         read_cache();
     }
+    float qp[D / 2];
     QRaw<T, D> qraw;
-    load_q_raw<T, D>(reinterpret_cast<const T*>(a.q) + (size_t)unit * D, lane, qraw);
-    if (a.early && lane == 0) prime_ring<T, D, TL>(S, Kc, Vc, f0, f1, 1, TL::NBUF);
+    if constexpr (Q8) load_q_q8<T, D>(reinterpret_cast<const T*>(a.q) + (size_t)unit * D, c.qscale, lane, qp);
+    else load_q_raw<T, D>(reinterpret_cast<const T*>(a.q) + (size_t)unit * D, lane, qraw);
+    if (a.early && lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, 1, TL::NBUF);
     const T* kg = reinterpret_cast<const T*>(a.k) + (size_t)unit * D;
     const T* vg = reinterpret_cast<const T*>(a.v) + (size_t)unit * D;
     // the new token's row, written into the victim slot at the end
     uint4 newrow = make_uint4(0u, 0u, 0u, 0u);
     if (rank == 0 && tid < 2 * NV)
         newrow = tid < NV ? reinterpret_cast<const uint4*>(kg)[tid] : reinterpret_cast<const uint4*>(vg)[tid - NV];
-    float qp[D / 2];
-    widen_q<T, D>(qraw, c.qscale, qp);
+    if constexpr (!Q8) widen_q<T, D>(qraw, c.qscale, qp);
 
     const int n = us.x, p = us.y;
     const bool full = (n >= B);
@@ -516,7 +674,9 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     for (int e = 0; e < EPL; ++e) o[e] = 0.f;
     if (rank == 0 && warp == 0) {          // the new token attends to itself
         float vr[EPL];
-        const float zn = row_dot<T, D, T>(kg, qp, lane);
+        float zn;
+        if constexpr (Q8) zn = row_dot_q8order<T, D>(kg, qp, lane);
+        else zn = row_dot<T, D, T>(kg, qp, lane);
         load_vec<T, EPL>(vg + lane * EPL, vr);
         m_run = zn;
         l_run = lane == 0 ? 1.f : 0.f;
@@ -526,10 +686,10 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     }
     __syncwarp();
 
-    attend_chunk<T, D, TL>(S, Kc, Vc, f0, f1, n, -1, true, qp, m_run, l_run, o, c.err);
+    attend_chunk<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, n, -1, true, qp, m_run, l_run, o, c.err);
 
     float Mc, Lc, Oc;
-    merge_warps<T, D, TL>(S, m_run, l_run, o, Mc, Lc, Oc);
+    merge_warps<T, D, TL, Q8>(S, m_run, l_run, o, Mc, Lc, Oc);
 
     // exchange 1: (max, normaliser, output) of every CTA into rank 0; a
     // single-CTA unit already has them
@@ -608,10 +768,14 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
             c.ustate[unit] = make_int2(min(n + 1, B), p + 1);
             if (a.victim_out) a.victim_out[unit] = full ? victim : -1;
         }
-        if (tid < NV)
-            reinterpret_cast<uint4*>(Kc + (size_t)victim * D)[tid] = newrow;
-        else if (tid < 2 * NV)
-            reinterpret_cast<uint4*>(Vc + (size_t)victim * D)[tid - NV] = newrow;
+        if constexpr (Q8) {
+            store_row_q8<T, D>(newrow, tid, Kc, Vc, Sc, victim);
+        } else {
+            if (tid < NV)
+                reinterpret_cast<uint4*>(Kc + (size_t)victim * D)[tid] = newrow;
+            else if (tid < 2 * NV)
+                reinterpret_cast<uint4*>(Vc + (size_t)victim * D)[tid - NV] = newrow;
+        }
     };
 
     if (C == 1) {
@@ -679,11 +843,11 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
 
 // ------------------------------------------------------------------ LSH
 
-template <typename T, int D, class TL>
+template <typename T, int D, class TL, bool Q8>
 __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const DecodeArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    auto& S = *reinterpret_cast<DecodeSmem<T, D, TL>*>(smem_raw);
+    auto& S = *reinterpret_cast<DecodeSmem<T, D, TL, Q8>*>(smem_raw);
     constexpr int EPL = D / 32;
     constexpr int NV = D * (int)sizeof(T) / 16;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -694,8 +858,10 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
 
     const int B = c.B;
     const size_t ub = (size_t)unit * B;
-    T* Kc = reinterpret_cast<T*>(c.K) + ub * D;
-    T* Vc = reinterpret_cast<T*>(c.V) + ub * D;
+    using CE = CacheElem<T, Q8>;
+    CE* Kc = reinterpret_cast<CE*>(c.K) + ub * D;
+    CE* Vc = reinterpret_cast<CE*>(c.V) + ub * D;
+    float2* Sc = Q8 ? c.kvs + (size_t)unit * c.Bp : nullptr;   // slot scale pairs
     int f0, f1;
     fetch_range(B, C, rank, f0, f1);
     if (lane == 0) {
@@ -758,7 +924,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
         xq = qg[tid];
         xk = kg[tid];
     }
-    if (lane == 0) prime_ring<T, D, TL>(S, Kc, Vc, f0, f1);
+    if (lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1);
     const int n = us.x, p = us.y;
     const bool full = (n >= B);
 
@@ -842,13 +1008,16 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
     __syncthreads();
     const int victim = S.victim;
     float qp[D / 2];
-    widen_q<T, D>(qraw, c.qscale, qp);
+    if constexpr (Q8) load_q_q8<T, D>(qg, c.qscale, lane, qp);
+    else widen_q<T, D>(qraw, c.qscale, qp);
 
     float m_run = -INFINITY, l_run = 0.f, o[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] = 0.f;
     if (rank == 0 && warp == 0) {          // the new token, now in the victim slot
-        const float zn = row_dot<T, D, T>(kg, qp, lane);
+        float zn;
+        if constexpr (Q8) zn = row_dot_q8order<T, D>(kg, qp, lane);
+        else zn = row_dot<T, D, T>(kg, qp, lane);
         float vr[EPL];
         load_vec<T, EPL>(vg + lane * EPL, vr);
         m_run = zn;
@@ -858,11 +1027,11 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
     }
     __syncwarp();
 
-    attend_chunk<T, D, TL>(S, Kc, Vc, f0, f1, n, full ? victim : -1, false, qp, m_run, l_run, o,
+    attend_chunk<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, n, full ? victim : -1, false, qp, m_run, l_run, o,
                            c.err);
 
     float Mc, Lc, Oc;
-    merge_warps<T, D, TL>(S, m_run, l_run, o, Mc, Lc, Oc);
+    merge_warps<T, D, TL, Q8>(S, m_run, l_run, o, Mc, Lc, Oc);
 
     if (C > 1) {
         cluster_arrive();                    // every CTA of the cluster is past its ring
@@ -898,10 +1067,14 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
         c.ustate[unit] = make_int2(min(n + 1, B), p + 1);
         if (a.victim_out) a.victim_out[unit] = full ? victim : -1;
     }
-    if (tid < NV)
-        reinterpret_cast<uint4*>(Kc + (size_t)victim * D)[tid] = newrow;
-    else if (tid < 2 * NV)
-        reinterpret_cast<uint4*>(Vc + (size_t)victim * D)[tid - NV] = newrow;
+    if constexpr (Q8) {
+        store_row_q8<T, D>(newrow, tid, Kc, Vc, Sc, victim);
+    } else {
+        if (tid < NV)
+            reinterpret_cast<uint4*>(Kc + (size_t)victim * D)[tid] = newrow;
+        else if (tid < 2 * NV)
+            reinterpret_cast<uint4*>(Vc + (size_t)victim * D)[tid - NV] = newrow;
+    }
 }
 
 // ------------------------------------------------------------- launching
@@ -931,11 +1104,11 @@ int tile_variant()
     return v;
 }
 
-template <typename T, int D, bool LSH, class TL>
+template <typename T, int D, bool LSH, class TL, bool Q8 = false>
 cudaError_t launch_decode_t(const DecodeArgs& a, int split, cudaStream_t st)
 {
-    auto kern = LSH ? lsh_decode_kernel<T, D, TL> : h2o_decode_kernel<T, D, TL>;
-    const size_t smem = sizeof(DecodeSmem<T, D, TL>);
+    auto kern = LSH ? lsh_decode_kernel<T, D, TL, Q8> : h2o_decode_kernel<T, D, TL, Q8>;
+    const size_t smem = sizeof(DecodeSmem<T, D, TL, Q8>);
     static bool configured[64] = {false};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -975,6 +1148,16 @@ template <bool LSH>
 cudaError_t dispatch(const DecodeArgs& a, int split, cudaStream_t st)
 {
     const bool bf = a.c.dtype == 1;
+    if (a.c.kv8) {
+        // int8 cache rows (default tile)
+        if (a.c.D == 128)
+            return bf ? launch_decode_t<__nv_bfloat16, 128, LSH, TileDefault, true>(a, split, st)
+                      : launch_decode_t<float, 128, LSH, TileDefault, true>(a, split, st);
+        if (a.c.D == 64)
+            return bf ? launch_decode_t<__nv_bfloat16, 64, LSH, TileDefault, true>(a, split, st)
+                      : launch_decode_t<float, 64, LSH, TileDefault, true>(a, split, st);
+        return cudaErrorInvalidValue;
+    }
     if (a.c.D == 128 && bf) {
         switch (tile_variant()) {
         case 1: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<4, 2>>(a, split, st);

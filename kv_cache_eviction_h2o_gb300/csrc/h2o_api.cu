@@ -112,6 +112,8 @@ struct h2o_ctx {
     void* K;
     void* V;
     float2* score;             // hi + lo fp32 pairs
+    float2* kvs;               // int8 cache: {K scale, V scale} per slot, [U][Bp]
+    int kv8, Bp;
     int* pos;
     uint32_t* code;
     int2* ustate;
@@ -158,7 +160,7 @@ void free_all(h2o_ctx* h)
 {
     free_prompt(h);
     cudaFree(h->K); cudaFree(h->V); cudaFree(h->score); cudaFree(h->pos); cudaFree(h->code);
-    cudaFree(h->ustate); cudaFree(h->err); cudaFree(h->W);
+    cudaFree(h->ustate); cudaFree(h->err); cudaFree(h->W); cudaFree(h->kvs);
     free(h->W_host);
     h->W_host = nullptr;
 }
@@ -169,6 +171,7 @@ CacheView view(const h2o_ctx* h)
 {
     CacheView v;
     v.K = h->K; v.V = h->V; v.score = h->score; v.pos = h->pos; v.code = h->code;
+    v.kvs = h->kvs; v.kv8 = h->kv8; v.Bp = h->Bp;
     v.ustate = h->ustate; v.err = h->err;
     v.U = h->U; v.B = h->B; v.D = h->D; v.dtype = h->dtype; v.r = h->r;
     v.qscale = (float)(h->scale * 1.4426950408889634);
@@ -187,7 +190,10 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
     if (batch < 1 || heads < 1) return fail(H2O_ERR_ARG, "batch and heads must be >= 1");
     if ((long long)batch * heads > (1LL << 24)) return fail(H2O_ERR_ARG, "batch * heads too large");
     if (head_dim != 64 && head_dim != 128) return fail(H2O_ERR_ARG, "head_dim must be 64 or 128 (got %d)", head_dim);
-    if (dtype != H2O_F32 && dtype != H2O_BF16) return fail(H2O_ERR_ARG, "dtype must be H2O_F32 or H2O_BF16");
+    if ((dtype & ~(H2O_BF16 | H2O_KV8)) != 0)
+        return fail(H2O_ERR_ARG, "dtype must be H2O_F32 or H2O_BF16, optionally | H2O_KV8");
+    const int kv8 = (dtype & H2O_KV8) ? 1 : 0;
+    dtype &= H2O_BF16;
     if (!(scale > 0.0) || !std::isfinite(scale)) return fail(H2O_ERR_ARG, "scale must be finite and > 0");
     if ((long long)budget >= (1LL << 20)) return fail(H2O_ERR_ARG, "budget must be below 2^20");
     if (kind == kLSH && budget > 28 * 1024)
@@ -200,6 +206,7 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
     memset(h, 0, sizeof(*h));
     h->kind = kind; h->B = budget; h->H = heavy; h->r = recent; h->batch = batch; h->heads = heads;
     h->D = head_dim; h->dtype = dtype; h->U = batch * heads; h->scale = scale;
+    h->kv8 = kv8; h->Bp = (budget + 1) & ~1;
     h->stream = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaGetDevice(&h->device);
     if (e != cudaSuccess) { delete h; cudaGetLastError(); return cuda_fail(e, "cudaGetDevice"); }
@@ -209,13 +216,16 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, h->device);
     if (major < 10) { delete h; return fail(H2O_ERR_UNSUPPORTED, "device compute capability %d.x is not sm_103", major); }
 
-    const size_t U = (size_t)h->U, B = (size_t)h->B, row = (size_t)h->D * elem_size(dtype);
+    const size_t U = (size_t)h->U, B = (size_t)h->B, row = (size_t)h->D * (kv8 ? 1 : elem_size(dtype));
     int rc = H2O_OK;
     if ((rc = dev_alloc(&h->K, U * B * row, "cache K")) ||
         (rc = dev_alloc(&h->V, U * B * row, "cache V")) ||
         (rc = dev_alloc((void**)&h->pos, U * B * sizeof(int), "positions")) ||
         (rc = dev_alloc((void**)&h->ustate, U * sizeof(int2), "unit state")) ||
         (rc = dev_alloc((void**)&h->err, sizeof(int), "error word"))) {
+        free_all(h); delete h; return rc;
+    }
+    if (kv8 && (rc = dev_alloc((void**)&h->kvs, U * (size_t)h->Bp * sizeof(float2), "slot scales"))) {
         free_all(h); delete h; return rc;
     }
     if (kind == kH2O) {
@@ -236,6 +246,7 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
     e = cudaMemsetAsync(h->err, 0, sizeof(int), h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->ustate, 0, U * sizeof(int2), h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->pos, 0xff, U * B * sizeof(int), h->stream);
+    if (e == cudaSuccess && kv8) e = cudaMemsetAsync(h->kvs, 0, U * (size_t)h->Bp * sizeof(float2), h->stream);
     if (e != cudaSuccess) { free_all(h); delete h; return cuda_fail(e, "initialise state"); }
     note_cache_write(h->device, h->stream, h);
     *out = h;
@@ -384,7 +395,7 @@ int h2o_get_state(h2o_handle h, void* K, void* V, double* score, int* pos, unsig
                   int* next_pos)
 {
     if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
-    const size_t UB = (size_t)h->U * h->B, row = (size_t)h->D * elem_size(h->dtype);
+    const size_t UB = (size_t)h->U * h->B, row = (size_t)h->D * (h->kv8 ? 1 : elem_size(h->dtype));
     cudaError_t e = cudaSuccess;
     if (K && e == cudaSuccess) e = cudaMemcpyAsync(K, h->K, UB * row, cudaMemcpyDeviceToHost, h->stream);
     if (V && e == cudaSuccess) e = cudaMemcpyAsync(V, h->V, UB * row, cudaMemcpyDeviceToHost, h->stream);
@@ -428,7 +439,7 @@ int h2o_set_state(h2o_handle h, const void* K, const void* V, const double* scor
                   const unsigned* code, const int* occupancy, const int* next_pos)
 {
     if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
-    const size_t UB = (size_t)h->U * h->B, row = (size_t)h->D * elem_size(h->dtype);
+    const size_t UB = (size_t)h->U * h->B, row = (size_t)h->D * (h->kv8 ? 1 : elem_size(h->dtype));
     if (occupancy)
         for (int u = 0; u < h->U; ++u)
             if (occupancy[u] < 0 || occupancy[u] > h->B) return fail(H2O_ERR_ARG, "occupancy out of range");
@@ -468,6 +479,48 @@ int h2o_set_state(h2o_handle h, const void* K, const void* V, const double* scor
     free(pairs);
     if (e != cudaSuccess) return cuda_fail(e, "h2o_set_state");
     h->ready = 1;
+    return H2O_OK;
+}
+
+int h2o_get_kv_scales(h2o_handle h, float* kscale, float* vscale)
+{
+    if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
+    if (!h->kv8) return fail(H2O_ERR_STATE, "the handle's cache is not int8 (H2O_KV8)");
+    const size_t n = (size_t)h->U * h->Bp;
+    float2* s = static_cast<float2*>(malloc(n * sizeof(float2)));
+    if (!s) return fail(H2O_ERR_ALLOC, "host allocation failed");
+    cudaError_t e = cudaMemcpyAsync(s, h->kvs, n * sizeof(float2), cudaMemcpyDeviceToHost, h->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+    if (e == cudaSuccess) {
+        for (int u = 0; u < h->U; ++u)
+            for (int b = 0; b < h->B; ++b) {
+                const float2 x = s[(size_t)u * h->Bp + b];
+                if (kscale) kscale[(size_t)u * h->B + b] = x.x;
+                if (vscale) vscale[(size_t)u * h->B + b] = x.y;
+            }
+    }
+    free(s);
+    if (e != cudaSuccess) return cuda_fail(e, "h2o_get_kv_scales");
+    return H2O_OK;
+}
+
+int h2o_set_kv_scales(h2o_handle h, const float* kscale, const float* vscale)
+{
+    if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
+    if (!h->kv8) return fail(H2O_ERR_STATE, "the handle's cache is not int8 (H2O_KV8)");
+    if (!kscale || !vscale) return fail(H2O_ERR_ARG, "kscale and vscale must be non-NULL");
+    const size_t n = (size_t)h->U * h->Bp;
+    float2* s = static_cast<float2*>(calloc(n, sizeof(float2)));
+    if (!s) return fail(H2O_ERR_ALLOC, "host allocation failed");
+    for (int u = 0; u < h->U; ++u)
+        for (int b = 0; b < h->B; ++b)
+            s[(size_t)u * h->Bp + b] = make_float2(kscale[(size_t)u * h->B + b], vscale[(size_t)u * h->B + b]);
+    cudaError_t e = cudaStreamSynchronize(h->stream);
+    note_cache_write(h->device, h->stream, h);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h->kvs, s, n * sizeof(float2), cudaMemcpyHostToDevice, h->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+    free(s);
+    if (e != cudaSuccess) return cuda_fail(e, "h2o_set_kv_scales");
     return H2O_OK;
 }
 

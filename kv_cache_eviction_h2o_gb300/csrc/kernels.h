@@ -8,8 +8,10 @@ namespace h2o {
 
 // One handle's device-resident cache.
 struct CacheView {
-    void* K;            // [U][B][D] element type per dtype
+    void* K;            // [U][B][D] element type per dtype (int8 codes when kv8)
     void* V;            // [U][B][D]
+    float2* kvs;        // kv8: [U][Bp] {K scale, V scale} of every slot, else nullptr
+    int kv8, Bp;        // kv8: rows stored as int8 codes; Bp = B rounded up to even
     float2* score;      // [U][B] accumulated attention (H2O) as an unevaluated fp32 pair hi + lo
     int* pos;           // [U][B] token position per slot, -1 = empty
     uint32_t* code;     // [U][B] key codes (LSH)

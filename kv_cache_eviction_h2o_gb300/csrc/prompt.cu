@@ -369,16 +369,59 @@ __global__ void __launch_bounds__(256) gather_kernel(CacheView cv, PromptArgs pa
     const long long total = (long long)cv.U * cv.B;
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+    constexpr int VE = 16 / (int)sizeof(T);       // elements per 16-byte vector
+    constexpr int VPL = (NV + 15) / 16;           // vectors per lane of a half-warp
     for (long long slot = wid; slot < total; slot += nw) {
         const int unit = (int)(slot / cv.B);
         const int p = cv.pos[slot];
         const int half = lane >> 4, l16 = lane & 15;
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(half ? cv.V : cv.K) + (size_t)slot * D);
         const T* srcbase = reinterpret_cast<const T*>(half ? pa.V : pa.K) + ((size_t)unit * pa.T) * D;
-        for (int v = l16; v < NV; v += 16) {
-            uint4 w = make_uint4(0u, 0u, 0u, 0u);
-            if (p >= 0) w = reinterpret_cast<const uint4*>(srcbase + (size_t)p * D)[v];
-            dst[v] = w;
+        if (!cv.kv8) {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(half ? cv.V : cv.K) + (size_t)slot * D);
+            for (int v = l16; v < NV; v += 16) {
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (p >= 0) w = reinterpret_cast<const uint4*>(srcbase + (size_t)p * D)[v];
+                dst[v] = w;
+            }
+        } else {
+            // int8 row: the half-warp's max magnitude gives the scale
+            float x[VPL][VE];
+            float amax = 0.f;
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) {
+                const int v = l16 + 16 * k;
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (p >= 0 && v < NV) w = reinterpret_cast<const uint4*>(srcbase + (size_t)p * D)[v];
+                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if constexpr (sizeof(T) == 2) {
+                        x[k][2 * i] = __uint_as_float(u[i] << 16);
+                        x[k][2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+                    } else {
+                        x[k][i] = __uint_as_float(u[i]);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < VE; ++e) amax = fmaxf(amax, fabsf(x[k][e]));
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+            const float inv = q8_inv(amax);
+            uint8_t* dst = reinterpret_cast<uint8_t*>(half ? cv.V : cv.K) + (size_t)slot * D;
+#pragma unroll
+            for (int k = 0; k < VPL; ++k) {
+                const int v = l16 + 16 * k;
+                if (v < NV) {
+                    if constexpr (VE == 8) {
+                        *reinterpret_cast<uint2*>(dst + v * VE) = make_uint2(q8_pack4(&x[k][0], inv), q8_pack4(&x[k][4], inv));
+                    } else {
+                        *reinterpret_cast<uint32_t*>(dst + v * VE) = q8_pack4(&x[k][0], inv);
+                    }
+                }
+            }
+            if (l16 == 0)
+                reinterpret_cast<float*>(cv.kvs + (size_t)unit * cv.Bp + (slot - (long long)unit * cv.B))[half] = q8_scale(amax);
         }
         if (with_codes && lane == 0) cv.code[slot] = p >= 0 ? pa.ck[(size_t)unit * pa.T + p] : 0u;
     }

@@ -46,14 +46,15 @@ def widen(a, dtype):
 class Dev:
     """One device handle (H2O or LSH) for U units with its own stream."""
 
-    def __init__(self, kind, U, d, B, H, r, dtype, scale, W=None, split=0):
-        self.kind, self.U, self.d, self.B, self.dtype = kind, U, d, B, dtype
+    def __init__(self, kind, U, d, B, H, r, dtype, scale, W=None, split=0, kv8=False):
+        self.kind, self.U, self.d, self.B, self.dtype, self.kv8 = kind, U, d, B, dtype, kv8
         self.stream = torch.cuda.current_stream()
+        dt = cdtype(dtype) | (L.H2O_KV8 if kv8 else 0)
         if kind == "h2o":
-            self.h = L.h2o_init(B, H, r, 1, U, d, cdtype(dtype), scale, self.stream)
+            self.h = L.h2o_init(B, H, r, 1, U, d, dt, scale, self.stream)
         else:
             self.Wd = torch.from_numpy(np.ascontiguousarray(W, np.float32)).cuda()
-            self.h = L.lsh_init(B, r, 1, U, d, cdtype(dtype), scale, self.Wd, self.stream)
+            self.h = L.lsh_init(B, r, 1, U, d, dt, scale, self.Wd, self.stream)
         if split:
             L.h2o_set_decode_split(self.h, split)
         self.out = torch.empty((U, d), dtype=torch.float32, device="cuda")
@@ -79,10 +80,17 @@ class Dev:
 
     def state(self):
         U, B, d = self.U, self.B, self.d
-        K = host_elems(self.dtype, (U, B, d)); V = host_elems(self.dtype, (U, B, d))
+        if self.kv8:
+            K = np.empty((U, B, d), np.int8); V = np.empty((U, B, d), np.int8)
+        else:
+            K = host_elems(self.dtype, (U, B, d)); V = host_elems(self.dtype, (U, B, d))
         score = np.empty((U, B)); pos = np.empty((U, B), np.int32)
         code = np.empty((U, B), np.uint32); occ = np.empty(U, np.int32); npos = np.empty(U, np.int32)
         L.h2o_get_state(self.h, K, V, score, pos, code, occ, npos)
+        if self.kv8:
+            ks = np.empty((U, B), np.float32); vs = np.empty((U, B), np.float32)
+            L.h2o_get_kv_scales(self.h, ks, vs)
+            return dict(K=K, V=V, ks=ks, vs=vs, score=score, pos=pos, code=code, occ=occ, npos=npos)
         return dict(K=widen(K, self.dtype), V=widen(V, self.dtype), score=score, pos=pos, code=code,
                     occ=occ, npos=npos)
 
@@ -94,6 +102,15 @@ class Dev:
 
     def close(self):
         L.h2o_destroy(self.h)
+
+
+def rows_equal(g, st):
+    """Cache rows bit-exact: int8 codes and fp32 scales for an int8 cache,
+    the stored values otherwise."""
+    if "ks" in g:
+        return ((g["K"] == st.kq).all() and (g["V"] == st.vq).all() and (g["ks"] == st.ks).all()
+                and (g["vs"] == st.vs).all())
+    return (g["K"] == st.K).all() and (g["V"] == st.V).all()
 
 
 def check_scores(g, o, what):
@@ -161,7 +178,7 @@ def h2o_lockstep(dev, st, q, k, v, T, r, scale, check_every=1):
             g = dev.state()
             assert (g["pos"] == st.pos).all(), "step %d: positions differ" % t
             assert (g["occ"] == st.occ).all() and (g["npos"] == p + 1).all()
-            assert (g["K"] == st.K).all() and (g["V"] == st.V).all(), "step %d: cache rows differ" % t
+            assert rows_equal(g, st), "step %d: cache rows differ" % t
             check_scores(g["score"], st.score, "step %d scores" % t)
     return near, st
 
@@ -179,7 +196,7 @@ def lsh_lockstep(dev, st, q, k, v, W, T, r, scale, check_every=1):
             assert (g["pos"] == st.pos).all(), "LSH step %d: positions differ" % t
             assert (g["code"] == st.code).all(), "LSH step %d: codes differ" % t
             assert (g["occ"] == st.occ).all()
-            assert (g["K"] == st.K).all() and (g["V"] == st.V).all(), "LSH step %d: cache rows differ" % t
+            assert rows_equal(g, st), "LSH step %d: cache rows differ" % t
     return st
 
 
