@@ -50,6 +50,8 @@ def parse():
     p.add_argument("--oracle-units", type=int, default=64)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--kv8", action="store_true",
+                   help="int8 cache slots (one fp32 scale per row) for both variants")
     return p.parse_args()
 
 
@@ -153,19 +155,23 @@ def dist_setup(args):
 
 # ------------------------------------------------------------ algorithmic
 
-def decode_bytes(U, B, d, eb, lsh):
+def decode_bytes(U, B, d, eb, lsh, kv8=False):
     """Algorithmic HBM bytes of one full-cache decode launch over U units:
-    per live slot K and V rows, plus score read+write (8-byte fp32 pair) and position
-    read (H2O) or code and position read (HashEvict); per unit q, k, v in,
-    fp32 out, one K/V row written, victim score/code and position written,
-    unit state read and written; plus the projection matrix once."""
+    per live slot K and V rows (int8 codes plus an 8-byte scale pair with
+    kv8), plus score read+write (8-byte fp32 pair) and position read (H2O)
+    or code and position read (HashEvict); per unit q, k, v in, fp32 out,
+    one K/V row written (and its scale pair), victim score/code and
+    position written, unit state read and written; plus the projection
+    matrix once."""
     row = d * eb
+    crow = d if kv8 else row
+    sc = 8 if kv8 else 0
     if lsh:
-        per_slot = 2 * row + 4 + 4
-        fixed = 3 * row + 4 * d + 2 * row + 4 + 4 + 16
+        per_slot = 2 * crow + sc + 4 + 4
+        fixed = 3 * row + 4 * d + 2 * crow + sc + 4 + 4 + 16
         return U * (B * per_slot + fixed) + d * 32 * 4
-    per_slot = 2 * row + 8 + 8 + 4
-    fixed = 3 * row + 4 * d + 2 * row + 8 + 4 + 16
+    per_slot = 2 * crow + sc + 8 + 8 + 4
+    fixed = 3 * row + 4 * d + 2 * crow + sc + 8 + 4 + 16
     return U * (B * per_slot + fixed)
 
 
@@ -177,9 +183,10 @@ def prefill_flops(U, T, d):
 
 # ------------------------------------------------------------------ oracle
 
-def oracle_job(w, wl_lsh, units, S):
+def oracle_job(w, wl_lsh, units, S, kv8=False):
     """The CPU oracle on a sample of units: H2O prompt + S steps and
-    HashEvict prompt + S steps.  Returns (seconds, threads)."""
+    HashEvict prompt + S steps (int8 cache slots with kv8).  Returns
+    (seconds, threads)."""
     import numpy as np
 
     import oracle
@@ -189,9 +196,13 @@ def oracle_job(w, wl_lsh, units, S):
     T = w.prompt
     t0 = time.perf_counter()
     st, _, _, _ = oracle.h2o_prefill(g["Q"], g["K"], g["V"], w.budget, w.heavy, w.recent, w.scale)
+    if kv8:
+        oracle.kv8(st)
     for t in range(S):
         oracle.h2o_decode_step(st, g["q"][t], g["k"][t], g["v"][t], T + t, w.recent, w.scale)
     ls = oracle.lsh_prefill(g["Q"], g["K"], g["V"], W, wl_lsh.budget, wl_lsh.recent)
+    if kv8:
+        oracle.kv8(ls)
     for t in range(S):
         oracle.lsh_decode_step(ls, g["q"][t], g["k"][t], g["v"][t], W, T + t, wl_lsh.recent, w.scale)
     return time.perf_counter() - t0, oracle.get_threads()
@@ -217,11 +228,11 @@ def run_reference(args):
     n = max(1, args.oracle_units // 4)
     units = list(range(n))
     for _ in range(args.warmup):
-        oracle_job(w, wl_lsh, units, S)
+        oracle_job(w, wl_lsh, units, S, args.kv8)
     times = []
     threads = 1
     for _ in range(args.steps):
-        t, threads = oracle_job(w, wl_lsh, units, S)
+        t, threads = oracle_job(w, wl_lsh, units, S, args.kv8)
         times.append(t)
     total = sum(times)
     value = oracle_rate(w, total / len(times), n, S)
@@ -263,7 +274,7 @@ def run_ours(args):
     S = args.decode_steps or w.steps
     NL = args.layers
     U, T, d, B = w.units, w.prompt, w.head_dim, w.budget
-    dt = L.H2O_BF16
+    dt = L.H2O_BF16 | (L.H2O_KV8 if args.kv8 else 0)
     stream = torch.cuda.Stream()
 
     # ---- inputs resident in HBM, one set per layer cache
@@ -379,10 +390,11 @@ def run_ours(args):
     for name, lsh_flag, src in (("h2o_decode", False, ["decode.cu", "common.cuh"]),
                                 ("lsh_decode", True, ["decode.cu", "common.cuh"])):
         t_launch = phase_ms[name] / n_dec / 1000.0
-        by = decode_bytes(U, B, d, eb, lsh_flag)
+        by = decode_bytes(U, B, d, eb, lsh_flag, args.kv8)
         ach = by / t_launch / 1e9
         rl.append({"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
-                   "frac": ach / hbm, "traffic": ncu_traffic(name), "algorithmic_bytes": by,
+                   "frac": ach / hbm, "traffic": ncu_traffic(name + ("_kv8" if args.kv8 else "")),
+                   "algorithmic_bytes": by,
                    "launch_us": t_launch * 1e6, "peak_source": peak_src, "share": phase_ms[name] / elapsed_ms})
     t_pre = phase_ms["h2o_prefill"] / (NL * K) / 1000.0
     fl = prefill_flops(U, T, d)
@@ -410,7 +422,7 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         n = args.oracle_units
-        secs, threads = oracle_job(w, wl_lsh, list(range(n)), S)
+        secs, threads = oracle_job(w, wl_lsh, list(range(n)), S, args.kv8)
         cpu = {"value": oracle_rate(w, secs, n, S), "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": "%d of %d units of one layer (prompt %d, %d decode steps, H2O + HashEvict), %.1f s"
                          % (n, U, T, S, secs)}
@@ -421,12 +433,14 @@ def run_ours(args):
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "%s-shaped layer x%d: H2O + HashEvict, prompt %d -> %d decode steps, budget %d "
-                               "(%d heavy + %d recent)" % (WORKLOAD, NL, T, S, B, w.heavy, w.recent),
+                               "(%d heavy + %d recent)%s" % (WORKLOAD, NL, T, S, B, w.heavy, w.recent,
+                                                             ", int8 cache slots" if args.kv8 else ""),
+                   "cache": "int8 codes + fp32 scale per row" if args.kv8 else "bf16",
                    "batch": w.batch, "heads": w.heads, "head_dim": d, "prompt": T, "decode_steps": S,
                    "budget": B, "layers": NL, "global_batch": w.batch * world,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2: %d layer caches (%.0f MB) + prompts (%.0f MB); a cache is reused "
-                         "only after %d others" % (NL, 2 * NL * decode_bytes(U, B, d, eb, False) / 1e6,
+                         "only after %d others" % (NL, 2 * NL * decode_bytes(U, B, d, eb, False, args.kv8) / 1e6,
                                                    NL * 3 * U * T * d * eb / 1e6, NL - 1),
                    "step": "one decode step = all %d (batch x head) units of one layer cache advance one token; "
                            "both eviction variants counted; prompt phases inside the timed step" % U},

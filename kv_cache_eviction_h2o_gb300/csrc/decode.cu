@@ -442,7 +442,9 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, Q8>& S, const 
             const float er = safe_exp2_diff(z, m_ref);
             if (h == 0) {
                 l_lane += er;
-                S.e[warp][r] = er;
+                // int8 values: the slot's V scale is folded into its weight
+                if constexpr (Q8) S.e[warp][r] = er * S.sbuf[warp][b][r].y;
+                else S.e[warp][r] = er;
                 if (keep_z && r < gl) S.z[s0 + r] = z;
             }
             __syncwarp();
@@ -453,7 +455,8 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, Q8>& S, const 
                 ev[j] = e4.x; ev[j + 1] = e4.y; ev[j + 2] = e4.z; ev[j + 3] = e4.w;
             }
             if constexpr (Q8) {
-                // int8 values: the slot's V scale folds into its weight
+                // int8 values (weights already carry the V scales)
+#pragma unroll
                 for (int j = 0; j < kStage; ++j) {
                     if (j < gl) {
                         float vr[4];
@@ -462,8 +465,7 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, Q8>& S, const 
                         } else {
                             q8_unpack4((uint32_t)*reinterpret_cast<const uint16_t*>(vst + j * D + lane * EPL), vr);
                         }
-                        const float w = ev[j] * S.sbuf[warp][b][j].y;
-                        const float2 pj = make_float2(w, w);
+                        const float2 pj = make_float2(ev[j], ev[j]);
 #pragma unroll
                         for (int e = 0; e < EPL; e += 2) {
                             const float2 acc = fma2(pj, make_float2(vr[e], vr[e + 1]), make_float2(o[e], o[e + 1]));
