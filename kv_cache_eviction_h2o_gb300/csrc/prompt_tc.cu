@@ -94,6 +94,33 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar)
                  : "memory");
 }
 
+// Issue the load of 32 consecutive fp32 columns of this thread's TMEM lane;
+// the registers are valid only after tc_ld32_wait on the same array.
+__device__ __forceinline__ void tc_ld32_issue(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+// Wait for every TMEM load issued so far; taking r as in/out operands keeps
+// the compiler from reading them before the wait.
+__device__ __forceinline__ void tc_ld32_wait(uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]) :: "memory");
+}
+
+// 2^x by the MUFU instruction (2 ulp; results below 2^-126 flush to 0)
+__device__ __forceinline__ float ex2_fast(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32])
 {
@@ -139,7 +166,7 @@ __device__ __forceinline__ void tile_mma(uint32_t d_tmem, const uint8_t* a, cons
 struct alignas(1024) TcSmem {
     uint8_t a[kTile];                 // the tile's own block (Q in pass 1, K in pass 2)
     uint8_t b[kStages][kTile];        // ring of the swept blocks
-    alignas(16) float colstat[2][2][kT];   // pass 2: per accumulator, m2 and 1/l of the 128 queries (read as float4)
+    alignas(16) float colstat[2][kT];      // pass 2: per accumulator, the 128 queries' m2 + log2(l) (read as float4)
     uint64_t a_full;
     uint64_t b_full[kStages];
     uint64_t b_empty[kStages];
@@ -259,7 +286,7 @@ __device__ __forceinline__ void tc_mma_loop(TcSmem& S, uint32_t tbase, int ntile
 
 // grid: U * nb CTAs; CTA x handles row block ib = nb - 1 - x / U of unit
 // x % U (heaviest blocks first)
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     rowstats_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK, int U,
                        int T, int nb, float c2, float* __restrict__ m2, float* __restrict__ lout, int* err)
 {
@@ -288,10 +315,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (__any_sync(0xffffffffu, !ok || aborted(S))) break;
             tc_fence_after();
             const bool diag = (t == ib);
-#pragma unroll 1
+            // the four 32-column chunks, each load issued while the
+            // previous chunk is processed
+            const uint32_t tcol = tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * kT);
+            uint32_t ra[32], rb[32];
+            tc_ld32_issue(tcol, ra);
+            tc_ld32_wait(ra);
+#pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
+                uint32_t (&cur)[32] = (ch & 1) ? rb : ra;
+                uint32_t (&nxt)[32] = (ch & 1) ? ra : rb;
+                if (ch + 1 < 4) tc_ld32_issue(tcol + (uint32_t)((ch + 1) * 32), nxt);
                 float v[32];
-                tc_ld32(tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * kT + ch * 32), v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(cur[e]);
                 const int j0 = t * kT + ch * 32;
                 float cm = -INFINITY;
 #pragma unroll
@@ -310,8 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float s0 = 0.f, s1 = 0.f;
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        s0 += exp2f(fmaf(v[e], c2, -m));
-                        s1 += exp2f(fmaf(v[e + 1], c2, -m));
+                        s0 += ex2_fast(fmaf(v[e], c2, -m));
+                        s1 += ex2_fast(fmaf(v[e + 1], c2, -m));
                     }
                     // Kahan step
                     const float y = (s0 + s1) - lc;
@@ -319,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     lc = (tsum - l) - y;
                     l = tsum;
                 }
+                if (ch + 1 < 4) tc_ld32_wait(nxt);
             }
             tc_fence_before();
             __syncwarp();
@@ -336,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // grid: U * nb CTAs; CTA x handles key block jb = x / U of unit x % U
 // (heaviest blocks, small jb, first) and sweeps query blocks jb..nb-1
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     colsum_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK, int U,
                      int T, int nb, float c2, const float* __restrict__ m2, const float* __restrict__ lin,
                      double* __restrict__ cout, int* err)
@@ -362,11 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int et = threadIdx.x - 64;          // epilogue thread 0..127
         const int q = warp & 3;
         const int j = jb * kT + 32 * q + lane;    // key within the unit
-        // stage the query statistics of tile 0 (m2 and 1/l; zero weight past T)
+        // stage the query statistics of tile 0 as one bias per query,
+        // m2 + log2(l), so a weight is 2^(s c2 - bias); +inf past T (weight 0)
         {
             const int i = jb * kT + et;
-            S.colstat[0][0][et] = i < T ? m2u[i] : 0.f;
-            S.colstat[0][1][et] = i < T ? 1.f / lu[i] : 0.f;
+            S.colstat[0][et] = i < T ? m2u[i] + log2f(lu[i]) : INFINITY;
         }
         float cs = 0.f, cc = 0.f;                 // Kahan-summed column sum
         for (int t = 0; t < ntiles; ++t) {
@@ -384,33 +422,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (epilogue_any(!ok || aborted(S))) break;
             tc_fence_after();
             const bool edge = (t == 0) || ((ib + 1) * kT > T);
-            const float* ms = S.colstat[b][0];
-            const float* is = S.colstat[b][1];
+            const float* bs = S.colstat[b];
             float part = 0.f;
-#pragma unroll 1
+            const uint32_t tcol = tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * kT);
+            uint32_t ra[32], rb[32];
+            tc_ld32_issue(tcol, ra);
+            tc_ld32_wait(ra);
+#pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
-                float v[32];
-                tc_ld32(tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * kT + ch * 32), v);
+                uint32_t (&cur)[32] = (ch & 1) ? rb : ra;
+                uint32_t (&nxt)[32] = (ch & 1) ? ra : rb;
+                if (ch + 1 < 4) tc_ld32_issue(tcol + (uint32_t)((ch + 1) * 32), nxt);
                 const int i0 = ib * kT + ch * 32;
                 float p0 = 0.f, p1 = 0.f;
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
-                    const float4 m4 = *reinterpret_cast<const float4*>(ms + ch * 32 + e);
-                    const float4 i4 = *reinterpret_cast<const float4*>(is + ch * 32 + e);
-                    float w0 = exp2f(fmaf(v[e], c2, -m4.x)) * i4.x;
-                    float w1 = exp2f(fmaf(v[e + 1], c2, -m4.y)) * i4.y;
-                    float w2 = exp2f(fmaf(v[e + 2], c2, -m4.z)) * i4.z;
-                    float w3 = exp2f(fmaf(v[e + 3], c2, -m4.w)) * i4.w;
+                    const float4 b4 = *reinterpret_cast<const float4*>(bs + ch * 32 + e);
+                    float w0 = ex2_fast(fmaf(__uint_as_float(cur[e]), c2, -b4.x));
+                    float w1 = ex2_fast(fmaf(__uint_as_float(cur[e + 1]), c2, -b4.y));
+                    float w2 = ex2_fast(fmaf(__uint_as_float(cur[e + 2]), c2, -b4.z));
+                    float w3 = ex2_fast(fmaf(__uint_as_float(cur[e + 3]), c2, -b4.w));
                     if (edge) {
-                        if (i0 + e < j || i0 + e >= T) w0 = 0.f;
-                        if (i0 + e + 1 < j || i0 + e + 1 >= T) w1 = 0.f;
-                        if (i0 + e + 2 < j || i0 + e + 2 >= T) w2 = 0.f;
-                        if (i0 + e + 3 < j || i0 + e + 3 >= T) w3 = 0.f;
+                        if (i0 + e < j) w0 = 0.f;
+                        if (i0 + e + 1 < j) w1 = 0.f;
+                        if (i0 + e + 2 < j) w2 = 0.f;
+                        if (i0 + e + 3 < j) w3 = 0.f;
                     }
                     p0 += w0 + w2;
                     p1 += w1 + w3;
                 }
                 part += p0 + p1;
+                if (ch + 1 < 4) tc_ld32_wait(nxt);
             }
             tc_fence_before();
             __syncwarp();
@@ -420,10 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             cc = (tsum - cs) - y;
             cs = tsum;
             // publish the next tile's statistics into the other buffer
-            if (t + 1 < ntiles) {
-                S.colstat[b ^ 1][0][et] = nm;
-                S.colstat[b ^ 1][1][et] = inext < T ? 1.f / nl : 0.f;
-            }
+            if (t + 1 < ntiles) S.colstat[b ^ 1][et] = inext < T ? nm + log2f(nl) : INFINITY;
         }
         if (j < T && !aborted(S)) cout[(size_t)u * T + j] = (double)cs - (double)cc;
     }
