@@ -14,7 +14,7 @@ import torch
 import oracle
 from kv_cache_eviction_h2o_gb300 import binding as L
 from kv_cache_eviction_h2o_gb300 import workloads as wl
-from parity import (Dev, align_prefill, check_scores, replay_h2o, replay_lsh, to_dev)
+from parity import (Dev, align_prefill, check_scores, replay_h2o, replay_lsh, rows_equal, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -37,7 +37,8 @@ def _order(counts, seed, repeat_p=0.35):
     return order
 
 
-def test_interleaved_caches_back_to_back():
+@pytest.mark.parametrize("kv8", [False, True])
+def test_interleaved_caches_back_to_back(kv8):
     S = 20
     wa = wl.WORKLOADS["opt-6.7b"]
     wc = wl.WORKLOADS["hashevict-opt-6.7b"]
@@ -45,9 +46,9 @@ def test_interleaved_caches_back_to_back():
     gb = wl.generate(wa, units=range(12, 24), steps=S)
     gc = wl.generate(wc, units=range(0, 10), steps=S)
     W = gc["W"]
-    devs = [Dev("h2o", 12, wa.head_dim, wa.budget, wa.heavy, wa.recent, wa.dtype, wa.scale),
-            Dev("h2o", 12, wa.head_dim, wa.budget, wa.heavy, wa.recent, wa.dtype, wa.scale),
-            Dev("lsh", 10, wc.head_dim, wc.budget, 0, wc.recent, wc.dtype, wc.scale, W=W)]
+    devs = [Dev("h2o", 12, wa.head_dim, wa.budget, wa.heavy, wa.recent, wa.dtype, wa.scale, kv8=kv8),
+            Dev("h2o", 12, wa.head_dim, wa.budget, wa.heavy, wa.recent, wa.dtype, wa.scale, kv8=kv8),
+            Dev("lsh", 10, wc.head_dim, wc.budget, 0, wc.recent, wc.dtype, wc.scale, W=W, kv8=kv8)]
     gens = [ga, gb, gc]
     for dev, g in zip(devs, gens):
         dev.prefill(g["Q"], g["K"], g["V"])
@@ -78,14 +79,18 @@ def test_interleaved_caches_back_to_back():
         if dev.kind == "h2o":
             st, _, _ = align_prefill(st0[i], g["Q"], g["K"], g["V"], wa.budget, wa.heavy, wa.recent, wa.scale)
             assert (st0[i]["pos"] == st.pos).all()
+            if kv8:
+                oracle.kv8(st)
             near, st = replay_h2o(st, g, T, wa.recent, wa.scale, o, v)
             check_scores(fin["score"], st.score, "cache %d final scores" % i)
         else:
             st = oracle.lsh_prefill(g["Q"], g["K"], g["V"], W, wc.budget, wc.recent)
+            if kv8:
+                oracle.kv8(st)
             replay_lsh(st, g, W, T, wc.recent, wc.scale, o, v)
             assert (fin["code"] == st.code).all()
         assert (fin["pos"] == st.pos).all(), "cache %d: final positions differ" % i
-        assert (fin["K"] == st.K).all() and (fin["V"] == st.V).all(), "cache %d: final rows differ" % i
+        assert rows_equal(fin, st), "cache %d: final rows differ" % i
         assert (fin["npos"] == T + S).all()
     for dev in devs:
         dev.close()
