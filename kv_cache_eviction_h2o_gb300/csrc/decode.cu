@@ -887,7 +887,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
     // This unit's occupancy, and the codes and positions of the slots this
     // thread scans (fetched for all B slots before the occupancy is known).
     // When the previous kernel in the stream cannot have written the cache,
-    // these are read before the dependency wait.
+    // these (and the first ring buffers, below) are read before the wait.
     constexpr int PF = 4;
     int2 us = make_int2(0, 0);
     unsigned pcode[PF];
@@ -902,10 +902,14 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
             if (s < B) { pcode[i] = c.code[ub + s]; ppos[i] = c.pos[ub + s]; }
         }
     };
-    // (The ring is always primed after the wait: primed before it, its data
-    // would land while the victim is still being decided and HBM would then
-    // idle until the attention starts.)
-    if (a.early) read_state();
+    // Early, each warp's first ring buffer is filled before the wait too;
+    // the rest follow the small loads after it (priming the whole ring early
+    // measured slower: its data landed while the victim was still being
+    // decided, and HBM then idled until the attention started).
+    if (a.early) {
+        read_state();
+        if (lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, 0, 1);
+    }
     // everything below may read memory the previous kernel in the stream
     // has written (the inputs, and the cache unless read above)
     grid_dependency_wait();
@@ -926,7 +930,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
         xq = qg[tid];
         xk = kg[tid];
     }
-    if (lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1);
+    if (lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, a.early ? 1 : 0, TL::NBUF);
     const int n = us.x, p = us.y;
     const bool full = (n >= B);
 
