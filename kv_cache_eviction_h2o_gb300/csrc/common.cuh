@@ -127,10 +127,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
 
 // --------------------------------------------------------- cluster barrier
 
-__device__ __forceinline__ void cluster_arrive_relaxed()
-{
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void cluster_arrive()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
@@ -161,10 +157,6 @@ __device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank)
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
 {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-__device__ __forceinline__ void st_cluster_f64(uint32_t addr, double v)
-{
-    asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(addr), "d"(v) : "memory");
 }
 __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v)
 {
@@ -220,15 +212,6 @@ __device__ __forceinline__ void grid_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// ------------------------------------------------------------- reductions
-
-__device__ __forceinline__ void prefetch_l1(const void* p)
-{
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
-}
-
-// Cheapest proxy fence that makes mbarrier initialisation visible to the
-// bulk-copy engine of this CTA.
 // ------------------------------------------------------------ int8 rows
 // A cache row x is stored as int8 codes with one fp32 scale: amax = max|x|,
 // inv = 127 / amax (0 when amax = 0), code = rint(x * inv) within +-127
@@ -321,10 +304,14 @@ __device__ __forceinline__ void named_barrier_arrive(int id, int nthreads)
     }
 }
 
+// Cheapest proxy fence that makes mbarrier initialisation visible to the
+// bulk-copy engine of this CTA.
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+
+// ------------------------------------------------------------- reductions
 
 __device__ __forceinline__ float warp_max(float v)
 {

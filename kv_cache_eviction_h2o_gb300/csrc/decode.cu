@@ -182,8 +182,8 @@ __device__ __forceinline__ void widen_q(const QRaw<T, D>& raw, float scale, floa
     }
 }
 
-// Half-row dot product of row `row` (global or shared, elements of type T or
-// float) with the rotated q half; every lane returns the full dot of its
+// Half-row dot product of row `row` (global or shared, elements of type T)
+// with the rotated q half; every lane returns the full dot of its
 // row after one exchange between the half-warps.
 // Raw 32-bit words of a vector of E elements of T, and their fp32 values.
 template <int BYTES> struct RawT;
@@ -212,8 +212,8 @@ __device__ __forceinline__ void widen_raw(const typename RawT<E * sizeof(T)>::ty
     }
 }
 
-// Half-row dot product of row `row` (global or shared, elements of type T or
-// float) with the rotated q half; every lane returns the full dot of its
+// Half-row dot product of row `row` (global or shared, elements of type T)
+// with the rotated q half; every lane returns the full dot of its
 // row after one exchange between the half-warps.  For rows of T all chunks
 // are loaded before the first multiply, and four accumulator pairs keep the
 // dependent chains short.
@@ -225,19 +225,8 @@ __device__ __forceinline__ float row_dot(const E* row, const float (&qp)[D / 2],
     const E* half = row + h * R::HALF;
     float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                      make_float2(0.f, 0.f)};
-    if constexpr (sizeof(E) == sizeof(float) && sizeof(T) == 2) {
-        // a float copy of a bf16 row (kept in shared memory)
-#pragma unroll
-        for (int c = 0; c < R::HCH; ++c) {
-            float kf[R::VE];
-#pragma unroll
-            for (int e = 0; e < R::VE; ++e) kf[e] = half[(c ^ (r & R::XM)) * R::VE + e];
-#pragma unroll
-            for (int e = 0; e < R::VE; e += 2)
-                acc[(e / 2) & 3] = fma2(make_float2(qp[c * R::VE + e], qp[c * R::VE + e + 1]),
-                                        make_float2(kf[e], kf[e + 1]), acc[(e / 2) & 3]);
-        }
-    } else {
+    static_assert(sizeof(E) == sizeof(T), "rows hold the input type");
+    {
         uint4 raw[R::HCH];
 #pragma unroll
         for (int c = 0; c < R::HCH; ++c)
