@@ -49,6 +49,9 @@ def lib():
                                              _i32p, _i32p, _f64p, _f64p, _f64p, _f64p,
                                              _vp, _vp, _vp, _vp]
         L.oracle_quantize_rows.argtypes = [_i, _i, _f64p, _vp, _f32p]
+        L.oracle_h2o_decode_step_gqa.argtypes = [_i, _i, _i, _i, _i, _d, _i, _f64p, _f64p, _f64p,
+                                                 _i32p, _i32p, _f64p, _f64p, _f64p, _f64p,
+                                                 _vp, _vp, _vp, _vp]
         L.oracle_lsh_code.argtypes = [_i, _f64p, _f32p]
         L.oracle_lsh_code.restype = ctypes.c_uint32
         L.oracle_lsh_codes.argtypes = [_i, _i, _f64p, _f32p, _u32p]
@@ -204,6 +207,46 @@ def _kv8_written(st, slots):
 
 def _written_slots(victim, occ_after):
     return [int(v) if v >= 0 else int(o) - 1 for v, o in zip(victim, occ_after)]
+
+
+def h2o_prefill_gqa(Q, K, V, B, H, r, scale):
+    """Prompt phase of a cache shared by G query heads: Q [U*G, T, d] (the
+    G heads of cache unit u are rows u*G .. u*G+G-1), K, V [U, T, d].  Each
+    head's column sums use its unit's keys; a unit's column sums are the sum
+    over its heads (g = 0..G-1); selection and cache as for one head.
+    Returns (state, c [U, T], kept [U, B], margin [U], per-head c [U*G, T])."""
+    Q = _c64(Q); K = _c64(K); V = _c64(V)
+    U, T, d = K.shape
+    G = Q.shape[0] // U
+    _, _, cq = prefill_scores(Q, np.repeat(K, G, axis=0), scale)
+    c = np.zeros((U, T))
+    for g in range(G):
+        c += cq[g::G]
+    kept = np.full((U, B), -1, np.int32)
+    margin = np.empty(U)
+    for u in range(U):
+        ku, margin[u] = select(c[u], B, H, r)
+        kept[u, :len(ku)] = ku
+    st = build_cache(K, V, c, kept, B)
+    return st, c, kept, margin, cq
+
+
+def h2o_decode_step_gqa(st, q, k, v, p, r, scale, forced=None):
+    """One grouped-query decode step in place on ``st``: q [U*G, d] (heads
+    of unit u in rows u*G ..), k, v [U, d].  Returns (out [U*G, d], victim
+    [U], margin [U], evicted [U])."""
+    q = _c64(q); k = _c64(k); v = _c64(v)
+    U, d = k.shape
+    G = q.shape[0] // U
+    out = np.empty((U * G, d))
+    victim = np.empty(U, dtype=np.int32)
+    margin = np.empty(U)
+    evicted = np.empty(U)
+    f = None if forced is None else np.ascontiguousarray(forced, dtype=np.int32)
+    lib().oracle_h2o_decode_step_gqa(U, G, d, st.B, r, float(scale), int(p), st.K, st.V,
+                                     st.score, st.pos, st.occ, q, k, v, out,
+                                     _ptr(victim), _ptr(margin), _ptr(evicted), _ptr(f))
+    return out, victim, margin, evicted
 
 
 def lsh_code(x, W):

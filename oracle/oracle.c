@@ -53,6 +53,8 @@
  *    first and then attends over the budget (the victim is not attended);
  *  - if no slot is an eviction candidate (possible only for a state that
  *    breaks the recent-window invariant), every live slot is a candidate;
+ *  - grouped-query attention (an optional mode): a cache unit shared by G
+ *    query heads accumulates the sum of their probabilities per slot;
  *  - int8 cache slots (an optional mode): each stored K or V row keeps int8
  *    codes and one fp32 scale, amax/127, with codes rint(x * (127/amax))
  *    in fp32, half to even; a step attends to its own new token at full
@@ -342,6 +344,90 @@ void oracle_h2o_decode_step(int U, int d, int B, int r, double scale, int p,
         memcpy(Vu + (size_t)slot * d, vu, sizeof(double) * d);
         su[slot] = P_new;
         pu[slot] = p;
+        free(z);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* H2O decode step for U cache units, each shared by G query heads      */
+/* (grouped-query attention; the cache is that of a key/value head).    */
+/* Every head attends with its own softmax over the unit's n live slots */
+/* and the new token; a slot's accumulated score grows by the sum of    */
+/* the G heads' probabilities this step (the reading of "accumulated   */
+/* attention" for a shared slot), and the new token's score is the sum  */
+/* of its G probabilities.  Eviction and insertion follow the one-head  */
+/* step.  q, out: [U][G][d]; k, v: [U][d].  Outputs as in the one-head  */
+/* step.                                                                */
+/* ------------------------------------------------------------------ */
+void oracle_h2o_decode_step_gqa(int U, int G, int d, int B, int r, double scale, int p,
+                                double* cK, double* cV, double* score, int* pos, int* occ,
+                                const double* q, const double* k, const double* v,
+                                double* out, int* victim, double* margin, double* evicted,
+                                const int* forced)
+{
+    #pragma omp parallel for schedule(dynamic, 4)
+    for (int u = 0; u < U; ++u) {
+        double* Ku = cK + (size_t)u * B * d;
+        double* Vu = cV + (size_t)u * B * d;
+        double* su = score + (size_t)u * B;
+        int* pu = pos + (size_t)u * B;
+        const double* ku = k + (size_t)u * d;
+        const double* vu = v + (size_t)u * d;
+        const int n = occ[u];
+        double* z = (double*)malloc(sizeof(double) * (size_t)(n + 1));
+        double* add = (double*)calloc((size_t)(n + 1), sizeof(double));
+        for (int g = 0; g < G; ++g) {
+            const double* qg = q + ((size_t)u * G + g) * d;
+            double* og = out + ((size_t)u * G + g) * d;
+            double mx = -INFINITY;
+            for (int s = 0; s < n; ++s) {
+                z[s] = scale * dot(qg, Ku + (size_t)s * d, d);
+                if (z[s] > mx) mx = z[s];
+            }
+            z[n] = scale * dot(qg, ku, d);
+            if (z[n] > mx) mx = z[n];
+            double lsum = 0.0;
+            for (int s = 0; s <= n; ++s) lsum += exp(z[s] - mx);
+            for (int e = 0; e < d; ++e) og[e] = 0.0;
+            for (int s = 0; s <= n; ++s) {
+                const double P = exp(z[s] - mx) / lsum;
+                const double* vs = (s < n) ? Vu + (size_t)s * d : vu;
+                for (int e = 0; e < d; ++e) og[e] += P * vs[e];
+                add[s] += P;                          /* heads in order g = 0..G-1 */
+            }
+        }
+        for (int s = 0; s < n; ++s) su[s] += add[s];
+        const double P_new = add[n];
+        int slot;
+        double mg = INFINITY, ev = 0.0;
+        if (n < B) {
+            slot = n;
+            occ[u] = n + 1;
+            if (victim) victim[u] = -1;
+        } else {
+            int ncand = 0;
+            for (int s = 0; s < n; ++s) if (pu[s] <= p - r) ++ncand;
+            int best = -1, second = -1;
+            for (int s = 0; s < n; ++s) {
+                if (ncand > 0 && !(pu[s] <= p - r)) continue;
+                if (best < 0 || su[s] < su[best]) { second = best; best = s; }
+                else if (second < 0 || su[s] < su[second]) second = s;
+            }
+            if (second >= 0) {
+                const double den = fabs(su[best]) > 1e-30 ? fabs(su[best]) : 1e-30;
+                mg = (su[second] - su[best]) / den;
+            }
+            slot = (forced && forced[u] >= 0) ? forced[u] : best;
+            ev = su[slot];
+            if (victim) victim[u] = slot;
+        }
+        if (margin) margin[u] = mg;
+        if (evicted) evicted[u] = ev;
+        memcpy(Ku + (size_t)slot * d, ku, sizeof(double) * d);
+        memcpy(Vu + (size_t)slot * d, vu, sizeof(double) * d);
+        su[slot] = P_new;
+        pu[slot] = p;
+        free(add);
         free(z);
     }
 }

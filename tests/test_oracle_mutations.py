@@ -42,6 +42,8 @@ MUTATIONS = {
     "kv8_ties_away_from_zero": ("float y = rintf((float)x[e] * inv);", "float y = roundf((float)x[e] * inv);"),
     "kv8_scale_over_128": ("scale[t] = amax / 127.0f;", "scale[t] = amax / 128.0f;"),
     "kv8_inverse_from_128": ("float inv = 127.0f / amax;", "float inv = 128.0f / amax;"),
+    "gqa_last_head_only": ("add[s] += P;                          /* heads in order g = 0..G-1 */",
+                           "add[s] = P;"),
 }
 
 

@@ -477,3 +477,68 @@ def test_kv8_step_attends_new_token_exactly_and_stores_it_quantised():
         assert (st.kq[u, s] == kq[0]).all() and st.ks[u, s] == ks[0]
         others = [x for x in range(B) if x != s]
         assert (st.K[u, others] == Kc[u, others]).all()
+
+
+# --------------------------------------------------- grouped-query caches ---
+
+def _gqa_inputs(seed, U, G, T, S, d):
+    rng = np.random.default_rng(seed)
+    Q = rng.standard_normal((U * G, T, d)); K = rng.standard_normal((U, T, d)); V = rng.standard_normal((U, T, d))
+    q = rng.standard_normal((S, U * G, d)); k = rng.standard_normal((S, U, d)); v = rng.standard_normal((S, U, d))
+    return Q, K, V, q, k, v
+
+
+def test_gqa_one_head_per_group_is_the_one_head_path():
+    U, T, S, d, B, H, r, sc = 3, 30, 12, 8, 10, 5, 5, 0.4
+    Q, K, V, q, k, v = _gqa_inputs(50, U, 1, T, S, d)
+    a, ca, kept_a, mg_a, _ = oracle.h2o_prefill_gqa(Q, K, V, B, H, r, sc)
+    b, cb, kept_b, mg_b = oracle.h2o_prefill(Q, K, V, B, H, r, sc)
+    assert (ca == cb).all() and (kept_a == kept_b).all() and (a.pos == b.pos).all()
+    for t in range(S):
+        oa, va, ma, ea = oracle.h2o_decode_step_gqa(a, q[t], k[t], v[t], T + t, r, sc)
+        ob, vb, mb, eb = oracle.h2o_decode_step(b, q[t], k[t], v[t], T + t, r, sc)
+        assert (oa == ob).all() and (va == vb).all() and (ma == mb).all() and (ea == eb).all()
+        assert (a.score == b.score).all() and (a.K == b.K).all()
+
+
+def test_gqa_identical_heads_scale_the_scores():
+    # G copies of one query: every head's output is the one-head output and
+    # every score is exactly G times the one-head score (G a power of two)
+    U, G, T, S, d, B, H, r, sc = 2, 4, 28, 10, 8, 9, 4, 5, 0.35
+    Q1, K, V, q1, k, v = _gqa_inputs(51, U, 1, T, S, d)
+    Q = np.repeat(Q1, G, axis=0); q = np.repeat(q1, G, axis=1)
+    a, ca, _, _, _ = oracle.h2o_prefill_gqa(Q, K, V, B, H, r, sc)
+    b, cb, _, _ = oracle.h2o_prefill(Q1, K, V, B, H, r, sc)
+    np.testing.assert_allclose(ca, G * cb, rtol=1e-14)
+    assert (a.pos == b.pos).all()
+    for t in range(S):
+        oa, va, _, _ = oracle.h2o_decode_step_gqa(a, q[t], k[t], v[t], T + t, r, sc)
+        ob, vb, _, _ = oracle.h2o_decode_step(b, q1[t], k[t], v[t], T + t, r, sc)
+        assert (va == vb).all()
+        for g in range(G):
+            np.testing.assert_allclose(oa[g::G], ob, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(a.score, G * b.score, rtol=1e-13, atol=1e-15)
+
+
+def test_gqa_decode_brute_force():
+    U, G, T, d, B, H, r, sc = 3, 2, 26, 6, 8, 4, 4, 0.5
+    Q, K, V, q, k, v = _gqa_inputs(52, U, G, T, 1, d)
+    st, c, _, _, cq = oracle.h2o_prefill_gqa(Q, K, V, B, H, r, sc)
+    # the prompt phase: a unit's column sums are its heads' sums; mass G*T
+    np.testing.assert_allclose(c.sum(axis=1), G * T, rtol=1e-12)
+    np.testing.assert_allclose(c, cq[0::G] + cq[1::G], rtol=0, atol=0)
+    Kc, Vc, sc0, pos0 = st.K.copy(), st.V.copy(), st.score.copy(), st.pos.copy()
+    out, vic, _, _ = oracle.h2o_decode_step_gqa(st, q[0], k[0], v[0], T, r, sc)
+    for u in range(U):
+        keys = np.concatenate([Kc[u], k[0, u][None]]); vals = np.concatenate([Vc[u], v[0, u][None]])
+        add = np.zeros(B + 1)
+        for g in range(G):
+            z = sc * keys @ q[0, u * G + g]
+            e = np.exp(z - z.max()); P = e / e.sum()
+            np.testing.assert_allclose(out[u * G + g], P @ vals, rtol=0, atol=1e-12)
+            add += P
+        new = sc0[u] + add[:B]
+        cands = [s for s in range(B) if pos0[u, s] <= T - r]
+        want = min(cands, key=lambda s: (new[s], s))
+        assert vic[u] == want
+        assert st.score[u, want] == pytest.approx(add[B], rel=1e-14)
