@@ -96,6 +96,27 @@ int h2o_init(h2o_handle* out, int budget, int heavy, int recent, int batch, int 
              int head_dim, int dtype, double scale, void* cuda_stream);
 
 /*
+ * h2o_init_gqa -- create an H2O handle whose caches are shared by groups
+ * of query heads (grouped-query attention) [H2O 提案手法: a slot's score
+ * is the attention it accumulates; the grouped form is this library's
+ * reading].  U = batch * kv_heads cache units (unit index b * kv_heads +
+ * h); each is shared by `groups` = G query heads (1 <= G <= 16), query head
+ * g of unit u being row u * G + g of Q, q and out.  Every head attends with
+ * its own softmax; a slot's score grows by the sum of its G heads'
+ * probabilities (added in head order), a prompt token's c_j is the sum of
+ * its G heads' column sums, and the new token's score is the sum of its G
+ * own probabilities.  Eviction and insertion are as for one head.
+ *   budget <= 1024 when G > 1.  Other arguments as h2o_init; G = 1 is
+ *   exactly h2o_init.
+ * h2o_prefill then takes Q [U*G][T][d] and K, V [U][T][d];
+ * h2o_decode_step takes q [U*G][d], k, v [U][d], out [U*G][d] and
+ * victim_out [U]; h2o_get_prefill_stats returns m and l [U*G][T] and the
+ * unit sums c [U][T].  State calls work on the U cache units.
+ */
+int h2o_init_gqa(h2o_handle* out, int budget, int heavy, int recent, int batch, int kv_heads, int groups,
+                 int head_dim, int dtype, double scale, void* cuda_stream);
+
+/*
  * h2o_prefill -- build the initial cache from a prompt of T >= 1 tokens
  * [H2O 提案手法]: the accumulated attention of prompt token j is
  *   c_j = sum_{i>=j} exp(z_ij - m_i) / l_i,  z_ij = scale q_i.k_j,
@@ -194,7 +215,9 @@ int h2o_set_kv_scales(h2o_handle h, const float* kscale, const float* vscale);
 /*
  * h2o_get_prefill_stats -- copy the last h2o_prefill's prompt statistics to
  * HOST buffers [U][T] (any may be NULL): m (row max of z, natural-log
- * units), l (row normaliser) and c (column sums, fp64).  Waits.
+ * units), l (row normaliser) and c (column sums, fp64).  Waits.  On a
+ * grouped-query handle m and l are [U*G][T] (per query head) and c is
+ * [U][T] (per cache unit, the sum over its heads).
  */
 int h2o_get_prefill_stats(h2o_handle h, float* m, float* l, double* c);
 

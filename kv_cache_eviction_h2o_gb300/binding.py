@@ -33,6 +33,7 @@ _i = ctypes.c_int
 _d = ctypes.c_double
 SIGNATURES = {
     "h2o_init": (_i, [ctypes.POINTER(_vp), _i, _i, _i, _i, _i, _i, _i, _d, _vp]),
+    "h2o_init_gqa": (_i, [ctypes.POINTER(_vp), _i, _i, _i, _i, _i, _i, _i, _i, _d, _vp]),
     "h2o_prefill": (_i, [_vp, _vp, _vp, _vp, _i]),
     "h2o_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp]),
     "lsh_init": (_i, [ctypes.POINTER(_vp), _i, _i, _i, _i, _i, _i, _d, _vp, _vp]),
@@ -114,6 +115,13 @@ def h2o_init(budget, heavy, recent, batch, heads, head_dim, dtype, scale, stream
     h = _vp()
     _check(lib().h2o_init(ctypes.byref(h), budget, heavy, recent, batch, heads, head_dim, dtype,
                           float(scale), _stream(stream)))
+    return h.value
+
+
+def h2o_init_gqa(budget, heavy, recent, batch, kv_heads, groups, head_dim, dtype, scale, stream=None):
+    h = _vp()
+    _check(lib().h2o_init_gqa(ctypes.byref(h), budget, heavy, recent, batch, kv_heads, groups, head_dim,
+                              dtype, float(scale), _stream(stream)))
     return h.value
 
 

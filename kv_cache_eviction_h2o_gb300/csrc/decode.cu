@@ -45,7 +45,8 @@ constexpr unsigned kFull = 0xffffffffu;
 template <int NW_, int NBUF_>
 struct Tile {
     static constexpr int NW = NW_, NT = 32 * NW_, NBUF = NBUF_;
-    static constexpr int SPT = kMaxChunk / NT;            // slots per thread in the score pass
+    static constexpr int SPT = (kMaxChunk + NT - 1) / NT; // slots per thread in the score pass (SPT * NT >= kMaxChunk)
+    static_assert(SPT * NT >= kMaxChunk, "the score pass covers every slot of a chunk");
     static constexpr int MINB = NT <= 192 ? 2 : 1;        // CTAs per SM the registers must allow
 };
 
@@ -584,7 +585,12 @@ __device__ __forceinline__ void fetch_range(int B, int C, int rank, int& f0, int
 
 // ------------------------------------------------------------------ H2O
 
-template <typename T, int D, class TL, bool Q8>
+// GQ: grouped-query cache.  The cluster's C CTAs are the C query heads that
+// share cache unit `unit`; each CTA attends over every slot of the unit with
+// its own query and softmax, and CTA g accumulates the heads' probabilities
+// into the scores of its share [s0, s1) of the slots.  Otherwise the
+// cluster's CTAs split one head's slots.
+template <typename T, int D, class TL, bool Q8, bool GQ>
 __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const DecodeArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -596,6 +602,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     const int C = (int)cluster_nctarank();
     const int rank = (int)cluster_ctarank();
     const int unit = blockIdx.x / C;
+    const size_t qrow = GQ ? (size_t)blockIdx.x : (size_t)unit;   // query / output row
 
     const int B = c.B;
     const size_t ub = (size_t)unit * B;
@@ -603,8 +610,16 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     CE* Kc = reinterpret_cast<CE*>(c.K) + ub * D;
     CE* Vc = reinterpret_cast<CE*>(c.V) + ub * D;
     float2* Sc = Q8 ? c.kvs + (size_t)unit * c.Bp : nullptr;   // slot scale pairs
-    int f0, f1;
-    fetch_range(B, C, rank, f0, f1);
+    int f0, f1, s0, s1;                      // fetched slots; slots whose scores this CTA updates
+    if constexpr (GQ) {
+        f0 = 0;
+        f1 = B;
+        fetch_range(B, C, rank, s0, s1);
+    } else {
+        fetch_range(B, C, rank, f0, f1);
+        s0 = f0;
+        s1 = f1;
+    }
     if (lane == 0) {
 #pragma unroll
         for (int b = 0; b < TL::NBUF; ++b) mbar_init(&S.bar[warp][b], 1);
@@ -622,10 +637,10 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
         us = c.ustate[unit];
 #pragma unroll
         for (int i = 0; i < TL::SPT; ++i) {
-            const int s = f0 + tid + i * TL::NT;
+            const int s = s0 + tid + i * TL::NT;
             sc_old[i] = make_float2(0.f, 0.f);
             ps[i] = 0;
-            if (s < f1) { sc_old[i] = c.score[ub + s]; ps[i] = c.pos[ub + s]; }
+            if (s < s1) { sc_old[i] = c.score[ub + s]; ps[i] = c.pos[ub + s]; }
         }
     };
     // Early, only each warp's first buffer is filled before the wait: the
@@ -645,8 +660,8 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     }
     float qp[D / 2];
     QRaw<T, D> qraw;
-    if constexpr (Q8) load_q_q8<T, D>(reinterpret_cast<const T*>(a.q) + (size_t)unit * D, c.qscale, lane, qp);
-    else load_q_raw<T, D>(reinterpret_cast<const T*>(a.q) + (size_t)unit * D, lane, qraw);
+    if constexpr (Q8) load_q_q8<T, D>(reinterpret_cast<const T*>(a.q) + qrow * D, c.qscale, lane, qp);
+    else load_q_raw<T, D>(reinterpret_cast<const T*>(a.q) + qrow * D, lane, qraw);
     if (a.early && lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, 1, TL::NBUF);
     const T* kg = reinterpret_cast<const T*>(a.k) + (size_t)unit * D;
     const T* vg = reinterpret_cast<const T*>(a.v) + (size_t)unit * D;
@@ -663,7 +678,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     float m_run = -INFINITY, l_run = 0.f, o[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] = 0.f;
-    if (rank == 0 && warp == 0) {          // the new token attends to itself
+    if ((GQ || rank == 0) && warp == 0) {  // the new token attends to itself
         float vr[EPL];
         float zn;
         if constexpr (Q8) zn = row_dot_q8order<T, D>(kg, qp, lane);
@@ -681,10 +696,107 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
 
     float Mc, Lc, Oc;
     merge_warps<T, D, TL, Q8>(S, m_run, l_run, o, Mc, Lc, Oc);
+    const uint32_t x0 = map_to_rank(&S.u.epi.x, 0);
+
+    // Write the new token into the victim slot (slot n while the cache is
+    // not full) with score `snew`.  `write_row` runs in the threads holding
+    // `newrow`.
+    auto finish = [&](int victim, float2 snew) {
+        if (victim < 0 || victim >= B) victim = 0;   // n == 0 with B == 0 cannot happen
+        if (tid == 0) {
+            c.score[ub + victim] = snew;
+            c.pos[ub + victim] = p;
+            c.ustate[unit] = make_int2(min(n + 1, B), p + 1);
+            if (a.victim_out) a.victim_out[unit] = full ? victim : -1;
+        }
+        if constexpr (Q8) {
+            store_row_q8<T, D>(newrow, tid, Kc, Vc, Sc, victim);
+        } else {
+            if (tid < NV)
+                reinterpret_cast<uint4*>(Kc + (size_t)victim * D)[tid] = newrow;
+            else if (tid < 2 * NV)
+                reinterpret_cast<uint4*>(Vc + (size_t)victim * D)[tid - NV] = newrow;
+        }
+    };
+
+    if constexpr (GQ) {
+        // this head's output, then its probabilities in place of its logits
+        const float invL = 1.f / Lc;
+        if (tid < D) a.out[qrow * D + tid] = Oc * invL;
+        for (int s = tid; s < n; s += TL::NT) S.z[s] = exp2f(S.z[s] - Mc) * invL;
+        if (tid == 0) S.P_new = exp2f(S.z_new - Mc) * invL;
+        cluster_arrive();                    // every head's probabilities are in place
+        cluster_wait();
+        // scores of this CTA's share: add the heads' probabilities in head
+        // order; arg-min as in the split path
+        const int sc1 = min(n, s1);
+        ArgMin best = argmin_none(), best_all = argmin_none();
+#pragma unroll
+        for (int i = 0; i < TL::SPT; ++i) {
+            const int s = s0 + tid + i * TL::NT;
+            if (s < sc1) {
+                float2 ns = sc_old[i];
+                for (int j = 0; j < C; ++j) ns = pair_add(ns, ld_cluster_f32(map_to_rank(&S.z[s], j)));
+                c.score[ub + s] = ns;
+                if (full) {
+                    const ArgMin k = ArgMin{ord_key(ns.x), ord_key(ns.y), (unsigned)s};
+                    if (ps[i] <= p - c.r) argmin_take(best, k);
+                    argmin_take(best_all, k);
+                }
+            }
+        }
+        if (full) {
+            best = warp_argmin(best);
+            best_all = warp_argmin(best_all);
+            if (lane == 0) {
+                S.am[0][0][warp] = best.hi; S.am[0][1][warp] = best.lo; S.am[0][2][warp] = best.slot;
+                S.am[1][0][warp] = best_all.hi; S.am[1][1][warp] = best_all.lo; S.am[1][2][warp] = best_all.slot;
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // this CTA's arg-mins and its head's new-token probability, pushed
+            // into rank 0's exchange
+            if (full) {
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    ArgMin w = lane < TL::NW ? ArgMin{S.am[k][0][lane], S.am[k][1][lane], S.am[k][2][lane]} : argmin_none();
+                    w = warp_argmin(w);
+                    if (lane == 0) {
+                        const uint32_t base = x0 + (uint32_t)offsetof(Exchange<D>, am) + (uint32_t)(k * 3 * kMaxSplit * 4);
+                        st_cluster_s32(base + rank * 4, (int)w.hi);
+                        st_cluster_s32(base + (kMaxSplit + rank) * 4, (int)w.lo);
+                        st_cluster_s32(base + (2 * kMaxSplit + rank) * 4, (int)w.slot);
+                    }
+                }
+            }
+            if (lane == 0) st_cluster_f32(x0 + (uint32_t)offsetof(Exchange<D>, m) + rank * 4, S.P_new);
+        }
+        cluster_arrive();                    // exchange complete; no CTA reads another's memory after this
+        cluster_wait();
+        if (rank != 0) return;
+        if (tid == 0) {
+            int victim = n;
+            if (full) {
+                ArgMin vc = argmin_none(), va = argmin_none();
+                for (int j = 0; j < C; ++j) {
+                    argmin_take(vc, ArgMin{S.u.epi.x.am[0][0][j], S.u.epi.x.am[0][1][j], S.u.epi.x.am[0][2][j]});
+                    argmin_take(va, ArgMin{S.u.epi.x.am[1][0][j], S.u.epi.x.am[1][1][j], S.u.epi.x.am[1][2][j]});
+                }
+                victim = (int)(vc.slot != 0xffffffffu ? vc.slot : va.slot);
+            }
+            S.victim = victim;
+        }
+        __syncthreads();
+        float2 snew = make_float2(0.f, 0.f);
+        if (tid == 0)
+            for (int j = 0; j < C; ++j) snew = pair_add(snew, S.u.epi.x.m[j]);
+        finish(S.victim, snew);
+        return;
+    }
 
     // exchange 1: (max, normaliser, output) of every CTA into rank 0; a
     // single-CTA unit already has them
-    const uint32_t x0 = map_to_rank(&S.u.epi.x, 0);
     float M, invL;
     if (C > 1) {
         cluster_arrive();                    // every CTA of the cluster is past its ring
@@ -744,30 +856,10 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
             acc = 0.f;
             for (int j = 0; j < C; ++j) acc += S.u.epi.x.o[j][tid] * safe_exp2_diff(S.u.epi.x.m[j], M);
         }
-        a.out[(size_t)unit * D + tid] = acc * invL;
+        a.out[qrow * D + tid] = acc * invL;
     }
     if (rank == 0 && tid == 0) S.P_new = exp2f(S.z_new - M) * invL;
     __syncthreads();
-
-    // Write the new token into the victim slot (slot n while the cache is
-    // not full).  `write_row` runs in the threads holding `newrow`.
-    auto finish = [&](int victim) {
-        if (victim < 0 || victim >= B) victim = 0;   // n == 0 with B == 0 cannot happen
-        if (tid == 0) {
-            c.score[ub + victim] = make_float2(S.P_new, 0.f);
-            c.pos[ub + victim] = p;
-            c.ustate[unit] = make_int2(min(n + 1, B), p + 1);
-            if (a.victim_out) a.victim_out[unit] = full ? victim : -1;
-        }
-        if constexpr (Q8) {
-            store_row_q8<T, D>(newrow, tid, Kc, Vc, Sc, victim);
-        } else {
-            if (tid < NV)
-                reinterpret_cast<uint4*>(Kc + (size_t)victim * D)[tid] = newrow;
-            else if (tid < 2 * NV)
-                reinterpret_cast<uint4*>(Vc + (size_t)victim * D)[tid - NV] = newrow;
-        }
-    };
 
     if (C == 1) {
         // one CTA holds the unit: warp 0 reduces the warps' candidates; with
@@ -789,11 +881,11 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
             victim = (int)w.slot;
         }
         if constexpr (2 * NV <= 32) {
-            if (warp == 0) finish(victim);
+            if (warp == 0) finish(victim, make_float2(S.P_new, 0.f));
         } else {
             if (tid == 0) S.victim = victim;
             __syncthreads();
-            finish(S.victim);
+            finish(S.victim, make_float2(S.P_new, 0.f));
         }
         return;
     }
@@ -829,7 +921,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
         S.victim = victim;
     }
     __syncthreads();
-    finish(S.victim);
+    finish(S.victim, make_float2(S.P_new, 0.f));
 }
 
 // ------------------------------------------------------------------ LSH
@@ -1099,10 +1191,13 @@ int tile_variant()
     return v;
 }
 
-template <typename T, int D, bool LSH, class TL, bool Q8 = false>
+template <typename T, int D, bool LSH, class TL, bool Q8 = false, bool GQ = false>
 cudaError_t launch_decode_t(const DecodeArgs& a, int split, cudaStream_t st)
 {
-    auto kern = LSH ? lsh_decode_kernel<T, D, TL, Q8> : h2o_decode_kernel<T, D, TL, Q8>;
+    void (*kern)(const DecodeArgs);
+    if constexpr (LSH) kern = lsh_decode_kernel<T, D, TL, Q8>;
+    else kern = h2o_decode_kernel<T, D, TL, Q8, GQ>;
+    if constexpr (GQ) split = a.G;             // one CTA per query head of a cache unit
     const size_t smem = sizeof(DecodeSmem<T, D, TL, Q8>);
     static bool configured[64] = {false};
     int dev = 0;
@@ -1143,6 +1238,26 @@ template <bool LSH>
 cudaError_t dispatch(const DecodeArgs& a, int split, cudaStream_t st)
 {
     const bool bf = a.c.dtype == 1;
+    if constexpr (!LSH) {
+        if (a.G > 1) {
+            // grouped-query cache (default tile): every dtype and row form
+            if (a.c.D == 128) {
+                if (a.c.kv8)
+                    return bf ? launch_decode_t<__nv_bfloat16, 128, false, TileDefault, true, true>(a, split, st)
+                              : launch_decode_t<float, 128, false, TileDefault, true, true>(a, split, st);
+                return bf ? launch_decode_t<__nv_bfloat16, 128, false, TileDefault, false, true>(a, split, st)
+                          : launch_decode_t<float, 128, false, TileDefault, false, true>(a, split, st);
+            }
+            if (a.c.D == 64) {
+                if (a.c.kv8)
+                    return bf ? launch_decode_t<__nv_bfloat16, 64, false, TileDefault, true, true>(a, split, st)
+                              : launch_decode_t<float, 64, false, TileDefault, true, true>(a, split, st);
+                return bf ? launch_decode_t<__nv_bfloat16, 64, false, TileDefault, false, true>(a, split, st)
+                          : launch_decode_t<float, 64, false, TileDefault, false, true>(a, split, st);
+            }
+            return cudaErrorInvalidValue;
+        }
+    }
     if (a.c.kv8) {
         // int8 cache rows (default tile)
         if (a.c.D == 128)

@@ -103,6 +103,7 @@ void forget_cache_writes(const void* h)
 struct h2o_ctx {
     int kind;
     int B, H, r, batch, heads, D, dtype, U;
+    int G;                     // query heads per cache unit (H2O grouped-query cache)
     double scale;
     cudaStream_t stream;
     int device;
@@ -124,7 +125,8 @@ struct h2o_ctx {
     int T_cap;
     float* m2;
     float* l;
-    double* c;
+    double* c;                 // per query head
+    double* ckv;               // per cache unit (G > 1): the sum over its heads
     uint32_t* cq;
     uint32_t* ck;
     int last_T;
@@ -151,8 +153,8 @@ int dev_alloc(void** p, size_t bytes, const char* what)
 
 void free_prompt(h2o_ctx* h)
 {
-    cudaFree(h->m2); cudaFree(h->l); cudaFree(h->c); cudaFree(h->cq); cudaFree(h->ck);
-    h->m2 = nullptr; h->l = nullptr; h->c = nullptr; h->cq = nullptr; h->ck = nullptr;
+    cudaFree(h->m2); cudaFree(h->l); cudaFree(h->c); cudaFree(h->ckv); cudaFree(h->cq); cudaFree(h->ck);
+    h->m2 = nullptr; h->l = nullptr; h->c = nullptr; h->ckv = nullptr; h->cq = nullptr; h->ck = nullptr;
     h->T_cap = 0;
 }
 
@@ -179,16 +181,20 @@ CacheView view(const h2o_ctx* h)
 }
 
 int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int batch, int heads,
-           int head_dim, int dtype, double scale, const float* W, void* stream)
+           int head_dim, int dtype, double scale, const float* W, void* stream, int groups = 1)
 {
     if (!out) return fail(H2O_ERR_ARG, "out handle pointer is NULL");
     *out = nullptr;
+    if (groups < 1 || groups > max_decode_split())
+        return fail(H2O_ERR_ARG, "groups must be in [1, %d] (got %d)", max_decode_split(), groups);
+    if (groups > 1 && budget > 1024)
+        return fail(H2O_ERR_ARG, "a grouped-query cache holds at most 1024 slots (got %d)", budget);
     if (budget < 1) return fail(H2O_ERR_ARG, "budget must be >= 1 (got %d)", budget);
     if (recent < 0 || recent > budget) return fail(H2O_ERR_ARG, "recent must be in [0, budget] (got %d)", recent);
     if (kind == kH2O && (heavy < 0 || heavy + recent != budget))
         return fail(H2O_ERR_ARG, "heavy + recent must equal budget (%d + %d != %d)", heavy, recent, budget);
     if (batch < 1 || heads < 1) return fail(H2O_ERR_ARG, "batch and heads must be >= 1");
-    if ((long long)batch * heads > (1LL << 24)) return fail(H2O_ERR_ARG, "batch * heads too large");
+    if ((long long)batch * heads * groups > (1LL << 24)) return fail(H2O_ERR_ARG, "batch * heads too large");
     if (head_dim != 64 && head_dim != 128) return fail(H2O_ERR_ARG, "head_dim must be 64 or 128 (got %d)", head_dim);
     if ((dtype & ~(H2O_BF16 | H2O_KV8)) != 0)
         return fail(H2O_ERR_ARG, "dtype must be H2O_F32 or H2O_BF16, optionally | H2O_KV8");
@@ -205,7 +211,7 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
     if (!h) return fail(H2O_ERR_ALLOC, "host allocation failed");
     memset(h, 0, sizeof(*h));
     h->kind = kind; h->B = budget; h->H = heavy; h->r = recent; h->batch = batch; h->heads = heads;
-    h->D = head_dim; h->dtype = dtype; h->U = batch * heads; h->scale = scale;
+    h->D = head_dim; h->dtype = dtype; h->U = batch * heads; h->G = groups; h->scale = scale;
     h->kv8 = kv8; h->Bp = (budget + 1) & ~1;
     h->stream = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaGetDevice(&h->device);
@@ -260,12 +266,15 @@ int ensure_prompt_scratch(h2o_ctx* h, int T)
     cudaError_t e = cudaStreamSynchronize(h->stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     free_prompt(h);
-    const size_t n = (size_t)h->U * (size_t)T;
+    const size_t n = (size_t)h->U * (size_t)T, nq = n * (size_t)h->G;
     int rc;
     if (h->kind == kH2O) {
-        if ((rc = dev_alloc((void**)&h->m2, n * sizeof(float), "row max")) ||
-            (rc = dev_alloc((void**)&h->l, n * sizeof(float), "row normaliser")) ||
-            (rc = dev_alloc((void**)&h->c, n * sizeof(double), "column sums"))) {
+        if ((rc = dev_alloc((void**)&h->m2, nq * sizeof(float), "row max")) ||
+            (rc = dev_alloc((void**)&h->l, nq * sizeof(float), "row normaliser")) ||
+            (rc = dev_alloc((void**)&h->c, nq * sizeof(double), "column sums"))) {
+            free_prompt(h); return rc;
+        }
+        if (h->G > 1 && (rc = dev_alloc((void**)&h->ckv, n * sizeof(double), "cache unit column sums"))) {
             free_prompt(h); return rc;
         }
     } else {
@@ -285,7 +294,7 @@ int check_prompt(h2o_ctx* h, int kind, const void* Q, const void* K, const void*
     if (!Q || !K || !V) return fail(H2O_ERR_ARG, "Q, K and V must be non-NULL");
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V)) return fail(H2O_ERR_ARG, "Q, K, V must be 16-byte aligned");
     if (T < 1) return fail(H2O_ERR_ARG, "prompt length must be >= 1 (got %d)", T);
-    if ((long long)T * h->U > (1LL << 31) / 4) return fail(H2O_ERR_ARG, "prompt too long for this batch");
+    if ((long long)T * h->U * h->G > (1LL << 31) / 4) return fail(H2O_ERR_ARG, "prompt too long for this batch");
     if (kind == kH2O && T >= (1 << 24)) return fail(H2O_ERR_ARG, "prompt too long");
     return H2O_OK;
 }
@@ -320,6 +329,13 @@ int h2o_init(h2o_handle* out, int budget, int heavy, int recent, int batch, int 
     return create(out, kH2O, budget, heavy, recent, batch, heads, head_dim, dtype, scale, nullptr, cuda_stream);
 }
 
+int h2o_init_gqa(h2o_handle* out, int budget, int heavy, int recent, int batch, int kv_heads, int groups,
+                 int head_dim, int dtype, double scale, void* cuda_stream)
+{
+    return create(out, kH2O, budget, heavy, recent, batch, kv_heads, head_dim, dtype, scale, nullptr, cuda_stream,
+                  groups);
+}
+
 int lsh_init(h2o_handle* out, int budget, int recent, int batch, int heads, int head_dim, int dtype,
              double scale, const float* W, void* cuda_stream)
 {
@@ -336,9 +352,19 @@ int h2o_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T
     CacheView cv = view(h);
     PromptArgs pa = {};
     pa.Q = Q; pa.K = K; pa.V = V; pa.T = T; pa.H = h->H;
-    pa.m2 = h->m2; pa.l = h->l; pa.c = h->c;
+    pa.m2 = h->m2; pa.l = h->l; pa.c = h->c; pa.G = h->G;
     note_cache_write(h->device, h->stream, h);
-    cudaError_t e = launch_prompt_stats(cv, pa, h->stream);
+    cudaError_t e;
+    if (h->G > 1) {
+        // column sums per query head, then per cache unit
+        CacheView qv = cv;
+        qv.U = h->U * h->G;
+        e = launch_prompt_stats(qv, pa, h->stream);
+        if (e == cudaSuccess) e = launch_group_sum(h->c, h->ckv, h->U, h->G, T, h->stream);
+        pa.c = h->ckv;
+    } else {
+        e = launch_prompt_stats(cv, pa, h->stream);
+    }
     if (e == cudaSuccess) e = launch_select(cv, pa, h->stream);
     if (e == cudaSuccess) e = launch_gather(cv, pa, false, h->stream);
     if (e != cudaSuccess) return cuda_fail(e, "h2o_prefill launch");
@@ -371,7 +397,7 @@ int h2o_decode_step(h2o_handle h, const void* q, const void* k, const void* v, f
     if (rc) return rc;
     if (inject("launch")) return fail(H2O_ERR_CUDA, "kernel launch failed (injected)");
     DecodeArgs a = {};
-    a.c = view(h); a.q = q; a.k = k; a.v = v; a.out = out; a.victim_out = victim_out;
+    a.c = view(h); a.q = q; a.k = k; a.v = v; a.out = out; a.victim_out = victim_out; a.G = h->G;
     a.early = note_cache_write(h->device, h->stream, h) ? 1 : 0;
     cudaError_t e = launch_h2o_decode(a, decode_split(h), h->stream);
     if (e != cudaSuccess) return cuda_fail(e, "h2o_decode_step launch");
@@ -529,15 +555,16 @@ int h2o_get_prefill_stats(h2o_handle h, float* m, float* l, double* c)
     if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
     if (h->kind != kH2O) return fail(H2O_ERR_STATE, "prompt statistics exist only on H2O handles");
     if (!h->last_T) return fail(H2O_ERR_STATE, "no prompt has been processed");
-    const size_t n = (size_t)h->U * h->last_T;
+    const size_t n = (size_t)h->U * h->last_T, nq = n * (size_t)h->G;
+    const double* cu = h->G > 1 ? h->ckv : h->c;
     cudaError_t e = cudaSuccess;
-    if (m) e = cudaMemcpyAsync(m, h->m2, n * sizeof(float), cudaMemcpyDeviceToHost, h->stream);
-    if (l && e == cudaSuccess) e = cudaMemcpyAsync(l, h->l, n * sizeof(float), cudaMemcpyDeviceToHost, h->stream);
-    if (c && e == cudaSuccess) e = cudaMemcpyAsync(c, h->c, n * sizeof(double), cudaMemcpyDeviceToHost, h->stream);
+    if (m) e = cudaMemcpyAsync(m, h->m2, nq * sizeof(float), cudaMemcpyDeviceToHost, h->stream);
+    if (l && e == cudaSuccess) e = cudaMemcpyAsync(l, h->l, nq * sizeof(float), cudaMemcpyDeviceToHost, h->stream);
+    if (c && e == cudaSuccess) e = cudaMemcpyAsync(c, cu, n * sizeof(double), cudaMemcpyDeviceToHost, h->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
     if (e != cudaSuccess) return cuda_fail(e, "h2o_get_prefill_stats");
     if (m)
-        for (size_t i = 0; i < n; ++i) m[i] = (float)((double)m[i] * 0.6931471805599453);
+        for (size_t i = 0; i < nq; ++i) m[i] = (float)((double)m[i] * 0.6931471805599453);
     return H2O_OK;
 }
 

@@ -23,14 +23,16 @@ struct CacheView {
 
 struct DecodeArgs {
     CacheView c;
-    const void* q;      // [U][D]
+    const void* q;      // [U][D] ([U * G][D] for a grouped-query cache)
     const void* k;      // [U][D]
     const void* v;      // [U][D]
-    float* out;         // [U][D]
+    float* out;         // [U][D] ([U * G][D])
     int* victim_out;    // [U] or nullptr
     const float* W;     // [D][32] (LSH)
     int early;          // 1: the previous kernel in the stream does not write this
                         // cache, so the cache may be read before the dependency wait
+    int G;              // H2O: query heads sharing each cache unit (0 or 1: one);
+                        // q and out then hold U * G rows, head g of unit u in row u * G + g
 };
 
 struct PromptArgs {
@@ -44,6 +46,8 @@ struct PromptArgs {
     double* c;          // [U][T] column sums
     uint32_t* cq;       // [U][T] query codes (LSH)
     uint32_t* ck;       // [U][T] key codes (LSH)
+    int G;              // prompt scorer: query heads per key row set (0 or 1: one);
+                        // query unit u reads the keys of unit u / G
 };
 
 cudaError_t launch_h2o_decode(const DecodeArgs& a, int split, cudaStream_t st);
@@ -56,6 +60,8 @@ cudaError_t launch_prompt_stats(const CacheView& c, const PromptArgs& p, cudaStr
 bool prompt_tc_supported(const CacheView& c);
 cudaError_t launch_prompt_stats_tc(const CacheView& c, const PromptArgs& p, cudaStream_t st);
 cudaError_t launch_select(const CacheView& c, const PromptArgs& p, cudaStream_t st);
+// ckv[u][j] = sum over g = 0..G-1 of c[u * G + g][j], u < U, j < T
+cudaError_t launch_group_sum(const double* c, double* ckv, int U, int G, int T, cudaStream_t st);
 cudaError_t launch_gather(const CacheView& c, const PromptArgs& p, bool with_codes, cudaStream_t st);
 // One CTA whose bounded wait on a barrier nobody completes must run out and
 // set *err.

@@ -99,7 +99,7 @@ __device__ __forceinline__ float red16_sum(float v)
 // 64-row block; the row's 64-column tiles are swept left to right.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) rowstats_kernel(const T* __restrict__ Q, const T* __restrict__ K,
-                                                      int T_, float qscale, float* __restrict__ m2,
+                                                      int T_, int G, float qscale, float* __restrict__ m2,
                                                       float* __restrict__ lout)
 {
     extern __shared__ __align__(16) float tiles[];
@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(256) rowstats_kernel(const T* __restrict__ Q, 
     const int unit = blockIdx.y, ib = blockIdx.x;
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const T* Qu = Q + (size_t)unit * T_ * D;
-    const T* Ku = K + (size_t)unit * T_ * D;
+    const T* Ku = K + (size_t)(unit / G) * T_ * D;   // keys of this query unit
     load_tile_t<T, D>(Qs, Qu, ib * kTile, T_, qscale);
     float m[4];
     double l[4];
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(256) rowstats_kernel(const T* __restrict__ Q, 
 // so every c_j is summed in a fixed order (fp32 within a tile, fp64 across).
 template <typename T, int D>
 __global__ void __launch_bounds__(256) colsum_kernel(const T* __restrict__ Q, const T* __restrict__ K,
-                                                    int T_, float qscale, const float* __restrict__ m2,
+                                                    int T_, int G, float qscale, const float* __restrict__ m2,
                                                     const float* __restrict__ lin, double* __restrict__ cout)
 {
     extern __shared__ __align__(16) float tiles[];
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(256) colsum_kernel(const T* __restrict__ Q, co
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const int nb = (T_ + kTile - 1) / kTile;
     const T* Qu = Q + (size_t)unit * T_ * D;
-    const T* Ku = K + (size_t)unit * T_ * D;
+    const T* Ku = K + (size_t)(unit / G) * T_ * D;   // keys of this query unit
     load_tile_t<T, D>(Ks, Ku, jb * kTile, T_, 1.f);
     double csum[4] = {0.0, 0.0, 0.0, 0.0};
     for (int ib = jb; ib < nb; ++ib) {
@@ -738,12 +738,13 @@ cudaError_t stats_t(const CacheView& c, const PromptArgs& p, cudaStream_t st)
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
+    const int G = p.G > 1 ? p.G : 1;
     rowstats_kernel<T, D><<<grid, 256, smem, st>>>(reinterpret_cast<const T*>(p.Q),
-                                                 reinterpret_cast<const T*>(p.K), p.T, c.qscale, p.m2, p.l);
+                                                 reinterpret_cast<const T*>(p.K), p.T, G, c.qscale, p.m2, p.l);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     colsum_kernel<T, D><<<grid, 256, smem, st>>>(reinterpret_cast<const T*>(p.Q),
-                                               reinterpret_cast<const T*>(p.K), p.T, c.qscale, p.m2, p.l,
+                                               reinterpret_cast<const T*>(p.K), p.T, G, c.qscale, p.m2, p.l,
                                                p.c);
     return cudaGetLastError();
 }
@@ -834,6 +835,29 @@ cudaError_t launch_prompt_stats(const CacheView& c, const PromptArgs& p, cudaStr
     if (c.D == 128) return bf ? stats_t<__nv_bfloat16, 128>(c, p, st) : stats_t<float, 128>(c, p, st);
     if (c.D == 64) return bf ? stats_t<__nv_bfloat16, 64>(c, p, st) : stats_t<float, 64>(c, p, st);
     return cudaErrorInvalidValue;
+}
+
+namespace {
+
+// A cache unit's column sums: its heads' sums added in head order.
+__global__ void group_sum_kernel(const double* __restrict__ c, double* __restrict__ ckv, int U, int G, int T_)
+{
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long long)U * T_) return;
+    const long long u = i / T_, j = i - u * T_;
+    const double* cu = c + (size_t)u * G * T_ + j;
+    double s = 0.0;
+    for (int g = 0; g < G; ++g) s += cu[(size_t)g * T_];
+    ckv[i] = s;
+}
+
+}  // namespace
+
+cudaError_t launch_group_sum(const double* c, double* ckv, int U, int G, int T, cudaStream_t st)
+{
+    const long long n = (long long)U * T;
+    group_sum_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(c, ckv, U, G, T);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_select(const CacheView& c, const PromptArgs& p, cudaStream_t st)

@@ -270,20 +270,20 @@ __device__ __forceinline__ void tc_mma_loop(TcSmem& S, uint32_t tbase, int ntile
 // x % U (heaviest blocks first)
 __global__ void __launch_bounds__(kThreads, 2)
     rowstats_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK, int U,
-                       int T, int nb, float c2, float* __restrict__ m2, float* __restrict__ lout, int* err)
+                       int G, int T, int nb, float c2, float* __restrict__ m2, float* __restrict__ lout, int* err)
 {
     extern __shared__ unsigned char smem_raw[];
     TcSmem& S = tc_smem(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int u = blockIdx.x % U;
     const int ib = nb - 1 - (int)(blockIdx.x / U);
-    const int row0 = u * T;
+    const int row0 = u * T, krow0 = (u / G) * T;   // query rows, key rows
     const int ntiles = ib + 1;
     tc_setup(S, warp);
     const uint32_t tbase = S.tmem_base;
 
     if (warp == 0) {
-        if (lane == 0) tc_producer(S, &mapQ, &mapK, row0 + ib * kT, row0, 0, ib, err);
+        if (lane == 0) tc_producer(S, &mapQ, &mapK, row0 + ib * kT, krow0, 0, ib, err);
     } else if (warp == 1) {
         if (lane == 0) tc_mma_loop(S, tbase, ntiles, err);
         __syncwarp();
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 // (heaviest blocks, small jb, first) and sweeps query blocks jb..nb-1
 __global__ void __launch_bounds__(kThreads, 2)
     colsum_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK, int U,
-                     int T, int nb, float c2, const float* __restrict__ m2, const float* __restrict__ lin,
+                     int G, int T, int nb, float c2, const float* __restrict__ m2, const float* __restrict__ lin,
                      double* __restrict__ cout, int* err)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int u = blockIdx.x % U;
     const int jb = (int)(blockIdx.x / U);
-    const int row0 = u * T;
+    const int row0 = u * T, krow0 = (u / G) * T;   // query rows, key rows
     const int ntiles = nb - jb;
     const float* m2u = m2 + (size_t)u * T;
     const float* lu = lin + (size_t)u * T;
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t tbase = S.tmem_base;
 
     if (warp == 0) {
-        if (lane == 0) tc_producer(S, &mapK, &mapQ, row0 + jb * kT, row0, jb, nb - 1, err);
+        if (lane == 0) tc_producer(S, &mapK, &mapQ, krow0 + jb * kT, row0, jb, nb - 1, err);
     } else if (warp == 1) {
         if (lane == 0) tc_mma_loop(S, tbase, ntiles, err);
         __syncwarp();
@@ -491,8 +491,9 @@ bool prompt_tc_supported(const CacheView& c) { return c.dtype == 1 && c.D == kD;
 cudaError_t launch_prompt_stats_tc(const CacheView& c, const PromptArgs& p, cudaStream_t st)
 {
     CUtensorMap mq, mk;
+    const int G = p.G > 1 ? p.G : 1;
     const long long rows = (long long)c.U * p.T;
-    if (!make_map(&mq, p.Q, rows) || !make_map(&mk, p.K, rows)) return cudaErrorInvalidValue;
+    if (!make_map(&mq, p.Q, rows) || !make_map(&mk, p.K, rows / G)) return cudaErrorInvalidValue;
     const size_t smem = sizeof(TcSmem) + 1024;
     static bool configured[64] = {false};
     int dev = 0;
@@ -508,10 +509,10 @@ cudaError_t launch_prompt_stats_tc(const CacheView& c, const PromptArgs& p, cuda
     }
     const int nb = (p.T + kT - 1) / kT;
     const unsigned grid = (unsigned)(c.U * nb);
-    rowstats_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, c.U, p.T, nb, c.qscale, p.m2, p.l, c.err);
+    rowstats_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, c.U, G, p.T, nb, c.qscale, p.m2, p.l, c.err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    colsum_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, c.U, p.T, nb, c.qscale, p.m2, p.l, p.c, c.err);
+    colsum_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, c.U, G, p.T, nb, c.qscale, p.m2, p.l, p.c, c.err);
     return cudaGetLastError();
 }
 

@@ -23,6 +23,8 @@ TAG_PROMPT = 1
 TAG_DECODE = 2
 TAG_SHARED = 3
 TAG_LSH = 4
+TAG_QUERY = 5          # grouped-query workloads: prompt queries of each query head
+TAG_DQUERY = 6         # grouped-query workloads: decode queries of each query head
 
 
 @dataclass(frozen=True)
@@ -41,10 +43,16 @@ class Workload:
     structure: tuple = field(default=())
     lsh: bool = False
     lsh_seed: int = 4
+    groups: int = 1       # query heads per cache unit (grouped-query attention)
 
     @property
     def units(self) -> int:
+        """Cache units (batch x key/value heads)."""
         return self.batch * self.heads
+
+    @property
+    def query_units(self) -> int:
+        return self.units * self.groups
 
     @property
     def scale(self) -> float:
@@ -75,6 +83,10 @@ WORKLOADS = {
     # seeded N(0,1) 128 x 32 matrix, recent window 205.
     "hashevict-opt-6.7b": Workload("hashevict-opt-6.7b", 8, 32, 128, 2048, 256, 410, 205, 205,
                                    "bf16", 1, ("rank", 4, 2.0), lsh=True, lsh_seed=4),
+    # Grouped-query layer with the OPT-6.7B prompt and budget: 8 x 8 key/value heads,
+    # each shared by 4 query heads (32 query heads), d 128, rank-4 keys.
+    "gqa-8x8x4": Workload("gqa-8x8x4", 8, 8, 128, 2048, 256, 410, 205, 205, "bf16", 5,
+                          ("rank", 4, 2.0), groups=4),
 }
 
 
@@ -166,6 +178,13 @@ def decode_unit(w: Workload, unit: int, steps: Optional[int] = None,
     return _finish(w, q), _finish(w, k), _finish(w, v)
 
 
+def query_rows(w: Workload, qunit: int, n: int, decode: bool) -> np.ndarray:
+    """Grouped-query workloads: prompt (or decode) queries [n, d] of query
+    head `qunit` (head g of cache unit u is qunit = u * groups + g)."""
+    g = _rng(w.seed, TAG_DQUERY if decode else TAG_QUERY, qunit)
+    return _finish(w, g.standard_normal((n, w.head_dim), dtype=np.float32))
+
+
 def lsh_matrix(w: Workload) -> np.ndarray:
     """HashEvict projection matrix W [d, 32] float32, N(0, 1)."""
     g = _rng(w.lsh_seed, TAG_LSH, 0)
@@ -174,24 +193,35 @@ def lsh_matrix(w: Workload) -> np.ndarray:
 
 def generate(w: Workload, units: Optional[Sequence[int]] = None,
              steps: Optional[int] = None, prompt: Optional[int] = None):
-    """Inputs for the listed units (default all): dict with Q, K, V
-    [U, T, d] and q, k, v [S, U, d] (float32) plus W for LSH workloads."""
+    """Inputs for the listed (cache) units (default all): dict with Q, K, V
+    [U, T, d] and q, k, v [S, U, d] (float32) plus W for LSH workloads.  A
+    grouped-query workload has G = groups query heads per unit: Q [U*G, T, d]
+    and q [S, U*G, d], head g of the i-th listed unit in row i * G + g."""
     if units is None:
         units = range(w.units)
     units = list(units)
     S = w.steps if steps is None else steps
     T = w.prompt if prompt is None else prompt
     d = w.head_dim
-    U = len(units)
+    U, G = len(units), w.groups
     out = {
-        "Q": np.empty((U, T, d), np.float32), "K": np.empty((U, T, d), np.float32),
-        "V": np.empty((U, T, d), np.float32), "q": np.empty((S, U, d), np.float32),
+        "Q": np.empty((U * G, T, d), np.float32), "K": np.empty((U, T, d), np.float32),
+        "V": np.empty((U, T, d), np.float32), "q": np.empty((S, U * G, d), np.float32),
         "k": np.empty((S, U, d), np.float32), "v": np.empty((S, U, d), np.float32),
     }
     for i, u in enumerate(units):
-        out["Q"][i], out["K"][i], out["V"][i] = prompt_unit(w, u, T)
+        Qu, out["K"][i], out["V"][i] = prompt_unit(w, u, T)
         if S > 0:
-            out["q"][:, i], out["k"][:, i], out["v"][:, i] = decode_unit(w, u, S, T)
+            qu, out["k"][:, i], out["v"][:, i] = decode_unit(w, u, S, T)
+        if G == 1:
+            out["Q"][i] = Qu
+            if S > 0:
+                out["q"][:, i] = qu
+            continue
+        for j in range(G):
+            out["Q"][i * G + j] = query_rows(w, u * G + j, T, False)
+            if S > 0:
+                out["q"][:, i * G + j] = query_rows(w, u * G + j, S, True)
     if w.lsh:
         out["W"] = lsh_matrix(w)
     return out
@@ -202,7 +232,8 @@ def generate_device(w: Workload, seed_offset: int = 0, prompt: Optional[int] = N
     """The same recipe drawn with torch's device generator, for full-size
     benchmark pools (values differ from ``generate``; distributions and
     structure match).  Returns device tensors Q, K, V [U, T, d] and q, k, v
-    [S, U, d] in the workload's element type, plus W [d, 32] for LSH."""
+    [S, U, d] in the workload's element type, plus W [d, 32] for LSH; a
+    grouped-query workload's Q and q have U * groups rows."""
     import torch
 
     T = w.prompt if prompt is None else prompt
@@ -249,12 +280,12 @@ def generate_device(w: Workload, seed_offset: int = 0, prompt: Optional[int] = N
         raise ValueError(kind)
 
     out = {
-        "Q": normal(U, T, d).to(dt).contiguous(),
+        "Q": normal(U * w.groups, T, d).to(dt).contiguous(),
         "K": keys(normal(U, T, d), 0).to(dt).contiguous(),
         "V": normal(U, T, d).to(dt).contiguous(),
     }
     if S > 0:
-        out["q"] = normal(S, U, d).to(dt).contiguous()
+        out["q"] = normal(S, U * w.groups, d).to(dt).contiguous()
         out["k"] = keys(normal(U, S, d), T).transpose(0, 1).to(dt).contiguous()
         out["v"] = normal(S, U, d).to(dt).contiguous()
     if w.lsh:

@@ -246,6 +246,9 @@ def h2o_decode_step_gqa(st, q, k, v, p, r, scale, forced=None):
     lib().oracle_h2o_decode_step_gqa(U, G, d, st.B, r, float(scale), int(p), st.K, st.V,
                                      st.score, st.pos, st.occ, q, k, v, out,
                                      _ptr(victim), _ptr(margin), _ptr(evicted), _ptr(f))
+    if hasattr(st, "kq"):
+        # int8 cache: as for one head, the written slot stores the quantised row
+        _kv8_written(st, _written_slots(victim, st.occ))
     return out, victim, margin, evicted
 
 

@@ -44,20 +44,25 @@ def widen(a, dtype):
 
 
 class Dev:
-    """One device handle (H2O or LSH) for U units with its own stream."""
+    """One device handle (H2O or LSH) for U units with its own stream;
+    groups > 1: an H2O handle whose U cache units are each shared by that
+    many query heads (q and out then have U * groups rows)."""
 
-    def __init__(self, kind, U, d, B, H, r, dtype, scale, W=None, split=0, kv8=False):
+    def __init__(self, kind, U, d, B, H, r, dtype, scale, W=None, split=0, kv8=False, groups=0):
         self.kind, self.U, self.d, self.B, self.dtype, self.kv8 = kind, U, d, B, dtype, kv8
+        self.G = max(groups, 1)
         self.stream = torch.cuda.current_stream()
         dt = cdtype(dtype) | (L.H2O_KV8 if kv8 else 0)
-        if kind == "h2o":
+        if kind == "h2o" and groups:
+            self.h = L.h2o_init_gqa(B, H, r, 1, U, groups, d, dt, scale, self.stream)
+        elif kind == "h2o":
             self.h = L.h2o_init(B, H, r, 1, U, d, dt, scale, self.stream)
         else:
             self.Wd = torch.from_numpy(np.ascontiguousarray(W, np.float32)).cuda()
             self.h = L.lsh_init(B, r, 1, U, d, dt, scale, self.Wd, self.stream)
         if split:
             L.h2o_set_decode_split(self.h, split)
-        self.out = torch.empty((U, d), dtype=torch.float32, device="cuda")
+        self.out = torch.empty((U * self.G, d), dtype=torch.float32, device="cuda")
         self.victim = torch.empty((U,), dtype=torch.int32, device="cuda")
 
     def prefill(self, Q, K, V):
@@ -95,7 +100,7 @@ class Dev:
                     occ=occ, npos=npos)
 
     def stats(self, T):
-        m = np.empty((self.U, T), np.float32); l = np.empty((self.U, T), np.float32)
+        m = np.empty((self.U * self.G, T), np.float32); l = np.empty((self.U * self.G, T), np.float32)
         c = np.empty((self.U, T))
         L.h2o_get_prefill_stats(self.h, m, l, c)
         return m, l, c
@@ -135,8 +140,13 @@ def kept_lists(pos, B):
 
 def align_prefill(dev_state, Q, K, V, B, H, r, scale):
     """Oracle prompt phase compared with the device's; returns (oracle state,
-    oracle column sums, near-tie count).  Fails on any other disagreement."""
-    st, c, kept_o, margin = oracle.h2o_prefill(Q, K, V, B, H, r, scale)
+    oracle column sums, near-tie count).  Fails on any other disagreement.
+    Q with more rows than K: a grouped-query cache (Q.shape[0] // K.shape[0]
+    heads per unit)."""
+    if Q.shape[0] != K.shape[0]:
+        st, c, kept_o, margin, _ = oracle.h2o_prefill_gqa(Q, K, V, B, H, r, scale)
+    else:
+        st, c, kept_o, margin = oracle.h2o_prefill(Q, K, V, B, H, r, scale)
     kept_g = kept_lists(dev_state["pos"], B)
     near = 0
     U, T = c.shape
@@ -156,14 +166,16 @@ def align_prefill(dev_state, Q, K, V, B, H, r, scale):
 
 
 def h2o_lockstep(dev, st, q, k, v, T, r, scale, check_every=1):
-    """Run the device and the oracle step by step; returns near-tie count."""
+    """Run the device and the oracle step by step; returns near-tie count.
+    q with more rows than k: a grouped-query cache."""
     near = 0
     S = q.shape[0]
+    step = oracle.h2o_decode_step_gqa if q.shape[1] != k.shape[1] else oracle.h2o_decode_step
     for t in range(S):
         p = T + t
         out_g, vic_g = dev.step(q[t], k[t], v[t])
         before = st.copy()
-        out_o, vic_o, mg, _ = oracle.h2o_decode_step(st, q[t], k[t], v[t], p, r, scale)
+        out_o, vic_o, mg, _ = step(st, q[t], k[t], v[t], p, r, scale)
         mism = vic_g != vic_o
         if mism.any():
             hard = mism & ~(mg < NEAR_TIE)
@@ -172,7 +184,7 @@ def h2o_lockstep(dev, st, q, k, v, T, r, scale, check_every=1):
             near += int(mism.sum())
             st = before
             forced = np.where(mism, vic_g, -1).astype(np.int32)
-            out_o, vic_o, mg, _ = oracle.h2o_decode_step(st, q[t], k[t], v[t], p, r, scale, forced)
+            out_o, vic_o, mg, _ = step(st, q[t], k[t], v[t], p, r, scale, forced)
         check_out(out_g, out_o, "step %d out" % t)
         if (t % check_every == 0) or t == S - 1:
             g = dev.state()

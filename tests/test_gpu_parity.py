@@ -95,6 +95,20 @@ def test_hashevict_units(split):
     dev.close()
 
 
+def test_h2o_one_cta_with_a_budget_near_the_chunk_limit():
+    # one CTA per unit holding 1000 slots: every slot of the chunk (past 960,
+    # the first 5 x 192) must take part in the score update and the arg-min
+    T, B, H, r, d = 1300, 1000, 500, 500, 128
+    U, S = 2, 6
+    Q, K, V, q, k, v = _rand(77, U, T, S, d, "bf16")
+    scale = 1.0 / np.sqrt(d)
+    dev = Dev("h2o", U, d, B, H, r, "bf16", scale, split=1)
+    dev.prefill(Q, K, V)
+    st, _, _ = align_prefill(dev.state(), Q, K, V, B, H, r, scale)
+    h2o_lockstep(dev, st, q, k, v, T, r, scale)
+    dev.close()
+
+
 @pytest.mark.parametrize("T,B,H,r", [
     (5, 8, 4, 4),        # prompt shorter than the budget: append phase
     (1, 8, 4, 4),        # single-token prompt

@@ -55,3 +55,23 @@ def test_structures_present():
     w2 = wl.WORKLOADS["opt-30b"]
     Q, K, V = wl.prompt_unit(w2, 3)
     assert K.shape == (512, 128)
+
+
+def test_grouped_query_workload_layout():
+    # G query heads per cache unit: head g of the i-th listed unit in row
+    # i * G + g; a subset agrees with the full draw; keys and values are the
+    # unit's own (the same recipe as a one-head workload)
+    w = wl.WORKLOADS["gqa-8x8x4"]
+    G = w.groups
+    assert G == 4 and w.query_units == 4 * w.units
+    part = wl.generate(w, units=[3, 1], steps=2, prompt=32)
+    assert part["Q"].shape == (2 * G, 32, 128) and part["K"].shape == (2, 32, 128)
+    assert part["q"].shape == (2, 2 * G, 128) and part["k"].shape == (2, 2, 128)
+    one = wl.generate(w, units=[1], steps=2, prompt=32)
+    np.testing.assert_array_equal(part["Q"][G:2 * G], one["Q"])
+    np.testing.assert_array_equal(part["q"][:, G:2 * G], one["q"])
+    np.testing.assert_array_equal(part["K"][1], one["K"][0])
+    _, K, V = wl.prompt_unit(w, 1, prompt=32)
+    np.testing.assert_array_equal(one["K"][0], K)
+    # the heads of one unit are distinct draws
+    assert not np.array_equal(one["Q"][0], one["Q"][1])
