@@ -18,6 +18,11 @@ copied out inside the timed region.  The CPU oracle is timed on a bounded
 sample of the same job.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With --gqa the job is H2O alone on a grouped-query layer (8 x 8 key/value
+heads, each cache shared by 4 query heads; the same prompt, budget and decode
+steps): one decode step there advances all 64 cache units (256 query heads)
+of one layer cache by one token.
 """
 import argparse
 import hashlib
@@ -52,6 +57,8 @@ def parse():
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--kv8", action="store_true",
                    help="int8 cache slots (one fp32 scale per row) for both variants")
+    p.add_argument("--gqa", action="store_true",
+                   help="H2O on the grouped-query layer (8 x 8 key/value heads x 4 query heads)")
     return p.parse_args()
 
 
@@ -175,6 +182,21 @@ def decode_bytes(U, B, d, eb, lsh, kv8=False):
     return U * (B * per_slot + fixed)
 
 
+def decode_bytes_gqa(U, G, B, d, eb, kv8=False):
+    """Algorithmic HBM bytes of one full-cache grouped-query H2O decode launch
+    over U cache units of G query heads: per live slot K and V rows (int8
+    codes plus an 8-byte scale pair with kv8), score read+write and position
+    read, each once per unit (the heads share them); per query head q in and
+    fp32 out; per unit k, v in, one K/V row written (and its scale pair),
+    victim score and position written, unit state read and written."""
+    row = d * eb
+    crow = d if kv8 else row
+    sc = 8 if kv8 else 0
+    per_slot = 2 * crow + sc + 8 + 8 + 4
+    fixed = G * (row + 4 * d) + 2 * row + 2 * crow + sc + 8 + 4 + 16
+    return U * (B * per_slot + fixed)
+
+
 def prefill_flops(U, T, d):
     """Both score passes of the H2O prompt phase: 2 x (2 d flops per causal
     (i, j) pair, T (T + 1) / 2 pairs per unit)."""
@@ -208,6 +230,22 @@ def oracle_job(w, wl_lsh, units, S, kv8=False):
     return time.perf_counter() - t0, oracle.get_threads()
 
 
+def oracle_job_gqa(w, units, S, kv8=False):
+    """The CPU oracle on a sample of cache units of a grouped-query workload:
+    H2O prompt + S steps.  Returns (seconds, threads)."""
+    import oracle
+    from kv_cache_eviction_h2o_gb300 import workloads as wl
+    g = wl.generate(w, units=units, steps=S)
+    T = w.prompt
+    t0 = time.perf_counter()
+    st, _, _, _, _ = oracle.h2o_prefill_gqa(g["Q"], g["K"], g["V"], w.budget, w.heavy, w.recent, w.scale)
+    if kv8:
+        oracle.kv8(st)
+    for t in range(S):
+        oracle.h2o_decode_step_gqa(st, g["q"][t], g["k"][t], g["v"][t], T + t, w.recent, w.scale)
+    return time.perf_counter() - t0, oracle.get_threads()
+
+
 def oracle_rate(w, seconds, n_units, S):
     """Oracle time on n_units scaled to the metric: decode steps (all units of
     one layer cache advancing one token, both variants) per second."""
@@ -221,6 +259,8 @@ def run_reference(args):
     world, rank, _ = dist_setup(args)
     if rank != 0:
         return
+    if args.gqa:
+        return run_reference_gqa(args, world)
     from kv_cache_eviction_h2o_gb300 import workloads as wl
     w = wl.WORKLOADS[WORKLOAD]
     wl_lsh = wl.WORKLOADS["hashevict-" + WORKLOAD]
@@ -249,6 +289,45 @@ def run_reference(args):
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
+
+
+def run_reference_gqa(args, world):
+    from kv_cache_eviction_h2o_gb300 import workloads as wl
+    w = wl.WORKLOADS[GQA_WORKLOAD]
+    S = args.decode_steps or w.steps
+    n = max(1, args.oracle_units // 16)
+    units = list(range(n))
+    for _ in range(args.warmup):
+        oracle_job_gqa(w, units, S, args.kv8)
+    times = []
+    threads = 1
+    for _ in range(args.steps):
+        t, threads = oracle_job_gqa(w, units, S, args.kv8)
+        times.append(t)
+    total = sum(times)
+    value = S / (total / len(times) * w.units / n)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * total / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": gqa_config_name(w, S, 1, args.kv8)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "%d of %d cache units of one %s layer per step (prompt %d, %d decode steps, H2O)"
+                                   % (n, w.units, GQA_WORKLOAD, w.prompt, S)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+GQA_WORKLOAD = "gqa-8x8x4"
+
+
+def gqa_config_name(w, S, NL, kv8):
+    return ("%s grouped-query layer x%d (%d x %d key/value heads x %d query heads): H2O, prompt %d -> %d decode "
+            "steps, budget %d (%d heavy + %d recent)%s" % (GQA_WORKLOAD, NL, w.batch, w.heads, w.groups, w.prompt,
+                                                          S, w.budget, w.heavy, w.recent,
+                                                          ", int8 cache slots" if kv8 else ""))
 
 
 # -------------------------------------------------------------------- ours
@@ -567,10 +646,237 @@ def run_e2e(args, L, torch, layers, h2o, lsh, out_h, out_l, vic_h, vic_l, W, S, 
             "ms_per_step": secs * 1000.0, "steps": n, "launch": mode}
 
 
+def run_gqa(args):
+    """H2O on the grouped-query layer: L layer caches, prompt phase then S
+    decode steps token-major over the layers, replayed from CUDA graphs with
+    inputs in HBM; e2e through the public API with host copies."""
+    import torch
+    import torch.distributed as dist
+
+    from kv_cache_eviction_h2o_gb300 import binding as L
+    from kv_cache_eviction_h2o_gb300 import build as lib_build
+    from kv_cache_eviction_h2o_gb300 import workloads as wl
+
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    lib_build.build()
+    L.lib()
+    w = wl.WORKLOADS[GQA_WORKLOAD]
+    S = args.decode_steps or w.steps
+    NL = args.layers
+    U, G, T, d, B = w.units, w.groups, w.prompt, w.head_dim, w.budget
+    dt = L.H2O_BF16 | (L.H2O_KV8 if args.kv8 else 0)
+    stream = torch.cuda.Stream()
+    layers = []
+    with torch.cuda.stream(stream):
+        for li in range(NL):
+            layers.append(wl.generate_device(w, seed_offset=li + 1000 * rank, steps=S))
+    torch.cuda.synchronize()
+    hs = [L.h2o_init_gqa(B, w.heavy, w.recent, w.batch, w.heads, G, d, dt, w.scale, stream) for _ in range(NL)]
+    outs = [torch.empty((S, U * G, d), dtype=torch.float32, device="cuda") for _ in range(NL)]
+    vics = [torch.empty((S, U), dtype=torch.int32, device="cuda") for _ in range(NL)]
+
+    def pre():
+        for li in range(NL):
+            g = layers[li]
+            L.h2o_prefill(hs[li], g["Q"], g["K"], g["V"], T)
+
+    def dec():
+        for t in range(S):
+            for li in range(NL):
+                g = layers[li]
+                L.h2o_decode_step(hs[li], g["q"][t], g["k"][t], g["v"][t], outs[li][t], vics[li][t])
+
+    phases = [("h2o_prefill", pre), ("h2o_decode", dec)]
+    with torch.cuda.stream(stream):
+        for _, f in phases:
+            f()
+    for h in hs:
+        L.h2o_sync(h)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for name, f in phases:
+            gr = torch.cuda.CUDAGraph()
+            gr.capture_begin()
+            f()
+            gr.capture_end()
+            graphs.append((name, gr))
+    torch.cuda.synchronize()
+
+    def one_step(evs=None):
+        with torch.cuda.stream(stream):
+            for i, (_, gr) in enumerate(graphs):
+                gr.replay()
+                if evs is not None:
+                    evs[i].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    for h in hs:
+        L.h2o_sync(h)
+
+    clocks = Clocks(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    step_events = [[torch.cuda.Event(enable_timing=True) for _ in graphs] for _ in range(args.steps)]
+    start.record(stream)
+    for i in range(args.steps):
+        one_step(step_events[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    elapsed_ms = start.elapsed_time(end)
+    phase_ms = {name: 0.0 for name, _ in graphs}
+    for i in range(args.steps):
+        prev = start if i == 0 else step_events[i - 1][-1]
+        for j, (name, _) in enumerate(graphs):
+            phase_ms[name] += prev.elapsed_time(step_events[i][j])
+            prev = step_events[i][j]
+    for h in hs:
+        L.h2o_sync(h)
+    elapsed_ms = max_over_ranks(elapsed_ms, world, device="cuda")
+    K = args.steps
+    ms_per_step = elapsed_ms / K
+    value = world * S * NL / (ms_per_step / 1000.0)
+    hbm, tf_burst, tf_sus, peak_src = load_peaks()
+
+    t_dec = phase_ms["h2o_decode"] / (S * NL * K) / 1000.0
+    by = decode_bytes_gqa(U, G, B, d, 2, args.kv8)
+    ach = by / t_dec / 1e9
+    rl = [{"kernel": "h2o_decode_gqa", "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+           "frac": ach / hbm, "traffic": ncu_traffic("h2o_gqa" + ("_kv8" if args.kv8 else "")),
+           "algorithmic_bytes": by, "launch_us": t_dec * 1e6, "peak_source": peak_src,
+           "share": phase_ms["h2o_decode"] / elapsed_ms}]
+    t_pre = phase_ms["h2o_prefill"] / (NL * K) / 1000.0
+    fl = prefill_flops(U * G, T, d)
+    ach = fl / t_pre / 1e12
+    rl.append({"kernel": "h2o_prefill_gqa", "bound": "tensor", "achieved": ach, "peak": tf_sus,
+               "unit": "TFLOP/s", "frac": ach / tf_sus, "traffic": None, "algorithmic_flops": fl,
+               "launch_us": t_pre * 1e6, "peak_source": peak_src, "share": phase_ms["h2o_prefill"] / elapsed_ms})
+    dominant = max(rl, key=lambda r: r["share"])
+    main_rl = {k: dominant[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+    main_rl["kernel"] = dominant["kernel"]
+    main_rl["peak_source"] = peak_src
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e_gqa(args, L, torch, layers, hs, outs, vics, S, NL, T, stream, world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        n = max(1, args.oracle_units // 4)
+        secs, threads = oracle_job_gqa(w, list(range(n)), S, args.kv8)
+        cpu = {"value": S / (secs * U / n), "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": "%d of %d cache units of one layer (prompt %d, %d decode steps, H2O), %.1f s"
+                         % (n, U, T, S, secs)}
+    # per layer: prompt scores (2 or 3 launches), group sum, select, gather; per step one launch
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": gqa_config_name(w, S, NL, args.kv8),
+                   "cache": "int8 codes + fp32 scale per row" if args.kv8 else "bf16",
+                   "batch": w.batch, "kv_heads": w.heads, "groups": G, "head_dim": d, "prompt": T,
+                   "decode_steps": S, "budget": B, "layers": NL, "global_batch": w.batch * world,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2: %d layer caches (%.0f MB) + prompts (%.0f MB); a cache is reused "
+                         "only after %d others" % (NL, NL * decode_bytes_gqa(U, G, B, d, 2, args.kv8) / 1e6,
+                                                   NL * (G + 2) * U * T * d * 2 / 1e6, NL - 1),
+                   "step": "one decode step = all %d cache units (%d query heads) of one layer cache advance one "
+                           "token; prompt phases inside the timed step" % (U, U * G)},
+        "roofline": main_rl,
+        "rooflines": rl,
+        "phases_ms_per_step": {k: v / K for k, v in phase_ms.items()},
+        "cpu_baseline": cpu,
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": (NL * 5 + S * NL) * K,
+    }
+    for h in hs:
+        L.h2o_destroy(h)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e_gqa(args, L, torch, layers, hs, outs, vics, S, NL, T, stream, world):
+    """The grouped-query job through the public API: every input copied in
+    from pinned host memory and every output copied out inside the timed
+    region, one step captured into a CUDA graph."""
+    host_in = [{k: g[k].cpu().pin_memory() for k in ("Q", "K", "V", "q", "k", "v")} for g in layers]
+    host_out = [(torch.empty(o.shape, dtype=o.dtype).pin_memory(), torch.empty(v.shape, dtype=v.dtype).pin_memory())
+                for o, v in zip(outs, vics)]
+    h2d = sum(x.numel() * x.element_size() for hi in host_in for x in hi.values())
+    d2h = sum(x.numel() * x.element_size() for ho in host_out for x in ho)
+    copy_stream = torch.cuda.Stream()
+    ready = [torch.cuda.Event() for _ in range(NL)]
+    ready_dec = torch.cuda.Event()
+
+    def step():
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_stream(stream)
+            for li in range(NL):
+                for k in ("Q", "K", "V"):
+                    layers[li][k].copy_(host_in[li][k], non_blocking=True)
+                ready[li].record(copy_stream)
+            for li in range(NL):
+                for k in ("q", "k", "v"):
+                    layers[li][k].copy_(host_in[li][k], non_blocking=True)
+            ready_dec.record(copy_stream)
+        with torch.cuda.stream(stream):
+            for li in range(NL):
+                stream.wait_event(ready[li])
+                g = layers[li]
+                L.h2o_prefill(hs[li], g["Q"], g["K"], g["V"], T)
+            stream.wait_event(ready_dec)
+            for t in range(S):
+                for li in range(NL):
+                    g = layers[li]
+                    L.h2o_decode_step(hs[li], g["q"][t], g["k"][t], g["v"][t], outs[li][t], vics[li][t])
+            for li in range(NL):
+                host_out[li][0].copy_(outs[li], non_blocking=True)
+                host_out[li][1].copy_(vics[li], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        gr.capture_begin()
+        step()
+        gr.capture_end()
+    torch.cuda.synchronize()
+
+    def run():
+        with torch.cuda.stream(stream):
+            gr.replay()
+    run()
+    torch.cuda.synchronize()
+    n = max(1, min(args.steps, 3))
+    t0 = time.perf_counter()
+    for _ in range(n):
+        run()
+    torch.cuda.synchronize()
+    secs = (time.perf_counter() - t0) / n
+    return {"value": world * S * NL / secs, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": secs * 1000.0, "steps": n, "launch": "graph"}
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.gqa:
+        run_gqa(args)
     else:
         run_ours(args)
 
