@@ -60,6 +60,12 @@ def lib():
         L.oracle_lsh_decode_step.argtypes = [_i, _i, _i, _i, _d, _i, _f64p, _f64p, _u32p,
                                              _i32p, _i32p, _f64p, _f64p, _f64p, _f32p,
                                              _f64p, _vp]
+        L.oracle_sh_prompt_masks.argtypes = [_i, _i, _i, _d, _f64p, _f64p, _u32p, _f64p]
+        L.oracle_sh_select.argtypes = [_i, _i, _i, _i, _u32p, _i32p]
+        L.oracle_sh_select.restype = _i
+        L.oracle_sh_decode_step.argtypes = [_i, _i, _i, _i, _d, _i, _f64p, _f64p, _u32p,
+                                            _i32p, _i32p, _f64p, _f64p, _f64p, _f64p,
+                                            _vp, _vp, _vp]
         _lib = L
     return _lib
 
@@ -299,3 +305,78 @@ def lsh_decode_step(st, q, k, v, W, p, r, scale):
     if hasattr(st, "kq"):
         _kv8_written(st, _written_slots(victim, st.occ))
     return out, victim
+
+
+class SHState:
+    """Oracle cache of the persistence-of-importance rule for U units: rows
+    (float64), each slot's 32-step pivotal history (uint32, bit 0 = the
+    latest step), positions and occupancy."""
+
+    def __init__(self, U, B, d):
+        self.U, self.B, self.d = U, B, d
+        self.K = np.zeros((U, B, d))
+        self.V = np.zeros((U, B, d))
+        self.mask = np.zeros((U, B), dtype=np.uint32)
+        self.pos = np.full((U, B), -1, dtype=np.int32)
+        self.occ = np.zeros(U, dtype=np.int32)
+
+    def copy(self):
+        s = SHState(self.U, self.B, self.d)
+        for name in ("K", "V", "mask", "pos", "occ"):
+            setattr(s, name, getattr(self, name).copy())
+        return s
+
+
+def sh_prompt_masks(Q, K, scale):
+    """Pivotal histories of every prompt token after the prompt: [U, T]
+    uint32 (bit T-1-i set when the token was pivotal for query row i, over
+    the last 32 rows), and the smallest |P * m - 1| among those decisions
+    per unit."""
+    Q = _c64(Q); K = _c64(K)
+    U, T, d = Q.shape
+    mask = np.empty((U, T), dtype=np.uint32)
+    margin = np.empty(U)
+    lib().oracle_sh_prompt_masks(U, T, d, float(scale), Q, K, mask, margin)
+    return mask, margin
+
+
+def sh_build_cache(K, V, mask, kept, B):
+    """Cache from explicit kept lists ([U, B] ascending positions, -1
+    padded): slot s holds kept position s with that token's history."""
+    K = _c64(K); V = _c64(V)
+    U, T, d = K.shape
+    st = SHState(U, B, d)
+    for u in range(U):
+        ks = kept[u][kept[u] >= 0]
+        n = len(ks)
+        st.K[u, :n] = K[u, ks]
+        st.V[u, :n] = V[u, ks]
+        st.mask[u, :n] = mask[u, ks]
+        st.pos[u, :n] = ks
+        st.occ[u] = n
+    return st
+
+
+def sh_prefill(Q, K, V, B, H, r, scale):
+    """Prompt phase of the persistence-of-importance cache: returns (state,
+    masks [U, T], kept [U, B] (-1 padded), margin [U])."""
+    mask, margin = sh_prompt_masks(Q, K, scale)
+    U, T = mask.shape
+    kept = np.empty((U, B), dtype=np.int32)
+    for u in range(U):
+        lib().oracle_sh_select(T, B, H, r, np.ascontiguousarray(mask[u]), kept[u])
+    return sh_build_cache(K, V, mask, kept, B), mask, kept, margin
+
+
+def sh_decode_step(st, q, k, v, p, r, scale, forced=None):
+    """One decode step in place on ``st``.  Returns (out [U, d], victim [U],
+    margin [U])."""
+    q = _c64(q); k = _c64(k); v = _c64(v)
+    U, d = q.shape
+    out = np.empty((U, d))
+    victim = np.empty(U, dtype=np.int32)
+    margin = np.empty(U)
+    f = None if forced is None else np.ascontiguousarray(forced, dtype=np.int32)
+    lib().oracle_sh_decode_step(U, d, st.B, r, float(scale), int(p), st.K, st.V, st.mask,
+                                st.pos, st.occ, q, k, v, out, _ptr(victim), _ptr(margin), _ptr(f))
+    return out, victim, margin

@@ -59,7 +59,15 @@
  *    codes and one fp32 scale, amax/127, with codes rint(x * (127/amax))
  *    in fp32, half to even; a step attends to its own new token at full
  *    precision and stores it quantised (the quantiser is below; the mode's
- *    bookkeeping is in the Python wrapper).
+ *    bookkeeping is in the Python wrapper);
+ *  - the persistence-of-importance rule (an optional cache kind, [SH]): a
+ *    token is pivotal at a step when its attention probability exceeds
+ *    the uniform share 1/m over the m tokens attended that step; each
+ *    token keeps its pivotal flags of the last 32 steps (prompt rows count
+ *    as steps); its importance is the number of flags set; the victim is
+ *    the candidate with the lowest importance, then the oldest position;
+ *    the prompt keeps the recent window and the H most important earlier
+ *    tokens, ties to the newer position.
  *
  * parity unpinned: the readings above that have no printed example on the
  * pages (self-attention of the new token, accumulate-before-evict order,
@@ -599,6 +607,167 @@ void oracle_lsh_decode_step(int U, int d, int B, int r, double scale, int p,
             double P = exp(z[s] - mx) / lsum;
             for (int e = 0; e < d; ++e) ou[e] += P * Vu[(size_t)s * d + e];
         }
+        free(z);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Persistence of importance [SH abstract: only tokens that were        */
+/* pivotal -- had a substantial influence -- at some step keep          */
+/* influencing later steps; the fixed-budget cache stores the pivotal   */
+/* tokens preferentially].  The reading (listed in the design notes):   */
+/*   pivotal at a step:  P_j > 1/m, m = tokens attended that step,      */
+/*                       tested as P_j * m > 1 in fp64;                 */
+/*   history:            a 32-bit word per token, bit 0 = the latest    */
+/*                       step; each step shifts it left by one and puts */
+/*                       the new flag in bit 0 (older flags fall out);  */
+/*   importance:         the number of set bits;                        */
+/*   victim:             among slots with position <= p - r (every live */
+/*                       slot if none), the lowest importance, then the */
+/*                       lowest position.                               */
+/* `margin` reports min |P_j * m - 1| over the flags a call decided     */
+/* with m > 1, so that a caller can tell a decision that fp32 rounding  */
+/* could flip (with m = 1, P = 1 exactly and the flag is 0).            */
+/* ------------------------------------------------------------------ */
+static int bits_set(uint32_t x)
+{
+    int n = 0;
+    for (int b = 0; b < 32; ++b) n += (int)((x >> b) & 1u);
+    return n;
+}
+
+/* Prompt flags: row i (query i, keys 0..i, m = i + 1 tokens) is a step;   */
+/* the last 32 rows T-32..T-1 set bit T-1-i of mask[j] for every pivotal */
+/* key j <= i.  mask: [U][T]; margin: [U].                               */
+void oracle_sh_prompt_masks(int U, int T, int d, double scale, const double* Q, const double* K,
+                            uint32_t* mask, double* margin)
+{
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int u = 0; u < U; ++u) {
+        const double* Qu = Q + (size_t)u * T * d;
+        const double* Ku = K + (size_t)u * T * d;
+        uint32_t* mu = mask + (size_t)u * T;
+        double* z = (double*)malloc(sizeof(double) * (size_t)T);
+        double mg = INFINITY;
+        for (int j = 0; j < T; ++j) mu[j] = 0u;
+        const int i0 = T > 32 ? T - 32 : 0;
+        for (int i = i0; i < T; ++i) {
+            double mx = -INFINITY;
+            for (int j = 0; j <= i; ++j) {
+                z[j] = scale * dot(Qu + (size_t)i * d, Ku + (size_t)j * d, d);
+                if (z[j] > mx) mx = z[j];
+            }
+            double l = 0.0;
+            for (int j = 0; j <= i; ++j) l += exp(z[j] - mx);
+            for (int j = 0; j <= i; ++j) {
+                const double t = exp(z[j] - mx) / l * (double)(i + 1);
+                if (t > 1.0) mu[j] |= 1u << (T - 1 - i);
+                if (i > 0 && fabs(t - 1.0) < mg) mg = fabs(t - 1.0);   /* m = 1: P = 1 exactly */
+            }
+        }
+        margin[u] = mg;
+        free(z);
+    }
+}
+
+/* Prompt selection: all T tokens when T <= B; otherwise the recent window  */
+/* T-r..T-1 and the H tokens among 0..T-r-1 with the most set bits, ties to */
+/* the newer position.  kept: [B] ascending positions, -1 padded; returns   */
+/* the number kept.                                                         */
+int oracle_sh_select(int T, int B, int H, int r, const uint32_t* mask, int* kept)
+{
+    for (int s = 0; s < B; ++s) kept[s] = -1;
+    if (T <= B) {
+        for (int j = 0; j < T; ++j) kept[j] = j;
+        return T;
+    }
+    const int ncand = T - r;
+    char* keep = (char*)calloc((size_t)T, 1);
+    for (int j = ncand; j < T; ++j) keep[j] = 1;
+    for (int h = 0; h < H && h < ncand; ++h) {
+        int best = -1;
+        for (int j = ncand - 1; j >= 0; --j) {        /* newest first: ties stay with the newer */
+            if (keep[j]) continue;
+            if (best < 0 || bits_set(mask[j]) > bits_set(mask[best])) best = j;
+        }
+        keep[best] = 1;
+    }
+    int n = 0;
+    for (int j = 0; j < T; ++j)
+        if (keep[j]) kept[n++] = j;
+    free(keep);
+    return n;
+}
+
+/* One decode step for U units (new token at position p): attend over the  */
+/* n live slots and the new token, shift every live slot's history and set  */
+/* this step's flag, evict (when full) by the rule above, insert the new   */
+/* token with its own flag as its history.  K, V: [U][B][d]; mask, pos:     */
+/* [U][B]; occ: [U]; q, k, v: [U][d]; out: [U][d]; victim: [U] (-1 when     */
+/* appended); margin: [U]; forced: [U] or NULL (a slot >= 0 replaces the     */
+/* rule's choice).                                                          */
+void oracle_sh_decode_step(int U, int d, int B, int r, double scale, int p,
+                           double* cK, double* cV, uint32_t* mask, int* pos, int* occ,
+                           const double* q, const double* k, const double* v,
+                           double* out, int* victim, double* margin, const int* forced)
+{
+    #pragma omp parallel for schedule(dynamic, 4)
+    for (int u = 0; u < U; ++u) {
+        double* Ku = cK + (size_t)u * B * d;
+        double* Vu = cV + (size_t)u * B * d;
+        uint32_t* mu = mask + (size_t)u * B;
+        int* pu = pos + (size_t)u * B;
+        const double* qu = q + (size_t)u * d;
+        const double* ku = k + (size_t)u * d;
+        const double* vu = v + (size_t)u * d;
+        double* ou = out + (size_t)u * d;
+        const int n = occ[u];
+        double* z = (double*)malloc(sizeof(double) * (size_t)(n + 1));
+        double mx = -INFINITY;
+        for (int s = 0; s < n; ++s) {
+            z[s] = scale * dot(qu, Ku + (size_t)s * d, d);
+            if (z[s] > mx) mx = z[s];
+        }
+        z[n] = scale * dot(qu, ku, d);
+        if (z[n] > mx) mx = z[n];
+        double l = 0.0;
+        for (int s = 0; s <= n; ++s) l += exp(z[s] - mx);
+        for (int e = 0; e < d; ++e) ou[e] = 0.0;
+        double mg = INFINITY;
+        uint32_t flag_new = 0u;
+        for (int s = 0; s <= n; ++s) {
+            const double P = exp(z[s] - mx) / l;
+            const double* vs = (s < n) ? Vu + (size_t)s * d : vu;
+            for (int e = 0; e < d; ++e) ou[e] += P * vs[e];
+            const double t = P * (double)(n + 1);
+            const uint32_t f = t > 1.0 ? 1u : 0u;
+            if (n > 0 && fabs(t - 1.0) < mg) mg = fabs(t - 1.0);        /* m = 1: P = 1 exactly */
+            if (s < n) mu[s] = (mu[s] << 1) | f;
+            else flag_new = f;
+        }
+        int slot;
+        if (n < B) {
+            slot = n;
+            occ[u] = n + 1;
+            if (victim) victim[u] = -1;
+        } else {
+            int ncand = 0;
+            for (int s = 0; s < n; ++s) if (pu[s] <= p - r) ++ncand;
+            int best = -1;
+            for (int s = 0; s < n; ++s) {
+                if (ncand > 0 && !(pu[s] <= p - r)) continue;
+                if (best < 0) { best = s; continue; }
+                const int a = bits_set(mu[s]), b = bits_set(mu[best]);
+                if (a < b || (a == b && pu[s] < pu[best])) best = s;
+            }
+            slot = (forced && forced[u] >= 0) ? forced[u] : best;
+            if (victim) victim[u] = slot;
+        }
+        if (margin) margin[u] = mg;
+        memcpy(Ku + (size_t)slot * d, ku, sizeof(double) * d);
+        memcpy(Vu + (size_t)slot * d, vu, sizeof(double) * d);
+        mu[slot] = flag_new;
+        pu[slot] = p;
         free(z);
     }
 }

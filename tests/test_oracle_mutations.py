@@ -44,6 +44,18 @@ MUTATIONS = {
     "kv8_inverse_from_128": ("float inv = 127.0f / amax;", "float inv = 128.0f / amax;"),
     "gqa_last_head_only": ("add[s] += P;                          /* heads in order g = 0..G-1 */",
                            "add[s] = P;"),
+    "sh_threshold_share_of_n": ("const double t = P * (double)(n + 1);", "const double t = P * (double)n;"),
+    "sh_prompt_threshold_share_of_i": ("exp(z[j] - mx) / l * (double)(i + 1);", "exp(z[j] - mx) / l * (double)i;"),
+    "sh_flag_at_equal": ("const uint32_t f = t > 1.0 ? 1u : 0u;", "const uint32_t f = t >= 1.0 ? 1u : 0u;"),
+    "sh_window_31": ("for (int b = 0; b < 32; ++b) n +=", "for (int b = 0; b < 31; ++b) n +="),
+    "sh_evict_newest": ("if (a < b || (a == b && pu[s] < pu[best])) best = s;",
+                        "if (a < b || (a == b && pu[s] > pu[best])) best = s;"),
+    "sh_evict_most_pivotal": ("if (a < b || (a == b && pu[s] < pu[best])) best = s;",
+                              "if (a > b || (a == b && pu[s] < pu[best])) best = s;"),
+    "sh_select_ties_older": ("for (int j = ncand - 1; j >= 0; --j) {", "for (int j = 0; j < ncand; ++j) {"),
+    "sh_prompt_rows_31": ("const int i0 = T > 32 ? T - 32 : 0;", "const int i0 = T > 31 ? T - 31 : 0;"),
+    "sh_new_flag_dropped": ("else flag_new = f;", "else flag_new = 0u;"),
+    "sh_history_not_shifted": ("if (s < n) mu[s] = (mu[s] << 1) | f;", "if (s < n) mu[s] = mu[s] | f;"),
 }
 
 
