@@ -22,7 +22,8 @@ sample of the same job.
 With --gqa the job is H2O alone on a grouped-query layer (8 x 8 key/value
 heads, each cache shared by 4 query heads; the same prompt, budget and decode
 steps): one decode step there advances all 64 cache units (256 query heads)
-of one layer cache by one token.
+of one layer cache by one token.  With --sh it is the persistence-of-importance
+rule alone on the OPT-6.7B-shaped layer.
 """
 import argparse
 import hashlib
@@ -59,6 +60,8 @@ def parse():
                    help="int8 cache slots (one fp32 scale per row) for both variants")
     p.add_argument("--gqa", action="store_true",
                    help="H2O on the grouped-query layer (8 x 8 key/value heads x 4 query heads)")
+    p.add_argument("--sh", action="store_true",
+                   help="the persistence-of-importance rule alone on the OPT-6.7B-shaped layer")
     return p.parse_args()
 
 
@@ -197,6 +200,18 @@ def decode_bytes_gqa(U, G, B, d, eb, kv8=False):
     return U * (B * per_slot + fixed)
 
 
+def decode_bytes_sh(U, B, d, eb):
+    """Algorithmic HBM bytes of one full-cache persistence-of-importance
+    decode launch over U units: per live slot K and V rows, the 32-step
+    history read and written and the position read; per unit q, k, v in,
+    fp32 out, one K/V row, its history and position written, unit state
+    read and written."""
+    row = d * eb
+    per_slot = 2 * row + 4 + 4 + 4
+    fixed = 3 * row + 4 * d + 2 * row + 4 + 4 + 16
+    return U * (B * per_slot + fixed)
+
+
 def prefill_flops(U, T, d):
     """Both score passes of the H2O prompt phase: 2 x (2 d flops per causal
     (i, j) pair, T (T + 1) / 2 pairs per unit)."""
@@ -246,6 +261,20 @@ def oracle_job_gqa(w, units, S, kv8=False):
     return time.perf_counter() - t0, oracle.get_threads()
 
 
+def oracle_job_sh(w, units, S):
+    """The CPU oracle on a sample of units: persistence-of-importance prompt
+    + S steps.  Returns (seconds, threads)."""
+    import oracle
+    from kv_cache_eviction_h2o_gb300 import workloads as wl
+    g = wl.generate(w, units=units, steps=S)
+    T = w.prompt
+    t0 = time.perf_counter()
+    st, _, _, _ = oracle.sh_prefill(g["Q"], g["K"], g["V"], w.budget, w.heavy, w.recent, w.scale)
+    for t in range(S):
+        oracle.sh_decode_step(st, g["q"][t], g["k"][t], g["v"][t], T + t, w.recent, w.scale)
+    return time.perf_counter() - t0, oracle.get_threads()
+
+
 def oracle_rate(w, seconds, n_units, S):
     """Oracle time on n_units scaled to the metric: decode steps (all units of
     one layer cache advancing one token, both variants) per second."""
@@ -259,8 +288,8 @@ def run_reference(args):
     world, rank, _ = dist_setup(args)
     if rank != 0:
         return
-    if args.gqa:
-        return run_reference_gqa(args, world)
+    if args.gqa or args.sh:
+        return run_reference_single(args, world, "gqa" if args.gqa else "sh")
     from kv_cache_eviction_h2o_gb300 import workloads as wl
     w = wl.WORKLOADS[WORKLOAD]
     wl_lsh = wl.WORKLOADS["hashevict-" + WORKLOAD]
@@ -291,18 +320,19 @@ def run_reference(args):
     print(json.dumps(line))
 
 
-def run_reference_gqa(args, world):
+def run_reference_single(args, world, variant):
     from kv_cache_eviction_h2o_gb300 import workloads as wl
-    w = wl.WORKLOADS[GQA_WORKLOAD]
+    w = wl.WORKLOADS[GQA_WORKLOAD if variant == "gqa" else WORKLOAD]
     S = args.decode_steps or w.steps
     n = max(1, args.oracle_units // 16)
     units = list(range(n))
+    job = (lambda: oracle_job_gqa(w, units, S, args.kv8)) if variant == "gqa" else (lambda: oracle_job_sh(w, units, S))
     for _ in range(args.warmup):
-        oracle_job_gqa(w, units, S, args.kv8)
+        job()
     times = []
     threads = 1
     for _ in range(args.steps):
-        t, threads = oracle_job_gqa(w, units, S, args.kv8)
+        t, threads = job()
         times.append(t)
     total = sum(times)
     value = S / (total / len(times) * w.units / n)
@@ -311,10 +341,11 @@ def run_reference_gqa(args, world):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * total / len(times), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": gqa_config_name(w, S, 1, args.kv8)},
+        "config": {"workload": gqa_config_name(w, S, 1, args.kv8) if variant == "gqa" else sh_config_name(w, S, 1)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": "%d of %d cache units of one %s layer per step (prompt %d, %d decode steps, H2O)"
-                                   % (n, w.units, GQA_WORKLOAD, w.prompt, S)},
+                         "sample": "%d of %d cache units of one %s layer per step (prompt %d, %d decode steps, %s)"
+                                   % (n, w.units, w.name, w.prompt, S,
+                                      "H2O" if variant == "gqa" else "persistence of importance")},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -328,6 +359,11 @@ def gqa_config_name(w, S, NL, kv8):
             "steps, budget %d (%d heavy + %d recent)%s" % (GQA_WORKLOAD, NL, w.batch, w.heads, w.groups, w.prompt,
                                                           S, w.budget, w.heavy, w.recent,
                                                           ", int8 cache slots" if kv8 else ""))
+
+
+def sh_config_name(w, S, NL):
+    return ("%s-shaped layer x%d: persistence-of-importance rule (32-step pivotal histories), prompt %d -> %d "
+            "decode steps, budget %d (%d heavy + %d recent)" % (w.name, NL, w.prompt, S, w.budget, w.heavy, w.recent))
 
 
 # -------------------------------------------------------------------- ours
@@ -646,10 +682,12 @@ def run_e2e(args, L, torch, layers, h2o, lsh, out_h, out_l, vic_h, vic_l, W, S, 
             "ms_per_step": secs * 1000.0, "steps": n, "launch": mode}
 
 
-def run_gqa(args):
-    """H2O on the grouped-query layer: L layer caches, prompt phase then S
-    decode steps token-major over the layers, replayed from CUDA graphs with
-    inputs in HBM; e2e through the public API with host copies."""
+def run_single(args, variant):
+    """One eviction rule alone: H2O on the grouped-query layer ("gqa") or the
+    persistence-of-importance rule on the OPT-6.7B-shaped layer ("sh").  L
+    layer caches, prompt phase then S decode steps token-major over the
+    layers, replayed from CUDA graphs with inputs in HBM; e2e through the
+    public API with host copies."""
     import torch
     import torch.distributed as dist
 
@@ -663,7 +701,8 @@ def run_gqa(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     lib_build.build()
     L.lib()
-    w = wl.WORKLOADS[GQA_WORKLOAD]
+    gqa = variant == "gqa"
+    w = wl.WORKLOADS[GQA_WORKLOAD if gqa else WORKLOAD]
     S = args.decode_steps or w.steps
     NL = args.layers
     U, G, T, d, B = w.units, w.groups, w.prompt, w.head_dim, w.budget
@@ -674,20 +713,28 @@ def run_gqa(args):
         for li in range(NL):
             layers.append(wl.generate_device(w, seed_offset=li + 1000 * rank, steps=S))
     torch.cuda.synchronize()
-    hs = [L.h2o_init_gqa(B, w.heavy, w.recent, w.batch, w.heads, G, d, dt, w.scale, stream) for _ in range(NL)]
+    if gqa:
+        hs = [L.h2o_init_gqa(B, w.heavy, w.recent, w.batch, w.heads, G, d, dt, w.scale, stream) for _ in range(NL)]
+        prefill, step = L.h2o_prefill, L.h2o_decode_step
+    else:
+        hs = [L.sh_init(B, w.heavy, w.recent, w.batch, w.heads, d, dt, w.scale, stream) for _ in range(NL)]
+        prefill, step = L.sh_prefill, L.sh_decode_step
+    if args.split:
+        for h in hs:
+            L.h2o_set_decode_split(h, args.split)
     outs = [torch.empty((S, U * G, d), dtype=torch.float32, device="cuda") for _ in range(NL)]
     vics = [torch.empty((S, U), dtype=torch.int32, device="cuda") for _ in range(NL)]
 
     def pre():
         for li in range(NL):
             g = layers[li]
-            L.h2o_prefill(hs[li], g["Q"], g["K"], g["V"], T)
+            prefill(hs[li], g["Q"], g["K"], g["V"], T)
 
     def dec():
         for t in range(S):
             for li in range(NL):
                 g = layers[li]
-                L.h2o_decode_step(hs[li], g["q"][t], g["k"][t], g["v"][t], outs[li][t], vics[li][t])
+                step(hs[li], g["q"][t], g["k"][t], g["v"][t], outs[li][t], vics[li][t])
 
     phases = [("h2o_prefill", pre), ("h2o_decode", dec)]
     with torch.cuda.stream(stream):
@@ -751,46 +798,54 @@ def run_gqa(args):
     hbm, tf_burst, tf_sus, peak_src = load_peaks()
 
     t_dec = phase_ms["h2o_decode"] / (S * NL * K) / 1000.0
-    by = decode_bytes_gqa(U, G, B, d, 2, args.kv8)
+    by = decode_bytes_gqa(U, G, B, d, 2, args.kv8) if gqa else decode_bytes_sh(U, B, d, 2)
     ach = by / t_dec / 1e9
-    rl = [{"kernel": "h2o_decode_gqa", "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
-           "frac": ach / hbm, "traffic": ncu_traffic("h2o_gqa" + ("_kv8" if args.kv8 else "")),
+    dname = "h2o_decode_gqa" if gqa else "sh_decode"
+    rl = [{"kernel": dname, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+           "frac": ach / hbm, "traffic": ncu_traffic(("h2o_gqa" if gqa else "sh") + ("_kv8" if args.kv8 else "")),
            "algorithmic_bytes": by, "launch_us": t_dec * 1e6, "peak_source": peak_src,
            "share": phase_ms["h2o_decode"] / elapsed_ms}]
     t_pre = phase_ms["h2o_prefill"] / (NL * K) / 1000.0
-    fl = prefill_flops(U * G, T, d)
-    ach = fl / t_pre / 1e12
-    rl.append({"kernel": "h2o_prefill_gqa", "bound": "tensor", "achieved": ach, "peak": tf_sus,
-               "unit": "TFLOP/s", "frac": ach / tf_sus, "traffic": None, "algorithmic_flops": fl,
-               "launch_us": t_pre * 1e6, "peak_source": peak_src, "share": phase_ms["h2o_prefill"] / elapsed_ms})
-    dominant = max(rl, key=lambda r: r["share"])
+    if gqa:
+        fl = prefill_flops(U * G, T, d)
+        ach = fl / t_pre / 1e12
+        rl.append({"kernel": "h2o_prefill_gqa", "bound": "tensor", "achieved": ach, "peak": tf_sus,
+                   "unit": "TFLOP/s", "frac": ach / tf_sus, "traffic": None, "algorithmic_flops": fl,
+                   "launch_us": t_pre * 1e6, "peak_source": peak_src,
+                   "share": phase_ms["h2o_prefill"] / elapsed_ms})
+    else:
+        rl.append({"kernel": "sh_prefill", "bound": "latency", "launch_us": t_pre * 1e6,
+                   "share": phase_ms["h2o_prefill"] / elapsed_ms})
+    dominant = max((r for r in rl if "achieved" in r), key=lambda r: r["share"])
     main_rl = {k: dominant[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
     main_rl["kernel"] = dominant["kernel"]
     main_rl["peak_source"] = peak_src
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e_gqa(args, L, torch, layers, hs, outs, vics, S, NL, T, stream, world)
+        e2e = run_e2e_single(args, L, torch, layers, hs, outs, vics, S, NL, T, stream, world, prefill, step)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         n = max(1, args.oracle_units // 4)
-        secs, threads = oracle_job_gqa(w, list(range(n)), S, args.kv8)
+        if gqa:
+            secs, threads = oracle_job_gqa(w, list(range(n)), S, args.kv8)
+        else:
+            secs, threads = oracle_job_sh(w, list(range(n)), S)
         cpu = {"value": S / (secs * U / n), "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": "%d of %d cache units of one layer (prompt %d, %d decode steps, H2O), %.1f s"
-                         % (n, U, T, S, secs)}
+               "sample": "%d of %d cache units of one layer (prompt %d, %d decode steps, %s), %.1f s"
+                         % (n, U, T, S, "H2O" if gqa else "persistence of importance", secs)}
     # per layer: prompt scores (2 or 3 launches), group sum, select, gather; per step one launch
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": gqa_config_name(w, S, NL, args.kv8),
+        "config": {"workload": gqa_config_name(w, S, NL, args.kv8) if gqa else sh_config_name(w, S, NL),
                    "cache": "int8 codes + fp32 scale per row" if args.kv8 else "bf16",
                    "batch": w.batch, "kv_heads": w.heads, "groups": G, "head_dim": d, "prompt": T,
                    "decode_steps": S, "budget": B, "layers": NL, "global_batch": w.batch * world,
                    "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2: %d layer caches (%.0f MB) + prompts (%.0f MB); a cache is reused "
-                         "only after %d others" % (NL, NL * decode_bytes_gqa(U, G, B, d, 2, args.kv8) / 1e6,
-                                                   NL * (G + 2) * U * T * d * 2 / 1e6, NL - 1),
+                         "only after %d others" % (NL, NL * by / 1e6, NL * (G + 2) * U * T * d * 2 / 1e6, NL - 1),
                    "step": "one decode step = all %d cache units (%d query heads) of one layer cache advance one "
                            "token; prompt phases inside the timed step" % (U, U * G)},
         "roofline": main_rl,
@@ -809,8 +864,8 @@ def run_gqa(args):
         dist.destroy_process_group()
 
 
-def run_e2e_gqa(args, L, torch, layers, hs, outs, vics, S, NL, T, stream, world):
-    """The grouped-query job through the public API: every input copied in
+def run_e2e_single(args, L, torch, layers, hs, outs, vics, S, NL, T, stream, world, prefill, step_call):
+    """The single-rule job through the public API: every input copied in
     from pinned host memory and every output copied out inside the timed
     region, one step captured into a CUDA graph."""
     host_in = [{k: g[k].cpu().pin_memory() for k in ("Q", "K", "V", "q", "k", "v")} for g in layers]
@@ -837,12 +892,12 @@ def run_e2e_gqa(args, L, torch, layers, hs, outs, vics, S, NL, T, stream, world)
             for li in range(NL):
                 stream.wait_event(ready[li])
                 g = layers[li]
-                L.h2o_prefill(hs[li], g["Q"], g["K"], g["V"], T)
+                prefill(hs[li], g["Q"], g["K"], g["V"], T)
             stream.wait_event(ready_dec)
             for t in range(S):
                 for li in range(NL):
                     g = layers[li]
-                    L.h2o_decode_step(hs[li], g["q"][t], g["k"][t], g["v"][t], outs[li][t], vics[li][t])
+                    step_call(hs[li], g["q"][t], g["k"][t], g["v"][t], outs[li][t], vics[li][t])
             for li in range(NL):
                 host_out[li][0].copy_(outs[li], non_blocking=True)
                 host_out[li][1].copy_(vics[li], non_blocking=True)
@@ -875,8 +930,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
-    elif args.gqa:
-        run_gqa(args)
+    elif args.gqa or args.sh:
+        run_single(args, "gqa" if args.gqa else "sh")
     else:
         run_ours(args)
 

@@ -150,6 +150,47 @@ int h2o_decode_step(h2o_handle h, const void* q, const void* k, const void* v,
                     float* out, int* victim_out);
 
 /*
+ * sh_init -- create a persistence-of-importance cache handle [SH abstract:
+ * tokens that were pivotal -- had a substantial influence -- at a step keep
+ * influencing later steps, so a fixed-budget cache keeps them; the exact
+ * rule is this library's reading]:
+ *   pivotal:    at a step that attends to m tokens, a token whose
+ *               probability exceeds the uniform share, P * m > 1;
+ *   history:    each slot keeps the flags of its last 32 steps, a uint32
+ *               with bit 0 = the latest step; importance = its set bits;
+ *   evict:      when full, among slots with position <= p - r (every live
+ *               slot if none) the lowest importance, then the lowest
+ *               position;
+ *   insert:     the new token's history is its own flag this step.
+ *   Arguments as h2o_init (heavy + recent = budget); H2O_KV8 is not
+ *   supported (H2O_ERR_UNSUPPORTED).
+ */
+int sh_init(h2o_handle* out, int budget, int heavy, int recent, int batch, int heads, int head_dim,
+            int dtype, double scale, void* cuda_stream);
+
+/*
+ * sh_prefill -- initial cache from a prompt of T >= 1 tokens [SH]: the last
+ * min(T, 32) prompt rows are steps (row i attends to keys 0..i, m = i + 1);
+ * a token's history has bit T-1-i set when it was pivotal for row i.  Keeps
+ * every token when T <= B, otherwise the recent window T-r..T-1 and the H
+ * tokens among 0..T-r-1 with the most set bits (ties to the newer
+ * position); slots 0..n-1 in ascending position with their histories.
+ *   Q, K, V: device [U][T][d] of the handle's dtype.  Allocates prompt
+ *   scratch (12 bytes per unit per token) when T exceeds the largest T seen.
+ */
+int sh_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T);
+
+/*
+ * sh_decode_step -- one decode step for all U units [SH]: attend as
+ * h2o_decode_step (live slots and the new token itself), shift every live
+ * slot's history and set this step's flag, evict by the rule of sh_init
+ * when full, insert (k, v) with position p.  Arguments as h2o_decode_step.
+ * h2o_get_state / h2o_set_state carry the histories in `code` (scores 0).
+ */
+int sh_decode_step(h2o_handle h, const void* q, const void* k, const void* v,
+                   float* out, int* victim_out);
+
+/*
  * lsh_init -- create a HashEvict cache handle [HE abstract].
  *   budget = B slots, recent = r slots never evicted (0 <= r <= B);
  *   W: device fp32 [d][32], the Gaussian projection matrix, copied at init.

@@ -34,6 +34,9 @@ _d = ctypes.c_double
 SIGNATURES = {
     "h2o_init": (_i, [ctypes.POINTER(_vp), _i, _i, _i, _i, _i, _i, _i, _d, _vp]),
     "h2o_init_gqa": (_i, [ctypes.POINTER(_vp), _i, _i, _i, _i, _i, _i, _i, _i, _d, _vp]),
+    "sh_init": (_i, [ctypes.POINTER(_vp), _i, _i, _i, _i, _i, _i, _i, _d, _vp]),
+    "sh_prefill": (_i, [_vp, _vp, _vp, _vp, _i]),
+    "sh_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp]),
     "h2o_prefill": (_i, [_vp, _vp, _vp, _vp, _i]),
     "h2o_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp]),
     "lsh_init": (_i, [ctypes.POINTER(_vp), _i, _i, _i, _i, _i, _i, _d, _vp, _vp]),
@@ -146,6 +149,21 @@ def h2o_decode_step(h, q, k, v, out, victim_out=None):
 
 def lsh_decode_step(h, q, k, v, out, victim_out=None):
     _check(lib().lsh_decode_step(h, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(victim_out)))
+
+
+def sh_init(budget, heavy, recent, batch, heads, head_dim, dtype, scale, stream=None):
+    h = _vp()
+    _check(lib().sh_init(ctypes.byref(h), budget, heavy, recent, batch, heads, head_dim, dtype,
+                         float(scale), _stream(stream)))
+    return h.value
+
+
+def sh_prefill(h, Q, K, V, T):
+    _check(lib().sh_prefill(h, _ptr(Q), _ptr(K), _ptr(V), int(T)))
+
+
+def sh_decode_step(h, q, k, v, out, victim_out=None):
+    _check(lib().sh_decode_step(h, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(victim_out)))
 
 
 def h2o_get_state(h, K=None, V=None, score=None, pos=None, code=None, occupancy=None, next_pos=None):

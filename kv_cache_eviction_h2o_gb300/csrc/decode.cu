@@ -590,7 +590,13 @@ __device__ __forceinline__ void fetch_range(int B, int C, int rank, int& f0, int
 // its own query and softmax, and CTA g accumulates the heads' probabilities
 // into the scores of its share [s0, s1) of the slots.  Otherwise the
 // cluster's CTAs split one head's slots.
-template <typename T, int D, class TL, bool Q8, bool GQ>
+// SH: persistence of importance [Scissorhands abstract].  In place of a
+// score every slot keeps a 32-step history of pivotal flags (`code`): this
+// step shifts it and sets bit 0 when the slot's probability exceeds the
+// uniform share, P (n + 1) > 1; the victim is the candidate with the fewest
+// set bits, then the lowest position; the new token's history is its own
+// flag.
+template <typename T, int D, class TL, bool Q8, bool GQ, bool SH = false>
 __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const DecodeArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -640,7 +646,11 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
             const int s = s0 + tid + i * TL::NT;
             sc_old[i] = make_float2(0.f, 0.f);
             ps[i] = 0;
-            if (s < s1) { sc_old[i] = c.score[ub + s]; ps[i] = c.pos[ub + s]; }
+            if (s < s1) {
+                if constexpr (SH) sc_old[i].x = __uint_as_float(c.code[ub + s]);
+                else sc_old[i] = c.score[ub + s];
+                ps[i] = c.pos[ub + s];
+            }
         }
     };
     // Early, only each warp's first buffer is filled before the wait: the
@@ -704,7 +714,8 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     auto finish = [&](int victim, float2 snew) {
         if (victim < 0 || victim >= B) victim = 0;   // n == 0 with B == 0 cannot happen
         if (tid == 0) {
-            c.score[ub + victim] = snew;
+            if constexpr (SH) c.code[ub + victim] = S.P_new * (float)(n + 1) > 1.f ? 1u : 0u;
+            else c.score[ub + victim] = snew;
             c.pos[ub + victim] = p;
             c.ustate[unit] = make_int2(min(n + 1, B), p + 1);
             if (a.victim_out) a.victim_out[unit] = full ? victim : -1;
@@ -833,10 +844,17 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
         const int s = c0 + tid + i * TL::NT;
         if (s < c1) {
             const float P = exp2f(S.z[s - c0] - M) * invL;
-            const float2 ns = pair_add(sc_old[i], P);
-            c.score[ub + s] = ns;
+            ArgMin k;
+            if constexpr (SH) {
+                const uint32_t h = (__float_as_uint(sc_old[i].x) << 1) | (P * (float)(n + 1) > 1.f ? 1u : 0u);
+                c.code[ub + s] = h;
+                k = ArgMin{(unsigned)__popc(h), (unsigned)ps[i], (unsigned)s};
+            } else {
+                const float2 ns = pair_add(sc_old[i], P);
+                c.score[ub + s] = ns;
+                k = ArgMin{ord_key(ns.x), ord_key(ns.y), (unsigned)s};
+            }
             if (full) {
-                const ArgMin k = ArgMin{ord_key(ns.x), ord_key(ns.y), (unsigned)s};
                 if (ps[i] <= p - c.r) argmin_take(best, k);
                 if (C > 1) argmin_take(best_all, k);
             }
@@ -873,8 +891,12 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
             if (w.slot == 0xffffffffu) {
                 ArgMin al = argmin_none();
                 for (int s = lane; s < n; s += 32) {
-                    const float2 sc = c.score[ub + s];
-                    argmin_take(al, ArgMin{ord_key(sc.x), ord_key(sc.y), (unsigned)s});
+                    if constexpr (SH) {
+                        argmin_take(al, ArgMin{(unsigned)__popc(c.code[ub + s]), (unsigned)c.pos[ub + s], (unsigned)s});
+                    } else {
+                        const float2 sc = c.score[ub + s];
+                        argmin_take(al, ArgMin{ord_key(sc.x), ord_key(sc.y), (unsigned)s});
+                    }
                 }
                 w = warp_argmin(al);
             }
@@ -1191,12 +1213,12 @@ int tile_variant()
     return v;
 }
 
-template <typename T, int D, bool LSH, class TL, bool Q8 = false, bool GQ = false>
+template <typename T, int D, bool LSH, class TL, bool Q8 = false, bool GQ = false, bool SH = false>
 cudaError_t launch_decode_t(const DecodeArgs& a, int split, cudaStream_t st)
 {
     void (*kern)(const DecodeArgs);
     if constexpr (LSH) kern = lsh_decode_kernel<T, D, TL, Q8>;
-    else kern = h2o_decode_kernel<T, D, TL, Q8, GQ>;
+    else kern = h2o_decode_kernel<T, D, TL, Q8, GQ, SH>;
     if constexpr (GQ) split = a.G;             // one CTA per query head of a cache unit
     const size_t smem = sizeof(DecodeSmem<T, D, TL, Q8>);
     static bool configured[64] = {false};
@@ -1334,6 +1356,19 @@ cudaError_t launch_h2o_decode(const DecodeArgs& a, int split, cudaStream_t st)
 cudaError_t launch_lsh_decode(const DecodeArgs& a, int split, cudaStream_t st)
 {
     return dispatch<true>(a, split, st);
+}
+
+cudaError_t launch_sh_decode(const DecodeArgs& a, int split, cudaStream_t st)
+{
+    const bool bf = a.c.dtype == 1;
+    if (a.c.kv8 || a.G > 1) return cudaErrorInvalidValue;
+    if (a.c.D == 128)
+        return bf ? launch_decode_t<__nv_bfloat16, 128, false, TileDefault, false, false, true>(a, split, st)
+                  : launch_decode_t<float, 128, false, TileDefault, false, false, true>(a, split, st);
+    if (a.c.D == 64)
+        return bf ? launch_decode_t<__nv_bfloat16, 64, false, TileDefault, false, false, true>(a, split, st)
+                  : launch_decode_t<float, 64, false, TileDefault, false, false, true>(a, split, st);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace h2o

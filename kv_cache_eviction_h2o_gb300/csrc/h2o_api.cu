@@ -52,7 +52,9 @@ bool inject(const char* what)
     return f && strcmp(f, what) == 0;
 }
 
-enum Kind { kH2O = 0, kLSH = 1 };
+enum Kind { kH2O = 0, kLSH = 1, kSH = 2 };
+
+const char* kind_name(int k) { return k == kH2O ? "H2O" : k == kLSH ? "LSH" : "persistence-of-importance"; }
 
 // The handle whose cache the library last wrote on each (device, stream).
 // A decode kernel may read its own cache before its programmatic-launch
@@ -191,7 +193,7 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
         return fail(H2O_ERR_ARG, "a grouped-query cache holds at most 1024 slots (got %d)", budget);
     if (budget < 1) return fail(H2O_ERR_ARG, "budget must be >= 1 (got %d)", budget);
     if (recent < 0 || recent > budget) return fail(H2O_ERR_ARG, "recent must be in [0, budget] (got %d)", recent);
-    if (kind == kH2O && (heavy < 0 || heavy + recent != budget))
+    if ((kind == kH2O || kind == kSH) && (heavy < 0 || heavy + recent != budget))
         return fail(H2O_ERR_ARG, "heavy + recent must equal budget (%d + %d != %d)", heavy, recent, budget);
     if (batch < 1 || heads < 1) return fail(H2O_ERR_ARG, "batch and heads must be >= 1");
     if ((long long)batch * heads * groups > (1LL << 24)) return fail(H2O_ERR_ARG, "batch * heads too large");
@@ -199,6 +201,7 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
     if ((dtype & ~(H2O_BF16 | H2O_KV8)) != 0)
         return fail(H2O_ERR_ARG, "dtype must be H2O_F32 or H2O_BF16, optionally | H2O_KV8");
     const int kv8 = (dtype & H2O_KV8) ? 1 : 0;
+    if (kind == kSH && kv8) return fail(H2O_ERR_UNSUPPORTED, "H2O_KV8 is not supported on persistence-of-importance handles");
     dtype &= H2O_BF16;
     if (!(scale > 0.0) || !std::isfinite(scale)) return fail(H2O_ERR_ARG, "scale must be finite and > 0");
     if ((long long)budget >= (1LL << 20)) return fail(H2O_ERR_ARG, "budget must be below 2^20");
@@ -236,6 +239,8 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
     }
     if (kind == kH2O) {
         if ((rc = dev_alloc((void**)&h->score, U * B * sizeof(float2), "scores"))) { free_all(h); delete h; return rc; }
+    } else if (kind == kSH) {
+        if ((rc = dev_alloc((void**)&h->code, U * B * sizeof(uint32_t), "pivotal histories"))) { free_all(h); delete h; return rc; }
     } else {
         if ((rc = dev_alloc((void**)&h->code, U * B * sizeof(uint32_t), "codes")) ||
             (rc = dev_alloc((void**)&h->W, (size_t)head_dim * 32 * sizeof(float), "projection"))) {
@@ -277,6 +282,11 @@ int ensure_prompt_scratch(h2o_ctx* h, int T)
         if (h->G > 1 && (rc = dev_alloc((void**)&h->ckv, n * sizeof(double), "cache unit column sums"))) {
             free_prompt(h); return rc;
         }
+    } else if (h->kind == kSH) {
+        if ((rc = dev_alloc((void**)&h->c, n * sizeof(double), "selection keys")) ||
+            (rc = dev_alloc((void**)&h->ck, n * sizeof(uint32_t), "prompt histories"))) {
+            free_prompt(h); return rc;
+        }
     } else {
         if ((rc = dev_alloc((void**)&h->cq, n * sizeof(uint32_t), "query codes")) ||
             (rc = dev_alloc((void**)&h->ck, n * sizeof(uint32_t), "key codes"))) {
@@ -290,19 +300,24 @@ int ensure_prompt_scratch(h2o_ctx* h, int T)
 int check_prompt(h2o_ctx* h, int kind, const void* Q, const void* K, const void* V, int T)
 {
     if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
-    if (h->kind != kind) return fail(H2O_ERR_STATE, "%s called on a %s handle", kind == kH2O ? "h2o_prefill" : "lsh_prefill", h->kind == kH2O ? "H2O" : "LSH");
+    if (h->kind != kind)
+        return fail(H2O_ERR_STATE, "%s called on a %s handle",
+                    kind == kH2O ? "h2o_prefill" : kind == kLSH ? "lsh_prefill" : "sh_prefill", kind_name(h->kind));
     if (!Q || !K || !V) return fail(H2O_ERR_ARG, "Q, K and V must be non-NULL");
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V)) return fail(H2O_ERR_ARG, "Q, K, V must be 16-byte aligned");
     if (T < 1) return fail(H2O_ERR_ARG, "prompt length must be >= 1 (got %d)", T);
     if ((long long)T * h->U * h->G > (1LL << 31) / 4) return fail(H2O_ERR_ARG, "prompt too long for this batch");
-    if (kind == kH2O && T >= (1 << 24)) return fail(H2O_ERR_ARG, "prompt too long");
+    if ((kind == kH2O || kind == kSH) && T >= (1 << 24)) return fail(H2O_ERR_ARG, "prompt too long");
     return H2O_OK;
 }
 
 int check_step(h2o_ctx* h, int kind, const void* q, const void* k, const void* v, const float* out)
 {
     if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
-    if (h->kind != kind) return fail(H2O_ERR_STATE, "%s called on a %s handle", kind == kH2O ? "h2o_decode_step" : "lsh_decode_step", h->kind == kH2O ? "H2O" : "LSH");
+    if (h->kind != kind)
+        return fail(H2O_ERR_STATE, "%s called on a %s handle",
+                    kind == kH2O ? "h2o_decode_step" : kind == kLSH ? "lsh_decode_step" : "sh_decode_step",
+                    kind_name(h->kind));
     if (!h->ready) return fail(H2O_ERR_STATE, "decode before prefill");
     if (!q || !k || !v || !out) return fail(H2O_ERR_ARG, "q, k, v and out must be non-NULL");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
@@ -334,6 +349,12 @@ int h2o_init_gqa(h2o_handle* out, int budget, int heavy, int recent, int batch, 
 {
     return create(out, kH2O, budget, heavy, recent, batch, kv_heads, head_dim, dtype, scale, nullptr, cuda_stream,
                   groups);
+}
+
+int sh_init(h2o_handle* out, int budget, int heavy, int recent, int batch, int heads, int head_dim, int dtype,
+            double scale, void* cuda_stream)
+{
+    return create(out, kSH, budget, heavy, recent, batch, heads, head_dim, dtype, scale, nullptr, cuda_stream);
 }
 
 int lsh_init(h2o_handle* out, int budget, int recent, int batch, int heads, int head_dim, int dtype,
@@ -388,6 +409,37 @@ int lsh_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T
     if (e != cudaSuccess) return cuda_fail(e, "lsh_prefill launch");
     h->last_T = T;
     h->ready = 1;
+    return H2O_OK;
+}
+
+int sh_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T)
+{
+    int rc = check_prompt(h, kSH, Q, K, V, T);
+    if (rc) return rc;
+    if ((rc = ensure_prompt_scratch(h, T))) return rc;
+    if (inject("launch")) return fail(H2O_ERR_CUDA, "kernel launch failed (injected)");
+    CacheView cv = view(h);
+    PromptArgs pa = {};
+    pa.Q = Q; pa.K = K; pa.V = V; pa.T = T; pa.H = h->H;
+    pa.c = h->c; pa.ck = h->ck;
+    note_cache_write(h->device, h->stream, h);
+    cudaError_t e = launch_sh_prompt(cv, pa, h->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "sh_prefill launch");
+    h->last_T = T;
+    h->ready = 1;
+    return H2O_OK;
+}
+
+int sh_decode_step(h2o_handle h, const void* q, const void* k, const void* v, float* out, int* victim_out)
+{
+    int rc = check_step(h, kSH, q, k, v, out);
+    if (rc) return rc;
+    if (inject("launch")) return fail(H2O_ERR_CUDA, "kernel launch failed (injected)");
+    DecodeArgs a = {};
+    a.c = view(h); a.q = q; a.k = k; a.v = v; a.out = out; a.victim_out = victim_out;
+    a.early = note_cache_write(h->device, h->stream, h) ? 1 : 0;
+    cudaError_t e = launch_sh_decode(a, decode_split(h), h->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "sh_decode_step launch");
     return H2O_OK;
 }
 

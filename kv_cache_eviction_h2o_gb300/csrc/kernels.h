@@ -14,7 +14,7 @@ struct CacheView {
     int kv8, Bp;        // kv8: rows stored as int8 codes; Bp = B rounded up to even
     float2* score;      // [U][B] accumulated attention (H2O) as an unevaluated fp32 pair hi + lo
     int* pos;           // [U][B] token position per slot, -1 = empty
-    uint32_t* code;     // [U][B] key codes (LSH)
+    uint32_t* code;     // [U][B] key codes (LSH); pivotal histories (persistence of importance)
     int2* ustate;       // [U] {occupancy, position of the next token}
     int* err;           // device error word (DeviceError bits)
     int U, B, D, dtype, r;
@@ -52,6 +52,8 @@ struct PromptArgs {
 
 cudaError_t launch_h2o_decode(const DecodeArgs& a, int split, cudaStream_t st);
 cudaError_t launch_lsh_decode(const DecodeArgs& a, int split, cudaStream_t st);
+// persistence-of-importance step (histories in CacheView::code)
+cudaError_t launch_sh_decode(const DecodeArgs& a, int split, cudaStream_t st);
 int auto_decode_split(int U, int B, int num_sms);
 int max_decode_split();
 
@@ -62,6 +64,9 @@ cudaError_t launch_prompt_stats_tc(const CacheView& c, const PromptArgs& p, cuda
 cudaError_t launch_select(const CacheView& c, const PromptArgs& p, cudaStream_t st);
 // ckv[u][j] = sum over g = 0..G-1 of c[u * G + g][j], u < U, j < T
 cudaError_t launch_group_sum(const double* c, double* ckv, int U, int G, int T, cudaStream_t st);
+// persistence-of-importance prompt: histories into p.ck, selection keys into
+// p.c, then the selection and the gather (histories copied into c.code)
+cudaError_t launch_sh_prompt(const CacheView& c, const PromptArgs& p, cudaStream_t st);
 cudaError_t launch_gather(const CacheView& c, const PromptArgs& p, bool with_codes, cudaStream_t st);
 // One CTA whose bounded wait on a barrier nobody completes must run out and
 // set *err.

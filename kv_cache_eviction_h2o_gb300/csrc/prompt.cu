@@ -272,9 +272,18 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(CacheView cv, Promp
         for (int shift = 56; shift >= 0; shift -= 8) {
             for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0u;
             __syncthreads();
-            for (int j = tid; j < ncand; j += kSelThreads) {
-                const unsigned long long key = (unsigned long long)__double_as_longlong(cu[j]);
-                if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255ull], 1u);
+            // warp-aggregated: one shared-memory atomic per distinct digit
+            // per warp (many candidates can share a digit, e.g. the zero low
+            // bytes of integer-valued keys)
+            for (int jb = tid - (tid & 31); jb < ncand; jb += kSelThreads) {
+                const int j = jb + (tid & 31);
+                int dig = -1;
+                if (j < ncand) {
+                    const unsigned long long key = (unsigned long long)__double_as_longlong(cu[j]);
+                    if ((key & mask) == prefix) dig = (int)((key >> shift) & 255ull);
+                }
+                const unsigned peers = __match_any_sync(0xffffffffu, dig);
+                if (dig >= 0 && (tid & 31) == __ffs(peers) - 1) atomicAdd(&hist[dig], (unsigned)__popc(peers));
             }
             __syncthreads();
             if (tid == 0) {
@@ -839,6 +848,146 @@ cudaError_t launch_prompt_stats(const CacheView& c, const PromptArgs& p, cudaStr
 
 namespace {
 
+// Pivotal histories of the prompt (persistence of importance): the last
+// WR = min(T, 32) query rows are steps; key j is pivotal for row i (j <= i)
+// when its probability exceeds the uniform share, P_ij (i + 1) > 1.  Lane r
+// of every warp holds row i0 + r (its scaled query in registers); each warp
+// takes every NW-th key of a shared-memory tile and dots it with all rows at
+// once (the key is broadcast to the lanes).  Pass 1: each lane's online
+// (max, sum) over its warp's keys, merged across warps; pass 2 recomputes
+// the logits, and the ballot of a key's flags, bit-reversed, is its history
+// (bit T-1-i = row i).  Writes ck[j] = history and c[j] = set bits * T + j,
+// a key that orders kept tokens by importance and then by newer position.
+// Key tiles are fetched with 16-byte loads into registers one tile ahead
+// (the next pass's first tile after a pass's last), so their latency
+// overlaps the current tile's dot products.
+constexpr int kShWarps = 4, kShTile = 32;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kShWarps * 32) sh_masks_kernel(const T* __restrict__ Q, const T* __restrict__ K,
+                                                                int T_, float qscale, uint32_t* __restrict__ ck,
+                                                                double* __restrict__ cout)
+{
+    __shared__ __align__(16) float ks[kShTile][D];
+    __shared__ float wm[kShWarps][32], wl[kShWarps][32];
+    const int unit = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int i0 = T_ > 32 ? T_ - 32 : 0, WR = T_ - i0;
+    const int i = i0 + lane;                    // this lane's query row
+    const bool row_ok = lane < WR;
+    const T* Qu = Q + (size_t)unit * T_ * D;
+    const T* Ku = K + (size_t)unit * T_ * D;
+    float2 q2[D / 2];
+#pragma unroll
+    for (int e = 0; e < D / 2; ++e) {
+        const float a = row_ok ? Elem<T>::to_f(Qu[(size_t)i * D + 2 * e]) : 0.f;
+        const float b = row_ok ? Elem<T>::to_f(Qu[(size_t)i * D + 2 * e + 1]) : 0.f;
+        q2[e] = make_float2(a * qscale, b * qscale);
+    }
+    constexpr int NT = kShWarps * 32;
+    constexpr int VE = 16 / (int)sizeof(T);          // elements per 16-byte vector
+    constexpr int RV = D / VE;                       // vectors per key row
+    constexpr int VPT = kShTile * RV / NT;           // vectors per thread per tile
+    static_assert(kShTile * RV % NT == 0, "a tile splits evenly over the threads");
+    uint4 nxt[VPT];
+    auto fetch = [&](int j0) {
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int x = tid + v * NT, jj = x / RV, cv = x - jj * RV;
+            nxt[v] = (j0 + jj < T_) ? reinterpret_cast<const uint4*>(Ku + (size_t)(j0 + jj) * D)[cv]
+                                    : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    // the fetched tile into shared memory, then the next fetch goes out
+    auto stage = [&](int j0) {
+        __syncthreads();                             // the previous tile is consumed
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int x = tid + v * NT, jj = x / RV, cv = x - jj * RV;
+            float f[VE];
+            chunk_to_f32<T>(nxt[v], f);
+#pragma unroll
+            for (int e = 0; e < VE; e += 4)
+                *reinterpret_cast<float4*>(&ks[jj][cv * VE + e]) = make_float4(f[e], f[e + 1], f[e + 2], f[e + 3]);
+        }
+        __syncthreads();
+        fetch(j0 + kShTile < T_ ? j0 + kShTile : 0);
+    };
+    fetch(0);
+    // logits of this lane's row against KG consecutive keys of the tile
+    // (KG independent multiply-add chains)
+    constexpr int KG = 4, KPW = kShTile / kShWarps;  // keys per group, keys per warp
+    static_assert(KPW % KG == 0, "a warp's keys split into groups");
+    auto logits = [&](int jj, float (&z)[KG]) {
+        float2 acc[KG];
+#pragma unroll
+        for (int g = 0; g < KG; ++g) acc[g] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < D / 4; ++e) {
+#pragma unroll
+            for (int g = 0; g < KG; ++g) {
+                const float4 kv = reinterpret_cast<const float4*>(ks[jj + g])[e];
+                acc[g] = __ffma2_rn(q2[2 * e], make_float2(kv.x, kv.y), acc[g]);
+                acc[g] = __ffma2_rn(q2[2 * e + 1], make_float2(kv.z, kv.w), acc[g]);
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < KG; ++g) z[g] = acc[g].x + acc[g].y;
+    };
+    // pass 1: row max and normaliser (base 2) over the keys j <= i
+    float m = -INFINITY, l = 0.f;
+    for (int j0 = 0; j0 < T_; j0 += kShTile) {
+        stage(j0);
+        for (int jg = warp * KPW; jg < warp * KPW + KPW; jg += KG) {
+            float z[KG];
+            logits(jg, z);
+#pragma unroll
+            for (int g = 0; g < KG; ++g) {
+                const int j = j0 + jg + g;
+                if (row_ok && j <= i) {
+                    if (z[g] > m) { l = l * exp2f(m - z[g]) + 1.f; m = z[g]; }
+                    else l += exp2f(z[g] - m);
+                }
+            }
+        }
+    }
+    wm[warp][lane] = m;
+    wl[warp][lane] = l;
+    __syncthreads();
+    float M = -INFINITY, L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kShWarps; ++w) M = fmaxf(M, wm[w][lane]);
+#pragma unroll
+    for (int w = 0; w < kShWarps; ++w) L += (wm[w][lane] == -INFINITY) ? 0.f : wl[w][lane] * exp2f(wm[w][lane] - M);
+    const float share = row_ok ? (float)(i + 1) / L : 0.f;   // P (i + 1) = exp2(z - M) * share
+    // pass 2: flags
+    for (int j0 = 0; j0 < T_; j0 += kShTile) {
+        stage(j0);
+        for (int jg = warp * KPW; jg < warp * KPW + KPW; jg += KG) {
+            float z[KG];
+            logits(jg, z);
+#pragma unroll
+            for (int g = 0; g < KG; ++g) {
+                const int j = j0 + jg + g;
+                const bool f = row_ok && j <= i && exp2f(z[g] - M) * share > 1.f;
+                const unsigned bits = __ballot_sync(0xffffffffu, f);
+                if (lane == g && j < T_) {
+                    const uint32_t h = __brev(bits) >> (32 - WR);
+                    ck[(size_t)unit * T_ + j] = h;
+                    cout[(size_t)unit * T_ + j] = (double)__popc(h) * (double)T_ + (double)j;
+                }
+            }
+        }
+    }
+}
+
+template <typename T, int D>
+cudaError_t sh_masks_t(const CacheView& c, const PromptArgs& p, cudaStream_t st)
+{
+    sh_masks_kernel<T, D><<<(unsigned)c.U, kShWarps * 32, 0, st>>>(
+        reinterpret_cast<const T*>(p.Q), reinterpret_cast<const T*>(p.K), p.T, c.qscale, p.ck, p.c);
+    return cudaGetLastError();
+}
+
 // A cache unit's column sums: its heads' sums added in head order.
 __global__ void group_sum_kernel(const double* __restrict__ c, double* __restrict__ ckv, int U, int G, int T_)
 {
@@ -852,6 +1001,18 @@ __global__ void group_sum_kernel(const double* __restrict__ c, double* __restric
 }
 
 }  // namespace
+
+cudaError_t launch_sh_prompt(const CacheView& c, const PromptArgs& p, cudaStream_t st)
+{
+    const bool bf = c.dtype == 1;
+    cudaError_t e;
+    if (c.D == 128) e = bf ? sh_masks_t<__nv_bfloat16, 128>(c, p, st) : sh_masks_t<float, 128>(c, p, st);
+    else if (c.D == 64) e = bf ? sh_masks_t<__nv_bfloat16, 64>(c, p, st) : sh_masks_t<float, 64>(c, p, st);
+    else return cudaErrorInvalidValue;
+    if (e == cudaSuccess) e = launch_select(c, p, st);
+    if (e == cudaSuccess) e = launch_gather(c, p, true, st);
+    return e;
+}
 
 cudaError_t launch_group_sum(const double* c, double* ckv, int U, int G, int T, cudaStream_t st)
 {

@@ -60,12 +60,12 @@ def lib():
         L.oracle_lsh_decode_step.argtypes = [_i, _i, _i, _i, _d, _i, _f64p, _f64p, _u32p,
                                              _i32p, _i32p, _f64p, _f64p, _f64p, _f32p,
                                              _f64p, _vp]
-        L.oracle_sh_prompt_masks.argtypes = [_i, _i, _i, _d, _f64p, _f64p, _u32p, _f64p]
+        L.oracle_sh_prompt_masks.argtypes = [_i, _i, _i, _d, _f64p, _f64p, _u32p, _f64p, _vp]
         L.oracle_sh_select.argtypes = [_i, _i, _i, _i, _u32p, _i32p]
         L.oracle_sh_select.restype = _i
         L.oracle_sh_decode_step.argtypes = [_i, _i, _i, _i, _d, _i, _f64p, _f64p, _u32p,
                                             _i32p, _i32p, _f64p, _f64p, _f64p, _f64p,
-                                            _vp, _vp, _vp]
+                                            _vp, _vp, _vp, _vp]
         _lib = L
     return _lib
 
@@ -327,17 +327,19 @@ class SHState:
         return s
 
 
-def sh_prompt_masks(Q, K, scale):
+def sh_prompt_masks(Q, K, scale, with_t=False):
     """Pivotal histories of every prompt token after the prompt: [U, T]
     uint32 (bit T-1-i set when the token was pivotal for query row i, over
     the last 32 rows), and the smallest |P * m - 1| among those decisions
-    per unit."""
+    per unit; with_t: also P * m of every decision, [U, 32, T] (window row
+    w = row i - max(0, T - 32))."""
     Q = _c64(Q); K = _c64(K)
     U, T, d = Q.shape
     mask = np.empty((U, T), dtype=np.uint32)
     margin = np.empty(U)
-    lib().oracle_sh_prompt_masks(U, T, d, float(scale), Q, K, mask, margin)
-    return mask, margin
+    t = np.empty((U, 32, T)) if with_t else None
+    lib().oracle_sh_prompt_masks(U, T, d, float(scale), Q, K, mask, margin, _ptr(t))
+    return (mask, margin, t) if with_t else (mask, margin)
 
 
 def sh_build_cache(K, V, mask, kept, B):
@@ -368,15 +370,17 @@ def sh_prefill(Q, K, V, B, H, r, scale):
     return sh_build_cache(K, V, mask, kept, B), mask, kept, margin
 
 
-def sh_decode_step(st, q, k, v, p, r, scale, forced=None):
+def sh_decode_step(st, q, k, v, p, r, scale, forced=None, with_t=False):
     """One decode step in place on ``st``.  Returns (out [U, d], victim [U],
-    margin [U])."""
+    margin [U]); with_t: also P * m of every decided flag, [U, B+1] (the new
+    token at index B)."""
     q = _c64(q); k = _c64(k); v = _c64(v)
     U, d = q.shape
     out = np.empty((U, d))
     victim = np.empty(U, dtype=np.int32)
     margin = np.empty(U)
+    t = np.zeros((U, st.B + 1)) if with_t else None
     f = None if forced is None else np.ascontiguousarray(forced, dtype=np.int32)
     lib().oracle_sh_decode_step(U, d, st.B, r, float(scale), int(p), st.K, st.V, st.mask,
-                                st.pos, st.occ, q, k, v, out, _ptr(victim), _ptr(margin), _ptr(f))
-    return out, victim, margin
+                                st.pos, st.occ, q, k, v, out, _ptr(victim), _ptr(margin), _ptr(f), _ptr(t))
+    return (out, victim, margin, t) if with_t else (out, victim, margin)

@@ -71,9 +71,10 @@
  *
  * parity unpinned: the readings above that have no printed example on the
  * pages (self-attention of the new token, accumulate-before-evict order,
- * slot order after the prompt, the LSH prompt replay and attend-after-evict)
- * are pinned only through the invariants the tests check, not against a
- * value the pages print.
+ * slot order after the prompt, the LSH prompt replay and attend-after-evict,
+ * the grouped-query sum, the whole persistence-of-importance rule) are
+ * pinned only through the invariants and closed forms the tests check, not
+ * against a value the pages print.
  */
 #include <math.h>
 #include <stdint.h>
@@ -638,9 +639,11 @@ static int bits_set(uint32_t x)
 
 /* Prompt flags: row i (query i, keys 0..i, m = i + 1 tokens) is a step;   */
 /* the last 32 rows T-32..T-1 set bit T-1-i of mask[j] for every pivotal */
-/* key j <= i.  mask: [U][T]; margin: [U].                               */
+/* key j <= i.  mask: [U][T]; margin: [U]; tval: NULL or [U][32][T], the    */
+/* value P_ij * m of row i = T-32+w (w = 0..31, clipped at 0) in row w     */
+/* (0 where j > i).                                                        */
 void oracle_sh_prompt_masks(int U, int T, int d, double scale, const double* Q, const double* K,
-                            uint32_t* mask, double* margin)
+                            uint32_t* mask, double* margin, double* tval)
 {
     #pragma omp parallel for schedule(dynamic, 1)
     for (int u = 0; u < U; ++u) {
@@ -651,6 +654,8 @@ void oracle_sh_prompt_masks(int U, int T, int d, double scale, const double* Q, 
         double mg = INFINITY;
         for (int j = 0; j < T; ++j) mu[j] = 0u;
         const int i0 = T > 32 ? T - 32 : 0;
+        if (tval)
+            for (size_t x = 0; x < (size_t)32 * T; ++x) tval[(size_t)u * 32 * T + x] = 0.0;
         for (int i = i0; i < T; ++i) {
             double mx = -INFINITY;
             for (int j = 0; j <= i; ++j) {
@@ -662,6 +667,7 @@ void oracle_sh_prompt_masks(int U, int T, int d, double scale, const double* Q, 
             for (int j = 0; j <= i; ++j) {
                 const double t = exp(z[j] - mx) / l * (double)(i + 1);
                 if (t > 1.0) mu[j] |= 1u << (T - 1 - i);
+                if (tval) tval[((size_t)u * 32 + (i - i0)) * T + j] = t;
                 if (i > 0 && fabs(t - 1.0) < mg) mg = fabs(t - 1.0);   /* m = 1: P = 1 exactly */
             }
         }
@@ -690,6 +696,7 @@ int oracle_sh_select(int T, int B, int H, int r, const uint32_t* mask, int* kept
             if (keep[j]) continue;
             if (best < 0 || bits_set(mask[j]) > bits_set(mask[best])) best = j;
         }
+        if (best < 0) break;                           /* cannot happen: h < ncand */
         keep[best] = 1;
     }
     int n = 0;
@@ -705,11 +712,13 @@ int oracle_sh_select(int T, int B, int H, int r, const uint32_t* mask, int* kept
 /* token with its own flag as its history.  K, V: [U][B][d]; mask, pos:     */
 /* [U][B]; occ: [U]; q, k, v: [U][d]; out: [U][d]; victim: [U] (-1 when     */
 /* appended); margin: [U]; forced: [U] or NULL (a slot >= 0 replaces the     */
-/* rule's choice).                                                          */
+/* rule's choice); tval: NULL or [U][B+1], P * m of slot s (s < n) and of   */
+/* the new token (index B).                                                 */
 void oracle_sh_decode_step(int U, int d, int B, int r, double scale, int p,
                            double* cK, double* cV, uint32_t* mask, int* pos, int* occ,
                            const double* q, const double* k, const double* v,
-                           double* out, int* victim, double* margin, const int* forced)
+                           double* out, int* victim, double* margin, const int* forced,
+                           double* tval)
 {
     #pragma omp parallel for schedule(dynamic, 4)
     for (int u = 0; u < U; ++u) {
@@ -742,6 +751,7 @@ void oracle_sh_decode_step(int U, int d, int B, int r, double scale, int p,
             const double t = P * (double)(n + 1);
             const uint32_t f = t > 1.0 ? 1u : 0u;
             if (n > 0 && fabs(t - 1.0) < mg) mg = fabs(t - 1.0);        /* m = 1: P = 1 exactly */
+            if (tval) tval[(size_t)u * (B + 1) + (s < n ? s : B)] = t;
             if (s < n) mu[s] = (mu[s] << 1) | f;
             else flag_new = f;
         }

@@ -55,6 +55,8 @@ class Dev:
         dt = cdtype(dtype) | (L.H2O_KV8 if kv8 else 0)
         if kind == "h2o" and groups:
             self.h = L.h2o_init_gqa(B, H, r, 1, U, groups, d, dt, scale, self.stream)
+        elif kind == "sh":
+            self.h = L.sh_init(B, H, r, 1, U, d, dt, scale, self.stream)
         elif kind == "h2o":
             self.h = L.h2o_init(B, H, r, 1, U, d, dt, scale, self.stream)
         else:
@@ -70,6 +72,8 @@ class Dev:
         T = Q.shape[1]
         if self.kind == "h2o":
             L.h2o_prefill(self.h, self.Qd, self.Kd, self.Vd, T)
+        elif self.kind == "sh":
+            L.sh_prefill(self.h, self.Qd, self.Kd, self.Vd, T)
         else:
             L.lsh_prefill(self.h, self.Qd, self.Kd, self.Vd, T)
         L.h2o_sync(self.h)
@@ -78,6 +82,8 @@ class Dev:
         qd, kd, vd = (to_dev(x, self.dtype) for x in (q, k, v))
         if self.kind == "h2o":
             L.h2o_decode_step(self.h, qd, kd, vd, self.out, self.victim)
+        elif self.kind == "sh":
+            L.sh_decode_step(self.h, qd, kd, vd, self.out, self.victim)
         else:
             L.lsh_decode_step(self.h, qd, kd, vd, self.out, self.victim)
         L.h2o_sync(self.h)
@@ -325,3 +331,117 @@ def _state_all(h, U, B, d, dtype):
     code = np.empty((U, B), np.uint32); occ = np.empty(U, np.int32); npos = np.empty(U, np.int32)
     L.h2o_get_state(h, K, V, score, pos, code, occ, npos)
     return dict(K=widen(K, dtype), V=widen(V, dtype), score=score, pos=pos, code=code, occ=occ, npos=npos)
+
+
+# ------------------------------------------------------- persistence of importance
+# A pivotal flag is decided in fp32 on the device and in fp64 by the oracle;
+# a flag may differ only where the oracle's P * m is within SH_NEAR of 1 at
+# that very decision.  Such flips are counted and the oracle then adopts the
+# device's histories (and its victim, when the flip changed it), after the
+# device's choice is checked to be the rule's choice under its own flags.
+
+SH_NEAR = 1e-4
+
+
+def _popc(x):
+    return bin(int(x)).count("1")
+
+
+def sh_align_prefill(dev_state, Q, K, V, B, H, r, scale):
+    """Oracle prompt phase against the device's; returns (oracle state,
+    flips).  Fails on a difference not explained by near-threshold flags."""
+    mask, margin, tv = oracle.sh_prompt_masks(Q, K, scale, with_t=True)
+    U, T = mask.shape
+    kept_o = np.empty((U, B), np.int32)
+    for u in range(U):
+        oracle.lib().oracle_sh_select(T, B, H, r, np.ascontiguousarray(mask[u]), kept_o[u])
+    kept_g = kept_lists(dev_state["pos"], B)
+    i0 = max(0, T - 32)
+    flips = 0
+    mask_g = mask.copy()
+    for u in range(U):
+        slots = np.argsort(dev_state["pos"][u])[B - (kept_g[u] >= 0).sum():]
+        for s in slots:
+            j = int(dev_state["pos"][u, s])
+            hg, ho = int(dev_state["code"][u, s]), int(mask[u, j])
+            if hg == ho:
+                continue
+            x = hg ^ ho
+            for b in range(32):
+                if (x >> b) & 1:
+                    i = T - 1 - b
+                    assert i >= i0 and i >= j, "unit %d token %d: history bit %d outside the window" % (u, j, b)
+                    t = tv[u, i - i0, j]
+                    assert abs(t - 1.0) < SH_NEAR, "unit %d token %d row %d: flag differs with P*m = %r" % (u, j, i, t)
+                    flips += 1
+            mask_g[u, j] = hg
+        if not (kept_g[u] == kept_o[u]).all():
+            # a flip moved a count across the selection cut: every token in
+            # the difference must sit within one flag of the cut
+            assert (np.abs(tv[u] - 1.0) < SH_NEAR).any(), "unit %d: kept sets differ" % u
+            cnt = np.array([_popc(m) for m in mask[u]])
+            ko = set(kept_o[u][kept_o[u] >= 0].tolist())
+            cut = min(cnt[j] for j in ko if j < T - r)
+            for j in ko ^ set(kept_g[u][kept_g[u] >= 0].tolist()):
+                assert abs(int(cnt[j]) - int(cut)) <= 1, "unit %d: token %d far from the cut" % (u, j)
+            flips += 1
+    return oracle.sh_build_cache(K, V, mask_g, kept_g, B), flips
+
+
+def sh_lockstep(dev, st, q, k, v, T, r, scale, check_every=1):
+    """Device and oracle step by step (histories compared every step);
+    returns (flips, final oracle state)."""
+    flips = 0
+    B = st.B
+    for t in range(q.shape[0]):
+        p = T + t
+        out_g, vic_g = dev.step(q[t], k[t], v[t])
+        before = st.copy()
+        out_o, vic_o, _, tv = oracle.sh_decode_step(st, q[t], k[t], v[t], p, r, scale, with_t=True)
+        g = dev.state()
+        bad = (g["code"] != st.mask).any(axis=1) | (vic_g != vic_o)
+        if bad.any():
+            forced = np.full(st.U, -1, np.int32)
+            for u in np.nonzero(bad)[0]:
+                n = int(before.occ[u])
+                # this step's flags: bit 0 of every surviving live slot, and
+                # the new token's own flag in the slot it took
+                fg = {}
+                for s in range(n):
+                    if s != vic_g[u]:
+                        assert (int(g["code"][u, s]) >> 1) == (int(before.mask[u, s]) << 1 & 0xffffffff) >> 1, \
+                            "step %d unit %d slot %d: older history bits differ" % (t, u, s)
+                        fg[s] = int(g["code"][u, s]) & 1
+                newslot = vic_g[u] if vic_g[u] >= 0 else n
+                fg[B] = int(g["code"][u, newslot]) & 1
+                for s, f in fg.items():
+                    want = int(tv[u, s] > 1.0)
+                    if f != want:
+                        assert abs(tv[u, s] - 1.0) < SH_NEAR, "step %d unit %d slot %d: flag differs with P*m = %r" % (
+                            t, u, s, tv[u, s])
+                        flips += 1
+                # the device's victim must be the rule's choice under its flags
+                if n >= B:
+                    hist = [((int(before.mask[u, s]) << 1) & 0xffffffff) | fg.get(s, 0) for s in range(n)]
+                    hist[vic_g[u]] = ((int(before.mask[u, vic_g[u]]) << 1) & 0xffffffff) | int(tv[u, vic_g[u]] > 1.0)
+                    cand = [s for s in range(n) if before.pos[u, s] <= p - r] or list(range(n))
+                    best = min(cand, key=lambda s: (_popc(hist[s]), int(before.pos[u, s])))
+                    if best != vic_g[u]:
+                        # the victim's own flag may be the flipped one
+                        hist[vic_g[u]] ^= 1
+                        best = min(cand, key=lambda s: (_popc(hist[s]), int(before.pos[u, s])))
+                        assert abs(tv[u, vic_g[u]] - 1.0) < SH_NEAR and best == vic_g[u], \
+                            "step %d unit %d: device victim %d is not the rule's choice" % (t, u, vic_g[u])
+                        flips += 1
+                    forced[u] = vic_g[u]
+            st = before
+            out_o, vic_o, _ = oracle.sh_decode_step(st, q[t], k[t], v[t], p, r, scale, forced)
+            st.mask[bad] = g["code"][bad]
+        check_out(out_g, out_o, "SH step %d out" % t)
+        assert (vic_g == vic_o).all()
+        if (t % check_every == 0) or t == q.shape[0] - 1:
+            assert (g["pos"] == st.pos).all(), "SH step %d: positions differ" % t
+            assert (g["occ"] == st.occ).all() and (g["npos"] == p + 1).all()
+            assert (g["code"] == st.mask).all(), "SH step %d: histories differ" % t
+            assert rows_equal(g, st), "SH step %d: cache rows differ" % t
+    return flips, st

@@ -14,7 +14,7 @@ HEADER = os.path.join(ROOT, "include", "h2o.h")
 def _declared():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b((?:h2o|lsh)_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:h2o|lsh|sh)_[a-z_]+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")
@@ -29,7 +29,7 @@ def test_header_declares_the_api():
     names = _declared()
     for must in ("h2o_init", "h2o_prefill", "h2o_decode_step", "lsh_decode_step", "lsh_init",
                  "lsh_prefill", "h2o_get_state", "h2o_set_state", "h2o_sync", "h2o_destroy",
-                 "h2o_last_error"):
+                 "h2o_last_error", "h2o_init_gqa", "sh_init", "sh_prefill", "sh_decode_step"):
         assert must in names
 
 
@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(L):
     # the binding wraps exactly the declared set
     assert set(L.SIGNATURES) == set(_declared())
     out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True, text=True).stdout
-    exported = set(re.findall(r" T ((?:h2o|lsh)_\w+)$", out, flags=re.M))
+    exported = set(re.findall(r" T ((?:h2o|lsh|sh)_\w+)$", out, flags=re.M))
     assert set(_declared()) <= exported
 
 
