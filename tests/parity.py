@@ -218,45 +218,61 @@ def lsh_lockstep(dev, st, q, k, v, W, T, r, scale, check_every=1):
     return st
 
 
-def run_full_config(name, sample, check_every=64):
+def run_full_config(name, sample, check_every=64, rule=None):
     """The whole workload on the device (every unit, full prompt, every
     decode step, automatic launch configuration as the benchmark uses), with
     the units in `sample` drawn from the seeded numpy recipe and replayed by
     the oracle in lockstep from the device's recorded outputs and victims.
-    Every unit is also checked against size-independent invariants."""
+    Every unit is also checked against size-independent invariants.  rule
+    "sh": the persistence-of-importance cache on an H2O workload; a
+    grouped-query workload (groups > 1) runs a grouped-query H2O handle."""
     from kv_cache_eviction_h2o_gb300 import workloads as wl
     w = wl.WORKLOADS[name]
-    U, T, d, B, S = w.units, w.prompt, w.head_dim, w.budget, w.steps
+    kind = "lsh" if w.lsh else ("sh" if rule == "sh" else "h2o")
+    U, T, d, B, S, G = w.units, w.prompt, w.head_dim, w.budget, w.steps, w.groups
     g = wl.generate_device(w)
     gs = wl.generate(w, units=sample)
     idx = torch.tensor(sample, device="cuda")
-    for key in ("Q", "K", "V"):
+    qidx = torch.tensor([u * G + j for u in sample for j in range(G)], device="cuda")
+    g["Q"][qidx] = to_dev(gs["Q"], w.dtype)
+    g["q"][:, qidx] = to_dev(gs["q"], w.dtype)
+    for key in ("K", "V"):
         g[key][idx] = to_dev(gs[key], w.dtype)
-    for key in ("q", "k", "v"):
+    for key in ("k", "v"):
         g[key][:, idx] = to_dev(gs[key], w.dtype)
     stream = torch.cuda.current_stream()
     dt = cdtype(w.dtype)
-    if w.lsh:
+    if kind == "lsh":
         W = gs["W"]
         Wd = torch.from_numpy(W).cuda()
         h = L.lsh_init(B, w.recent, w.batch, w.heads, d, dt, w.scale, Wd, stream)
-        L.lsh_prefill(h, g["Q"], g["K"], g["V"], T)
+        prefill, step = L.lsh_prefill, L.lsh_decode_step
+    elif kind == "sh":
+        h = L.sh_init(B, w.heavy, w.recent, w.batch, w.heads, d, dt, w.scale, stream)
+        prefill, step = L.sh_prefill, L.sh_decode_step
+    elif G > 1:
+        h = L.h2o_init_gqa(B, w.heavy, w.recent, w.batch, w.heads, G, d, dt, w.scale, stream)
+        prefill, step = L.h2o_prefill, L.h2o_decode_step
     else:
         h = L.h2o_init(B, w.heavy, w.recent, w.batch, w.heads, d, dt, w.scale, stream)
-        L.h2o_prefill(h, g["Q"], g["K"], g["V"], T)
+        prefill, step = L.h2o_prefill, L.h2o_decode_step
+    prefill(h, g["Q"], g["K"], g["V"], T)
     L.h2o_sync(h)
     st0 = _state_all(h, U, B, d, w.dtype)
     st0 = {k: (v[sample] if getattr(v, "ndim", 0) >= 1 else v) for k, v in st0.items()}
-    out = torch.empty((U, d), dtype=torch.float32, device="cuda")
+    out = torch.empty((U * G, d), dtype=torch.float32, device="cuda")
     vic = torch.empty((U,), dtype=torch.int32, device="cuda")
-    outs, vics = [], []
+    outs, vics, hist = [], [], []
     for t in range(S):
-        if w.lsh:
-            L.lsh_decode_step(h, g["q"][t], g["k"][t], g["v"][t], out, vic)
-        else:
-            L.h2o_decode_step(h, g["q"][t], g["k"][t], g["v"][t], out, vic)
-        outs.append(out[idx].cpu().numpy().astype(np.float64))
+        step(h, g["q"][t], g["k"][t], g["v"][t], out, vic)
+        outs.append(out[qidx].cpu().numpy().astype(np.float64))
         vics.append(vic[idx].cpu().numpy())
+        if kind == "sh":
+            # the sampled units' histories and positions after every step
+            pos_t = np.empty((U, B), np.int32); code_t = np.empty((U, B), np.uint32)
+            occ_t = np.empty(U, np.int32); np_t = np.empty(U, np.int32)
+            L.h2o_get_state(h, None, None, None, pos_t, code_t, occ_t, np_t)
+            hist.append(dict(pos=pos_t[sample], code=code_t[sample], occ=occ_t[sample], npos=np_t[sample]))
     L.h2o_sync(h)
     st_all = _state_all(h, U, B, d, w.dtype)
     L.h2o_destroy(h)
@@ -273,16 +289,29 @@ def run_full_config(name, sample, check_every=64):
     if pF - lo + 1 > 0:
         recent = np.arange(lo, pF + 1)
         assert all(np.isin(recent, pos[u]).all() for u in range(U)), "recent window missing"
-    if not w.lsh:
+    if kind == "h2o":
         assert np.isfinite(st_all["score"]).all() and (st_all["score"] >= 0).all()
+    if kind == "sh":
+        # a slot's history holds no more steps than the token has lived
+        age = (T + S - 1) - pos
+        nb = np.vectorize(lambda x: bin(int(x)).count("1"))(st_all["code"])
+        assert (nb <= np.minimum(32, age + 1)).all(), "history longer than the token's life"
 
     # the sampled units against the oracle, step by step
     sub = {k: v[sample] if k in ("K", "V", "score", "pos", "code", "occ", "npos") else v for k, v in st_all.items()}
     near = 0
-    if w.lsh:
+    if kind == "lsh":
         st = oracle.lsh_prefill(gs["Q"], gs["K"], gs["V"], W, B, w.recent)
         replay_lsh(st, gs, W, T, w.recent, w.scale, outs, vics)
         assert (sub["code"] == st.code).all()
+    elif kind == "sh":
+        st, near = sh_align_prefill(st0, gs["Q"], gs["K"], gs["V"], B, w.heavy, w.recent, w.scale)
+        assert (st0["pos"] == st.pos).all(), "prompt positions differ"
+        assert (st0["code"] == st.mask).all(), "prompt histories differ"
+        n2, st = sh_lockstep(_Recorded(outs, vics, hist), st, gs["q"], gs["k"], gs["v"], T, w.recent, w.scale,
+                             check_rows=False)
+        near += n2
+        assert (sub["code"] == st.mask).all(), "final histories differ"
     else:
         # prompt phase: the device's kept set against the oracle's (near ties counted)
         st, c, near = align_prefill(st0, gs["Q"], gs["K"], gs["V"], B, w.heavy, w.recent, w.scale)
@@ -296,21 +325,39 @@ def run_full_config(name, sample, check_every=64):
     return near
 
 
+class _Recorded:
+    """A finished device run played back step by step: its outputs, victims
+    and per-step states of the sampled units, in the shape the lockstep
+    checkers read from a live handle."""
+
+    def __init__(self, outs, vics, states):
+        self.outs, self.vics, self.states, self.t = outs, vics, states, -1
+
+    def step(self, q, k, v):
+        self.t += 1
+        return self.outs[self.t], self.vics[self.t]
+
+    def state(self):
+        return self.states[self.t]
+
+
 def replay_h2o(st, g, T, r, scale, outs, vics):
     """Replay the oracle's H2O decode steps over the device's recorded
     outputs and victims (near ties counted and followed); returns
-    (near-tie count, final oracle state)."""
+    (near-tie count, final oracle state).  q with more rows than k: a
+    grouped-query cache."""
     near = 0
+    step = oracle.h2o_decode_step_gqa if g["q"].shape[1] != g["k"].shape[1] else oracle.h2o_decode_step
     for t in range(len(outs)):
         before = st.copy()
-        o_ref, v_ref, mg, _ = oracle.h2o_decode_step(st, g["q"][t], g["k"][t], g["v"][t], T + t, r, scale)
+        o_ref, v_ref, mg, _ = step(st, g["q"][t], g["k"][t], g["v"][t], T + t, r, scale)
         mism = vics[t] != v_ref
         if mism.any():
             assert (mg[mism] < NEAR_TIE).all(), "step %d: victims differ outside a near tie" % t
             near += int(mism.sum())
             st = before
             forced = np.where(mism, vics[t], -1).astype(np.int32)
-            o_ref, _, _, _ = oracle.h2o_decode_step(st, g["q"][t], g["k"][t], g["v"][t], T + t, r, scale, forced)
+            o_ref, _, _, _ = step(st, g["q"][t], g["k"][t], g["v"][t], T + t, r, scale, forced)
         check_out(outs[t], o_ref, "step %d out" % t)
     return near, st
 
@@ -388,9 +435,10 @@ def sh_align_prefill(dev_state, Q, K, V, B, H, r, scale):
     return oracle.sh_build_cache(K, V, mask_g, kept_g, B), flips
 
 
-def sh_lockstep(dev, st, q, k, v, T, r, scale, check_every=1):
+def sh_lockstep(dev, st, q, k, v, T, r, scale, check_every=1, check_rows=True):
     """Device and oracle step by step (histories compared every step);
-    returns (flips, final oracle state)."""
+    returns (flips, final oracle state).  check_rows=False: the device state
+    carries no cache rows (compared by the caller)."""
     flips = 0
     B = st.B
     for t in range(q.shape[0]):
@@ -443,5 +491,6 @@ def sh_lockstep(dev, st, q, k, v, T, r, scale, check_every=1):
             assert (g["pos"] == st.pos).all(), "SH step %d: positions differ" % t
             assert (g["occ"] == st.occ).all() and (g["npos"] == p + 1).all()
             assert (g["code"] == st.mask).all(), "SH step %d: histories differ" % t
-            assert rows_equal(g, st), "SH step %d: cache rows differ" % t
+            if check_rows:
+                assert rows_equal(g, st), "SH step %d: cache rows differ" % t
     return flips, st

@@ -23,3 +23,20 @@ pytestmark = pytest.mark.gpu
 def test_full_size_workload(name, sample):
     near = run_full_config(name, sample)
     print("%s: near ties forced %d" % (name, near))
+
+
+@pytest.mark.parametrize("name,sample", [
+    ("gqa-8x8x4", [0, 37, 63]),
+])
+def test_full_size_grouped_query(name, sample):
+    near = run_full_config(name, sample)
+    print("%s: near ties forced %d" % (name, near))
+
+
+@pytest.mark.parametrize("name,sample", [
+    ("opt-6.7b", [0, 131, 255]),
+    ("opt-30b", [0, 1791, 3583]),
+])
+def test_full_size_persistence_rule(name, sample):
+    flips = run_full_config(name, sample, rule="sh")
+    print("%s persistence rule: flag flips %d" % (name, flips))
