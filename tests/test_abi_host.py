@@ -87,3 +87,28 @@ def test_null_handle_is_rejected(L):
 def test_out_pointer_is_required(L):
     lib = L.lib()
     assert lib.h2o_init(None, 10, 5, 5, 1, 1, 128, 1, 0.1, None) == L.H2O_ERR_ARG
+
+
+@pytest.mark.parametrize("groups,budget,frag", [
+    (0, 64, "groups"),
+    (17, 64, "groups"),
+    (4, 1025, "1024 slots"),
+])
+def test_grouped_query_init_rejects_bad_groups(L, groups, budget, frag):
+    with pytest.raises(L.H2OError) as e:
+        L.h2o_init_gqa(budget, budget // 2, budget - budget // 2, 1, 2, groups, 128, 1, 0.1)
+    assert e.value.code == L.H2O_ERR_ARG
+    assert frag in str(e.value)
+
+
+def test_persistence_rule_init_checks(L):
+    with pytest.raises(L.H2OError) as e:
+        L.sh_init(10, 5, 6, 1, 1, 128, 1, 0.1)          # heavy + recent != budget
+    assert e.value.code == L.H2O_ERR_ARG
+    with pytest.raises(L.H2OError) as e:
+        L.sh_init(10, 5, 5, 1, 1, 128, 1 | L.H2O_KV8, 0.1)
+    assert e.value.code == L.H2O_ERR_UNSUPPORTED
+    lib = L.lib()
+    assert lib.sh_prefill(None, None, None, None, 4) == L.H2O_ERR_ARG
+    assert lib.sh_decode_step(None, None, None, None, None, None) == L.H2O_ERR_ARG
+    assert lib.sh_init(None, 10, 5, 5, 1, 1, 128, 1, 0.1, None) == L.H2O_ERR_ARG
