@@ -283,7 +283,9 @@ int ensure_prompt_scratch(h2o_ctx* h, int T)
             free_prompt(h); return rc;
         }
     } else if (h->kind == kSH) {
-        if ((rc = dev_alloc((void**)&h->c, n * sizeof(double), "selection keys")) ||
+        if ((rc = dev_alloc((void**)&h->m2, n * sizeof(float), "row max")) ||
+            (rc = dev_alloc((void**)&h->l, n * sizeof(float), "row normaliser")) ||
+            (rc = dev_alloc((void**)&h->c, n * sizeof(double), "selection keys")) ||
             (rc = dev_alloc((void**)&h->ck, n * sizeof(uint32_t), "prompt histories"))) {
             free_prompt(h); return rc;
         }
@@ -421,7 +423,7 @@ int sh_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T)
     CacheView cv = view(h);
     PromptArgs pa = {};
     pa.Q = Q; pa.K = K; pa.V = V; pa.T = T; pa.H = h->H;
-    pa.c = h->c; pa.ck = h->ck;
+    pa.c = h->c; pa.ck = h->ck; pa.m2 = h->m2; pa.l = h->l;
     note_cache_write(h->device, h->stream, h);
     cudaError_t e = launch_sh_prompt(cv, pa, h->stream);
     if (e != cudaSuccess) return cuda_fail(e, "sh_prefill launch");

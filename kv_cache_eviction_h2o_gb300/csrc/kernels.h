@@ -67,6 +67,8 @@ cudaError_t launch_group_sum(const double* c, double* ckv, int U, int G, int T, 
 // persistence-of-importance prompt: histories into p.ck, selection keys into
 // p.c, then the selection and the gather (histories copied into c.code)
 cudaError_t launch_sh_prompt(const CacheView& c, const PromptArgs& p, cudaStream_t st);
+// its tensor-core history pass (bf16, head_dim 128; needs p.m2, p.l scratch)
+cudaError_t launch_sh_flags_tc(const CacheView& c, const PromptArgs& p, cudaStream_t st);
 cudaError_t launch_gather(const CacheView& c, const PromptArgs& p, bool with_codes, cudaStream_t st);
 // One CTA whose bounded wait on a barrier nobody completes must run out and
 // set *err.

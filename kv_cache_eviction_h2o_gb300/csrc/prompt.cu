@@ -1006,7 +1006,8 @@ cudaError_t launch_sh_prompt(const CacheView& c, const PromptArgs& p, cudaStream
 {
     const bool bf = c.dtype == 1;
     cudaError_t e;
-    if (c.D == 128) e = bf ? sh_masks_t<__nv_bfloat16, 128>(c, p, st) : sh_masks_t<float, 128>(c, p, st);
+    if (prompt_tc_supported(c) && p.m2 && p.l && !getenv_flag("H2O_PROMPT_CUDA_CORES")) e = launch_sh_flags_tc(c, p, st);
+    else if (c.D == 128) e = bf ? sh_masks_t<__nv_bfloat16, 128>(c, p, st) : sh_masks_t<float, 128>(c, p, st);
     else if (c.D == 64) e = bf ? sh_masks_t<__nv_bfloat16, 64>(c, p, st) : sh_masks_t<float, 64>(c, p, st);
     else return cudaErrorInvalidValue;
     if (e == cudaSuccess) e = launch_select(c, p, st);

@@ -451,6 +451,89 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_teardown(S, warp, ntiles);
 }
 
+// ------------------------------------------------- persistence of importance
+
+// Prompt pivotal histories [Scissorhands abstract; the rule is this
+// library's reading]: the rows i of the window [max(0, T-32), T) are steps;
+// key j <= i is pivotal for row i when P_ij (i + 1) > 1, that is when
+// s_ij c2 > m2_i + log2(l_i / (i + 1)) -- a comparison, no exponential.
+// grid: U * nb CTAs; CTA x takes key block jb = x / U of unit x % U and
+// sweeps only the query blocks that hold window rows, from max(jb, qb0) to
+// nb - 1 (one or two).  Each epilogue thread owns one key, sets bit T-1-i
+// of its history for every pivotal window row i, and writes the history
+// and the selection key (set bits * T + j).
+__global__ void __launch_bounds__(kThreads, 2)
+    sh_flags_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK, int U,
+                       int T, int nb, int qb0, float c2, const float* __restrict__ m2, const float* __restrict__ lin,
+                       uint32_t* __restrict__ ck, double* __restrict__ cout, int* err)
+{
+    extern __shared__ unsigned char smem_raw[];
+    TcSmem& S = tc_smem(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int u = blockIdx.x % U;
+    const int jb = (int)(blockIdx.x / U);
+    const int row0 = u * T;
+    const int first = jb > qb0 ? jb : qb0;
+    const int ntiles = nb - first;
+    const int w0 = T > 32 ? T - 32 : 0;
+    const float* m2u = m2 + (size_t)u * T;
+    const float* lu = lin + (size_t)u * T;
+    tc_setup(S, warp);
+    const uint32_t tbase = S.tmem_base;
+
+    // threshold of query row i in base-2 logit units; +inf outside the window
+    auto thr = [&](int i) { return (i >= w0 && i < T) ? m2u[i] + log2f(lu[i] / (float)(i + 1)) : INFINITY; };
+
+    if (warp == 0) {
+        if (lane == 0) tc_producer(S, &mapK, &mapQ, row0 + jb * kT, row0, first, nb - 1, err);
+    } else if (warp == 1) {
+        if (lane == 0) tc_mma_loop(S, tbase, ntiles, err);
+        __syncwarp();
+    } else {
+        const int et = threadIdx.x - 64;          // epilogue thread 0..127
+        const int q = warp & 3;
+        const int j = jb * kT + 32 * q + lane;    // key within the unit
+        S.colstat[0][et] = thr(first * kT + et);
+        uint32_t hist = 0u;
+        for (int t = 0; t < ntiles; ++t) {
+            const int b = t & 1;
+            const int ib = first + t;
+            const float nthr = (t + 1 < ntiles) ? thr((ib + 1) * kT + et) : INFINITY;
+            const bool ok = tc_wait(S, &S.acc_full[b], (uint32_t)(t >> 1) & 1u, err);
+            // agreed by all epilogue threads; also publishes last iteration's thresholds
+            if (epilogue_any(!ok || aborted(S))) break;
+            tc_fence_after();
+            const float* th = S.colstat[b];
+            const uint32_t tcol = tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * kT);
+            uint32_t ra[32], rb[32];
+            tc_ld32_issue(tcol, ra);
+            tc_ld32_wait(ra);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t (&cur)[32] = (ch & 1) ? rb : ra;
+                uint32_t (&nxt)[32] = (ch & 1) ? ra : rb;
+                if (ch + 1 < 4) tc_ld32_issue(tcol + (uint32_t)((ch + 1) * 32), nxt);
+                const int i0 = ib * kT + ch * 32;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int i = i0 + e;
+                    if (i >= j && __uint_as_float(cur[e]) * c2 > th[ch * 32 + e]) hist |= 1u << ((T - 1 - i) & 31);
+                }
+                if (ch + 1 < 4) tc_ld32_wait(nxt);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.acc_empty[b]);
+            if (t + 1 < ntiles) S.colstat[b ^ 1][et] = nthr;
+        }
+        if (j < T && !aborted(S)) {
+            ck[(size_t)u * T + j] = hist;
+            cout[(size_t)u * T + j] = (double)__popc(hist) * (double)T + (double)j;
+        }
+    }
+    tc_teardown(S, warp, ntiles);
+}
+
 // ------------------------------------------------------------- host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -513,6 +596,40 @@ cudaError_t launch_prompt_stats_tc(const CacheView& c, const PromptArgs& p, cuda
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     colsum_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, c.U, G, p.T, nb, c.qscale, p.m2, p.l, p.c, c.err);
+    return cudaGetLastError();
+}
+
+// Prompt histories of the persistence-of-importance cache on the tensor
+// cores: row statistics of the query blocks holding the last 32 rows only
+// (the row-statistics kernel takes its blocks from the last one down, so a
+// grid of U * nq CTAs covers exactly the last nq blocks), then the flags.
+cudaError_t launch_sh_flags_tc(const CacheView& c, const PromptArgs& p, cudaStream_t st)
+{
+    CUtensorMap mq, mk;
+    const long long rows = (long long)c.U * p.T;
+    if (!make_map(&mq, p.Q, rows) || !make_map(&mk, p.K, rows)) return cudaErrorInvalidValue;
+    const size_t smem = sizeof(TcSmem) + 1024;
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(rowstats_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(sh_flags_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    const int nb = (p.T + kT - 1) / kT;
+    const int w0 = p.T > 32 ? p.T - 32 : 0;
+    const int qb0 = w0 / kT, nq = nb - qb0;
+    rowstats_tc_kernel<<<(unsigned)(c.U * nq), kThreads, smem, st>>>(mq, mk, c.U, 1, p.T, nb, c.qscale, p.m2, p.l,
+                                                                     c.err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    sh_flags_tc_kernel<<<(unsigned)(c.U * nb), kThreads, smem, st>>>(mq, mk, c.U, p.T, nb, qb0, c.qscale, p.m2, p.l,
+                                                                     p.ck, p.c, c.err);
     return cudaGetLastError();
 }
 
