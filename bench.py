@@ -671,15 +671,27 @@ def run_e2e(args, L, torch, layers, h2o, lsh, out_h, out_l, vic_h, vic_l, W, S, 
     except Exception as e:  # capture unsupported: keep the eager loop
         print("e2e: graph capture failed (%s); timing eager calls" % e, file=sys.stderr)
         torch.cuda.synchronize()
-    n = max(1, min(args.steps, 3))
-    t0 = time.perf_counter()
-    for _ in range(n):
-        run()
-    torch.cuda.synchronize()
-    secs = (time.perf_counter() - t0) / n
+    secs, each = time_e2e_steps(args, run, torch)
     value = world * 2 * S * NL / secs
     return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": secs * 1000.0, "steps": n, "launch": mode}
+            "ms_per_step": secs * 1000.0, "steps": len(each), "ms_each": each, "statistic": "median",
+            "launch": mode}
+
+
+def time_e2e_steps(args, run, torch):
+    """Each end-to-end step timed on its own (host clock, device synchronised
+    on both sides); returns the median seconds and every step's ms.  The
+    host-device link is shared with other GPUs of the machine, so single
+    steps can be slowed by traffic that is not this job's."""
+    n = max(1, min(args.steps, 5))
+    each = []
+    for _ in range(n):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        run()
+        torch.cuda.synchronize()
+        each.append(time.perf_counter() - t0)
+    return statistics.median(each), [round(1000.0 * x, 3) for x in each]
 
 
 def run_single(args, variant):
@@ -916,14 +928,10 @@ def run_e2e_single(args, L, torch, layers, hs, outs, vics, S, NL, T, stream, wor
             gr.replay()
     run()
     torch.cuda.synchronize()
-    n = max(1, min(args.steps, 3))
-    t0 = time.perf_counter()
-    for _ in range(n):
-        run()
-    torch.cuda.synchronize()
-    secs = (time.perf_counter() - t0) / n
+    secs, each = time_e2e_steps(args, run, torch)
     return {"value": world * S * NL / secs, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": secs * 1000.0, "steps": n, "launch": "graph"}
+            "ms_per_step": secs * 1000.0, "steps": len(each), "ms_each": each, "statistic": "median",
+            "launch": "graph"}
 
 
 def main():
