@@ -897,7 +897,6 @@ def run_single(args, variant):
         cpu = {"value": S / (secs * U / n), "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": "%d of %d cache units of one layer (prompt %d, %d decode steps, %s), %.1f s"
                          % (n, U, T, S, "H2O" if gqa else "persistence of importance", secs)}
-    # per layer: prompt scores (2 or 3 launches), group sum, select, gather; per step one launch
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -917,7 +916,10 @@ def run_single(args, variant):
         "cpu_baseline": cpu,
         "clocks": clk,
         "e2e": e2e,
-        "gpu_launches": (NL * 5 + S * NL) * K,
+        # prompt launches per layer: row statistics, column sums, head sums,
+        # selection, gather (grouped-query); row statistics, flags, selection,
+        # gather (persistence rule, tensor-core path); one launch per decode step
+        "gpu_launches": (NL * (5 if gqa else 4) + S * NL) * K,
     }
     for h in hs:
         L.h2o_destroy(h)
