@@ -6,7 +6,8 @@ cache's step reads its own cache before its dependency wait; a step that
 follows a step of the same cache waits first.  A seeded random interleaving
 exercises both, and every output and victim is compared with the oracle
 (H2O: Heavy-Hitter Oracle, the decode-phase eviction rule; HashEvict: the
-Hamming-distance eviction rule)."""
+Hamming-distance eviction rule; the grouped-query and persistence-of-importance
+caches with the same interleaving)."""
 import numpy as np
 import pytest
 import torch
@@ -89,6 +90,74 @@ def test_interleaved_caches_back_to_back(kv8):
                 oracle.kv8(st)
             replay_lsh(st, g, W, T, wc.recent, wc.scale, o, v)
             assert (fin["code"] == st.code).all()
+        assert (fin["pos"] == st.pos).all(), "cache %d: final positions differ" % i
+        assert rows_equal(fin, st), "cache %d: final rows differ" % i
+        assert (fin["npos"] == T + S).all()
+    for dev in devs:
+        dev.close()
+
+
+def test_interleaved_grouped_query_and_persistence_caches():
+    # a persistence-of-importance cache, a grouped-query cache and a one-head
+    # H2O cache, steps interleaved back to back on one stream
+    from parity import SH_NEAR, sh_align_prefill
+    S = 20
+    wa = wl.WORKLOADS["opt-6.7b"]
+    wq = wl.WORKLOADS["gqa-8x8x4"]
+    gs = wl.generate(wa, units=range(24, 32), steps=S)
+    gq = wl.generate(wq, units=range(0, 6), steps=S)
+    ga = wl.generate(wa, units=range(0, 12), steps=S)
+    devs = [Dev("sh", 8, wa.head_dim, wa.budget, wa.heavy, wa.recent, wa.dtype, wa.scale),
+            Dev("h2o", 6, wq.head_dim, wq.budget, wq.heavy, wq.recent, wq.dtype, wq.scale, groups=wq.groups),
+            Dev("h2o", 12, wa.head_dim, wa.budget, wa.heavy, wa.recent, wa.dtype, wa.scale)]
+    gens = [gs, gq, ga]
+    for dev, g in zip(devs, gens):
+        dev.prefill(g["Q"], g["K"], g["V"])
+    st0 = [dev.state() for dev in devs]
+    ins = [{key: to_dev(g[key], dev.dtype) for key in ("q", "k", "v")} for dev, g in zip(devs, gens)]
+    outs = [torch.empty((S, dev.U * dev.G, dev.d), dtype=torch.float32, device="cuda") for dev in devs]
+    vics = [torch.empty((S, dev.U), dtype=torch.int32, device="cuda") for dev in devs]
+    order = _order([S, S, S], seed=11)
+    pairs = list(zip(order[:-1], order[1:]))
+    assert any(a == b for a, b in pairs) and any(a != b for a, b in pairs)
+    t_of = [0, 0, 0]
+    for i in order:
+        dev, t = devs[i], t_of[i]
+        fn = L.sh_decode_step if dev.kind == "sh" else L.h2o_decode_step
+        fn(dev.h, ins[i]["q"][t], ins[i]["k"][t], ins[i]["v"][t], outs[i][t], vics[i][t])
+        t_of[i] += 1
+    torch.cuda.synchronize()
+    for dev in devs:
+        L.h2o_sync(dev.h)
+
+    T = wa.prompt
+    for i, (dev, g) in enumerate(zip(devs, gens)):
+        o = [x.astype(np.float64) for x in outs[i].cpu().numpy()]
+        v = list(vics[i].cpu().numpy())
+        fin = dev.state()
+        if dev.kind == "sh":
+            st, _ = sh_align_prefill(st0[i], g["Q"], g["K"], g["V"], wa.budget, wa.heavy, wa.recent, wa.scale)
+            loose = np.zeros(dev.U, dtype=bool)
+            for t in range(S):
+                before = st.copy()
+                o_ref, v_ref, mg = oracle.sh_decode_step(st, g["q"][t], g["k"][t], g["v"][t], T + t, wa.recent,
+                                                         wa.scale)
+                loose |= mg < SH_NEAR
+                mism = v[t] != v_ref
+                if mism.any():
+                    assert (mg[mism] < SH_NEAR).all(), "step %d: victims differ with no flag near the threshold" % t
+                    st = before
+                    forced = np.where(mism, v[t], -1).astype(np.int32)
+                    o_ref, _, _ = oracle.sh_decode_step(st, g["q"][t], g["k"][t], g["v"][t], T + t, wa.recent,
+                                                        wa.scale, forced)
+                err = np.abs(o[t] - o_ref)
+                assert (err <= 2e-3 + 1e-2 * np.abs(o_ref)).all(), "persistence step %d out" % t
+            assert (fin["code"][~loose] == st.mask[~loose]).all(), "final histories differ"
+        else:
+            st, _, _ = align_prefill(st0[i], g["Q"], g["K"], g["V"], dev.B, wa.heavy, wa.recent, wa.scale)
+            assert (st0[i]["pos"] == st.pos).all()
+            near, st = replay_h2o(st, g, T, wa.recent, wa.scale, o, v)
+            check_scores(fin["score"], st.score, "cache %d final scores" % i)
         assert (fin["pos"] == st.pos).all(), "cache %d: final positions differ" % i
         assert rows_equal(fin, st), "cache %d: final rows differ" % i
         assert (fin["npos"] == T + S).all()
