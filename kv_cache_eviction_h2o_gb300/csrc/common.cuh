@@ -201,6 +201,26 @@ __device__ __forceinline__ unsigned ord_key(float x)
 // Block until the grid this one depends on (the previous kernel in the
 // stream) has completed and its memory is visible; a no-op when the grid was
 // launched without a programmatic dependency.
+// Ask L2 for the 128-byte line holding p (no register is written; L2 is the
+// device's coherence point, so a later load still sees any write that lands
+// in between).
+__device__ __forceinline__ void prefetch_l2(const void* p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Prefetch the lines of three input rows of `bytes` each (q, k, v of a
+// unit), one line per calling thread tid < 3 * lines.
+__device__ __forceinline__ void prefetch_rows_l2(const void* q, const void* k, const void* v, int bytes, int tid)
+{
+    const int lines = (bytes + 127) / 128;
+    if (tid < 3 * lines) {
+        const int r = tid / lines, l = tid - r * lines;
+        const char* base = static_cast<const char*>(r == 0 ? q : r == 1 ? k : v);
+        prefetch_l2(base + 128 * l);
+    }
+}
+
 __device__ __forceinline__ void grid_dependency_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");

@@ -660,6 +660,10 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
         if (lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, 0, 1);
         read_cache();
     }
+    // the input rows are read only after the wait, but their lines can be
+    // on their way to L2 meanwhile
+    prefetch_rows_l2(reinterpret_cast<const T*>(a.q) + qrow * D, reinterpret_cast<const T*>(a.k) + (size_t)unit * D,
+                     reinterpret_cast<const T*>(a.v) + (size_t)unit * D, D * (int)sizeof(T), tid);
     // everything below may read memory the previous kernel in the stream
     // has written (the inputs, and the cache unless read above)
     grid_dependency_wait();
@@ -1013,6 +1017,10 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
         read_state();
         if (lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, 0, 1);
     }
+    // the input rows are read only after the wait, but their lines can be
+    // on their way to L2 meanwhile
+    prefetch_rows_l2(reinterpret_cast<const T*>(a.q) + (size_t)unit * D, reinterpret_cast<const T*>(a.k) + (size_t)unit * D,
+                     reinterpret_cast<const T*>(a.v) + (size_t)unit * D, D * (int)sizeof(T), tid);
     // everything below may read memory the previous kernel in the stream
     // has written (the inputs, and the cache unless read above)
     grid_dependency_wait();
