@@ -66,6 +66,7 @@ def lib():
         L.oracle_sh_decode_step.argtypes = [_i, _i, _i, _i, _d, _i, _f64p, _f64p, _u32p,
                                             _i32p, _i32p, _f64p, _f64p, _f64p, _f64p,
                                             _vp, _vp, _vp, _vp]
+        L.oracle_fg_profile.argtypes = [_i, _i, _i, _i, _i, _i, _d, _d, _f64p, _f64p, _i32p, _f64p, _f64p]
         _lib = L
     return _lib
 
@@ -384,3 +385,16 @@ def sh_decode_step(st, q, k, v, p, r, scale, forced=None, with_t=False):
     lib().oracle_sh_decode_step(U, d, st.B, r, float(scale), int(p), st.K, st.V, st.mask,
                                 st.pos, st.occ, q, k, v, out, _ptr(victim), _ptr(margin), _ptr(f), _ptr(t))
     return (out, victim, margin, t) if with_t else (out, victim, margin)
+
+
+def fg_profile(Q, K, B, H, r, scale, tau):
+    """Per-head cache policy from the prompt's attention: (policy [U] int32,
+    0 local / 1 frequency + local / 2 full; recovery of local [U]; recovery
+    of frequency + local [U])."""
+    Q = _c64(Q); K = _c64(K)
+    U, T, d = Q.shape
+    policy = np.empty(U, dtype=np.int32)
+    rl = np.empty(U)
+    rf = np.empty(U)
+    lib().oracle_fg_profile(U, T, d, B, H, r, float(scale), float(tau), Q, K, policy, rl, rf)
+    return policy, rl, rf

@@ -67,7 +67,11 @@
  *    as steps); its importance is the number of flags set; the victim is
  *    the candidate with the lowest importance, then the oldest position;
  *    the prompt keeps the recent window and the H most important earlier
- *    tokens, ties to the newer position.
+ *    tokens, ties to the newer position;
+ *  - the per-head policy (an optional profile, [FG]): a policy's recovery
+ *    is the average over the prompt's rows of the attention mass it keeps
+ *    at that row; the first of local, frequency + local and full cache
+ *    whose recovery reaches the threshold is the head's policy.
  *
  * parity unpinned: the readings above that have no printed example on the
  * pages (self-attention of the new token, accumulate-before-evict order,
@@ -778,6 +782,75 @@ void oracle_sh_decode_step(int U, int d, int B, int r, double scale, int p,
         memcpy(Vu + (size_t)slot * d, vu, sizeof(double) * d);
         mu[slot] = flag_new;
         pu[slot] = p;
+        free(z);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Per-head cache policy from the prompt's attention [FG abstract:      */
+/* profile the attention heads; evict long-range context on heads that  */
+/* attend locally, keep the frequent tokens on heads that attend to a   */
+/* few of them, keep the standard cache on heads that attend broadly;   */
+/* FG Figure 2: "Frequency + Local" is the fixed H2O cache.  The        */
+/* recovery test is this library's reading]:                            */
+/*   A_ij = exp(z_ij - m_i) / l_i over keys j <= i (prompt rows);        */
+/*   local:      row i keeps keys i-B+1 .. i;                            */
+/*   frequency:  row i keeps keys i-r+1 .. i and the heavy keys j <= i-r,*/
+/*               heavy = the H largest column sums among j < T-r (ties  */
+/*               to the lower j, as the prompt selection);              */
+/*   recovery = (1/T) sum_i sum_{j kept at row i} A_ij;                 */
+/*   policy 0 (local) if recovery(local) >= tau, else 1 (frequency +    */
+/*   local) if recovery(frequency) >= tau, else 2 (full cache).         */
+/* policy, rec_local, rec_freq: [U].                                     */
+/* ------------------------------------------------------------------ */
+void oracle_fg_profile(int U, int T, int d, int B, int H, int r, double scale, double tau,
+                       const double* Q, const double* K, int* policy, double* rec_local, double* rec_freq)
+{
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int u = 0; u < U; ++u) {
+        const double* Qu = Q + (size_t)u * T * d;
+        const double* Ku = K + (size_t)u * T * d;
+        double* z = (double*)malloc(sizeof(double) * (size_t)T);
+        double* c = (double*)calloc((size_t)T, sizeof(double));
+        char* heavy = (char*)calloc((size_t)T, 1);
+        /* pass 1: column sums, then the heavy keys */
+        for (int pass = 0; pass < 2; ++pass) {
+            double keep_l = 0.0, keep_f = 0.0;
+            for (int i = 0; i < T; ++i) {
+                double mi = -INFINITY;
+                for (int j = 0; j <= i; ++j) {
+                    z[j] = scale * dot(Qu + (size_t)i * d, Ku + (size_t)j * d, d);
+                    if (z[j] > mi) mi = z[j];
+                }
+                double li = 0.0;
+                for (int j = 0; j <= i; ++j) li += exp(z[j] - mi);
+                for (int j = 0; j <= i; ++j) {
+                    const double a = exp(z[j] - mi) / li;
+                    if (pass == 0) {
+                        c[j] += a;
+                    } else {
+                        if (j >= i - B + 1) keep_l += a;
+                        if (j >= i - r + 1 || (heavy[j] && j <= i - r)) keep_f += a;
+                    }
+                }
+            }
+            if (pass == 0) {
+                const int ncand = T - r;
+                if (ncand > 0) {
+                    cand_t* cs = (cand_t*)malloc(sizeof(cand_t) * (size_t)ncand);
+                    for (int j = 0; j < ncand; ++j) { cs[j].c = c[j]; cs[j].j = j; }
+                    qsort(cs, (size_t)ncand, sizeof(cand_t), cand_cmp);
+                    for (int t = 0; t < H && t < ncand; ++t) heavy[cs[t].j] = 1;
+                    free(cs);
+                }
+            } else {
+                rec_local[u] = keep_l / (double)T;
+                rec_freq[u] = keep_f / (double)T;
+                policy[u] = rec_local[u] >= tau ? 0 : (rec_freq[u] >= tau ? 1 : 2);
+            }
+        }
+        free(heavy);
+        free(c);
         free(z);
     }
 }

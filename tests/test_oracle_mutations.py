@@ -56,6 +56,11 @@ MUTATIONS = {
     "sh_prompt_rows_31": ("const int i0 = T > 32 ? T - 32 : 0;", "const int i0 = T > 31 ? T - 31 : 0;"),
     "sh_new_flag_dropped": ("else flag_new = f;", "else flag_new = 0u;"),
     "sh_history_not_shifted": ("if (s < n) mu[s] = (mu[s] << 1) | f;", "if (s < n) mu[s] = mu[s] | f;"),
+    "fg_local_window_short": ("if (j >= i - B + 1) keep_l += a;", "if (j >= i - B + 2) keep_l += a;"),
+    "fg_heavy_ignored": ("(heavy[j] && j <= i - r)) keep_f += a;", "(0 && heavy[j])) keep_f += a;"),
+    "fg_frequency_first": ("policy[u] = rec_local[u] >= tau ? 0 : (rec_freq[u] >= tau ? 1 : 2);",
+                           "policy[u] = rec_freq[u] >= tau ? 1 : (rec_local[u] >= tau ? 0 : 2);"),
+    "fg_recovery_over_t_minus_1": ("rec_local[u] = keep_l / (double)T;", "rec_local[u] = keep_l / (double)(T - 1);"),
 }
 
 

@@ -727,3 +727,77 @@ def test_sh_matches_brute_force(seed, T, B, H, r):
             want = ref[u][2][t]
             got = None if vic[u] < 0 else int(before[u, vic[u]])
             assert got == want, (u, t, got, want)
+
+
+# ------------------------------------------------------------ per-head policy profile
+# (FG abstract: local heads lose long-range context, frequency heads keep their
+# frequent tokens, broad heads keep the full cache; the recovery test is the
+# reading: the average over prompt rows of the attention mass a policy keeps)
+
+def _harmonic(n):
+    import math
+    return math.fsum(1.0 / k for k in range(1, n + 1))
+
+
+def test_fg_zero_logits_closed_form():
+    # every row attends uniformly: A_ij = 1/(i+1); column sums H_T - H_j fall
+    # with j, so the heavy keys are 0..H-1; the recoveries are sums of
+    # harmonic numbers
+    T, B, H, r, d = 60, 12, 5, 7, 8
+    g = np.random.default_rng(3)
+    Q = np.zeros((1, T, d)); K = np.zeros((1, T, d))
+    Q[..., :4] = g.standard_normal((1, T, 4)); K[..., 4:] = g.standard_normal((1, T, 4))
+    pol, rl, rf = oracle.fg_profile(Q, K, B, H, r, 0.5, 0.95)
+    HT = _harmonic(T)
+    want_l = (B + B * (HT - _harmonic(B))) / T
+    heavy = sum(HT - _harmonic(j + r) for j in range(H))
+    want_f = (r + r * (HT - _harmonic(r)) + heavy) / T
+    assert abs(rl[0] - want_l) < 1e-12 and abs(rf[0] - want_f) < 1e-12
+    assert pol[0] == 2                                   # broad attention keeps the full cache
+
+
+def test_fg_local_head_takes_the_local_policy():
+    # row i puts logit 30 on keys i-w+1..i and 0 elsewhere: a window of
+    # B >= w recovers all but ~e^-30 of every row
+    T, w, B, H, r = 48, 6, 8, 4, 4
+    K = np.eye(T)[None]
+    Q = np.zeros((1, T, T))
+    for i in range(T):
+        Q[0, i, max(0, i - w + 1):i + 1] = 30.0
+    pol, rl, rf = oracle.fg_profile(Q, K, B, H, r, 1.0, 0.95)
+    assert pol[0] == 0 and rl[0] > 0.999
+
+
+def test_fg_heavy_hitter_head_takes_the_frequency_policy():
+    # every row puts logit 30 on key 0: the local window loses it once the
+    # row is past the window, the frequency policy keeps it as a heavy key
+    T, B, H, r = 48, 8, 2, 4
+    K = np.eye(T)[None]
+    Q = np.zeros((1, T, T)); Q[0, :, 0] = 30.0
+    pol, rl, rf = oracle.fg_profile(Q, K, B, H, r, 1.0, 0.95)
+    assert rl[0] < 0.2 + 1e-9 and rf[0] > 0.999 and pol[0] == 1
+    # with no heavy slot the same head needs the full cache
+    pol0, _, rf0 = oracle.fg_profile(Q, K, B, 0, r, 1.0, 0.95)
+    assert pol0[0] == 2 and rf0[0] < 0.2
+
+
+def test_fg_matches_brute_force():
+    # attention rows by a numpy softmax, kept sets as Python sets
+    g = np.random.default_rng(5)
+    U, T, d, B, H, r = 3, 30, 6, 9, 4, 3
+    Q = g.standard_normal((U, T, d)) * 2; K = g.standard_normal((U, T, d))
+    scale = 0.6
+    pol, rl, rf = oracle.fg_profile(Q, K, B, H, r, scale, 0.5)
+    for u in range(U):
+        A = np.zeros((T, T))
+        for i in range(T):
+            zz = scale * (K[u, :i + 1] @ Q[u, i])
+            e = np.exp(zz - zz.max())
+            A[i, :i + 1] = e / e.sum()
+        c = A.sum(axis=0)
+        cand = sorted(range(T - r), key=lambda j: (-c[j], j))[:H]
+        loc = sum(A[i, j] for i in range(T) for j in range(max(0, i - B + 1), i + 1)) / T
+        fr = sum(A[i, j] for i in range(T) for j in range(i + 1)
+                 if j >= i - r + 1 or (j in cand and j <= i - r)) / T
+        assert abs(rl[u] - loc) < 1e-12 and abs(rf[u] - fr) < 1e-12
+        assert pol[u] == (0 if loc >= 0.5 else 1 if fr >= 0.5 else 2)
