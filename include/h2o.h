@@ -268,7 +268,8 @@ int h2o_set_stream(h2o_handle h, void* cuda_stream);
 /*
  * h2o_set_decode_split -- CTAs (1..16) that share one unit's slots in the
  * decode kernels (a thread-block cluster); 0 restores the automatic choice.
- * Affects performance only, never results.
+ * Affects performance only, never results.  H2O_ERR_STATE on a grouped-query
+ * handle (G > 1), whose cluster is always its G query heads.
  */
 int h2o_set_decode_split(h2o_handle h, int ctas_per_unit);
 

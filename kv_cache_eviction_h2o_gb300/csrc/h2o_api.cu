@@ -632,6 +632,8 @@ int h2o_set_stream(h2o_handle h, void* cuda_stream)
 int h2o_set_decode_split(h2o_handle h, int ctas_per_unit)
 {
     if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
+    if (h->G > 1)
+        return fail(H2O_ERR_STATE, "a grouped-query handle runs one CTA per query head; its split is not settable");
     if (ctas_per_unit < 0 || ctas_per_unit > max_decode_split())
         return fail(H2O_ERR_ARG, "ctas_per_unit must be in [0, %d]", max_decode_split());
     if (ctas_per_unit > 0 && ctas_per_unit < (h->B + 1023) / 1024)
