@@ -141,3 +141,9 @@ def test_gqa_rejects_bad_groups():
     for groups, budget in ((0, 64), (17, 64), (4, 1025)):
         with pytest.raises(L.H2OError):
             L.h2o_init_gqa(budget, budget // 2, budget - budget // 2, 1, 2, groups, 128, L.H2O_BF16, 0.1, s)
+    # the cluster of a grouped-query cache is its query heads: no split to set
+    h = L.h2o_init_gqa(64, 32, 32, 1, 2, 4, 128, L.H2O_BF16, 0.1, s)
+    with pytest.raises(L.H2OError) as e:
+        L.h2o_set_decode_split(h, 2)
+    assert e.value.code == L.H2O_ERR_STATE
+    L.h2o_destroy(h)
