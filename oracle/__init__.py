@@ -398,3 +398,38 @@ def fg_profile(Q, K, B, H, r, scale, tau):
     rf = np.empty(U)
     lib().oracle_fg_profile(U, T, d, B, H, r, float(scale), float(tau), Q, K, policy, rl, rf)
     return policy, rl, rf
+
+
+def fg_policy_params(policy, B, H, r, B_full):
+    """(budget, heavy, recent) of a head's policy: local keeps the newest B
+    tokens (no heavy slots, the window is the whole budget), frequency +
+    local is the H2O cache (B, H, r), full keeps up to B_full tokens with
+    nothing evicted while they fit."""
+    return {0: (B, 0, B), 1: (B, H, r), 2: (B_full, 0, B_full)}[int(policy)]
+
+
+def fg_prefill(Q, K, V, B, H, r, scale, tau, B_full):
+    """Per-head policies from the prompt (fg_profile), then each unit's
+    cache built by the H2O prompt rule with its policy's parameters.
+    Returns (policy [U], per-unit H2OState list, per-unit (B, H, r))."""
+    policy, _, _ = fg_profile(Q, K, B, H, r, scale, tau)
+    states, params = [], []
+    for u in range(Q.shape[0]):
+        Bu, Hu, ru = fg_policy_params(policy[u], B, H, r, B_full)
+        st, _, _, _ = h2o_prefill(Q[u:u + 1], K[u:u + 1], V[u:u + 1], Bu, Hu, ru, scale)
+        states.append(st)
+        params.append((Bu, Hu, ru))
+    return policy, states, params
+
+
+def fg_decode_step(states, params, q, k, v, p, scale):
+    """One decode step of every unit with its own policy's window.  Returns
+    (out [U, d], victim [U])."""
+    U, d = q.shape
+    out = np.empty((U, d))
+    victim = np.empty(U, dtype=np.int32)
+    for u in range(U):
+        o, vic, _, _ = h2o_decode_step(states[u], q[u:u + 1], k[u:u + 1], v[u:u + 1], p, params[u][2], scale)
+        out[u] = o[0]
+        victim[u] = vic[0]
+    return out, victim

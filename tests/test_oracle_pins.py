@@ -801,3 +801,43 @@ def test_fg_matches_brute_force():
                  if j >= i - r + 1 or (j in cand and j <= i - r)) / T
         assert abs(rl[u] - loc) < 1e-12 and abs(rf[u] - fr) < 1e-12
         assert pol[u] == (0 if loc >= 0.5 else 1 if fr >= 0.5 else 2)
+
+
+def test_fg_policies_decode_by_their_closed_forms():
+    # a local head keeps exactly the newest B tokens at every step; a
+    # full-cache head keeps every token and attends exactly like full causal
+    # attention; a heavy-hitter head keeps its heavy key
+    T, B, H, r, S, Bf = 40, 8, 2, 4, 12, 64
+    K = np.zeros((3, T, T + S)); V = np.random.default_rng(1).standard_normal((3, T, 5))
+    Kf = np.eye(T + S)
+    Q = np.zeros((3, T, T + S))
+    for i in range(T):
+        Q[0, i, max(0, i - 3):i + 1] = 30.0          # head 0: local
+        Q[1, i, 0] = 30.0                             # head 1: heavy key 0
+    K[:] = Kf[:T]
+    g = np.random.default_rng(2)
+    Q[2] = g.standard_normal((T, T + S)) * 0.01       # head 2: broad
+    q = np.zeros((S, 3, T + S)); k = np.zeros((S, 3, T + S)); v = g.standard_normal((S, 3, 5))
+    for t in range(S):
+        p = T + t
+        q[t, 0, max(0, p - 3):p + 1] = 30.0
+        q[t, 1, 0] = 30.0
+        q[t, 2] = g.standard_normal(T + S) * 0.01
+        k[t, :, p] = 1.0
+    D = T + S
+    # V needs the head dimension of K for the oracle's cache rows: pad to D
+    Vp = np.zeros((3, T, D)); Vp[..., :5] = V
+    vp = np.zeros((S, 3, D)); vp[..., :5] = v
+    pol, states, params = oracle.fg_prefill(Q, K, Vp, B, H, r, 1.0, 0.95, Bf)
+    assert list(pol) == [0, 1, 2]
+    for t in range(S):
+        p = T + t
+        out, vic = oracle.fg_decode_step(states, params, q[t], k[t], vp[t], p, 1.0)
+        assert sorted(states[0].pos[0].tolist()) == list(range(p - B + 1, p + 1))
+        assert 0 in states[1].pos[0]
+        assert sorted(states[2].pos[0][:states[2].occ[0]].tolist()) == list(range(p + 1))
+        # full cache: softmax over every token so far
+        keys = np.concatenate([K[2], k[:t + 1, 2]]); vals = np.concatenate([Vp[2], vp[:t + 1, 2]])
+        z = keys @ q[t, 2]
+        w = np.exp(z - z.max()); w /= w.sum()
+        np.testing.assert_allclose(out[2], w @ vals, rtol=1e-12, atol=1e-12)
