@@ -12,17 +12,17 @@
 //   there, then attend over the cache.
 //
 // Layout and parallel plan (GB300): a unit's slots are split into `split`
-// contiguous chunks, one CTA each, the CTAs of a unit forming one
-// thread-block cluster.  Inside a CTA every warp streams its own 8-slot
-// groups of K and V rows with 1-D bulk copies (TMA) into a private ring of
-// shared-memory buffers completed on mbarriers, and keeps its own online
-// softmax (base-2 logits).  Warps merge through shared memory, CTAs merge
-// through distributed shared memory into cluster rank 0.  H2O needs the
-// global normaliser before any score update, so the cluster exchanges
-// (max, sum) once, every CTA updates its own slots' scores from the logits
-// it kept in shared memory (P never goes to HBM), and a second exchange
-// reduces the arg-min.  Every wait is bounded; a wait that runs out sets the
-// handle's error word.
+// contiguous chunks, one CTA each, a unit's CTAs forming one cluster (a
+// grouped-query cache: one CTA per query head).  In a CTA every warp streams
+// its own 16-slot stages of K and V rows with 1-D bulk copies (TMA) into a
+// private ring of shared-memory buffers completed on mbarriers, and keeps
+// its own online softmax (base-2 logits).  Warps merge through shared
+// memory, CTAs through distributed shared memory into cluster rank 0.  H2O
+// needs the global normaliser before any score update, so the cluster
+// exchanges (max, sum) once, every CTA updates its own slots' scores (or
+// pivotal histories) from the logits it kept in shared memory (P never goes
+// to HBM), and a second exchange reduces the arg-min.  Every wait is
+// bounded; a wait that runs out sets the handle's error word.
 #include <cfloat>
 #include <climits>
 #include <cstdlib>
