@@ -11,6 +11,12 @@
 // HashEvict [HashEvict abstract]: sign codes of every prompt query and key,
 // then a per-unit replay of the decode replacement rule over the prompt.
 //
+// Grouped-query caches: query unit u reads the keys of cache unit u / G, and
+// a cache unit's column sums are its G heads' sums.  Persistence of
+// importance [Scissorhands abstract]: the pivotal histories of the last 32
+// rows (CUDA-core kernel here, tensor-core one in prompt_tc.cu) feed the same
+// select and gather.
+//
 // The score passes here run on the CUDA cores in fp32 with fp64 running
 // sums; logits are kept in base 2 (q is pre-multiplied by scale * log2 e).
 #include <cfloat>
