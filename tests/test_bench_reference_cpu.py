@@ -1,0 +1,37 @@
+"""The benchmark's reference arm (the CPU oracle) on the host: one JSON line
+from rank 0 with the contract's keys, nothing from another rank (as when it
+is launched at two ranks), for the default job and the grouped-query and
+persistence-of-importance legs."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ARGS = ["--impl", "reference", "--steps", "1", "--warmup", "0", "--decode-steps", "2", "--oracle-units", "4"]
+
+
+def _run(extra, rank, world):
+    env = dict(os.environ, RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + ARGS + extra, env=env, cwd=ROOT,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return [line for line in r.stdout.splitlines() if line.startswith("{")]
+
+
+@pytest.mark.parametrize("extra", [[], ["--gqa"], ["--sh"]])
+def test_reference_arm_line(extra):
+    lines = _run(extra, 0, 2)
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["steps"] == 1
+    for key in ("metric", "value", "unit", "ms_per_step", "higher_is_better", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_reference_arm_other_rank_is_silent():
+    assert _run([], 1, 2) == []
