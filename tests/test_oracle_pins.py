@@ -501,6 +501,20 @@ def test_gqa_one_head_per_group_is_the_one_head_path():
         assert (a.score == b.score).all() and (a.K == b.K).all()
 
 
+def test_gqa_one_head_per_group_with_int8_slots():
+    # the grouped step's int8 bookkeeping (the written slot re-quantised)
+    # reduces to the one-head int8 step at G = 1: codes and scales identical
+    U, T, S, d, B, H, r, sc = 3, 30, 12, 8, 10, 5, 5, 0.4
+    Q, K, V, q, k, v = _gqa_inputs(52, U, 1, T, S, d)
+    a = oracle.kv8(oracle.h2o_prefill_gqa(Q, K, V, B, H, r, sc)[0])
+    b = oracle.kv8(oracle.h2o_prefill(Q, K, V, B, H, r, sc)[0])
+    for t in range(S):
+        oa, va, _, _ = oracle.h2o_decode_step_gqa(a, q[t], k[t], v[t], T + t, r, sc)
+        ob, vb, _, _ = oracle.h2o_decode_step(b, q[t], k[t], v[t], T + t, r, sc)
+        assert (oa == ob).all() and (va == vb).all()
+        assert (a.kq == b.kq).all() and (a.ks == b.ks).all() and (a.vq == b.vq).all() and (a.K == b.K).all()
+
+
 def test_gqa_identical_heads_scale_the_scores():
     # G copies of one query: every head's output is the one-head output and
     # every score is exactly G times the one-head score (G a power of two)
