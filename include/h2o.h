@@ -26,6 +26,13 @@
  *  - U = batch * heads independent (batch, head) units; the unit index is
  *    b * heads + h.  d = head_dim (64 or 128).  Element type is fp32
  *    (H2O_F32) or bf16 (H2O_BF16) for every Q/K/V/q/k/v buffer of a handle.
+ *    A grouped-query handle (h2o_init_gqa) has U = batch * kv_heads cache
+ *    units and G query heads per unit: its Q, q and out have U * G rows.
+ *  - Three handle kinds: H2O (h2o_init, h2o_init_gqa; h2o_* calls),
+ *    HashEvict (lsh_init; lsh_* calls) and persistence of importance
+ *    (sh_init; sh_* calls).  State, sync, stream and destroy calls (h2o_*)
+ *    take any kind; a prefill or decode call of another kind is
+ *    H2O_ERR_STATE.
  *  - Pointers named "device" must point to device memory of the current
  *    device, C-contiguous, 16-byte aligned.  The caller owns them.
  *  - The library owns the cache (K, V [U][B][d]), the scores (fp64
