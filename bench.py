@@ -1,29 +1,33 @@
 #!/usr/bin/env python3
 """Whole-job throughput of the budgeted-KV decode path on GB300.
 
-One bench step is one pass of the whole hot path over one batch of synthetic
-input shaped like an OPT-6.7B attention layer (8 x 32 heads, head_dim 128,
-prompt 2048, 256 decode steps, budget 410 = 205 heavy + 205 recent, bf16):
+One bench step is one pass of the hot path over one batch of synthetic input
+shaped like an attention layer of the named configuration:
 
-  for each of L layer caches: H2O prompt phase (scores, top-k, gather) and
-  HashEvict prompt phase (codes, replay, gather) on the same prompt;
-  then 256 H2O decode steps and 256 HashEvict decode steps, token-major over
-  the L layers, as a model decodes.
+  for each of L layer caches: the prompt phase (H2O: row statistics and
+  column sums on the tensor cores, top-k, gather; HashEvict: sign codes,
+  replacement replay, gather), then S decode steps (attend, accumulate,
+  evict, insert), token-major over the L layers, as a model decodes.
 
-L layers (default 8, ~890 MB of caches plus 3.2 GB of prompts) keep every
-cache out of L2 between its uses.  The device-timed value replays the step
-from CUDA graphs with inputs already in HBM; the e2e value drives the same
-job through the public API with pinned host inputs copied in and outputs
-copied out inside the timed region.  The CPU oracle is timed on a bounded
-sample of the same job.
+The default configuration is the OPT-30B-shaped layer in its throughput
+regime (64 x 56 heads, head_dim 128, prompt 512, 1024 decode steps, budget
+308 = 154 heavy + 154 recent, bf16): the largest single-GPU configuration,
+the one the headline value is quoted on.  Its value is H2O decode steps per
+second, one decode step being all batch x head units of one layer cache
+advancing one token.  The same run then measures the other configurations as
+sub-records (each with its own timed region, rooflines and CPU baseline):
+the OPT-6.7B-shaped layer, the Llama-7B-shaped 32K-token context and the
+HashEvict variant on the OPT-6.7B shapes.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Every layer cache is used again only after the L - 1 others, and the caches
+plus the prompts exceed L2, so decode reads come from HBM.  The device-timed
+value replays the step from CUDA graphs with inputs already in HBM; the e2e
+value drives the same job through the public API with pinned host inputs
+copied in and outputs copied out inside the timed region.  The CPU oracle is
+timed on a bounded sample of the same job.
 
-With --gqa the job is H2O alone on a grouped-query layer (8 x 8 key/value
-heads, each cache shared by 4 query heads; the same prompt, budget and decode
-steps): one decode step there advances all 64 cache units (256 query heads)
-of one layer cache by one token.  With --sh it is the persistence-of-importance
-rule alone on the OPT-6.7B-shaped layer.
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                    [--rule h2o|sh] [--kv8] [--impl reference] [--no-sub]
 """
 import argparse
 import hashlib
@@ -40,31 +44,54 @@ if ROOT not in sys.path:
 
 METRIC = "H2O decode steps/s (batch×heads) at 1 GB300; achieved HBM GB/s vs peak"
 UNIT = "steps/s"
-WORKLOAD = "opt-6.7b"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 
+# name -> (workload, eviction rule, layer caches in rotation).  The layer
+# count keeps the caches plus prompts well above L2 (129 MB) and makes every
+# cache wait for the others before it is read again.
+CONFIGS = {
+    "opt-30b": ("opt-30b", "h2o", 2),                       # 2 x 565 MB caches
+    "opt-6.7b": ("opt-6.7b", "h2o", 8),                     # 8 x 113 MB
+    "llama-7b-32k": ("llama-7b-32k", "h2o", 8),             # 8 x 68.7 MB
+    "hashevict-opt-6.7b": ("hashevict-opt-6.7b", "lsh", 8),
+    "gqa-8x8x4": ("gqa-8x8x4", "h2o", 8),
+}
+DEFAULT_CONFIG = "opt-30b"
+SUB_CONFIGS = ("opt-6.7b", "llama-7b-32k", "hashevict-opt-6.7b")
 
-def parse():
+
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--layers", type=int, default=8)
+    p.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(CONFIGS))
+    p.add_argument("--rule", default=None, choices=["h2o", "sh"],
+                   help="eviction rule on an H2O workload: h2o (accumulated attention) or sh "
+                        "(persistence of importance); default: the configuration's own")
+    p.add_argument("--layers", type=int, default=None, help="layer caches in rotation (default per config)")
     p.add_argument("--decode-steps", type=int, default=None)
     p.add_argument("--split", type=int, default=0, help="CTAs per unit in decode (0 = automatic)")
-    p.add_argument("--oracle-units", type=int, default=64)
+    p.add_argument("--oracle-seconds", type=float, default=10.0,
+                   help="CPU work the oracle sample of the main configuration aims at")
+    p.add_argument("--oracle-units", type=int, default=0,
+                   help="units per oracle sample of the reference arm (default: the host's threads)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
-    p.add_argument("--kv8", action="store_true",
-                   help="int8 cache slots (one fp32 scale per row) for both variants")
-    p.add_argument("--gqa", action="store_true",
-                   help="H2O on the grouped-query layer (8 x 8 key/value heads x 4 query heads)")
-    p.add_argument("--sh", action="store_true",
-                   help="the persistence-of-importance rule alone on the OPT-6.7B-shaped layer")
-    p.add_argument("--no-overlap", action="store_true",
-                   help="skip the second timed region with the two eviction jobs on two streams")
-    return p.parse_args()
+    p.add_argument("--no-sub", action="store_true", help="measure the main configuration only")
+    p.add_argument("--sub", default=None, help="comma-separated sub-record configurations (default: %s)"
+                   % ",".join(SUB_CONFIGS))
+    p.add_argument("--kv8", action="store_true", help="int8 cache slots (one fp32 scale per row)")
+    # older spellings
+    p.add_argument("--gqa", action="store_true", help="same as --config gqa-8x8x4")
+    p.add_argument("--sh", action="store_true", help="same as --config opt-6.7b --rule sh")
+    a = p.parse_args(argv)
+    if a.gqa:
+        a.config = "gqa-8x8x4"
+    if a.sh:
+        a.config, a.rule = ("opt-6.7b" if a.config == DEFAULT_CONFIG else a.config), "sh"
+    return a
 
 
 # ------------------------------------------------------------------ helpers
@@ -74,7 +101,8 @@ def load_peaks():
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]),
+                float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured")
     except Exception:
         return 6800.0, 1900.0, 1700.0, "fallback"
 
@@ -87,13 +115,13 @@ def file_digest(*names):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel):
+def ncu_traffic(key):
     """Per-launch DRAM bytes from the committed ncu capture, if it was taken
     on the current kernel source; None otherwise."""
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
-        e = d[kernel]
+        e = d[key]
         if e["source_digest"] != file_digest(*e["sources"]):
             return None
         return float(e["bytes_per_launch"])
@@ -102,7 +130,7 @@ def ncu_traffic(kernel):
 
 
 class Clocks:
-    """nvidia-smi sampler for the timed region."""
+    """nvidia-smi sampler for the timed regions."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -128,22 +156,26 @@ class Clocks:
         except Exception:
             self.proc.kill()
             return None
-        rows = []
-        for line in out.strip().splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                rows.append((float(f[1]), float(f[2]), float(f[3]), f[5:9]))
-            except ValueError:
-                continue
-        if not rows:
-            return None
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
-        loaded = [r for r in rows if r[2] > 0.25 * max(x[2] for x in rows)] or rows
-        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows), "power_w_max": max(r[2] for r in rows)}
+        return summarize_clocks(out)
+
+
+def summarize_clocks(text):
+    rows = []
+    for line in text.strip().splitlines():
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            rows.append((float(f[1]), float(f[2]), float(f[3]), f[5:9]))
+        except ValueError:
+            continue
+    if not rows:
+        return None
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+    loaded = [r for r in rows if r[2] > 0.25 * max(x[2] for x in rows)] or rows
+    return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+            "reasons": reasons, "samples": len(rows), "power_w_max": max(r[2] for r in rows)}
 
 
 def max_over_ranks(x, world, device="cpu"):
@@ -158,7 +190,7 @@ def max_over_ranks(x, world, device="cpu"):
     return float(t.item())
 
 
-def dist_setup(args):
+def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -185,6 +217,12 @@ def decode_bytes(U, B, d, eb, lsh, kv8=False):
     per_slot = 2 * crow + sc + 8 + 8 + 4
     fixed = 3 * row + 4 * d + 2 * crow + sc + 8 + 4 + 16
     return U * (B * per_slot + fixed)
+
+
+def method_bytes(U, B, d, eb):
+    """The method's own bytes per H2O step (one fp32 score per slot, no
+    pair): 2 rows + 4 + 4 + 4 per live slot, 1804 B per unit at d = 128."""
+    return U * (B * (2 * d * eb + 12) + 3 * d * eb + 4 * d + 2 * d * eb + 12)
 
 
 def decode_bytes_gqa(U, G, B, d, eb, kv8=False):
@@ -220,722 +258,439 @@ def prefill_flops(U, T, d):
     return 2 * 2 * U * d * T * (T + 1) // 2
 
 
+def lsh_code_flops(U, T, d):
+    """Prompt sign codes: 32 fp32 multiply-add chains of d terms for every
+    query and key row (2 flops per multiply-add)."""
+    return 2 * U * T * 2 * d * 32
+
+
+def prompt_launches(rule, G):
+    """Kernels one prompt phase launches: row statistics, column sums,
+    selection, gather (H2O; + head sums for a grouped-query cache); sign
+    codes, replay, gather (HashEvict); row statistics, flags, selection,
+    gather (persistence rule, tensor-core path)."""
+    if rule == "lsh":
+        return 3
+    if rule == "sh":
+        return 4
+    return 5 if G > 1 else 4
+
+
 # ------------------------------------------------------------------ oracle
 
-def oracle_job(w, wl_lsh, units, S, kv8=False):
-    """The CPU oracle on a sample of units: H2O prompt + S steps and
-    HashEvict prompt + S steps (int8 cache slots with kv8).  Returns
-    (seconds, threads)."""
-    import numpy as np
+ORACLE_MAX_PROMPT = 4096
 
+
+def oracle_job(w, rule, units, S, kv8=False, prompt=None):
+    """The CPU oracle on a sample of units of workload w: the prompt phase
+    (of `prompt` tokens, default the workload's) and S decode steps of the
+    rule.  Returns (prompt seconds, decode seconds, threads)."""
     import oracle
     from kv_cache_eviction_h2o_gb300 import workloads as wl
-    g = wl.generate(w, units=units, steps=S)
-    W = wl.lsh_matrix(wl_lsh)
-    T = w.prompt
+    T = prompt or w.prompt
+    g = wl.generate(w, units=units, steps=S, prompt=T)
     t0 = time.perf_counter()
-    st, _, _, _ = oracle.h2o_prefill(g["Q"], g["K"], g["V"], w.budget, w.heavy, w.recent, w.scale)
-    if kv8:
-        oracle.kv8(st)
-    for t in range(S):
-        oracle.h2o_decode_step(st, g["q"][t], g["k"][t], g["v"][t], T + t, w.recent, w.scale)
-    ls = oracle.lsh_prefill(g["Q"], g["K"], g["V"], W, wl_lsh.budget, wl_lsh.recent)
-    if kv8:
-        oracle.kv8(ls)
-    for t in range(S):
-        oracle.lsh_decode_step(ls, g["q"][t], g["k"][t], g["v"][t], W, T + t, wl_lsh.recent, w.scale)
-    return time.perf_counter() - t0, oracle.get_threads()
+    if rule == "lsh":
+        W = g["W"]
+        st = oracle.lsh_prefill(g["Q"], g["K"], g["V"], W, w.budget, w.recent)
+        if kv8:
+            oracle.kv8(st)
+        t1 = time.perf_counter()
+        for t in range(S):
+            oracle.lsh_decode_step(st, g["q"][t], g["k"][t], g["v"][t], W, T + t, w.recent, w.scale)
+    elif rule == "sh":
+        st, _, _, _ = oracle.sh_prefill(g["Q"], g["K"], g["V"], w.budget, w.heavy, w.recent, w.scale)
+        t1 = time.perf_counter()
+        for t in range(S):
+            oracle.sh_decode_step(st, g["q"][t], g["k"][t], g["v"][t], T + t, w.recent, w.scale)
+    elif w.groups > 1:
+        st, _, _, _, _ = oracle.h2o_prefill_gqa(g["Q"], g["K"], g["V"], w.budget, w.heavy, w.recent, w.scale)
+        if kv8:
+            oracle.kv8(st)
+        t1 = time.perf_counter()
+        for t in range(S):
+            oracle.h2o_decode_step_gqa(st, g["q"][t], g["k"][t], g["v"][t], T + t, w.recent, w.scale)
+    else:
+        st, _, _, _ = oracle.h2o_prefill(g["Q"], g["K"], g["V"], w.budget, w.heavy, w.recent, w.scale)
+        if kv8:
+            oracle.kv8(st)
+        t1 = time.perf_counter()
+        for t in range(S):
+            oracle.h2o_decode_step(st, g["q"][t], g["k"][t], g["v"][t], T + t, w.recent, w.scale)
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1, oracle.get_threads()
 
 
-def oracle_job_gqa(w, units, S, kv8=False):
-    """The CPU oracle on a sample of cache units of a grouped-query workload:
-    H2O prompt + S steps.  Returns (seconds, threads)."""
-    import oracle
-    from kv_cache_eviction_h2o_gb300 import workloads as wl
-    g = wl.generate(w, units=units, steps=S)
-    T = w.prompt
-    t0 = time.perf_counter()
-    st, _, _, _, _ = oracle.h2o_prefill_gqa(g["Q"], g["K"], g["V"], w.budget, w.heavy, w.recent, w.scale)
-    if kv8:
-        oracle.kv8(st)
-    for t in range(S):
-        oracle.h2o_decode_step_gqa(st, g["q"][t], g["k"][t], g["v"][t], T + t, w.recent, w.scale)
-    return time.perf_counter() - t0, oracle.get_threads()
+class OracleSample:
+    """The oracle timed on a bounded sample of a configuration's job, scaled
+    to the metric (decode steps per second, one step = all units of one
+    layer cache advancing one token, the prompt phase included).  Units:
+    the host's thread count, then once more with as many as the target time
+    allows.  A prompt longer than ORACLE_MAX_PROMPT (H2O only, whose prompt
+    work grows with the causal pair count) is timed on its first
+    ORACLE_MAX_PROMPT rows and scaled by the pair count."""
 
+    def __init__(self, w, rule, kv8, target_s, units=None, steps=None):
+        import oracle
+        self.w, self.rule = w, rule
+        self.S = steps or w.steps
+        self.Tp = w.prompt
+        if w.prompt > ORACLE_MAX_PROMPT:
+            assert rule == "h2o", "prompt truncation is only scaled for the H2O prompt phase"
+            self.Tp = ORACLE_MAX_PROMPT
+        self.pair_scale = (w.prompt * (w.prompt + 1)) / (self.Tp * (self.Tp + 1))
+        n = min(w.units, units or max(1, oracle.get_threads()))
+        tp, td, th = oracle_job(w, rule, list(range(n)), self.S, kv8, self.Tp)
+        if units is None and tp + td < target_s / 2 and n < w.units:
+            n = min(w.units, max(n + 1, int(n * target_s / max(tp + td, 1e-3))))
+            tp, td, th = oracle_job(w, rule, list(range(n)), self.S, kv8, self.Tp)
+        self.n, self.tp, self.td, self.threads = n, tp, td, th
 
-def oracle_job_sh(w, units, S):
-    """The CPU oracle on a sample of units: persistence-of-importance prompt
-    + S steps.  Returns (seconds, threads)."""
-    import oracle
-    from kv_cache_eviction_h2o_gb300 import workloads as wl
-    g = wl.generate(w, units=units, steps=S)
-    T = w.prompt
-    t0 = time.perf_counter()
-    st, _, _, _ = oracle.sh_prefill(g["Q"], g["K"], g["V"], w.budget, w.heavy, w.recent, w.scale)
-    for t in range(S):
-        oracle.sh_decode_step(st, g["q"][t], g["k"][t], g["v"][t], T + t, w.recent, w.scale)
-    return time.perf_counter() - t0, oracle.get_threads()
+    def seconds(self):
+        return self.tp + self.td
 
+    def layer_job_seconds(self):
+        return (self.tp * self.pair_scale + self.td) * self.w.units / self.n
 
-def oracle_rate(w, seconds, n_units, S):
-    """Oracle time on n_units scaled to the metric: decode steps (all units of
-    one layer cache advancing one token, both variants) per second."""
-    per_layer_job = seconds * w.units / n_units
-    return 2 * S / per_layer_job
+    def rate(self):
+        return self.S / self.layer_job_seconds()
+
+    def describe(self):
+        w = self.w
+        if self.Tp != w.prompt:
+            pr = "prompt phase on the first %d of %d rows, scaled x%.1f by the causal pair count" % (
+                self.Tp, w.prompt, self.pair_scale)
+        else:
+            pr = "prompt %d" % w.prompt
+        return "%d of %d units of one layer (%s, %d decode steps, %s), %.1f s" % (
+            self.n, w.units, pr, self.S, rule_name(self.rule, w), self.seconds())
+
+    def record(self):
+        return {"value": self.rate(), "unit": UNIT, "cores": self.threads, "kind": "oracle",
+                "sample": self.describe()}
 
 
 # -------------------------------------------------------------- reference
 
 def run_reference(args):
-    world, rank, _ = dist_setup(args)
+    """The oracle, as it stands, timed on the host cores on this run's
+    configuration: each step a bounded sample of the job (the prompt phase
+    and the decode steps of as many units as the host has threads)."""
+    world, rank, _ = dist_setup()
     if rank != 0:
         return
-    if args.gqa or args.sh:
-        return run_reference_single(args, world, "gqa" if args.gqa else "sh")
     from kv_cache_eviction_h2o_gb300 import workloads as wl
-    w = wl.WORKLOADS[WORKLOAD]
-    wl_lsh = wl.WORKLOADS["hashevict-" + WORKLOAD]
+    import oracle
+    wname, rule0, _ = CONFIGS[args.config]
+    rule = args.rule or rule0
+    w = wl.WORKLOADS[wname]
+    n = min(w.units, args.oracle_units or max(1, oracle.get_threads()))
     S = args.decode_steps or w.steps
-    n = max(1, args.oracle_units // 4)
-    units = list(range(n))
     for _ in range(args.warmup):
-        oracle_job(w, wl_lsh, units, S, args.kv8)
-    times = []
-    threads = 1
-    for _ in range(args.steps):
-        t, threads = oracle_job(w, wl_lsh, units, S, args.kv8)
-        times.append(t)
-    total = sum(times)
-    value = oracle_rate(w, total / len(times), n, S)
-    sample = "%d of %d units of one %s layer per step (prompt %d, %d decode steps, H2O + HashEvict)" % (
-        n, w.units, WORKLOAD, w.prompt, S)
+        OracleSample(w, rule, args.kv8, 0, units=n, steps=S)
+    samples = [OracleSample(w, rule, args.kv8, 0, units=n, steps=S) for _ in range(args.steps)]
+    per = sum(x.layer_job_seconds() for x in samples) / len(samples)
+    value = S / per
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1000.0 * total / len(times), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "%s-shaped layer: H2O + HashEvict, prompt %d -> %d decode steps, budget %d"
-                               % (WORKLOAD, w.prompt, S, w.budget)},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "ms_per_step": 1000.0 * per, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, shaped like the configuration's layer)",
+        "config": {"workload": config_name(w, rule, S, 1, args.kv8)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": samples[0].threads, "kind": "oracle",
+                         "sample": "per step: " + samples[0].describe()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
 
 
-def run_reference_single(args, world, variant):
-    from kv_cache_eviction_h2o_gb300 import workloads as wl
-    w = wl.WORKLOADS[GQA_WORKLOAD if variant == "gqa" else WORKLOAD]
-    S = args.decode_steps or w.steps
-    n = max(1, args.oracle_units // 16)
-    units = list(range(n))
-    job = (lambda: oracle_job_gqa(w, units, S, args.kv8)) if variant == "gqa" else (lambda: oracle_job_sh(w, units, S))
-    for _ in range(args.warmup):
-        job()
-    times = []
-    threads = 1
-    for _ in range(args.steps):
-        t, threads = job()
-        times.append(t)
-    total = sum(times)
-    value = S / (total / len(times) * w.units / n)
-    line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1000.0 * total / len(times), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": gqa_config_name(w, S, 1, args.kv8) if variant == "gqa" else sh_config_name(w, S, 1)},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": "%d of %d cache units of one %s layer per step (prompt %d, %d decode steps, %s)"
-                                   % (n, w.units, w.name, w.prompt, S,
-                                      "H2O" if variant == "gqa" else "persistence of importance")},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line))
+def rule_name(rule, w):
+    if rule == "lsh":
+        return "HashEvict"
+    if rule == "sh":
+        return "persistence of importance"
+    return "H2O" + (" grouped-query" if w.groups > 1 else "")
 
 
-GQA_WORKLOAD = "gqa-8x8x4"
-
-
-def gqa_config_name(w, S, NL, kv8):
-    return ("%s grouped-query layer x%d (%d x %d key/value heads x %d query heads): H2O, prompt %d -> %d decode "
-            "steps, budget %d (%d heavy + %d recent)%s" % (GQA_WORKLOAD, NL, w.batch, w.heads, w.groups, w.prompt,
-                                                          S, w.budget, w.heavy, w.recent,
-                                                          ", int8 cache slots" if kv8 else ""))
-
-
-def sh_config_name(w, S, NL):
-    return ("%s-shaped layer x%d: persistence-of-importance rule (32-step pivotal histories), prompt %d -> %d "
-            "decode steps, budget %d (%d heavy + %d recent)" % (w.name, NL, w.prompt, S, w.budget, w.heavy, w.recent))
+def config_name(w, rule, S, NL, kv8):
+    heads = ("%d x %d key/value heads x %d query heads" % (w.batch, w.heads, w.groups) if w.groups > 1
+             else "%d x %d heads" % (w.batch, w.heads))
+    split = ("recent %d" % w.recent) if rule == "lsh" else ("%d heavy + %d recent" % (w.heavy, w.recent))
+    return ("%s-shaped layer x%d (%s, head_dim %d): %s, prompt %d -> %d decode steps, budget %d (%s)%s"
+            % (w.name, NL, heads, w.head_dim, rule_name(rule, w), w.prompt, S, w.budget, split,
+               ", int8 cache slots" if kv8 else ""))
 
 
 # -------------------------------------------------------------------- ours
 
-def run_ours(args):
-    import torch
-    import torch.distributed as dist
+class Job:
+    """L layer caches of one configuration on the device: inputs resident
+    in HBM, the handles, the prompt and decode phases as callables over the
+    public API, and their algorithmic work."""
 
-    from kv_cache_eviction_h2o_gb300 import binding as L
-    from kv_cache_eviction_h2o_gb300 import build as lib_build
-    from kv_cache_eviction_h2o_gb300 import workloads as wl
-
-    world, rank, local = dist_setup(args)
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(local)
-    lib_build.build()
-    L.lib()
-    w = wl.WORKLOADS[WORKLOAD]
-    wl_lsh = wl.WORKLOADS["hashevict-" + WORKLOAD]
-    S = args.decode_steps or w.steps
-    NL = args.layers
-    U, T, d, B = w.units, w.prompt, w.head_dim, w.budget
-    dt = L.H2O_BF16 | (L.H2O_KV8 if args.kv8 else 0)
-    stream = torch.cuda.Stream()
-
-    # ---- inputs resident in HBM, one set per layer cache
-    layers = []
-    with torch.cuda.stream(stream):
-        for li in range(NL):
-            g = wl.generate_device(w, seed_offset=li + 1000 * rank, steps=S)
-            layers.append(g)
-        W = torch.from_numpy(wl.lsh_matrix(wl_lsh)).cuda()
-    torch.cuda.synchronize()
-    h2o = [L.h2o_init(B, w.heavy, w.recent, w.batch, w.heads, d, dt, w.scale, stream) for _ in range(NL)]
-    lsh = [L.lsh_init(B, wl_lsh.recent, w.batch, w.heads, d, dt, w.scale, W, stream) for _ in range(NL)]
-    if args.split:
-        for h in h2o + lsh:
-            L.h2o_set_decode_split(h, args.split)
-    out_h = [torch.empty((S, U, d), dtype=torch.float32, device="cuda") for _ in range(NL)]
-    out_l = [torch.empty((S, U, d), dtype=torch.float32, device="cuda") for _ in range(NL)]
-    vic_h = [torch.empty((S, U), dtype=torch.int32, device="cuda") for _ in range(NL)]
-    vic_l = [torch.empty((S, U), dtype=torch.int32, device="cuda") for _ in range(NL)]
-
-    def pre_h2o():
-        for li in range(NL):
-            g = layers[li]
-            L.h2o_prefill(h2o[li], g["Q"], g["K"], g["V"], T)
-
-    def pre_lsh():
-        for li in range(NL):
-            g = layers[li]
-            L.lsh_prefill(lsh[li], g["Q"], g["K"], g["V"], T)
-
-    def dec_h2o():
-        for t in range(S):
-            for li in range(NL):
-                g = layers[li]
-                L.h2o_decode_step(h2o[li], g["q"][t], g["k"][t], g["v"][t], out_h[li][t], vic_h[li][t])
-
-    def dec_lsh():
-        for t in range(S):
-            for li in range(NL):
-                g = layers[li]
-                L.lsh_decode_step(lsh[li], g["q"][t], g["k"][t], g["v"][t], out_l[li][t], vic_l[li][t])
-
-    phases = [("h2o_prefill", pre_h2o), ("lsh_prefill", pre_lsh), ("h2o_decode", dec_h2o), ("lsh_decode", dec_lsh)]
-    # eager pass: allocates prompt scratch, sets kernel attributes, checks errors
-    with torch.cuda.stream(stream):
-        for _, f in phases:
-            f()
-    for h in h2o + lsh:
-        L.h2o_sync(h)
-
-    graphs = []
-    with torch.cuda.stream(stream):
-        for name, f in phases:
-            gr = torch.cuda.CUDAGraph()
-            gr.capture_begin()
-            f()
-            gr.capture_end()
-            graphs.append((name, gr))
-    torch.cuda.synchronize()
-
-    def one_step(evs=None):
+    def __init__(self, L, torch, w, rule, NL, S, kv8, split, stream, rank):
+        from kv_cache_eviction_h2o_gb300 import workloads as wl
+        self.L, self.torch, self.w, self.rule, self.NL, self.S, self.kv8 = L, torch, w, rule, NL, S, kv8
+        self.stream = stream
+        U, G, d, B = w.units, w.groups, w.head_dim, w.budget
+        dt = L.H2O_BF16 | (L.H2O_KV8 if kv8 else 0)
+        self.layers = []
         with torch.cuda.stream(stream):
-            for i, (name, gr) in enumerate(graphs):
+            for li in range(NL):
+                self.layers.append(wl.generate_device(w, seed_offset=li + 1000 * rank, steps=S))
+        torch.cuda.synchronize()
+        if rule == "lsh":
+            self.W = self.layers[0]["W"]
+            self.hs = [L.lsh_init(B, w.recent, w.batch, w.heads, d, dt, w.scale, self.W, stream) for _ in range(NL)]
+            self.prefill_call, self.step_call = L.lsh_prefill, L.lsh_decode_step
+        elif rule == "sh":
+            self.hs = [L.sh_init(B, w.heavy, w.recent, w.batch, w.heads, d, dt, w.scale, stream) for _ in range(NL)]
+            self.prefill_call, self.step_call = L.sh_prefill, L.sh_decode_step
+        elif G > 1:
+            self.hs = [L.h2o_init_gqa(B, w.heavy, w.recent, w.batch, w.heads, G, d, dt, w.scale, stream)
+                       for _ in range(NL)]
+            self.prefill_call, self.step_call = L.h2o_prefill, L.h2o_decode_step
+        else:
+            self.hs = [L.h2o_init(B, w.heavy, w.recent, w.batch, w.heads, d, dt, w.scale, stream)
+                       for _ in range(NL)]
+            self.prefill_call, self.step_call = L.h2o_prefill, L.h2o_decode_step
+        if split:
+            for h in self.hs:
+                L.h2o_set_decode_split(h, split)
+        self.outs = [torch.empty((S, U * G, d), dtype=torch.float32, device="cuda") for _ in range(NL)]
+        self.vics = [torch.empty((S, U), dtype=torch.int32, device="cuda") for _ in range(NL)]
+        # raw device addresses of every per-step argument (the binding takes
+        # plain integers; no tensor views per call)
+
+        def rows(x):
+            base, stride = x.data_ptr(), x.stride(0) * x.element_size()
+            return [base + t * stride for t in range(x.shape[0])]
+        self.ptr = [{k: rows(g[k]) for k in ("q", "k", "v")} for g in self.layers]
+        self.optr = [(rows(o), rows(v)) for o, v in zip(self.outs, self.vics)]
+        self.hh = [int(h) for h in self.hs]
+        self.graphs = None
+
+    # the two phases, over the public API
+    def prefill(self):
+        T = self.w.prompt
+        for li in range(self.NL):
+            g = self.layers[li]
+            self.prefill_call(self.hs[li], g["Q"], g["K"], g["V"], T)
+
+    def decode(self):
+        step = self.step_call
+        for t in range(self.S):
+            for li in range(self.NL):
+                pp, op = self.ptr[li], self.optr[li]
+                step(self.hh[li], pp["q"][t], pp["k"][t], pp["v"][t], op[0][t], op[1][t])
+
+    def sync(self):
+        for h in self.hs:
+            self.L.h2o_sync(h)
+
+    def capture(self):
+        torch = self.torch
+        phases = [("prefill", self.prefill), ("decode", self.decode)]
+        with torch.cuda.stream(self.stream):      # eager pass: scratch, kernel attributes, errors
+            for _, f in phases:
+                f()
+        self.sync()
+        self.graphs = []
+        with torch.cuda.stream(self.stream):
+            for name, f in phases:
+                gr = torch.cuda.CUDAGraph()
+                gr.capture_begin()
+                f()
+                gr.capture_end()
+                self.graphs.append((name, gr))
+        torch.cuda.synchronize()
+
+    def one_step(self, evs=None):
+        with self.torch.cuda.stream(self.stream):
+            for i, (_, gr) in enumerate(self.graphs):
                 gr.replay()
                 if evs is not None:
-                    evs[i].record(stream)
+                    evs[i].record(self.stream)
 
-    for _ in range(args.warmup):
-        one_step()
-    torch.cuda.synchronize()
-    for h in h2o + lsh:
-        L.h2o_sync(h)
+    def time(self, K, W, world):
+        """W warm-up steps, then K steps bracketed by a barrier and device
+        synchronisation; device events after every phase.  Returns
+        (elapsed ms max over ranks, per-phase ms summed over the K steps)."""
+        torch = self.torch
+        import torch.distributed as dist
+        for _ in range(W):
+            self.one_step()
+        torch.cuda.synchronize()
+        self.sync()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in self.graphs] for _ in range(K)]
+        start.record(self.stream)
+        for i in range(K):
+            self.one_step(evs[i])
+        end.record(self.stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        elapsed = start.elapsed_time(end)
+        phase = {name: 0.0 for name, _ in self.graphs}
+        for i in range(K):
+            prev = start if i == 0 else evs[i - 1][-1]
+            for j, (name, _) in enumerate(self.graphs):
+                phase[name] += prev.elapsed_time(evs[i][j])
+                prev = evs[i][j]
+        self.sync()
+        return max_over_ranks(elapsed, world, device="cuda"), phase
 
-    # ---- timed region
-    clocks = Clocks(local)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    step_events = [[torch.cuda.Event(enable_timing=True) for _ in graphs] for _ in range(args.steps)]
-    start.record(stream)
-    for i in range(args.steps):
-        one_step(step_events[i])
-    end.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    clk = clocks.stop()
-    elapsed_ms = start.elapsed_time(end)
-    phase_ms = {name: 0.0 for name, _ in graphs}
-    for i in range(args.steps):
-        prev = start if i == 0 else step_events[i - 1][-1]
-        for j, (name, _) in enumerate(graphs):
-            phase_ms[name] += prev.elapsed_time(step_events[i][j])
-            prev = step_events[i][j]
-    for h in h2o + lsh:
-        L.h2o_sync(h)
-    elapsed_ms = max_over_ranks(elapsed_ms, world, device="cuda")
-    overlap = None if args.no_overlap else time_overlapped(args, torch, dist, graphs, stream, world,
-                                                           2 * S * NL, h2o + lsh, L)
+    # algorithmic work of one launch / phase
+    def decode_kernel(self):
+        if self.rule == "lsh":
+            return "lsh_decode"
+        if self.rule == "sh":
+            return "sh_decode"
+        return "h2o_decode_gqa" if self.w.groups > 1 else "h2o_decode"
 
-    K = args.steps
-    ms_per_step = elapsed_ms / K
-    decode_steps_per_bench_step = 2 * S * NL
-    value = world * decode_steps_per_bench_step / (ms_per_step / 1000.0)
+    def decode_launch_bytes(self):
+        w = self.w
+        U, G, d, B = w.units, w.groups, w.head_dim, w.budget
+        if self.rule == "lsh":
+            return decode_bytes(U, B, d, 2, True, self.kv8)
+        if self.rule == "sh":
+            return decode_bytes_sh(U, B, d, 2)
+        if G > 1:
+            return decode_bytes_gqa(U, G, B, d, 2, self.kv8)
+        return decode_bytes(U, B, d, 2, False, self.kv8)
+
+    def traffic_key(self):
+        return "%s%s@%s" % (self.decode_kernel(), "_kv8" if self.kv8 else "", self.w.name)
+
+    def launches_per_step(self):
+        return self.NL * (prompt_launches(self.rule, self.w.groups) + self.S)
+
+    def destroy(self):
+        for h in self.hs:
+            self.L.h2o_destroy(h)
+        self.hs = []
+        self.graphs = None
+        self.layers = self.outs = self.vics = None
+        self.torch.cuda.synchronize()
+        self.torch.cuda.empty_cache()
+
+
+def rooflines(job, phase_ms, elapsed_ms, K):
+    """Per-kernel rooflines from the live phase times (per-launch averages
+    on the launching stream)."""
     hbm, tf_burst, tf_sus, peak_src = load_peaks()
-
-    # ---- rooflines from the phase times (per-launch averages)
-    eb = 2
-    rl = []
-    n_dec = S * NL * K
-    for name, lsh_flag, src in (("h2o_decode", False, ["decode.cu", "common.cuh"]),
-                                ("lsh_decode", True, ["decode.cu", "common.cuh"])):
-        t_launch = phase_ms[name] / n_dec / 1000.0
-        by = decode_bytes(U, B, d, eb, lsh_flag, args.kv8)
-        ach = by / t_launch / 1e9
-        rl.append({"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
-                   "frac": ach / hbm, "traffic": ncu_traffic(name + ("_kv8" if args.kv8 else "")),
-                   "algorithmic_bytes": by,
-                   "launch_us": t_launch * 1e6, "peak_source": peak_src, "share": phase_ms[name] / elapsed_ms})
-    t_pre = phase_ms["h2o_prefill"] / (NL * K) / 1000.0
-    fl = prefill_flops(U, T, d)
-    ach = fl / t_pre / 1e12
-    rl.append({"kernel": "h2o_prefill", "bound": "tensor", "achieved": ach, "peak": tf_sus, "unit": "TFLOP/s",
-               "frac": ach / tf_sus, "traffic": None, "algorithmic_flops": fl, "launch_us": t_pre * 1e6,
-               "peak_source": peak_src, "share": phase_ms["h2o_prefill"] / elapsed_ms})
-    t_lp = phase_ms["lsh_prefill"] / (NL * K) / 1000.0
-    rl.append({"kernel": "lsh_prefill", "bound": "latency", "launch_us": t_lp * 1e6,
-               "share": phase_ms["lsh_prefill"] / elapsed_ms})
-    dominant = max(rl, key=lambda r: r["share"])
-    main_rl = {k: dominant[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic") if k in dominant}
-    main_rl["kernel"] = dominant["kernel"]
-    main_rl["peak_source"] = peak_src
-    if "achieved" not in main_rl:
-        main_rl = {k: rl[0][k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
-        main_rl["kernel"] = rl[0]["kernel"]
-
-    # ---- end to end through the public API with pinned host buffers
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(args, L, torch, layers, h2o, lsh, out_h, out_l, vic_h, vic_l, W, S, NL, T, stream, world)
-
-    # ---- CPU oracle on a bounded sample (rank 0, one GPU only)
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
-        n = args.oracle_units
-        secs, threads = oracle_job(w, wl_lsh, list(range(n)), S, args.kv8)
-        cpu = {"value": oracle_rate(w, secs, n, S), "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": "%d of %d units of one layer (prompt %d, %d decode steps, H2O + HashEvict), %.1f s"
-                         % (n, U, T, S, secs)}
-
-    launches_per_step = NL * (4 + 3) + 2 * S * NL
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "%s-shaped layer x%d: H2O + HashEvict, prompt %d -> %d decode steps, budget %d "
-                               "(%d heavy + %d recent)%s" % (WORKLOAD, NL, T, S, B, w.heavy, w.recent,
-                                                             ", int8 cache slots" if args.kv8 else ""),
-                   "cache": "int8 codes + fp32 scale per row" if args.kv8 else "bf16",
-                   "batch": w.batch, "heads": w.heads, "head_dim": d, "prompt": T, "decode_steps": S,
-                   "budget": B, "layers": NL, "global_batch": w.batch * world,
-                   "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "inputs larger than L2: %d layer caches (%.0f MB) + prompts (%.0f MB); a cache is reused "
-                         "only after %d others" % (NL, 2 * NL * decode_bytes(U, B, d, eb, False, args.kv8) / 1e6,
-                                                   NL * 3 * U * T * d * eb / 1e6, NL - 1),
-                   "step": "one decode step = all %d (batch x head) units of one layer cache advance one token; "
-                           "both eviction variants counted; prompt phases inside the timed step" % U},
-        "roofline": main_rl,
-        "rooflines": rl,
-        "phases_ms_per_step": {k: v / K for k, v in phase_ms.items()},
-        "head_steps_per_s": value * U,
-        "cpu_baseline": cpu,
-        "clocks": clk,
-        "e2e": e2e,
-        "gpu_launches": launches_per_step * K,
-        "overlap": overlap,
-    }
-    for h in h2o + lsh:
-        L.h2o_destroy(h)
-    if rank == 0:
-        print(json.dumps(line))
-    if world > 1:
-        dist.destroy_process_group()
-
-
-def time_overlapped(args, torch, dist, graphs, stream, world, units_per_step, handles, L):
-    """The same K steps with the two eviction jobs, independent of each
-    other, on two streams: the H2O prompt and decode graphs on `stream`, the
-    HashEvict ones on a second stream, joined at the end of every step, so a
-    job's prompt phase and per-launch fixed costs run under the other job's
-    HBM-bound decode.  Timed like the main region (barrier, device events,
-    max over ranks); per-kernel rooflines come from the serial region."""
-    gd = dict(graphs)
-    side = torch.cuda.Stream()
-    fork = [torch.cuda.Event() for _ in range(2)]
-    join = [torch.cuda.Event() for _ in range(2)]
-
-    def step(i):
-        fork[i % 2].record(stream)
-        side.wait_event(fork[i % 2])
-        with torch.cuda.stream(side):
-            gd["lsh_prefill"].replay()
-            gd["lsh_decode"].replay()
-            join[i % 2].record(side)
-        with torch.cuda.stream(stream):
-            gd["h2o_prefill"].replay()
-            gd["h2o_decode"].replay()
-            stream.wait_event(join[i % 2])
-
-    for i in range(max(args.warmup, 3)):
-        step(i)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for i in range(args.steps):
-        step(i)
-    end.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    for h in handles:
-        L.h2o_sync(h)
-    ms = max_over_ranks(start.elapsed_time(end), world, device="cuda") / args.steps
-    return {"value": world * units_per_step / (ms / 1000.0), "unit": UNIT, "ms_per_step": ms, "steps": args.steps,
-            "schedule": "H2O job and HashEvict job on two streams, joined every step"}
-
-
-def run_e2e(args, L, torch, layers, h2o, lsh, out_h, out_l, vic_h, vic_l, W, S, NL, T, stream, world):
-    """Same job through the public API, eager, with every input copied in from
-    pinned host memory and every output copied out inside the timed region."""
-    host_in = []
-    for g in layers:
-        host_in.append({k: g[k].cpu().pin_memory() for k in ("Q", "K", "V", "q", "k", "v")})
-    host_out = [(torch.empty(o.shape, dtype=o.dtype).pin_memory(), torch.empty(o2.shape, dtype=o2.dtype).pin_memory(),
-                 torch.empty(v.shape, dtype=v.dtype).pin_memory(), torch.empty(v2.shape, dtype=v2.dtype).pin_memory())
-                for o, o2, v, v2 in zip(out_h, out_l, vic_h, vic_l)]
-    h2d = sum(x.numel() * x.element_size() for hi in host_in for x in hi.values())
-    d2h = sum(x.numel() * x.element_size() for ho in host_out for x in ho)
-
-    copy_stream = torch.cuda.Stream()
-    ready = [torch.cuda.Event() for _ in range(NL)]
-    ready_dec = torch.cuda.Event()
-    h2o_done = torch.cuda.Event()
-    out_h_home = torch.cuda.Event()
-    # raw device addresses of every per-step argument, computed once (the
-    # binding takes plain integers; no tensor views per call)
-    def rows(x):
-        base, stride = x.data_ptr(), x.stride(0) * x.element_size()
-        return [base + t * stride for t in range(x.shape[0])]
-    ptr = [{k: rows(layers[li][k]) for k in ("q", "k", "v")} for li in range(NL)]
-    optr = [(rows(out_h[li]), rows(out_l[li]), rows(vic_h[li]), rows(vic_l[li])) for li in range(NL)]
-    hh = [int(h) for h in h2o]
-    hl = [int(h) for h in lsh]
-
-    def step():
-        # inputs stream in on a copy stream: every layer's prompt rows first
-        # (each layer's prompt phase waits only for its own), the decode
-        # steps' rows last; the H2O outputs go home while the HashEvict
-        # steps run
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_stream(stream)
-            for li in range(NL):
-                for k in ("Q", "K", "V"):
-                    layers[li][k].copy_(host_in[li][k], non_blocking=True)
-                ready[li].record(copy_stream)
-            for li in range(NL):
-                for k in ("q", "k", "v"):
-                    layers[li][k].copy_(host_in[li][k], non_blocking=True)
-            ready_dec.record(copy_stream)
-        with torch.cuda.stream(stream):
-            for li in range(NL):
-                stream.wait_event(ready[li])
-                g = layers[li]
-                L.h2o_prefill(h2o[li], g["Q"], g["K"], g["V"], T)
-                L.lsh_prefill(lsh[li], g["Q"], g["K"], g["V"], T)
-            stream.wait_event(ready_dec)
-            for t in range(S):
-                for li in range(NL):
-                    pp, op = ptr[li], optr[li]
-                    L.h2o_decode_step(hh[li], pp["q"][t], pp["k"][t], pp["v"][t], op[0][t], op[2][t])
-            h2o_done.record(stream)
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(h2o_done)
-            for li in range(NL):
-                host_out[li][0].copy_(out_h[li], non_blocking=True)
-                host_out[li][2].copy_(vic_h[li], non_blocking=True)
-            out_h_home.record(copy_stream)
-        with torch.cuda.stream(stream):
-            for t in range(S):
-                for li in range(NL):
-                    pp, op = ptr[li], optr[li]
-                    L.lsh_decode_step(hl[li], pp["q"][t], pp["k"][t], pp["v"][t], op[1][t], op[3][t])
-            for li in range(NL):
-                host_out[li][1].copy_(out_l[li], non_blocking=True)
-                host_out[li][3].copy_(vic_l[li], non_blocking=True)
-            stream.wait_event(out_h_home)
-
-    step()
-    torch.cuda.synchronize()
-    # One step's calls -- the input copies, every prompt and decode call and
-    # the output copies -- captured once into a CUDA graph (all step state
-    # lives on the device, so a replay is a new step); a replay still moves
-    # every input in and every output out.  Eager launches are the fallback.
-    run = step
-    mode = "eager"
-    try:
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            gr.capture_begin()
-            step()
-            gr.capture_end()
-        torch.cuda.synchronize()
-
-        def run():
-            with torch.cuda.stream(stream):
-                gr.replay()
-        run()
-        torch.cuda.synchronize()
-        mode = "graph"
-    except Exception as e:  # capture unsupported: keep the eager loop
-        print("e2e: graph capture failed (%s); timing eager calls" % e, file=sys.stderr)
-        torch.cuda.synchronize()
-    secs, each = time_e2e_steps(args, run, torch)
-    value = world * 2 * S * NL / secs
-    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": secs * 1000.0, "steps": len(each), "ms_each": each, "statistic": "median",
-            "launch": mode}
-
-
-def time_e2e_steps(args, run, torch):
-    """Each end-to-end step timed on its own (host clock, device synchronised
-    on both sides); returns the median seconds and every step's ms.  The
-    host-device link is shared with other GPUs of the machine, so single
-    steps can be slowed by traffic that is not this job's."""
-    n = max(1, min(args.steps, 5))
-    each = []
-    for _ in range(n):
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        run()
-        torch.cuda.synchronize()
-        each.append(time.perf_counter() - t0)
-    return statistics.median(each), [round(1000.0 * x, 3) for x in each]
-
-
-def run_single(args, variant):
-    """One eviction rule alone: H2O on the grouped-query layer ("gqa") or the
-    persistence-of-importance rule on the OPT-6.7B-shaped layer ("sh").  L
-    layer caches, prompt phase then S decode steps token-major over the
-    layers, replayed from CUDA graphs with inputs in HBM; e2e through the
-    public API with host copies."""
-    import torch
-    import torch.distributed as dist
-
-    from kv_cache_eviction_h2o_gb300 import binding as L
-    from kv_cache_eviction_h2o_gb300 import build as lib_build
-    from kv_cache_eviction_h2o_gb300 import workloads as wl
-
-    world, rank, local = dist_setup(args)
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    lib_build.build()
-    L.lib()
-    gqa = variant == "gqa"
-    w = wl.WORKLOADS[GQA_WORKLOAD if gqa else WORKLOAD]
-    S = args.decode_steps or w.steps
-    NL = args.layers
+    w, NL, S = job.w, job.NL, job.S
     U, G, T, d, B = w.units, w.groups, w.prompt, w.head_dim, w.budget
-    dt = L.H2O_BF16 | (L.H2O_KV8 if args.kv8 else 0)
-    stream = torch.cuda.Stream()
-    layers = []
-    with torch.cuda.stream(stream):
-        for li in range(NL):
-            layers.append(wl.generate_device(w, seed_offset=li + 1000 * rank, steps=S))
-    torch.cuda.synchronize()
-    if gqa:
-        hs = [L.h2o_init_gqa(B, w.heavy, w.recent, w.batch, w.heads, G, d, dt, w.scale, stream) for _ in range(NL)]
-        prefill, step = L.h2o_prefill, L.h2o_decode_step
-    else:
-        hs = [L.sh_init(B, w.heavy, w.recent, w.batch, w.heads, d, dt, w.scale, stream) for _ in range(NL)]
-        prefill, step = L.sh_prefill, L.sh_decode_step
-    if args.split:
-        for h in hs:
-            L.h2o_set_decode_split(h, args.split)
-    outs = [torch.empty((S, U * G, d), dtype=torch.float32, device="cuda") for _ in range(NL)]
-    vics = [torch.empty((S, U), dtype=torch.int32, device="cuda") for _ in range(NL)]
-
-    def pre():
-        for li in range(NL):
-            g = layers[li]
-            prefill(hs[li], g["Q"], g["K"], g["V"], T)
-
-    def dec():
-        for t in range(S):
-            for li in range(NL):
-                g = layers[li]
-                step(hs[li], g["q"][t], g["k"][t], g["v"][t], outs[li][t], vics[li][t])
-
-    phases = [("h2o_prefill", pre), ("h2o_decode", dec)]
-    with torch.cuda.stream(stream):
-        for _, f in phases:
-            f()
-    for h in hs:
-        L.h2o_sync(h)
-    graphs = []
-    with torch.cuda.stream(stream):
-        for name, f in phases:
-            gr = torch.cuda.CUDAGraph()
-            gr.capture_begin()
-            f()
-            gr.capture_end()
-            graphs.append((name, gr))
-    torch.cuda.synchronize()
-
-    def one_step(evs=None):
-        with torch.cuda.stream(stream):
-            for i, (_, gr) in enumerate(graphs):
-                gr.replay()
-                if evs is not None:
-                    evs[i].record(stream)
-
-    for _ in range(args.warmup):
-        one_step()
-    torch.cuda.synchronize()
-    for h in hs:
-        L.h2o_sync(h)
-
-    clocks = Clocks(local)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    step_events = [[torch.cuda.Event(enable_timing=True) for _ in graphs] for _ in range(args.steps)]
-    start.record(stream)
-    for i in range(args.steps):
-        one_step(step_events[i])
-    end.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    clk = clocks.stop()
-    elapsed_ms = start.elapsed_time(end)
-    phase_ms = {name: 0.0 for name, _ in graphs}
-    for i in range(args.steps):
-        prev = start if i == 0 else step_events[i - 1][-1]
-        for j, (name, _) in enumerate(graphs):
-            phase_ms[name] += prev.elapsed_time(step_events[i][j])
-            prev = step_events[i][j]
-    for h in hs:
-        L.h2o_sync(h)
-    elapsed_ms = max_over_ranks(elapsed_ms, world, device="cuda")
-    K = args.steps
-    ms_per_step = elapsed_ms / K
-    value = world * S * NL / (ms_per_step / 1000.0)
-    hbm, tf_burst, tf_sus, peak_src = load_peaks()
-
-    t_dec = phase_ms["h2o_decode"] / (S * NL * K) / 1000.0
-    by = decode_bytes_gqa(U, G, B, d, 2, args.kv8) if gqa else decode_bytes_sh(U, B, d, 2)
-    ach = by / t_dec / 1e9
-    dname = "h2o_decode_gqa" if gqa else "sh_decode"
-    rl = [{"kernel": dname, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
-           "frac": ach / hbm, "traffic": ncu_traffic(("h2o_gqa" if gqa else "sh") + ("_kv8" if args.kv8 else "")),
-           "algorithmic_bytes": by, "launch_us": t_dec * 1e6, "peak_source": peak_src,
-           "share": phase_ms["h2o_decode"] / elapsed_ms}]
-    t_pre = phase_ms["h2o_prefill"] / (NL * K) / 1000.0
-    if gqa:
+    rl = []
+    t_launch = phase_ms["decode"] / (S * NL * K) / 1000.0
+    by = job.decode_launch_bytes()
+    ach = by / t_launch / 1e9
+    rec = {"kernel": job.decode_kernel(), "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+           "frac": ach / hbm, "traffic": ncu_traffic(job.traffic_key()), "algorithmic_bytes": by,
+           "launch_us": t_launch * 1e6, "peak_source": peak_src, "share": phase_ms["decode"] / elapsed_ms}
+    if job.rule == "h2o" and G == 1 and not job.kv8:
+        mb = method_bytes(U, B, d, 2)
+        rec["method_bytes"] = mb
+        rec["method_frac"] = mb / t_launch / 1e9 / hbm
+    rl.append(rec)
+    t_pre = phase_ms["prefill"] / (NL * K) / 1000.0
+    if job.rule == "h2o":
         fl = prefill_flops(U * G, T, d)
         ach = fl / t_pre / 1e12
-        rl.append({"kernel": "h2o_prefill_gqa", "bound": "tensor", "achieved": ach, "peak": tf_sus,
-                   "unit": "TFLOP/s", "frac": ach / tf_sus, "traffic": None, "algorithmic_flops": fl,
-                   "launch_us": t_pre * 1e6, "peak_source": peak_src,
-                   "share": phase_ms["h2o_prefill"] / elapsed_ms})
+        rl.append({"kernel": "h2o_prefill" + ("_gqa" if G > 1 else ""), "bound": "tensor", "achieved": ach,
+                   "peak": tf_sus, "unit": "TFLOP/s", "frac": ach / tf_sus, "traffic": None,
+                   "algorithmic_flops": fl, "launch_us": t_pre * 1e6, "peak_source": peak_src + " (sustained)",
+                   "share": phase_ms["prefill"] / elapsed_ms})
+    elif job.rule == "lsh":
+        rl.append({"kernel": "lsh_prefill", "bound": "latency", "launch_us": t_pre * 1e6,
+                   "serial_steps": max(0, T - B),
+                   "ns_per_serial_step": t_pre * 1e9 / max(1, T - B),
+                   "code_flops": lsh_code_flops(U, T, d),
+                   "share": phase_ms["prefill"] / elapsed_ms})
     else:
         rl.append({"kernel": "sh_prefill", "bound": "latency", "launch_us": t_pre * 1e6,
-                   "share": phase_ms["h2o_prefill"] / elapsed_ms})
-    dominant = max((r for r in rl if "achieved" in r), key=lambda r: r["share"])
-    main_rl = {k: dominant[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
-    main_rl["kernel"] = dominant["kernel"]
-    main_rl["peak_source"] = peak_src
+                   "share": phase_ms["prefill"] / elapsed_ms})
+    return rl
 
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e_single(args, L, torch, layers, hs, outs, vics, S, NL, T, stream, world, prefill, step)
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
-        n = max(1, args.oracle_units // 4)
-        if gqa:
-            secs, threads = oracle_job_gqa(w, list(range(n)), S, args.kv8)
-        else:
-            secs, threads = oracle_job_sh(w, list(range(n)), S)
-        cpu = {"value": S / (secs * U / n), "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": "%d of %d cache units of one layer (prompt %d, %d decode steps, %s), %.1f s"
-                         % (n, U, T, S, "H2O" if gqa else "persistence of importance", secs)}
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": gqa_config_name(w, S, NL, args.kv8) if gqa else sh_config_name(w, S, NL),
+
+def main_roofline(rl):
+    measured = [r for r in rl if "achieved" in r]
+    dom = max(measured, key=lambda r: r["share"])
+    out = {k: dom[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+    out["kernel"] = dom["kernel"]
+    out["peak_source"] = dom["peak_source"]
+    return out
+
+
+def l2_note(job):
+    w = job.w
+    by = job.decode_launch_bytes()
+    prompts = job.NL * (w.groups + 2) * w.units * w.prompt * w.head_dim * 2
+    return ("inputs larger than L2 (129 MB): %d layer caches (%.0f MB) + prompts (%.0f MB); a cache is "
+            "reused only after %d others" % (job.NL, job.NL * by / 1e6, prompts / 1e6, job.NL - 1))
+
+
+def measure(args, L, torch, cname, rule, NL, S, stream, world, rank, want_e2e, cpu_seconds, clocks=None):
+    """Build, time and describe one configuration's job (clocks sampled
+    during its timed region when a sampler is given)."""
+    from kv_cache_eviction_h2o_gb300 import workloads as wl
+    wname, rule0, NL0 = CONFIGS[cname]
+    w = wl.WORKLOADS[wname]
+    rule = rule or rule0
+    NL = NL or NL0
+    S = S or w.steps
+    job = Job(L, torch, w, rule, NL, S, args.kv8, args.split, stream, rank)
+    job.capture()
+    if clocks is not None:
+        clocks.start()
+        time.sleep(0.3)
+    elapsed, phase = job.time(args.steps, args.warmup, world)
+    clk = clocks.stop() if clocks is not None else None
+    K = args.steps
+    ms = elapsed / K
+    rl = rooflines(job, phase, elapsed, K)
+    rec = {
+        "config": {"workload": config_name(w, rule, S, NL, args.kv8),
                    "cache": "int8 codes + fp32 scale per row" if args.kv8 else "bf16",
-                   "batch": w.batch, "kv_heads": w.heads, "groups": G, "head_dim": d, "prompt": T,
-                   "decode_steps": S, "budget": B, "layers": NL, "global_batch": w.batch * world,
-                   "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "inputs larger than L2: %d layer caches (%.0f MB) + prompts (%.0f MB); a cache is reused "
-                         "only after %d others" % (NL, NL * by / 1e6, NL * (G + 2) * U * T * d * 2 / 1e6, NL - 1),
-                   "step": "one decode step = all %d cache units (%d query heads) of one layer cache advance one "
-                           "token; prompt phases inside the timed step" % (U, U * G)},
-        "roofline": main_rl,
-        "rooflines": rl,
-        "phases_ms_per_step": {k: v / K for k, v in phase_ms.items()},
-        "cpu_baseline": cpu,
-        "clocks": clk,
-        "e2e": e2e,
-        # prompt launches per layer: row statistics, column sums, head sums,
-        # selection, gather (grouped-query); row statistics, flags, selection,
-        # gather (persistence rule, tensor-core path); one launch per decode step
-        "gpu_launches": (NL * (5 if gqa else 4) + S * NL) * K,
+                   "batch": w.batch, "heads": w.heads, "groups": w.groups, "head_dim": w.head_dim,
+                   "prompt": w.prompt, "decode_steps": S, "budget": w.budget, "heavy": w.heavy,
+                   "recent": w.recent, "layers": NL, "l2": l2_note(job),
+                   "step": "one decode step = all %d units of one layer cache advance one token (%s); prompt "
+                           "phases inside the timed step" % (w.units, rule_name(rule, w))},
+        "value": world * S * NL / (ms / 1000.0), "unit": UNIT, "ms_per_step": ms,
+        "head_steps_per_s": world * S * NL * w.query_units / (ms / 1000.0),
+        "roofline": main_roofline(rl), "rooflines": rl,
+        "launch_us": {r["kernel"]: r["launch_us"] for r in rl},
+        "phases_ms_per_step": {k: v / K for k, v in phase.items()},
+        "gpu_launches": job.launches_per_step() * K,
     }
-    for h in hs:
-        L.h2o_destroy(h)
-    if rank == 0:
-        print(json.dumps(line))
-    if world > 1:
-        dist.destroy_process_group()
+    if want_e2e:
+        rec["e2e"] = run_e2e(job, world)
+    job.destroy()
+    del job
+    rec["clocks"] = clk
+    rec["cpu_baseline"] = None
+    if rank == 0 and world == 1 and cpu_seconds > 0:
+        rec["cpu_baseline"] = OracleSample(w, rule, args.kv8, cpu_seconds, steps=S).record()
+    return rec
 
 
-def run_e2e_single(args, L, torch, layers, hs, outs, vics, S, NL, T, stream, world, prefill, step_call):
-    """The single-rule job through the public API: every input copied in
-    from pinned host memory and every output copied out inside the timed
-    region, one step captured into a CUDA graph."""
-    host_in = [{k: g[k].cpu().pin_memory() for k in ("Q", "K", "V", "q", "k", "v")} for g in layers]
+def run_e2e(job, world):
+    """The job through the public API: every input copied in from pinned host
+    memory and every output copied out inside the timed region, one step
+    captured into a CUDA graph (all step state lives on the device, so a
+    replay is a new step that still moves every input in and every output
+    out)."""
+    torch = job.torch
+    NL, stream = job.NL, job.stream
+    host_in = [{k: g[k].cpu().pin_memory() for k in ("Q", "K", "V", "q", "k", "v")} for g in job.layers]
     host_out = [(torch.empty(o.shape, dtype=o.dtype).pin_memory(), torch.empty(v.shape, dtype=v.dtype).pin_memory())
-                for o, v in zip(outs, vics)]
+                for o, v in zip(job.outs, job.vics)]
     h2d = sum(x.numel() * x.element_size() for hi in host_in for x in hi.values())
     d2h = sum(x.numel() * x.element_size() for ho in host_out for x in ho)
     copy_stream = torch.cuda.Stream()
@@ -943,29 +698,29 @@ def run_e2e_single(args, L, torch, layers, hs, outs, vics, S, NL, T, stream, wor
     ready_dec = torch.cuda.Event()
 
     def step():
+        # prompt rows first (each layer's prompt phase waits only for its
+        # own), the decode rows last
         with torch.cuda.stream(copy_stream):
             copy_stream.wait_stream(stream)
             for li in range(NL):
                 for k in ("Q", "K", "V"):
-                    layers[li][k].copy_(host_in[li][k], non_blocking=True)
+                    job.layers[li][k].copy_(host_in[li][k], non_blocking=True)
                 ready[li].record(copy_stream)
             for li in range(NL):
                 for k in ("q", "k", "v"):
-                    layers[li][k].copy_(host_in[li][k], non_blocking=True)
+                    job.layers[li][k].copy_(host_in[li][k], non_blocking=True)
             ready_dec.record(copy_stream)
         with torch.cuda.stream(stream):
+            T = job.w.prompt
             for li in range(NL):
                 stream.wait_event(ready[li])
-                g = layers[li]
-                prefill(hs[li], g["Q"], g["K"], g["V"], T)
+                g = job.layers[li]
+                job.prefill_call(job.hs[li], g["Q"], g["K"], g["V"], T)
             stream.wait_event(ready_dec)
-            for t in range(S):
-                for li in range(NL):
-                    g = layers[li]
-                    step_call(hs[li], g["q"][t], g["k"][t], g["v"][t], outs[li][t], vics[li][t])
+            job.decode()
             for li in range(NL):
-                host_out[li][0].copy_(outs[li], non_blocking=True)
-                host_out[li][1].copy_(vics[li], non_blocking=True)
+                host_out[li][0].copy_(job.outs[li], non_blocking=True)
+                host_out[li][1].copy_(job.vics[li], non_blocking=True)
 
     step()
     torch.cuda.synchronize()
@@ -981,18 +736,66 @@ def run_e2e_single(args, L, torch, layers, hs, outs, vics, S, NL, T, stream, wor
             gr.replay()
     run()
     torch.cuda.synchronize()
-    secs, each = time_e2e_steps(args, run, torch)
-    return {"value": world * S * NL / secs, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": secs * 1000.0, "steps": len(each), "ms_each": each, "statistic": "median",
-            "launch": "graph"}
+    job.sync()
+    n = 5
+    each = []
+    for _ in range(n):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        run()
+        torch.cuda.synchronize()
+        each.append(time.perf_counter() - t0)
+    job.sync()
+    secs = statistics.median(each)
+    return {"value": world * job.S * NL / secs, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": secs * 1000.0, "steps": n, "ms_each": [round(1000.0 * x, 3) for x in each],
+            "statistic": "median (the host link is shared with the machine's other GPUs)", "launch": "graph"}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from kv_cache_eviction_h2o_gb300 import binding as L
+    from kv_cache_eviction_h2o_gb300 import build as lib_build
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    lib_build.build()
+    L.lib()
+    stream = torch.cuda.Stream()
+    main = measure(args, L, torch, args.config, args.rule, args.layers, args.decode_steps, stream, world, rank,
+                   not args.no_e2e, 0 if args.no_cpu else args.oracle_seconds, Clocks(local))
+    subs = {}
+    if not args.no_sub:
+        names = [s for s in (args.sub.split(",") if args.sub else SUB_CONFIGS) if s and s != args.config]
+        for name in names:
+            subs[name] = measure(args, L, torch, name, None, None, None, stream, world, rank, False,
+                                 0 if args.no_cpu else args.oracle_seconds / 2)
+    line = {
+        "metric": METRIC, "value": main["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": main["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, shaped like the configuration's layer)",
+        "config": dict(main["config"], global_batch=main["config"]["batch"] * world,
+                       parallelism="replicas" if world > 1 else "single"),
+        "roofline": main["roofline"], "rooflines": main["rooflines"], "launch_us": main["launch_us"],
+        "phases_ms_per_step": main["phases_ms_per_step"], "head_steps_per_s": main["head_steps_per_s"],
+        "cpu_baseline": main["cpu_baseline"], "clocks": main["clocks"], "e2e": main.get("e2e"),
+        "gpu_launches": main["gpu_launches"],
+        "sub_records": subs,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
 
 
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
-    elif args.gqa or args.sh:
-        run_single(args, "gqa" if args.gqa else "sh")
     else:
         run_ours(args)
 

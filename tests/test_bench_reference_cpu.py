@@ -1,6 +1,8 @@
 """The benchmark's reference arm (the CPU oracle) on the host: one JSON line
 from rank 0 with the contract's keys, nothing from another rank (as when it
-is launched at two ranks), for the default job and the grouped-query and
+is launched at two ranks), for the default configuration (the OPT-30B-shaped
+layer), the long-context configuration (its prompt phase timed on a shorter
+prompt and scaled), HashEvict, and the grouped-query and
 persistence-of-importance legs."""
 import json
 import os
@@ -10,7 +12,7 @@ import sys
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-ARGS = ["--impl", "reference", "--steps", "1", "--warmup", "0", "--decode-steps", "2", "--oracle-units", "4"]
+ARGS = ["--impl", "reference", "--steps", "1", "--warmup", "0", "--decode-steps", "2", "--oracle-units", "2"]
 
 
 def _run(extra, rank, world):
@@ -21,7 +23,8 @@ def _run(extra, rank, world):
     return [line for line in r.stdout.splitlines() if line.startswith("{")]
 
 
-@pytest.mark.parametrize("extra", [[], ["--gqa"], ["--sh"]])
+@pytest.mark.parametrize("extra", [[], ["--config", "llama-7b-32k"], ["--config", "hashevict-opt-6.7b"],
+                                   ["--gqa"], ["--sh"]])
 def test_reference_arm_line(extra):
     lines = _run(extra, 0, 2)
     assert len(lines) == 1
@@ -31,6 +34,7 @@ def test_reference_arm_line(extra):
         assert key in d, key
     assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    assert d["metric"].startswith("H2O decode steps/s") and d["unit"] == "steps/s"
 
 
 def test_reference_arm_other_rank_is_silent():
