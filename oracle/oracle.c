@@ -836,7 +836,12 @@ void oracle_fg_profile(int U, int T, int d, int B, int H, int r, double scale, d
             }
             if (pass == 0) {
                 const int ncand = T - r;
-                if (ncand > 0) {
+                if (T <= B) {
+                    /* the H2O prompt rule keeps every token of a prompt that
+                       fits the budget, so the frequency + local cache holds
+                       them all */
+                    for (int j = 0; j < T; ++j) heavy[j] = 1;
+                } else if (ncand > 0) {
                     cand_t* cs = (cand_t*)malloc(sizeof(cand_t) * (size_t)ncand);
                     for (int j = 0; j < ncand; ++j) { cs[j].c = c[j]; cs[j].j = j; }
                     qsort(cs, (size_t)ncand, sizeof(cand_t), cand_cmp);

@@ -795,6 +795,19 @@ def test_fg_heavy_hitter_head_takes_the_frequency_policy():
     assert pol0[0] == 2 and rf0[0] < 0.2
 
 
+def test_fg_prompt_within_budget_keeps_everything():
+    # T <= B: the local window and the H2O prompt cache (which keeps every
+    # token of a prompt that fits the budget) both hold every key a row sees,
+    # so both recover each row's whole mass, 1, and the local policy wins
+    g = np.random.default_rng(6)
+    Q = g.standard_normal((2, 20, 8)) * 3; K = g.standard_normal((2, 20, 8)) * 3
+    for B, H, r in ((20, 10, 10), (32, 16, 16), (25, 0, 25)):
+        pol, rl, rf = oracle.fg_profile(Q, K, B, H, r, 0.7, 0.95)
+        np.testing.assert_allclose(rl, 1.0, atol=1e-13)
+        np.testing.assert_allclose(rf, 1.0, atol=1e-13)
+        assert (pol == 0).all()
+
+
 def test_fg_matches_brute_force():
     # attention rows by a numpy softmax, kept sets as Python sets
     g = np.random.default_rng(5)
