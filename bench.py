@@ -38,6 +38,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -55,9 +57,10 @@ CONFIGS = {
     "llama-7b-32k": ("llama-7b-32k", "h2o", 8),             # 8 x 68.7 MB
     "hashevict-opt-6.7b": ("hashevict-opt-6.7b", "lsh", 8),
     "gqa-8x8x4": ("gqa-8x8x4", "h2o", 8),
+    "fastgen-opt-6.7b": ("fastgen-opt-6.7b", "fg", 8),         # per-head policies, mixed budgets
 }
 DEFAULT_CONFIG = "opt-30b"
-SUB_CONFIGS = ("opt-6.7b", "llama-7b-32k", "hashevict-opt-6.7b")
+SUB_CONFIGS = ("opt-6.7b", "llama-7b-32k", "hashevict-opt-6.7b", "fastgen-opt-6.7b")
 
 
 def parse(argv=None):
@@ -273,6 +276,8 @@ def prompt_launches(rule, G):
         return 3
     if rule == "sh":
         return 4
+    if rule == "fg":
+        return 5          # row statistics, column and band sums, selection, policy, gather
     return 5 if G > 1 else 4
 
 
@@ -303,6 +308,12 @@ def oracle_job(w, rule, units, S, kv8=False, prompt=None):
         t1 = time.perf_counter()
         for t in range(S):
             oracle.sh_decode_step(st, g["q"][t], g["k"][t], g["v"][t], T + t, w.recent, w.scale)
+    elif rule == "fg":
+        _, states, params = oracle.fg_prefill(g["Q"], g["K"], g["V"], w.budget, w.heavy, w.recent, w.scale, w.tau,
+                                              w.full_budget)
+        t1 = time.perf_counter()
+        for t in range(S):
+            oracle.fg_decode_step(states, params, g["q"][t], g["k"][t], g["v"][t], T + t, w.scale)
     elif w.groups > 1:
         st, _, _, _, _ = oracle.h2o_prefill_gqa(g["Q"], g["K"], g["V"], w.budget, w.heavy, w.recent, w.scale)
         if kv8:
@@ -407,6 +418,8 @@ def run_reference(args):
 def rule_name(rule, w):
     if rule == "lsh":
         return "HashEvict"
+    if rule == "fg":
+        return "per-head policies (local / frequency + local / full, tau %g, full budget %d)" % (w.tau, w.full_budget)
     if rule == "sh":
         return "persistence of importance"
     return "H2O" + (" grouped-query" if w.groups > 1 else "")
@@ -446,6 +459,10 @@ class Job:
         elif rule == "sh":
             self.hs = [L.sh_init(B, w.heavy, w.recent, w.batch, w.heads, d, dt, w.scale, stream) for _ in range(NL)]
             self.prefill_call, self.step_call = L.sh_prefill, L.sh_decode_step
+        elif rule == "fg":
+            self.hs = [L.fg_init(B, w.heavy, w.recent, w.full_budget, w.tau, w.batch, w.heads, d, dt, w.scale, stream)
+                       for _ in range(NL)]
+            self.prefill_call, self.step_call = L.fg_prefill, L.fg_decode_step
         elif G > 1:
             self.hs = [L.h2o_init_gqa(B, w.heavy, w.recent, w.batch, w.heads, G, d, dt, w.scale, stream)
                        for _ in range(NL)]
@@ -549,6 +566,8 @@ class Job:
     def decode_kernel(self):
         if self.rule == "lsh":
             return "lsh_decode"
+        if self.rule == "fg":
+            return "fg_decode"
         if self.rule == "sh":
             return "sh_decode"
         return "h2o_decode_gqa" if self.w.groups > 1 else "h2o_decode"
@@ -560,6 +579,21 @@ class Job:
             return decode_bytes(U, B, d, 2, True, self.kv8)
         if self.rule == "sh":
             return decode_bytes_sh(U, B, d, 2)
+        if self.rule == "fg":
+            # every unit on its own policy's budget; a full-cache unit grows by
+            # one slot a step: the average over the S steps of each launch
+            L = self.L
+            pol = np.empty(U, np.int32)
+            L.h2o_sync(self.hs[0])
+            L.fg_get_policy(self.hs[0], pol)
+            tot = 0.0
+            for u in range(U):
+                Bu = w.full_budget if pol[u] == 2 else B
+                n0 = min(Bu, w.prompt)
+                avg_n = sum(min(Bu, n0 + t) for t in range(self.S)) / self.S
+                tot += decode_bytes(1, avg_n, d, 2, False)
+            self.policy_mix = {int(k): int((pol == k).sum()) for k in (0, 1, 2)}
+            return tot
         if G > 1:
             return decode_bytes_gqa(U, G, B, d, 2, self.kv8)
         return decode_bytes(U, B, d, 2, False, self.kv8)
@@ -599,10 +633,11 @@ def rooflines(job, phase_ms, elapsed_ms, K):
         rec["method_frac"] = mb / t_launch / 1e9 / hbm
     rl.append(rec)
     t_pre = phase_ms["prefill"] / (NL * K) / 1000.0
-    if job.rule == "h2o":
+    if job.rule in ("h2o", "fg"):
         fl = prefill_flops(U * G, T, d)
         ach = fl / t_pre / 1e12
-        rl.append({"kernel": "h2o_prefill" + ("_gqa" if G > 1 else ""), "bound": "tensor", "achieved": ach,
+        rl.append({"kernel": ("fg_prefill" if job.rule == "fg" else "h2o_prefill") + ("_gqa" if G > 1 else ""),
+                   "bound": "tensor", "achieved": ach,
                    "peak": tf_sus, "unit": "TFLOP/s", "frac": ach / tf_sus, "traffic": None,
                    "algorithmic_flops": fl, "launch_us": t_pre * 1e6, "peak_source": peak_src + " (sustained)",
                    "share": phase_ms["prefill"] / elapsed_ms})
@@ -654,6 +689,7 @@ def measure(args, L, torch, cname, rule, NL, S, stream, world, rank, want_e2e, c
     K = args.steps
     ms = elapsed / K
     rl = rooflines(job, phase, elapsed, K)
+    mix = getattr(job, "policy_mix", None)
     rec = {
         "config": {"workload": config_name(w, rule, S, NL, args.kv8),
                    "cache": "int8 codes + fp32 scale per row" if args.kv8 else "bf16",
@@ -677,6 +713,8 @@ def measure(args, L, torch, cname, rule, NL, S, stream, world, rank, want_e2e, c
     rec["cpu_baseline"] = None
     if rank == 0 and world == 1 and cpu_seconds > 0:
         rec["cpu_baseline"] = OracleSample(w, rule, args.kv8, cpu_seconds, steps=S).record()
+    if mix:
+        rec["policies"] = {"local": mix[0], "frequency+local": mix[1], "full": mix[2]}
     return rec
 
 

@@ -28,9 +28,9 @@
  *    (H2O_F32) or bf16 (H2O_BF16) for every Q/K/V/q/k/v buffer of a handle.
  *    A grouped-query handle (h2o_init_gqa) has U = batch * kv_heads cache
  *    units and G query heads per unit: its Q, q and out have U * G rows.
- *  - Three handle kinds: H2O (h2o_init, h2o_init_gqa; h2o_* calls),
- *    HashEvict (lsh_init; lsh_* calls) and persistence of importance
- *    (sh_init; sh_* calls).  State, sync, stream and destroy calls (h2o_*)
+ *  - Four handle kinds: H2O (h2o_init, h2o_init_gqa; h2o_* calls),
+ *    HashEvict (lsh_init; lsh_* calls), persistence of importance
+ *    (sh_init; sh_* calls) and per-head policies (fg_init; fg_* calls).  State, sync, stream and destroy calls (h2o_*)
  *    take any kind; a prefill or decode call of another kind is
  *    H2O_ERR_STATE.
  *  - Pointers named "device" must point to device memory of the current
@@ -53,6 +53,16 @@
  *    h2o_last_error() then describes the failure (thread-local).
  *  - Positions are 0-based.  After a prompt of T tokens the next decoded
  *    token has position T, then T+1, ...
+ *  - Argument types chosen for the host side: the softmax scale is a
+ *    double; accumulated scores cross the boundary as fp64 (the device keeps
+ *    each as an unevaluated pair of fp32 values, about 48 significant bits);
+ *    occupancy and next position are per-unit arrays, since every unit
+ *    advances on its own once a state is loaded by hand.
+ *  - The library keeps per-device set-up (kernel attributes, device
+ *    addresses of its fixed arrays) for the life of the process, and a
+ *    handle's buffers live in the device's context: after cudaDeviceReset
+ *    on a device, no handle created before it and no call of this library
+ *    may be used on that device again in the process.
  */
 #ifndef H2O_GB300_H
 #define H2O_GB300_H
@@ -198,6 +208,59 @@ int sh_decode_step(h2o_handle h, const void* q, const void* k, const void* v,
                    float* out, int* victim_out);
 
 /*
+ * fg_init -- create a per-head policy cache handle [FG, method section:
+ * each attention head is profiled on the prompt and given its own cache
+ * policy, the first that recovers enough of its attention; Figure 2
+ * caption: the fixed "Frequency + Local" policy is the H2O cache].  Three
+ * policies, tried in this order (special-token and punctuation policies
+ * need token ids and are not offered):
+ *   0 local:              the newest `budget` tokens (H2O with heavy 0,
+ *                         recent = budget: a sliding window);
+ *   1 frequency + local:  the H2O cache (budget, heavy, recent);
+ *   2 full:               every token up to `full_budget` (H2O with heavy 0,
+ *                         recent = full_budget);
+ * and a head takes the first whose recovery -- the attention mass its kept
+ * set holds at each prompt row, averaged over the rows -- reaches tau.  The
+ * recovery test and the order are this library's reading of the page.
+ *   budget = heavy + recent as h2o_init; full_budget >= 1 (usually the
+ *   prompt plus the decode steps); 0 < tau <= 1.  H2O_KV8 is not supported.
+ *   Every unit holds max(budget, full_budget) slots; a unit of policy 0 or 1
+ *   uses `budget` of them.  State calls see that many slots per unit.
+ */
+int fg_init(h2o_handle* out, int budget, int heavy, int recent, int full_budget, double tau, int batch, int heads,
+            int head_dim, int dtype, double scale, void* cuda_stream);
+
+/*
+ * fg_prefill -- profile every head on a prompt of T >= 1 tokens and build
+ * its cache by its policy [FG method section; H2O 提案手法]:
+ *   local recovery     = (1/T) sum_i sum_{j = i-budget+1 .. i} P_ij,
+ *   frequency + local  = (1/T) sum_i sum_{j = i-recent+1 .. i, or j heavy
+ *                        and j <= i-recent} P_ij, the heavy keys being the
+ *                        H2O prompt selection's (all kept tokens when
+ *                        T <= budget),
+ * with P_ij the causal softmax of the prompt (as h2o_prefill); then the
+ * unit's cache is built by the H2O prompt rule with its policy's budget,
+ * heavy count and window.  Q, K, V: device [U][T][d].  Allocates prompt
+ * scratch (32 bytes per unit per token) when T exceeds the largest T seen.
+ */
+int fg_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T);
+
+/*
+ * fg_decode_step -- one decode step of every unit by the H2O rule
+ * (h2o_decode_step) with its own policy's budget and recent window, all
+ * units in one launch.  Arguments as h2o_decode_step.
+ */
+int fg_decode_step(h2o_handle h, const void* q, const void* k, const void* v, float* out, int* victim_out);
+
+/*
+ * fg_get_policy -- copy the last fg_prefill's choice to HOST buffers [U]
+ * (any may be NULL): policy (0 local, 1 frequency + local, 2 full) and the
+ * two recoveries.  Before any fg_prefill every unit reads policy 1 with
+ * recoveries 0.  Waits for the handle's stream.
+ */
+int fg_get_policy(h2o_handle h, int* policy, double* rec_local, double* rec_freq);
+
+/*
  * lsh_init -- create a HashEvict cache handle [HE abstract].
  *   budget = B slots, recent = r slots never evicted (0 <= r <= B);
  *   W: device fp32 [d][32], the Gaussian projection matrix, copied at init.
@@ -261,7 +324,7 @@ int h2o_get_kv_scales(h2o_handle h, float* kscale, float* vscale);
 int h2o_set_kv_scales(h2o_handle h, const float* kscale, const float* vscale);
 
 /*
- * h2o_get_prefill_stats -- copy the last h2o_prefill's prompt statistics to
+ * h2o_get_prefill_stats -- copy the last h2o_prefill's (or fg_prefill's) prompt statistics to
  * HOST buffers [U][T] (any may be NULL): m (row max of z, natural-log
  * units), l (row normaliser) and c (column sums, fp64).  Waits.  On a
  * grouped-query handle m and l are [U*G][T] (per query head) and c is
@@ -294,9 +357,10 @@ void h2o_destroy(h2o_handle h);
  * h2o_prompt_scores_noalloc -- the prompt column sums c [U][T] (fp64) that
  * h2o_prefill ranks prompt tokens by, computed without allocating device
  * memory.  The pages have no counterpart: this is a variant of the prompt
- * scorer for callers that cannot call cudaMalloc, such as code running
- * while a stream is captured into a CUDA graph, or serving runtimes that
- * reserve all device memory at start-up and forbid allocations afterwards.
+ * scorer for callers that cannot call cudaMalloc -- serving runtimes that
+ * reserve all device memory for their own pool at start-up and forbid
+ * allocations afterwards, and hosts whose allocation calls may synchronise
+ * the device in the middle of their own streams' work.
  *
  * The scorer's scratch (row max and normaliser, 8 bytes per unit per token)
  * is a fixed device array inside the library of H2O_NOALLOC_MAX_TOKENS
@@ -312,6 +376,10 @@ void h2o_destroy(h2o_handle h);
  * capture.  All calls share the one array and nothing in it carries over
  * between calls, but calls whose work overlaps on the GPU (other streams,
  * other host threads) race on it: the caller must serialise them.
+ * There is no handle and so no h2o_sync for this call: if one of the
+ * scorer's bounded waits runs out on the device (about a second), the
+ * column sums it could not finish are written as NaN instead, so a caller
+ * that checks c for NaN sees the failure.
  */
 #define H2O_NOALLOC_MAX_TOKENS (1 << 20)
 int h2o_prompt_scores_noalloc(const void* Q, const void* K, int batch, int heads, int T,

@@ -26,6 +26,7 @@
 #include <cfloat>
 #include <climits>
 #include <cstdlib>
+#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
@@ -85,7 +86,6 @@ struct Ring {
 
 template <int D, class TL>
 struct Epilogue {
-    Exchange<D> x;
     float wo[TL::NW][D];
 };
 
@@ -97,6 +97,11 @@ struct DecodeSmem {
         Ring<T, D, TL, Q8> ring;
         Epilogue<D, TL> epi;
     } u;
+    // the cluster exchange lies outside the ring, so other CTAs may write
+    // into it while this one still streams
+    Exchange<D> x;
+    // this step's q, k, v rows, fetched in one round trip after the wait
+    alignas(16) unsigned char in[3][D * sizeof(T)];
     // Q8: {K scale, V scale} of every slot of a ring stage
     alignas(16) float2 sbuf[Q8 ? TL::NW : 1][TL::NBUF][kStage];
     uint64_t bar[TL::NW][TL::NBUF];
@@ -163,6 +168,25 @@ __device__ __forceinline__ void load_q_raw(const T* q, int lane, QRaw<T, D>& raw
         raw.w[c] = *reinterpret_cast<const uint4*>(q + h * R::HALF + (c ^ (r & R::XM)) * R::VE);
 }
 
+// This step's q, k and v rows as 16-byte vectors: thread tid < 3 * NV loads
+// vector tid % NV of row tid / NV (q, k, v); the others return zeros.
+template <typename T, int D>
+__device__ __forceinline__ uint4 load_rows_16b(const T* q, const T* k, const T* v, int tid)
+{
+    constexpr int NV = D * (int)sizeof(T) / 16;
+    if (tid >= 3 * NV) return make_uint4(0u, 0u, 0u, 0u);
+    const int r = tid / NV;
+    const T* row = r == 0 ? q : r == 1 ? k : v;
+    return reinterpret_cast<const uint4*>(row)[tid - r * NV];
+}
+
+template <typename T, int D>
+__device__ __forceinline__ void store_rows_16b(unsigned char (*in)[D * sizeof(T)], uint4 w, int tid)
+{
+    constexpr int NV = D * (int)sizeof(T) / 16;
+    if (tid < 3 * NV) reinterpret_cast<uint4*>(in[tid / NV])[tid % NV] = w;
+}
+
 // Widen the raw chunks to fp32 and scale them to base-2 logits.
 template <typename T, int D>
 __device__ __forceinline__ void widen_q(const QRaw<T, D>& raw, float scale, float (&qp)[D / 2])
@@ -213,20 +237,39 @@ __device__ __forceinline__ void widen_raw(const typename RawT<E * sizeof(T)>::ty
     }
 }
 
+// Pairwise sum of the per-chunk partial sums s[0..N) over the chunk index:
+// level w adds s[c + w] into s[c] for c a multiple of 2w.  A lane that read
+// its chunks in the order c ^ m (m < N) holds, at every node of this tree,
+// the sum of the same data chunks as a lane with any other m (the XOR maps
+// aligned blocks onto aligned blocks), and fp32 addition is commutative, so
+// every lane -- every slot of a stage -- gets the same bits for the same
+// row: equal keys give equal logits wherever they sit.
+template <int N>
+__device__ __forceinline__ float chunk_tree(float (&s)[N])
+{
+    static_assert((N & (N - 1)) == 0, "power-of-two chunk count");
+#pragma unroll
+    for (int w = 1; w < N; w <<= 1) {
+#pragma unroll
+        for (int c = 0; c < N; c += 2 * w) s[c] = s[c] + s[c + w];
+    }
+    return s[0];
+}
+
 // Half-row dot product of row `row` (global or shared, elements of type T)
-// with the rotated q half; every lane returns the full dot of its
-// row after one exchange between the half-warps.  For rows of T all chunks
-// are loaded before the first multiply, and four accumulator pairs keep the
-// dependent chains short.
+// with the rotated q half; every lane returns the full dot of its row after
+// one exchange between the half-warps.  All chunks are loaded before the
+// first multiply; each chunk's products are summed in element order, and
+// the chunks by chunk_tree, so the result does not depend on the slot's
+// place in its stage.
 template <typename T, int D, typename E>
 __device__ __forceinline__ float row_dot(const E* row, const float (&qp)[D / 2], int lane)
 {
     using R = Rows<T, D>;
     const int r = lane & 15, h = lane >> 4;
     const E* half = row + h * R::HALF;
-    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                     make_float2(0.f, 0.f)};
     static_assert(sizeof(E) == sizeof(T), "rows hold the input type");
+    float part[R::HCH];
     {
         uint4 raw[R::HCH];
 #pragma unroll
@@ -236,15 +279,15 @@ __device__ __forceinline__ float row_dot(const E* row, const float (&qp)[D / 2],
         for (int c = 0; c < R::HCH; ++c) {
             float kf[R::VE];
             widen_raw<T, R::VE>(raw[c], kf);
+            float2 t = fma2(make_float2(qp[c * R::VE], qp[c * R::VE + 1]), make_float2(kf[0], kf[1]),
+                            make_float2(0.f, 0.f));
 #pragma unroll
-            for (int e = 0; e < R::VE; e += 2) {
-                const int a = (c * (R::VE / 2) + e / 2) & 3;
-                acc[a] = fma2(make_float2(qp[c * R::VE + e], qp[c * R::VE + e + 1]), make_float2(kf[e], kf[e + 1]),
-                              acc[a]);
-            }
+            for (int e = 2; e < R::VE; e += 2)
+                t = fma2(make_float2(qp[c * R::VE + e], qp[c * R::VE + e + 1]), make_float2(kf[e], kf[e + 1]), t);
+            part[c] = t.x + t.y;
         }
     }
-    const float zh = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+    const float zh = chunk_tree<R::HCH>(part);
     return zh + __shfl_xor_sync(kFull, zh, 16);
 }
 
@@ -278,29 +321,33 @@ __device__ __forceinline__ void load_q_q8(const T* q, float scale, int lane, flo
 }
 
 // Dot of an int8 row (codes, unscaled) with the lane's half of q; every
-// lane returns the full dot of its row.
+// lane returns the full dot of its row.  As row_dot: per-chunk sums in
+// element order (two fixed accumulator pairs), then chunk_tree, so equal
+// rows give equal bits in every slot.
 template <int D>
 __device__ __forceinline__ float row_dot_q8(const int8_t* row, const float (&qp)[D / 2], int lane)
 {
     constexpr int HCH = D / 32;
-    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                     make_float2(0.f, 0.f)};
     uint4 raw[HCH];
 #pragma unroll
     for (int c = 0; c < HCH; ++c) raw[c] = *reinterpret_cast<const uint4*>(row + q8_chunk<D>(lane, c) * 16);
+    float part[HCH];
 #pragma unroll
     for (int c = 0; c < HCH; ++c) {
         const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+        float2 t0 = make_float2(0.f, 0.f), t1 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             float f[4];
             q8_unpack4(u[i], f);
             const int e = c * 16 + 4 * i;
-            acc[(2 * i) & 3] = fma2(make_float2(qp[e], qp[e + 1]), make_float2(f[0], f[1]), acc[(2 * i) & 3]);
-            acc[(2 * i + 1) & 3] = fma2(make_float2(qp[e + 2], qp[e + 3]), make_float2(f[2], f[3]), acc[(2 * i + 1) & 3]);
+            float2& t = i < 2 ? t0 : t1;
+            t = fma2(make_float2(qp[e], qp[e + 1]), make_float2(f[0], f[1]), t);
+            t = fma2(make_float2(qp[e + 2], qp[e + 3]), make_float2(f[2], f[3]), t);
         }
+        part[c] = (t0.x + t0.y) + (t1.x + t1.y);
     }
-    const float zh = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
+    const float zh = chunk_tree<HCH>(part);
     return zh + __shfl_xor_sync(kFull, zh, 16);
 }
 
@@ -616,21 +663,43 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     CE* Kc = reinterpret_cast<CE*>(c.K) + ub * D;
     CE* Vc = reinterpret_cast<CE*>(c.V) + ub * D;
     float2* Sc = Q8 ? c.kvs + (size_t)unit * c.Bp : nullptr;   // slot scale pairs
+    // this unit's budget and recent window: the cache's own, or the unit's
+    // policy (per-head policies; then the unit uses Bu of its B slots)
+    int Bu = B, ru = c.r;
     int f0, f1, s0, s1;                      // fetched slots; slots whose scores this CTA updates
-    if constexpr (GQ) {
-        f0 = 0;
-        f1 = B;
-        fetch_range(B, C, rank, s0, s1);
-    } else {
-        fetch_range(B, C, rank, f0, f1);
-        s0 = f0;
-        s1 = f1;
-    }
+    auto unit_ranges = [&]() {
+        if (c.upol) {
+            const int4 pp = c.upol[unit];
+            Bu = pp.x;
+            ru = pp.z;
+        }
+        if constexpr (GQ) {
+            f0 = 0;
+            f1 = Bu;
+            fetch_range(Bu, C, rank, s0, s1);
+        } else {
+            fetch_range(Bu, C, rank, f0, f1);
+            s0 = f0;
+            s1 = f1;
+        }
+    };
+    // the policy is written by this handle's prompt phase only, so it is
+    // read before the dependency wait under the same rule as the cache
+    if (a.early || !c.upol) unit_ranges();
     if (lane == 0) {
 #pragma unroll
         for (int b = 0; b < TL::NBUF; ++b) mbar_init(&S.bar[warp][b], 1);
         if (C > 1) fence_mbar_init(); else fence_proxy_async_smem();
     }
+    // paired with the wait before the first exchange: by then every CTA of
+    // the cluster runs, so its shared memory may be written
+    if (C > 1) cluster_arrive_relaxed();
+    const T* qg = reinterpret_cast<const T*>(a.q) + qrow * D;
+    const T* kg = reinterpret_cast<const T*>(a.k) + (size_t)unit * D;
+    const T* vg = reinterpret_cast<const T*>(a.v) + (size_t)unit * D;
+    // the input rows are read only after the wait, but their lines can be
+    // on their way to L2 meanwhile, ahead of the cache traffic below
+    prefetch_rows_l2(qg, kg, vg, D * (int)sizeof(T), tid);
     // This unit's cache: the ring's first stages (the attention starts on
     // them, so their bulk copies go out first), the occupancy, and the scores
     // and positions of this thread's fetched slots (consumed after the merge).
@@ -660,33 +729,39 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
         if (lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, 0, 1);
         read_cache();
     }
-    // the input rows are read only after the wait, but their lines can be
-    // on their way to L2 meanwhile
-    prefetch_rows_l2(reinterpret_cast<const T*>(a.q) + qrow * D, reinterpret_cast<const T*>(a.k) + (size_t)unit * D,
-                     reinterpret_cast<const T*>(a.v) + (size_t)unit * D, D * (int)sizeof(T), tid);
     // everything below may read memory the previous kernel in the stream
     // has written (the inputs, and the cache unless read above)
     grid_dependency_wait();
     grid_launch_dependents();
     if (!a.early) {
+        if (c.upol) unit_ranges();
         if (lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1);
         read_cache();
     }
+    // q, k, v in one round trip (requested before the rest of the ring)
+    {
+        const uint4 w = load_rows_16b<T, D>(qg, kg, vg, tid);
+        if (a.early && lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, 1, TL::NBUF);
+        store_rows_16b<T, D>(S.in, w, tid);
+    }
+    __syncthreads();
+    const T* qs = reinterpret_cast<const T*>(S.in[0]);
+    const T* ks = reinterpret_cast<const T*>(S.in[1]);
+    const T* vs = reinterpret_cast<const T*>(S.in[2]);
     float qp[D / 2];
-    QRaw<T, D> qraw;
-    if constexpr (Q8) load_q_q8<T, D>(reinterpret_cast<const T*>(a.q) + qrow * D, c.qscale, lane, qp);
-    else load_q_raw<T, D>(reinterpret_cast<const T*>(a.q) + qrow * D, lane, qraw);
-    if (a.early && lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, 1, TL::NBUF);
-    const T* kg = reinterpret_cast<const T*>(a.k) + (size_t)unit * D;
-    const T* vg = reinterpret_cast<const T*>(a.v) + (size_t)unit * D;
+    if constexpr (Q8) {
+        load_q_q8<T, D>(qs, c.qscale, lane, qp);
+    } else {
+        QRaw<T, D> qraw;
+        load_q_raw<T, D>(qs, lane, qraw);
+        widen_q<T, D>(qraw, c.qscale, qp);
+    }
     // the new token's row, written into the victim slot at the end
     uint4 newrow = make_uint4(0u, 0u, 0u, 0u);
-    if (rank == 0 && tid < 2 * NV)
-        newrow = tid < NV ? reinterpret_cast<const uint4*>(kg)[tid] : reinterpret_cast<const uint4*>(vg)[tid - NV];
-    if constexpr (!Q8) widen_q<T, D>(qraw, c.qscale, qp);
+    if (rank == 0 && tid < 2 * NV) newrow = reinterpret_cast<const uint4*>(S.in[1])[tid];
 
     const int n = us.x, p = us.y;
-    const bool full = (n >= B);
+    const bool full = (n >= Bu);
     const int c0 = f0, c1 = min(n, f1);     // live slots of this CTA
 
     float m_run = -INFINITY, l_run = 0.f, o[EPL];
@@ -695,9 +770,9 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     if ((GQ || rank == 0) && warp == 0) {  // the new token attends to itself
         float vr[EPL];
         float zn;
-        if constexpr (Q8) zn = row_dot_q8order<T, D>(kg, qp, lane);
-        else zn = row_dot<T, D, T>(kg, qp, lane);
-        load_vec<T, EPL>(vg + lane * EPL, vr);
+        if constexpr (Q8) zn = row_dot_q8order<T, D>(ks, qp, lane);
+        else zn = row_dot<T, D, T>(ks, qp, lane);
+        load_vec<T, EPL>(vs + lane * EPL, vr);
         m_run = zn;
         l_run = lane == 0 ? 1.f : 0.f;
 #pragma unroll
@@ -710,18 +785,19 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
 
     float Mc, Lc, Oc;
     merge_warps<T, D, TL, Q8>(S, m_run, l_run, o, Mc, Lc, Oc);
-    const uint32_t x0 = map_to_rank(&S.u.epi.x, 0);
+    if (C > 1) cluster_wait();               // every CTA of the cluster runs (arrive at the start)
+    const uint32_t x0 = map_to_rank(&S.x, 0);
 
     // Write the new token into the victim slot (slot n while the cache is
     // not full) with score `snew`.  `write_row` runs in the threads holding
     // `newrow`.
     auto finish = [&](int victim, float2 snew) {
-        if (victim < 0 || victim >= B) victim = 0;   // n == 0 with B == 0 cannot happen
+        if (victim < 0 || victim >= Bu) victim = 0;   // n == 0 with Bu == 0 cannot happen
         if (tid == 0) {
             if constexpr (SH) c.code[ub + victim] = S.P_new * (float)(n + 1) > 1.f ? 1u : 0u;
             else c.score[ub + victim] = snew;
             c.pos[ub + victim] = p;
-            c.ustate[unit] = make_int2(min(n + 1, B), p + 1);
+            c.ustate[unit] = make_int2(min(n + 1, Bu), p + 1);
             if (a.victim_out) a.victim_out[unit] = full ? victim : -1;
         }
         if constexpr (Q8) {
@@ -755,7 +831,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
                 c.score[ub + s] = ns;
                 if (full) {
                     const ArgMin k = ArgMin{ord_key(ns.x), ord_key(ns.y), (unsigned)s};
-                    if (ps[i] <= p - c.r) argmin_take(best, k);
+                    if (ps[i] <= p - ru) argmin_take(best, k);
                     argmin_take(best_all, k);
                 }
             }
@@ -795,8 +871,8 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
             if (full) {
                 ArgMin vc = argmin_none(), va = argmin_none();
                 for (int j = 0; j < C; ++j) {
-                    argmin_take(vc, ArgMin{S.u.epi.x.am[0][0][j], S.u.epi.x.am[0][1][j], S.u.epi.x.am[0][2][j]});
-                    argmin_take(va, ArgMin{S.u.epi.x.am[1][0][j], S.u.epi.x.am[1][1][j], S.u.epi.x.am[1][2][j]});
+                    argmin_take(vc, ArgMin{S.x.am[0][0][j], S.x.am[0][1][j], S.x.am[0][2][j]});
+                    argmin_take(va, ArgMin{S.x.am[1][0][j], S.x.am[1][1][j], S.x.am[1][2][j]});
                 }
                 victim = (int)(vc.slot != 0xffffffffu ? vc.slot : va.slot);
             }
@@ -805,7 +881,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
         __syncthreads();
         float2 snew = make_float2(0.f, 0.f);
         if (tid == 0)
-            for (int j = 0; j < C; ++j) snew = pair_add(snew, S.u.epi.x.m[j]);
+            for (int j = 0; j < C; ++j) snew = pair_add(snew, S.x.m[j]);
         finish(S.victim, snew);
         return;
     }
@@ -814,27 +890,22 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     // single-CTA unit already has them
     float M, invL;
     if (C > 1) {
-        cluster_arrive();                    // every CTA of the cluster is past its ring
-        cluster_wait();
+        // every CTA's (max, normaliser) into every CTA, its output into rank 0
         const uint32_t off_m = (uint32_t)offsetof(Exchange<D>, m), off_l = (uint32_t)offsetof(Exchange<D>, l);
         const uint32_t off_o = (uint32_t)offsetof(Exchange<D>, o);
         if (tid < D) st_cluster_f32(x0 + off_o + (uint32_t)((rank * D + tid) * 4), Oc);
-        if (tid == 0) {
-            st_cluster_f32(x0 + off_m + rank * 4, Mc);
-            st_cluster_f32(x0 + off_l + rank * 4, Lc);
+        if (tid < C) {
+            const uint32_t xt = map_to_rank(&S.x, (uint32_t)tid);
+            st_cluster_f32(xt + off_m + rank * 4, Mc);
+            st_cluster_f32(xt + off_l + rank * 4, Lc);
         }
         cluster_arrive();
         cluster_wait();
-        if (warp == 0) {
-            const float mj = lane < C ? ld_cluster_f32(x0 + off_m + lane * 4) : -INFINITY;
-            const float lj = lane < C ? ld_cluster_f32(x0 + off_l + lane * 4) : 0.f;
-            const float Mx = warp_max(mj);
-            const float Lx = warp_sum(lane < C ? lj * safe_exp2_diff(mj, Mx) : 0.f);
-            if (lane == 0) { S.M = Mx; S.invL = 1.f / Lx; }
-        }
-        __syncthreads();
-        M = S.M;
-        invL = S.invL;
+        float Mx = -INFINITY, Lx = 0.f;
+        for (int j = 0; j < C; ++j) Mx = fmaxf(Mx, S.x.m[j]);
+        for (int j = 0; j < C; ++j) Lx += S.x.l[j] * safe_exp2_diff(S.x.m[j], Mx);
+        M = Mx;
+        invL = 1.f / Lx;
     } else {
         M = Mc;
         invL = 1.f / Lc;
@@ -859,7 +930,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
                 k = ArgMin{ord_key(ns.x), ord_key(ns.y), (unsigned)s};
             }
             if (full) {
-                if (ps[i] <= p - c.r) argmin_take(best, k);
+                if (ps[i] <= p - ru) argmin_take(best, k);
                 if (C > 1) argmin_take(best_all, k);
             }
         }
@@ -876,7 +947,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
         float acc = Oc;
         if (C > 1) {
             acc = 0.f;
-            for (int j = 0; j < C; ++j) acc += S.u.epi.x.o[j][tid] * safe_exp2_diff(S.u.epi.x.m[j], M);
+            for (int j = 0; j < C; ++j) acc += S.x.o[j][tid] * safe_exp2_diff(S.x.m[j], M);
         }
         a.out[qrow * D + tid] = acc * invL;
     }
@@ -939,8 +1010,8 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
         if (full) {
             ArgMin vc = argmin_none(), va = argmin_none();
             for (int j = 0; j < C; ++j) {
-                argmin_take(vc, ArgMin{S.u.epi.x.am[0][0][j], S.u.epi.x.am[0][1][j], S.u.epi.x.am[0][2][j]});
-                argmin_take(va, ArgMin{S.u.epi.x.am[1][0][j], S.u.epi.x.am[1][1][j], S.u.epi.x.am[1][2][j]});
+                argmin_take(vc, ArgMin{S.x.am[0][0][j], S.x.am[0][1][j], S.x.am[0][2][j]});
+                argmin_take(va, ArgMin{S.x.am[1][0][j], S.x.am[1][1][j], S.x.am[1][2][j]});
             }
             victim = (int)(vc.slot != 0xffffffffu ? vc.slot : va.slot);
         }
@@ -978,6 +1049,13 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
         for (int b = 0; b < TL::NBUF; ++b) mbar_init(&S.bar[warp][b], 1);
         if (C > 1) fence_mbar_init(); else fence_proxy_async_smem();
     }
+    if (C > 1) cluster_arrive_relaxed();     // paired with the wait before the exchange
+    const T* qg = reinterpret_cast<const T*>(a.q) + (size_t)unit * D;
+    const T* kg = reinterpret_cast<const T*>(a.k) + (size_t)unit * D;
+    const T* vg = reinterpret_cast<const T*>(a.v) + (size_t)unit * D;
+    // the input rows are read only after the wait, but their lines can be
+    // on their way to L2 meanwhile, ahead of the cache traffic below
+    prefetch_rows_l2(qg, kg, vg, D * (int)sizeof(T), tid);
     // The projection matrix is written once when the cache is created, never
     // by a previous kernel in the stream, so it is read before the wait:
     // warp w holds rows [w*RPW, w*RPW + RPW) of W, lane j the column of bit j.
@@ -1017,37 +1095,33 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
         read_state();
         if (lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, 0, 1);
     }
-    // the input rows are read only after the wait, but their lines can be
-    // on their way to L2 meanwhile
-    prefetch_rows_l2(reinterpret_cast<const T*>(a.q) + (size_t)unit * D, reinterpret_cast<const T*>(a.k) + (size_t)unit * D,
-                     reinterpret_cast<const T*>(a.v) + (size_t)unit * D, D * (int)sizeof(T), tid);
     // everything below may read memory the previous kernel in the stream
     // has written (the inputs, and the cache unless read above)
     grid_dependency_wait();
     grid_launch_dependents();
     // the victim (which gates the attention) depends only on small loads:
-    // they go out before the bulk copies, which would otherwise delay them
-    const T* qg = reinterpret_cast<const T*>(a.q) + (size_t)unit * D;
-    const T* kg = reinterpret_cast<const T*>(a.k) + (size_t)unit * D;
-    const T* vg = reinterpret_cast<const T*>(a.v) + (size_t)unit * D;
-    uint4 newrow = make_uint4(0u, 0u, 0u, 0u);
-    if (rank == 0 && tid < 2 * NV)
-        newrow = tid < NV ? reinterpret_cast<const uint4*>(kg)[tid] : reinterpret_cast<const uint4*>(vg)[tid - NV];
-    if (!a.early) read_state();
-    QRaw<T, D> qraw;
-    load_q_raw<T, D>(qg, lane, qraw);
-    T xq = T(), xk = T();
-    if (tid < D) {
-        xq = qg[tid];
-        xk = kg[tid];
+    // q, k, v in one round trip, before the bulk copies, which would
+    // otherwise delay them
+    {
+        const uint4 w = load_rows_16b<T, D>(qg, kg, vg, tid);
+        if (!a.early) read_state();
+        if (lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, a.early ? 1 : 0, TL::NBUF);
+        store_rows_16b<T, D>(S.in, w, tid);
     }
-    if (lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, a.early ? 1 : 0, TL::NBUF);
+    __syncthreads();
+    const T* qs = reinterpret_cast<const T*>(S.in[0]);
+    const T* ks = reinterpret_cast<const T*>(S.in[1]);
+    const T* vs = reinterpret_cast<const T*>(S.in[2]);
+    uint4 newrow = make_uint4(0u, 0u, 0u, 0u);
+    if (rank == 0 && tid < 2 * NV) newrow = reinterpret_cast<const uint4*>(S.in[1])[tid];
+    QRaw<T, D> qraw;
+    load_q_raw<T, D>(qs, lane, qraw);
     const int n = us.x, p = us.y;
     const bool full = (n >= B);
 
     if (tid < D) {
-        S.qf[tid] = Elem<T>::to_f(xq);
-        S.kf[tid] = Elem<T>::to_f(xk);
+        S.qf[tid] = Elem<T>::to_f(qs[tid]);
+        S.kf[tid] = Elem<T>::to_f(ks[tid]);
     }
     __syncthreads();
     // sign codes: bit j is the sign of an fp32 fused multiply-add chain over
@@ -1125,7 +1199,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
     __syncthreads();
     const int victim = S.victim;
     float qp[D / 2];
-    if constexpr (Q8) load_q_q8<T, D>(qg, c.qscale, lane, qp);
+    if constexpr (Q8) load_q_q8<T, D>(qs, c.qscale, lane, qp);
     else widen_q<T, D>(qraw, c.qscale, qp);
 
     float m_run = -INFINITY, l_run = 0.f, o[EPL];
@@ -1133,10 +1207,10 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
     for (int e = 0; e < EPL; ++e) o[e] = 0.f;
     if (rank == 0 && warp == 0) {          // the new token, now in the victim slot
         float zn;
-        if constexpr (Q8) zn = row_dot_q8order<T, D>(kg, qp, lane);
-        else zn = row_dot<T, D, T>(kg, qp, lane);
+        if constexpr (Q8) zn = row_dot_q8order<T, D>(ks, qp, lane);
+        else zn = row_dot<T, D, T>(ks, qp, lane);
         float vr[EPL];
-        load_vec<T, EPL>(vg + lane * EPL, vr);
+        load_vec<T, EPL>(vs + lane * EPL, vr);
         m_run = zn;
         l_run = lane == 0 ? 1.f : 0.f;
 #pragma unroll
@@ -1151,9 +1225,8 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
     merge_warps<T, D, TL, Q8>(S, m_run, l_run, o, Mc, Lc, Oc);
 
     if (C > 1) {
-        cluster_arrive();                    // every CTA of the cluster is past its ring
-        cluster_wait();
-        const uint32_t x0 = map_to_rank(&S.u.epi.x, 0);
+        cluster_wait();                      // every CTA of the cluster runs (arrive at the start)
+        const uint32_t x0 = map_to_rank(&S.x, 0);
         const uint32_t off_m = (uint32_t)offsetof(Exchange<D>, m), off_l = (uint32_t)offsetof(Exchange<D>, l);
         const uint32_t off_o = (uint32_t)offsetof(Exchange<D>, o);
         if (tid < D) st_cluster_f32(x0 + off_o + (uint32_t)((rank * D + tid) * 4), Oc);
@@ -1166,12 +1239,12 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
         if (rank != 0) return;
         if (tid < D) {
             float Mx = -INFINITY;
-            for (int j = 0; j < C; ++j) Mx = fmaxf(Mx, S.u.epi.x.m[j]);
+            for (int j = 0; j < C; ++j) Mx = fmaxf(Mx, S.x.m[j]);
             float L = 0.f, acc = 0.f;
             for (int j = 0; j < C; ++j) {
-                const float f = safe_exp2_diff(S.u.epi.x.m[j], Mx);
-                L += S.u.epi.x.l[j] * f;
-                acc += S.u.epi.x.o[j][tid] * f;
+                const float f = safe_exp2_diff(S.x.m[j], Mx);
+                L += S.x.l[j] * f;
+                acc += S.x.o[j][tid] * f;
             }
             a.out[(size_t)unit * D + tid] = acc / L;
         }
@@ -1197,6 +1270,20 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
 // ------------------------------------------------------------- launching
 
 using TileDefault = Tile<6, 2>;
+// bf16 rows of 128: fewer units than SMs (one CTA per SM, often a cluster
+// per unit) stream with 8 warps; very many units with 4 warps x 3 stages
+using TileFew = Tile<8, 2>;
+using TileMany = Tile<4, 3>;
+
+// Tile for bf16 rows of 128 (numbers as H2O_DECODE_TILE): TileFew when the
+// units do not fill the SMs, TileMany from four units per SM on, else the
+// default.
+int auto_tile(int U, int num_sms)
+{
+    if (num_sms > 0 && U < num_sms) return 6;
+    if (num_sms > 0 && U >= 4 * num_sms) return 3;
+    return 2;
+}
 
 // Programmatic dependent launch is on unless H2O_PDL=0 (for comparisons).
 bool pdl_enabled()
@@ -1299,13 +1386,11 @@ cudaError_t dispatch(const DecodeArgs& a, int split, cudaStream_t st)
         return cudaErrorInvalidValue;
     }
     if (a.c.D == 128 && bf) {
-        switch (tile_variant()) {
+        switch (tile_variant() ? tile_variant() : auto_tile(a.c.U, a.num_sms)) {
         case 1: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<4, 2>>(a, split, st);
-        case 2: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<6, 2>>(a, split, st);
-        case 3: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<4, 3>>(a, split, st);
-        case 4: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<12, 1>>(a, split, st);
-        case 5: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<13, 1>>(a, split, st);
-        case 6: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<8, 2>>(a, split, st);
+        case 3: return launch_decode_t<__nv_bfloat16, 128, LSH, TileMany>(a, split, st);
+        case 6: return launch_decode_t<__nv_bfloat16, 128, LSH, TileFew>(a, split, st);
+        case 9: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<8, 3>>(a, split, st);
         default: return launch_decode_t<__nv_bfloat16, 128, LSH, TileDefault>(a, split, st);
         }
     }
@@ -1340,6 +1425,71 @@ cudaError_t launch_wait_selftest(int* err, cudaStream_t st)
 }
 
 int max_decode_split() { return kMaxSplit; }
+
+namespace {
+
+// Largest number of clusters of `split` CTAs of the TileFew H2O or HashEvict
+// kernel (bf16, head_dim 128) that the device runs at once; 0 on error.
+int clusters_that_fit(int split, bool lsh)
+{
+    using TL = TileFew;
+    void (*kern)(const DecodeArgs);
+    if (lsh) kern = lsh_decode_kernel<__nv_bfloat16, 128, TL, false>;
+    else kern = h2o_decode_kernel<__nv_bfloat16, 128, TL, false, false>;
+    const size_t smem = sizeof(DecodeSmem<__nv_bfloat16, 128, TL, false>);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)split, 1, 1);
+    cfg.blockDim = dim3(TL::NT, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void*)kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+}  // namespace
+
+// Decode split for a bf16, head_dim 128 one-head H2O or HashEvict cache with
+// fewer units than SMs (the TileFew kernel, one CTA per SM): the most CTAs
+// per unit with all U clusters resident at once (clusters are placed within
+// a GPC, so U * split <= num_sms alone does not ensure it), at least one
+// CTA per 1024 slots.  Results are cached per (device, U, B, kernel).
+int few_units_split(int U, int B, int num_sms, bool lsh)
+{
+    struct Entry { int dev, U, B, lsh, split; };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int n_cache = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < n_cache; ++i)
+            if (cache[i].dev == dev && cache[i].U == U && cache[i].B == B && cache[i].lsh == (int)lsh)
+                return cache[i].split;
+    }
+    const int lo = max(1, (B + kMaxChunk - 1) / kMaxChunk);
+    const int hi = max(1, (B + 63) / 64);
+    int s = min(kMaxSplit, min(hi, max(lo, num_sms / max(U, 1))));
+    while (s > lo && clusters_that_fit(s, lsh) < U) --s;
+    std::lock_guard<std::mutex> lock(mu);
+    if (n_cache < 64) cache[n_cache++] = Entry{dev, U, B, (int)lsh, s};
+    return s;
+}
 
 // One CTA per unit whenever the units alone cover the SMs: the cluster
 // exchange costs more than it saves.  Otherwise enough CTAs per unit to give

@@ -52,9 +52,12 @@ bool inject(const char* what)
     return f && strcmp(f, what) == 0;
 }
 
-enum Kind { kH2O = 0, kLSH = 1, kSH = 2 };
+enum Kind { kH2O = 0, kLSH = 1, kSH = 2, kFG = 3 };
 
-const char* kind_name(int k) { return k == kH2O ? "H2O" : k == kLSH ? "LSH" : "persistence-of-importance"; }
+const char* kind_name(int k)
+{
+    return k == kH2O ? "H2O" : k == kLSH ? "LSH" : k == kSH ? "persistence-of-importance" : "per-head policy";
+}
 
 // The handle whose cache the library last wrote on each (device, stream).
 // A decode kernel may read its own cache before its programmatic-launch
@@ -133,6 +136,13 @@ struct h2o_ctx {
     uint32_t* ck;
     int last_T;
     int ready;                 // 1 once a prompt or a state was loaded
+    // per-head policies (kind kFG): B above is the slot stride max(B_sel, B_full)
+    int B_sel, B_full;         // frequency + local budget; full-cache budget
+    double tau;
+    int4* upol;                // [U] {budget, heavy, recent, policy}
+    double2* rec;              // [U] {local, frequency + local} recoveries
+    double* bandB;             // prompt scratch [U][T]: band sums of width B_sel and r
+    double* bandr;
 };
 
 namespace {
@@ -156,7 +166,9 @@ int dev_alloc(void** p, size_t bytes, const char* what)
 void free_prompt(h2o_ctx* h)
 {
     cudaFree(h->m2); cudaFree(h->l); cudaFree(h->c); cudaFree(h->ckv); cudaFree(h->cq); cudaFree(h->ck);
+    cudaFree(h->bandB); cudaFree(h->bandr);
     h->m2 = nullptr; h->l = nullptr; h->c = nullptr; h->ckv = nullptr; h->cq = nullptr; h->ck = nullptr;
+    h->bandB = nullptr; h->bandr = nullptr;
     h->T_cap = 0;
 }
 
@@ -164,12 +176,22 @@ void free_all(h2o_ctx* h)
 {
     free_prompt(h);
     cudaFree(h->K); cudaFree(h->V); cudaFree(h->score); cudaFree(h->pos); cudaFree(h->code);
-    cudaFree(h->ustate); cudaFree(h->err); cudaFree(h->W); cudaFree(h->kvs);
+    cudaFree(h->ustate); cudaFree(h->err); cudaFree(h->W); cudaFree(h->kvs); cudaFree(h->upol); cudaFree(h->rec);
     free(h->W_host);
     h->W_host = nullptr;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// the per-unit policy arrays of a per-head policy handle
+int rc0_alloc(h2o_ctx* h, size_t U)
+{
+    int rc;
+    if ((rc = dev_alloc((void**)&h->upol, U * sizeof(int4), "unit policies")) ||
+        (rc = dev_alloc((void**)&h->rec, U * sizeof(double2), "policy recoveries")))
+        return rc;
+    return H2O_OK;
+}
 
 CacheView view(const h2o_ctx* h)
 {
@@ -178,12 +200,14 @@ CacheView view(const h2o_ctx* h)
     v.kvs = h->kvs; v.kv8 = h->kv8; v.Bp = h->Bp;
     v.ustate = h->ustate; v.err = h->err;
     v.U = h->U; v.B = h->B; v.D = h->D; v.dtype = h->dtype; v.r = h->r;
+    v.upol = h->upol;
     v.qscale = (float)(h->scale * 1.4426950408889634);
     return v;
 }
 
 int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int batch, int heads,
-           int head_dim, int dtype, double scale, const float* W, void* stream, int groups = 1)
+           int head_dim, int dtype, double scale, const float* W, void* stream, int groups = 1,
+           int full_budget = 0, double tau = 0.0)
 {
     if (!out) return fail(H2O_ERR_ARG, "out handle pointer is NULL");
     *out = nullptr;
@@ -193,7 +217,7 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
         return fail(H2O_ERR_ARG, "a grouped-query cache holds at most 1024 slots (got %d)", budget);
     if (budget < 1) return fail(H2O_ERR_ARG, "budget must be >= 1 (got %d)", budget);
     if (recent < 0 || recent > budget) return fail(H2O_ERR_ARG, "recent must be in [0, budget] (got %d)", recent);
-    if ((kind == kH2O || kind == kSH) && (heavy < 0 || heavy + recent != budget))
+    if ((kind == kH2O || kind == kSH || kind == kFG) && (heavy < 0 || heavy + recent != budget))
         return fail(H2O_ERR_ARG, "heavy + recent must equal budget (%d + %d != %d)", heavy, recent, budget);
     if (batch < 1 || heads < 1) return fail(H2O_ERR_ARG, "batch and heads must be >= 1");
     if ((long long)batch * heads * groups > (1LL << 24)) return fail(H2O_ERR_ARG, "batch * heads too large");
@@ -202,6 +226,10 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
         return fail(H2O_ERR_ARG, "dtype must be H2O_F32 or H2O_BF16, optionally | H2O_KV8");
     const int kv8 = (dtype & H2O_KV8) ? 1 : 0;
     if (kind == kSH && kv8) return fail(H2O_ERR_UNSUPPORTED, "H2O_KV8 is not supported on persistence-of-importance handles");
+    if (kind == kFG && kv8) return fail(H2O_ERR_UNSUPPORTED, "H2O_KV8 is not supported on per-head policy handles");
+    if (kind == kFG && (full_budget < 1 || full_budget >= (1 << 20)))
+        return fail(H2O_ERR_ARG, "full_budget must be in [1, 2^20) (got %d)", full_budget);
+    if (kind == kFG && !(tau > 0.0 && tau <= 1.0)) return fail(H2O_ERR_ARG, "tau must be in (0, 1]");
     dtype &= H2O_BF16;
     if (!(scale > 0.0) || !std::isfinite(scale)) return fail(H2O_ERR_ARG, "scale must be finite and > 0");
     if ((long long)budget >= (1LL << 20)) return fail(H2O_ERR_ARG, "budget must be below 2^20");
@@ -216,6 +244,12 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
     h->kind = kind; h->B = budget; h->H = heavy; h->r = recent; h->batch = batch; h->heads = heads;
     h->D = head_dim; h->dtype = dtype; h->U = batch * heads; h->G = groups; h->scale = scale;
     h->kv8 = kv8; h->Bp = (budget + 1) & ~1;
+    if (kind == kFG) {
+        h->B_sel = budget;
+        h->B_full = full_budget;
+        h->tau = tau;
+        h->B = budget > full_budget ? budget : full_budget;   // slot stride
+    }
     h->stream = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaGetDevice(&h->device);
     if (e != cudaSuccess) { delete h; cudaGetLastError(); return cuda_fail(e, "cudaGetDevice"); }
@@ -226,6 +260,7 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
     if (major < 10) { delete h; return fail(H2O_ERR_UNSUPPORTED, "device compute capability %d.x is not sm_103", major); }
 
     const size_t U = (size_t)h->U, B = (size_t)h->B, row = (size_t)h->D * (kv8 ? 1 : elem_size(dtype));
+    if (kind == kFG && ((rc0_alloc(h, U) != H2O_OK))) { free_all(h); delete h; return H2O_ERR_ALLOC; }
     int rc = H2O_OK;
     if ((rc = dev_alloc(&h->K, U * B * row, "cache K")) ||
         (rc = dev_alloc(&h->V, U * B * row, "cache V")) ||
@@ -237,7 +272,7 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
     if (kv8 && (rc = dev_alloc((void**)&h->kvs, U * (size_t)h->Bp * sizeof(float2), "slot scales"))) {
         free_all(h); delete h; return rc;
     }
-    if (kind == kH2O) {
+    if (kind == kH2O || kind == kFG) {
         if ((rc = dev_alloc((void**)&h->score, U * B * sizeof(float2), "scores"))) { free_all(h); delete h; return rc; }
     } else if (kind == kSH) {
         if ((rc = dev_alloc((void**)&h->code, U * B * sizeof(uint32_t), "pivotal histories"))) { free_all(h); delete h; return rc; }
@@ -258,6 +293,15 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
     if (e == cudaSuccess) e = cudaMemsetAsync(h->ustate, 0, U * sizeof(int2), h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->pos, 0xff, U * B * sizeof(int), h->stream);
     if (e == cudaSuccess && kv8) e = cudaMemsetAsync(h->kvs, 0, U * (size_t)h->Bp * sizeof(float2), h->stream);
+    if (e == cudaSuccess && kind == kFG) {
+        int4* init = static_cast<int4*>(malloc(U * sizeof(int4)));
+        if (!init) { free_all(h); delete h; return fail(H2O_ERR_ALLOC, "host allocation failed"); }
+        for (size_t u = 0; u < U; ++u) init[u] = make_int4(budget, heavy, recent, 1);
+        e = cudaMemcpyAsync(h->upol, init, U * sizeof(int4), cudaMemcpyHostToDevice, h->stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(h->rec, 0, U * sizeof(double2), h->stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+        free(init);
+    }
     if (e != cudaSuccess) { free_all(h); delete h; return cuda_fail(e, "initialise state"); }
     note_cache_write(h->device, h->stream, h);
     *out = h;
@@ -273,7 +317,15 @@ int ensure_prompt_scratch(h2o_ctx* h, int T)
     free_prompt(h);
     const size_t n = (size_t)h->U * (size_t)T, nq = n * (size_t)h->G;
     int rc;
-    if (h->kind == kH2O) {
+    if (h->kind == kFG) {
+        if ((rc = dev_alloc((void**)&h->m2, n * sizeof(float), "row max")) ||
+            (rc = dev_alloc((void**)&h->l, n * sizeof(float), "row normaliser")) ||
+            (rc = dev_alloc((void**)&h->c, n * sizeof(double), "column sums")) ||
+            (rc = dev_alloc((void**)&h->bandB, n * sizeof(double), "band sums (budget)")) ||
+            (rc = dev_alloc((void**)&h->bandr, n * sizeof(double), "band sums (window)"))) {
+            free_prompt(h); return rc;
+        }
+    } else if (h->kind == kH2O) {
         if ((rc = dev_alloc((void**)&h->m2, nq * sizeof(float), "row max")) ||
             (rc = dev_alloc((void**)&h->l, nq * sizeof(float), "row normaliser")) ||
             (rc = dev_alloc((void**)&h->c, nq * sizeof(double), "column sums"))) {
@@ -304,12 +356,13 @@ int check_prompt(h2o_ctx* h, int kind, const void* Q, const void* K, const void*
     if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
     if (h->kind != kind)
         return fail(H2O_ERR_STATE, "%s called on a %s handle",
-                    kind == kH2O ? "h2o_prefill" : kind == kLSH ? "lsh_prefill" : "sh_prefill", kind_name(h->kind));
+                    kind == kH2O ? "h2o_prefill" : kind == kLSH ? "lsh_prefill" : kind == kSH ? "sh_prefill" : "fg_prefill",
+                    kind_name(h->kind));
     if (!Q || !K || !V) return fail(H2O_ERR_ARG, "Q, K and V must be non-NULL");
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V)) return fail(H2O_ERR_ARG, "Q, K, V must be 16-byte aligned");
     if (T < 1) return fail(H2O_ERR_ARG, "prompt length must be >= 1 (got %d)", T);
     if ((long long)T * h->U * h->G > (1LL << 31) / 4) return fail(H2O_ERR_ARG, "prompt too long for this batch");
-    if ((kind == kH2O || kind == kSH) && T >= (1 << 24)) return fail(H2O_ERR_ARG, "prompt too long");
+    if ((kind == kH2O || kind == kSH || kind == kFG) && T >= (1 << 24)) return fail(H2O_ERR_ARG, "prompt too long");
     return H2O_OK;
 }
 
@@ -318,7 +371,8 @@ int check_step(h2o_ctx* h, int kind, const void* q, const void* k, const void* v
     if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
     if (h->kind != kind)
         return fail(H2O_ERR_STATE, "%s called on a %s handle",
-                    kind == kH2O ? "h2o_decode_step" : kind == kLSH ? "lsh_decode_step" : "sh_decode_step",
+                    kind == kH2O ? "h2o_decode_step" : kind == kLSH ? "lsh_decode_step"
+                                     : kind == kSH ? "sh_decode_step" : "fg_decode_step",
                     kind_name(h->kind));
     if (!h->ready) return fail(H2O_ERR_STATE, "decode before prefill");
     if (!q || !k || !v || !out) return fail(H2O_ERR_ARG, "q, k, v and out must be non-NULL");
@@ -329,7 +383,14 @@ int check_step(h2o_ctx* h, int kind, const void* q, const void* k, const void* v
 
 int decode_split(const h2o_ctx* h)
 {
-    int s = h->split > 0 ? h->split : auto_decode_split(h->U, h->B, h->num_sms);
+    int s;
+    if (h->split > 0)
+        s = h->split;
+    else if (h->dtype == H2O_BF16 && h->D == 128 && !h->kv8 && h->G == 1 && (h->kind == kH2O || h->kind == kLSH) &&
+             h->U < h->num_sms)
+        s = few_units_split(h->U, h->B, h->num_sms, h->kind == kLSH);
+    else
+        s = auto_decode_split(h->U, h->B, h->num_sms);
     const int lo = (h->B + 1023) / 1024;
     if (s < lo) s = lo;
     if (s > max_decode_split()) s = max_decode_split();
@@ -440,6 +501,7 @@ int sh_decode_step(h2o_handle h, const void* q, const void* k, const void* v, fl
     DecodeArgs a = {};
     a.c = view(h); a.q = q; a.k = k; a.v = v; a.out = out; a.victim_out = victim_out;
     a.early = note_cache_write(h->device, h->stream, h) ? 1 : 0;
+    a.num_sms = h->num_sms;
     cudaError_t e = launch_sh_decode(a, decode_split(h), h->stream);
     if (e != cudaSuccess) return cuda_fail(e, "sh_decode_step launch");
     return H2O_OK;
@@ -453,6 +515,7 @@ int h2o_decode_step(h2o_handle h, const void* q, const void* k, const void* v, f
     DecodeArgs a = {};
     a.c = view(h); a.q = q; a.k = k; a.v = v; a.out = out; a.victim_out = victim_out; a.G = h->G;
     a.early = note_cache_write(h->device, h->stream, h) ? 1 : 0;
+    a.num_sms = h->num_sms;
     cudaError_t e = launch_h2o_decode(a, decode_split(h), h->stream);
     if (e != cudaSuccess) return cuda_fail(e, "h2o_decode_step launch");
     return H2O_OK;
@@ -466,8 +529,80 @@ int lsh_decode_step(h2o_handle h, const void* q, const void* k, const void* v, f
     DecodeArgs a = {};
     a.c = view(h); a.q = q; a.k = k; a.v = v; a.out = out; a.victim_out = victim_out; a.W = h->W;
     a.early = note_cache_write(h->device, h->stream, h) ? 1 : 0;
+    a.num_sms = h->num_sms;
     cudaError_t e = launch_lsh_decode(a, decode_split(h), h->stream);
     if (e != cudaSuccess) return cuda_fail(e, "lsh_decode_step launch");
+    return H2O_OK;
+}
+
+int fg_init(h2o_handle* out, int budget, int heavy, int recent, int full_budget, double tau, int batch, int heads,
+            int head_dim, int dtype, double scale, void* cuda_stream)
+{
+    return create(out, kFG, budget, heavy, recent, batch, heads, head_dim, dtype, scale, nullptr, cuda_stream, 1,
+                  full_budget, tau);
+}
+
+int fg_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T)
+{
+    int rc = check_prompt(h, kFG, Q, K, V, T);
+    if (rc) return rc;
+    if ((rc = ensure_prompt_scratch(h, T))) return rc;
+    if (inject("launch")) return fail(H2O_ERR_CUDA, "kernel launch failed (injected)");
+    CacheView cv = view(h);
+    PromptArgs pa = {};
+    pa.Q = Q; pa.K = K; pa.V = V; pa.T = T; pa.H = h->H; pa.G = 1;
+    pa.m2 = h->m2; pa.l = h->l; pa.c = h->c;
+    pa.budget = h->B_sel;
+    pa.bandB = h->bandB; pa.bandr = h->bandr; pa.wB = h->B_sel; pa.wr = h->r;
+    FgArgs fa = {};
+    fa.upol = h->upol; fa.rec = h->rec; fa.tau = h->tau;
+    fa.B = h->B_sel; fa.H = h->H; fa.r = h->r; fa.B_full = h->B_full;
+    note_cache_write(h->device, h->stream, h);
+    cudaError_t e = launch_prompt_stats(cv, pa, h->stream);
+    if (e == cudaSuccess) e = launch_select(cv, pa, h->stream);
+    if (e == cudaSuccess) e = launch_fg_policy(cv, pa, fa, h->stream);
+    if (e == cudaSuccess) e = launch_gather(cv, pa, false, h->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fg_prefill launch");
+    h->last_T = T;
+    h->ready = 1;
+    return H2O_OK;
+}
+
+int fg_decode_step(h2o_handle h, const void* q, const void* k, const void* v, float* out, int* victim_out)
+{
+    int rc = check_step(h, kFG, q, k, v, out);
+    if (rc) return rc;
+    if (inject("launch")) return fail(H2O_ERR_CUDA, "kernel launch failed (injected)");
+    DecodeArgs a = {};
+    a.c = view(h); a.q = q; a.k = k; a.v = v; a.out = out; a.victim_out = victim_out; a.G = 1;
+    a.early = note_cache_write(h->device, h->stream, h) ? 1 : 0;
+    a.num_sms = h->num_sms;
+    cudaError_t e = launch_h2o_decode(a, decode_split(h), h->stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fg_decode_step launch");
+    return H2O_OK;
+}
+
+int fg_get_policy(h2o_handle h, int* policy, double* rec_local, double* rec_freq)
+{
+    if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
+    if (h->kind != kFG) return fail(H2O_ERR_STATE, "fg_get_policy called on a %s handle", kind_name(h->kind));
+    const size_t U = (size_t)h->U;
+    int4* pp = static_cast<int4*>(malloc(U * sizeof(int4)));
+    double2* rr = static_cast<double2*>(malloc(U * sizeof(double2)));
+    if (!pp || !rr) { free(pp); free(rr); return fail(H2O_ERR_ALLOC, "host allocation failed"); }
+    cudaError_t e = cudaMemcpyAsync(pp, h->upol, U * sizeof(int4), cudaMemcpyDeviceToHost, h->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(rr, h->rec, U * sizeof(double2), cudaMemcpyDeviceToHost, h->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+    if (e == cudaSuccess) {
+        for (size_t u = 0; u < U; ++u) {
+            if (policy) policy[u] = pp[u].w;
+            if (rec_local) rec_local[u] = rr[u].x;
+            if (rec_freq) rec_freq[u] = rr[u].y;
+        }
+    }
+    free(pp);
+    free(rr);
+    if (e != cudaSuccess) return cuda_fail(e, "fg_get_policy");
     return H2O_OK;
 }
 
@@ -607,7 +742,8 @@ int h2o_set_kv_scales(h2o_handle h, const float* kscale, const float* vscale)
 int h2o_get_prefill_stats(h2o_handle h, float* m, float* l, double* c)
 {
     if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
-    if (h->kind != kH2O) return fail(H2O_ERR_STATE, "prompt statistics exist only on H2O handles");
+    if (h->kind != kH2O && h->kind != kFG)
+        return fail(H2O_ERR_STATE, "prompt statistics exist only on H2O and per-head policy handles");
     if (!h->last_T) return fail(H2O_ERR_STATE, "no prompt has been processed");
     const size_t n = (size_t)h->U * h->last_T, nq = n * (size_t)h->G;
     const double* cu = h->G > 1 ? h->ckv : h->c;

@@ -17,6 +17,8 @@ struct CacheView {
     uint32_t* code;     // [U][B] key codes (LSH); pivotal histories (persistence of importance)
     int2* ustate;       // [U] {occupancy, position of the next token}
     int* err;           // device error word (DeviceError bits)
+    const int4* upol;   // per-unit {budget, heavy, recent, policy} (per-head policies), else nullptr:
+                        // unit u then holds at most upol[u].x of its B slots
     int U, B, D, dtype, r;
     float qscale;       // softmax scale * log2(e): logits are kept in base 2
 };
@@ -33,6 +35,7 @@ struct DecodeArgs {
                         // cache, so the cache may be read before the dependency wait
     int G;              // H2O: query heads sharing each cache unit (0 or 1: one);
                         // q and out then hold U * G rows, head g of unit u in row u * G + g
+    int num_sms;        // the device's SM count (selects the tile)
 };
 
 struct PromptArgs {
@@ -48,6 +51,21 @@ struct PromptArgs {
     uint32_t* ck;       // [U][T] key codes (LSH)
     int G;              // prompt scorer: query heads per key row set (0 or 1: one);
                         // query unit u reads the keys of unit u / G
+    int budget;         // selection budget (0: the cache's B)
+    double* bandB;      // [U][T] or nullptr: per key j, the probabilities of rows j .. j+wB-1
+    double* bandr;      // [U][T] or nullptr: the same for rows j .. j+wr-1
+    int wB, wr;
+};
+
+// Per-head policy profile [the "Model Tells You What to Discard" review
+// page, method section]: per unit, the recoveries of the local and the
+// frequency + local caches and the first policy reaching tau.
+struct FgArgs {
+    int4* upol;         // out: [U] {budget, heavy, recent, policy}
+    double2* rec;       // out: [U] {local recovery, frequency + local recovery}
+    double tau;
+    int B, H, r;        // frequency + local (H2O) parameters; local is (B, 0, B)
+    int B_full;         // full cache: (B_full, 0, B_full)
 };
 
 cudaError_t launch_h2o_decode(const DecodeArgs& a, int split, cudaStream_t st);
@@ -55,6 +73,8 @@ cudaError_t launch_lsh_decode(const DecodeArgs& a, int split, cudaStream_t st);
 // persistence-of-importance step (histories in CacheView::code)
 cudaError_t launch_sh_decode(const DecodeArgs& a, int split, cudaStream_t st);
 int auto_decode_split(int U, int B, int num_sms);
+// split of a bf16, head_dim 128 one-head H2O / HashEvict cache with U < SMs
+int few_units_split(int U, int B, int num_sms, bool lsh);
 int max_decode_split();
 
 cudaError_t launch_prompt_stats(const CacheView& c, const PromptArgs& p, cudaStream_t st);
@@ -70,6 +90,10 @@ cudaError_t launch_sh_prompt(const CacheView& c, const PromptArgs& p, cudaStream
 // its tensor-core history pass (bf16, head_dim 128; needs p.m2, p.l scratch)
 cudaError_t launch_sh_flags_tc(const CacheView& c, const PromptArgs& p, cudaStream_t st);
 cudaError_t launch_gather(const CacheView& c, const PromptArgs& p, bool with_codes, cudaStream_t st);
+// per-head policies: recoveries from the column and band sums and the H2O
+// selection already made, the policy, and the kept set of local and full
+// units rewritten (the gather follows)
+cudaError_t launch_fg_policy(const CacheView& c, const PromptArgs& p, const FgArgs& f, cudaStream_t st);
 // One CTA whose bounded wait on a barrier nobody completes must run out and
 // set *err.
 cudaError_t launch_wait_selftest(int* err, cudaStream_t st);

@@ -1,13 +1,16 @@
 // noalloc.cu -- the prompt scorer without any device allocation.
 //
-// Some callers cannot call cudaMalloc: code that runs while a CUDA stream is
-// being captured into a graph, or serving runtimes that reserve all device
-// memory at start-up and forbid allocations afterwards.  This entry point
-// computes the same prompt column sums as h2o_prefill, with the scorer's
-// scratch (per-row max and normaliser, 8 bytes per unit per token) held in
-// a fixed device array inside the library instead of memory it allocates.
-// The array occupies kNoallocTokens * 8 bytes (8 MiB) on every device that
-// loads the library, until the process exits.
+// Some callers cannot call cudaMalloc: serving runtimes that reserve all
+// device memory for their own pool at start-up and forbid allocations
+// afterwards, and hosts whose allocation calls may synchronise the device in
+// the middle of their own streams' work.  This entry point computes the
+// same prompt column sums as h2o_prefill, with the scorer's scratch (per-row
+// max and normaliser, 8 bytes per unit per token) held in a fixed device
+// array inside the library instead of memory it allocates.  The array
+// occupies kNoallocTokens * 8 bytes (8 MiB) on every device that loads the
+// library, until the process exits.  With no handle there is no error word
+// to sync on: a scorer CTA whose bounded wait runs out writes NaN into the
+// statistics it owns, so the failure shows in the column sums.
 #include <mutex>
 
 #include "h2o.h"

@@ -168,7 +168,9 @@ __global__ void __launch_bounds__(256) rowstats_kernel(const T* __restrict__ Q, 
 template <typename T, int D>
 __global__ void __launch_bounds__(256) colsum_kernel(const T* __restrict__ Q, const T* __restrict__ K,
                                                     int T_, int G, float qscale, const float* __restrict__ m2,
-                                                    const float* __restrict__ lin, double* __restrict__ cout)
+                                                    const float* __restrict__ lin, double* __restrict__ cout,
+                                                    double* __restrict__ bandB, double* __restrict__ bandr,
+                                                    int wB, int wr)
 {
     extern __shared__ __align__(16) float tiles[];
     float (*Ks)[kTile + kPad] = reinterpret_cast<float (*)[kTile + kPad]>(tiles);
@@ -181,6 +183,8 @@ __global__ void __launch_bounds__(256) colsum_kernel(const T* __restrict__ Q, co
     const T* Ku = K + (size_t)(unit / G) * T_ * D;   // keys of this query unit
     load_tile_t<T, D>(Ks, Ku, jb * kTile, T_, 1.f);
     double csum[4] = {0.0, 0.0, 0.0, 0.0};
+    double bsum[4] = {0.0, 0.0, 0.0, 0.0}, rsum[4] = {0.0, 0.0, 0.0, 0.0};   // band sums
+    const int wmax = max(wB, wr);
     for (int ib = jb; ib < nb; ++ib) {
         __syncthreads();
         load_tile_t<T, D>(Qs, Qu, ib * kTile, T_, qscale);
@@ -192,24 +196,43 @@ __global__ void __launch_bounds__(256) colsum_kernel(const T* __restrict__ Q, co
         __syncthreads();
         float acc[4][4];
         tile_mma<D>(Ks, Qs, ty, tx, acc);       // acc[a][b]: key ty*4+a, query tx*4+b
+        // rows of this tile within the widest band of some key of the block
+        const bool band = bandB && ib * kTile < (jb + 1) * kTile + wmax;
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
             const int j = jb * kTile + ty * 4 + a;
-            float part = 0.f;
+            float part = 0.f, pB = 0.f, pr = 0.f;
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
                 const int i = ib * kTile + tx * 4 + b;
-                if (i >= j && i < T_) part += exp2f(acc[a][b] - ms[tx * 4 + b]) * il[tx * 4 + b];
+                if (i >= j && i < T_) {
+                    const float x = exp2f(acc[a][b] - ms[tx * 4 + b]) * il[tx * 4 + b];
+                    part += x;
+                    if (band) {
+                        if (i - j < wB) pB += x;
+                        if (i - j < wr) pr += x;
+                    }
+                }
             }
             part = red16_sum(part);
             csum[a] += (double)part;
+            if (band) {
+                bsum[a] += (double)red16_sum(pB);
+                rsum[a] += (double)red16_sum(pr);
+            }
         }
     }
     if (tx == 0) {
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
             const int j = jb * kTile + ty * 4 + a;
-            if (j < T_) cout[(size_t)unit * T_ + j] = csum[a];
+            if (j < T_) {
+                cout[(size_t)unit * T_ + j] = csum[a];
+                if (bandB) {
+                    bandB[(size_t)unit * T_ + j] = bsum[a];
+                    bandr[(size_t)unit * T_ + j] = rsum[a];
+                }
+            }
         }
     }
 }
@@ -259,9 +282,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(CacheView cv, Promp
     __shared__ unsigned long long s_prefix;
     __shared__ int s_need;
     const int unit = blockIdx.x;
-    const int T_ = pa.T, B = cv.B, r = cv.r;
+    const int T_ = pa.T, B = pa.budget > 0 ? pa.budget : cv.B, r = cv.r;
     const double* cu = pa.c + (size_t)unit * T_;
-    const size_t ub = (size_t)unit * B;
+    const size_t ub = (size_t)unit * cv.B;     // slot stride: the cache's B
     const int tid = threadIdx.x;
     const int per = (T_ + kSelThreads - 1) / kSelThreads;   // contiguous positions per thread
     const int j0 = tid * per, j1 = min(T_, j0 + per);
@@ -367,11 +390,82 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(CacheView cv, Promp
             }
         }
     }
-    for (int s = nkept + tid; s < B; s += kSelThreads) {
+    for (int s = nkept + tid; s < cv.B; s += kSelThreads) {
         cv.pos[ub + s] = -1;
         if (cv.score) cv.score[ub + s] = make_float2(0.f, 0.f);
     }
     if (tid == 0) cv.ustate[unit] = make_int2(nkept, T_);
+}
+
+// Per-head policy of every unit ["Model Tells You What to Discard" review
+// page, method section: each head is profiled on the prompt and takes the
+// first policy whose cache recovers enough of its attention; Figure 2
+// caption: the frequency + local policy is the H2O cache].  Recovery of a
+// policy = the attention mass its kept set holds at each prompt row,
+// averaged over the rows:
+//   local (the newest B keys):   sum_j bandB_j / T
+//   frequency + local:           (sum_j bandr_j + sum_{j heavy} (c_j - bandr_j)) / T
+// where band*_j is key j's probability mass from rows j .. j+w-1 (the rows
+// whose window holds it) and the heavy keys are the H2O selection's kept
+// keys older than the window (all kept keys hold, for a prompt within the
+// budget).  Policy: local if its recovery reaches tau, else frequency +
+// local if its does, else full.  Local and full units then keep the newest
+// min(T, budget) tokens.  One CTA (256 threads) per unit, after the H2O
+// selection (budget B) and before the gather.
+__global__ void __launch_bounds__(256) fg_policy_kernel(CacheView cv, PromptArgs pa, FgArgs fa)
+{
+    __shared__ double red[3][8];
+    __shared__ int s_n;
+    const int unit = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int T_ = pa.T;
+    const size_t ub = (size_t)unit * cv.B;
+    const double* cu = pa.c + (size_t)unit * T_;
+    const double* bB = pa.bandB + (size_t)unit * T_;
+    const double* br = pa.bandr + (size_t)unit * T_;
+    double sB = 0.0, sr = 0.0, sh = 0.0;
+    for (int j = tid; j < T_; j += 256) {
+        sB += bB[j];
+        sr += br[j];
+    }
+    const int n = cv.ustate[unit].x;
+    for (int s = tid; s < n; s += 256) {
+        const int j = cv.pos[ub + s];
+        if (j >= 0 && j < T_ - fa.r) sh += cu[j] - br[j];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        sB += __shfl_xor_sync(kFull, sB, o);
+        sr += __shfl_xor_sync(kFull, sr, o);
+        sh += __shfl_xor_sync(kFull, sh, o);
+    }
+    if (lane == 0) { red[0][warp] = sB; red[1][warp] = sr; red[2][warp] = sh; }
+    __syncthreads();
+    if (tid == 0) {
+        double a = 0.0, b = 0.0, h = 0.0;
+        for (int w = 0; w < 8; ++w) { a += red[0][w]; b += red[1][w]; h += red[2][w]; }
+        const double rl = a / (double)T_, rf = (b + h) / (double)T_;
+        const int policy = rl >= fa.tau ? 0 : (rf >= fa.tau ? 1 : 2);
+        const int4 pp = policy == 0 ? make_int4(fa.B, 0, fa.B, 0)
+                      : policy == 1 ? make_int4(fa.B, fa.H, fa.r, 1)
+                                    : make_int4(fa.B_full, 0, fa.B_full, 2);
+        fa.upol[unit] = pp;
+        fa.rec[unit] = make_double2(rl, rf);
+        s_n = policy == 1 ? -1 : min(T_, pp.x);
+    }
+    __syncthreads();
+    const int nk = s_n;
+    if (nk < 0) return;                     // frequency + local: the H2O selection stands
+    for (int s = tid; s < cv.B; s += 256) {
+        const int j = s < nk ? T_ - nk + s : -1;
+        cv.pos[ub + s] = j;
+        float2 sc = make_float2(0.f, 0.f);
+        if (j >= 0) {
+            const float hi = __double2float_rn(cu[j]);
+            sc = make_float2(hi, __double2float_rn(cu[j] - (double)hi));
+        }
+        cv.score[ub + s] = sc;
+    }
+    if (tid == 0) cv.ustate[unit] = make_int2(nk, T_);
 }
 
 // Copy the prompt rows named by pos[] into the slots (zero for empty slots);
@@ -760,7 +854,7 @@ cudaError_t stats_t(const CacheView& c, const PromptArgs& p, cudaStream_t st)
     if (e != cudaSuccess) return e;
     colsum_kernel<T, D><<<grid, 256, smem, st>>>(reinterpret_cast<const T*>(p.Q),
                                                reinterpret_cast<const T*>(p.K), p.T, G, c.qscale, p.m2, p.l,
-                                               p.c);
+                                               p.c, p.bandB, p.bandr, p.wB, p.wr);
     return cudaGetLastError();
 }
 
@@ -1031,6 +1125,12 @@ cudaError_t launch_group_sum(const double* c, double* ckv, int U, int G, int T, 
 cudaError_t launch_select(const CacheView& c, const PromptArgs& p, cudaStream_t st)
 {
     select_kernel<<<(unsigned)c.U, kSelThreads, 0, st>>>(c, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fg_policy(const CacheView& c, const PromptArgs& p, const FgArgs& f, cudaStream_t st)
+{
+    fg_policy_kernel<<<(unsigned)c.U, 256, 0, st>>>(c, p, f);
     return cudaGetLastError();
 }
 

@@ -17,9 +17,10 @@
 // one of two TMEM accumulators and commits to mbarriers; warps 2..5 drain
 // the accumulators with tcgen05.ld (thread = TMEM lane = tile row).  The
 // MMA of tile t+1 overlaps the exponentials of tile t.  Every wait is
-// bounded: a wait that runs out sets the handle's error word and the CTA
-// abandons its loop, waits (bounded) for its copies in flight, frees its
-// TMEM and returns.
+// bounded: a wait that runs out sets the handle's error word (when there is
+// one) and the CTA abandons its loop, writes NaN into the statistics it owns
+// (so pass 2 and every reader of the column sums see the failure), waits
+// (bounded) for its copies in flight, frees its TMEM and returns.
 #include <cuda.h>
 #include <cfloat>
 #include <cstddef>
@@ -344,9 +345,11 @@ __global__ void __launch_bounds__(kThreads, 2)
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.acc_empty[b]);
         }
-        if (i < T && !aborted(S)) {
-            m2[(size_t)u * T + i] = m;
-            lout[(size_t)u * T + i] = l - lc;
+        if (i < T) {
+            // an abandoned CTA leaves NaN, which the column sums carry on
+            const bool ab = aborted(S);
+            m2[(size_t)u * T + i] = ab ? __int_as_float(0x7fffffff) : m;
+            lout[(size_t)u * T + i] = ab ? __int_as_float(0x7fffffff) : l - lc;
         }
     }
     tc_teardown(S, warp, ntiles);
@@ -359,7 +362,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 __global__ void __launch_bounds__(kThreads, 2)
     colsum_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK, int U,
                      int G, int T, int nb, float c2, const float* __restrict__ m2, const float* __restrict__ lin,
-                     double* __restrict__ cout, int* err)
+                     double* __restrict__ cout, double* __restrict__ bandB, double* __restrict__ bandr, int wB,
+                     int wr, int* err)
 {
     extern __shared__ unsigned char smem_raw[];
     TcSmem& S = tc_smem(smem_raw);
@@ -389,9 +393,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             S.colstat[0][et] = i < T ? m2u[i] + log2f(lu[i]) : INFINITY;
         }
         float cs = 0.f, cc = 0.f;                 // Kahan-summed column sum
+        double bsB = 0.0, bsr = 0.0;              // band sums (rows j .. j+w-1)
+        const int wmax = max(wB, wr);
         for (int t = 0; t < ntiles; ++t) {
             const int b = t & 1;
             const int ib = jb + t;
+            // some key of the block has rows of this tile in its band
+            const bool band = bandB && ib * kT < (jb + 1) * kT + wmax;
             // the next tile's statistics, stored after this tile
             float nm = 0.f, nl = 0.f;
             const int inext = (ib + 1) * kT + et;
@@ -405,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             tc_fence_after();
             const bool edge = (t == 0) || ((ib + 1) * kT > T);
             const float* bs = S.colstat[b];
-            float part = 0.f;
+            float part = 0.f, partB = 0.f, partr = 0.f;
             const uint32_t tcol = tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * kT);
             uint32_t ra[32], rb[32];
             tc_ld32_issue(tcol, ra);
@@ -416,6 +424,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 uint32_t (&nxt)[32] = (ch & 1) ? ra : rb;
                 if (ch + 1 < 4) tc_ld32_issue(tcol + (uint32_t)((ch + 1) * 32), nxt);
                 const int i0 = ib * kT + ch * 32;
+                const int dj = i0 - j;                    // i - j of the chunk's first row
                 float p0 = 0.f, p1 = 0.f;
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
@@ -432,6 +441,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                     p0 += w0 + w2;
                     p1 += w1 + w3;
+                    if (band) {
+                        const int d0 = dj + e;
+                        partB += (d0 < wB ? w0 : 0.f) + (d0 + 1 < wB ? w1 : 0.f) + (d0 + 2 < wB ? w2 : 0.f) +
+                                 (d0 + 3 < wB ? w3 : 0.f);
+                        partr += (d0 < wr ? w0 : 0.f) + (d0 + 1 < wr ? w1 : 0.f) + (d0 + 2 < wr ? w2 : 0.f) +
+                                 (d0 + 3 < wr ? w3 : 0.f);
+                    }
                 }
                 part += p0 + p1;
                 if (ch + 1 < 4) tc_ld32_wait(nxt);
@@ -443,10 +459,23 @@ __global__ void __launch_bounds__(kThreads, 2)
             const float tsum = cs + y;
             cc = (tsum - cs) - y;
             cs = tsum;
+            if (band) {
+                bsB += (double)partB;
+                bsr += (double)partr;
+            }
             // publish the next tile's statistics into the other buffer
             if (t + 1 < ntiles) S.colstat[b ^ 1][et] = inext < T ? nm + log2f(nl) : INFINITY;
         }
-        if (j < T && !aborted(S)) cout[(size_t)u * T + j] = (double)cs - (double)cc;
+        // an abandoned CTA leaves NaN in its columns
+        if (j < T) {
+            const bool ab = aborted(S);
+            const double nan = __longlong_as_double(0x7ff8000000000000LL);
+            cout[(size_t)u * T + j] = ab ? nan : (double)cs - (double)cc;
+            if (bandB) {
+                bandB[(size_t)u * T + j] = ab ? nan : bsB;
+                bandr[(size_t)u * T + j] = ab ? nan : bsr;
+            }
+        }
     }
     tc_teardown(S, warp, ntiles);
 }
@@ -595,7 +624,8 @@ cudaError_t launch_prompt_stats_tc(const CacheView& c, const PromptArgs& p, cuda
     rowstats_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, c.U, G, p.T, nb, c.qscale, p.m2, p.l, c.err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    colsum_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, c.U, G, p.T, nb, c.qscale, p.m2, p.l, p.c, c.err);
+    colsum_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, c.U, G, p.T, nb, c.qscale, p.m2, p.l, p.c, p.bandB,
+                                                   p.bandr, p.wB, p.wr, c.err);
     return cudaGetLastError();
 }
 

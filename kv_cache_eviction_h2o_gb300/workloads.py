@@ -44,6 +44,8 @@ class Workload:
     lsh: bool = False
     lsh_seed: int = 4
     groups: int = 1       # query heads per cache unit (grouped-query attention)
+    tau: float = 0.0      # per-head policy workloads: recovery threshold
+    full_budget: int = 0  # per-head policy workloads: budget of the full-cache policy
 
     @property
     def units(self) -> int:
@@ -83,6 +85,15 @@ WORKLOADS = {
     # seeded N(0,1) 128 x 32 matrix, recent window 205.
     "hashevict-opt-6.7b": Workload("hashevict-opt-6.7b", 8, 32, 128, 2048, 256, 410, 205, 205,
                                    "bf16", 1, ("rank", 4, 2.0), lsh=True, lsh_seed=4),
+    # Per-head policies on the OPT-6.7B shapes: head h of each batch row is a
+    # local head (h % 3 == 0), a heavy-hitter head (1) or a broad head (2);
+    # recovery threshold 0.95; the full-cache policy keeps prompt + decode.
+    "fastgen-opt-6.7b": Workload("fastgen-opt-6.7b", 8, 32, 128, 2048, 256, 410, 205, 205, "bf16", 6,
+                                 ("fastgen", 2.0, 0.5, 10.0, 10.0, 0.01, 4, 0.5), tau=0.95, full_budget=2304),
+    # The same head mix, small: fp32, head_dim 64, 1 x 6 heads, prompt 256, 32 steps,
+    # budget 64 = 32 + 32, full-cache budget 288.
+    "fastgen-tiny": Workload("fastgen-tiny", 1, 6, 64, 256, 32, 64, 32, 32, "f32", 7,
+                             ("fastgen", 2.0, 0.5, 10.0, 10.0, 0.01, 4, 0.5), tau=0.95, full_budget=288),
     # Grouped-query layer with the OPT-6.7B prompt and budget: 8 x 8 key/value heads,
     # each shared by 4 query heads (32 query heads), d 128, rank-4 keys.
     "gqa-8x8x4": Workload("gqa-8x8x4", 8, 8, 128, 2048, 256, 410, 205, 205, "bf16", 5,
@@ -151,6 +162,46 @@ def _finish(w: Workload, x: np.ndarray) -> np.ndarray:
     return round_bf16(x) if w.dtype == "bf16" else x
 
 
+def head_kind(w: Workload, unit: int) -> int:
+    """Per-head policy workloads: 0 local head, 1 heavy-hitter head, 2 broad
+    head, by the head index of the unit (h % 3)."""
+    return (unit % w.heads) % 3
+
+
+def _positions_embedding(d: int, pos: np.ndarray) -> np.ndarray:
+    """[cos(w_m t), sin(w_m t)] over m < d/2, w_m = 10000^(-2m/d): rows whose
+    dot product decays with the distance between their positions."""
+    m = np.arange(d // 2)
+    om = 10000.0 ** (-m / (d // 2))
+    t = pos.astype(np.float64)[:, None]
+    return np.concatenate([np.cos(om * t), np.sin(om * t)], axis=1)
+
+
+def _fastgen_qk(w: Workload, unit: int, Q: np.ndarray, K: np.ndarray, g: np.random.Generator,
+                first_pos: int):
+    """Per-head policy workloads: shape Q, K [n, d] (float64, i.i.d. N(0,1)
+    on entry) by the unit's head kind.  Local: amp * E(t) + noise * N for
+    both (attention concentrated on nearby positions).  Heavy hitter:
+    queries + beta * u, keys N(0,1) with a fraction (and the first nsink
+    prompt positions) + gamma * u, u a unit vector of the unit.  Broad:
+    scale * N for both (near-uniform attention)."""
+    _, amp, noise, beta, gamma, frac, nsink, broad = w.structure
+    n, d = Q.shape
+    kind = head_kind(w, unit)
+    if kind == 0:
+        E = _positions_embedding(d, first_pos + np.arange(n))
+        return amp * E + noise * Q, amp * E + noise * K
+    if kind == 1:
+        gu = _rng(w.seed, TAG_SHARED, 1 + unit)
+        u = gu.standard_normal(d)
+        u /= np.linalg.norm(u)
+        mask = g.random(n) < frac
+        mask |= (first_pos + np.arange(n)) < nsink
+        K = K + np.where(mask[:, None], gamma * u[None, :], 0.0)
+        return Q + beta * u[None, :], K
+    return broad * Q, broad * K
+
+
 def prompt_unit(w: Workload, unit: int, prompt: Optional[int] = None):
     """Prompt Q, K, V of one unit, each [T, d] float32."""
     T = w.prompt if prompt is None else prompt
@@ -159,7 +210,10 @@ def prompt_unit(w: Workload, unit: int, prompt: Optional[int] = None):
     Q = g.standard_normal((T, d), dtype=np.float32).astype(np.float64)
     K = g.standard_normal((T, d), dtype=np.float32).astype(np.float64)
     V = g.standard_normal((T, d), dtype=np.float32).astype(np.float64)
-    K = _structure_keys(w, unit, K, g, 0)
+    if w.structure and w.structure[0] == "fastgen":
+        Q, K = _fastgen_qk(w, unit, Q, K, g, 0)
+    else:
+        K = _structure_keys(w, unit, K, g, 0)
     return _finish(w, Q), _finish(w, K), _finish(w, V)
 
 
@@ -174,7 +228,10 @@ def decode_unit(w: Workload, unit: int, steps: Optional[int] = None,
     q = g.standard_normal((S, d), dtype=np.float32).astype(np.float64)
     k = g.standard_normal((S, d), dtype=np.float32).astype(np.float64)
     v = g.standard_normal((S, d), dtype=np.float32).astype(np.float64)
-    k = _structure_keys(w, unit, k, g, T)
+    if w.structure and w.structure[0] == "fastgen":
+        q, k = _fastgen_qk(w, unit, q, k, g, T)
+    else:
+        k = _structure_keys(w, unit, k, g, T)
     return _finish(w, q), _finish(w, k), _finish(w, v)
 
 
@@ -278,6 +335,37 @@ def generate_device(w: Workload, seed_offset: int = 0, prompt: Optional[int] = N
             mask |= (posn < nsink).unsqueeze(0)
             return torch.where(mask.unsqueeze(-1), Kx * factor, Kx)
         raise ValueError(kind)
+
+    if w.structure and w.structure[0] == "fastgen":
+        _, amp, noise, beta, gamma, frac, nsink, broad = w.structure
+        kind = torch.tensor([head_kind(w, u) for u in range(U)], device=device).view(U, 1, 1)
+        udir = normal(U, d)
+        udir = (udir / udir.norm(dim=1, keepdim=True)).unsqueeze(1)
+
+        def emb(first, n):
+            return torch.from_numpy(_positions_embedding(d, first + np.arange(n)).astype(np.float32)).to(device)
+
+        def fastgen(Qx, Kx, first):
+            # Qx, Kx: [U, n, d] N(0,1); the three head kinds as in the numpy recipe
+            n = Qx.shape[1]
+            E = emb(first, n).unsqueeze(0)
+            mask = (torch.rand(U, n, 1, generator=g, device=device) < frac) | \
+                ((first + torch.arange(n, device=device)) < nsink).view(1, n, 1)
+            Ql, Kl = amp * E + noise * Qx, amp * E + noise * Kx
+            Qh, Kh = Qx + beta * udir, Kx + torch.where(mask, gamma * udir, torch.zeros_like(Kx))
+            Qb, Kb = broad * Qx, broad * Kx
+            Qo = torch.where(kind == 0, Ql, torch.where(kind == 1, Qh, Qb))
+            Ko = torch.where(kind == 0, Kl, torch.where(kind == 1, Kh, Kb))
+            return Qo, Ko
+
+        Qp, Kp = fastgen(normal(U, T, d), normal(U, T, d), 0)
+        out = {"Q": Qp.to(dt).contiguous(), "K": Kp.to(dt).contiguous(), "V": normal(U, T, d).to(dt).contiguous()}
+        if S > 0:
+            qd, kd = fastgen(normal(U, S, d), normal(U, S, d), T)
+            out["q"] = qd.transpose(0, 1).to(dt).contiguous()
+            out["k"] = kd.transpose(0, 1).to(dt).contiguous()
+            out["v"] = normal(S, U, d).to(dt).contiguous()
+        return out
 
     out = {
         "Q": normal(U * w.groups, T, d).to(dt).contiguous(),
