@@ -14,7 +14,7 @@ HEADER = os.path.join(ROOT, "include", "h2o.h")
 def _declared():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b((?:h2o|lsh|sh)_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:h2o|lsh|sh|fg)_[a-z_]+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")
@@ -29,7 +29,8 @@ def test_header_declares_the_api():
     names = _declared()
     for must in ("h2o_init", "h2o_prefill", "h2o_decode_step", "lsh_decode_step", "lsh_init",
                  "lsh_prefill", "h2o_get_state", "h2o_set_state", "h2o_sync", "h2o_destroy",
-                 "h2o_last_error", "h2o_init_gqa", "sh_init", "sh_prefill", "sh_decode_step"):
+                 "h2o_last_error", "h2o_init_gqa", "sh_init", "sh_prefill", "sh_decode_step",
+                 "fg_init", "fg_prefill", "fg_decode_step", "fg_get_policy"):
         assert must in names
 
 
@@ -40,7 +41,7 @@ def test_library_exports_every_declared_symbol(L):
     # the binding wraps exactly the declared set
     assert set(L.SIGNATURES) == set(_declared())
     out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True, text=True).stdout
-    exported = set(re.findall(r" T ((?:h2o|lsh|sh)_\w+)$", out, flags=re.M))
+    exported = set(re.findall(r" T ((?:h2o|lsh|sh|fg)_\w+)$", out, flags=re.M))
     assert set(_declared()) <= exported
 
 
@@ -112,3 +113,44 @@ def test_persistence_rule_init_checks(L):
     assert lib.sh_prefill(None, None, None, None, 4) == L.H2O_ERR_ARG
     assert lib.sh_decode_step(None, None, None, None, None, None) == L.H2O_ERR_ARG
     assert lib.sh_init(None, 10, 5, 5, 1, 1, 128, 1, 0.1, None) == L.H2O_ERR_ARG
+
+
+def test_binding_checks_host_buffers(L):
+    import numpy as np
+    # a handle shape recorded as the init call records it (no device needed:
+    # every check below fails before the library is called)
+    h = L._remember(0xDEAD0, "h2o", 4, 8, 64, L.H2O_BF16)
+    try:
+        with pytest.raises(TypeError, match="score"):
+            L.h2o_get_state(h, score=np.empty(32, np.float32))
+        with pytest.raises(ValueError, match="pos"):
+            L.h2o_get_state(h, pos=np.empty(31, np.int32))
+        with pytest.raises(TypeError, match="K"):
+            L.h2o_set_state(h, K=np.empty(4 * 8 * 64, np.float32))      # bf16 rows are uint16 on the host
+        with pytest.raises(ValueError, match="occupancy"):
+            L.h2o_set_state(h, occupancy=np.empty(5, np.int32))
+        with pytest.raises(ValueError, match="kscale"):
+            L.h2o_get_kv_scales(h, np.empty(31, np.float32))
+        with pytest.raises(ValueError, match="c"):
+            L.h2o_get_prefill_stats(h, c=np.empty(1))
+        with pytest.raises(TypeError, match="numpy"):
+            L.h2o_get_state(h, score=[0.0] * 32)
+    finally:
+        L._meta.pop(h, None)
+    with pytest.raises(ValueError, match="unknown handle"):
+        L.h2o_get_state(0xDEAD0, score=np.empty(32))
+
+
+def test_per_head_policy_init_checks(L):
+    lib = L.lib()
+    for args, frag in (((10, 5, 6, 64, 0.95), "heavy + recent"), ((10, 5, 5, 0, 0.95), "full_budget"),
+                       ((10, 5, 5, 64, 0.0), "tau"), ((10, 5, 5, 64, 1.5), "tau")):
+        with pytest.raises(L.H2OError) as e:
+            L.fg_init(*args, 1, 1, 128, 1, 0.1)
+        assert e.value.code == L.H2O_ERR_ARG and frag in str(e.value)
+    with pytest.raises(L.H2OError) as e:
+        L.fg_init(10, 5, 5, 64, 0.95, 1, 1, 128, 1 | L.H2O_KV8, 0.1)
+    assert e.value.code == L.H2O_ERR_UNSUPPORTED
+    assert lib.fg_prefill(None, None, None, None, 4) == L.H2O_ERR_ARG
+    assert lib.fg_decode_step(None, None, None, None, None, None) == L.H2O_ERR_ARG
+    assert lib.fg_get_policy(None, None, None, None) == L.H2O_ERR_ARG

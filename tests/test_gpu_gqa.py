@@ -17,7 +17,7 @@ if not torch.cuda.is_available():
 import oracle                                              # noqa: E402
 from kv_cache_eviction_h2o_gb300 import binding as L       # noqa: E402
 from kv_cache_eviction_h2o_gb300 import workloads as wl    # noqa: E402
-from parity import (Dev, align_prefill, check_out, check_scores, h2o_lockstep,  # noqa: E402
+from parity import (record, Dev, align_prefill, check_out, check_scores, h2o_lockstep,  # noqa: E402
                     rows_equal)
 
 pytestmark = pytest.mark.gpu
@@ -132,7 +132,7 @@ def test_gqa_workload_units():
     assert (s["pos"] == st.pos).all() and rows_equal(s, st)
     check_scores(s["score"], st.score, "prompt scores")
     near, _ = h2o_lockstep(dev, st, g["q"], g["k"], g["v"], w.prompt, w.recent, w.scale, check_every=4)
-    print("gqa-8x8x4: near ties prefill %d decode %d" % (near0, near))
+    record("gqa-8x8x4 lockstep", near_ties=near0 + near)
     dev.close()
 
 

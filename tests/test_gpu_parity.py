@@ -10,7 +10,7 @@ if not torch.cuda.is_available():
 
 import oracle                                              # noqa: E402
 from kv_cache_eviction_h2o_gb300 import workloads as wl    # noqa: E402
-from parity import (Dev, align_prefill, check_out, check_scores, h2o_lockstep,  # noqa: E402
+from parity import (record, Dev, align_prefill, check_out, check_scores, h2o_lockstep,  # noqa: E402
                     kept_lists, lsh_lockstep)
 
 pytestmark = pytest.mark.gpu
@@ -55,7 +55,7 @@ def test_tiny_workload_h2o():
     assert (s["pos"] == st.pos).all()
     check_scores(s["score"], st.score, "prefill scores")
     near, _ = h2o_lockstep(dev, st, g["q"], g["k"], g["v"], w.prompt, w.recent, w.scale)
-    print("tiny: near ties prefill %d decode %d" % (near0, near))
+    record("tiny lockstep", near_ties=near0 + near)
     dev.close()
 
 
@@ -73,7 +73,7 @@ def test_opt67b_units_h2o(split):
     assert (s["K"] == st.K).all()
     check_scores(s["score"], st.score, "prefill scores")
     near, _ = h2o_lockstep(dev, st, g["q"], g["k"], g["v"], w.prompt, w.recent, w.scale, check_every=4)
-    print("opt-6.7b split %d: near ties prefill %d decode %d" % (split, near0, near))
+    record("opt-6.7b lockstep split=%d" % split, near_ties=near0 + near)
     dev.close()
 
 

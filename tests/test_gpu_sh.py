@@ -16,7 +16,7 @@ if not torch.cuda.is_available():
 import oracle                                              # noqa: E402
 from kv_cache_eviction_h2o_gb300 import binding as L       # noqa: E402
 from kv_cache_eviction_h2o_gb300 import workloads as wl    # noqa: E402
-from parity import Dev, rows_equal, sh_align_prefill, sh_lockstep  # noqa: E402
+from parity import record, Dev, rows_equal, sh_align_prefill, sh_lockstep  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -74,7 +74,7 @@ def test_sh_opt67b_units(split):
     g = wl.generate(w, units=list(range(12)), steps=40)
     f0, f1 = _run(U=12, T=w.prompt, B=w.budget, H=w.heavy, r=w.recent, S=40, d=w.head_dim, dtype=w.dtype,
                   seed=0, split=split, inputs=(g["Q"], g["K"], g["V"], g["q"], g["k"], g["v"]))
-    print("sh opt-6.7b split %d: flips prompt %d decode %d" % (split, f0, f1))
+    record("persistence rule opt-6.7b split=%d" % split, flips=f0 + f1)
 
 
 def test_sh_one_cta_with_a_budget_near_the_chunk_limit():
