@@ -202,6 +202,22 @@ __device__ __forceinline__ unsigned ord_key(float x)
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// Loads whose issue point is fixed (volatile): a value needed only much
+// later is requested where the load is written, so its latency hides under
+// the work in between instead of being paid at the use.
+__device__ __forceinline__ uint32_t ld_issue_u32(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.global.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float2 ld_issue_f2(const float2* p)
+{
+    float2 v;
+    asm volatile("ld.global.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+    return v;
+}
+
 // ---------------------------------------------- programmatic dependent launch
 
 // Block until the grid this one depends on (the previous kernel in the

@@ -708,6 +708,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     int2 us = make_int2(0, 0);
     float2 sc_old[TL::SPT];
     int ps[TL::SPT];
+    // (volatile loads: issued here, not sunk to their use after the stream)
     auto read_cache = [&]() {
         us = c.ustate[unit];
 #pragma unroll
@@ -716,9 +717,9 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
             sc_old[i] = make_float2(0.f, 0.f);
             ps[i] = 0;
             if (s < s1) {
-                if constexpr (SH) sc_old[i].x = __uint_as_float(c.code[ub + s]);
-                else sc_old[i] = c.score[ub + s];
-                ps[i] = c.pos[ub + s];
+                if constexpr (SH) sc_old[i].x = __uint_as_float(ld_issue_u32(c.code + ub + s));
+                else sc_old[i] = ld_issue_f2(c.score + ub + s);
+                ps[i] = (int)ld_issue_u32(reinterpret_cast<const uint32_t*>(c.pos + ub + s));
             }
         }
     };

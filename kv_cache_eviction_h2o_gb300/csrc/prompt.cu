@@ -239,7 +239,6 @@ __global__ void __launch_bounds__(256) colsum_kernel(const T* __restrict__ Q, co
 
 // ------------------------------------------------------------ block scan
 
-constexpr int kSelThreads = 1024;
 
 // exclusive prefix sum of one int per thread over the block; returns the
 // thread's offset, *total receives the block sum
@@ -275,7 +274,45 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* t
 // select on the fp64 bit patterns, which order like the values because
 // every c_j >= 0; ties to the lower position), plus the recent window; kept
 // positions go to slots 0.. in ascending order with their scores.
-__global__ void __launch_bounds__(kSelThreads) select_kernel(CacheView cv, PromptArgs pa)
+// The digit of a radix round: with hist[d] the candidates of digit d still
+// in play and `remaining` of them to keep, the largest digit d such that at
+// least `remaining` candidates have digit >= d, and how many of those with
+// digit > d there are (cum).  One warp: each lane sums 8 bins, a suffix scan
+// over the lanes and a ballot find the lane holding the digit, which then
+// walks its 8 bins from the top.
+__device__ __forceinline__ void radix_digit(const unsigned* hist, int remaining, int lane, int& dig, int& cum)
+{
+    unsigned b[8];
+    unsigned tot = 0u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        b[k] = hist[8 * lane + k];
+        tot += b[k];
+    }
+    // inclusive suffix sum over lanes: bins of this lane and every higher one
+    unsigned suf = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_down_sync(kFull, suf, o);
+        if (lane + o < 32) suf += y;
+    }
+    const unsigned hit = __ballot_sync(kFull, suf >= (unsigned)remaining);
+    const int L = hit ? 31 - __clz(hit) : 0;             // highest lane reaching the target
+    const unsigned above = __shfl_sync(kFull, suf - tot, L);   // bins of the lanes above L
+    int d = 8 * L, c = (int)above;
+    if (lane == L) {
+#pragma unroll
+        for (int k = 7; k >= 0; --k) {
+            if (c + (int)b[k] >= remaining) { d = 8 * L + k; break; }
+            c += (int)b[k];
+        }
+    }
+    dig = __shfl_sync(kFull, d, L);
+    cum = __shfl_sync(kFull, c, L);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT) select_kernel(CacheView cv, PromptArgs pa)
 {
     __shared__ unsigned hist[256];
     __shared__ int warp_tot[32];
@@ -286,7 +323,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(CacheView cv, Promp
     const double* cu = pa.c + (size_t)unit * T_;
     const size_t ub = (size_t)unit * cv.B;     // slot stride: the cache's B
     const int tid = threadIdx.x;
-    const int per = (T_ + kSelThreads - 1) / kSelThreads;   // contiguous positions per thread
+    const int per = (T_ + NT - 1) / NT;      // contiguous positions per thread
     const int j0 = tid * per, j1 = min(T_, j0 + per);
 
     const bool keep_all = T_ <= B;
@@ -299,12 +336,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(CacheView cv, Promp
         unsigned long long prefix = 0ull, mask = 0ull;
         int remaining = H;
         for (int shift = 56; shift >= 0; shift -= 8) {
-            for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0u;
+            for (int i = tid; i < 256; i += NT) hist[i] = 0u;
             __syncthreads();
             // warp-aggregated: one shared-memory atomic per distinct digit
             // per warp (many candidates can share a digit, e.g. the zero low
             // bytes of integer-valued keys)
-            for (int jb = tid - (tid & 31); jb < ncand; jb += kSelThreads) {
+            for (int jb = tid - (tid & 31); jb < ncand; jb += NT) {
                 const int j = jb + (tid & 31);
                 int dig = -1;
                 if (j < ncand) {
@@ -315,16 +352,13 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(CacheView cv, Promp
                 if (dig >= 0 && (tid & 31) == __ffs(peers) - 1) atomicAdd(&hist[dig], (unsigned)__popc(peers));
             }
             __syncthreads();
-            if (tid == 0) {
-                int cum = 0;
-                int dig = 0;
-                for (int d = 255; d >= 0; --d) {
-                    if (cum + (int)hist[d] >= remaining) { dig = d; break; }
-                    cum += (int)hist[d];
+            if (tid < 32) {
+                int dig, cum;
+                radix_digit(hist, remaining, tid, dig, cum);
+                if (tid == 0) {
+                    s_prefix = prefix | ((unsigned long long)dig << shift);
+                    s_need = remaining - cum;
                 }
-                remaining -= cum;
-                s_prefix = prefix | ((unsigned long long)dig << shift);
-                s_need = remaining;
             }
             __syncthreads();
             prefix = s_prefix;
@@ -390,7 +424,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(CacheView cv, Promp
             }
         }
     }
-    for (int s = nkept + tid; s < cv.B; s += kSelThreads) {
+    for (int s = nkept + tid; s < cv.B; s += NT) {
         cv.pos[ub + s] = -1;
         if (cv.score) cv.score[ub + s] = make_float2(0.f, 0.f);
     }
@@ -1124,7 +1158,10 @@ cudaError_t launch_group_sum(const double* c, double* ckv, int U, int G, int T, 
 
 cudaError_t launch_select(const CacheView& c, const PromptArgs& p, cudaStream_t st)
 {
-    select_kernel<<<(unsigned)c.U, kSelThreads, 0, st>>>(c, p);
+    // a block of 256 threads for prompts up to 4096 tokens (more units per
+    // SM), 1024 above
+    if (p.T <= 4096) select_kernel<256><<<(unsigned)c.U, 256, 0, st>>>(c, p);
+    else select_kernel<1024><<<(unsigned)c.U, 1024, 0, st>>>(c, p);
     return cudaGetLastError();
 }
 

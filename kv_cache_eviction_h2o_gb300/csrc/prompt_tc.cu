@@ -22,6 +22,7 @@
 // (so pass 2 and every reader of the column sums see the failure), waits
 // (bounded) for its copies in flight, frees its TMEM and returns.
 #include <cuda.h>
+#include <algorithm>
 #include <cfloat>
 #include <cstddef>
 
@@ -265,19 +266,39 @@ __device__ __forceinline__ void tc_mma_loop(TcSmem& S, uint32_t tbase, int ntile
     }
 }
 
+// ------------------------------------------------------- CTA schedule
+
+// CTA x -> (unit u, block rank k): units go in groups of g, and within a
+// group the k-th heaviest block of every unit comes before the (k+1)-th.  A
+// group's blocks all sweep the same K (pass 1) or Q (pass 2) tiles of its g
+// units, so with g about the number of resident CTAs over the blocks per
+// unit those tiles are read from HBM about once and then served by L2,
+// while the heaviest blocks still start first.
+__device__ __forceinline__ void group_order(int x, int U, int nb, int g, int& u, int& k)
+{
+    const int grp = x / (g * nb);
+    const int u0 = grp * g;
+    const int gs = min(g, U - u0);
+    const int r = x - grp * g * nb;
+    k = r / gs;
+    u = u0 + r % gs;
+}
+
 // ------------------------------------------------------------- pass 1
 
-// grid: U * nb CTAs; CTA x handles row block ib = nb - 1 - x / U of unit
-// x % U (heaviest blocks first)
+// grid: U * nb CTAs (or U * nq for the last nq blocks, with g = U); CTA x
+// handles row block ib = nb - 1 - k of unit u (group_order)
 __global__ void __launch_bounds__(kThreads, 2)
     rowstats_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK, int U,
-                       int G, int T, int nb, float c2, float* __restrict__ m2, float* __restrict__ lout, int* err)
+                       int G, int T, int nb, int g, float c2, float* __restrict__ m2, float* __restrict__ lout,
+                       int* err)
 {
     extern __shared__ unsigned char smem_raw[];
     TcSmem& S = tc_smem(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int u = blockIdx.x % U;
-    const int ib = nb - 1 - (int)(blockIdx.x / U);
+    int u, k;
+    group_order((int)blockIdx.x, U, nb, g, u, k);
+    const int ib = nb - 1 - k;
     const int row0 = u * T, krow0 = (u / G) * T;   // query rows, key rows
     const int ntiles = ib + 1;
     tc_setup(S, warp);
@@ -357,19 +378,23 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 // ------------------------------------------------------------- pass 2
 
-// grid: U * nb CTAs; CTA x handles key block jb = x / U of unit x % U
-// (heaviest blocks, small jb, first) and sweeps query blocks jb..nb-1
+// grid: U * nb CTAs; CTA x handles key block jb = k of unit u
+// (group_order: heaviest blocks, small jb, first within a group of units)
+// and sweeps query blocks jb..nb-1.
+// BAND: also the band sums of the per-head policy profile (a separate
+// instantiation, so the plain pass carries none of their instructions).
+template <bool BAND>
 __global__ void __launch_bounds__(kThreads, 2)
     colsum_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK, int U,
-                     int G, int T, int nb, float c2, const float* __restrict__ m2, const float* __restrict__ lin,
-                     double* __restrict__ cout, double* __restrict__ bandB, double* __restrict__ bandr, int wB,
-                     int wr, int* err)
+                     int G, int T, int nb, int g, float c2, const float* __restrict__ m2,
+                     const float* __restrict__ lin, double* __restrict__ cout, double* __restrict__ bandB,
+                     double* __restrict__ bandr, int wB, int wr, int* err)
 {
     extern __shared__ unsigned char smem_raw[];
     TcSmem& S = tc_smem(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int u = blockIdx.x % U;
-    const int jb = (int)(blockIdx.x / U);
+    int u, jb;
+    group_order((int)blockIdx.x, U, nb, g, u, jb);
     const int row0 = u * T, krow0 = (u / G) * T;   // query rows, key rows
     const int ntiles = nb - jb;
     const float* m2u = m2 + (size_t)u * T;
@@ -399,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int b = t & 1;
             const int ib = jb + t;
             // some key of the block has rows of this tile in its band
-            const bool band = bandB && ib * kT < (jb + 1) * kT + wmax;
+            const bool band = BAND && ib * kT < (jb + 1) * kT + wmax;
             // the next tile's statistics, stored after this tile
             float nm = 0.f, nl = 0.f;
             const int inext = (ib + 1) * kT + et;
@@ -471,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             const bool ab = aborted(S);
             const double nan = __longlong_as_double(0x7ff8000000000000LL);
             cout[(size_t)u * T + j] = ab ? nan : (double)cs - (double)cc;
-            if (bandB) {
+            if constexpr (BAND) {
                 bandB[(size_t)u * T + j] = ab ? nan : bsB;
                 bandr[(size_t)u * T + j] = ab ? nan : bsr;
             }
@@ -600,6 +625,24 @@ bool make_map(CUtensorMap* m, const void* base, long long rows)
 
 bool prompt_tc_supported(const CacheView& c) { return c.dtype == 1 && c.D == kD; }
 
+namespace {
+
+// SM count of the current device (cached per device)
+int sm_count()
+{
+    static int n[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!n[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        n[dev] = v;
+    }
+    return n[dev];
+}
+
+}  // namespace
+
 cudaError_t launch_prompt_stats_tc(const CacheView& c, const PromptArgs& p, cudaStream_t st)
 {
     CUtensorMap mq, mk;
@@ -615,17 +658,25 @@ cudaError_t launch_prompt_stats_tc(const CacheView& c, const PromptArgs& p, cuda
     if (!configured[dev]) {
         e = cudaFuncSetAttribute(rowstats_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(colsum_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(colsum_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(colsum_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
     const int nb = (p.T + kT - 1) / kT;
     const unsigned grid = (unsigned)(c.U * nb);
-    rowstats_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, c.U, G, p.T, nb, c.qscale, p.m2, p.l, c.err);
+    // units per schedule group: the resident CTAs (2 per SM) over the blocks per unit
+    const int g = std::max(1, std::min(c.U, 2 * sm_count() / nb));
+    rowstats_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, c.U, G, p.T, nb, g, c.qscale, p.m2, p.l, c.err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    colsum_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, c.U, G, p.T, nb, c.qscale, p.m2, p.l, p.c, p.bandB,
-                                                   p.bandr, p.wB, p.wr, c.err);
+    if (p.bandB)
+        colsum_tc_kernel<true><<<grid, kThreads, smem, st>>>(mq, mk, c.U, G, p.T, nb, g, c.qscale, p.m2, p.l, p.c,
+                                                             p.bandB, p.bandr, p.wB, p.wr, c.err);
+    else
+        colsum_tc_kernel<false><<<grid, kThreads, smem, st>>>(mq, mk, c.U, G, p.T, nb, g, c.qscale, p.m2, p.l, p.c,
+                                                              nullptr, nullptr, 0, 0, c.err);
     return cudaGetLastError();
 }
 
@@ -654,8 +705,8 @@ cudaError_t launch_sh_flags_tc(const CacheView& c, const PromptArgs& p, cudaStre
     const int nb = (p.T + kT - 1) / kT;
     const int w0 = p.T > 32 ? p.T - 32 : 0;
     const int qb0 = w0 / kT, nq = nb - qb0;
-    rowstats_tc_kernel<<<(unsigned)(c.U * nq), kThreads, smem, st>>>(mq, mk, c.U, 1, p.T, nb, c.qscale, p.m2, p.l,
-                                                                     c.err);
+    rowstats_tc_kernel<<<(unsigned)(c.U * nq), kThreads, smem, st>>>(mq, mk, c.U, 1, p.T, nb, c.U, c.qscale, p.m2,
+                                                                     p.l, c.err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     sh_flags_tc_kernel<<<(unsigned)(c.U * nb), kThreads, smem, st>>>(mq, mk, c.U, p.T, nb, qb0, c.qscale, p.m2, p.l,
