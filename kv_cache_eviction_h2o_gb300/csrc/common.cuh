@@ -276,14 +276,17 @@ __device__ __forceinline__ uint32_t q8_pack4(const float* x, float inv)
 }
 
 // Four int8 codes (little-endian in w) -> fp32, exactly: each biased byte
-// becomes the low mantissa byte of 2^23, and the bias is subtracted.
+// becomes the low mantissa byte of 2^23, and the bias (2^23 + 128) is
+// subtracted two values at a time.
 __device__ __forceinline__ void q8_unpack4(uint32_t w, float* f)
 {
     const uint32_t x = w ^ 0x80808080u;
-    f[0] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540)) - 8388736.f;
-    f[1] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7541)) - 8388736.f;
-    f[2] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7542)) - 8388736.f;
-    f[3] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7543)) - 8388736.f;
+    const float2 nb = make_float2(-8388736.f, -8388736.f);
+    const float2 lo = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540)),
+                                             __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7541))), nb);
+    const float2 hi = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7542)),
+                                             __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7543))), nb);
+    f[0] = lo.x; f[1] = lo.y; f[2] = hi.x; f[3] = hi.y;
 }
 
 // Named CTA barriers (ids 1..15; id 0 is __syncthreads).  Memory

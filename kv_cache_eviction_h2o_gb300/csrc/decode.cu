@@ -449,6 +449,21 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, Q8>& S, const 
     const int r = lane & 15, h = lane >> 4;
     const int nst = (f1 - f0 + kStage - 1) / kStage;
     bool timed_out = false;
+    // odd rows of every stage accumulate into o2 (merged into o at the end),
+    // which halves the dependent multiply-add chain of a stage
+    float o2[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o2[e] = 0.f;
+    auto vfma = [&](float p, const float* vr, bool odd) {
+        const float2 pj = make_float2(p, p);
+#pragma unroll
+        for (int e = 0; e < EPL; e += 2) {
+            float* acc = odd ? o2 : o;
+            const float2 r = fma2(pj, make_float2(vr[e], vr[e + 1]), make_float2(acc[e], acc[e + 1]));
+            acc[e] = r.x;
+            acc[e + 1] = r.y;
+        }
+    };
     int it = 0;
     for (int g = warp; g < nst; g += NW, ++it) {
         const int b = it % NBUF;
@@ -473,7 +488,10 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, Q8>& S, const 
                 const float alpha = safe_exp2_diff(m_ref, zm);
                 l_lane *= alpha;
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) o[e] *= alpha;
+                for (int e = 0; e < EPL; ++e) {
+                    o[e] *= alpha;
+                    o2[e] *= alpha;
+                }
                 m_ref = zm;
             }
             const float er = safe_exp2_diff(z, m_ref);
@@ -492,24 +510,31 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, Q8>& S, const 
                 ev[j] = e4.x; ev[j + 1] = e4.y; ev[j + 2] = e4.z; ev[j + 3] = e4.w;
             }
             if constexpr (Q8) {
-                // int8 values (weights already carry the V scales)
+                // int8 values (weights already carry the V scales); a full
+                // stage loads each half's code words before the first
+                // widening, as the bf16 path does
+                auto v_word = [&](int j) -> uint32_t {
+                    if constexpr (EPL == 4) return *reinterpret_cast<const uint32_t*>(vst + j * D + lane * EPL);
+                    else return (uint32_t)*reinterpret_cast<const uint16_t*>(vst + j * D + lane * EPL);
+                };
+                auto v_acc = [&](uint32_t w, float p, bool odd) {
+                    float vr[4];
+                    q8_unpack4(w, vr);
+                    vfma(p, vr, odd);
+                };
+                if (gl == kStage) {
 #pragma unroll
-                for (int j = 0; j < kStage; ++j) {
-                    if (j < gl) {
-                        float vr[4];
-                        if constexpr (EPL == 4) {
-                            q8_unpack4(*reinterpret_cast<const uint32_t*>(vst + j * D + lane * EPL), vr);
-                        } else {
-                            q8_unpack4((uint32_t)*reinterpret_cast<const uint16_t*>(vst + j * D + lane * EPL), vr);
-                        }
-                        const float2 pj = make_float2(ev[j], ev[j]);
+                    for (int j0 = 0; j0 < kStage; j0 += kStage / 2) {
+                        uint32_t vw[kStage / 2];
 #pragma unroll
-                        for (int e = 0; e < EPL; e += 2) {
-                            const float2 acc = fma2(pj, make_float2(vr[e], vr[e + 1]), make_float2(o[e], o[e + 1]));
-                            o[e] = acc.x;
-                            o[e + 1] = acc.y;
-                        }
+                        for (int j = 0; j < kStage / 2; ++j) vw[j] = v_word(j0 + j);
+#pragma unroll
+                        for (int j = 0; j < kStage / 2; ++j) v_acc(vw[j], ev[j0 + j], j & 1);
                     }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < kStage; ++j)
+                        if (j < gl) v_acc(v_word(j), ev[j], j & 1);
                 }
             } else {
             using RV = typename RawT<EPL * sizeof(T)>::type;
@@ -527,13 +552,7 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, Q8>& S, const 
                     for (int j = 0; j < kStage / 2; ++j) {
                         float vr[EPL];
                         widen_raw<T, EPL>(vraw[j], vr);
-                        const float2 pj = make_float2(ev[j0 + j], ev[j0 + j]);
-#pragma unroll
-                        for (int e = 0; e < EPL; e += 2) {
-                            const float2 acc = fma2(pj, make_float2(vr[e], vr[e + 1]), make_float2(o[e], o[e + 1]));
-                            o[e] = acc.x;
-                            o[e + 1] = acc.y;
-                        }
+                        vfma(ev[j0 + j], vr, j & 1);
                     }
                 }
             } else {
@@ -542,13 +561,7 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, Q8>& S, const 
                     if (j < gl) {
                         float vr[EPL];
                         load_vec<T, EPL>(vst + j * D + lane * EPL, vr);
-                        const float2 pj = make_float2(ev[j], ev[j]);
-#pragma unroll
-                        for (int e = 0; e < EPL; e += 2) {
-                            const float2 acc = fma2(pj, make_float2(vr[e], vr[e + 1]), make_float2(o[e], o[e + 1]));
-                            o[e] = acc.x;
-                            o[e + 1] = acc.y;
-                        }
+                        vfma(ev[j], vr, j & 1);
                     }
                 }
             }
@@ -561,6 +574,8 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, Q8>& S, const 
             if (gn < nst) issue_stage<T, D, TL, Q8>(S, Kc, Vc, Sc, f0 + gn * kStage, f1, b);
         }
     }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] += o2[e];
 }
 
 // Kick off ring buffers [b_lo, b_hi) of each warp -- by default all NBUF --
@@ -1275,6 +1290,10 @@ using TileDefault = Tile<6, 2>;
 // per unit) stream with 8 warps; very many units with 4 warps x 3 stages
 using TileFew = Tile<8, 2>;
 using TileMany = Tile<4, 3>;
+// int8 rows: a stage holds the same 16 slots in half the bytes, so twice the
+// stages keep as many bytes in flight as the bf16 tiles
+using TileQ8 = Tile<5, 4>;
+using TileQ8Few = Tile<8, 4>;
 
 // Tile for bf16 rows of 128 (numbers as H2O_DECODE_TILE): TileFew when the
 // units do not fill the SMs, TileMany from four units per SM on, else the
@@ -1377,13 +1396,17 @@ cudaError_t dispatch(const DecodeArgs& a, int split, cudaStream_t st)
         }
     }
     if (a.c.kv8) {
-        // int8 cache rows (default tile)
+        // int8 cache rows: one CTA per SM with 8 warps when the units do not
+        // fill the SMs (bf16 rows of 128), else 5 warps x 4 stages (two CTAs
+        // per SM: 6 x 4 would not fit twice)
+        if (a.c.D == 128 && bf && a.num_sms > 0 && a.c.U < a.num_sms)
+            return launch_decode_t<__nv_bfloat16, 128, LSH, TileQ8Few, true>(a, split, st);
         if (a.c.D == 128)
-            return bf ? launch_decode_t<__nv_bfloat16, 128, LSH, TileDefault, true>(a, split, st)
-                      : launch_decode_t<float, 128, LSH, TileDefault, true>(a, split, st);
+            return bf ? launch_decode_t<__nv_bfloat16, 128, LSH, TileQ8, true>(a, split, st)
+                      : launch_decode_t<float, 128, LSH, TileQ8, true>(a, split, st);
         if (a.c.D == 64)
-            return bf ? launch_decode_t<__nv_bfloat16, 64, LSH, TileDefault, true>(a, split, st)
-                      : launch_decode_t<float, 64, LSH, TileDefault, true>(a, split, st);
+            return bf ? launch_decode_t<__nv_bfloat16, 64, LSH, TileQ8, true>(a, split, st)
+                      : launch_decode_t<float, 64, LSH, TileQ8, true>(a, split, st);
         return cudaErrorInvalidValue;
     }
     if (a.c.D == 128 && bf) {
@@ -1429,15 +1452,16 @@ int max_decode_split() { return kMaxSplit; }
 
 namespace {
 
-// Largest number of clusters of `split` CTAs of the TileFew H2O or HashEvict
-// kernel (bf16, head_dim 128) that the device runs at once; 0 on error.
-int clusters_that_fit(int split, bool lsh)
+// Largest number of clusters of `split` CTAs of the few-units H2O or
+// HashEvict kernel (bf16, head_dim 128; TileFew, or TileQ8Few for int8
+// rows) that the device runs at once; 0 on error.
+template <class TL, bool Q8>
+int clusters_that_fit_t(int split, bool lsh)
 {
-    using TL = TileFew;
     void (*kern)(const DecodeArgs);
-    if (lsh) kern = lsh_decode_kernel<__nv_bfloat16, 128, TL, false>;
-    else kern = h2o_decode_kernel<__nv_bfloat16, 128, TL, false, false>;
-    const size_t smem = sizeof(DecodeSmem<__nv_bfloat16, 128, TL, false>);
+    if (lsh) kern = lsh_decode_kernel<__nv_bfloat16, 128, TL, Q8>;
+    else kern = h2o_decode_kernel<__nv_bfloat16, 128, TL, Q8, false>;
+    const size_t smem = sizeof(DecodeSmem<__nv_bfloat16, 128, TL, Q8>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
         cudaGetLastError();
@@ -1462,6 +1486,11 @@ int clusters_that_fit(int split, bool lsh)
     return n;
 }
 
+int clusters_that_fit(int split, bool lsh, bool q8)
+{
+    return q8 ? clusters_that_fit_t<TileQ8Few, true>(split, lsh) : clusters_that_fit_t<TileFew, false>(split, lsh);
+}
+
 }  // namespace
 
 // Decode split for a bf16, head_dim 128 one-head H2O or HashEvict cache with
@@ -1469,9 +1498,10 @@ int clusters_that_fit(int split, bool lsh)
 // per unit with all U clusters resident at once (clusters are placed within
 // a GPC, so U * split <= num_sms alone does not ensure it), at least one
 // CTA per 1024 slots.  Results are cached per (device, U, B, kernel).
-int few_units_split(int U, int B, int num_sms, bool lsh)
+int few_units_split(int U, int B, int num_sms, bool lsh, bool q8)
 {
     struct Entry { int dev, U, B, lsh, split; };
+    const int key = (lsh ? 1 : 0) | (q8 ? 2 : 0);
     static std::mutex mu;
     static Entry cache[64];
     static int n_cache = 0;
@@ -1480,15 +1510,15 @@ int few_units_split(int U, int B, int num_sms, bool lsh)
     {
         std::lock_guard<std::mutex> lock(mu);
         for (int i = 0; i < n_cache; ++i)
-            if (cache[i].dev == dev && cache[i].U == U && cache[i].B == B && cache[i].lsh == (int)lsh)
+            if (cache[i].dev == dev && cache[i].U == U && cache[i].B == B && cache[i].lsh == key)
                 return cache[i].split;
     }
     const int lo = max(1, (B + kMaxChunk - 1) / kMaxChunk);
     const int hi = max(1, (B + 63) / 64);
     int s = min(kMaxSplit, min(hi, max(lo, num_sms / max(U, 1))));
-    while (s > lo && clusters_that_fit(s, lsh) < U) --s;
+    while (s > lo && clusters_that_fit(s, lsh, q8) < U) --s;
     std::lock_guard<std::mutex> lock(mu);
-    if (n_cache < 64) cache[n_cache++] = Entry{dev, U, B, (int)lsh, s};
+    if (n_cache < 64) cache[n_cache++] = Entry{dev, U, B, key, s};
     return s;
 }
 

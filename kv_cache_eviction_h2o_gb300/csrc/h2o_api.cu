@@ -386,9 +386,9 @@ int decode_split(const h2o_ctx* h)
     int s;
     if (h->split > 0)
         s = h->split;
-    else if (h->dtype == H2O_BF16 && h->D == 128 && !h->kv8 && h->G == 1 && (h->kind == kH2O || h->kind == kLSH) &&
+    else if (h->dtype == H2O_BF16 && h->D == 128 && h->G == 1 && (h->kind == kH2O || h->kind == kLSH) &&
              h->U < h->num_sms)
-        s = few_units_split(h->U, h->B, h->num_sms, h->kind == kLSH);
+        s = few_units_split(h->U, h->B, h->num_sms, h->kind == kLSH, h->kv8 != 0);
     else
         s = auto_decode_split(h->U, h->B, h->num_sms);
     const int lo = (h->B + 1023) / 1024;

@@ -74,7 +74,8 @@ cudaError_t launch_lsh_decode(const DecodeArgs& a, int split, cudaStream_t st);
 cudaError_t launch_sh_decode(const DecodeArgs& a, int split, cudaStream_t st);
 int auto_decode_split(int U, int B, int num_sms);
 // split of a bf16, head_dim 128 one-head H2O / HashEvict cache with U < SMs
-int few_units_split(int U, int B, int num_sms, bool lsh);
+// (q8: int8 rows)
+int few_units_split(int U, int B, int num_sms, bool lsh, bool q8);
 int max_decode_split();
 
 cudaError_t launch_prompt_stats(const CacheView& c, const PromptArgs& p, cudaStream_t st);
