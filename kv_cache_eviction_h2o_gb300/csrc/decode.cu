@@ -26,6 +26,7 @@
 #include <cfloat>
 #include <climits>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <type_traits>
 
@@ -1037,6 +1038,431 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     finish(S.victim, make_float2(S.P_new, 0.f));
 }
 
+// ------------------------------------------------------------ grouped query
+//
+// Grouped-query H2O step in one pass over each cache unit's rows for all of
+// its G query heads [H2O review page, 提案手法; the grouped form is this
+// library's reading: a slot's score grows by the sum of its G heads'
+// probabilities, added in head order].  A CTA -- or a cluster of C CTAs
+// splitting the unit's slots -- has NW = G * NG warps: stage group sg takes
+// the 16-slot stages sg, sg + NG, ... of the CTA's slots, and its G warps,
+// one per head, read each stage from a ring the group shares (filled by the
+// group's head-0 warp with 1-D bulk copies; a full and an empty mbarrier per
+// buffer, G arrivals on the empty one).  Every K and V row therefore crosses
+// from L2 once per unit, not once per head.  Each warp keeps its head's
+// online softmax and logits; after the stream the heads' states are merged
+// per head (and across the cluster), one score pass adds the G
+// probabilities to each slot, and one arg-min and insert follow.
+
+template <int G>
+struct GqaShape {
+    static constexpr int NW = 8;                          // warps
+    static constexpr int NG = NW / G;                     // stage groups
+    static constexpr int NT = 32 * NW;
+    // about 128 KB of stages in flight per CTA (one CTA per SM: registers)
+    static constexpr int NBUF = 16 / NG;
+    static constexpr int CMAX = 32 / G;                   // the exchange holds C * G <= 32 head states
+    static constexpr int SPT = (kMaxChunk + NT - 1) / NT;
+    static_assert(NW % G == 0, "heads divide the warps");
+};
+
+// cluster exchange of the grouped-query kernel: every CTA's per-head max
+// and normaliser (index rank * G + head), outputs gathered in rank 0, and
+// the CTAs' arg-min keys
+template <int D>
+struct GqaExchange {
+    float m[32];
+    float l[32];
+    unsigned am[2][3][kMaxSplit];
+    float o[32][D];
+};
+
+template <typename T, int D, int G>
+struct GqaSmem {
+    using SH = GqaShape<G>;
+    union {
+        struct {
+            T kbuf[SH::NG][SH::NBUF][kStage * D];
+            T vbuf[SH::NG][SH::NBUF][kStage * D];
+        } ring;
+        float wo[SH::NW][D];                  // per-warp outputs at the merge
+    } u;
+    GqaExchange<D> x;
+    alignas(16) unsigned char in[G + 2][D * sizeof(T)];   // the G heads' q, then k, v
+    uint64_t full[SH::NG][SH::NBUF];
+    uint64_t empty[SH::NG][SH::NBUF];
+    float z[G][kMaxChunk];                    // base-2 logits of this CTA's slots, per head
+    alignas(16) float e[SH::NW][kStage];
+    float wm[SH::NW], wl[SH::NW];
+    float hm[G], hl[G];                       // this CTA's per-head max and normaliser
+    float M[G], invL[G];                      // per-head max and 1 / normaliser over the unit
+    float zn[G];                              // the new token's logit per head
+    unsigned am[2][3][SH::NW];
+    float2 P_new;                             // the new token's score: its G probabilities
+    int victim;
+};
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(GqaShape<G>::NT, 1) gqa_decode_kernel(const DecodeArgs a)
+{
+    using SH = GqaShape<G>;
+    constexpr int EPL = D / 32, NV = D * (int)sizeof(T) / 16, NW = SH::NW, NG = SH::NG, NBUF = SH::NBUF;
+    constexpr int NT = SH::NT, SPT = SH::SPT;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    auto& S = *reinterpret_cast<GqaSmem<T, D, G>*>(smem_raw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int head = warp % G, sg = warp / G;
+    const bool leader = (head == 0);          // refills its group's ring
+    const int r = lane & 15, hh = lane >> 4;
+    const CacheView& c = a.c;
+    const int C = (int)cluster_nctarank(), rank = (int)cluster_ctarank();
+    const int unit = blockIdx.x / C;
+    const int B = c.B;
+    const size_t ub = (size_t)unit * B;
+    T* Kc = reinterpret_cast<T*>(c.K) + ub * D;
+    T* Vc = reinterpret_cast<T*>(c.V) + ub * D;
+    int f0, f1;
+    fetch_range(B, C, rank, f0, f1);
+    const int nst = (f1 - f0 + kStage - 1) / kStage;
+    if (leader && lane == 0) {
+#pragma unroll
+        for (int b = 0; b < NBUF; ++b) {
+            mbar_init(&S.full[sg][b], 1);
+            mbar_init(&S.empty[sg][b], G);
+        }
+        if (C > 1) fence_mbar_init(); else fence_proxy_async_smem();
+    }
+    if (C > 1) cluster_arrive_relaxed();      // paired with the wait before the exchange
+    const T* qg = reinterpret_cast<const T*>(a.q) + (size_t)unit * G * D;
+    const T* kg = reinterpret_cast<const T*>(a.k) + (size_t)unit * D;
+    const T* vg = reinterpret_cast<const T*>(a.v) + (size_t)unit * D;
+    {
+        // the input rows' lines on their way to L2 before the wait
+        constexpr int lines = (D * (int)sizeof(T) + 127) / 128;
+        if (tid < (G + 2) * lines) {
+            const int row = tid / lines, l = tid - row * lines;
+            const T* base = row < G ? qg + (size_t)row * D : (row == G ? kg : vg);
+            prefetch_l2(reinterpret_cast<const char*>(base) + 128 * l);
+        }
+    }
+    __syncthreads();                          // the group barriers are initialised
+    // stage j (CTA-relative) of group sg into buffer b
+    auto issue = [&](int j, int b) {
+        const int s = f0 + j * kStage;
+        const int rows = min(kStage, f1 - s);
+        const uint32_t bytes = (uint32_t)(rows * D * sizeof(T));
+        mbar_arrive_expect_tx(&S.full[sg][b], 2 * bytes);
+        bulk_g2s(S.u.ring.kbuf[sg][b], Kc + (size_t)s * D, bytes, &S.full[sg][b]);
+        bulk_g2s(S.u.ring.vbuf[sg][b], Vc + (size_t)s * D, bytes, &S.full[sg][b]);
+    };
+    auto prime = [&](int b_lo, int b_hi) {
+        for (int b = b_lo; b < b_hi; ++b) {
+            const int j = sg + NG * b;
+            if (j < nst) issue(j, b);
+        }
+    };
+    int2 us = make_int2(0, 0);
+    float2 sc_old[SPT];
+    int ps[SPT];
+    auto read_cache = [&]() {
+        us = c.ustate[unit];
+#pragma unroll
+        for (int i = 0; i < SPT; ++i) {
+            const int s = f0 + tid + i * NT;
+            sc_old[i] = make_float2(0.f, 0.f);
+            ps[i] = 0;
+            if (s < f1) {
+                sc_old[i] = ld_issue_f2(c.score + ub + s);
+                ps[i] = (int)ld_issue_u32(reinterpret_cast<const uint32_t*>(c.pos + ub + s));
+            }
+        }
+    };
+    if (a.early) {
+        if (leader && lane == 0) prime(0, 1);
+        read_cache();
+    }
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (!a.early) {
+        if (leader && lane == 0) prime(0, NBUF);
+        read_cache();
+    }
+    {
+        // the G heads' q, k and v in one round trip
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (tid < (G + 2) * NV) {
+            const int row = tid / NV;
+            const T* base = row < G ? qg + (size_t)row * D : (row == G ? kg : vg);
+            w = reinterpret_cast<const uint4*>(base)[tid - row * NV];
+        }
+        if (a.early && leader && lane == 0) prime(1, NBUF);
+        if (tid < (G + 2) * NV) reinterpret_cast<uint4*>(S.in[tid / NV])[tid % NV] = w;
+    }
+    __syncthreads();
+    const T* qs = reinterpret_cast<const T*>(S.in[head]);
+    const T* ks = reinterpret_cast<const T*>(S.in[G]);
+    const T* vs = reinterpret_cast<const T*>(S.in[G + 1]);
+    float qp[D / 2];
+    {
+        QRaw<T, D> qraw;
+        load_q_raw<T, D>(qs, lane, qraw);
+        widen_q<T, D>(qraw, c.qscale, qp);
+    }
+    uint4 newrow = make_uint4(0u, 0u, 0u, 0u);       // k then v (adjacent rows of S.in)
+    if (rank == 0 && tid < 2 * NV) newrow = reinterpret_cast<const uint4*>(S.in[G])[tid];
+    const int n = us.x, p = us.y;
+    const bool full = (n >= B);
+    const int c1 = min(n, f1);
+
+    float m_ref = -INFINITY, l_lane = 0.f, o[EPL], o2[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) { o[e] = 0.f; o2[e] = 0.f; }
+    if (rank == 0 && sg == 0) {              // each head's new token attends to itself
+        const float zn = row_dot<T, D, T>(ks, qp, lane);
+        float vr[EPL];
+        load_vec<T, EPL>(vs + lane * EPL, vr);
+        m_ref = zn;
+        l_lane = lane == 0 ? 1.f : 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[e] = vr[e];
+        if (lane == 0) S.zn[head] = zn;
+    }
+    __syncwarp();
+    auto vfma = [&](float pw, const float* vr, bool odd) {
+        const float2 pj = make_float2(pw, pw);
+#pragma unroll
+        for (int e = 0; e < EPL; e += 2) {
+            float* acc = odd ? o2 : o;
+            const float2 rr = fma2(pj, make_float2(vr[e], vr[e + 1]), make_float2(acc[e], acc[e + 1]));
+            acc[e] = rr.x;
+            acc[e + 1] = rr.y;
+        }
+    };
+    bool timed_out = false;
+    int it = 0;
+    for (int j = sg; j < nst; j += NG, ++it) {
+        const int b = it % NBUF;
+        const uint32_t par = (uint32_t)(it / NBUF) & 1u;
+        if (!mbar_wait(&S.full[sg][b], par)) {
+            if (!timed_out && lane == 0) atomicOr(c.err, kErrWaitTimeout);
+            timed_out = true;
+        }
+        const int s0 = j * kStage;                         // CTA-relative first slot
+        const int gl = max(0, min(kStage, n - (f0 + s0)));  // live rows of this stage
+        if (gl > 0) {
+            const T* kst = S.u.ring.kbuf[sg][b];
+            const T* vst = S.u.ring.vbuf[sg][b];
+            float z = row_dot<T, D, T>(kst + r * D, qp, lane);
+            if (r >= gl) z = -INFINITY;
+            if (__any_sync(kFull, z > m_ref + 8.f)) {
+                float zm = z;
+#pragma unroll
+                for (int sh = 1; sh < 16; sh <<= 1) zm = fmaxf(zm, __shfl_xor_sync(kFull, zm, sh));
+                const float alpha = safe_exp2_diff(m_ref, zm);
+                l_lane *= alpha;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) {
+                    o[e] *= alpha;
+                    o2[e] *= alpha;
+                }
+                m_ref = zm;
+            }
+            const float er = safe_exp2_diff(z, m_ref);
+            if (hh == 0) {
+                l_lane += er;
+                S.e[warp][r] = er;
+                if (r < gl) S.z[head][s0 + r] = z;
+            }
+            __syncwarp();
+            float ev[kStage];
+#pragma unroll
+            for (int q4 = 0; q4 < kStage; q4 += 4) {
+                const float4 e4 = *reinterpret_cast<const float4*>(&S.e[warp][q4]);
+                ev[q4] = e4.x; ev[q4 + 1] = e4.y; ev[q4 + 2] = e4.z; ev[q4 + 3] = e4.w;
+            }
+            using RV = typename RawT<EPL * sizeof(T)>::type;
+            if (gl == kStage) {
+#pragma unroll
+                for (int j0 = 0; j0 < kStage; j0 += kStage / 2) {
+                    RV vraw[kStage / 2];
+#pragma unroll
+                    for (int jj = 0; jj < kStage / 2; ++jj)
+                        vraw[jj] = *reinterpret_cast<const RV*>(vst + (j0 + jj) * D + lane * EPL);
+#pragma unroll
+                    for (int jj = 0; jj < kStage / 2; ++jj) {
+                        float vr[EPL];
+                        widen_raw<T, EPL>(vraw[jj], vr);
+                        vfma(ev[j0 + jj], vr, jj & 1);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < kStage; ++jj) {
+                    if (jj < gl) {
+                        float vr[EPL];
+                        load_vec<T, EPL>(vst + jj * D + lane * EPL, vr);
+                        vfma(ev[jj], vr, jj & 1);
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        // this head is done with the buffer; the group's head-0 warp refills
+        // it once every head has released it
+        if (lane == 0) mbar_arrive_one(&S.empty[sg][b]);
+        if (leader && lane == 0) {
+            const int jn = j + NG * NBUF;
+            if (jn < nst) {
+                if (!mbar_wait(&S.empty[sg][b], par)) {
+                    if (!timed_out) atomicOr(c.err, kErrWaitTimeout);
+                    timed_out = true;
+                }
+                issue(jn, b);
+            }
+        }
+        __syncwarp();
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] += o2[e];
+
+    // merge: per head over the stage groups (and then the cluster)
+    const float l_warp = warp_sum(l_lane);
+    __syncthreads();                          // every warp is past the ring the outputs overlay
+    if (lane == 0) { S.wm[warp] = m_ref; S.wl[warp] = l_warp; }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) S.u.wo[warp][lane * EPL + e] = o[e];
+    __syncthreads();
+    if (tid < G) {
+        float mx = -INFINITY, lx = 0.f;
+        for (int q = 0; q < NG; ++q) mx = fmaxf(mx, S.wm[q * G + tid]);
+        for (int q = 0; q < NG; ++q) lx += S.wl[q * G + tid] * safe_exp2_diff(S.wm[q * G + tid], mx);
+        S.hm[tid] = mx;
+        S.hl[tid] = lx;
+    }
+    __syncthreads();
+    const uint32_t x0 = map_to_rank(&S.x, 0);
+    if (C > 1) {
+        cluster_wait();                      // every CTA of the cluster runs (arrive at the start)
+        const uint32_t off_m = (uint32_t)offsetof(GqaExchange<D>, m), off_l = (uint32_t)offsetof(GqaExchange<D>, l);
+        const uint32_t off_o = (uint32_t)offsetof(GqaExchange<D>, o);
+        for (int idx = tid; idx < G * D; idx += NT) {
+            const int g = idx / D, e = idx - g * D;
+            float oc = 0.f;
+            for (int q = 0; q < NG; ++q) oc += S.u.wo[q * G + g][e] * safe_exp2_diff(S.wm[q * G + g], S.hm[g]);
+            st_cluster_f32(x0 + off_o + (uint32_t)(((rank * G + g) * D + e) * 4), oc);
+        }
+        if (tid < C * G) {
+            const int t = tid / G, g = tid - t * G;
+            const uint32_t xt = map_to_rank(&S.x, (uint32_t)t);
+            st_cluster_f32(xt + off_m + (uint32_t)((rank * G + g) * 4), S.hm[g]);
+            st_cluster_f32(xt + off_l + (uint32_t)((rank * G + g) * 4), S.hl[g]);
+        }
+        cluster_arrive();
+        cluster_wait();
+        if (tid < G) {
+            float mx = -INFINITY, lx = 0.f;
+            for (int t = 0; t < C; ++t) mx = fmaxf(mx, S.x.m[t * G + tid]);
+            for (int t = 0; t < C; ++t) lx += S.x.l[t * G + tid] * safe_exp2_diff(S.x.m[t * G + tid], mx);
+            S.M[tid] = mx;
+            S.invL[tid] = 1.f / lx;
+        }
+        __syncthreads();
+        if (rank == 0) {
+            for (int idx = tid; idx < G * D; idx += NT) {
+                const int g = idx / D, e = idx - g * D;
+                float acc = 0.f;
+                for (int t = 0; t < C; ++t) acc += S.x.o[t * G + g][e] * safe_exp2_diff(S.x.m[t * G + g], S.M[g]);
+                a.out[((size_t)unit * G + g) * D + e] = acc * S.invL[g];
+            }
+        }
+    } else {
+        if (tid < G) {
+            S.M[tid] = S.hm[tid];
+            S.invL[tid] = 1.f / S.hl[tid];
+        }
+        __syncthreads();
+        for (int idx = tid; idx < G * D; idx += NT) {
+            const int g = idx / D, e = idx - g * D;
+            float oc = 0.f;
+            for (int q = 0; q < NG; ++q) oc += S.u.wo[q * G + g][e] * safe_exp2_diff(S.wm[q * G + g], S.M[g]);
+            a.out[((size_t)unit * G + g) * D + e] = oc * S.invL[g];
+        }
+    }
+
+    // accumulate: every live slot gains its G heads' probabilities (head
+    // order); arg-min over candidates (position <= p - r)
+    ArgMin best = argmin_none(), best_all = argmin_none();
+#pragma unroll
+    for (int i = 0; i < SPT; ++i) {
+        const int s = f0 + tid + i * NT;
+        if (s < c1) {
+            float2 ns = sc_old[i];
+#pragma unroll
+            for (int g = 0; g < G; ++g) ns = pair_add(ns, exp2f(S.z[g][s - f0] - S.M[g]) * S.invL[g]);
+            c.score[ub + s] = ns;
+            const ArgMin k = ArgMin{ord_key(ns.x), ord_key(ns.y), (unsigned)s};
+            if (full) {
+                if (ps[i] <= p - c.r) argmin_take(best, k);
+                argmin_take(best_all, k);
+            }
+        }
+    }
+    if (full) {
+        best = warp_argmin(best);
+        best_all = warp_argmin(best_all);
+        if (lane == 0) {
+            S.am[0][0][warp] = best.hi; S.am[0][1][warp] = best.lo; S.am[0][2][warp] = best.slot;
+            S.am[1][0][warp] = best_all.hi; S.am[1][1][warp] = best_all.lo; S.am[1][2][warp] = best_all.slot;
+        }
+    }
+    if (rank == 0 && tid == 0) {
+        float2 pn = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int g = 0; g < G; ++g) pn = pair_add(pn, exp2f(S.zn[g] - S.M[g]) * S.invL[g]);
+        S.P_new = pn;
+    }
+    __syncthreads();
+    if (full && warp == 0) {
+        // this CTA's arg-mins; with C > 1 into rank 0's exchange
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            ArgMin w = lane < NW ? ArgMin{S.am[k][0][lane], S.am[k][1][lane], S.am[k][2][lane]} : argmin_none();
+            w = warp_argmin(w);
+            if (lane == 0) {
+                const uint32_t base = x0 + (uint32_t)offsetof(GqaExchange<D>, am) + (uint32_t)(k * 3 * kMaxSplit * 4);
+                st_cluster_s32(base + rank * 4, (int)w.hi);
+                st_cluster_s32(base + (kMaxSplit + rank) * 4, (int)w.lo);
+                st_cluster_s32(base + (2 * kMaxSplit + rank) * 4, (int)w.slot);
+            }
+        }
+    }
+    cta_group_sync(C);
+    if (rank != 0) return;
+    if (tid == 0) {
+        int victim = n;
+        if (full) {
+            ArgMin vc = argmin_none(), va = argmin_none();
+            for (int t = 0; t < C; ++t) {
+                argmin_take(vc, ArgMin{S.x.am[0][0][t], S.x.am[0][1][t], S.x.am[0][2][t]});
+                argmin_take(va, ArgMin{S.x.am[1][0][t], S.x.am[1][1][t], S.x.am[1][2][t]});
+            }
+            victim = (int)(vc.slot != 0xffffffffu ? vc.slot : va.slot);
+        }
+        if (victim < 0 || victim >= B) victim = 0;
+        S.victim = victim;
+        c.score[ub + victim] = S.P_new;
+        c.pos[ub + victim] = p;
+        c.ustate[unit] = make_int2(min(n + 1, B), p + 1);
+        if (a.victim_out) a.victim_out[unit] = full ? victim : -1;
+    }
+    __syncthreads();
+    const int victim = S.victim;
+    if (tid < NV)
+        reinterpret_cast<uint4*>(Kc + (size_t)victim * D)[tid] = newrow;
+    else if (tid < 2 * NV)
+        reinterpret_cast<uint4*>(Vc + (size_t)victim * D)[tid - NV] = newrow;
+}
+
 // ------------------------------------------------------------------ LSH
 
 template <typename T, int D, class TL, bool Q8>
@@ -1371,13 +1797,78 @@ cudaError_t launch_decode_t(const DecodeArgs& a, int split, cudaStream_t st)
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
+template <typename T, int D, int G>
+cudaError_t launch_gqa_t(const DecodeArgs& a, cudaStream_t st)
+{
+    void (*kern)(const DecodeArgs) = gqa_decode_kernel<T, D, G>;
+    const size_t smem = sizeof(GqaSmem<T, D, G>);
+    static bool configured[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    // CTAs per unit: enough to give every SM one while the exchange holds
+    // their head states, never fewer than one per kMaxChunk slots
+    int split = a.num_sms > 0 ? a.num_sms / max(1, a.c.U) : 1;
+    split = max(split, (a.c.B + kMaxChunk - 1) / kMaxChunk);
+    split = max(1, min(split, GqaShape<G>::CMAX));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.c.U * split), 1, 1);
+    cfg.blockDim = dim3(GqaShape<G>::NT, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    int na = 1;
+    if (split > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)split;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        na = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// the one-pass grouped-query kernel unless H2O_GQA_PATH=cluster (one CTA per
+// query head, kept for comparison)
+bool gqa_one_pass()
+{
+    static int v = -1;
+    if (v < 0) {
+        const char* e = getenv("H2O_GQA_PATH");
+        v = (e && strcmp(e, "cluster") == 0) ? 0 : 1;
+    }
+    return v == 1;
+}
+
 template <bool LSH>
 cudaError_t dispatch(const DecodeArgs& a, int split, cudaStream_t st)
 {
     const bool bf = a.c.dtype == 1;
     if constexpr (!LSH) {
         if (a.G > 1) {
-            // grouped-query cache (default tile): every dtype and row form
+            // one pass over each unit's rows for all heads (bf16 rows of 128,
+            // 2, 4 or 8 heads per unit)
+            // (4 heads on fewer units than half the SMs: the cluster path below
+            // measured faster -- each of its CTAs walks fewer stages)
+            const bool small4 = a.G == 4 && a.num_sms > 0 && 2 * a.c.U < a.num_sms;
+            if (a.c.D == 128 && bf && !a.c.kv8 && gqa_one_pass() && !small4) {
+                if (a.G == 2) return launch_gqa_t<__nv_bfloat16, 128, 2>(a, st);
+                if (a.G == 4) return launch_gqa_t<__nv_bfloat16, 128, 4>(a, st);
+                if (a.G == 8) return launch_gqa_t<__nv_bfloat16, 128, 8>(a, st);
+            }
+            // grouped-query cache (default tile), one CTA per query head: every dtype and row form
             if (a.c.D == 128) {
                 if (a.c.kv8)
                     return bf ? launch_decode_t<__nv_bfloat16, 128, false, TileDefault, true, true>(a, split, st)

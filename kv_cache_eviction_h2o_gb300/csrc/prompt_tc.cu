@@ -150,7 +150,7 @@ __device__ __forceinline__ void tile_mma(uint32_t d_tmem, const uint8_t* a, cons
 struct alignas(1024) TcSmem {
     uint8_t a[kTile];                 // the tile's own block (Q in pass 1, K in pass 2)
     uint8_t b[kStages][kTile];        // ring of the swept blocks
-    alignas(16) float colstat[2][kT];      // pass 2: per accumulator, the 128 queries' m2 + log2(l) (read as float4)
+    alignas(16) float colstat[2][kT];      // pass 2: per accumulator, the 128 queries' -(m2 + log2(l)) (read as float4)
     uint64_t a_full;
     uint64_t b_full[kStages];
     uint64_t b_empty[kStages];
@@ -348,14 +348,18 @@ __global__ void __launch_bounds__(kThreads, 2)
                         lc *= alpha;
                         m = cm;
                     }
-                    float s0 = 0.f, s1 = 0.f;
+                    // exponent arguments and running sums two columns at a time
+                    const float2 c22 = make_float2(c2, c2), nm2 = make_float2(-m, -m);
+                    float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        s0 += ex2_fast(fmaf(v[e], c2, -m));
-                        s1 += ex2_fast(fmaf(v[e + 1], c2, -m));
+                    for (int e = 0; e < 32; e += 4) {
+                        const float2 ta = __ffma2_rn(make_float2(v[e], v[e + 1]), c22, nm2);
+                        const float2 tb = __ffma2_rn(make_float2(v[e + 2], v[e + 3]), c22, nm2);
+                        sa = __fadd2_rn(sa, make_float2(ex2_fast(ta.x), ex2_fast(ta.y)));
+                        sb = __fadd2_rn(sb, make_float2(ex2_fast(tb.x), ex2_fast(tb.y)));
                     }
                     // Kahan step
-                    const float y = (s0 + s1) - lc;
+                    const float y = ((sa.x + sa.y) + (sb.x + sb.y)) - lc;
                     const float tsum = l + y;
                     lc = (tsum - l) - y;
                     l = tsum;
@@ -411,11 +415,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int et = threadIdx.x - 64;          // epilogue thread 0..127
         const int q = warp & 3;
         const int j = jb * kT + 32 * q + lane;    // key within the unit
-        // stage the query statistics of tile 0 as one bias per query,
-        // m2 + log2(l), so a weight is 2^(s c2 - bias); +inf past T (weight 0)
+        // stage the query statistics of tile 0 as one negated bias per query,
+        // -(m2 + log2(l)), so a weight is 2^(s c2 + nbias); -inf past T
+        // (weight 0)
         {
             const int i = jb * kT + et;
-            S.colstat[0][et] = i < T ? m2u[i] + log2f(lu[i]) : INFINITY;
+            S.colstat[0][et] = i < T ? -(m2u[i] + log2f(lu[i])) : -INFINITY;
         }
         float cs = 0.f, cc = 0.f;                 // Kahan-summed column sum
         double bsB = 0.0, bsr = 0.0;              // band sums (rows j .. j+w-1)
@@ -450,22 +455,24 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (ch + 1 < 4) tc_ld32_issue(tcol + (uint32_t)((ch + 1) * 32), nxt);
                 const int i0 = ib * kT + ch * 32;
                 const int dj = i0 - j;                    // i - j of the chunk's first row
-                float p0 = 0.f, p1 = 0.f;
+                const float2 c22 = make_float2(c2, c2);
+                float2 pa = make_float2(0.f, 0.f), pb = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
                     const float4 b4 = *reinterpret_cast<const float4*>(bs + ch * 32 + e);
-                    float w0 = ex2_fast(fmaf(__uint_as_float(cur[e]), c2, -b4.x));
-                    float w1 = ex2_fast(fmaf(__uint_as_float(cur[e + 1]), c2, -b4.y));
-                    float w2 = ex2_fast(fmaf(__uint_as_float(cur[e + 2]), c2, -b4.z));
-                    float w3 = ex2_fast(fmaf(__uint_as_float(cur[e + 3]), c2, -b4.w));
+                    const float2 ta = __ffma2_rn(make_float2(__uint_as_float(cur[e]), __uint_as_float(cur[e + 1])), c22,
+                                                 make_float2(b4.x, b4.y));
+                    const float2 tb = __ffma2_rn(make_float2(__uint_as_float(cur[e + 2]), __uint_as_float(cur[e + 3])),
+                                                 c22, make_float2(b4.z, b4.w));
+                    float w0 = ex2_fast(ta.x), w1 = ex2_fast(ta.y), w2 = ex2_fast(tb.x), w3 = ex2_fast(tb.y);
                     if (edge) {
                         if (i0 + e < j) w0 = 0.f;
                         if (i0 + e + 1 < j) w1 = 0.f;
                         if (i0 + e + 2 < j) w2 = 0.f;
                         if (i0 + e + 3 < j) w3 = 0.f;
                     }
-                    p0 += w0 + w2;
-                    p1 += w1 + w3;
+                    pa = __fadd2_rn(pa, make_float2(w0, w1));
+                    pb = __fadd2_rn(pb, make_float2(w2, w3));
                     if (band) {
                         const int d0 = dj + e;
                         partB += (d0 < wB ? w0 : 0.f) + (d0 + 1 < wB ? w1 : 0.f) + (d0 + 2 < wB ? w2 : 0.f) +
@@ -474,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                                  (d0 + 3 < wr ? w3 : 0.f);
                     }
                 }
-                part += p0 + p1;
+                part += (pa.x + pa.y) + (pb.x + pb.y);
                 if (ch + 1 < 4) tc_ld32_wait(nxt);
             }
             tc_fence_before();
@@ -489,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 bsr += (double)partr;
             }
             // publish the next tile's statistics into the other buffer
-            if (t + 1 < ntiles) S.colstat[b ^ 1][et] = inext < T ? nm + log2f(nl) : INFINITY;
+            if (t + 1 < ntiles) S.colstat[b ^ 1][et] = inext < T ? -(nm + log2f(nl)) : -INFINITY;
         }
         // an abandoned CTA leaves NaN in its columns
         if (j < T) {
