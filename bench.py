@@ -48,19 +48,20 @@ METRIC = "H2O decode steps/s (batch×heads) at 1 GB300; achieved HBM GB/s vs pea
 UNIT = "steps/s"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 
-# name -> (workload, eviction rule, layer caches in rotation).  The layer
-# count keeps the caches plus prompts well above L2 (129 MB) and makes every
-# cache wait for the others before it is read again.
+# name -> (workload, eviction rule, layer caches in rotation, int8 slots).
+# The layer count keeps the caches plus prompts well above L2 (129 MB) and
+# makes every cache wait for the others before it is read again.
 CONFIGS = {
-    "opt-30b": ("opt-30b", "h2o", 2),                       # 2 x 565 MB caches
-    "opt-6.7b": ("opt-6.7b", "h2o", 8),                     # 8 x 113 MB
-    "llama-7b-32k": ("llama-7b-32k", "h2o", 8),             # 8 x 68.7 MB
-    "hashevict-opt-6.7b": ("hashevict-opt-6.7b", "lsh", 8),
-    "gqa-8x8x4": ("gqa-8x8x4", "h2o", 8),
-    "fastgen-opt-6.7b": ("fastgen-opt-6.7b", "fg", 8),         # per-head policies, mixed budgets
+    "opt-30b": ("opt-30b", "h2o", 2, False),                    # 2 x 594 MB caches
+    "opt-6.7b": ("opt-6.7b", "h2o", 8, False),                  # 8 x 113 MB
+    "llama-7b-32k": ("llama-7b-32k", "h2o", 8, False),          # 8 x 70 MB
+    "hashevict-opt-6.7b": ("hashevict-opt-6.7b", "lsh", 8, False),
+    "fastgen-opt-6.7b": ("fastgen-opt-6.7b", "fg", 8, False),   # per-head policies, mixed budgets
+    "gqa-8x8x4": ("gqa-8x8x4", "h2o", 8, False),                # caches shared by 4 query heads
+    "opt-30b-int8": ("opt-30b", "h2o", 2, True),                # the main layer with int8 slots
 }
 DEFAULT_CONFIG = "opt-30b"
-SUB_CONFIGS = ("opt-6.7b", "llama-7b-32k", "hashevict-opt-6.7b", "fastgen-opt-6.7b")
+SUB_CONFIGS = ("opt-6.7b", "llama-7b-32k", "hashevict-opt-6.7b", "fastgen-opt-6.7b", "gqa-8x8x4", "opt-30b-int8")
 
 
 def parse(argv=None):
@@ -392,14 +393,15 @@ def run_reference(args):
         return
     from kv_cache_eviction_h2o_gb300 import workloads as wl
     import oracle
-    wname, rule0, _ = CONFIGS[args.config]
+    wname, rule0, _, kv8_0 = CONFIGS[args.config]
     rule = args.rule or rule0
+    kv8 = args.kv8 or kv8_0
     w = wl.WORKLOADS[wname]
     n = min(w.units, args.oracle_units or max(1, oracle.get_threads()))
     S = args.decode_steps or w.steps
     for _ in range(args.warmup):
-        OracleSample(w, rule, args.kv8, 0, units=n, steps=S)
-    samples = [OracleSample(w, rule, args.kv8, 0, units=n, steps=S) for _ in range(args.steps)]
+        OracleSample(w, rule, kv8, 0, units=n, steps=S)
+    samples = [OracleSample(w, rule, kv8, 0, units=n, steps=S) for _ in range(args.steps)]
     per = sum(x.layer_job_seconds() for x in samples) / len(samples)
     value = S / per
     line = {
@@ -407,7 +409,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * per, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, shaped like the configuration's layer)",
-        "config": {"workload": config_name(w, rule, S, 1, args.kv8)},
+        "config": {"workload": config_name(w, rule, S, 1, kv8)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": samples[0].threads, "kind": "oracle",
                          "sample": "per step: " + samples[0].describe()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -494,9 +496,9 @@ class Job:
             g = self.layers[li]
             self.prefill_call(self.hs[li], g["Q"], g["K"], g["V"], T)
 
-    def decode(self):
+    def decode(self, t0=0, t1=None):
         step = self.step_call
-        for t in range(self.S):
+        for t in range(t0, self.S if t1 is None else t1):
             for li in range(self.NL):
                 pp, op = self.ptr[li], self.optr[li]
                 step(self.hh[li], pp["q"][t], pp["k"][t], pp["v"][t], op[0][t], op[1][t])
@@ -674,12 +676,13 @@ def measure(args, L, torch, cname, rule, NL, S, stream, world, rank, want_e2e, c
     """Build, time and describe one configuration's job (clocks sampled
     during its timed region when a sampler is given)."""
     from kv_cache_eviction_h2o_gb300 import workloads as wl
-    wname, rule0, NL0 = CONFIGS[cname]
+    wname, rule0, NL0, kv8_0 = CONFIGS[cname]
     w = wl.WORKLOADS[wname]
     rule = rule or rule0
     NL = NL or NL0
     S = S or w.steps
-    job = Job(L, torch, w, rule, NL, S, args.kv8, args.split, stream, rank)
+    kv8 = args.kv8 or kv8_0
+    job = Job(L, torch, w, rule, NL, S, kv8, args.split, stream, rank)
     job.capture()
     if clocks is not None:
         clocks.start()
@@ -691,8 +694,8 @@ def measure(args, L, torch, cname, rule, NL, S, stream, world, rank, want_e2e, c
     rl = rooflines(job, phase, elapsed, K)
     mix = getattr(job, "policy_mix", None)
     rec = {
-        "config": {"workload": config_name(w, rule, S, NL, args.kv8),
-                   "cache": "int8 codes + fp32 scale per row" if args.kv8 else "bf16",
+        "config": {"workload": config_name(w, rule, S, NL, kv8),
+                   "cache": "int8 codes + fp32 scale per row" if kv8 else "bf16",
                    "batch": w.batch, "heads": w.heads, "groups": w.groups, "head_dim": w.head_dim,
                    "prompt": w.prompt, "decode_steps": S, "budget": w.budget, "heavy": w.heavy,
                    "recent": w.recent, "layers": NL, "l2": l2_note(job),
@@ -712,53 +715,68 @@ def measure(args, L, torch, cname, rule, NL, S, stream, world, rank, want_e2e, c
     rec["clocks"] = clk
     rec["cpu_baseline"] = None
     if rank == 0 and world == 1 and cpu_seconds > 0:
-        rec["cpu_baseline"] = OracleSample(w, rule, args.kv8, cpu_seconds, steps=S).record()
+        rec["cpu_baseline"] = OracleSample(w, rule, kv8, cpu_seconds, steps=S).record()
     if mix:
         rec["policies"] = {"local": mix[0], "frequency+local": mix[1], "full": mix[2]}
     return rec
 
 
-def run_e2e(job, world):
+def run_e2e(job, world, chunk_steps=64):
     """The job through the public API: every input copied in from pinned host
     memory and every output copied out inside the timed region, one step
     captured into a CUDA graph (all step state lives on the device, so a
     replay is a new step that still moves every input in and every output
-    out)."""
+    out).  The copies are pipelined with the compute on two copy streams:
+    each layer's prompt rows ahead of its prompt phase, the decode rows in
+    chunks of `chunk_steps` steps ahead of the chunk that reads them, and
+    each chunk's outputs out while the next chunk decodes."""
     torch = job.torch
-    NL, stream = job.NL, job.stream
+    NL, S, stream = job.NL, job.S, job.stream
     host_in = [{k: g[k].cpu().pin_memory() for k in ("Q", "K", "V", "q", "k", "v")} for g in job.layers]
     host_out = [(torch.empty(o.shape, dtype=o.dtype).pin_memory(), torch.empty(v.shape, dtype=v.dtype).pin_memory())
                 for o, v in zip(job.outs, job.vics)]
     h2d = sum(x.numel() * x.element_size() for hi in host_in for x in hi.values())
     d2h = sum(x.numel() * x.element_size() for ho in host_out for x in ho)
-    copy_stream = torch.cuda.Stream()
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    chunks = [(t0, min(S, t0 + chunk_steps)) for t0 in range(0, S, chunk_steps)]
     ready = [torch.cuda.Event() for _ in range(NL)]
-    ready_dec = torch.cuda.Event()
+    in_ready = [torch.cuda.Event() for _ in chunks]
+    out_ready = [torch.cuda.Event() for _ in chunks]
+    start_ev, done_in, done_out = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+    T = job.w.prompt
 
     def step():
-        # prompt rows first (each layer's prompt phase waits only for its
-        # own), the decode rows last
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_stream(stream)
+        start_ev.record(stream)
+        with torch.cuda.stream(cin):
+            cin.wait_event(start_ev)
             for li in range(NL):
                 for k in ("Q", "K", "V"):
                     job.layers[li][k].copy_(host_in[li][k], non_blocking=True)
-                ready[li].record(copy_stream)
-            for li in range(NL):
-                for k in ("q", "k", "v"):
-                    job.layers[li][k].copy_(host_in[li][k], non_blocking=True)
-            ready_dec.record(copy_stream)
+                ready[li].record(cin)
+            for c, (t0, t1) in enumerate(chunks):
+                for li in range(NL):
+                    for k in ("q", "k", "v"):
+                        job.layers[li][k][t0:t1].copy_(host_in[li][k][t0:t1], non_blocking=True)
+                in_ready[c].record(cin)
+            done_in.record(cin)
         with torch.cuda.stream(stream):
-            T = job.w.prompt
             for li in range(NL):
                 stream.wait_event(ready[li])
                 g = job.layers[li]
                 job.prefill_call(job.hs[li], g["Q"], g["K"], g["V"], T)
-            stream.wait_event(ready_dec)
-            job.decode()
-            for li in range(NL):
-                host_out[li][0].copy_(job.outs[li], non_blocking=True)
-                host_out[li][1].copy_(job.vics[li], non_blocking=True)
+            for c, (t0, t1) in enumerate(chunks):
+                stream.wait_event(in_ready[c])
+                job.decode(t0, t1)
+                out_ready[c].record(stream)
+        with torch.cuda.stream(cout):
+            for c, (t0, t1) in enumerate(chunks):
+                cout.wait_event(out_ready[c])
+                for li in range(NL):
+                    host_out[li][0][t0:t1].copy_(job.outs[li][t0:t1], non_blocking=True)
+                    host_out[li][1][t0:t1].copy_(job.vics[li][t0:t1], non_blocking=True)
+            done_out.record(cout)
+        stream.wait_event(done_in)
+        stream.wait_event(done_out)
 
     step()
     torch.cuda.synchronize()
@@ -787,7 +805,8 @@ def run_e2e(job, world):
     secs = statistics.median(each)
     return {"value": world * job.S * NL / secs, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": secs * 1000.0, "steps": n, "ms_each": [round(1000.0 * x, 3) for x in each],
-            "statistic": "median (the host link is shared with the machine's other GPUs)", "launch": "graph"}
+            "statistic": "median (the host link is shared with the machine's other GPUs)", "launch": "graph",
+            "copies": "pipelined: prompt rows per layer, decode rows and outputs in chunks of %d steps" % chunk_steps}
 
 
 def run_ours(args):
