@@ -49,6 +49,7 @@ def lib():
                                              _i32p, _i32p, _f64p, _f64p, _f64p, _f64p,
                                              _vp, _vp, _vp, _vp]
         L.oracle_quantize_rows.argtypes = [_i, _i, _f64p, _vp, _f32p]
+        L.oracle_quantize_rows4.argtypes = [_i, _i, _f64p, _vp, _f32p]
         L.oracle_h2o_decode_step_gqa.argtypes = [_i, _i, _i, _i, _i, _d, _i, _f64p, _f64p, _f64p,
                                                  _i32p, _i32p, _f64p, _f64p, _f64p, _f64p,
                                                  _vp, _vp, _vp, _vp]
@@ -121,7 +122,7 @@ class H2OState:
 
     def copy(self):
         s = H2OState(self.U, self.B, self.d)
-        for name in ("K", "V", "score", "pos", "occ", "kq", "ks", "vq", "vs"):
+        for name in ("K", "V", "score", "pos", "occ", "kq", "ks", "vq", "vs", "qbits"):
             if hasattr(self, name):
                 setattr(s, name, getattr(self, name).copy())
         return s
@@ -174,15 +175,24 @@ def h2o_decode_step(st, q, k, v, p, r, scale, forced=None):
     return out, victim, margin, evicted
 
 
-def quantize_rows(X):
-    """int8 codes [..., d] and fp32 scales [...] of every row of X (values
-    exactly representable in fp32)."""
+def quantize_rows(X, bits=8):
+    """int8 (bits 8, codes within +-127) or 4-bit (bits 4, codes within
+    +-7, one per byte) codes [..., d] and fp32 scales [...] of every row of
+    X (values exactly representable in fp32)."""
     X = _c64(X)
     flat = X.reshape(-1, X.shape[-1])
     code = np.empty(flat.shape, dtype=np.int8)
     scale = np.empty(flat.shape[0], dtype=np.float32)
-    lib().oracle_quantize_rows(flat.shape[0], flat.shape[1], flat, code.ctypes.data_as(ctypes.c_void_p), scale)
+    fn = lib().oracle_quantize_rows if bits == 8 else lib().oracle_quantize_rows4
+    fn(flat.shape[0], flat.shape[1], flat, code.ctypes.data_as(ctypes.c_void_p), scale)
     return code.reshape(X.shape), scale.reshape(X.shape[:-1])
+
+
+def pack4(code):
+    """4-bit codes [..., d] (one per byte) packed two per byte [..., d/2]:
+    element 2i in the low nibble, 2i+1 in the high one (two's complement)."""
+    c = (np.asarray(code, np.int16) & 0xF).astype(np.uint8)
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
 
 
 def dequantize(code, scale):
@@ -190,22 +200,30 @@ def dequantize(code, scale):
     return code.astype(np.float64) * scale.astype(np.float64)[..., None]
 
 
-def kv8(st):
-    """Turn a freshly built cache (exact rows) into an int8 cache: every
-    row is quantised, its codes and scales kept on the state, and the rows
-    the arithmetic reads become the dequantised values."""
-    st.kq, st.ks = quantize_rows(st.K)
-    st.vq, st.vs = quantize_rows(st.V)
+def kv8(st, bits=8):
+    """Turn a freshly built cache (exact rows) into a quantised cache (int8
+    rows, or 4-bit rows with bits=4): every row is quantised, its codes and
+    scales kept on the state, and the rows the arithmetic reads become the
+    dequantised values."""
+    st.qbits = bits
+    st.kq, st.ks = quantize_rows(st.K, bits)
+    st.vq, st.vs = quantize_rows(st.V, bits)
     st.K = dequantize(st.kq, st.ks)
     st.V = dequantize(st.vq, st.vs)
     return st
 
 
+def kv4(st):
+    """kv8 with 4-bit rows."""
+    return kv8(st, 4)
+
+
 def _kv8_written(st, slots):
     """Quantise the row each unit's step wrote (slots[u], exact values)."""
+    bits = getattr(st, "qbits", 8)
     for u, s in enumerate(slots):
-        kq, ks = quantize_rows(st.K[u, s][None])
-        vq, vs = quantize_rows(st.V[u, s][None])
+        kq, ks = quantize_rows(st.K[u, s][None], bits)
+        vq, vs = quantize_rows(st.V[u, s][None], bits)
         st.kq[u, s], st.ks[u, s] = kq[0], ks[0]
         st.vq[u, s], st.vs[u, s] = vq[0], vs[0]
         st.K[u, s] = dequantize(kq, ks)[0]

@@ -59,7 +59,8 @@
  *    codes and one fp32 scale, amax/127, with codes rint(x * (127/amax))
  *    in fp32, half to even; a step attends to its own new token at full
  *    precision and stores it quantised (the quantiser is below; the mode's
- *    bookkeeping is in the Python wrapper);
+ *    bookkeeping is in the Python wrapper); 4-bit slots are the same with
+ *    codes in [-7, 7], scale amax/7 and codes rint((7/amax) * x);
  *  - the persistence-of-importance rule (an optional cache kind, [SH]): a
  *    token is pivotal at a step when its attention probability exceeds
  *    the uniform share 1/m over the m tokens attended that step; each
@@ -481,6 +482,40 @@ void oracle_quantize_rows(int n, int d, const double* X, signed char* code, floa
             c[e] = (signed char)y;
         }
         scale[t] = amax / 127.0f;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* 4-bit cache rows [Scissorhands abstract: a budgeted cache combines  */
+/* with quantisation of its entries, down to 4 bits; the form is this  */
+/* library's reading]: per row amax = max |x_e| (fp32), code_e =       */
+/* rint(x_e * (7 / amax)) in fp32 (half to even), clamped to +-7, and  */
+/* scale = amax / 7; all codes 0 and scale 0 when amax = 0.  The row   */
+/* reads back as code_e * scale.  Codes are returned one per byte.      */
+/* ------------------------------------------------------------------ */
+void oracle_quantize_rows4(int n, int d, const double* X, signed char* code, float* scale)
+{
+    for (int t = 0; t < n; ++t) {
+        const double* x = X + (size_t)t * d;
+        signed char* c = code + (size_t)t * d;
+        float amax = 0.0f;
+        for (int e = 0; e < d; ++e) {
+            float a = fabsf((float)x[e]);
+            if (a > amax) amax = a;
+        }
+        if (amax == 0.0f) {
+            for (int e = 0; e < d; ++e) c[e] = 0;
+            scale[t] = 0.0f;
+            continue;
+        }
+        float inv = 7.0f / amax;
+        for (int e = 0; e < d; ++e) {
+            float y = rintf(inv * (float)x[e]);
+            if (y > 7.0f) y = 7.0f;
+            if (y < -7.0f) y = -7.0f;
+            c[e] = (signed char)y;
+        }
+        scale[t] = amax / 7.0f;
     }
 }
 

@@ -42,6 +42,10 @@ MUTATIONS = {
     "kv8_ties_away_from_zero": ("float y = rintf((float)x[e] * inv);", "float y = roundf((float)x[e] * inv);"),
     "kv8_scale_over_128": ("scale[t] = amax / 127.0f;", "scale[t] = amax / 128.0f;"),
     "kv8_inverse_from_128": ("float inv = 127.0f / amax;", "float inv = 128.0f / amax;"),
+    "kv4_ties_away_from_zero": ("float y = rintf(inv * (float)x[e]);", "float y = roundf(inv * (float)x[e]);"),
+    "kv4_product_in_fp64": ("float y = rintf(inv * (float)x[e]);", "float y = (float)rint((double)inv * x[e]);"),
+    "kv4_scale_over_8": ("scale[t] = amax / 7.0f;", "scale[t] = amax / 8.0f;"),
+    "kv4_inverse_from_8": ("float inv = 7.0f / amax;", "float inv = 8.0f / amax;"),
     "gqa_last_head_only": ("add[s] += P;                          /* heads in order g = 0..G-1 */",
                            "add[s] = P;"),
     "sh_threshold_share_of_n": ("const double t = P * (double)(n + 1);", "const double t = P * (double)n;"),

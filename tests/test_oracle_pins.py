@@ -479,6 +479,94 @@ def test_kv8_step_attends_new_token_exactly_and_stores_it_quantised():
         assert (st.K[u, others] == Kc[u, others]).all()
 
 
+# ----------------------------------------------------------- 4-bit slots ---
+
+def test_quantize4_hand_worked():
+    g = _golden("quantize_rows4.json")
+    code, scale = oracle.quantize_rows(np.array(g["x"], float), 4)
+    assert code.tolist() == g["code"]
+    want = [np.float32(n) / np.float32(g["scale_den"]) for n in g["scale_num"]]
+    assert scale.tolist() == [float(w) for w in want]
+    assert oracle.pack4(code[0]).tolist() == g["packed_row0"]
+
+
+def test_quantize4_round_trip_bound_and_symmetry():
+    rng = np.random.default_rng(44)
+    X = (rng.standard_normal((300, 64)) * rng.uniform(0.01, 50, (300, 1))).astype(np.float32).astype(float)
+    code, scale = oracle.quantize_rows(X, 4)
+    err = np.abs(X - oracle.dequantize(code, scale))
+    s = scale.astype(float)[:, None]
+    assert (err <= 0.5 * s * (1 + 1e-5) + 1e-30).all()
+    top = np.abs(X).argmax(axis=1)
+    assert (np.abs(code[np.arange(300), top]) == 7).all()
+    assert (np.abs(code) <= 7).all()
+    # every code a row can take is reached somewhere in a large sample
+    assert set(np.unique(code).tolist()) == set(range(-7, 8))
+    code_n, scale_n = oracle.quantize_rows(-X, 4)
+    assert (code_n == -code).all() and (scale_n == scale).all()
+    # unpacking the packed bytes gives the codes back
+    p = oracle.pack4(code).astype(np.int16)
+    lo = ((p & 0xF) ^ 8) - 8
+    hi = ((p >> 4) ^ 8) - 8
+    assert (lo == code[:, 0::2]).all() and (hi == code[:, 1::2]).all()
+
+
+def test_quantize4_grid_rows_are_exact():
+    """Rows whose entries are integer multiples k of amax/7 (|k| <= 7) are
+    stored exactly: the codes are k and the scale amax/7."""
+    rng = np.random.default_rng(45)
+    k = rng.integers(-7, 8, size=(50, 32)); k[:, 0] = 7
+    X = k.astype(float)                       # amax = 7: scale 1, codes = x
+    code, scale = oracle.quantize_rows(X, 4)
+    assert (code == k).all() and (scale == 1.0).all()
+    X2 = X * 0.25                             # a power-of-two scale changes nothing but the scale
+    code2, scale2 = oracle.quantize_rows(X2, 4)
+    assert (code2 == k).all() and (scale2 == 0.25).all()
+
+
+def test_kv4_exact_rows_reproduce_full_precision():
+    rng = np.random.default_rng(46)
+    U, T, S, d, B, H, r, scale = 3, 24, 10, 8, 8, 4, 4, 1e-2
+
+    def rows(shape):
+        x = rng.integers(-6, 7, size=shape).astype(float)
+        x[..., 0] = np.where(rng.random(shape[:-1]) < 0.5, 7.0, -7.0)
+        return x
+    Q, K, V = (rows((U, T, d)) for _ in range(3))
+    q, k, v = (rows((S, U, d)) for _ in range(3))
+    st, _, _, _ = oracle.h2o_prefill(Q, K, V, B, H, r, scale)
+    st4 = oracle.kv4(st.copy())
+    assert (st4.ks[st4.pos >= 0] == 1.0).all() and st4.qbits == 4
+    for t in range(S):
+        o, vic, _, _ = oracle.h2o_decode_step(st, q[t], k[t], v[t], T + t, r, scale)
+        o4, vic4, _, _ = oracle.h2o_decode_step(st4, q[t], k[t], v[t], T + t, r, scale)
+        assert (vic == vic4).all() and (o == o4).all()
+        assert (st.K == st4.K).all() and (st.score == st4.score).all()
+
+
+def test_kv4_step_stores_the_new_row_in_four_bits():
+    rng = np.random.default_rng(47)
+    U, T, d, B, H, r, scale = 2, 30, 16, 10, 5, 5, 0.3
+    Q, K, V = (rng.standard_normal((U, T, d)).astype(np.float32).astype(float) for _ in range(3))
+    q, k, v = (rng.standard_normal((U, d)).astype(np.float32).astype(float) for _ in range(3))
+    st = oracle.kv4(oracle.h2o_prefill(Q, K, V, B, H, r, scale)[0])
+    Kc, Vc = st.K.copy(), st.V.copy()
+    assert np.array_equal(Kc, st.kq.astype(float) * st.ks.astype(float)[..., None])
+    assert (np.abs(st.kq) <= 7).all() and (np.abs(st.vq) <= 7).all()
+    out, vic, _, _ = oracle.h2o_decode_step(st, q, k, v, T, r, scale)
+    for u in range(U):
+        keys = np.concatenate([Kc[u], k[u][None]]); vals = np.concatenate([Vc[u], v[u][None]])
+        z = scale * keys @ q[u]
+        e = np.exp(z - z.max())
+        np.testing.assert_allclose(out[u], (e / e.sum()) @ vals, rtol=0, atol=1e-12)
+        s = vic[u]
+        kq, ks = oracle.quantize_rows(k[u][None], 4)
+        vq, vs = oracle.quantize_rows(v[u][None], 4)
+        assert (st.kq[u, s] == kq[0]).all() and st.ks[u, s] == ks[0]
+        assert (st.vq[u, s] == vq[0]).all() and st.vs[u, s] == vs[0]
+        assert (st.V[u, s] == vq[0] * float(vs[0])).all()
+
+
 # --------------------------------------------------- grouped-query caches ---
 
 def _gqa_inputs(seed, U, G, T, S, d):
