@@ -189,9 +189,10 @@ def quantize_rows(X, bits=8):
 
 
 def pack4(code):
-    """4-bit codes [..., d] (one per byte) packed two per byte [..., d/2]:
-    element 2i in the low nibble, 2i+1 in the high one (two's complement)."""
-    c = (np.asarray(code, np.int16) & 0xF).astype(np.uint8)
+    """4-bit codes [..., d] (one per byte, within +-7) packed two per byte
+    [..., d/2] in offset binary: each nibble holds code + 8 (1..15), element
+    2i in the low nibble and 2i+1 in the high one."""
+    c = (np.asarray(code, np.int16) + 8).astype(np.uint8)
     return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
 
 

@@ -506,8 +506,8 @@ def test_quantize4_round_trip_bound_and_symmetry():
     assert (code_n == -code).all() and (scale_n == scale).all()
     # unpacking the packed bytes gives the codes back
     p = oracle.pack4(code).astype(np.int16)
-    lo = ((p & 0xF) ^ 8) - 8
-    hi = ((p >> 4) ^ 8) - 8
+    lo = (p & 0xF) - 8
+    hi = (p >> 4) - 8
     assert (lo == code[:, 0::2]).all() and (hi == code[:, 1::2]).all()
 
 
