@@ -27,7 +27,7 @@ copied in and outputs copied out inside the timed region.  The CPU oracle is
 timed on a bounded sample of the same job.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
-                    [--rule h2o|sh] [--kv8] [--impl reference] [--no-sub]
+                    [--rule h2o|sh] [--kv8 | --kv4] [--impl reference] [--no-sub]
 """
 import argparse
 import hashlib
@@ -48,20 +48,23 @@ METRIC = "H2O decode steps/s (batch×heads) at 1 GB300; achieved HBM GB/s vs pea
 UNIT = "steps/s"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 
-# name -> (workload, eviction rule, layer caches in rotation, int8 slots).
+# name -> (workload, eviction rule, layer caches in rotation, quantised slots:
+# 0 = bf16 rows, 8 = int8 codes, 4 = 4-bit codes).
 # The layer count keeps the caches plus prompts well above L2 (129 MB) and
 # makes every cache wait for the others before it is read again.
 CONFIGS = {
-    "opt-30b": ("opt-30b", "h2o", 2, False),                    # 2 x 594 MB caches
-    "opt-6.7b": ("opt-6.7b", "h2o", 8, False),                  # 8 x 113 MB
-    "llama-7b-32k": ("llama-7b-32k", "h2o", 8, False),          # 8 x 70 MB
-    "hashevict-opt-6.7b": ("hashevict-opt-6.7b", "lsh", 8, False),
-    "fastgen-opt-6.7b": ("fastgen-opt-6.7b", "fg", 8, False),   # per-head policies, mixed budgets
-    "gqa-8x8x4": ("gqa-8x8x4", "h2o", 8, False),                # caches shared by 4 query heads
-    "opt-30b-int8": ("opt-30b", "h2o", 2, True),                # the main layer with int8 slots
+    "opt-30b": ("opt-30b", "h2o", 2, 0),                    # 2 x 594 MB caches
+    "opt-6.7b": ("opt-6.7b", "h2o", 8, 0),                  # 8 x 113 MB
+    "llama-7b-32k": ("llama-7b-32k", "h2o", 8, 0),          # 8 x 70 MB
+    "hashevict-opt-6.7b": ("hashevict-opt-6.7b", "lsh", 8, 0),
+    "fastgen-opt-6.7b": ("fastgen-opt-6.7b", "fg", 8, 0),   # per-head policies, mixed budgets
+    "gqa-8x8x4": ("gqa-8x8x4", "h2o", 8, 0),                # caches shared by 4 query heads
+    "opt-30b-int8": ("opt-30b", "h2o", 2, 8),               # the main layer with int8 slots
+    "opt-30b-int4": ("opt-30b", "h2o", 2, 4),               # ... and with 4-bit slots
 }
 DEFAULT_CONFIG = "opt-30b"
-SUB_CONFIGS = ("opt-6.7b", "llama-7b-32k", "hashevict-opt-6.7b", "fastgen-opt-6.7b", "gqa-8x8x4", "opt-30b-int8")
+SUB_CONFIGS = ("opt-6.7b", "llama-7b-32k", "hashevict-opt-6.7b", "fastgen-opt-6.7b", "gqa-8x8x4", "opt-30b-int8",
+               "opt-30b-int4")
 
 
 def parse(argv=None):
@@ -87,6 +90,7 @@ def parse(argv=None):
     p.add_argument("--sub", default=None, help="comma-separated sub-record configurations (default: %s)"
                    % ",".join(SUB_CONFIGS))
     p.add_argument("--kv8", action="store_true", help="int8 cache slots (one fp32 scale per row)")
+    p.add_argument("--kv4", action="store_true", help="4-bit cache slots (one fp32 scale per row)")
     # older spellings
     p.add_argument("--gqa", action="store_true", help="same as --config gqa-8x8x4")
     p.add_argument("--sh", action="store_true", help="same as --config opt-6.7b --rule sh")
@@ -95,7 +99,19 @@ def parse(argv=None):
         a.config = "gqa-8x8x4"
     if a.sh:
         a.config, a.rule = ("opt-6.7b" if a.config == DEFAULT_CONFIG else a.config), "sh"
+    if a.kv8 and a.kv4:
+        p.error("--kv8 and --kv4 are exclusive")
     return a
+
+
+def qbits(args, q0):
+    """Cache row form of a run: the flags, else the configuration's own."""
+    return 8 if args.kv8 else 4 if args.kv4 else q0
+
+
+def code_row(d, eb, qb):
+    """Bytes of one stored row: the input type, int8 or 4-bit codes."""
+    return d if qb == 8 else d // 2 if qb == 4 else d * eb
 
 
 # ------------------------------------------------------------------ helpers
@@ -203,17 +219,17 @@ def dist_setup():
 
 # ------------------------------------------------------------ algorithmic
 
-def decode_bytes(U, B, d, eb, lsh, kv8=False):
+def decode_bytes(U, B, d, eb, lsh, qb=0):
     """Algorithmic HBM bytes of one full-cache decode launch over U units:
-    per live slot K and V rows (int8 codes plus an 8-byte scale pair with
-    kv8), plus score read+write (8-byte fp32 pair) and position read (H2O)
+    per live slot K and V rows (int8 or 4-bit codes plus an 8-byte scale
+    pair with qb 8 or 4), plus score read+write (8-byte fp32 pair) and position read (H2O)
     or code and position read (HashEvict); per unit q, k, v in, fp32 out,
     one K/V row written (and its scale pair), victim score/code and
     position written, unit state read and written; plus the projection
     matrix once."""
     row = d * eb
-    crow = d if kv8 else row
-    sc = 8 if kv8 else 0
+    crow = code_row(d, eb, qb)
+    sc = 8 if qb else 0
     if lsh:
         per_slot = 2 * crow + sc + 4 + 4
         fixed = 3 * row + 4 * d + 2 * crow + sc + 4 + 4 + 16
@@ -229,16 +245,16 @@ def method_bytes(U, B, d, eb):
     return U * (B * (2 * d * eb + 12) + 3 * d * eb + 4 * d + 2 * d * eb + 12)
 
 
-def decode_bytes_gqa(U, G, B, d, eb, kv8=False):
+def decode_bytes_gqa(U, G, B, d, eb, qb=0):
     """Algorithmic HBM bytes of one full-cache grouped-query H2O decode launch
-    over U cache units of G query heads: per live slot K and V rows (int8
-    codes plus an 8-byte scale pair with kv8), score read+write and position
+    over U cache units of G query heads: per live slot K and V rows (int8 or
+    4-bit codes plus an 8-byte scale pair with qb 8 or 4), score read+write and position
     read, each once per unit (the heads share them); per query head q in and
     fp32 out; per unit k, v in, one K/V row written (and its scale pair),
     victim score and position written, unit state read and written."""
     row = d * eb
-    crow = d if kv8 else row
-    sc = 8 if kv8 else 0
+    crow = code_row(d, eb, qb)
+    sc = 8 if qb else 0
     per_slot = 2 * crow + sc + 8 + 8 + 4
     fixed = G * (row + 4 * d) + 2 * row + 2 * crow + sc + 8 + 4 + 16
     return U * (B * per_slot + fixed)
@@ -287,7 +303,7 @@ def prompt_launches(rule, G):
 ORACLE_MAX_PROMPT = 4096
 
 
-def oracle_job(w, rule, units, S, kv8=False, prompt=None):
+def oracle_job(w, rule, units, S, qb=0, prompt=None):
     """The CPU oracle on a sample of units of workload w: the prompt phase
     (of `prompt` tokens, default the workload's) and S decode steps of the
     rule.  Returns (prompt seconds, decode seconds, threads)."""
@@ -299,8 +315,8 @@ def oracle_job(w, rule, units, S, kv8=False, prompt=None):
     if rule == "lsh":
         W = g["W"]
         st = oracle.lsh_prefill(g["Q"], g["K"], g["V"], W, w.budget, w.recent)
-        if kv8:
-            oracle.kv8(st)
+        if qb:
+            oracle.kv8(st, qb)
         t1 = time.perf_counter()
         for t in range(S):
             oracle.lsh_decode_step(st, g["q"][t], g["k"][t], g["v"][t], W, T + t, w.recent, w.scale)
@@ -317,15 +333,15 @@ def oracle_job(w, rule, units, S, kv8=False, prompt=None):
             oracle.fg_decode_step(states, params, g["q"][t], g["k"][t], g["v"][t], T + t, w.scale)
     elif w.groups > 1:
         st, _, _, _, _ = oracle.h2o_prefill_gqa(g["Q"], g["K"], g["V"], w.budget, w.heavy, w.recent, w.scale)
-        if kv8:
-            oracle.kv8(st)
+        if qb:
+            oracle.kv8(st, qb)
         t1 = time.perf_counter()
         for t in range(S):
             oracle.h2o_decode_step_gqa(st, g["q"][t], g["k"][t], g["v"][t], T + t, w.recent, w.scale)
     else:
         st, _, _, _ = oracle.h2o_prefill(g["Q"], g["K"], g["V"], w.budget, w.heavy, w.recent, w.scale)
-        if kv8:
-            oracle.kv8(st)
+        if qb:
+            oracle.kv8(st, qb)
         t1 = time.perf_counter()
         for t in range(S):
             oracle.h2o_decode_step(st, g["q"][t], g["k"][t], g["v"][t], T + t, w.recent, w.scale)
@@ -342,7 +358,7 @@ class OracleSample:
     work grows with the causal pair count) is timed on its first
     ORACLE_MAX_PROMPT rows and scaled by the pair count."""
 
-    def __init__(self, w, rule, kv8, target_s, units=None, steps=None):
+    def __init__(self, w, rule, qb, target_s, units=None, steps=None):
         import oracle
         self.w, self.rule = w, rule
         self.S = steps or w.steps
@@ -352,10 +368,10 @@ class OracleSample:
             self.Tp = ORACLE_MAX_PROMPT
         self.pair_scale = (w.prompt * (w.prompt + 1)) / (self.Tp * (self.Tp + 1))
         n = min(w.units, units or max(1, oracle.get_threads()))
-        tp, td, th = oracle_job(w, rule, list(range(n)), self.S, kv8, self.Tp)
+        tp, td, th = oracle_job(w, rule, list(range(n)), self.S, qb, self.Tp)
         if units is None and tp + td < target_s / 2 and n < w.units:
             n = min(w.units, max(n + 1, int(n * target_s / max(tp + td, 1e-3))))
-            tp, td, th = oracle_job(w, rule, list(range(n)), self.S, kv8, self.Tp)
+            tp, td, th = oracle_job(w, rule, list(range(n)), self.S, qb, self.Tp)
         self.n, self.tp, self.td, self.threads = n, tp, td, th
 
     def seconds(self):
@@ -393,15 +409,15 @@ def run_reference(args):
         return
     from kv_cache_eviction_h2o_gb300 import workloads as wl
     import oracle
-    wname, rule0, _, kv8_0 = CONFIGS[args.config]
+    wname, rule0, _, q0 = CONFIGS[args.config]
     rule = args.rule or rule0
-    kv8 = args.kv8 or kv8_0
+    qb = qbits(args, q0)
     w = wl.WORKLOADS[wname]
     n = min(w.units, args.oracle_units or max(1, oracle.get_threads()))
     S = args.decode_steps or w.steps
     for _ in range(args.warmup):
-        OracleSample(w, rule, kv8, 0, units=n, steps=S)
-    samples = [OracleSample(w, rule, kv8, 0, units=n, steps=S) for _ in range(args.steps)]
+        OracleSample(w, rule, qb, 0, units=n, steps=S)
+    samples = [OracleSample(w, rule, qb, 0, units=n, steps=S) for _ in range(args.steps)]
     per = sum(x.layer_job_seconds() for x in samples) / len(samples)
     value = S / per
     line = {
@@ -409,7 +425,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * per, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, shaped like the configuration's layer)",
-        "config": {"workload": config_name(w, rule, S, 1, kv8)},
+        "config": {"workload": config_name(w, rule, S, 1, qb)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": samples[0].threads, "kind": "oracle",
                          "sample": "per step: " + samples[0].describe()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -427,13 +443,13 @@ def rule_name(rule, w):
     return "H2O" + (" grouped-query" if w.groups > 1 else "")
 
 
-def config_name(w, rule, S, NL, kv8):
+def config_name(w, rule, S, NL, qb):
     heads = ("%d x %d key/value heads x %d query heads" % (w.batch, w.heads, w.groups) if w.groups > 1
              else "%d x %d heads" % (w.batch, w.heads))
     split = ("recent %d" % w.recent) if rule == "lsh" else ("%d heavy + %d recent" % (w.heavy, w.recent))
     return ("%s-shaped layer x%d (%s, head_dim %d): %s, prompt %d -> %d decode steps, budget %d (%s)%s"
             % (w.name, NL, heads, w.head_dim, rule_name(rule, w), w.prompt, S, w.budget, split,
-               ", int8 cache slots" if kv8 else ""))
+               {8: ", int8 cache slots", 4: ", 4-bit cache slots"}.get(qb, "")))
 
 
 # -------------------------------------------------------------------- ours
@@ -443,12 +459,12 @@ class Job:
     in HBM, the handles, the prompt and decode phases as callables over the
     public API, and their algorithmic work."""
 
-    def __init__(self, L, torch, w, rule, NL, S, kv8, split, stream, rank):
+    def __init__(self, L, torch, w, rule, NL, S, qb, split, stream, rank):
         from kv_cache_eviction_h2o_gb300 import workloads as wl
-        self.L, self.torch, self.w, self.rule, self.NL, self.S, self.kv8 = L, torch, w, rule, NL, S, kv8
+        self.L, self.torch, self.w, self.rule, self.NL, self.S, self.qb = L, torch, w, rule, NL, S, qb
         self.stream = stream
         U, G, d, B = w.units, w.groups, w.head_dim, w.budget
-        dt = L.H2O_BF16 | (L.H2O_KV8 if kv8 else 0)
+        dt = L.H2O_BF16 | {0: 0, 8: L.H2O_KV8, 4: L.H2O_KV4}[qb]
         self.layers = []
         with torch.cuda.stream(stream):
             for li in range(NL):
@@ -578,7 +594,7 @@ class Job:
         w = self.w
         U, G, d, B = w.units, w.groups, w.head_dim, w.budget
         if self.rule == "lsh":
-            return decode_bytes(U, B, d, 2, True, self.kv8)
+            return decode_bytes(U, B, d, 2, True, self.qb)
         if self.rule == "sh":
             return decode_bytes_sh(U, B, d, 2)
         if self.rule == "fg":
@@ -597,11 +613,11 @@ class Job:
             self.policy_mix = {int(k): int((pol == k).sum()) for k in (0, 1, 2)}
             return tot
         if G > 1:
-            return decode_bytes_gqa(U, G, B, d, 2, self.kv8)
-        return decode_bytes(U, B, d, 2, False, self.kv8)
+            return decode_bytes_gqa(U, G, B, d, 2, self.qb)
+        return decode_bytes(U, B, d, 2, False, self.qb)
 
     def traffic_key(self):
-        return "%s%s@%s" % (self.decode_kernel(), "_kv8" if self.kv8 else "", self.w.name)
+        return "%s%s@%s" % (self.decode_kernel(), {8: "_kv8", 4: "_kv4"}.get(self.qb, ""), self.w.name)
 
     def launches_per_step(self):
         return self.NL * (prompt_launches(self.rule, self.w.groups) + self.S)
@@ -629,7 +645,7 @@ def rooflines(job, phase_ms, elapsed_ms, K):
     rec = {"kernel": job.decode_kernel(), "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
            "frac": ach / hbm, "traffic": ncu_traffic(job.traffic_key()), "algorithmic_bytes": by,
            "launch_us": t_launch * 1e6, "peak_source": peak_src, "share": phase_ms["decode"] / elapsed_ms}
-    if job.rule == "h2o" and G == 1 and not job.kv8:
+    if job.rule == "h2o" and G == 1 and not job.qb:
         mb = method_bytes(U, B, d, 2)
         rec["method_bytes"] = mb
         rec["method_frac"] = mb / t_launch / 1e9 / hbm
@@ -676,13 +692,13 @@ def measure(args, L, torch, cname, rule, NL, S, stream, world, rank, want_e2e, c
     """Build, time and describe one configuration's job (clocks sampled
     during its timed region when a sampler is given)."""
     from kv_cache_eviction_h2o_gb300 import workloads as wl
-    wname, rule0, NL0, kv8_0 = CONFIGS[cname]
+    wname, rule0, NL0, q0 = CONFIGS[cname]
     w = wl.WORKLOADS[wname]
     rule = rule or rule0
     NL = NL or NL0
     S = S or w.steps
-    kv8 = args.kv8 or kv8_0
-    job = Job(L, torch, w, rule, NL, S, kv8, args.split, stream, rank)
+    qb = qbits(args, q0)
+    job = Job(L, torch, w, rule, NL, S, qb, args.split, stream, rank)
     job.capture()
     if clocks is not None:
         clocks.start()
@@ -694,8 +710,9 @@ def measure(args, L, torch, cname, rule, NL, S, stream, world, rank, want_e2e, c
     rl = rooflines(job, phase, elapsed, K)
     mix = getattr(job, "policy_mix", None)
     rec = {
-        "config": {"workload": config_name(w, rule, S, NL, kv8),
-                   "cache": "int8 codes + fp32 scale per row" if kv8 else "bf16",
+        "config": {"workload": config_name(w, rule, S, NL, qb),
+                   "cache": {8: "int8 codes + fp32 scale per row", 4: "4-bit codes (two per byte) + fp32 scale per row"}
+                   .get(qb, "bf16"),
                    "batch": w.batch, "heads": w.heads, "groups": w.groups, "head_dim": w.head_dim,
                    "prompt": w.prompt, "decode_steps": S, "budget": w.budget, "heavy": w.heavy,
                    "recent": w.recent, "layers": NL, "l2": l2_note(job),
@@ -715,7 +732,7 @@ def measure(args, L, torch, cname, rule, NL, S, stream, world, rank, want_e2e, c
     rec["clocks"] = clk
     rec["cpu_baseline"] = None
     if rank == 0 and world == 1 and cpu_seconds > 0:
-        rec["cpu_baseline"] = OracleSample(w, rule, kv8, cpu_seconds, steps=S).record()
+        rec["cpu_baseline"] = OracleSample(w, rule, qb, cpu_seconds, steps=S).record()
     if mix:
         rec["policies"] = {"local": mix[0], "frequency+local": mix[1], "full": mix[2]}
     return rec

@@ -100,11 +100,23 @@ enum { H2O_F32 = 0, H2O_BF16 = 1 };
 enum { H2O_KV8 = 2 };
 
 /*
+ * H2O_KV4 -- OR into dtype instead of H2O_KV8 to store the rows as 4-bit
+ * codes with one fp32 scale per row [SH abstract: quantisation of the
+ * entries down to 4 bits; the form is this library's reading]:
+ * scale = amax / 7, code_e = rint(x_e * (7 / amax)) (fp32, half to even,
+ * within +-7; all zero when amax = 0).  A row of d codes takes d/2 bytes:
+ * byte i holds element 2i in its low nibble and element 2i+1 in its high
+ * nibble, each in offset binary (code + 8).  Everything else as H2O_KV8;
+ * the two flags are exclusive.
+ */
+enum { H2O_KV4 = 4 };
+
+/*
  * h2o_init -- create an H2O cache handle [H2O 提案手法; FG Figure 2; SH].
  *   budget = B slots per unit (>= 1), heavy = H heavy-hitter slots,
  *   recent = r recent-window slots; heavy + recent must equal budget.
  *   batch, heads >= 1; head_dim in {64, 128}; dtype H2O_F32 or H2O_BF16,
- *   optionally | H2O_KV8;
+ *   optionally | H2O_KV8 or | H2O_KV4;
  *   scale > 0 is the softmax scale (usually 1/sqrt(head_dim)).
  *   cuda_stream: the cudaStream_t to enqueue on (NULL = legacy stream).
  * On success *out holds the handle; destroy it with h2o_destroy.
@@ -179,8 +191,8 @@ int h2o_decode_step(h2o_handle h, const void* q, const void* k, const void* v,
  *               slot if none) the lowest importance, then the lowest
  *               position;
  *   insert:     the new token's history is its own flag this step.
- *   Arguments as h2o_init (heavy + recent = budget); H2O_KV8 is not
- *   supported (H2O_ERR_UNSUPPORTED).
+ *   Arguments as h2o_init (heavy + recent = budget); H2O_KV8 and H2O_KV4
+ *   are not supported (H2O_ERR_UNSUPPORTED).
  */
 int sh_init(h2o_handle* out, int budget, int heavy, int recent, int batch, int heads, int head_dim,
             int dtype, double scale, void* cuda_stream);
@@ -223,7 +235,8 @@ int sh_decode_step(h2o_handle h, const void* q, const void* k, const void* v,
  * set holds at each prompt row, averaged over the rows -- reaches tau.  The
  * recovery test and the order are this library's reading of the page.
  *   budget = heavy + recent as h2o_init; full_budget >= 1 (usually the
- *   prompt plus the decode steps); 0 < tau <= 1.  H2O_KV8 is not supported.
+ *   prompt plus the decode steps); 0 < tau <= 1.  H2O_KV8 and H2O_KV4 are not
+ *   supported.
  *   Every unit holds max(budget, full_budget) slots; a unit of policy 0 or 1
  *   uses `budget` of them.  State calls see that many slots per unit.
  */
@@ -295,8 +308,9 @@ int lsh_decode_step(h2o_handle h, const void* q, const void* k, const void* v,
 
 /*
  * h2o_get_state -- copy the cache to HOST buffers (any pointer may be NULL):
- *   K, V [U][B][d] of the handle's dtype (int8 codes for H2O_KV8 handles,
- *   whose scales h2o_get_kv_scales returns); score fp64 [U][B] (H2O handles;
+ *   K, V [U][B][d] of the handle's dtype (int8 codes for H2O_KV8 handles;
+ *   [U][B][d/2] bytes of packed codes for H2O_KV4 handles; the scales of
+ *   both from h2o_get_kv_scales); score fp64 [U][B] (H2O handles;
  *   zeros for LSH); pos int32 [U][B]; code uint32 [U][B] (LSH handles;
  *   zeros for H2O); occupancy int32 [U]; next_pos int32 [U].
  * Waits for the handle's stream.
@@ -315,10 +329,11 @@ int h2o_set_state(h2o_handle h, const void* K, const void* V, const double* scor
 
 /*
  * h2o_get_kv_scales / h2o_set_kv_scales -- the fp32 K and V row scales
- * [U][B] of an H2O_KV8 handle, to / from HOST buffers (get: either may be
- * NULL; set: both required).  H2O_ERR_STATE on a handle without H2O_KV8.
- * Both wait for the handle's stream.  The int8 cache is this library's
- * reading of the quantised budgeted cache (see H2O_KV8).
+ * [U][B] of an H2O_KV8 or H2O_KV4 handle, to / from HOST buffers (get:
+ * either may be NULL; set: both required).  H2O_ERR_STATE on a handle
+ * with neither flag.  Both wait for the handle's stream.  The quantised
+ * caches are this library's reading of the quantised budgeted cache (see
+ * H2O_KV8, H2O_KV4).
  */
 int h2o_get_kv_scales(h2o_handle h, float* kscale, float* vscale);
 int h2o_set_kv_scales(h2o_handle h, const float* kscale, const float* vscale);

@@ -32,6 +32,7 @@ H2O_ERR_UNSUPPORTED = -6
 H2O_F32 = 0
 H2O_BF16 = 1
 H2O_KV8 = 2
+H2O_KV4 = 4
 
 # every symbol include/h2o.h declares, with (restype, argtypes)
 _vp = ctypes.c_void_p
@@ -125,10 +126,11 @@ _meta = {}
 
 
 def _remember(h, kind, U, B, d, dtype, G=1):
-    kv8 = bool(dtype & H2O_KV8)
-    elem = np.int8 if kv8 else (np.uint16 if (dtype & H2O_BF16) else np.float32)
-    _meta[h] = dict(kind=kind, U=U, B=B, d=d, G=G, elem=np.dtype(elem), esize=1 if kv8 else (2 if dtype & H2O_BF16 else 4),
-                    kv8=kv8, T=0, in_size=2 if dtype & H2O_BF16 else 4)
+    kv8, kv4 = bool(dtype & H2O_KV8), bool(dtype & H2O_KV4)
+    elem = np.int8 if kv8 else np.uint8 if kv4 else (np.uint16 if (dtype & H2O_BF16) else np.float32)
+    # elements of one stored row: a 4-bit row packs two codes per byte
+    _meta[h] = dict(kind=kind, U=U, B=B, d=d, G=G, elem=np.dtype(elem), row=d // 2 if kv4 else d,
+                    kv8=kv8, kv4=kv4, T=0, in_size=2 if dtype & H2O_BF16 else 4)
     return h
 
 
@@ -256,8 +258,8 @@ def _step_args(h, q, k, v, out, victim_out):
 def _state_args(h, K, V, score, pos, code, occupancy, next_pos):
     m = _info(h)
     UB = m["U"] * m["B"]
-    _host(K, m["elem"], UB * m["d"], "K")
-    _host(V, m["elem"], UB * m["d"], "V")
+    _host(K, m["elem"], UB * m["row"], "K")
+    _host(V, m["elem"], UB * m["row"], "V")
     _host(score, np.float64, UB, "score")
     _host(pos, np.int32, UB, "pos")
     _host(code, np.uint32, UB, "code")

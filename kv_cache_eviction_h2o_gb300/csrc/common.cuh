@@ -295,6 +295,77 @@ __device__ __forceinline__ void q8_unpack4(uint32_t w, float* f)
     f[0] = lo.x; f[1] = lo.y; f[2] = hi.x; f[3] = hi.y;
 }
 
+// ------------------------------------------------------------ 4-bit rows
+// A cache row x is stored as 4-bit codes with one fp32 scale: amax = max|x|,
+// inv = 7 / amax (0 when amax = 0), code = rint(inv * x) within +-7 (fp32
+// product, half to even), scale = amax / 7.  Two codes share a byte, element
+// 2i in the low nibble, each nibble in offset binary (code + 8), so widening
+// needs no sign handling.
+__device__ __forceinline__ float q4_inv(float amax) { return amax > 0.f ? __fdiv_rn(7.f, amax) : 0.f; }
+__device__ __forceinline__ float q4_scale(float amax) { return __fdiv_rn(amax, 7.f); }
+
+__device__ __forceinline__ uint32_t q4_nibble(float x, float inv)
+{
+    int c = __float2int_rn(__fmul_rn(inv, x));
+    c = max(-7, min(7, c));
+    return (uint32_t)(c + 8);
+}
+
+// 2K fp32 values -> K bytes of packed codes, little-endian (K = 2 or 4).
+template <int K>
+__device__ __forceinline__ uint32_t q4_pack(const float* x, float inv)
+{
+    uint32_t w = 0u;
+#pragma unroll
+    for (int i = 0; i < 2 * K; ++i) w |= q4_nibble(x[i], inv) << (4 * i);
+    return w;
+}
+
+// One 32-bit word of eight codes (elements 0..7) -> fp32, exactly, in the
+// order 0, 2, 4, 6, 1, 3, 5, 7: the even elements' nibbles are masked into
+// bytes, the odd ones' shifted down first; each byte becomes the low
+// mantissa byte of 2^23 and the bias (2^23 + 8) is subtracted two values at
+// a time.
+__device__ __forceinline__ void q4_unpack8(uint32_t w, float* f)
+{
+    const uint32_t lo = w & 0x0F0F0F0Fu;
+    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+    const float2 nb = make_float2(-8388616.f, -8388616.f);
+    const float2 a = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7540)),
+                                            __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7541))), nb);
+    const float2 b = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7542)),
+                                            __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7543))), nb);
+    const float2 c = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7540)),
+                                            __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7541))), nb);
+    const float2 d = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7542)),
+                                            __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7543))), nb);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
+// The low 16 bits of w hold four codes (elements 0..3) -> fp32 in element
+// order: (w | w << 12) & 0x0F0F0F0F puts elements 0, 2, 1, 3 in bytes 0..3.
+__device__ __forceinline__ void q4_unpack4(uint32_t w, float* f)
+{
+    const uint32_t x = (w | (w << 12)) & 0x0F0F0F0Fu;
+    const float2 nb = make_float2(-8388616.f, -8388616.f);
+    const float2 a = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540)),
+                                            __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7542))), nb);
+    const float2 b = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7541)),
+                                            __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7543))), nb);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+}
+
+// The low 8 bits of w hold two codes (elements 0, 1) -> fp32.
+__device__ __forceinline__ void q4_unpack2(uint32_t w, float* f)
+{
+    const uint32_t x = (w | (w << 12)) & 0x000F000Fu;
+    const float2 a = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540)),
+                                            __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7542))),
+                                make_float2(-8388616.f, -8388616.f));
+    f[0] = a.x; f[1] = a.y;
+}
+
 // Named CTA barriers (ids 1..15; id 0 is __syncthreads).  Memory
 // accesses made before the arrive are visible to the threads that pass the
 // sync.  The id is an immediate in the instruction (a register id makes the

@@ -75,14 +75,20 @@ struct Exchange {                 // every CTA has one; rank 0's is the meeting 
     float o[kMaxSplit][D];        // per-CTA unnormalised output
 };
 
-// Element a cache row is stored in: the input type, or int8 codes (Q8).
-template <typename T, bool Q8>
-using CacheElem = typename std::conditional<Q8, int8_t, T>::type;
+// Form of a cache row, QB: 0 = the input type, 8 = int8 codes, 4 = 4-bit
+// codes (two per byte, offset binary).  CacheElem is the element a row is
+// addressed in and RowElems<D, QB> the elements of one row.
+template <typename T, int QB>
+using CacheElem = typename std::conditional<QB == 8, int8_t,
+                  typename std::conditional<QB == 4, uint8_t, T>::type>::type;
 
-template <typename T, int D, class TL, bool Q8>
+template <int D, int QB>
+constexpr int RowElems = QB == 4 ? D / 2 : D;
+
+template <typename T, int D, class TL, int QB>
 struct Ring {
-    CacheElem<T, Q8> kbuf[TL::NW][TL::NBUF][kStage * D];   // per-warp ring of K rows
-    CacheElem<T, Q8> vbuf[TL::NW][TL::NBUF][kStage * D];   // per-warp ring of V rows
+    CacheElem<T, QB> kbuf[TL::NW][TL::NBUF][kStage * RowElems<D, QB>];   // per-warp ring of K rows
+    CacheElem<T, QB> vbuf[TL::NW][TL::NBUF][kStage * RowElems<D, QB>];   // per-warp ring of V rows
 };
 
 template <int D, class TL>
@@ -90,12 +96,12 @@ struct Epilogue {
     float wo[TL::NW][D];
 };
 
-template <typename T, int D, class TL, bool Q8>
+template <typename T, int D, class TL, int QB>
 struct DecodeSmem {
     // the epilogue buffers reuse the ring once every copy has landed and
     // been consumed (after the barrier that opens merge_warps)
     union {
-        Ring<T, D, TL, Q8> ring;
+        Ring<T, D, TL, QB> ring;
         Epilogue<D, TL> epi;
     } u;
     // the cluster exchange lies outside the ring, so other CTAs may write
@@ -103,8 +109,8 @@ struct DecodeSmem {
     Exchange<D> x;
     // this step's q, k, v rows, fetched in one round trip after the wait
     alignas(16) unsigned char in[3][D * sizeof(T)];
-    // Q8: {K scale, V scale} of every slot of a ring stage
-    alignas(16) float2 sbuf[Q8 ? TL::NW : 1][TL::NBUF][kStage];
+    // quantised rows: {K scale, V scale} of every slot of a ring stage
+    alignas(16) float2 sbuf[QB ? TL::NW : 1][TL::NBUF][kStage];
     uint64_t bar[TL::NW][TL::NBUF];
     float z[kMaxChunk];                     // base-2 logits of this CTA's slots
     alignas(16) float e[TL::NW][kStage];
@@ -292,7 +298,7 @@ __device__ __forceinline__ float row_dot(const E* row, const float (&qp)[D / 2],
     return zh + __shfl_xor_sync(kFull, zh, 16);
 }
 
-// int8 rows (Q8): a row of D codes is D / 16 chunks of 16.  Lane (r, h)
+// int8 rows (QB): a row of D codes is D / 16 chunks of 16.  Lane (r, h)
 // takes half hh = h ^ ((r / HCH) & 1) of row r -- the halves swap every HCH
 // rows -- and at step c reads chunk HCH * hh + (c ^ (r % HCH)), so the 8
 // lanes of one 16-byte shared-memory phase hit 8 different bank groups
@@ -412,22 +418,178 @@ __device__ __forceinline__ void store_row_q8(uint4 newrow, int tid, int8_t* Kc8,
     }
 }
 
+// 4-bit rows (QB 4): a row of D codes is D / 2 bytes, D / 32 chunks of 16
+// bytes (32 codes each), HC = D / 64 per half.  Lane (r, h) takes half
+// hh = h ^ ((r >> S) & 1) of row r and at step c reads chunk
+// HC * hh + (c ^ ((r >> (S + 1)) & (HC - 1))), S = log2(4 / HC): the rows'
+// own offsets separate r mod 4 / HC, the half and chunk swaps the rest, so
+// the 8 lanes of one 16-byte shared-memory phase hit 8 different bank
+// groups.  q is held per 32-bit code word in the order q4_unpack8 widens
+// (elements 0, 2, 4, 6, 1, 3, 5, 7), scaled to base-2 logits.
+template <int D>
+__device__ __forceinline__ int q4_chunk(int lane, int c)
+{
+    constexpr int HC = D / 64, SH = HC == 2 ? 1 : 2;
+    static_assert(HC == 1 || HC == 2, "head_dim 64 or 128");
+    const int r = lane & 15, h = lane >> 4;
+    const int hh = h ^ ((r >> SH) & 1);
+    return HC * hh + (c ^ ((r >> (SH + 1)) & (HC - 1)));
+}
+
+// element k of a code word in the widened order
+__device__ __forceinline__ constexpr int q4_elem(int k) { return k < 4 ? 2 * k : 2 * (k - 4) + 1; }
+
+template <typename T, int D>
+__device__ __forceinline__ void load_q_q4(const T* q, float scale, int lane, float (&qp)[D / 2])
+{
+    constexpr int HC = D / 64;
+#pragma unroll
+    for (int c = 0; c < HC; ++c) {
+        const T* src = q + q4_chunk<D>(lane, c) * 32;
+        float x[32];
+#pragma unroll
+        for (int v = 0; v < 32; v += 16 / (int)sizeof(T)) load_vec<T, 16 / (int)sizeof(T)>(src + v, &x[v]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) qp[c * 32 + 8 * i + k] = x[8 * i + q4_elem(k)] * scale;
+    }
+}
+
+// Dot of a 4-bit row (codes, unscaled) with the lane's half of q; every lane
+// returns the full dot of its row.  Each code word has its own accumulator
+// pair, summed in word order, then chunk_tree over the chunks: equal rows
+// give equal bits in every slot.
+template <int D>
+__device__ __forceinline__ float row_dot_q4(const uint8_t* row, const float (&qp)[D / 2], int lane)
+{
+    constexpr int HC = D / 64;
+    uint4 raw[HC];
+#pragma unroll
+    for (int c = 0; c < HC; ++c) raw[c] = *reinterpret_cast<const uint4*>(row + q4_chunk<D>(lane, c) * 16);
+    float part[HC];
+#pragma unroll
+    for (int c = 0; c < HC; ++c) {
+        const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+        float2 t[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float f[8];
+            q4_unpack8(u[i], f);
+            const float* qq = &qp[c * 32 + 8 * i];
+            t[i] = fma2(make_float2(qq[0], qq[1]), make_float2(f[0], f[1]), make_float2(0.f, 0.f));
+            t[i] = fma2(make_float2(qq[2], qq[3]), make_float2(f[2], f[3]), t[i]);
+            t[i] = fma2(make_float2(qq[4], qq[5]), make_float2(f[4], f[5]), t[i]);
+            t[i] = fma2(make_float2(qq[6], qq[7]), make_float2(f[6], f[7]), t[i]);
+        }
+        part[c] = ((t[0].x + t[0].y) + (t[1].x + t[1].y)) + ((t[2].x + t[2].y) + (t[3].x + t[3].y));
+    }
+    const float zh = chunk_tree<HC>(part);
+    return zh + __shfl_xor_sync(kFull, zh, 16);
+}
+
+// Dot of a row of T (the new token's key, in shared memory) with q held in
+// the 4-bit order.
+template <typename T, int D>
+__device__ __forceinline__ float row_dot_q4order(const T* row, const float (&qp)[D / 2], int lane)
+{
+    constexpr int HC = D / 64;
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < HC; ++c) {
+        const T* src = row + q4_chunk<D>(lane, c) * 32;
+        float x[32];
+#pragma unroll
+        for (int v = 0; v < 32; v += 16 / (int)sizeof(T)) load_vec<T, 16 / (int)sizeof(T)>(src + v, &x[v]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc = __fmaf_rn(qp[c * 32 + 8 * i + k], x[8 * i + q4_elem(k)], acc);
+    }
+    return acc + __shfl_xor_sync(kFull, acc, 16);
+}
+
+// As store_row_q8, for 4-bit rows: each thread's 16 bytes of T become
+// VE / 2 bytes of codes.
+template <typename T, int D>
+__device__ __forceinline__ void store_row_q4(uint4 newrow, int tid, uint8_t* Kc4, uint8_t* Vc4, float2* slot_scales,
+                                             int victim)
+{
+    constexpr int NV = D * (int)sizeof(T) / 16, VE = 16 / (int)sizeof(T);
+    static_assert(NV <= 32, "a row's threads must fit one warp");
+    float x[VE];
+    const uint32_t u[4] = {newrow.x, newrow.y, newrow.z, newrow.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if constexpr (sizeof(T) == 2) {
+            x[2 * i] = __uint_as_float(u[i] << 16);
+            x[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+        } else {
+            x[i] = __uint_as_float(u[i]);
+        }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < VE; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+    for (int o = NV / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+    const float inv = q4_inv(amax);
+    if (tid < 2 * NV) {
+        const bool isv = tid >= NV;
+        const int v = isv ? tid - NV : tid;
+        uint8_t* dst = (isv ? Vc4 : Kc4) + (size_t)victim * (D / 2) + v * (VE / 2);
+        if constexpr (VE == 8) *reinterpret_cast<uint32_t*>(dst) = q4_pack<4>(x, inv);
+        else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)q4_pack<2>(x, inv);
+        if (v == 0) reinterpret_cast<float*>(slot_scales + victim)[isv ? 1 : 0] = q4_scale(amax);
+    }
+}
+
+// Quantised-row dispatch: QB 8 or 4.
+template <int QB, typename T, int D>
+__device__ __forceinline__ void load_q_quant(const T* q, float scale, int lane, float (&qp)[D / 2])
+{
+    if constexpr (QB == 8) load_q_q8<T, D>(q, scale, lane, qp);
+    else load_q_q4<T, D>(q, scale, lane, qp);
+}
+
+template <int QB, int D, typename E>
+__device__ __forceinline__ float row_dot_quant(const E* row, const float (&qp)[D / 2], int lane)
+{
+    if constexpr (QB == 8) return row_dot_q8<D>(row, qp, lane);
+    else return row_dot_q4<D>(row, qp, lane);
+}
+
+template <int QB, typename T, int D>
+__device__ __forceinline__ float row_dot_quant_order(const T* row, const float (&qp)[D / 2], int lane)
+{
+    if constexpr (QB == 8) return row_dot_q8order<T, D>(row, qp, lane);
+    else return row_dot_q4order<T, D>(row, qp, lane);
+}
+
+template <int QB, typename T, int D, typename E>
+__device__ __forceinline__ void store_row_quant(uint4 newrow, int tid, E* Kc, E* Vc, float2* slot_scales, int victim)
+{
+    if constexpr (QB == 8) store_row_q8<T, D>(newrow, tid, Kc, Vc, slot_scales, victim);
+    else store_row_q4<T, D>(newrow, tid, Kc, Vc, slot_scales, victim);
+}
+
 // Bulk copies of one stage (slots s .. min(s + 16, f1) - 1) into this warp's
 // ring buffer b: K and V rows and, for int8 rows, the slots' scale pairs
 // (an even count, so the copy stays a multiple of 16 bytes; the scale rows
 // are padded to an even length).
-template <typename T, int D, class TL, bool Q8>
-__device__ __forceinline__ void issue_stage(DecodeSmem<T, D, TL, Q8>& S, const CacheElem<T, Q8>* Kc,
-                                            const CacheElem<T, Q8>* Vc, const float2* Sc, int s, int f1, int b)
+template <typename T, int D, class TL, int QB>
+__device__ __forceinline__ void issue_stage(DecodeSmem<T, D, TL, QB>& S, const CacheElem<T, QB>* Kc,
+                                            const CacheElem<T, QB>* Vc, const float2* Sc, int s, int f1, int b)
 {
     const int warp = threadIdx.x >> 5;
     const int rows = min(kStage, f1 - s);
-    const uint32_t bytes = (uint32_t)(rows * D * sizeof(CacheElem<T, Q8>));
-    const uint32_t sbytes = Q8 ? (uint32_t)(((rows + 1) & ~1) * sizeof(float2)) : 0u;
+    constexpr int RE = RowElems<D, QB>;
+    const uint32_t bytes = (uint32_t)(rows * RE * sizeof(CacheElem<T, QB>));
+    const uint32_t sbytes = QB ? (uint32_t)(((rows + 1) & ~1) * sizeof(float2)) : 0u;
     mbar_arrive_expect_tx(&S.bar[warp][b], 2 * bytes + sbytes);
-    bulk_g2s(S.u.ring.kbuf[warp][b], Kc + (size_t)s * D, bytes, &S.bar[warp][b]);
-    bulk_g2s(S.u.ring.vbuf[warp][b], Vc + (size_t)s * D, bytes, &S.bar[warp][b]);
-    if constexpr (Q8) bulk_g2s(S.sbuf[warp][b], Sc + s, sbytes, &S.bar[warp][b]);
+    bulk_g2s(S.u.ring.kbuf[warp][b], Kc + (size_t)s * RE, bytes, &S.bar[warp][b]);
+    bulk_g2s(S.u.ring.vbuf[warp][b], Vc + (size_t)s * RE, bytes, &S.bar[warp][b]);
+    if constexpr (QB != 0) bulk_g2s(S.sbuf[warp][b], Sc + s, sbytes, &S.bar[warp][b]);
 }
 
 // Per-warp streaming softmax over the rows this CTA fetched, [f0, f1); only
@@ -437,9 +599,9 @@ __device__ __forceinline__ void issue_stage(DecodeSmem<T, D, TL, Q8>& S, const C
 // 2^8), so most stages need no cross-lane max.  l_lane is this lane's share
 // of the normaliser (lanes 0..15 count their slot once); o holds the lane's
 // EPL output columns lane*EPL.. of the unnormalised sum, relative to m_ref.
-template <typename T, int D, class TL, bool Q8>
-__device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, Q8>& S, const CacheElem<T, Q8>* Kc,
-                                             const CacheElem<T, Q8>* Vc, const float2* Sc,
+template <typename T, int D, class TL, int QB>
+__device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, QB>& S, const CacheElem<T, QB>* Kc,
+                                             const CacheElem<T, QB>* Vc, const float2* Sc,
                                              int f0, int f1, int n, int skip, bool keep_z,
                                              const float (&qp)[D / 2], float& m_ref,
                                              float& l_lane, float (&o)[D / 32], int* err)
@@ -479,7 +641,7 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, Q8>& S, const 
             const auto* kst = S.u.ring.kbuf[warp][b];
             const auto* vst = S.u.ring.vbuf[warp][b];
             float z;
-            if constexpr (Q8) z = row_dot_q8<D>(kst + r * D, qp, lane) * S.sbuf[warp][b][r].x;
+            if constexpr (QB != 0) z = row_dot_quant<QB, D>(kst + r * RowElems<D, QB>, qp, lane) * S.sbuf[warp][b][r].x;
             else z = row_dot<T, D, T>(kst + r * D, qp, lane);
             if (r >= gl || f0 + s0 + r == skip) z = -INFINITY;
             if (__any_sync(kFull, z > m_ref + 8.f)) {
@@ -499,7 +661,7 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, Q8>& S, const 
             if (h == 0) {
                 l_lane += er;
                 // int8 values: the slot's V scale is folded into its weight
-                if constexpr (Q8) S.e[warp][r] = er * S.sbuf[warp][b][r].y;
+                if constexpr (QB != 0) S.e[warp][r] = er * S.sbuf[warp][b][r].y;
                 else S.e[warp][r] = er;
                 if (keep_z && r < gl) S.z[s0 + r] = z;
             }
@@ -510,17 +672,22 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, Q8>& S, const 
                 const float4 e4 = *reinterpret_cast<const float4*>(&S.e[warp][j]);
                 ev[j] = e4.x; ev[j + 1] = e4.y; ev[j + 2] = e4.z; ev[j + 3] = e4.w;
             }
-            if constexpr (Q8) {
-                // int8 values (weights already carry the V scales); a full
-                // stage loads each half's code words before the first
+            if constexpr (QB != 0) {
+                // quantised values (weights already carry the V scales); a
+                // full stage loads each half's code words before the first
                 // widening, as the bf16 path does
+                constexpr int RE = RowElems<D, QB>;
                 auto v_word = [&](int j) -> uint32_t {
-                    if constexpr (EPL == 4) return *reinterpret_cast<const uint32_t*>(vst + j * D + lane * EPL);
-                    else return (uint32_t)*reinterpret_cast<const uint16_t*>(vst + j * D + lane * EPL);
+                    if constexpr (QB == 8 && EPL == 4) return *reinterpret_cast<const uint32_t*>(vst + j * RE + lane * EPL);
+                    else if constexpr (QB == 8) return (uint32_t)*reinterpret_cast<const uint16_t*>(vst + j * RE + lane * EPL);
+                    else if constexpr (EPL == 4) return (uint32_t)*reinterpret_cast<const uint16_t*>(vst + j * RE + lane * 2);
+                    else return (uint32_t)vst[j * RE + lane];
                 };
                 auto v_acc = [&](uint32_t w, float p, bool odd) {
                     float vr[4];
-                    q8_unpack4(w, vr);
+                    if constexpr (QB == 8) q8_unpack4(w, vr);
+                    else if constexpr (EPL == 4) q4_unpack4(w, vr);
+                    else q4_unpack2(w, vr);
                     vfma(p, vr, odd);
                 };
                 if (gl == kStage) {
@@ -572,7 +739,7 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, Q8>& S, const 
         // refill this buffer with the warp's stage NBUF rounds ahead
         if (lane == 0) {
             const int gn = g + NW * NBUF;
-            if (gn < nst) issue_stage<T, D, TL, Q8>(S, Kc, Vc, Sc, f0 + gn * kStage, f1, b);
+            if (gn < nst) issue_stage<T, D, TL, QB>(S, Kc, Vc, Sc, f0 + gn * kStage, f1, b);
         }
     }
 #pragma unroll
@@ -582,9 +749,9 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, Q8>& S, const 
 // Kick off ring buffers [b_lo, b_hi) of each warp -- by default all NBUF --
 // with their first stages (called by lane 0 of every warp after its barriers
 // are initialised).
-template <typename T, int D, class TL, bool Q8>
-__device__ __forceinline__ void prime_ring(DecodeSmem<T, D, TL, Q8>& S, const CacheElem<T, Q8>* Kc,
-                                           const CacheElem<T, Q8>* Vc, const float2* Sc,
+template <typename T, int D, class TL, int QB>
+__device__ __forceinline__ void prime_ring(DecodeSmem<T, D, TL, QB>& S, const CacheElem<T, QB>* Kc,
+                                           const CacheElem<T, QB>* Vc, const float2* Sc,
                                            int c0, int c1, int b_lo = 0, int b_hi = TL::NBUF)
 {
     const int warp = threadIdx.x >> 5;
@@ -593,13 +760,13 @@ __device__ __forceinline__ void prime_ring(DecodeSmem<T, D, TL, Q8>& S, const Ca
     for (int b = 0; b < TL::NBUF; ++b) {
         if (b < b_lo || b >= b_hi) continue;
         const int g = warp + TL::NW * b;
-        if (g < nst) issue_stage<T, D, TL, Q8>(S, Kc, Vc, Sc, c0 + g * kStage, c1, b);
+        if (g < nst) issue_stage<T, D, TL, QB>(S, Kc, Vc, Sc, c0 + g * kStage, c1, b);
     }
 }
 
 // Merge the warps' softmax states; threads < D get their output column.
-template <typename T, int D, class TL, bool Q8>
-__device__ __forceinline__ void merge_warps(DecodeSmem<T, D, TL, Q8>& S, float m_run, float l_run,
+template <typename T, int D, class TL, int QB>
+__device__ __forceinline__ void merge_warps(DecodeSmem<T, D, TL, QB>& S, float m_run, float l_run,
                                             const float (&o)[D / 32], float& Mc, float& Lc,
                                             float& Oc)
 {
@@ -659,11 +826,11 @@ __device__ __forceinline__ void fetch_range(int B, int C, int rank, int& f0, int
 // uniform share, P (n + 1) > 1; the victim is the candidate with the fewest
 // set bits, then the lowest position; the new token's history is its own
 // flag.
-template <typename T, int D, class TL, bool Q8, bool GQ, bool SH = false>
+template <typename T, int D, class TL, int QB, bool GQ, bool SH = false>
 __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const DecodeArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    auto& S = *reinterpret_cast<DecodeSmem<T, D, TL, Q8>*>(smem_raw);
+    auto& S = *reinterpret_cast<DecodeSmem<T, D, TL, QB>*>(smem_raw);
     constexpr int EPL = D / 32;
     constexpr int NV = D * (int)sizeof(T) / 16;          // 16-byte vectors per row
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -675,10 +842,10 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
 
     const int B = c.B;
     const size_t ub = (size_t)unit * B;
-    using CE = CacheElem<T, Q8>;
-    CE* Kc = reinterpret_cast<CE*>(c.K) + ub * D;
-    CE* Vc = reinterpret_cast<CE*>(c.V) + ub * D;
-    float2* Sc = Q8 ? c.kvs + (size_t)unit * c.Bp : nullptr;   // slot scale pairs
+    using CE = CacheElem<T, QB>;
+    CE* Kc = reinterpret_cast<CE*>(c.K) + ub * RowElems<D, QB>;
+    CE* Vc = reinterpret_cast<CE*>(c.V) + ub * RowElems<D, QB>;
+    float2* Sc = QB ? c.kvs + (size_t)unit * c.Bp : nullptr;   // slot scale pairs
     // this unit's budget and recent window: the cache's own, or the unit's
     // policy (per-head policies; then the unit uses Bu of its B slots)
     int Bu = B, ru = c.r;
@@ -743,7 +910,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     // query row, requested right after the wait, then queues behind less
     // traffic, and the remaining buffers keep HBM busy while it is in flight.
     if (a.early) {
-        if (lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, 0, 1);
+        if (lane == 0) prime_ring<T, D, TL, QB>(S, Kc, Vc, Sc, f0, f1, 0, 1);
         read_cache();
     }
     // everything below may read memory the previous kernel in the stream
@@ -752,13 +919,13 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     grid_launch_dependents();
     if (!a.early) {
         if (c.upol) unit_ranges();
-        if (lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1);
+        if (lane == 0) prime_ring<T, D, TL, QB>(S, Kc, Vc, Sc, f0, f1);
         read_cache();
     }
     // q, k, v in one round trip (requested before the rest of the ring)
     {
         const uint4 w = load_rows_16b<T, D>(qg, kg, vg, tid);
-        if (a.early && lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, 1, TL::NBUF);
+        if (a.early && lane == 0) prime_ring<T, D, TL, QB>(S, Kc, Vc, Sc, f0, f1, 1, TL::NBUF);
         store_rows_16b<T, D>(S.in, w, tid);
     }
     __syncthreads();
@@ -766,8 +933,8 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     const T* ks = reinterpret_cast<const T*>(S.in[1]);
     const T* vs = reinterpret_cast<const T*>(S.in[2]);
     float qp[D / 2];
-    if constexpr (Q8) {
-        load_q_q8<T, D>(qs, c.qscale, lane, qp);
+    if constexpr (QB != 0) {
+        load_q_quant<QB, T, D>(qs, c.qscale, lane, qp);
     } else {
         QRaw<T, D> qraw;
         load_q_raw<T, D>(qs, lane, qraw);
@@ -787,7 +954,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     if ((GQ || rank == 0) && warp == 0) {  // the new token attends to itself
         float vr[EPL];
         float zn;
-        if constexpr (Q8) zn = row_dot_q8order<T, D>(ks, qp, lane);
+        if constexpr (QB != 0) zn = row_dot_quant_order<QB, T, D>(ks, qp, lane);
         else zn = row_dot<T, D, T>(ks, qp, lane);
         load_vec<T, EPL>(vs + lane * EPL, vr);
         m_run = zn;
@@ -798,10 +965,10 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     }
     __syncwarp();
 
-    attend_chunk<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, n, -1, true, qp, m_run, l_run, o, c.err);
+    attend_chunk<T, D, TL, QB>(S, Kc, Vc, Sc, f0, f1, n, -1, true, qp, m_run, l_run, o, c.err);
 
     float Mc, Lc, Oc;
-    merge_warps<T, D, TL, Q8>(S, m_run, l_run, o, Mc, Lc, Oc);
+    merge_warps<T, D, TL, QB>(S, m_run, l_run, o, Mc, Lc, Oc);
     if (C > 1) cluster_wait();               // every CTA of the cluster runs (arrive at the start)
     const uint32_t x0 = map_to_rank(&S.x, 0);
 
@@ -817,8 +984,8 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
             c.ustate[unit] = make_int2(min(n + 1, Bu), p + 1);
             if (a.victim_out) a.victim_out[unit] = full ? victim : -1;
         }
-        if constexpr (Q8) {
-            store_row_q8<T, D>(newrow, tid, Kc, Vc, Sc, victim);
+        if constexpr (QB != 0) {
+            store_row_quant<QB, T, D>(newrow, tid, Kc, Vc, Sc, victim);
         } else {
             if (tid < NV)
                 reinterpret_cast<uint4*>(Kc + (size_t)victim * D)[tid] = newrow;
@@ -1465,11 +1632,11 @@ __global__ void __launch_bounds__(GqaShape<G>::NT, 1) gqa_decode_kernel(const De
 
 // ------------------------------------------------------------------ LSH
 
-template <typename T, int D, class TL, bool Q8>
+template <typename T, int D, class TL, int QB>
 __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const DecodeArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    auto& S = *reinterpret_cast<DecodeSmem<T, D, TL, Q8>*>(smem_raw);
+    auto& S = *reinterpret_cast<DecodeSmem<T, D, TL, QB>*>(smem_raw);
     constexpr int EPL = D / 32;
     constexpr int NV = D * (int)sizeof(T) / 16;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1480,10 +1647,10 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
 
     const int B = c.B;
     const size_t ub = (size_t)unit * B;
-    using CE = CacheElem<T, Q8>;
-    CE* Kc = reinterpret_cast<CE*>(c.K) + ub * D;
-    CE* Vc = reinterpret_cast<CE*>(c.V) + ub * D;
-    float2* Sc = Q8 ? c.kvs + (size_t)unit * c.Bp : nullptr;   // slot scale pairs
+    using CE = CacheElem<T, QB>;
+    CE* Kc = reinterpret_cast<CE*>(c.K) + ub * RowElems<D, QB>;
+    CE* Vc = reinterpret_cast<CE*>(c.V) + ub * RowElems<D, QB>;
+    float2* Sc = QB ? c.kvs + (size_t)unit * c.Bp : nullptr;   // slot scale pairs
     int f0, f1;
     fetch_range(B, C, rank, f0, f1);
     if (lane == 0) {
@@ -1535,7 +1702,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
     // decided, and HBM then idled until the attention started).
     if (a.early) {
         read_state();
-        if (lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, 0, 1);
+        if (lane == 0) prime_ring<T, D, TL, QB>(S, Kc, Vc, Sc, f0, f1, 0, 1);
     }
     // everything below may read memory the previous kernel in the stream
     // has written (the inputs, and the cache unless read above)
@@ -1547,7 +1714,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
     {
         const uint4 w = load_rows_16b<T, D>(qg, kg, vg, tid);
         if (!a.early) read_state();
-        if (lane == 0) prime_ring<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, a.early ? 1 : 0, TL::NBUF);
+        if (lane == 0) prime_ring<T, D, TL, QB>(S, Kc, Vc, Sc, f0, f1, a.early ? 1 : 0, TL::NBUF);
         store_rows_16b<T, D>(S.in, w, tid);
     }
     __syncthreads();
@@ -1641,7 +1808,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
     __syncthreads();
     const int victim = S.victim;
     float qp[D / 2];
-    if constexpr (Q8) load_q_q8<T, D>(qs, c.qscale, lane, qp);
+    if constexpr (QB != 0) load_q_quant<QB, T, D>(qs, c.qscale, lane, qp);
     else widen_q<T, D>(qraw, c.qscale, qp);
 
     float m_run = -INFINITY, l_run = 0.f, o[EPL];
@@ -1649,7 +1816,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
     for (int e = 0; e < EPL; ++e) o[e] = 0.f;
     if (rank == 0 && warp == 0) {          // the new token, now in the victim slot
         float zn;
-        if constexpr (Q8) zn = row_dot_q8order<T, D>(ks, qp, lane);
+        if constexpr (QB != 0) zn = row_dot_quant_order<QB, T, D>(ks, qp, lane);
         else zn = row_dot<T, D, T>(ks, qp, lane);
         float vr[EPL];
         load_vec<T, EPL>(vs + lane * EPL, vr);
@@ -1660,11 +1827,11 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
     }
     __syncwarp();
 
-    attend_chunk<T, D, TL, Q8>(S, Kc, Vc, Sc, f0, f1, n, full ? victim : -1, false, qp, m_run, l_run, o,
+    attend_chunk<T, D, TL, QB>(S, Kc, Vc, Sc, f0, f1, n, full ? victim : -1, false, qp, m_run, l_run, o,
                            c.err);
 
     float Mc, Lc, Oc;
-    merge_warps<T, D, TL, Q8>(S, m_run, l_run, o, Mc, Lc, Oc);
+    merge_warps<T, D, TL, QB>(S, m_run, l_run, o, Mc, Lc, Oc);
 
     if (C > 1) {
         cluster_wait();                      // every CTA of the cluster runs (arrive at the start)
@@ -1699,8 +1866,8 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
         c.ustate[unit] = make_int2(min(n + 1, B), p + 1);
         if (a.victim_out) a.victim_out[unit] = full ? victim : -1;
     }
-    if constexpr (Q8) {
-        store_row_q8<T, D>(newrow, tid, Kc, Vc, Sc, victim);
+    if constexpr (QB != 0) {
+        store_row_quant<QB, T, D>(newrow, tid, Kc, Vc, Sc, victim);
     } else {
         if (tid < NV)
             reinterpret_cast<uint4*>(Kc + (size_t)victim * D)[tid] = newrow;
@@ -1720,6 +1887,10 @@ using TileMany = Tile<4, 3>;
 // stages keep as many bytes in flight as the bf16 tiles
 using TileQ8 = Tile<5, 4>;
 using TileQ8Few = Tile<8, 4>;
+// 4-bit rows: a quarter of the bf16 bytes per stage; six warps measured
+// faster than five or eight
+using TileQ4 = Tile<6, 4>;
+using TileQ4Few = Tile<8, 4>;
 
 // Tile for bf16 rows of 128 (numbers as H2O_DECODE_TILE): TileFew when the
 // units do not fill the SMs, TileMany from four units per SM on, else the
@@ -1754,14 +1925,14 @@ int tile_variant()
     return v;
 }
 
-template <typename T, int D, bool LSH, class TL, bool Q8 = false, bool GQ = false, bool SH = false>
+template <typename T, int D, bool LSH, class TL, int QB = 0, bool GQ = false, bool SH = false>
 cudaError_t launch_decode_t(const DecodeArgs& a, int split, cudaStream_t st)
 {
     void (*kern)(const DecodeArgs);
-    if constexpr (LSH) kern = lsh_decode_kernel<T, D, TL, Q8>;
-    else kern = h2o_decode_kernel<T, D, TL, Q8, GQ, SH>;
+    if constexpr (LSH) kern = lsh_decode_kernel<T, D, TL, QB>;
+    else kern = h2o_decode_kernel<T, D, TL, QB, GQ, SH>;
     if constexpr (GQ) split = a.G;             // one CTA per query head of a cache unit
-    const size_t smem = sizeof(DecodeSmem<T, D, TL, Q8>);
+    const size_t smem = sizeof(DecodeSmem<T, D, TL, QB>);
     static bool configured[64] = {false};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1852,6 +2023,24 @@ bool gqa_one_pass()
     return v == 1;
 }
 
+// One row form QB over the dtypes and head sizes: tile TL, or TLF for bf16
+// rows of 128 with fewer units than SMs (one-head caches).
+template <bool LSH, int QB, class TL, class TLF, bool GQ = false>
+cudaError_t dispatch_form(const DecodeArgs& a, int split, cudaStream_t st)
+{
+    const bool bf = a.c.dtype == 1;
+    if (a.c.D == 128) {
+        if (!GQ && bf && a.num_sms > 0 && a.c.U < a.num_sms)
+            return launch_decode_t<__nv_bfloat16, 128, LSH, TLF, QB, GQ>(a, split, st);
+        return bf ? launch_decode_t<__nv_bfloat16, 128, LSH, TL, QB, GQ>(a, split, st)
+                  : launch_decode_t<float, 128, LSH, TL, QB, GQ>(a, split, st);
+    }
+    if (a.c.D == 64)
+        return bf ? launch_decode_t<__nv_bfloat16, 64, LSH, TL, QB, GQ>(a, split, st)
+                  : launch_decode_t<float, 64, LSH, TL, QB, GQ>(a, split, st);
+    return cudaErrorInvalidValue;
+}
+
 template <bool LSH>
 cudaError_t dispatch(const DecodeArgs& a, int split, cudaStream_t st)
 {
@@ -1863,43 +2052,21 @@ cudaError_t dispatch(const DecodeArgs& a, int split, cudaStream_t st)
             // (4 heads on fewer units than half the SMs: the cluster path below
             // measured faster -- each of its CTAs walks fewer stages)
             const bool small4 = a.G == 4 && a.num_sms > 0 && 2 * a.c.U < a.num_sms;
-            if (a.c.D == 128 && bf && !a.c.kv8 && gqa_one_pass() && !small4) {
+            if (a.c.D == 128 && bf && a.c.qbits == 0 && gqa_one_pass() && !small4) {
                 if (a.G == 2) return launch_gqa_t<__nv_bfloat16, 128, 2>(a, st);
                 if (a.G == 4) return launch_gqa_t<__nv_bfloat16, 128, 4>(a, st);
                 if (a.G == 8) return launch_gqa_t<__nv_bfloat16, 128, 8>(a, st);
             }
             // grouped-query cache (default tile), one CTA per query head: every dtype and row form
-            if (a.c.D == 128) {
-                if (a.c.kv8)
-                    return bf ? launch_decode_t<__nv_bfloat16, 128, false, TileDefault, true, true>(a, split, st)
-                              : launch_decode_t<float, 128, false, TileDefault, true, true>(a, split, st);
-                return bf ? launch_decode_t<__nv_bfloat16, 128, false, TileDefault, false, true>(a, split, st)
-                          : launch_decode_t<float, 128, false, TileDefault, false, true>(a, split, st);
-            }
-            if (a.c.D == 64) {
-                if (a.c.kv8)
-                    return bf ? launch_decode_t<__nv_bfloat16, 64, false, TileDefault, true, true>(a, split, st)
-                              : launch_decode_t<float, 64, false, TileDefault, true, true>(a, split, st);
-                return bf ? launch_decode_t<__nv_bfloat16, 64, false, TileDefault, false, true>(a, split, st)
-                          : launch_decode_t<float, 64, false, TileDefault, false, true>(a, split, st);
-            }
-            return cudaErrorInvalidValue;
+            if (a.c.qbits == 8) return dispatch_form<false, 8, TileDefault, TileDefault, true>(a, split, st);
+            if (a.c.qbits == 4) return dispatch_form<false, 4, TileDefault, TileDefault, true>(a, split, st);
+            return dispatch_form<false, 0, TileDefault, TileDefault, true>(a, split, st);
         }
     }
-    if (a.c.kv8) {
-        // int8 cache rows: one CTA per SM with 8 warps when the units do not
-        // fill the SMs (bf16 rows of 128), else 5 warps x 4 stages (two CTAs
-        // per SM: 6 x 4 would not fit twice)
-        if (a.c.D == 128 && bf && a.num_sms > 0 && a.c.U < a.num_sms)
-            return launch_decode_t<__nv_bfloat16, 128, LSH, TileQ8Few, true>(a, split, st);
-        if (a.c.D == 128)
-            return bf ? launch_decode_t<__nv_bfloat16, 128, LSH, TileQ8, true>(a, split, st)
-                      : launch_decode_t<float, 128, LSH, TileQ8, true>(a, split, st);
-        if (a.c.D == 64)
-            return bf ? launch_decode_t<__nv_bfloat16, 64, LSH, TileQ8, true>(a, split, st)
-                      : launch_decode_t<float, 64, LSH, TileQ8, true>(a, split, st);
-        return cudaErrorInvalidValue;
-    }
+    // quantised rows: one CTA per SM with 8 warps when the units do not fill
+    // the SMs (bf16 rows of 128), else 5 (int8) or 6 (4-bit) warps x 4 stages
+    if (a.c.qbits == 8) return dispatch_form<LSH, 8, TileQ8, TileQ8Few>(a, split, st);
+    if (a.c.qbits == 4) return dispatch_form<LSH, 4, TileQ4, TileQ4Few>(a, split, st);
     if (a.c.D == 128 && bf) {
         switch (tile_variant() ? tile_variant() : auto_tile(a.c.U, a.num_sms)) {
         case 1: return launch_decode_t<__nv_bfloat16, 128, LSH, Tile<4, 2>>(a, split, st);
@@ -1944,15 +2111,15 @@ int max_decode_split() { return kMaxSplit; }
 namespace {
 
 // Largest number of clusters of `split` CTAs of the few-units H2O or
-// HashEvict kernel (bf16, head_dim 128; TileFew, or TileQ8Few for int8
-// rows) that the device runs at once; 0 on error.
-template <class TL, bool Q8>
+// HashEvict kernel (bf16, head_dim 128; TileFew, or TileQ8Few / TileQ4Few
+// for int8 / 4-bit rows) that the device runs at once; 0 on error.
+template <class TL, int QB>
 int clusters_that_fit_t(int split, bool lsh)
 {
     void (*kern)(const DecodeArgs);
-    if (lsh) kern = lsh_decode_kernel<__nv_bfloat16, 128, TL, Q8>;
-    else kern = h2o_decode_kernel<__nv_bfloat16, 128, TL, Q8, false>;
-    const size_t smem = sizeof(DecodeSmem<__nv_bfloat16, 128, TL, Q8>);
+    if (lsh) kern = lsh_decode_kernel<__nv_bfloat16, 128, TL, QB>;
+    else kern = h2o_decode_kernel<__nv_bfloat16, 128, TL, QB, false>;
+    const size_t smem = sizeof(DecodeSmem<__nv_bfloat16, 128, TL, QB>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
         cudaGetLastError();
@@ -1977,9 +2144,11 @@ int clusters_that_fit_t(int split, bool lsh)
     return n;
 }
 
-int clusters_that_fit(int split, bool lsh, bool q8)
+int clusters_that_fit(int split, bool lsh, int qbits)
 {
-    return q8 ? clusters_that_fit_t<TileQ8Few, true>(split, lsh) : clusters_that_fit_t<TileFew, false>(split, lsh);
+    if (qbits == 8) return clusters_that_fit_t<TileQ8Few, 8>(split, lsh);
+    if (qbits == 4) return clusters_that_fit_t<TileQ4Few, 4>(split, lsh);
+    return clusters_that_fit_t<TileFew, 0>(split, lsh);
 }
 
 }  // namespace
@@ -1989,10 +2158,10 @@ int clusters_that_fit(int split, bool lsh, bool q8)
 // per unit with all U clusters resident at once (clusters are placed within
 // a GPC, so U * split <= num_sms alone does not ensure it), at least one
 // CTA per 1024 slots.  Results are cached per (device, U, B, kernel).
-int few_units_split(int U, int B, int num_sms, bool lsh, bool q8)
+int few_units_split(int U, int B, int num_sms, bool lsh, int qbits)
 {
     struct Entry { int dev, U, B, lsh, split; };
-    const int key = (lsh ? 1 : 0) | (q8 ? 2 : 0);
+    const int key = (lsh ? 1 : 0) | (qbits << 1);
     static std::mutex mu;
     static Entry cache[64];
     static int n_cache = 0;
@@ -2007,7 +2176,7 @@ int few_units_split(int U, int B, int num_sms, bool lsh, bool q8)
     const int lo = max(1, (B + kMaxChunk - 1) / kMaxChunk);
     const int hi = max(1, (B + 63) / 64);
     int s = min(kMaxSplit, min(hi, max(lo, num_sms / max(U, 1))));
-    while (s > lo && clusters_that_fit(s, lsh, q8) < U) --s;
+    while (s > lo && clusters_that_fit(s, lsh, qbits) < U) --s;
     std::lock_guard<std::mutex> lock(mu);
     if (n_cache < 64) cache[n_cache++] = Entry{dev, U, B, key, s};
     return s;
@@ -2041,13 +2210,13 @@ cudaError_t launch_lsh_decode(const DecodeArgs& a, int split, cudaStream_t st)
 cudaError_t launch_sh_decode(const DecodeArgs& a, int split, cudaStream_t st)
 {
     const bool bf = a.c.dtype == 1;
-    if (a.c.kv8 || a.G > 1) return cudaErrorInvalidValue;
+    if (a.c.qbits || a.G > 1) return cudaErrorInvalidValue;
     if (a.c.D == 128)
-        return bf ? launch_decode_t<__nv_bfloat16, 128, false, TileDefault, false, false, true>(a, split, st)
-                  : launch_decode_t<float, 128, false, TileDefault, false, false, true>(a, split, st);
+        return bf ? launch_decode_t<__nv_bfloat16, 128, false, TileDefault, 0, false, true>(a, split, st)
+                  : launch_decode_t<float, 128, false, TileDefault, 0, false, true>(a, split, st);
     if (a.c.D == 64)
-        return bf ? launch_decode_t<__nv_bfloat16, 64, false, TileDefault, false, false, true>(a, split, st)
-                  : launch_decode_t<float, 64, false, TileDefault, false, false, true>(a, split, st);
+        return bf ? launch_decode_t<__nv_bfloat16, 64, false, TileDefault, 0, false, true>(a, split, st)
+                  : launch_decode_t<float, 64, false, TileDefault, 0, false, true>(a, split, st);
     return cudaErrorInvalidValue;
 }
 

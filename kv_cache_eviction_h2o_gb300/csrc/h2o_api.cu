@@ -118,8 +118,8 @@ struct h2o_ctx {
     void* K;
     void* V;
     float2* score;             // hi + lo fp32 pairs
-    float2* kvs;               // int8 cache: {K scale, V scale} per slot, [U][Bp]
-    int kv8, Bp;
+    float2* kvs;               // quantised cache: {K scale, V scale} per slot, [U][Bp]
+    int qbits, Bp;             // 8 / 4: rows stored as int8 / 4-bit codes; 0: the input type
     int* pos;
     uint32_t* code;
     int2* ustate;
@@ -148,6 +148,15 @@ struct h2o_ctx {
 namespace {
 
 size_t elem_size(int dtype) { return dtype == H2O_BF16 ? 2 : 4; }
+
+// Bytes of one stored K or V row: the input type, int8 codes, or packed
+// 4-bit codes.
+size_t row_bytes(const h2o_ctx* h)
+{
+    if (h->qbits == 8) return (size_t)h->D;
+    if (h->qbits == 4) return (size_t)h->D / 2;
+    return (size_t)h->D * elem_size(h->dtype);
+}
 
 int dev_alloc(void** p, size_t bytes, const char* what)
 {
@@ -197,7 +206,7 @@ CacheView view(const h2o_ctx* h)
 {
     CacheView v;
     v.K = h->K; v.V = h->V; v.score = h->score; v.pos = h->pos; v.code = h->code;
-    v.kvs = h->kvs; v.kv8 = h->kv8; v.Bp = h->Bp;
+    v.kvs = h->kvs; v.qbits = h->qbits; v.Bp = h->Bp;
     v.ustate = h->ustate; v.err = h->err;
     v.U = h->U; v.B = h->B; v.D = h->D; v.dtype = h->dtype; v.r = h->r;
     v.upol = h->upol;
@@ -222,11 +231,13 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
     if (batch < 1 || heads < 1) return fail(H2O_ERR_ARG, "batch and heads must be >= 1");
     if ((long long)batch * heads * groups > (1LL << 24)) return fail(H2O_ERR_ARG, "batch * heads too large");
     if (head_dim != 64 && head_dim != 128) return fail(H2O_ERR_ARG, "head_dim must be 64 or 128 (got %d)", head_dim);
-    if ((dtype & ~(H2O_BF16 | H2O_KV8)) != 0)
-        return fail(H2O_ERR_ARG, "dtype must be H2O_F32 or H2O_BF16, optionally | H2O_KV8");
-    const int kv8 = (dtype & H2O_KV8) ? 1 : 0;
-    if (kind == kSH && kv8) return fail(H2O_ERR_UNSUPPORTED, "H2O_KV8 is not supported on persistence-of-importance handles");
-    if (kind == kFG && kv8) return fail(H2O_ERR_UNSUPPORTED, "H2O_KV8 is not supported on per-head policy handles");
+    if ((dtype & ~(H2O_BF16 | H2O_KV8 | H2O_KV4)) != 0 || (dtype & (H2O_KV8 | H2O_KV4)) == (H2O_KV8 | H2O_KV4))
+        return fail(H2O_ERR_ARG, "dtype must be H2O_F32 or H2O_BF16, optionally | H2O_KV8 or | H2O_KV4");
+    const int qbits = (dtype & H2O_KV8) ? 8 : (dtype & H2O_KV4) ? 4 : 0;
+    if (kind == kSH && qbits)
+        return fail(H2O_ERR_UNSUPPORTED, "H2O_KV8 / H2O_KV4 are not supported on persistence-of-importance handles");
+    if (kind == kFG && qbits)
+        return fail(H2O_ERR_UNSUPPORTED, "H2O_KV8 / H2O_KV4 are not supported on per-head policy handles");
     if (kind == kFG && (full_budget < 1 || full_budget >= (1 << 20)))
         return fail(H2O_ERR_ARG, "full_budget must be in [1, 2^20) (got %d)", full_budget);
     if (kind == kFG && !(tau > 0.0 && tau <= 1.0)) return fail(H2O_ERR_ARG, "tau must be in (0, 1]");
@@ -243,7 +254,7 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
     memset(h, 0, sizeof(*h));
     h->kind = kind; h->B = budget; h->H = heavy; h->r = recent; h->batch = batch; h->heads = heads;
     h->D = head_dim; h->dtype = dtype; h->U = batch * heads; h->G = groups; h->scale = scale;
-    h->kv8 = kv8; h->Bp = (budget + 1) & ~1;
+    h->qbits = qbits; h->Bp = (budget + 1) & ~1;
     if (kind == kFG) {
         h->B_sel = budget;
         h->B_full = full_budget;
@@ -259,7 +270,7 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, h->device);
     if (major < 10) { delete h; return fail(H2O_ERR_UNSUPPORTED, "device compute capability %d.x is not sm_103", major); }
 
-    const size_t U = (size_t)h->U, B = (size_t)h->B, row = (size_t)h->D * (kv8 ? 1 : elem_size(dtype));
+    const size_t U = (size_t)h->U, B = (size_t)h->B, row = row_bytes(h);
     if (kind == kFG && ((rc0_alloc(h, U) != H2O_OK))) { free_all(h); delete h; return H2O_ERR_ALLOC; }
     int rc = H2O_OK;
     if ((rc = dev_alloc(&h->K, U * B * row, "cache K")) ||
@@ -269,7 +280,7 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
         (rc = dev_alloc((void**)&h->err, sizeof(int), "error word"))) {
         free_all(h); delete h; return rc;
     }
-    if (kv8 && (rc = dev_alloc((void**)&h->kvs, U * (size_t)h->Bp * sizeof(float2), "slot scales"))) {
+    if (qbits && (rc = dev_alloc((void**)&h->kvs, U * (size_t)h->Bp * sizeof(float2), "slot scales"))) {
         free_all(h); delete h; return rc;
     }
     if (kind == kH2O || kind == kFG) {
@@ -292,7 +303,7 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
     e = cudaMemsetAsync(h->err, 0, sizeof(int), h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->ustate, 0, U * sizeof(int2), h->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->pos, 0xff, U * B * sizeof(int), h->stream);
-    if (e == cudaSuccess && kv8) e = cudaMemsetAsync(h->kvs, 0, U * (size_t)h->Bp * sizeof(float2), h->stream);
+    if (e == cudaSuccess && qbits) e = cudaMemsetAsync(h->kvs, 0, U * (size_t)h->Bp * sizeof(float2), h->stream);
     if (e == cudaSuccess && kind == kFG) {
         int4* init = static_cast<int4*>(malloc(U * sizeof(int4)));
         if (!init) { free_all(h); delete h; return fail(H2O_ERR_ALLOC, "host allocation failed"); }
@@ -388,7 +399,7 @@ int decode_split(const h2o_ctx* h)
         s = h->split;
     else if (h->dtype == H2O_BF16 && h->D == 128 && h->G == 1 && (h->kind == kH2O || h->kind == kLSH) &&
              h->U < h->num_sms)
-        s = few_units_split(h->U, h->B, h->num_sms, h->kind == kLSH, h->kv8 != 0);
+        s = few_units_split(h->U, h->B, h->num_sms, h->kind == kLSH, h->qbits);
     else
         s = auto_decode_split(h->U, h->B, h->num_sms);
     const int lo = (h->B + 1023) / 1024;
@@ -610,7 +621,7 @@ int h2o_get_state(h2o_handle h, void* K, void* V, double* score, int* pos, unsig
                   int* next_pos)
 {
     if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
-    const size_t UB = (size_t)h->U * h->B, row = (size_t)h->D * (h->kv8 ? 1 : elem_size(h->dtype));
+    const size_t UB = (size_t)h->U * h->B, row = row_bytes(h);
     cudaError_t e = cudaSuccess;
     if (K && e == cudaSuccess) e = cudaMemcpyAsync(K, h->K, UB * row, cudaMemcpyDeviceToHost, h->stream);
     if (V && e == cudaSuccess) e = cudaMemcpyAsync(V, h->V, UB * row, cudaMemcpyDeviceToHost, h->stream);
@@ -654,7 +665,7 @@ int h2o_set_state(h2o_handle h, const void* K, const void* V, const double* scor
                   const unsigned* code, const int* occupancy, const int* next_pos)
 {
     if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
-    const size_t UB = (size_t)h->U * h->B, row = (size_t)h->D * (h->kv8 ? 1 : elem_size(h->dtype));
+    const size_t UB = (size_t)h->U * h->B, row = row_bytes(h);
     if (occupancy)
         for (int u = 0; u < h->U; ++u)
             if (occupancy[u] < 0 || occupancy[u] > h->B) return fail(H2O_ERR_ARG, "occupancy out of range");
@@ -700,7 +711,7 @@ int h2o_set_state(h2o_handle h, const void* K, const void* V, const double* scor
 int h2o_get_kv_scales(h2o_handle h, float* kscale, float* vscale)
 {
     if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
-    if (!h->kv8) return fail(H2O_ERR_STATE, "the handle's cache is not int8 (H2O_KV8)");
+    if (!h->qbits) return fail(H2O_ERR_STATE, "the handle's cache is not quantised (H2O_KV8 or H2O_KV4)");
     const size_t n = (size_t)h->U * h->Bp;
     float2* s = static_cast<float2*>(malloc(n * sizeof(float2)));
     if (!s) return fail(H2O_ERR_ALLOC, "host allocation failed");
@@ -722,7 +733,7 @@ int h2o_get_kv_scales(h2o_handle h, float* kscale, float* vscale)
 int h2o_set_kv_scales(h2o_handle h, const float* kscale, const float* vscale)
 {
     if (!h) return fail(H2O_ERR_ARG, "handle is NULL");
-    if (!h->kv8) return fail(H2O_ERR_STATE, "the handle's cache is not int8 (H2O_KV8)");
+    if (!h->qbits) return fail(H2O_ERR_STATE, "the handle's cache is not quantised (H2O_KV8 or H2O_KV4)");
     if (!kscale || !vscale) return fail(H2O_ERR_ARG, "kscale and vscale must be non-NULL");
     const size_t n = (size_t)h->U * h->Bp;
     float2* s = static_cast<float2*>(calloc(n, sizeof(float2)));

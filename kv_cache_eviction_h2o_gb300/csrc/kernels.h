@@ -8,10 +8,10 @@ namespace h2o {
 
 // One handle's device-resident cache.
 struct CacheView {
-    void* K;            // [U][B][D] element type per dtype (int8 codes when kv8)
+    void* K;            // [U][B][D] element type per dtype; int8 codes when qbits 8, [U][B][D/2] bytes of 4-bit codes when qbits 4
     void* V;            // [U][B][D]
-    float2* kvs;        // kv8: [U][Bp] {K scale, V scale} of every slot, else nullptr
-    int kv8, Bp;        // kv8: rows stored as int8 codes; Bp = B rounded up to even
+    float2* kvs;        // qbits: [U][Bp] {K scale, V scale} of every slot, else nullptr
+    int qbits, Bp;      // rows stored as codes of 8 or 4 bits (0: the input type); Bp = B rounded up to even
     float2* score;      // [U][B] accumulated attention (H2O) as an unevaluated fp32 pair hi + lo
     int* pos;           // [U][B] token position per slot, -1 = empty
     uint32_t* code;     // [U][B] key codes (LSH); pivotal histories (persistence of importance)
@@ -74,8 +74,8 @@ cudaError_t launch_lsh_decode(const DecodeArgs& a, int split, cudaStream_t st);
 cudaError_t launch_sh_decode(const DecodeArgs& a, int split, cudaStream_t st);
 int auto_decode_split(int U, int B, int num_sms);
 // split of a bf16, head_dim 128 one-head H2O / HashEvict cache with U < SMs
-// (q8: int8 rows)
-int few_units_split(int U, int B, int num_sms, bool lsh, bool q8);
+// (qbits: 8 or 4 for quantised rows, else 0)
+int few_units_split(int U, int B, int num_sms, bool lsh, int qbits);
 int max_decode_split();
 
 cudaError_t launch_prompt_stats(const CacheView& c, const PromptArgs& p, cudaStream_t st);

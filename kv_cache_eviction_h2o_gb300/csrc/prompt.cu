@@ -519,7 +519,7 @@ __global__ void __launch_bounds__(256) gather_kernel(CacheView cv, PromptArgs pa
         const int p = cv.pos[slot];
         const int half = lane >> 4, l16 = lane & 15;
         const T* srcbase = reinterpret_cast<const T*>(half ? pa.V : pa.K) + ((size_t)unit * pa.T) * D;
-        if (!cv.kv8) {
+        if (!cv.qbits) {
             uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(half ? cv.V : cv.K) + (size_t)slot * D);
             for (int v = l16; v < NV; v += 16) {
                 uint4 w = make_uint4(0u, 0u, 0u, 0u);
@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(256) gather_kernel(CacheView cv, PromptArgs pa
                 dst[v] = w;
             }
         } else {
-            // int8 row: the half-warp's max magnitude gives the scale
+            // quantised row: the half-warp's max magnitude gives the scale
             float x[VPL][VE];
             float amax = 0.f;
 #pragma unroll
@@ -550,21 +550,36 @@ __global__ void __launch_bounds__(256) gather_kernel(CacheView cv, PromptArgs pa
             }
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-            const float inv = q8_inv(amax);
-            uint8_t* dst = reinterpret_cast<uint8_t*>(half ? cv.V : cv.K) + (size_t)slot * D;
+            float* scale_out = reinterpret_cast<float*>(cv.kvs + (size_t)unit * cv.Bp + (slot - (long long)unit * cv.B)) + half;
+            if (cv.qbits == 8) {
+                const float inv = q8_inv(amax);
+                uint8_t* dst = reinterpret_cast<uint8_t*>(half ? cv.V : cv.K) + (size_t)slot * D;
 #pragma unroll
-            for (int k = 0; k < VPL; ++k) {
-                const int v = l16 + 16 * k;
-                if (v < NV) {
-                    if constexpr (VE == 8) {
-                        *reinterpret_cast<uint2*>(dst + v * VE) = make_uint2(q8_pack4(&x[k][0], inv), q8_pack4(&x[k][4], inv));
-                    } else {
-                        *reinterpret_cast<uint32_t*>(dst + v * VE) = q8_pack4(&x[k][0], inv);
+                for (int k = 0; k < VPL; ++k) {
+                    const int v = l16 + 16 * k;
+                    if (v < NV) {
+                        if constexpr (VE == 8) {
+                            *reinterpret_cast<uint2*>(dst + v * VE) = make_uint2(q8_pack4(&x[k][0], inv), q8_pack4(&x[k][4], inv));
+                        } else {
+                            *reinterpret_cast<uint32_t*>(dst + v * VE) = q8_pack4(&x[k][0], inv);
+                        }
                     }
                 }
+                if (l16 == 0) *scale_out = q8_scale(amax);
+            } else {
+                // 4-bit row: D / 2 bytes, VE / 2 per 16-byte input vector
+                const float inv = q4_inv(amax);
+                uint8_t* dst = reinterpret_cast<uint8_t*>(half ? cv.V : cv.K) + (size_t)slot * (D / 2);
+#pragma unroll
+                for (int k = 0; k < VPL; ++k) {
+                    const int v = l16 + 16 * k;
+                    if (v < NV) {
+                        if constexpr (VE == 8) *reinterpret_cast<uint32_t*>(dst + v * 4) = q4_pack<4>(&x[k][0], inv);
+                        else *reinterpret_cast<uint16_t*>(dst + v * 2) = (uint16_t)q4_pack<2>(&x[k][0], inv);
+                    }
+                }
+                if (l16 == 0) *scale_out = q4_scale(amax);
             }
-            if (l16 == 0)
-                reinterpret_cast<float*>(cv.kvs + (size_t)unit * cv.Bp + (slot - (long long)unit * cv.B))[half] = q8_scale(amax);
         }
         if (with_codes && lane == 0) cv.code[slot] = p >= 0 ? pa.ck[(size_t)unit * pa.T + p] : 0u;
     }

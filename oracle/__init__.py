@@ -122,9 +122,11 @@ class H2OState:
 
     def copy(self):
         s = H2OState(self.U, self.B, self.d)
-        for name in ("K", "V", "score", "pos", "occ", "kq", "ks", "vq", "vs", "qbits"):
+        for name in ("K", "V", "score", "pos", "occ", "kq", "ks", "vq", "vs"):
             if hasattr(self, name):
                 setattr(s, name, getattr(self, name).copy())
+        if hasattr(self, "qbits"):
+            s.qbits = self.qbits
         return s
 
 

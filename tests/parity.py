@@ -61,11 +61,11 @@ class Dev:
     groups > 1: an H2O handle whose U cache units are each shared by that
     many query heads (q and out then have U * groups rows)."""
 
-    def __init__(self, kind, U, d, B, H, r, dtype, scale, W=None, split=0, kv8=False, groups=0, fg=None):
-        self.kind, self.U, self.d, self.B, self.dtype, self.kv8 = kind, U, d, B, dtype, kv8
+    def __init__(self, kind, U, d, B, H, r, dtype, scale, W=None, split=0, kv8=False, groups=0, fg=None, kv4=False):
+        self.kind, self.U, self.d, self.B, self.dtype, self.kv8, self.kv4 = kind, U, d, B, dtype, kv8, kv4
         self.G = max(groups, 1)
         self.stream = torch.cuda.current_stream()
-        dt = cdtype(dtype) | (L.H2O_KV8 if kv8 else 0)
+        dt = cdtype(dtype) | (L.H2O_KV8 if kv8 else 0) | (L.H2O_KV4 if kv4 else 0)
         if kind == "fg":
             # fg = (full_budget, tau); the handle holds max(B, full_budget) slots per unit
             self.h = L.fg_init(B, H, r, fg[0], fg[1], 1, U, d, dt, scale, self.stream)
@@ -114,14 +114,18 @@ class Dev:
         U, B, d = self.U, self.B, self.d
         if self.kv8:
             K = np.empty((U, B, d), np.int8); V = np.empty((U, B, d), np.int8)
+        elif self.kv4:
+            K = np.empty((U, B, d // 2), np.uint8); V = np.empty((U, B, d // 2), np.uint8)
         else:
             K = host_elems(self.dtype, (U, B, d)); V = host_elems(self.dtype, (U, B, d))
         score = np.empty((U, B)); pos = np.empty((U, B), np.int32)
         code = np.empty((U, B), np.uint32); occ = np.empty(U, np.int32); npos = np.empty(U, np.int32)
         L.h2o_get_state(self.h, K, V, score, pos, code, occ, npos)
-        if self.kv8:
+        if self.kv8 or self.kv4:
             ks = np.empty((U, B), np.float32); vs = np.empty((U, B), np.float32)
             L.h2o_get_kv_scales(self.h, ks, vs)
+            if self.kv4:
+                K, V = unpack4(K), unpack4(V)
             return dict(K=K, V=V, ks=ks, vs=vs, score=score, pos=pos, code=code, occ=occ, npos=npos)
         return dict(K=widen(K, self.dtype), V=widen(V, self.dtype), score=score, pos=pos, code=code,
                     occ=occ, npos=npos)
@@ -141,9 +145,19 @@ class Dev:
         L.h2o_destroy(self.h)
 
 
+def unpack4(b):
+    """Packed 4-bit rows [..., d/2] (offset binary, element 2i in the low
+    nibble) -> int8 codes [..., d]."""
+    b = b.astype(np.int16)
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), np.int8)
+    out[..., 0::2] = (b & 0xF) - 8
+    out[..., 1::2] = (b >> 4) - 8
+    return out
+
+
 def rows_equal(g, st):
-    """Cache rows bit-exact: int8 codes and fp32 scales for an int8 cache,
-    the stored values otherwise."""
+    """Cache rows bit-exact: codes and fp32 scales for a quantised cache
+    (int8 or 4-bit), the stored values otherwise."""
     if "ks" in g:
         return ((g["K"] == st.kq).all() and (g["V"] == st.vq).all() and (g["ks"] == st.ks).all()
                 and (g["vs"] == st.vs).all())

@@ -106,9 +106,10 @@ def test_persistence_rule_init_checks(L):
     with pytest.raises(L.H2OError) as e:
         L.sh_init(10, 5, 6, 1, 1, 128, 1, 0.1)          # heavy + recent != budget
     assert e.value.code == L.H2O_ERR_ARG
-    with pytest.raises(L.H2OError) as e:
-        L.sh_init(10, 5, 5, 1, 1, 128, 1 | L.H2O_KV8, 0.1)
-    assert e.value.code == L.H2O_ERR_UNSUPPORTED
+    for flag in (L.H2O_KV8, L.H2O_KV4):
+        with pytest.raises(L.H2OError) as e:
+            L.sh_init(10, 5, 5, 1, 1, 128, 1 | flag, 0.1)
+        assert e.value.code == L.H2O_ERR_UNSUPPORTED
     lib = L.lib()
     assert lib.sh_prefill(None, None, None, None, 4) == L.H2O_ERR_ARG
     assert lib.sh_decode_step(None, None, None, None, None, None) == L.H2O_ERR_ARG
@@ -148,9 +149,31 @@ def test_per_head_policy_init_checks(L):
         with pytest.raises(L.H2OError) as e:
             L.fg_init(*args, 1, 1, 128, 1, 0.1)
         assert e.value.code == L.H2O_ERR_ARG and frag in str(e.value)
-    with pytest.raises(L.H2OError) as e:
-        L.fg_init(10, 5, 5, 64, 0.95, 1, 1, 128, 1 | L.H2O_KV8, 0.1)
-    assert e.value.code == L.H2O_ERR_UNSUPPORTED
+    for flag in (L.H2O_KV8, L.H2O_KV4):
+        with pytest.raises(L.H2OError) as e:
+            L.fg_init(10, 5, 5, 64, 0.95, 1, 1, 128, 1 | flag, 0.1)
+        assert e.value.code == L.H2O_ERR_UNSUPPORTED
     assert lib.fg_prefill(None, None, None, None, 4) == L.H2O_ERR_ARG
     assert lib.fg_decode_step(None, None, None, None, None, None) == L.H2O_ERR_ARG
     assert lib.fg_get_policy(None, None, None, None) == L.H2O_ERR_ARG
+
+
+def test_quantised_flags_are_exclusive(L):
+    for init in (lambda dt: L.h2o_init(8, 4, 4, 1, 2, 64, dt, 0.125),
+                 lambda dt: L.lsh_init(8, 4, 1, 2, 64, dt, 0.125, None)):
+        with pytest.raises(L.H2OError) as e:
+            init(L.H2O_BF16 | L.H2O_KV8 | L.H2O_KV4)
+        assert e.value.code == L.H2O_ERR_ARG and "H2O_KV4" in str(e.value)
+
+
+def test_binding_sizes_4bit_rows(L):
+    import numpy as np
+    # a 4-bit handle's rows are d/2 bytes on the host
+    h = L._remember(0xDEAD4, "h2o", 4, 8, 64, L.H2O_BF16 | L.H2O_KV4)
+    try:
+        with pytest.raises(ValueError, match="K"):
+            L.h2o_get_state(h, K=np.empty(4 * 8 * 64, np.uint8))
+        with pytest.raises(TypeError, match="V"):
+            L.h2o_get_state(h, V=np.empty(4 * 8 * 32, np.int8))
+    finally:
+        L._meta.pop(h, None)

@@ -2,8 +2,8 @@
 from rank 0 with the contract's keys, nothing from another rank (as when it
 is launched at two ranks), for the default configuration (the OPT-30B-shaped
 layer), the long-context configuration (its prompt phase timed on a shorter
-prompt and scaled), HashEvict, and the grouped-query and
-persistence-of-importance legs."""
+prompt and scaled), HashEvict, the grouped-query and
+persistence-of-importance legs, and 4-bit cache slots."""
 import json
 import os
 import subprocess
@@ -24,7 +24,7 @@ def _run(extra, rank, world):
 
 
 @pytest.mark.parametrize("extra", [[], ["--config", "llama-7b-32k"], ["--config", "hashevict-opt-6.7b"],
-                                   ["--gqa"], ["--sh"]])
+                                   ["--gqa"], ["--sh"], ["--config", "opt-30b-int4"]])
 def test_reference_arm_line(extra):
     lines = _run(extra, 0, 2)
     assert len(lines) == 1
@@ -39,3 +39,15 @@ def test_reference_arm_line(extra):
 
 def test_reference_arm_other_rank_is_silent():
     assert _run([], 1, 2) == []
+
+
+def test_bench_byte_model_for_quantised_rows():
+    sys.path.insert(0, ROOT)
+    import bench
+    U, B, d = 10, 300, 128
+    full = bench.decode_bytes(U, B, d, 2, False)
+    b8 = bench.decode_bytes(U, B, d, 2, False, 8)
+    b4 = bench.decode_bytes(U, B, d, 2, False, 4)
+    # per slot: two rows of 256, 128 or 64 bytes, the scale pair for codes
+    assert (full - b8) == U * (B * (2 * 128 - 8) + (2 * 128 - 8))
+    assert (b8 - b4) == U * (B * 2 * 64 + 2 * 64)

@@ -35,15 +35,17 @@ def _rand(seed, U, G, T, S, d, dtype, key_scale=1.0):
     return Q, K, V, q, k, v
 
 
-def _run(U, G, T, B, H, r, S, d, dtype, seed, kv8=False, key_scale=1.5, check_every=1):
+def _run(U, G, T, B, H, r, S, d, dtype, seed, kv8=False, key_scale=1.5, check_every=1, kv4=False):
     Q, K, V, q, k, v = _rand(seed, U, G, T, S, d, dtype, key_scale)
     scale = 1.0 / np.sqrt(d)
-    dev = Dev("h2o", U, d, B, H, r, dtype, scale, kv8=kv8, groups=G)
+    dev = Dev("h2o", U, d, B, H, r, dtype, scale, kv8=kv8, groups=G, kv4=kv4)
     dev.prefill(Q, K, V)
     s = dev.state()
     st, c, near0 = align_prefill(s, Q, K, V, B, H, r, scale)
     if kv8:
         st = oracle.kv8(st)
+    if kv4:
+        st = oracle.kv4(st)
     assert (s["pos"] == st.pos).all(), "prompt positions differ"
     assert rows_equal(s, st), "prompt cache rows differ"
     check_scores(s["score"], st.score, "prompt scores")
@@ -81,6 +83,11 @@ def test_gqa_sixteen_heads_per_unit():
 @pytest.mark.parametrize("G", [1, 4])
 def test_gqa_int8_slots(G):
     _run(U=3, G=G, T=400, B=200, H=100, r=100, S=8, d=128, dtype="bf16", seed=21 + G, kv8=True)
+
+
+@pytest.mark.parametrize("G,dtype,d", [(1, "bf16", 128), (4, "bf16", 128), (2, "f32", 64)])
+def test_gqa_4bit_slots(G, dtype, d):
+    _run(U=3, G=G, T=400, B=200, H=100, r=100, S=8, d=d, dtype=dtype, seed=31 + G, kv4=True)
 
 
 def test_gqa_one_head_per_unit_is_the_one_head_handle():

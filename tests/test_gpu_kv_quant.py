@@ -1,8 +1,10 @@
-"""int8 cache slots (H2O_KV8) on the GPU against the oracle.
+"""Quantised cache slots (H2O_KV8, H2O_KV4) on the GPU against the oracle.
 
-Every stored row is int8 codes with one fp32 scale (the quantiser the oracle
-defines: amax / 127, codes rint(x * 127 / amax) in fp32, half to even); a
-step attends to its own new token at full precision and stores it quantised.
+Every stored row is int8 or 4-bit codes with one fp32 scale (the quantisers
+the oracle defines: amax / 127 or amax / 7, codes rint(x * 127 / amax) or
+rint(7 / amax * x) in fp32, half to even; 4-bit codes packed two per byte in
+offset binary); a step attends to its own new token at full precision and
+stores it quantised.
 Codes, scales, positions and victims are compared bit-exactly (H2O victims
 up to the counted near ties), outputs and scores within the usual
 tolerances.  (H2O: Heavy-Hitter Oracle decode rule; HashEvict: Hamming
@@ -14,23 +16,31 @@ import pytest
 import oracle
 from kv_cache_eviction_h2o_gb300 import binding as L
 from kv_cache_eviction_h2o_gb300 import workloads as wl
-from parity import (Dev, align_prefill, check_scores, h2o_lockstep, lsh_lockstep, rows_equal)
+from parity import (Dev, align_prefill, check_scores, h2o_lockstep, lsh_lockstep, record, rows_equal)
 
 pytestmark = pytest.mark.gpu
 
 
-def _h2o_run(w, units, steps, split=0, zero_rows=False):
+BITS = [8, 4]
+
+
+def _quant(st, bits):
+    return oracle.kv8(st, bits)
+
+
+def _h2o_run(w, units, steps, split=0, zero_rows=False, bits=8):
     g = wl.generate(w, units=units, steps=steps)
     if zero_rows:
         # rows with nothing to scale: prompt key/value rows and decode rows of zeros
         g["K"][:, 3] = 0.0; g["V"][:, 5] = 0.0; g["K"][:, -1] = 0.0
         g["k"][2] = 0.0; g["v"][4] = 0.0
     U = len(units)
-    dev = Dev("h2o", U, w.head_dim, w.budget, w.heavy, w.recent, w.dtype, w.scale, split=split, kv8=True)
+    dev = Dev("h2o", U, w.head_dim, w.budget, w.heavy, w.recent, w.dtype, w.scale, split=split,
+              kv8=bits == 8, kv4=bits == 4)
     dev.prefill(g["Q"], g["K"], g["V"])
     s = dev.state()
     st, c, near0 = align_prefill(s, g["Q"], g["K"], g["V"], w.budget, w.heavy, w.recent, w.scale)
-    st = oracle.kv8(st)
+    st = _quant(st, bits)
     assert (s["pos"] == st.pos).all()
     assert rows_equal(s, st), "prompt cache rows differ"
     check_scores(s["score"], st.score, "prefill scores")
@@ -39,29 +49,41 @@ def _h2o_run(w, units, steps, split=0, zero_rows=False):
     return near0, near
 
 
-def test_kv8_tiny_h2o():
+@pytest.mark.parametrize("bits", BITS)
+def test_quant_tiny_h2o(bits):
     w = wl.WORKLOADS["tiny"]
-    _h2o_run(w, list(range(w.units)), w.steps)
+    _h2o_run(w, list(range(w.units)), w.steps, bits=bits)
 
 
+@pytest.mark.parametrize("bits", BITS)
 @pytest.mark.parametrize("split", [1, 3])
-def test_kv8_opt67b_units_h2o(split):
-    _h2o_run(wl.WORKLOADS["opt-6.7b"], list(range(12)), 24, split=split)
+def test_quant_opt67b_units_h2o(split, bits):
+    _h2o_run(wl.WORKLOADS["opt-6.7b"], list(range(12)), 24, split=split, bits=bits)
 
 
-def test_kv8_zero_rows_h2o():
-    _h2o_run(wl.WORKLOADS["tiny"], list(range(4)), 12, zero_rows=True)
+@pytest.mark.parametrize("bits", BITS)
+def test_quant_opt67b_many_units_h2o(bits):
+    # more units than SMs: one CTA per unit, the many-units tile
+    near0, near = _h2o_run(wl.WORKLOADS["opt-6.7b"], list(range(160)), 6, bits=bits)
+    record("quant%d opt-6.7b 160 units" % bits, near_ties=near0 + near, sampled_units=160)
 
 
+@pytest.mark.parametrize("bits", BITS)
+def test_quant_zero_rows_h2o(bits):
+    _h2o_run(wl.WORKLOADS["tiny"], list(range(4)), 12, zero_rows=True, bits=bits)
+
+
+@pytest.mark.parametrize("bits", BITS)
 @pytest.mark.parametrize("split", [1, 3])
-def test_kv8_hashevict_units(split):
+def test_quant_hashevict_units(split, bits):
     w = wl.WORKLOADS["hashevict-opt-6.7b"]
     units = list(range(10))
     g = wl.generate(w, units=units, steps=24)
     W = g["W"]
-    dev = Dev("lsh", len(units), w.head_dim, w.budget, 0, w.recent, w.dtype, w.scale, W=W, split=split, kv8=True)
+    dev = Dev("lsh", len(units), w.head_dim, w.budget, 0, w.recent, w.dtype, w.scale, W=W, split=split,
+              kv8=bits == 8, kv4=bits == 4)
     dev.prefill(g["Q"], g["K"], g["V"])
-    st = oracle.kv8(oracle.lsh_prefill(g["Q"], g["K"], g["V"], W, w.budget, w.recent))
+    st = _quant(oracle.lsh_prefill(g["Q"], g["K"], g["V"], W, w.budget, w.recent), bits)
     s = dev.state()
     assert (s["pos"] == st.pos).all() and (s["code"] == st.code).all()
     assert rows_equal(s, st)
@@ -76,8 +98,9 @@ def test_kv8_hashevict_units(split):
     ("lsh", 40, 8, 0, 8),
     ("lsh", 70, 33, 0, 16),
 ])
-@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
-def test_kv8_edge_cases(kind, T, B, H, r, dtype, d):
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128), ("f32", 128), ("bf16", 64)])
+@pytest.mark.parametrize("bits", BITS)
+def test_quant_edge_cases(kind, T, B, H, r, dtype, d, bits):
     rng = np.random.default_rng(7 * T + B)
     U, S = 3, 10
     def draw(*shape):
@@ -87,32 +110,33 @@ def test_kv8_edge_cases(kind, T, B, H, r, dtype, d):
     q, k, v = draw(S, U, d), draw(S, U, d), draw(S, U, d)
     scale = 1.0 / np.sqrt(d)
     if kind == "h2o":
-        dev = Dev("h2o", U, d, B, H, r, dtype, scale, kv8=True)
+        dev = Dev("h2o", U, d, B, H, r, dtype, scale, kv8=bits == 8, kv4=bits == 4)
         dev.prefill(Q, K, V)
         s = dev.state()
         st, _, _ = align_prefill(s, Q, K, V, B, H, r, scale)
-        st = oracle.kv8(st)
+        st = _quant(st, bits)
         assert rows_equal(s, st)
         h2o_lockstep(dev, st, q, k, v, T, r, scale)
     else:
         W = np.random.default_rng(5).standard_normal((d, 32), dtype=np.float32)
-        dev = Dev("lsh", U, d, B, 0, r, dtype, scale, W=W, kv8=True)
+        dev = Dev("lsh", U, d, B, 0, r, dtype, scale, W=W, kv8=bits == 8, kv4=bits == 4)
         dev.prefill(Q, K, V)
-        st = oracle.kv8(oracle.lsh_prefill(Q, K, V, W, B, r))
+        st = _quant(oracle.lsh_prefill(Q, K, V, W, B, r), bits)
         s = dev.state()
         assert (s["pos"] == st.pos).all() and rows_equal(s, st)
         lsh_lockstep(dev, st, q, k, v, W, T, r, scale)
     dev.close()
 
 
-def test_kv8_scale_calls():
+@pytest.mark.parametrize("flag", ["H2O_KV8", "H2O_KV4"])
+def test_quant_scale_calls(flag):
     h = L.h2o_init(8, 4, 4, 1, 2, 64, L.H2O_F32, 0.125, None)
     ks = np.zeros((2, 8), np.float32)
     with pytest.raises(L.H2OError) as e:
         L.h2o_get_kv_scales(h, ks, ks)
     assert e.value.code == L.H2O_ERR_STATE
     L.h2o_destroy(h)
-    h = L.h2o_init(8, 4, 4, 1, 2, 64, L.H2O_F32 | L.H2O_KV8, 0.125, None)
+    h = L.h2o_init(8, 4, 4, 1, 2, 64, L.H2O_F32 | getattr(L, flag), 0.125, None)
     a = np.arange(16, dtype=np.float32).reshape(2, 8) / 7
     b = -a
     L.h2o_set_kv_scales(h, a, b)
@@ -122,3 +146,9 @@ def test_kv8_scale_calls():
     with pytest.raises(L.H2OError):
         L.h2o_set_kv_scales(h, a, None)
     L.h2o_destroy(h)
+
+
+def test_kv4_and_kv8_together_rejected():
+    with pytest.raises(L.H2OError) as e:
+        L.h2o_init(8, 4, 4, 1, 2, 64, L.H2O_F32 | L.H2O_KV8 | L.H2O_KV4, 0.125, None)
+    assert e.value.code == L.H2O_ERR_ARG
