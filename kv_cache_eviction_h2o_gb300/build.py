@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libh2o_gb300.so")
-SOURCES = ["h2o_api.cu", "decode.cu", "prompt.cu", "prompt_tc.cu", "noalloc.cu"]
+SOURCES = ["h2o_api.cu", "decode.cu", "decode_warp.cu", "prompt.cu", "prompt_tc.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -69,6 +69,9 @@ struct FgArgs {
 };
 
 cudaError_t launch_h2o_decode(const DecodeArgs& a, int split, cudaStream_t st);
+// one-head H2O step over many units, one warp per unit; *used = false
+// (nothing launched) when it does not apply
+cudaError_t launch_h2o_decode_warps(const DecodeArgs& a, cudaStream_t st, bool* used);
 cudaError_t launch_lsh_decode(const DecodeArgs& a, int split, cudaStream_t st);
 // persistence-of-importance step (histories in CacheView::code)
 cudaError_t launch_sh_decode(const DecodeArgs& a, int split, cudaStream_t st);
