@@ -150,14 +150,8 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     const T* qs = reinterpret_cast<const T*>(S.in[0]);
     const T* ks = reinterpret_cast<const T*>(S.in[1]);
     const T* vs = reinterpret_cast<const T*>(S.in[2]);
-    float qp[D / 2];
-    if constexpr (QB != 0) {
-        load_q_quant<QB, T, D>(qs, c.qscale, lane, qp);
-    } else {
-        QRaw<T, D> qraw;
-        load_q_raw<T, D>(qs, lane, qraw);
-        widen_q<T, D>(qraw, c.qscale, qp);
-    }
+    QVec<T, D, QB> qv;
+    load_qvec<QB, T, D>(qs, c.qscale, lane, QB ? S.qpl[warp] : nullptr, qv);
     // the new token's row, written into the victim slot at the end
     uint4 newrow = make_uint4(0u, 0u, 0u, 0u);
     if (rank == 0 && tid < 2 * NV) newrow = reinterpret_cast<const uint4*>(S.in[1])[tid];
@@ -171,9 +165,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     for (int e = 0; e < EPL; ++e) o[e] = 0.f;
     if ((GQ || rank == 0) && warp == 0) {  // the new token attends to itself
         float vr[EPL];
-        float zn;
-        if constexpr (QB != 0) zn = row_dot_quant_order<QB, T, D>(ks, qp, lane);
-        else zn = row_dot<T, D, T>(ks, qp, lane);
+        const float zn = new_logit<QB, T, D>(qs, ks, c.qscale, qv, lane);
         load_vec<T, EPL>(vs + lane * EPL, vr);
         m_run = zn;
         l_run = lane == 0 ? 1.f : 0.f;
@@ -183,7 +175,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     }
     __syncwarp();
 
-    attend_chunk<T, D, TL, QB>(S, Kc, Vc, Sc, f0, f1, n, -1, true, qp, m_run, l_run, o, c.err);
+    attend_chunk<T, D, TL, QB>(S, Kc, Vc, Sc, f0, f1, n, -1, true, qv, m_run, l_run, o, c.err);
 
     float Mc, Lc, Oc;
     merge_warps<T, D, TL, QB>(S, m_run, l_run, o, Mc, Lc, Oc);
@@ -1025,17 +1017,15 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
     }
     __syncthreads();
     const int victim = S.victim;
-    float qp[D / 2];
-    if constexpr (QB != 0) load_q_quant<QB, T, D>(qs, c.qscale, lane, qp);
-    else widen_q<T, D>(qraw, c.qscale, qp);
+    QVec<T, D, QB> qv;
+    if constexpr (QB != 0) load_q_fix<QB, T, D>(qs, c.qscale, lane, S.qpl[warp], qv);
+    else widen_q<T, D>(qraw, c.qscale, qv.v);
 
     float m_run = -INFINITY, l_run = 0.f, o[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] = 0.f;
     if (rank == 0 && warp == 0) {          // the new token, now in the victim slot
-        float zn;
-        if constexpr (QB != 0) zn = row_dot_quant_order<QB, T, D>(ks, qp, lane);
-        else zn = row_dot<T, D, T>(ks, qp, lane);
+        const float zn = new_logit<QB, T, D>(qs, ks, c.qscale, qv, lane);
         float vr[EPL];
         load_vec<T, EPL>(vs + lane * EPL, vr);
         m_run = zn;
@@ -1045,8 +1035,8 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) lsh_decode_kernel(const Deco
     }
     __syncwarp();
 
-    attend_chunk<T, D, TL, QB>(S, Kc, Vc, Sc, f0, f1, n, full ? victim : -1, false, qp, m_run, l_run, o,
-                           c.err);
+    attend_chunk<T, D, TL, QB>(S, Kc, Vc, Sc, f0, f1, n, full ? victim : -1, false, qv, m_run, l_run, o,
+                               c.err);
 
     float Mc, Lc, Oc;
     merge_warps<T, D, TL, QB>(S, m_run, l_run, o, Mc, Lc, Oc);

@@ -93,6 +93,8 @@ struct DecodeSmem {
     alignas(16) unsigned char in[3][D * sizeof(T)];
     // quantised rows: {K scale, V scale} of every slot of a ring stage
     alignas(16) float2 sbuf[QB ? TL::NW : 1][TL::NBUF][kStage];
+    // quantised rows: each warp's byte planes of q (built per warp)
+    alignas(16) unsigned char qpl[QB ? TL::NW : 1][QB ? 3 * D : 16];
     uint64_t bar[TL::NW][TL::NBUF];
     float z[kMaxChunk];                     // base-2 logits of this CTA's slots
     alignas(16) float e[TL::NW][kStage];
@@ -295,72 +297,6 @@ __device__ __forceinline__ int q8_chunk(int lane, int c)
     return HCH * hh + (c ^ (r % HCH));
 }
 
-template <typename T, int D>
-__device__ __forceinline__ void load_q_q8(const T* q, float scale, int lane, float (&qp)[D / 2])
-{
-    constexpr int HCH = D / 32, VE = 16 / (int)sizeof(T);
-#pragma unroll
-    for (int c = 0; c < HCH; ++c) {
-        const T* src = q + q8_chunk<D>(lane, c) * 16;
-#pragma unroll
-        for (int v = 0; v < 16; v += VE) load_vec<T, VE>(src + v, &qp[c * 16 + v]);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) qp[c * 16 + e] *= scale;
-    }
-}
-
-// Dot of an int8 row (codes, unscaled) with the lane's half of q; every
-// lane returns the full dot of its row.  As row_dot: per-chunk sums in
-// element order (two fixed accumulator pairs), then chunk_tree, so equal
-// rows give equal bits in every slot.
-template <int D>
-__device__ __forceinline__ float row_dot_q8(const int8_t* row, const float (&qp)[D / 2], int lane)
-{
-    constexpr int HCH = D / 32;
-    uint4 raw[HCH];
-#pragma unroll
-    for (int c = 0; c < HCH; ++c) raw[c] = *reinterpret_cast<const uint4*>(row + q8_chunk<D>(lane, c) * 16);
-    float part[HCH];
-#pragma unroll
-    for (int c = 0; c < HCH; ++c) {
-        const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
-        float2 t0 = make_float2(0.f, 0.f), t1 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float f[4];
-            q8_unpack4(u[i], f);
-            const int e = c * 16 + 4 * i;
-            float2& t = i < 2 ? t0 : t1;
-            t = fma2(make_float2(qp[e], qp[e + 1]), make_float2(f[0], f[1]), t);
-            t = fma2(make_float2(qp[e + 2], qp[e + 3]), make_float2(f[2], f[3]), t);
-        }
-        part[c] = (t0.x + t0.y) + (t1.x + t1.y);
-    }
-    const float zh = chunk_tree<HCH>(part);
-    return zh + __shfl_xor_sync(kFull, zh, 16);
-}
-
-// Dot of a row of T (the new token's key, in global memory) with q held in
-// the int8 order.
-template <typename T, int D>
-__device__ __forceinline__ float row_dot_q8order(const T* row, const float (&qp)[D / 2], int lane)
-{
-    constexpr int HCH = D / 32, VE = 16 / (int)sizeof(T);
-    float acc = 0.f;
-#pragma unroll
-    for (int c = 0; c < HCH; ++c) {
-        const T* src = row + q8_chunk<D>(lane, c) * 16;
-#pragma unroll
-        for (int v = 0; v < 16; v += VE) {
-            float x[VE];
-            load_vec<T, VE>(src + v, x);
-#pragma unroll
-            for (int e = 0; e < VE; ++e) acc = __fmaf_rn(qp[c * 16 + v + e], x[e], acc);
-        }
-    }
-    return acc + __shfl_xor_sync(kFull, acc, 16);
-}
-
 // The new token's row, held as 16 bytes of T by threads tid < 2 * NV (K rows
 // first, then V), stored quantised into slot `victim`: the NV threads of a
 // row form an aligned lane group, which reduces the row's max magnitude.
@@ -418,79 +354,6 @@ __device__ __forceinline__ int q4_chunk(int lane, int c)
     return HC * hh + (c ^ ((r >> (SH + 1)) & (HC - 1)));
 }
 
-// element k of a code word in the widened order
-__device__ __forceinline__ constexpr int q4_elem(int k) { return k < 4 ? 2 * k : 2 * (k - 4) + 1; }
-
-template <typename T, int D>
-__device__ __forceinline__ void load_q_q4(const T* q, float scale, int lane, float (&qp)[D / 2])
-{
-    constexpr int HC = D / 64;
-#pragma unroll
-    for (int c = 0; c < HC; ++c) {
-        const T* src = q + q4_chunk<D>(lane, c) * 32;
-        float x[32];
-#pragma unroll
-        for (int v = 0; v < 32; v += 16 / (int)sizeof(T)) load_vec<T, 16 / (int)sizeof(T)>(src + v, &x[v]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int k = 0; k < 8; ++k) qp[c * 32 + 8 * i + k] = x[8 * i + q4_elem(k)] * scale;
-    }
-}
-
-// Dot of a 4-bit row (codes, unscaled) with the lane's half of q; every lane
-// returns the full dot of its row.  Each code word has its own accumulator
-// pair, summed in word order, then chunk_tree over the chunks: equal rows
-// give equal bits in every slot.
-template <int D>
-__device__ __forceinline__ float row_dot_q4(const uint8_t* row, const float (&qp)[D / 2], int lane)
-{
-    constexpr int HC = D / 64;
-    uint4 raw[HC];
-#pragma unroll
-    for (int c = 0; c < HC; ++c) raw[c] = *reinterpret_cast<const uint4*>(row + q4_chunk<D>(lane, c) * 16);
-    float part[HC];
-#pragma unroll
-    for (int c = 0; c < HC; ++c) {
-        const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
-        float2 t[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float f[8];
-            q4_unpack8(u[i], f);
-            const float* qq = &qp[c * 32 + 8 * i];
-            t[i] = fma2(make_float2(qq[0], qq[1]), make_float2(f[0], f[1]), make_float2(0.f, 0.f));
-            t[i] = fma2(make_float2(qq[2], qq[3]), make_float2(f[2], f[3]), t[i]);
-            t[i] = fma2(make_float2(qq[4], qq[5]), make_float2(f[4], f[5]), t[i]);
-            t[i] = fma2(make_float2(qq[6], qq[7]), make_float2(f[6], f[7]), t[i]);
-        }
-        part[c] = ((t[0].x + t[0].y) + (t[1].x + t[1].y)) + ((t[2].x + t[2].y) + (t[3].x + t[3].y));
-    }
-    const float zh = chunk_tree<HC>(part);
-    return zh + __shfl_xor_sync(kFull, zh, 16);
-}
-
-// Dot of a row of T (the new token's key, in shared memory) with q held in
-// the 4-bit order.
-template <typename T, int D>
-__device__ __forceinline__ float row_dot_q4order(const T* row, const float (&qp)[D / 2], int lane)
-{
-    constexpr int HC = D / 64;
-    float acc = 0.f;
-#pragma unroll
-    for (int c = 0; c < HC; ++c) {
-        const T* src = row + q4_chunk<D>(lane, c) * 32;
-        float x[32];
-#pragma unroll
-        for (int v = 0; v < 32; v += 16 / (int)sizeof(T)) load_vec<T, 16 / (int)sizeof(T)>(src + v, &x[v]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int k = 0; k < 8; ++k) acc = __fmaf_rn(qp[c * 32 + 8 * i + k], x[8 * i + q4_elem(k)], acc);
-    }
-    return acc + __shfl_xor_sync(kFull, acc, 16);
-}
-
 // As store_row_q8, for 4-bit rows: each thread's 16 bytes of T become
 // VE / 2 bytes of codes.
 template <typename T, int D>
@@ -526,26 +389,247 @@ __device__ __forceinline__ void store_row_q4(uint4 newrow, int tid, uint8_t* Kc4
     }
 }
 
-// Quantised-row dispatch: QB 8 or 4.
-template <int QB, typename T, int D>
-__device__ __forceinline__ void load_q_quant(const T* q, float scale, int lane, float (&qp)[D / 2])
+// ------------------------------------------------ q against quantised rows
+//
+// The logit of a quantised row is an integer dot product: the codes against
+// q held as fixed point.  x = q * scale (base-2 logit units, fp32) is
+// rounded to xi = rint(x * 2^F), F chosen per row so that |xi| < 2^23, and
+// xi is split into three byte planes, xi = 2^16 b2 + 2^8 b1 + b0 (b2 signed,
+// b1 and b0 unsigned).  dp4a sums four code x byte products exactly in
+// 32-bit integers, so a row's dot is (2^16 A2 + 2^8 A1 + A0) * 2^-F with
+// A_k = sum_e code_e * b_k,e exact whatever order the lanes take: equal
+// rows give equal bits in every slot.  The rounding of x to the 2^-F grid
+// is at most 2^-23 of the row's largest |x|, the size of an fp32 rounding.
+// Lane (r, h) holds its half row in the order of its chunk reads.
+template <typename T, int D, int QB>
+struct QVec {                     // q for rows of the input type
+    float v[D / 2];
+};
+
+template <typename T, int D>
+struct QFix {
+    uint32_t p[3][D / 8];         // byte planes b0, b1, b2 of the lane's D / 2 elements, 4 per word
+    int s[3];                     // 4-bit rows: the lane's sum of every plane (for the code offset)
+    float unscale;                // 2^-F
+};
+template <typename T, int D> struct QVec<T, D, 8> : QFix<T, D> {};
+template <typename T, int D> struct QVec<T, D, 4> : QFix<T, D> {};
+
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c)
 {
-    if constexpr (QB == 8) load_q_q8<T, D>(q, scale, lane, qp);
-    else load_q_q4<T, D>(q, scale, lane, qp);
+    int d;
+    asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_su(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
 }
 
-template <int QB, int D, typename E>
-__device__ __forceinline__ float row_dot_quant(const E* row, const float (&qp)[D / 2], int lane)
+// Building the planes: the warp's lanes take EPL = D / 32 consecutive
+// elements each, round them (one multiply-add onto 1.5 * 2^23 rounds to the
+// nearest integer, ties to even, for |x 2^F| < 2^22), and write their plane
+// bytes to a 3 x D shared buffer -- int8 rows in element order, 4-bit rows
+// with every group of 8 elements stored even elements first -- from which
+// every lane reads the words of its chunks.  A plane's sum over each half
+// row (for the offset of 4-bit codes) is reduced over the 16 lanes holding
+// that half.  pl: this warp's 3 * D bytes, 16-byte aligned.
+template <int QB, int D>
+__device__ __forceinline__ int qfix_pos(int e)
 {
-    if constexpr (QB == 8) return row_dot_q8<D>(row, qp, lane);
-    else return row_dot_q4<D>(row, qp, lane);
+    if constexpr (QB == 8) return e;
+    else return (e & ~7) + (e & 1) * 4 + ((e & 7) >> 1);
 }
 
 template <int QB, typename T, int D>
-__device__ __forceinline__ float row_dot_quant_order(const T* row, const float (&qp)[D / 2], int lane)
+__device__ __forceinline__ void load_q_fix(const T* q, float scale, int lane, unsigned char* pl, QFix<T, D>& qf)
 {
-    if constexpr (QB == 8) return row_dot_q8order<T, D>(row, qp, lane);
-    else return row_dot_q4order<T, D>(row, qp, lane);
+    constexpr int EPL = D / 32, NWD = D / 8;
+    float x[EPL];
+    load_vec<T, EPL>(q + lane * EPL, x);
+    float m = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+        x[e] *= scale;
+        m = fmaxf(m, fabsf(x[e]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    // m < 2^E, read from the exponent field (frexpf for the rare subnormal m)
+    int E = 0;
+    if (m >= FLT_MIN) E = (int)((__float_as_uint(m) >> 23) & 0xffu) - 126;
+    else if (m > 0.f) frexpf(m, &E);
+    const int F = 22 - E;                            // |x| 2^F < 2^22
+    // 2^F and 2^-F, built from their exponent fields while they are normal
+    const float up = (F >= -126 && F <= 127) ? __uint_as_float((uint32_t)(F + 127) << 23) : ldexpf(1.f, F);
+    qf.unscale = m > 0.f ? ((F >= -127 && F <= 126) ? __uint_as_float((uint32_t)(127 - F) << 23) : ldexpf(1.f, -F))
+                         : 1.f;
+    int ps[3] = {0, 0, 0};
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+        const int xi = m > 0.f ? __float_as_int(__fmaf_rn(x[e], up, 12582912.f)) - 0x4B400000 : 0;
+        const int pos = qfix_pos<QB, D>(lane * EPL + e);
+        pl[pos] = (unsigned char)(xi & 0xff);
+        pl[D + pos] = (unsigned char)((xi >> 8) & 0xff);
+        pl[2 * D + pos] = (unsigned char)((xi >> 16) & 0xff);
+        ps[0] += xi & 0xff;
+        ps[1] += (xi >> 8) & 0xff;
+        ps[2] += xi >> 16;
+    }
+    __syncwarp();
+    // the half of the row this lane reads: the half its first chunk lies in
+    int hh;
+    if constexpr (QB == 8) hh = q8_chunk<D>(lane, 0) >= D / 32;
+    else hh = q4_chunk<D>(lane, 0) >= D / 64;
+    if constexpr (QB == 4) {
+        // lanes 0..15 hold elements of the first half, 16..31 of the second
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) ps[k] += __shfl_xor_sync(kFull, ps[k], o);
+            const int s0 = __shfl_sync(kFull, ps[k], 0), s1 = __shfl_sync(kFull, ps[k], 16);
+            qf.s[k] = hh ? s1 : s0;
+        }
+    } else {
+        qf.s[0] = qf.s[1] = qf.s[2] = 0;
+    }
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        const unsigned char* plane = pl + k * D;
+        if constexpr (QB == 8) {
+#pragma unroll
+            for (int c = 0; c < NWD / 4; ++c) {
+                const uint4 w = *reinterpret_cast<const uint4*>(plane + q8_chunk<D>(lane, c) * 16);
+                qf.p[k][4 * c] = w.x; qf.p[k][4 * c + 1] = w.y; qf.p[k][4 * c + 2] = w.z; qf.p[k][4 * c + 3] = w.w;
+            }
+        } else {
+            // chunk c: 32 elements = 4 groups of 8 = 32 plane bytes
+#pragma unroll
+            for (int c = 0; c < NWD / 8; ++c) {
+                const unsigned char* src = plane + q4_chunk<D>(lane, c) * 32;
+                const uint4 w0 = *reinterpret_cast<const uint4*>(src);
+                const uint4 w1 = *reinterpret_cast<const uint4*>(src + 16);
+                uint32_t* dst = &qf.p[k][8 * c];
+                dst[0] = w0.x; dst[1] = w0.y; dst[2] = w0.z; dst[3] = w0.w;
+                dst[4] = w1.x; dst[5] = w1.y; dst[6] = w1.z; dst[7] = w1.w;
+            }
+        }
+    }
+    __syncwarp();                                    // pl may be written again
+}
+
+template <int QB, typename T, int D>
+__device__ __forceinline__ void load_qvec(const T* q, float scale, int lane, unsigned char* pl, QVec<T, D, QB>& qv)
+{
+    if constexpr (QB == 0) {
+        QRaw<T, D> raw;
+        load_q_raw<T, D>(q, lane, raw);
+        widen_q<T, D>(raw, scale, qv.v);
+    } else {
+        load_q_fix<QB, T, D>(q, scale, lane, pl, qv);
+    }
+}
+
+// Dot (unscaled by the row's scale) of a quantised row with q; every lane
+// returns the full dot of its row.
+template <int QB, int D, typename T>
+__device__ __forceinline__ float row_dot_fix(const CacheElem<T, QB>* row, const QFix<T, D>& qf, int lane)
+{
+    int a0 = 0, a1 = 0, a2 = 0;
+    if constexpr (QB == 8) {
+        constexpr int HCH = D / 32;
+        uint4 raw[HCH];
+#pragma unroll
+        for (int c = 0; c < HCH; ++c)
+            raw[c] = *reinterpret_cast<const uint4*>(reinterpret_cast<const int8_t*>(row) + q8_chunk<D>(lane, c) * 16);
+#pragma unroll
+        for (int c = 0; c < HCH; ++c) {
+            const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = 4 * c + i;
+                a0 = dp4a_su(u[i], qf.p[0][j], a0);
+                a1 = dp4a_su(u[i], qf.p[1][j], a1);
+                a2 = dp4a_ss(u[i], qf.p[2][j], a2);
+            }
+        }
+    } else {
+        // offset-binary nibbles: sum (code + 8) b, then take 8 sum b off
+        constexpr int HC = D / 64;
+        uint4 raw[HC];
+#pragma unroll
+        for (int c = 0; c < HC; ++c)
+            raw[c] = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(row) + q4_chunk<D>(lane, c) * 16);
+#pragma unroll
+        for (int c = 0; c < HC; ++c) {
+            const uint32_t u[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = 2 * (4 * c + i);
+                const uint32_t lo = u[i] & 0x0F0F0F0Fu, hi = (u[i] >> 4) & 0x0F0F0F0Fu;
+                a0 = dp4a_uu(lo, qf.p[0][j], a0);
+                a0 = dp4a_uu(hi, qf.p[0][j + 1], a0);
+                a1 = dp4a_uu(lo, qf.p[1][j], a1);
+                a1 = dp4a_uu(hi, qf.p[1][j + 1], a1);
+                a2 = dp4a_us(lo, qf.p[2][j], a2);
+                a2 = dp4a_us(hi, qf.p[2][j + 1], a2);
+            }
+        }
+        a0 -= 8 * qf.s[0];
+        a1 -= 8 * qf.s[1];
+        a2 -= 8 * qf.s[2];
+    }
+    a0 += __shfl_xor_sync(kFull, a0, 16);
+    a1 += __shfl_xor_sync(kFull, a1, 16);
+    a2 += __shfl_xor_sync(kFull, a2, 16);
+    return __fmaf_rn((float)a2, 65536.f, __fmaf_rn((float)a1, 256.f, (float)a0)) * qf.unscale;
+}
+
+// Dot of q and k (rows of T in shared memory) times scale, in fp32: the new
+// token's logit on the quantised paths (any lane order; every lane gets it).
+template <typename T, int D>
+__device__ __forceinline__ float new_token_dot(const T* q, const T* k, float scale, int lane)
+{
+    constexpr int EPL = D / 32;
+    float qv[EPL], kv[EPL];
+    load_vec<T, EPL>(q + lane * EPL, qv);
+    load_vec<T, EPL>(k + lane * EPL, kv);
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc = __fmaf_rn(qv[e], kv[e], acc);
+    return warp_sum(acc) * scale;
+}
+
+// Logit (before the row's scale) of row `row` against q: the float path for
+// rows of the input type, the integer path for codes.
+template <int QB, typename T, int D>
+__device__ __forceinline__ float row_logit(const CacheElem<T, QB>* row, const QVec<T, D, QB>& qv, int lane)
+{
+    if constexpr (QB == 0) return row_dot<T, D, T>(row, qv.v, lane);
+    else return row_dot_fix<QB, D, T>(row, qv, lane);
+}
+
+// The new token's logit: row_dot for rows of the input type (the same
+// arithmetic as a cached row), new_token_dot otherwise.
+template <int QB, typename T, int D>
+__device__ __forceinline__ float new_logit(const T* q, const T* k, float scale, const QVec<T, D, QB>& qv, int lane)
+{
+    if constexpr (QB == 0) return row_dot<T, D, T>(k, qv.v, lane);
+    else return new_token_dot<T, D>(q, k, scale, lane);
 }
 
 template <int QB, typename T, int D, typename E>
@@ -588,7 +672,7 @@ __device__ __forceinline__ void issue_stage(DecodeSmem<T, D, TL, QB>& S, const C
 template <typename T, int D, int QB>
 __device__ __forceinline__ void attend_rows(const CacheElem<T, QB>* kst, const CacheElem<T, QB>* vst,
                                             const float2* sc, float* e_buf, float* zdst, int gl, int skip_r,
-                                            const float (&qp)[D / 2], float& m_ref, float& l_lane,
+                                            const QVec<T, D, QB>& qv, float& m_ref, float& l_lane,
                                             float (&o)[D / 32], float (&o2)[D / 32])
 {
     using R = Rows<T, D>;
@@ -606,8 +690,8 @@ __device__ __forceinline__ void attend_rows(const CacheElem<T, QB>* kst, const C
         }
     };
     float z;
-    if constexpr (QB != 0) z = row_dot_quant<QB, D>(kst + r * RowElems<D, QB>, qp, lane) * sc[r].x;
-    else z = row_dot<T, D, T>(kst + r * D, qp, lane);
+    if constexpr (QB != 0) z = row_logit<QB, T, D>(kst + r * RowElems<D, QB>, qv, lane) * sc[r].x;
+    else z = row_logit<QB, T, D>(kst + r * D, qv, lane);
     if (r >= gl || r == skip_r) z = -INFINITY;
     if (__any_sync(kFull, z > m_ref + 8.f)) {
         float zm = z;
@@ -707,13 +791,13 @@ __device__ __forceinline__ void attend_rows(const CacheElem<T, QB>* kst, const C
 // keep_z the logits go to S.z[s0 + r]).
 template <typename T, int D, class TL, int QB>
 __device__ __forceinline__ void attend_stage(DecodeSmem<T, D, TL, QB>& S, int b, int s0, int gl, int f0, int skip,
-                                             bool keep_z, const float (&qp)[D / 2], float& m_ref, float& l_lane,
+                                             bool keep_z, const QVec<T, D, QB>& qv, float& m_ref, float& l_lane,
                                              float (&o)[D / 32], float (&o2)[D / 32])
 {
     const int warp = threadIdx.x >> 5;
     const int sr = skip - f0 - s0;
     attend_rows<T, D, QB>(S.u.ring.kbuf[warp][b], S.u.ring.vbuf[warp][b], QB ? S.sbuf[warp][b] : nullptr, S.e[warp],
-                          keep_z ? &S.z[s0] : nullptr, gl, (sr >= 0 && sr < kStage) ? sr : -1, qp, m_ref, l_lane,
+                          keep_z ? &S.z[s0] : nullptr, gl, (sr >= 0 && sr < kStage) ? sr : -1, qv, m_ref, l_lane,
                           o, o2);
 }
 
@@ -726,7 +810,7 @@ template <typename T, int D, class TL, int QB>
 __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, QB>& S, const CacheElem<T, QB>* Kc,
                                              const CacheElem<T, QB>* Vc, const float2* Sc,
                                              int f0, int f1, int n, int skip, bool keep_z,
-                                             const float (&qp)[D / 2], float& m_ref,
+                                             const QVec<T, D, QB>& qv, float& m_ref,
                                              float& l_lane, float (&o)[D / 32], int* err)
 {
     constexpr int EPL = D / 32, NW = TL::NW, NBUF = TL::NBUF;
@@ -746,7 +830,7 @@ __device__ __forceinline__ void attend_chunk(DecodeSmem<T, D, TL, QB>& S, const 
         }
         const int s0 = g * kStage;                 // fetch-relative first slot
         const int gl = max(0, min(kStage, n - (f0 + s0)));   // live rows of this stage
-        if (gl > 0) attend_stage<T, D, TL, QB>(S, b, s0, gl, f0, skip, keep_z, qp, m_ref, l_lane, o, o2);
+        if (gl > 0) attend_stage<T, D, TL, QB>(S, b, s0, gl, f0, skip, keep_z, qv, m_ref, l_lane, o, o2);
         __syncwarp();                              // every lane is past the wait and the buffer
         // refill this buffer with the warp's stage NBUF rounds ahead
         if (lane == 0) {

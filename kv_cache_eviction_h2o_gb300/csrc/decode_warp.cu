@@ -38,6 +38,7 @@ struct WarpSlice {
     alignas(16) float2 sbuf[QB ? NBUF : 1][kStage];     // quantised rows: {K scale, V scale} per slot
     alignas(16) unsigned char in[3][D * sizeof(T)];     // this unit's q, k, v rows
     alignas(16) float e[kStage];                        // a stage's weights
+    alignas(16) unsigned char qpl[QB ? 3 * D : 16];     // quantised rows: byte planes of q
     uint64_t bar[NBUF];
 };
 
@@ -202,18 +203,10 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, MINB) h2o_warp_kernel(const
         const T* qs = reinterpret_cast<const T*>(W.in[0]);
         const T* ks = reinterpret_cast<const T*>(W.in[1]);
         const T* vs = reinterpret_cast<const T*>(W.in[2]);
-        float qp[D / 2];
-        if constexpr (QB != 0) {
-            load_q_quant<QB, T, D>(qs, c.qscale, lane, qp);
-        } else {
-            QRaw<T, D> qraw;
-            load_q_raw<T, D>(qs, lane, qraw);
-            widen_q<T, D>(qraw, c.qscale, qp);
-        }
+        QVec<T, D, QB> qv;
+        load_qvec<QB, T, D>(qs, c.qscale, lane, QB ? W.qpl : nullptr, qv);
         // the new token attends to itself
-        float zn;
-        if constexpr (QB != 0) zn = row_dot_quant_order<QB, T, D>(ks, qp, lane);
-        else zn = row_dot<T, D, T>(ks, qp, lane);
+        const float zn = new_logit<QB, T, D>(qs, ks, c.qscale, qv, lane);
         float m_run = zn, l_run = lane == 0 ? 1.f : 0.f, o[EPL], o2[EPL];
         load_vec<T, EPL>(vs + lane * EPL, o);
 #pragma unroll
@@ -230,7 +223,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, MINB) h2o_warp_kernel(const
             const int gl = max(0, min(kStage, n - g * kStage));
             if (gl > 0)
                 attend_rows<T, D, QB>(W.kbuf[b], W.vbuf[b], QB ? W.sbuf[b] : nullptr, W.e, z + g * kStage, gl, -1,
-                                      qp, m_run, l_run, o, o2);
+                                      qv, m_run, l_run, o, o2);
             __syncwarp();                                        // every lane is past the wait and the buffer
             if (lane == 0) issue_item(k_it + NBUF);
         }
@@ -351,7 +344,7 @@ template <typename T, int D, int QB>
 cudaError_t launch_warp_t(const DecodeArgs& a, cudaStream_t st)
 {
     constexpr int NBUF = warp_nbuf<QB>();
-    constexpr int MINB = 3;
+    constexpr int MINB = 3;                     // 12 warps per SM (16 measured slower for 4-bit rows)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
