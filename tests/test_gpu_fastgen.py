@@ -126,3 +126,19 @@ def test_prompt_within_budget_takes_the_local_policy(T):
         _lockstep(dev, states, params, g, T, w.scale)
     finally:
         dev.close()
+
+
+def test_policy_profile_on_a_persistent_walk():
+    """40 units of the OPT-6.7B-shaped prompt: 640 (unit, block) items, more
+    than the resident CTAs, so the band sums of the scorer's second pass are
+    taken on CTAs that walk several items."""
+    w = wl.WORKLOADS["fastgen-opt-6.7b"]
+    g = wl.generate(w, units=list(range(40)), steps=1)
+    U = g["Q"].shape[0]
+    dev = Dev("fg", U, w.head_dim, w.budget, w.heavy, w.recent, w.dtype, w.scale, fg=(w.full_budget, w.tau))
+    try:
+        dev.prefill(g["Q"], g["K"], g["V"])
+        pol, _, _, flips, near0 = _profile_and_align(dev, g, w, w.tau, w.full_budget)
+        record("fastgen persistent walk", policy_flips=flips, near_ties=near0, units=U)
+    finally:
+        dev.close()

@@ -45,6 +45,24 @@ def test_prefill_statistics(T, dtype, d):
     dev.close()
 
 
+@pytest.mark.parametrize("U,T", [(1300, 1), (700, 100), (700, 129), (400, 300), (40, 4100)])
+def test_prefill_statistics_persistent_walk(U, T):
+    """The tensor-core scorer's persistent grid: more (unit, block) items than
+    resident CTAs, so every CTA walks several items (short, ragged and
+    longest-walked prompts; 4100 tokens = 33 blocks takes one item per CTA)."""
+    Q, K, V, *_ = _rand(900 + T, U, T, 0, 128, "bf16", key_scale=2.0)
+    scale = 1.0 / np.sqrt(128)
+    dev = Dev("h2o", U, 128, 16, 8, 8, "bf16", scale)
+    dev.prefill(Q, K, V)
+    m, l, c = dev.stats(T)
+    mo, lo, co = oracle.prefill_scores(Q, K, scale)
+    np.testing.assert_allclose(m, mo, rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(l, lo, rtol=1e-4)
+    check_scores(c, co, "column sums")
+    np.testing.assert_allclose(c.sum(axis=1), T, rtol=1e-5)
+    dev.close()
+
+
 def test_tiny_workload_h2o():
     w = wl.WORKLOADS["tiny"]
     g = wl.generate(w)
