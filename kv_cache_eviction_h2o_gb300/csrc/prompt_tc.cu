@@ -566,6 +566,19 @@ __global__ void __launch_bounds__(kThreads, 2)
         const double nan = __longlong_as_double(0x7ff8000000000000LL);
         int gt = 0;                               // tiles of the walk so far
         bool dead = false;                        // a wait ran out: the rest is NaN
+        // the next item of the walk after round r (nitems if none)
+        auto next_item = [&](int r) {
+            for (int r2 = r + 1; r2 * (int)gridDim.x < nitems; ++r2) {
+                const int x2 = walk_item(r2, nitems);
+                if (x2 < nitems) return x2;
+            }
+            return nitems;
+        };
+        // stage the query statistics of a tile as one negated bias per
+        // query, -(m2 + log2(l)), so a weight is 2^(s c2 + nbias); -inf past
+        // T (weight 0)
+        auto nbias = [&](int uq, int iq) { return iq < T ? -(m2[(size_t)uq * T + iq] + log2f(lin[(size_t)uq * T + iq])) : -INFINITY; };
+        bool staged = false;                      // the item's first tile already staged by the previous item
         for (int r = 0; r * (int)gridDim.x < nitems; ++r) {
             const int x = walk_item(r, nitems);
             if (x >= nitems) continue;
@@ -575,14 +588,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int j = jb * kT + 32 * q + lane;    // key within the unit
             const float* m2u = m2 + (size_t)u * T;
             const float* lu = lin + (size_t)u * T;
-            // stage the query statistics of the item's first tile as one
-            // negated bias per query, -(m2 + log2(l)), so a weight is
-            // 2^(s c2 + nbias); -inf past T (weight 0).  The buffer was last
-            // read two tiles ago, before the barrier that opened the last one.
-            if (!dead) {
-                const int i = jb * kT + et;
-                S.colstat[gt & 1][et] = i < T ? -(m2u[i] + log2f(lu[i])) : -INFINITY;
-            }
+            // the next item's first tile, staged during this item's last one
+            const int xn = next_item(r);
+            int un = 0, jbn = 0;
+            if (xn < nitems) group_order(xn, U, nb, g, un, jbn);
+            // (the buffer was last read two tiles ago, before the barrier
+            // that opened the last one)
+            if (!dead && !staged) S.colstat[gt & 1][et] = nbias(u, jb * kT + et);
             float cs = 0.f, cc = 0.f;                 // Kahan-summed column sum
             double bsB = 0.0, bsr = 0.0;              // band sums (rows j .. j+w-1)
             for (int t = 0; t < ntiles && !dead; ++t, ++gt) {
@@ -590,12 +602,17 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int ib = jb + t;
                 // some key of the block has rows of this tile in its band
                 const bool band = BAND && ib * kT < (jb + 1) * kT + wmax;
-                // the next tile's statistics, stored after this tile
+                // the next tile's statistics (this item's, or the next item's
+                // first), stored after this tile
                 float nm = 0.f, nl = 0.f;
-                const int inext = (ib + 1) * kT + et;
-                if (t + 1 < ntiles && inext < T) {
-                    nm = m2u[inext];
-                    nl = lu[inext];
+                const bool last = t + 1 == ntiles;
+                const int inext = last ? jbn * kT + et : (ib + 1) * kT + et;
+                const float* m2n = last ? m2 + (size_t)un * T : m2u;
+                const float* ln = last ? lin + (size_t)un * T : lu;
+                const bool more = !last || xn < nitems;
+                if (more && inext < T) {
+                    nm = m2n[inext];
+                    nl = ln[inext];
                 }
                 const bool ok = tc_wait(S, &S.acc_full[b], (uint32_t)(gt >> 1) & 1u, err);
                 // agreed by all epilogue threads; also publishes the statistics staged before
@@ -659,8 +676,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                     bsr += (double)partr;
                 }
                 // publish the next tile's statistics into the other buffer
-                if (t + 1 < ntiles) S.colstat[b ^ 1][et] = inext < T ? -(nm + log2f(nl)) : -INFINITY;
+                if (more) S.colstat[b ^ 1][et] = inext < T ? -(nm + log2f(nl)) : -INFINITY;
             }
+            staged = !dead && xn < nitems;
             // an abandoned walk leaves NaN in its columns
             if (j < T) {
                 cout[(size_t)u * T + j] = dead ? nan : (double)cs - (double)cc;
