@@ -116,6 +116,14 @@ __device__ __forceinline__ void tc_ld32_wait(uint32_t (&r)[32])
     asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]) :: "memory");
 }
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3f(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // 2^x by the MUFU instruction (2 ulp; results below 2^-126 flush to 0)
 __device__ __forceinline__ float ex2_fast(float x)
 {
@@ -470,12 +478,15 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(cur[e]);
                     const int j0 = t * kT + ch * 32;
-                    float cm = -INFINITY;
+                    if (diag) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        if (diag && j0 + e > i) v[e] = -INFINITY;
-                        cm = fmaxf(cm, v[e]);
+                        for (int e = 0; e < 32; ++e)
+                            if (j0 + e > i) v[e] = -INFINITY;
                     }
+                    // the chunk's max two columns per instruction (three-input max)
+                    float cm = fmaxf(v[0], v[1]);
+#pragma unroll
+                    for (int e = 2; e < 32; e += 2) cm = max3f(cm, v[e], v[e + 1]);
                     if (cm != -INFINITY) {
                         cm *= c2;
                         if (cm > m) {
