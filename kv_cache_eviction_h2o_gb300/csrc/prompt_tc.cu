@@ -487,14 +487,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                     float cm = fmaxf(v[0], v[1]);
 #pragma unroll
                     for (int e = 2; e < 32; e += 2) cm = max3f(cm, v[e], v[e + 1]);
-                    if (cm != -INFINITY) {
-                        cm *= c2;
-                        if (cm > m) {
-                            const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - cm);
-                            l *= alpha;
-                            lc *= alpha;
-                            m = cm;
-                        }
+                    {
+                        // branch-free rescale: alpha is exactly 1 when the max
+                        // stays, 0 before the first finite column; a chunk of
+                        // masked columns (-inf) leaves m, and adds nothing
+                        const float mn = fmaxf(m, cm * c2);
+                        const float alpha = (mn == m) ? 1.f : ((m == -INFINITY) ? 0.f : exp2f(m - mn));
+                        l *= alpha;
+                        lc *= alpha;
+                        m = mn;
                         // exponent arguments and running sums two columns at a time
                         const float2 c22 = make_float2(c2, c2), nm2 = make_float2(-m, -m);
                         float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
