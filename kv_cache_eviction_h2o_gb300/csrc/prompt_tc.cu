@@ -25,6 +25,7 @@
 #include <algorithm>
 #include <cfloat>
 #include <cstddef>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -641,41 +642,48 @@ __global__ void __launch_bounds__(kThreads, 2)
                 uint32_t ra[32], rb[32];
                 tc_ld32_issue(tcol, ra);
                 tc_ld32_wait(ra);
+                // the tile's four 32-column chunks; the causal and past-T
+                // masks are compiled only into the edge tiles' copy
+                auto chunks = [&](auto edge_tag) {
+                    constexpr bool EDGE = decltype(edge_tag)::value;
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t (&cur)[32] = (ch & 1) ? rb : ra;
-                    uint32_t (&nxt)[32] = (ch & 1) ? ra : rb;
-                    if (ch + 1 < 4) tc_ld32_issue(tcol + (uint32_t)((ch + 1) * 32), nxt);
-                    const int i0 = ib * kT + ch * 32;
-                    const float2 c22 = make_float2(c2, c2);
-                    float2 pa = make_float2(0.f, 0.f), pb = make_float2(0.f, 0.f);
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint32_t (&cur)[32] = (ch & 1) ? rb : ra;
+                        uint32_t (&nxt)[32] = (ch & 1) ? ra : rb;
+                        if (ch + 1 < 4) tc_ld32_issue(tcol + (uint32_t)((ch + 1) * 32), nxt);
+                        const int i0 = ib * kT + ch * 32;
+                        const float2 c22 = make_float2(c2, c2);
+                        float2 pa = make_float2(0.f, 0.f), pb = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        const float4 b4 = *reinterpret_cast<const float4*>(bs + ch * 32 + e);
-                        const float2 ta = __ffma2_rn(make_float2(__uint_as_float(cur[e]), __uint_as_float(cur[e + 1])),
-                                                     c22, make_float2(b4.x, b4.y));
-                        const float2 tb = __ffma2_rn(make_float2(__uint_as_float(cur[e + 2]), __uint_as_float(cur[e + 3])),
-                                                     c22, make_float2(b4.z, b4.w));
-                        float w0 = ex2_fast(ta.x), w1 = ex2_fast(ta.y), w2 = ex2_fast(tb.x), w3 = ex2_fast(tb.y);
-                        if (edge) {
-                            if (i0 + e < j) w0 = 0.f;
-                            if (i0 + e + 1 < j) w1 = 0.f;
-                            if (i0 + e + 2 < j) w2 = 0.f;
-                            if (i0 + e + 3 < j) w3 = 0.f;
+                        for (int e = 0; e < 32; e += 4) {
+                            const float4 b4 = *reinterpret_cast<const float4*>(bs + ch * 32 + e);
+                            const float2 ta = __ffma2_rn(make_float2(__uint_as_float(cur[e]), __uint_as_float(cur[e + 1])),
+                                                         c22, make_float2(b4.x, b4.y));
+                            const float2 tb = __ffma2_rn(make_float2(__uint_as_float(cur[e + 2]), __uint_as_float(cur[e + 3])),
+                                                         c22, make_float2(b4.z, b4.w));
+                            float w0 = ex2_fast(ta.x), w1 = ex2_fast(ta.y), w2 = ex2_fast(tb.x), w3 = ex2_fast(tb.y);
+                            if constexpr (EDGE) {
+                                if (i0 + e < j) w0 = 0.f;
+                                if (i0 + e + 1 < j) w1 = 0.f;
+                                if (i0 + e + 2 < j) w2 = 0.f;
+                                if (i0 + e + 3 < j) w3 = 0.f;
+                            }
+                            pa = __fadd2_rn(pa, make_float2(w0, w1));
+                            pb = __fadd2_rn(pb, make_float2(w2, w3));
+                            if (band) {
+                                const int d0 = dj + ch * 32 + e;
+                                partB += (d0 < wB ? w0 : 0.f) + (d0 + 1 < wB ? w1 : 0.f) + (d0 + 2 < wB ? w2 : 0.f) +
+                                         (d0 + 3 < wB ? w3 : 0.f);
+                                partr += (d0 < wr ? w0 : 0.f) + (d0 + 1 < wr ? w1 : 0.f) + (d0 + 2 < wr ? w2 : 0.f) +
+                                         (d0 + 3 < wr ? w3 : 0.f);
+                            }
                         }
-                        pa = __fadd2_rn(pa, make_float2(w0, w1));
-                        pb = __fadd2_rn(pb, make_float2(w2, w3));
-                        if (band) {
-                            const int d0 = dj + ch * 32 + e;
-                            partB += (d0 < wB ? w0 : 0.f) + (d0 + 1 < wB ? w1 : 0.f) + (d0 + 2 < wB ? w2 : 0.f) +
-                                     (d0 + 3 < wB ? w3 : 0.f);
-                            partr += (d0 < wr ? w0 : 0.f) + (d0 + 1 < wr ? w1 : 0.f) + (d0 + 2 < wr ? w2 : 0.f) +
-                                     (d0 + 3 < wr ? w3 : 0.f);
-                        }
+                        part += (pa.x + pa.y) + (pb.x + pb.y);
+                        if (ch + 1 < 4) tc_ld32_wait(nxt);
                     }
-                    part += (pa.x + pa.y) + (pb.x + pb.y);
-                    if (ch + 1 < 4) tc_ld32_wait(nxt);
-                }
+                };
+                if (edge) chunks(std::true_type{});
+                else chunks(std::false_type{});
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&S.acc_empty[b]);
