@@ -825,6 +825,119 @@ __global__ void __launch_bounds__(64) lsh_replay_pipe_kernel(CacheView cv, Promp
     if (lane == 0) cv.ustate[unit] = make_int2(n0, T_);
 }
 
+// The pipelined replay with one CTA of WU warps per unit (recent window
+// r >= 2, budgets up to 32 WU NR): thread tid owns slots tid + 32 WU i, so a
+// step scans NR slots per thread instead of B / 32, and the warps' largest
+// keys meet through shared memory (one buffer per step parity) and one CTA
+// barrier.  Same rule, keys and pipelining as lsh_replay_pipe_kernel:
+// step t + 1's scan runs before step t's victim is applied (that slot holds
+// position t, no candidate at t + 1), each thread keeping its two largest
+// candidate keys.
+template <int NR, int WU>
+__global__ void __launch_bounds__(32 * WU) lsh_replay_wide_kernel(CacheView cv, PromptArgs pa)
+{
+    constexpr int NT = 32 * WU;
+    __shared__ unsigned red[2][WU];
+    const int B = cv.B, T_ = pa.T, r = cv.r;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int unit = blockIdx.x;
+    const uint32_t* cq = pa.cq + (size_t)unit * T_;
+    const uint32_t* ck = pa.ck + (size_t)unit * T_;
+    const int n0 = min(T_, B);
+    uint32_t code[NR];
+    int pos[NR];
+    unsigned vmask = 0u;                        // bit i: slot tid + NT i exists
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+        const int s = tid + NT * i;
+        const bool ok = s < n0;
+        vmask |= ok ? (1u << i) : 0u;
+        pos[i] = ok ? s : INT_MAX;
+        code[i] = ok ? ck[s] : 0u;
+    }
+    auto slot_key = [&](uint32_t q, int i) -> unsigned {
+        return ((unsigned)__popc(q ^ code[i]) << 20) | (0xFFFFFu - (unsigned)(tid + NT * i));
+    };
+    // the CTA-wide max of every thread's `v` (parity: the step's buffer)
+    auto cta_max = [&](unsigned v, int parity) -> unsigned {
+        v = __reduce_max_sync(kFull, v);
+        if (lane == 0) red[parity][warp] = v;
+        __syncthreads();
+        unsigned m = red[parity][0];
+#pragma unroll
+        for (int w = 1; w < WU; ++w) m = max(m, red[parity][w]);
+        return m;
+    };
+    auto every_slot_best = [&](uint32_t q, int parity) -> unsigned {
+        unsigned b = 0u;
+#pragma unroll
+        for (int i = 0; i < NR; ++i)
+            if (vmask >> i & 1u) b = max(b, slot_key(q, i));
+        return cta_max(b, parity);
+    };
+    auto replace = [&](unsigned key, uint32_t kcode, int p) {
+        const int v = (int)(0xFFFFFu - (key & 0xFFFFFu));
+        const int vt = v % NT, iv = v / NT;
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            const bool hit = (tid == vt) && (i == iv);
+            code[i] = hit ? kcode : code[i];
+            pos[i] = hit ? p : pos[i];
+        }
+    };
+    uint32_t qb = 0u, kb = 0u, qn = 0u, kn = 0u;
+    {
+        const int t0 = B + lane, t1 = B + 32 + lane;
+        if (t0 < T_) { qb = cq[t0]; kb = ck[t0]; }
+        if (t1 < T_) { qn = cq[t1]; kn = ck[t1]; }
+    }
+    unsigned prev = 0u;
+    uint32_t qprev = 0u, kprev = 0u;
+    int par = 0;                                // parity of the reduction buffer
+    for (int t = B; t < T_; ++t) {
+        const int o = (t - B) & 31;
+        if (o == 0 && t > B) {
+            qb = qn; kb = kn;
+            const int tt = t + 32 + lane;
+            qn = tt < T_ ? cq[tt] : 0u;
+            kn = tt < T_ ? ck[tt] : 0u;
+        }
+        const uint32_t q = __shfl_sync(kFull, qb, o);
+        const uint32_t knew = __shfl_sync(kFull, kb, o);
+        const int tr = t - r;
+        unsigned b1 = 0u, b2 = 0u;
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            const unsigned k = pos[i] <= tr ? slot_key(q, i) : 0u;
+            b2 = max(b2, min(b1, k));
+            b1 = max(b1, k);
+        }
+        if (t > B) {
+            if (prev == 0u) {
+                prev = every_slot_best(qprev, par);
+                par ^= 1;
+            }
+            if ((b1 & 0xFFFFFu) == (prev & 0xFFFFFu)) b1 = b2;
+            replace(prev, kprev, t - 1);
+        }
+        prev = cta_max(b1, par);
+        par ^= 1;
+        qprev = q;
+        kprev = knew;
+    }
+    if (T_ > B) {
+        if (prev == 0u) prev = every_slot_best(qprev, par);
+        replace(prev, kprev, T_ - 1);
+    }
+    const size_t ub = (size_t)unit * B;
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+        const int s = tid + NT * i;
+        if (s < B) cv.pos[ub + s] = (vmask >> i & 1u) ? pos[i] : -1;
+    }
+    if (tid == 0) cv.ustate[unit] = make_int2(n0, T_);
+}
+
 // Replay the HashEvict replacement rule over the prompt, one warp per unit:
 // the first B tokens fill the slots; token t >= B replaces the slot with the
 // largest Hamming distance to code(q_t) among slots with position <= t - r
@@ -947,6 +1060,18 @@ cudaError_t lsh_t(const CacheView& c, const PromptArgs& p, const float* W_host, 
         reinterpret_cast<const T*>(p.Q), reinterpret_cast<const T*>(p.K), wp, ntok, p.cq, p.ck);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (c.r >= 2 && c.B > 96 && c.B <= 128 * 4) {
+        // four warps per unit, one CTA each (measured against two and eight
+        // warps: 538 / 599 / 598 us for the OPT-6.7B-shaped layer's prompt phase)
+        const int nr = (c.B + 127) / 128;
+        if (nr <= 1) lsh_replay_wide_kernel<1, 4><<<(unsigned)c.U, 128, 0, st>>>(c, p);
+        else if (nr <= 2) lsh_replay_wide_kernel<2, 4><<<(unsigned)c.U, 128, 0, st>>>(c, p);
+        else if (nr <= 3) lsh_replay_wide_kernel<3, 4><<<(unsigned)c.U, 128, 0, st>>>(c, p);
+        else lsh_replay_wide_kernel<4, 4><<<(unsigned)c.U, 128, 0, st>>>(c, p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return gather_t<T, D>(c, p, true, st);
+    }
     if (c.r >= 2 && c.B <= 32 * 16) {
         const unsigned blocks = (unsigned)((c.U + 1) / 2);
         const int nr = (c.B + 31) / 32;

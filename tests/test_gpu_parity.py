@@ -154,6 +154,7 @@ def test_edge_cases_h2o(T, B, H, r, dtype, d):
                                    (300, 100, 2),      # smallest window of the pipelined prompt replay
                                    (400, 250, 60), (700, 500, 250),
                                    (600, 480, 480),    # window = budget: one candidate per step
+                                   (300, 129, 3), (600, 384, 64), (700, 512, 200),   # four-warp replay: 2, 3, 4 slots a thread
                                    (1500, 1100, 100)])
 @pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
 def test_edge_cases_lsh(T, B, r, dtype, d):
