@@ -294,7 +294,7 @@ def prompt_launches(rule, G):
     if rule == "sh":
         return 4
     if rule == "fg":
-        return 5          # row statistics, column and band sums, selection, policy, gather
+        return 6          # row statistics, column and band sums, selection, policy, unit lists, gather
     return 5 if G > 1 else 4
 
 
@@ -619,8 +619,13 @@ class Job:
     def traffic_key(self):
         return "%s%s@%s" % (self.decode_kernel(), {8: "_kv8", 4: "_kv4"}.get(self.qb, ""), self.w.name)
 
+    def decode_launches(self):
+        """Kernels one decode step launches: per-head policies take two (the
+        compressed policies' units, then the full caches'), the rest one."""
+        return 2 if self.rule == "fg" else 1
+
     def launches_per_step(self):
-        return self.NL * (prompt_launches(self.rule, self.w.groups) + self.S)
+        return self.NL * (prompt_launches(self.rule, self.w.groups) + self.S * self.decode_launches())
 
     def destroy(self):
         for h in self.hs:
@@ -645,6 +650,9 @@ def rooflines(job, phase_ms, elapsed_ms, K):
     rec = {"kernel": job.decode_kernel(), "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
            "frac": ach / hbm, "traffic": ncu_traffic(job.traffic_key()), "algorithmic_bytes": by,
            "launch_us": t_launch * 1e6, "peak_source": peak_src, "share": phase_ms["decode"] / elapsed_ms}
+    if job.decode_launches() > 1:
+        # bytes and time of the step's launches together
+        rec["launches_per_decode_step"] = job.decode_launches()
     if job.rule == "h2o" and G == 1 and not job.qb:
         mb = method_bytes(U, B, d, 2)
         rec["method_bytes"] = mb

@@ -353,8 +353,11 @@ int h2o_set_stream(h2o_handle h, void* cuda_stream);
 /*
  * h2o_set_decode_split -- CTAs (1..16) that share one unit's slots in the
  * decode kernels (a thread-block cluster); 0 restores the automatic choice.
- * Affects performance only, never results.  H2O_ERR_STATE on a grouped-query
- * handle (G > 1), whose cluster is always its G query heads.
+ * Affects performance only, never results.  H2O_ERR_ARG below
+ * ceil(budget / 1024); on a per-head-policy handle the bound is the
+ * compressed policies' budget, and the units on the full cache take at
+ * least ceil(full_budget / 1024) CTAs whatever is set.  H2O_ERR_STATE on a
+ * grouped-query handle (G > 1), whose cluster is always its G query heads.
  */
 int h2o_set_decode_split(h2o_handle h, int ctas_per_unit);
 

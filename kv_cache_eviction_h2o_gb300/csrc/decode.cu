@@ -55,7 +55,20 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     const CacheView& c = a.c;
     const int C = (int)cluster_nctarank();
     const int rank = (int)cluster_ctarank();
-    const int unit = blockIdx.x / C;
+    int unit = blockIdx.x / C;
+    if (a.ulist) {
+        // a unit list (per-head policies): written by the handle's earlier
+        // kernels, so read after the dependency wait unless the previous
+        // kernel cannot have written it; a whole cluster exits together, and
+        // only after the wait, so that this grid's end still implies the
+        // previous kernel's (the next launch waits on this one alone)
+        if (!a.early) grid_dependency_wait();
+        if (unit >= *a.ucount) {
+            if (a.early) grid_dependency_wait();
+            return;
+        }
+        unit = a.ulist[unit];
+    }
     const size_t qrow = GQ ? (size_t)blockIdx.x : (size_t)unit;   // query / output row
 
     const int B = c.B;

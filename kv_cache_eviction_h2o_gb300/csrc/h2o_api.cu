@@ -143,6 +143,7 @@ struct h2o_ctx {
     double2* rec;              // [U] {local, frequency + local} recoveries
     double* bandB;             // prompt scratch [U][T]: band sums of width B_sel and r
     double* bandr;
+    int* ulists;               // [2U + 2]: units of policy 0/1, of policy 2, then the two counts
 };
 
 namespace {
@@ -184,6 +185,7 @@ void free_prompt(h2o_ctx* h)
 void free_all(h2o_ctx* h)
 {
     free_prompt(h);
+    cudaFree(h->ulists);
     cudaFree(h->K); cudaFree(h->V); cudaFree(h->score); cudaFree(h->pos); cudaFree(h->code);
     cudaFree(h->ustate); cudaFree(h->err); cudaFree(h->W); cudaFree(h->kvs); cudaFree(h->upol); cudaFree(h->rec);
     free(h->W_host);
@@ -197,7 +199,8 @@ int rc0_alloc(h2o_ctx* h, size_t U)
 {
     int rc;
     if ((rc = dev_alloc((void**)&h->upol, U * sizeof(int4), "unit policies")) ||
-        (rc = dev_alloc((void**)&h->rec, U * sizeof(double2), "policy recoveries")))
+        (rc = dev_alloc((void**)&h->rec, U * sizeof(double2), "policy recoveries")) ||
+        (rc = dev_alloc((void**)&h->ulists, (2 * U + 2) * sizeof(int), "policy unit lists")))
         return rc;
     return H2O_OK;
 }
@@ -310,7 +313,16 @@ int create(h2o_handle* out, int kind, int budget, int heavy, int recent, int bat
         for (size_t u = 0; u < U; ++u) init[u] = make_int4(budget, heavy, recent, 1);
         e = cudaMemcpyAsync(h->upol, init, U * sizeof(int4), cudaMemcpyHostToDevice, h->stream);
         if (e == cudaSuccess) e = cudaMemsetAsync(h->rec, 0, U * sizeof(double2), h->stream);
+        // every unit on policy 1 until a prompt is profiled
+        int* lists = static_cast<int*>(malloc((2 * U + 2) * sizeof(int)));
+        if (!lists) { free(init); free_all(h); delete h; return fail(H2O_ERR_ALLOC, "host allocation failed"); }
+        for (size_t u = 0; u < U; ++u) { lists[u] = (int)u; lists[U + u] = 0; }
+        lists[2 * U] = (int)U;
+        lists[2 * U + 1] = 0;
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(h->ulists, lists, (2 * U + 2) * sizeof(int), cudaMemcpyHostToDevice, h->stream);
         if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+        free(lists);
         free(init);
     }
     if (e != cudaSuccess) { free_all(h); delete h; return cuda_fail(e, "initialise state"); }
@@ -572,6 +584,7 @@ int fg_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T)
     cudaError_t e = launch_prompt_stats(cv, pa, h->stream);
     if (e == cudaSuccess) e = launch_select(cv, pa, h->stream);
     if (e == cudaSuccess) e = launch_fg_policy(cv, pa, fa, h->stream);
+    if (e == cudaSuccess) e = launch_fg_lists(h->upol, h->U, h->ulists, h->ulists + 2 * h->U, h->stream);
     if (e == cudaSuccess) e = launch_gather(cv, pa, false, h->stream);
     if (e != cudaSuccess) return cuda_fail(e, "fg_prefill launch");
     h->last_T = T;
@@ -584,11 +597,30 @@ int fg_decode_step(h2o_handle h, const void* q, const void* k, const void* v, fl
     int rc = check_step(h, kFG, q, k, v, out);
     if (rc) return rc;
     if (inject("launch")) return fail(H2O_ERR_CUDA, "kernel launch failed (injected)");
+    // two launches over the units' lists: the compressed policies (budget
+    // B_sel) with their own split, then the full caches (B_full) with theirs;
+    // a unit's CTAs exist in one of them only, so the second may read its
+    // units' caches while the first drains
     DecodeArgs a = {};
     a.c = view(h); a.q = q; a.k = k; a.v = v; a.out = out; a.victim_out = victim_out; a.G = 1;
     a.early = note_cache_write(h->device, h->stream, h) ? 1 : 0;
     a.num_sms = h->num_sms;
-    cudaError_t e = launch_h2o_decode(a, decode_split(h), h->stream);
+    const int* counts = h->ulists + 2 * h->U;
+    int s_small = h->split > 0 ? h->split : auto_decode_split(h->U, h->B_sel, h->num_sms);
+    int s_full = h->split > 0 ? h->split : auto_decode_split(h->U, h->B_full, h->num_sms);
+    s_small = std::max(s_small, (h->B_sel + 1023) / 1024);
+    s_full = std::max(s_full, (h->B_full + 1023) / 1024);
+    s_small = std::min(s_small, max_decode_split());
+    s_full = std::min(s_full, max_decode_split());
+    a.ulist = h->ulists;
+    a.ucount = counts;
+    cudaError_t e = launch_h2o_decode(a, s_small, h->stream);
+    if (e == cudaSuccess) {
+        a.ulist = h->ulists + h->U;
+        a.ucount = counts + 1;
+        a.early = 1;
+        e = launch_h2o_decode(a, s_full, h->stream);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "fg_decode_step launch");
     return H2O_OK;
 }
@@ -783,8 +815,11 @@ int h2o_set_decode_split(h2o_handle h, int ctas_per_unit)
         return fail(H2O_ERR_STATE, "a grouped-query handle runs one CTA per query head; its split is not settable");
     if (ctas_per_unit < 0 || ctas_per_unit > max_decode_split())
         return fail(H2O_ERR_ARG, "ctas_per_unit must be in [0, %d]", max_decode_split());
-    if (ctas_per_unit > 0 && ctas_per_unit < (h->B + 1023) / 1024)
-        return fail(H2O_ERR_ARG, "ctas_per_unit must be >= %d for budget %d", (h->B + 1023) / 1024, h->B);
+    // per-head policies: the compressed policies' budget bounds the split;
+    // the full caches' launch raises it to what their budget needs
+    const int Bmin = h->kind == kFG ? h->B_sel : h->B;
+    if (ctas_per_unit > 0 && ctas_per_unit < (Bmin + 1023) / 1024)
+        return fail(H2O_ERR_ARG, "ctas_per_unit must be >= %d for budget %d", (Bmin + 1023) / 1024, Bmin);
     h->split = ctas_per_unit;
     return H2O_OK;
 }

@@ -36,6 +36,8 @@ struct DecodeArgs {
     int G;              // H2O: query heads sharing each cache unit (0 or 1: one);
                         // q and out then hold U * G rows, head g of unit u in row u * G + g
     int num_sms;        // the device's SM count (selects the tile)
+    const int* ulist;   // or nullptr: CTA group g takes unit ulist[g] for g < *ucount and exits beyond
+    const int* ucount;  // (written by earlier kernels of the handle: read after the dependency wait)
 };
 
 struct PromptArgs {
@@ -98,6 +100,9 @@ cudaError_t launch_gather(const CacheView& c, const PromptArgs& p, bool with_cod
 // selection already made, the policy, and the kept set of local and full
 // units rewritten (the gather follows)
 cudaError_t launch_fg_policy(const CacheView& c, const PromptArgs& p, const FgArgs& f, cudaStream_t st);
+// per-head policies: the units of policy 0 or 1 into lists[0 ..), those of
+// policy 2 into lists[U ..), in unit order; counts[0], counts[1]
+cudaError_t launch_fg_lists(const int4* upol, int U, int* lists, int* counts, cudaStream_t st);
 // One CTA whose bounded wait on a barrier nobody completes must run out and
 // set *err.
 cudaError_t launch_wait_selftest(int* err, cudaStream_t st);

@@ -1311,6 +1311,44 @@ cudaError_t launch_fg_policy(const CacheView& c, const PromptArgs& p, const FgAr
     return cudaGetLastError();
 }
 
+// One CTA: the units of the compressed policies (0, 1) and of the full
+// cache (2), each list in unit order (a ballot and a running offset per
+// 1024 units).
+__global__ void __launch_bounds__(1024) fg_lists_kernel(const int4* __restrict__ upol, int U, int* __restrict__ lists,
+                                                        int* __restrict__ counts)
+{
+    __shared__ int wsum[2][32];
+    __shared__ int base[2];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) { base[0] = 0; base[1] = 0; }
+    __syncthreads();
+    for (int u0 = 0; u0 < U; u0 += 1024) {
+        const int u = u0 + tid;
+        const bool live = u < U;
+        const bool full = live && upol[u].w == 2;
+        const unsigned mf = __ballot_sync(0xffffffffu, full), ms = __ballot_sync(0xffffffffu, live && !full);
+        if (lane == 0) { wsum[0][warp] = __popc(ms); wsum[1][warp] = __popc(mf); }
+        __syncthreads();
+        int off0 = base[0], off1 = base[1];
+        for (int w = 0; w < warp; ++w) { off0 += wsum[0][w]; off1 += wsum[1][w]; }
+        const unsigned below = (1u << lane) - 1u;
+        if (live && !full) lists[off0 + __popc(ms & below)] = u;
+        if (full) lists[U + off1 + __popc(mf & below)] = u;
+        __syncthreads();
+        if (tid == 0) {
+            for (int w = 0; w < 32; ++w) { base[0] += wsum[0][w]; base[1] += wsum[1][w]; }
+        }
+        __syncthreads();
+    }
+    if (tid == 0) { counts[0] = base[0]; counts[1] = base[1]; }
+}
+
+cudaError_t launch_fg_lists(const int4* upol, int U, int* lists, int* counts, cudaStream_t st)
+{
+    fg_lists_kernel<<<1, 1024, 0, st>>>(upol, U, lists, counts);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gather(const CacheView& c, const PromptArgs& p, bool with_codes, cudaStream_t st)
 {
     const bool bf = c.dtype == 1;

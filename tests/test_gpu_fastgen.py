@@ -142,3 +142,43 @@ def test_policy_profile_on_a_persistent_walk():
         record("fastgen persistent walk", policy_flips=flips, near_ties=near0, units=U)
     finally:
         dev.close()
+
+
+def test_every_head_on_the_full_cache():
+    """tau = 1 on diffuse attention (Gaussian queries and keys, a prompt four
+    times the budget): no compressed policy recovers the whole attention, so
+    every head keeps its full cache and the decode step's launch over the
+    compressed policies' units has none."""
+    from types import SimpleNamespace
+    U, T, S, d = 4, 64, 6, 64
+    rng = np.random.default_rng(31)
+    f = lambda *shape: rng.standard_normal(shape, dtype=np.float32)
+    g = {"Q": f(U, T, d), "K": f(U, T, d), "V": f(U, T, d), "q": f(S, U, d), "k": f(S, U, d), "v": f(S, U, d)}
+    w = SimpleNamespace(units=U, budget=16, heavy=8, recent=8, scale=1.0 / np.sqrt(d))
+    full = T + S
+    dev = Dev("fg", U, d, w.budget, w.heavy, w.recent, "f32", w.scale, fg=(full, 1.0))
+    try:
+        dev.prefill(g["Q"], g["K"], g["V"])
+        pol_g, states, params, flips, near0 = _profile_and_align(dev, g, w, 1.0, full)
+        assert (pol_g == 2).all(), pol_g
+        _lockstep(dev, states, params, g, T, w.scale)
+    finally:
+        dev.close()
+
+
+@pytest.mark.parametrize("split", [1, 2, 4])
+def test_per_head_policies_with_a_set_split(split):
+    """A decode split set on the handle: both launches (compressed policies,
+    full caches) take it, raised where a full cache needs more CTAs."""
+    w = wl.WORKLOADS["fastgen-opt-6.7b"]
+    g = wl.generate(w, units=[0, 1, 2, 3, 33, 64], steps=8)
+    U = g["Q"].shape[0]
+    dev = Dev("fg", U, w.head_dim, w.budget, w.heavy, w.recent, w.dtype, w.scale, fg=(w.full_budget, w.tau),
+              split=split)
+    try:
+        dev.prefill(g["Q"], g["K"], g["V"])
+        pol, states, params, flips, near0 = _profile_and_align(dev, g, w, w.tau, w.full_budget)
+        near = _lockstep(dev, states, params, g, w.prompt, w.scale)
+        record("fastgen split=%d" % split, policy_flips=flips, near_ties=near0 + near, units=U)
+    finally:
+        dev.close()
