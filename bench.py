@@ -278,6 +278,24 @@ def prefill_flops(U, T, d):
     return 2 * 2 * U * d * T * (T + 1) // 2
 
 
+def prefill_bytes(U, G, T, d, B, qb=0, fg=False):
+    """Algorithmic HBM bytes of one H2O prompt phase (U cache units, G query
+    heads each): each score pass reads Q and K once; pass 1 writes the row
+    max and normaliser (4 + 4 B per query row) that pass 2 reads; pass 2
+    writes the fp64 column sums that the selection reads (per query head,
+    then per unit, for G > 1); the gather reads the kept prompt rows of K
+    and V and writes the slots' rows (codes and a scale pair when
+    quantised), positions and 8-byte score pairs.  Per-head policies add
+    two fp64 band sums per key, written and read."""
+    rows = U * G * T * d * 2 + U * T * d * 2
+    stats = 2 * U * G * T * 8
+    cols = 2 * U * G * T * 8 + (2 * U * T * 8 if G > 1 else 0)
+    kept = min(B, T)
+    gather = U * kept * d * 2 * 2 + U * B * (2 * code_row(d, 2, qb) + (8 if qb else 0) + 4 + 8)
+    band = 2 * 2 * U * T * 8 if fg else 0
+    return 2 * rows + stats + cols + gather + band
+
+
 def lsh_code_flops(U, T, d):
     """Prompt sign codes: 32 fp32 multiply-add chains of d terms for every
     query and key row (2 flops per multiply-add)."""
@@ -662,11 +680,21 @@ def rooflines(job, phase_ms, elapsed_ms, K):
     if job.rule in ("h2o", "fg"):
         fl = prefill_flops(U * G, T, d)
         ach = fl / t_pre / 1e12
-        rl.append({"kernel": ("fg_prefill" if job.rule == "fg" else "h2o_prefill") + ("_gqa" if G > 1 else ""),
-                   "bound": "tensor", "achieved": ach,
-                   "peak": tf_sus, "unit": "TFLOP/s", "frac": ach / tf_sus, "traffic": None,
-                   "algorithmic_flops": fl, "launch_us": t_pre * 1e6, "peak_source": peak_src + " (sustained)",
-                   "share": phase_ms["prefill"] / elapsed_ms})
+        Bp = w.full_budget if job.rule == "fg" else B
+        by = prefill_bytes(U, G, T, d, Bp, job.qb, job.rule == "fg")
+        hb = by / t_pre / 1e9
+        tens = {"bound": "tensor", "achieved": ach, "peak": tf_sus, "unit": "TFLOP/s", "frac": ach / tf_sus,
+                "peak_source": peak_src + " (sustained)"}
+        mem = {"bound": "hbm", "achieved": hb, "peak": hbm, "unit": "GB/s", "frac": hb / hbm, "peak_source": peak_src}
+        # the phase is tensor-bound on long prompts and HBM-bound on short
+        # ones: the nearer roof is the one reported, the other beside it
+        top, other = (tens, mem) if tens["frac"] >= mem["frac"] else (mem, tens)
+        rec = {"kernel": ("fg_prefill" if job.rule == "fg" else "h2o_prefill") + ("_gqa" if G > 1 else "")}
+        rec.update(top)
+        rec.update({"traffic": None, "algorithmic_flops": fl, "algorithmic_bytes": by, "launch_us": t_pre * 1e6,
+                    "share": phase_ms["prefill"] / elapsed_ms,
+                    "other_roof": {k: other[k] for k in ("bound", "achieved", "peak", "unit", "frac")}})
+        rl.append(rec)
     elif job.rule == "lsh":
         rl.append({"kernel": "lsh_prefill", "bound": "latency", "launch_us": t_pre * 1e6,
                    "serial_steps": max(0, T - B),

@@ -503,85 +503,109 @@ __global__ void __launch_bounds__(256) fg_policy_kernel(CacheView cv, PromptArgs
 }
 
 // Copy the prompt rows named by pos[] into the slots (zero for empty slots);
-// one warp per slot: lanes 0..15 move K, 16..31 move V (16 bytes each).
+// lanes 0..15 of a warp move K, 16..31 move V (16 bytes each).  A warp takes
+// kGatherSlots consecutive slots and requests all their positions, then all
+// their rows, before it stores any: four rows in flight per lane instead of
+// one, which the copy needs to reach HBM speed.
+constexpr int kGatherSlots = 4;
+
 template <typename T, int D>
 __global__ void __launch_bounds__(256) gather_kernel(CacheView cv, PromptArgs pa, int with_codes)
 {
     constexpr int NV = D * (int)sizeof(T) / 16;   // 16-byte vectors per row
-    const int lane = threadIdx.x & 31;
+    constexpr int VE = 16 / (int)sizeof(T);       // elements per 16-byte vector
+    constexpr int VPL = (NV + 15) / 16;           // vectors per lane of a half-warp
+    constexpr int SW = kGatherSlots;
+    const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
     const long long total = (long long)cv.U * cv.B;
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
-    constexpr int VE = 16 / (int)sizeof(T);       // elements per 16-byte vector
-    constexpr int VPL = (NV + 15) / 16;           // vectors per lane of a half-warp
-    for (long long slot = wid; slot < total; slot += nw) {
-        const int unit = (int)(slot / cv.B);
-        const int p = cv.pos[slot];
-        const int half = lane >> 4, l16 = lane & 15;
-        const T* srcbase = reinterpret_cast<const T*>(half ? pa.V : pa.K) + ((size_t)unit * pa.T) * D;
-        if (!cv.qbits) {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(half ? cv.V : cv.K) + (size_t)slot * D);
-            for (int v = l16; v < NV; v += 16) {
-                uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                if (p >= 0) w = reinterpret_cast<const uint4*>(srcbase + (size_t)p * D)[v];
-                dst[v] = w;
-            }
-        } else {
-            // quantised row: the half-warp's max magnitude gives the scale
-            float x[VPL][VE];
-            float amax = 0.f;
+    for (long long s0 = wid * SW; s0 < total; s0 += nw * SW) {
+        int p[SW], unit[SW];
 #pragma unroll
-            for (int k = 0; k < VPL; ++k) {
-                const int v = l16 + 16 * k;
-                uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                if (p >= 0 && v < NV) w = reinterpret_cast<const uint4*>(srcbase + (size_t)p * D)[v];
-                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+        for (int k = 0; k < SW; ++k) {
+            const long long slot = s0 + k;
+            unit[k] = (int)(slot / cv.B);
+            p[k] = slot < total ? cv.pos[slot] : -1;
+        }
+        uint4 w[SW][VPL];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if constexpr (sizeof(T) == 2) {
-                        x[k][2 * i] = __uint_as_float(u[i] << 16);
-                        x[k][2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
-                    } else {
-                        x[k][i] = __uint_as_float(u[i]);
-                    }
-                }
+        for (int k = 0; k < SW; ++k) {
+            const T* src = reinterpret_cast<const T*>(half ? pa.V : pa.K) + ((size_t)unit[k] * pa.T + (size_t)max(p[k], 0)) * D;
 #pragma unroll
-                for (int e = 0; e < VE; ++e) amax = fmaxf(amax, fabsf(x[k][e]));
-            }
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-            float* scale_out = reinterpret_cast<float*>(cv.kvs + (size_t)unit * cv.Bp + (slot - (long long)unit * cv.B)) + half;
-            if (cv.qbits == 8) {
-                const float inv = q8_inv(amax);
-                uint8_t* dst = reinterpret_cast<uint8_t*>(half ? cv.V : cv.K) + (size_t)slot * D;
-#pragma unroll
-                for (int k = 0; k < VPL; ++k) {
-                    const int v = l16 + 16 * k;
-                    if (v < NV) {
-                        if constexpr (VE == 8) {
-                            *reinterpret_cast<uint2*>(dst + v * VE) = make_uint2(q8_pack4(&x[k][0], inv), q8_pack4(&x[k][4], inv));
-                        } else {
-                            *reinterpret_cast<uint32_t*>(dst + v * VE) = q8_pack4(&x[k][0], inv);
-                        }
-                    }
-                }
-                if (l16 == 0) *scale_out = q8_scale(amax);
-            } else {
-                // 4-bit row: D / 2 bytes, VE / 2 per 16-byte input vector
-                const float inv = q4_inv(amax);
-                uint8_t* dst = reinterpret_cast<uint8_t*>(half ? cv.V : cv.K) + (size_t)slot * (D / 2);
-#pragma unroll
-                for (int k = 0; k < VPL; ++k) {
-                    const int v = l16 + 16 * k;
-                    if (v < NV) {
-                        if constexpr (VE == 8) *reinterpret_cast<uint32_t*>(dst + v * 4) = q4_pack<4>(&x[k][0], inv);
-                        else *reinterpret_cast<uint16_t*>(dst + v * 2) = (uint16_t)q4_pack<2>(&x[k][0], inv);
-                    }
-                }
-                if (l16 == 0) *scale_out = q4_scale(amax);
+            for (int i = 0; i < VPL; ++i) {
+                const int v = l16 + 16 * i;
+                w[k][i] = make_uint4(0u, 0u, 0u, 0u);
+                if (p[k] >= 0 && v < NV) w[k][i] = reinterpret_cast<const uint4*>(src)[v];
             }
         }
-        if (with_codes && lane == 0) cv.code[slot] = p >= 0 ? pa.ck[(size_t)unit * pa.T + p] : 0u;
+#pragma unroll
+        for (int k = 0; k < SW; ++k) {
+            const long long slot = s0 + k;
+            if (slot >= total) break;
+            if (!cv.qbits) {
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(half ? cv.V : cv.K) + (size_t)slot * D);
+#pragma unroll
+                for (int i = 0; i < VPL; ++i) {
+                    const int v = l16 + 16 * i;
+                    if (v < NV) dst[v] = w[k][i];
+                }
+            } else {
+                // quantised row: the half-warp's max magnitude gives the scale
+                float x[VPL][VE];
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < VPL; ++i) {
+                    const uint32_t u[4] = {w[k][i].x, w[k][i].y, w[k][i].z, w[k][i].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if constexpr (sizeof(T) == 2) {
+                            x[i][2 * e] = __uint_as_float(u[e] << 16);
+                            x[i][2 * e + 1] = __uint_as_float(u[e] & 0xffff0000u);
+                        } else {
+                            x[i][e] = __uint_as_float(u[e]);
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < VE; ++e) amax = fmaxf(amax, fabsf(x[i][e]));
+                }
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+                float* scale_out =
+                    reinterpret_cast<float*>(cv.kvs + (size_t)unit[k] * cv.Bp + (slot - (long long)unit[k] * cv.B)) + half;
+                if (cv.qbits == 8) {
+                    const float inv = q8_inv(amax);
+                    uint8_t* dst = reinterpret_cast<uint8_t*>(half ? cv.V : cv.K) + (size_t)slot * D;
+#pragma unroll
+                    for (int i = 0; i < VPL; ++i) {
+                        const int v = l16 + 16 * i;
+                        if (v < NV) {
+                            if constexpr (VE == 8) {
+                                *reinterpret_cast<uint2*>(dst + v * VE) =
+                                    make_uint2(q8_pack4(&x[i][0], inv), q8_pack4(&x[i][4], inv));
+                            } else {
+                                *reinterpret_cast<uint32_t*>(dst + v * VE) = q8_pack4(&x[i][0], inv);
+                            }
+                        }
+                    }
+                    if (l16 == 0) *scale_out = q8_scale(amax);
+                } else {
+                    // 4-bit row: D / 2 bytes, VE / 2 per 16-byte input vector
+                    const float inv = q4_inv(amax);
+                    uint8_t* dst = reinterpret_cast<uint8_t*>(half ? cv.V : cv.K) + (size_t)slot * (D / 2);
+#pragma unroll
+                    for (int i = 0; i < VPL; ++i) {
+                        const int v = l16 + 16 * i;
+                        if (v < NV) {
+                            if constexpr (VE == 8) *reinterpret_cast<uint32_t*>(dst + v * 4) = q4_pack<4>(&x[i][0], inv);
+                            else *reinterpret_cast<uint16_t*>(dst + v * 2) = (uint16_t)q4_pack<2>(&x[i][0], inv);
+                        }
+                    }
+                    if (l16 == 0) *scale_out = q4_scale(amax);
+                }
+            }
+            if (with_codes && lane == 0) cv.code[slot] = p[k] >= 0 ? pa.ck[(size_t)unit[k] * pa.T + p[k]] : 0u;
+        }
     }
 }
 
@@ -1023,7 +1047,7 @@ cudaError_t stats_t(const CacheView& c, const PromptArgs& p, cudaStream_t st)
 template <typename T, int D>
 cudaError_t gather_t(const CacheView& c, const PromptArgs& p, bool with_codes, cudaStream_t st)
 {
-    const long long warps = (long long)c.U * c.B;
+    const long long warps = ((long long)c.U * c.B + kGatherSlots - 1) / kGatherSlots;
     long long blocks = (warps + 7) / 8;
     if (blocks > 65535LL * 8) blocks = 65535LL * 8;
     gather_kernel<T, D><<<(unsigned)blocks, 256, 0, st>>>(c, p, with_codes ? 1 : 0);

@@ -484,10 +484,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                         for (int e = 0; e < 32; ++e)
                             if (j0 + e > i) v[e] = -INFINITY;
                     }
-                    // the chunk's max two columns per instruction (three-input max)
-                    float cm = fmaxf(v[0], v[1]);
+                    // the chunk's max as a tree of three-input max
+                    // instructions: 17 of them, four deep (a chain of 16
+                    // would put all of them on the critical path)
+                    float t1[11];
 #pragma unroll
-                    for (int e = 2; e < 32; e += 2) cm = max3f(cm, v[e], v[e + 1]);
+                    for (int k = 0; k < 10; ++k) t1[k] = max3f(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+                    t1[10] = fmaxf(v[30], v[31]);
+                    const float t20 = max3f(t1[0], t1[1], t1[2]), t21 = max3f(t1[3], t1[4], t1[5]);
+                    const float t22 = max3f(t1[6], t1[7], t1[8]), t23 = fmaxf(t1[9], t1[10]);
+                    const float cm = fmaxf(max3f(t20, t21, t22), t23);
                     {
                         // branch-free rescale: alpha is exactly 1 when the max
                         // stays, 0 before the first finite column; a chunk of

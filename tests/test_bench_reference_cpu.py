@@ -51,3 +51,19 @@ def test_bench_byte_model_for_quantised_rows():
     # per slot: two rows of 256, 128 or 64 bytes, the scale pair for codes
     assert (full - b8) == U * (B * (2 * 128 - 8) + (2 * 128 - 8))
     assert (b8 - b4) == U * (B * 2 * 64 + 2 * 64)
+
+
+def test_bench_prompt_phase_byte_model():
+    """The prompt phase's HBM bytes, worked by hand for one unit of four
+    tokens, d = 2, budget 2: Q and K (16 + 16 B) read by both passes = 64;
+    row max and normaliser written and read = 64; column sums written and
+    read = 64; two kept rows of K and V read (16) and two slots written,
+    rows of 4 B twice plus position and score pair (2 x 20) = 56."""
+    import bench
+    assert bench.prefill_bytes(1, 1, 4, 2, 2) == 64 + 64 + 64 + 56
+    # grouped queries: two query heads read Q twice as large, keep per-head
+    # statistics and column sums, and sum the heads' columns per unit
+    assert bench.prefill_bytes(1, 2, 4, 2, 2) == 2 * (32 + 16) + 128 + 128 + 64 + 56
+    # budget 8 over four tokens: all four prompt rows read (two more, 16 B),
+    # and all eight slots written (six more, 6 x 20 B)
+    assert bench.prefill_bytes(1, 1, 4, 2, 8) - bench.prefill_bytes(1, 1, 4, 2, 2) == 16 + 6 * 20
