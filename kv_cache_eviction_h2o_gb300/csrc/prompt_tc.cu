@@ -11,12 +11,14 @@
 // thread owns one key and sums its 128 query columns in registers; no
 // cross-thread reduction is needed for the column sums.
 //
-// Per CTA (192 threads): warp 0 issues TMA loads (128-byte swizzled boxes
-// of 128 rows x 64 columns) into a ring of stages; lane 0 of warp 1 issues
-// tcgen05.mma (M = N = 128, K = 16 per instruction, fp32 accumulate) into
-// one of two TMEM accumulators and commits to mbarriers; warps 2..5 drain
-// the accumulators with tcgen05.ld (thread = TMEM lane = tile row).  The
-// MMA of tile t+1 overlaps the exponentials of tile t.  Every wait is
+// Per CTA (320 threads, two CTAs per SM): warp 0 issues TMA loads (128-byte
+// swizzled boxes of 128 rows x 64 columns) into a ring of stages; lane 0 of
+// warp 1 issues tcgen05.mma (M = N = 128, K = 16 per instruction, fp32
+// accumulate) into one of two TMEM accumulators and commits to mbarriers;
+// warps 2..5 drain accumulator 0 and warps 6..9 accumulator 1 with
+// tcgen05.ld (thread = TMEM lane = tile row), so the exponentials of two
+// tiles run at once and each scheduler has four epilogue warps to switch
+// between.  Every wait is
 // bounded: a wait that runs out sets the handle's error word (when there is
 // one) and the CTA abandons its loop, writes NaN into the statistics it owns
 // (so pass 2 and every reader of the column sums see the failure), waits
@@ -36,11 +38,11 @@ namespace {
 
 constexpr int kT = 128;                          // tile rows / columns
 constexpr int kD = 128;                          // head dim handled here
-constexpr int kStages = 2;                       // B-operand ring depth
 constexpr uint32_t kBox = kT * 64 * 2;           // one 128 x 64 bf16 box: 16 KB
 constexpr uint32_t kTile = 2 * kBox;             // 128 x 128 bf16: 32 KB
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 2 * kT;           // two fp32 accumulators
+constexpr int kThreads = 192;                   // one epilogue group (persistence-of-importance flags)
+constexpr int kThreadsW = 320;                  // two epilogue groups (the score passes)
+constexpr int kScoreCtasPerSM = 2;
 constexpr int kPersistBlocks = 32;               // prompts of up to 32 blocks run on a persistent grid
 
 // instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits
@@ -117,6 +119,24 @@ __device__ __forceinline__ void tc_ld32_wait(uint32_t (&r)[32])
     asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]) :: "memory");
 }
 
+// The same for 16 columns.
+__device__ __forceinline__ void tc_ld16_issue(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tc_ld16_wait(uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]) :: "memory");
+}
+__device__ __forceinline__ void tc_ld_issue(uint32_t taddr, uint32_t (&r)[32]) { tc_ld32_issue(taddr, r); }
+__device__ __forceinline__ void tc_ld_issue(uint32_t taddr, uint32_t (&r)[16]) { tc_ld16_issue(taddr, r); }
+__device__ __forceinline__ void tc_ld_wait(uint32_t (&r)[32]) { tc_ld32_wait(r); }
+__device__ __forceinline__ void tc_ld_wait(uint32_t (&r)[16]) { tc_ld16_wait(r); }
+
 // max(a, b, c) in one instruction
 __device__ __forceinline__ float max3f(float a, float b, float c)
 {
@@ -157,30 +177,56 @@ __device__ __forceinline__ void tile_mma(uint32_t d_tmem, const uint8_t* a, cons
     }
 }
 
-struct alignas(1024) TcSmem {
-    uint8_t a[kTile];                 // the tile's own block (Q in pass 1, K in pass 2)
-    uint8_t b[kStages][kTile];        // ring of the swept blocks
-    alignas(16) float colstat[2][kT];      // pass 2: per accumulator, the 128 queries' -(m2 + log2(l)) (read as float4)
-    uint64_t a_full;
-    uint64_t a_empty;                 // persistent passes: the MMAs have read the A tile
-    uint64_t b_full[kStages];
-    uint64_t b_empty[kStages];
-    uint64_t acc_full[2];
-    uint64_t acc_empty[2];
+// Shared memory of a scorer CTA: NA buffers of the A tile (the item's own
+// block), a ring of NS B stages (the swept blocks), NACC fp32 accumulators
+// of 128 TMEM columns, NGRP epilogue groups of four warps (group e drains
+// accumulator e).
+template <int NA, int NS, int NACC, int NGRP>
+struct alignas(1024) TcSmemT {
+    static constexpr int kA = NA, kS = NS, kAcc = NACC, kGrp = NGRP;
+    static constexpr uint32_t kCols = (uint32_t)NACC * kT;   // TMEM columns (a power of 2)
+    uint8_t a[NA][kTile];             // the item's own block (Q in pass 1, K in pass 2)
+    uint8_t b[NS][kTile];             // ring of the swept blocks
+    alignas(16) float colstat[NGRP][2][kT];   // pass 2: per group, two buffers of the 128 queries' -(m2 + log2(l)) (read as float4)
+    double xch[2][NGRP > 1 ? NGRP - 1 : 1][3][kT];   // groups 1.. hand their per-item results to group 0, two items deep
+    uint64_t a_full[NA];
+    uint64_t a_empty[NA];             // the MMAs have read the A buffer
+    uint64_t b_full[NS];
+    uint64_t b_empty[NS];
+    uint64_t acc_full[NACC];
+    uint64_t acc_empty[NACC];
     uint32_t tmem_base;
     int abort;
 };
+// persistence-of-importance flags: one item per CTA, two CTAs per SM
+using TcSmem = TcSmemT<1, 2, 2, 1>;
+// the score passes: two CTAs per SM, each with two accumulators drained by
+// two epilogue groups.  (One CTA per SM holding all of TMEM, with four
+// groups, a double-buffered A tile and four B stages, measured 20-30 %
+// slower: its groups meet at every item's merge and share one in-order
+// MMA issuer.)
+using TcSmemW = TcSmemT<1, 2, 2, 2>;
+static_assert(TcSmemW::kAcc == TcSmemW::kGrp, "group e drains accumulator e");
+static_assert(TcSmemW::kGrp * 128 + 64 == kThreadsW, "a producer warp, an MMA warp and the epilogue groups");
 static_assert(offsetof(TcSmem, colstat) % 16 == 0, "colstat is read as float4");
 static_assert(offsetof(TcSmem, b) % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+static_assert(offsetof(TcSmemW, colstat) % 16 == 0, "colstat is read as float4");
+static_assert(offsetof(TcSmemW, b) % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+// the dynamic size (the struct and its alignment slack) and the SM's 1 KB
+// per CTA, for the CTAs that share an SM, within its 228 KB
+static_assert(kScoreCtasPerSM * (sizeof(TcSmemW) + 1024 + 1024) <= 228 * 1024, "the score-pass CTAs must fit one SM");
+static_assert(2 * (sizeof(TcSmem) + 1024 + 1024) <= 228 * 1024, "two flag CTAs must fit one SM");
 
-__device__ __forceinline__ TcSmem& tc_smem(unsigned char* raw)
+template <class SM>
+__device__ __forceinline__ SM& tc_smem(unsigned char* raw)
 {
     const uintptr_t p = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~(uintptr_t)1023;
-    return *reinterpret_cast<TcSmem*>(p);
+    return *reinterpret_cast<SM*>(p);
 }
 
 // bounded wait that also watches the CTA's abort flag
-__device__ __forceinline__ bool tc_wait(TcSmem& S, uint64_t* bar, uint32_t parity, int* err)
+template <class SM>
+__device__ __forceinline__ bool tc_wait(SM& S, uint64_t* bar, uint32_t parity, int* err)
 {
     if (mbar_wait(bar, parity)) return true;
     if (err) atomicOr(err, kErrWaitTimeout);
@@ -188,40 +234,54 @@ __device__ __forceinline__ bool tc_wait(TcSmem& S, uint64_t* bar, uint32_t parit
     return false;
 }
 
-__device__ __forceinline__ bool aborted(TcSmem& S) { return *(volatile int*)&S.abort != 0; }
+template <class SM>
+__device__ __forceinline__ bool aborted(SM& S) { return *(volatile int*)&S.abort != 0; }
 
-// OR of `pred` over the 128 epilogue threads (named barrier 1); also orders
-// their earlier shared-memory writes before the later reads
+// OR of `pred` over the 128 threads of one epilogue group (named barrier
+// `id`: 1 + the group); also orders their earlier shared-memory writes
+// before the later reads
+template <int ID = 1>
 __device__ __forceinline__ bool epilogue_any(bool pred)
 {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "barrier.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        "barrier.red.or.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)pred)
+        : "r"((uint32_t)pred), "n"(ID)
         : "memory");
     return r != 0;
 }
 
-__device__ __forceinline__ void tc_setup(TcSmem& S, int warp)
+// All epilogue groups (named barrier 5): groups 1.. have put their per-item
+// results in `xch` for group 0
+template <int NG>
+__device__ __forceinline__ void groups_sync()
+{
+    asm volatile("bar.sync 5, %0;" ::"n"(NG * 128) : "memory");
+}
+
+template <class SM>
+__device__ __forceinline__ void tc_setup(SM& S, int warp)
 {
     if (threadIdx.x == 0) {
-        mbar_init(&S.a_full, 1);
-        mbar_init(&S.a_empty, 1);
-        for (int s = 0; s < kStages; ++s) {
+        for (int k = 0; k < SM::kA; ++k) {
+            mbar_init(&S.a_full[k], 1);
+            mbar_init(&S.a_empty[k], 1);
+        }
+        for (int s = 0; s < SM::kS; ++s) {
             mbar_init(&S.b_full[s], 1);
             mbar_init(&S.b_empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < SM::kAcc; ++b) {
             mbar_init(&S.acc_full[b], 1);
-            mbar_init(&S.acc_empty[b], 4);        // one arrival per epilogue warp
+            mbar_init(&S.acc_empty[b], 4);        // one arrival per warp of the group draining it
         }
         S.abort = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(&S.tmem_base, kTmemCols);
+        tmem_alloc(&S.tmem_base, SM::kCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -229,32 +289,35 @@ __device__ __forceinline__ void tc_setup(TcSmem& S, int warp)
     tc_fence_after();
 }
 
+// End of a one-item CTA (the flags kernel).
 __device__ __forceinline__ void tc_teardown(TcSmem& S, int warp, int n_b_loads)
 {
+    constexpr int NS = TcSmem::kS;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (aborted(S) && threadIdx.x == 0) {
         // copies may still be in flight: wait (bounded) for every stage's
         // last load before the CTA's shared memory is released
-        for (int t = (n_b_loads > kStages ? n_b_loads - kStages : 0); t < n_b_loads; ++t)
-            mbar_wait(&S.b_full[t % kStages], (uint32_t)(t / kStages) & 1u);
-        mbar_wait(&S.a_full, 0);
+        for (int t = (n_b_loads > NS ? n_b_loads - NS : 0); t < n_b_loads; ++t)
+            mbar_wait(&S.b_full[t % NS], (uint32_t)(t / NS) & 1u);
+        mbar_wait(&S.a_full[0], 0);
     }
-    if (warp == 1) tmem_dealloc(S.tmem_base, kTmemCols);
+    if (warp == 1) tmem_dealloc(S.tmem_base, TcSmem::kCols);
 }
 
-// Producer: the CTA's own block once, then the swept blocks `first..last`
-// (inclusive) through the ring.  In pass 2 it also stages nothing else.
+// Producer of a one-item CTA: its own block once, then the swept blocks
+// `first..last` (inclusive) through the ring.
 __device__ __forceinline__ void tc_producer(TcSmem& S, const CUtensorMap* map_a, const CUtensorMap* map_b,
                                             int row_a, int row0_b, int first, int last, int* err)
 {
-    mbar_arrive_expect_tx(&S.a_full, kTile);
-    tma_load_2d(S.a, map_a, 0, row_a, &S.a_full);
-    tma_load_2d(S.a + kBox, map_a, 64, row_a, &S.a_full);
+    constexpr int NS = TcSmem::kS;
+    mbar_arrive_expect_tx(&S.a_full[0], kTile);
+    tma_load_2d(S.a[0], map_a, 0, row_a, &S.a_full[0]);
+    tma_load_2d(S.a[0] + kBox, map_a, 64, row_a, &S.a_full[0]);
     for (int t = 0; first + t <= last; ++t) {
-        const int s = t % kStages;
-        if (t >= kStages && !tc_wait(S, &S.b_empty[s], ((uint32_t)(t / kStages) & 1u) ^ 1u, err)) return;
+        const int s = t % NS;
+        if (t >= NS && !tc_wait(S, &S.b_empty[s], ((uint32_t)(t / NS) & 1u) ^ 1u, err)) return;
         if (aborted(S)) return;
         mbar_arrive_expect_tx(&S.b_full[s], kTile);
         tma_load_2d(S.b[s], map_b, 0, row0_b + (first + t) * kT, &S.b_full[s]);
@@ -262,17 +325,19 @@ __device__ __forceinline__ void tc_producer(TcSmem& S, const CUtensorMap* map_a,
     }
 }
 
-// MMA issuer (one thread): tile t of the sweep into accumulator t & 1.
+// MMA issuer of a one-item CTA (one thread): tile t of the sweep into
+// accumulator t & 1.
 __device__ __forceinline__ void tc_mma_loop(TcSmem& S, uint32_t tbase, int ntiles, int* err)
 {
-    if (!tc_wait(S, &S.a_full, 0, err)) return;
+    constexpr int NS = TcSmem::kS;
+    if (!tc_wait(S, &S.a_full[0], 0, err)) return;
     for (int t = 0; t < ntiles; ++t) {
-        const int s = t % kStages, b = t & 1;
-        if (!tc_wait(S, &S.b_full[s], (uint32_t)(t / kStages) & 1u, err)) return;
+        const int s = t % NS, b = t & 1;
+        if (!tc_wait(S, &S.b_full[s], (uint32_t)(t / NS) & 1u, err)) return;
         if (t >= 2 && !tc_wait(S, &S.acc_empty[b], ((uint32_t)(t >> 1) & 1u) ^ 1u, err)) return;
         if (aborted(S)) return;
         tc_fence_after();
-        tile_mma(tbase + (uint32_t)b * kT, S.a, S.b[s]);
+        tile_mma(tbase + (uint32_t)b * kT, S.a[0], S.b[s]);
         tc_commit(&S.b_empty[s]);       // the stage is free once these MMAs have read it
         tc_commit(&S.acc_full[b]);      // and the accumulator is ready for the epilogue
     }
@@ -280,14 +345,15 @@ __device__ __forceinline__ void tc_mma_loop(TcSmem& S, uint32_t tbase, int ntile
 
 // ------------------------------------------------ persistent item loops
 //
-// The scorer passes run on a persistent grid: CTA c takes one work item per
+// The score passes run on a persistent grid: CTA c takes one work item per
 // round of P = gridDim.x items (walk_item), an item being one (unit, block)
-// of group_order below; with P = the item count every CTA takes one item.  TMEM, the barriers and the ring stay live across
-// items, and every role counts ring stages, accumulators and A tiles over
-// the whole walk, so the next item's tiles are loaded and multiplied while
-// the epilogue still drains this item's accumulators.  The A tile (the
-// item's own block) has one buffer: the MMA issuer commits `a_empty` after
-// an item's last MMA and the producer waits for it before loading the next.
+// of group_order below; with P = the item count every CTA takes one item.
+// TMEM, the barriers and the ring stay live across items, and every role
+// counts ring stages, accumulators and A tiles over the whole walk, so the
+// next item's tiles are loaded and multiplied while the epilogue still
+// drains this item's accumulators.  Item k's A tile goes to buffer k % NA;
+// the MMA issuer commits that buffer's `a_empty` after the item's last MMA
+// and the producer waits for it before loading item k + NA there.
 
 struct ItemWalk {
     int n_b;                          // B tiles the producer issued
@@ -307,25 +373,28 @@ __device__ __forceinline__ int walk_item(int i, int nitems)
 
 // Producer over the items: `item(x, row_a, row0_b, first, last)` gives the
 // A row, the first B row and the swept block range of item x.
-template <class ItemFn>
-__device__ __forceinline__ ItemWalk tc_producer_items(TcSmem& S, const CUtensorMap* map_a, const CUtensorMap* map_b,
+template <class SM, class ItemFn>
+__device__ __forceinline__ ItemWalk tc_producer_items(SM& S, const CUtensorMap* map_a, const CUtensorMap* map_b,
                                                       int nitems, ItemFn item, int* err)
 {
+    constexpr int NA = SM::kA, NS = SM::kS;
     ItemWalk w{0, 0};
     for (int i = 0; i * (int)gridDim.x < nitems; ++i) {
         const int x = walk_item(i, nitems);
         if (x >= nitems) continue;
         int row_a, row0_b, first, last;
         item(x, row_a, row0_b, first, last);
-        if (w.n_a > 0 && !tc_wait(S, &S.a_empty, (uint32_t)((w.n_a - 1) & 1), err)) return w;
+        const int ka = w.n_a % NA;
+        // the buffer's previous item (w.n_a - NA) has been multiplied
+        if (w.n_a >= NA && !tc_wait(S, &S.a_empty[ka], (uint32_t)((w.n_a / NA - 1) & 1), err)) return w;
         if (aborted(S)) return w;
-        mbar_arrive_expect_tx(&S.a_full, kTile);
-        tma_load_2d(S.a, map_a, 0, row_a, &S.a_full);
-        tma_load_2d(S.a + kBox, map_a, 64, row_a, &S.a_full);
+        mbar_arrive_expect_tx(&S.a_full[ka], kTile);
+        tma_load_2d(S.a[ka], map_a, 0, row_a, &S.a_full[ka]);
+        tma_load_2d(S.a[ka] + kBox, map_a, 64, row_a, &S.a_full[ka]);
         ++w.n_a;
         for (int bk = first; bk <= last; ++bk) {
-            const int s = w.n_b % kStages;
-            if (w.n_b >= kStages && !tc_wait(S, &S.b_empty[s], ((uint32_t)(w.n_b / kStages) & 1u) ^ 1u, err))
+            const int s = w.n_b % NS;
+            if (w.n_b >= NS && !tc_wait(S, &S.b_empty[s], ((uint32_t)(w.n_b / NS) & 1u) ^ 1u, err))
                 return w;
             if (aborted(S)) return w;
             mbar_arrive_expect_tx(&S.b_full[s], kTile);
@@ -338,47 +407,52 @@ __device__ __forceinline__ ItemWalk tc_producer_items(TcSmem& S, const CUtensorM
 }
 
 // MMA issuer over the items: `tiles(x)` is item x's tile count.  Tile g of
-// the walk goes to accumulator g & 1.
-template <class TilesFn>
-__device__ __forceinline__ void tc_mma_items(TcSmem& S, uint32_t tbase, int nitems, TilesFn tiles, int* err)
+// the walk goes to accumulator g % NACC.
+template <class SM, class TilesFn>
+__device__ __forceinline__ void tc_mma_items(SM& S, uint32_t tbase, int nitems, TilesFn tiles, int* err)
 {
+    constexpr int NA = SM::kA, NS = SM::kS, NACC = SM::kAcc;
     int g = 0, ia = 0;
     for (int i = 0; i * (int)gridDim.x < nitems; ++i) {
         const int x = walk_item(i, nitems);
         if (x >= nitems) continue;
         const int ntiles = tiles(x);
-        if (!tc_wait(S, &S.a_full, (uint32_t)(ia & 1), err)) return;
+        const int ka = ia % NA;
+        if (!tc_wait(S, &S.a_full[ka], (uint32_t)((ia / NA) & 1), err)) return;
         for (int t = 0; t < ntiles; ++t, ++g) {
-            const int s = g % kStages, b = g & 1;
-            if (!tc_wait(S, &S.b_full[s], (uint32_t)(g / kStages) & 1u, err)) return;
-            if (g >= 2 && !tc_wait(S, &S.acc_empty[b], ((uint32_t)(g >> 1) & 1u) ^ 1u, err)) return;
+            const int s = g % NS, b = g % NACC;
+            if (!tc_wait(S, &S.b_full[s], (uint32_t)(g / NS) & 1u, err)) return;
+            if (g >= NACC && !tc_wait(S, &S.acc_empty[b], ((uint32_t)(g / NACC) & 1u) ^ 1u, err)) return;
             if (aborted(S)) return;
             tc_fence_after();
-            tile_mma(tbase + (uint32_t)b * kT, S.a, S.b[s]);
+            tile_mma(tbase + (uint32_t)b * kT, S.a[ka], S.b[s]);
             tc_commit(&S.b_empty[s]);     // the stage is free once these MMAs have read it
             tc_commit(&S.acc_full[b]);    // and the accumulator is ready for the epilogue
         }
-        tc_commit(&S.a_empty);            // this item's A tile has been read
+        tc_commit(&S.a_empty[ka]);        // this item's A tile has been read
         ++ia;
     }
-    // the last release lands before the CTA can leave
-    if (ia > 0) tc_wait(S, &S.a_empty, (uint32_t)((ia - 1) & 1), err);
+    // the last releases land before the CTA can leave
+    for (int k = (ia > NA ? ia - NA : 0); k < ia; ++k) tc_wait(S, &S.a_empty[k % NA], (uint32_t)((k / NA) & 1), err);
 }
 
 // End of a walk: every role is past its loop.  An aborted CTA waits
 // (bounded) for the copies it may still have in flight -- the last stages of
-// the ring and the last A tile -- before its shared memory is released.
-__device__ __forceinline__ void tc_teardown_items(TcSmem& S, int warp, const ItemWalk& w)
+// the ring and the last A tiles -- before its shared memory is released.
+template <class SM>
+__device__ __forceinline__ void tc_teardown_items(SM& S, int warp, const ItemWalk& w)
 {
+    constexpr int NA = SM::kA, NS = SM::kS;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (aborted(S) && threadIdx.x == 0) {
-        for (int t = (w.n_b > kStages ? w.n_b - kStages : 0); t < w.n_b; ++t)
-            mbar_wait(&S.b_full[t % kStages], (uint32_t)(t / kStages) & 1u);
-        if (w.n_a > 0) mbar_wait(&S.a_full, (uint32_t)((w.n_a - 1) & 1));
+        for (int t = (w.n_b > NS ? w.n_b - NS : 0); t < w.n_b; ++t)
+            mbar_wait(&S.b_full[t % NS], (uint32_t)(t / NS) & 1u);
+        for (int k = (w.n_a > NA ? w.n_a - NA : 0); k < w.n_a; ++k)
+            mbar_wait(&S.a_full[k % NA], (uint32_t)((k / NA) & 1));
     }
-    if (warp == 1) tmem_dealloc(S.tmem_base, kTmemCols);
+    if (warp == 1) tmem_dealloc(S.tmem_base, SM::kCols);
 }
 
 // ------------------------------------------------------- CTA schedule
@@ -404,13 +478,14 @@ __device__ __forceinline__ void group_order(int x, int U, int nb, int g, int& u,
 // Items x < nitems (U * nb, or U * nq for the last nq blocks with g = U):
 // item x is row block ib = nb - 1 - k of unit u (group_order); it sweeps key
 // blocks 0..ib.  Persistent grid (see the item loops above).
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreadsW, kScoreCtasPerSM)
     rowstats_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK, int U,
                        int G, int T, int nb, int g, int nitems, float c2, float* __restrict__ m2,
                        float* __restrict__ lout, int* err)
 {
     extern __shared__ unsigned char smem_raw[];
-    TcSmem& S = tc_smem(smem_raw);
+    TcSmemW& S = tc_smem<TcSmemW>(smem_raw);
+    constexpr int NG = TcSmemW::kGrp;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto unit_block = [&](int x, int& u, int& ib) {
         int k;
@@ -444,20 +519,30 @@ __global__ void __launch_bounds__(kThreads, 2)
                          err);
         __syncwarp();
     } else {
+        // Four epilogue groups of four warps: group e drains accumulator e,
+        // that is tiles g of the walk with g % 4 == e, so four tiles are in
+        // the exponentials at once and each scheduler holds four epilogue
+        // warps.  Each group keeps the running statistics of its own tiles;
+        // at the end of an item groups 1..3 hand their (m, l) to group 0,
+        // which merges and writes.
         const int q = warp & 3;                   // TMEM lane quarter of this warp
-        int gt = 0;                               // tiles of the walk so far
+        const int grp = (warp - 2) >> 2;
+        const int kk = 32 * q + lane;             // row of the block (TMEM lane)
+        int gt = 0;                               // tiles of the walk so far (both groups)
+        int ia = 0;                               // items so far
         bool dead = false;                        // a wait ran out: the rest is NaN
+        const float qnan = __int_as_float(0x7fffffff);
         for (int r = 0; r * (int)gridDim.x < nitems; ++r) {
             const int x = walk_item(r, nitems);
             if (x >= nitems) continue;
             int u, ib;
             unit_block(x, u, ib);
-            const int i = ib * kT + 32 * q + lane;    // query row within the unit
+            const int i = ib * kT + kk;               // query row within the unit
             const int ntiles = ib + 1;
             float m = -INFINITY, l = 0.f, lc = 0.f;   // running base-2 max, Kahan-summed normaliser
-            for (int t = 0; t < ntiles && !dead; ++t, ++gt) {
-                const int b = gt & 1;
-                const bool ok = tc_wait(S, &S.acc_full[b], (uint32_t)(gt >> 1) & 1u, err);
+            for (int t = (grp - (gt & (NG - 1))) & (NG - 1); t < ntiles && !dead; t += NG) {
+                const int gg = gt + t;                // this tile of the walk: accumulator grp
+                const bool ok = tc_wait(S, &S.acc_full[grp], (uint32_t)(gg / NG) & 1u, err);
                 if (__any_sync(0xffffffffu, !ok || aborted(S))) {
                     dead = true;
                     break;
@@ -466,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const bool diag = (t == ib);
                 // the four 32-column chunks, each load issued while the
                 // previous chunk is processed
-                const uint32_t tcol = tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * kT);
+                const uint32_t tcol = tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(grp * kT);
                 uint32_t ra[32], rb[32];
                 tc_ld32_issue(tcol, ra);
                 tc_ld32_wait(ra);
@@ -523,13 +608,41 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&S.acc_empty[b]);
+                if (lane == 0) mbar_arrive(&S.acc_empty[grp]);
             }
-            if (i < T) {
+            gt += ntiles;
+            // merge the groups' statistics of the block's rows:
+            // m = max_e m_e, l = sum_e l_e 2^(m_e - m)
+            if (grp > 0) {
+                float* xm = reinterpret_cast<float*>(S.xch[ia & 1][grp - 1][0]);
+                xm[kk] = dead ? qnan : m;
+                xm[kT + kk] = dead ? qnan : l - lc;
+            }
+            groups_sync<NG>();
+            if (grp == 0 && i < T) {
+                float me[NG], le[NG];
+                me[0] = m;
+                le[0] = dead ? qnan : l - lc;
+#pragma unroll
+                for (int e = 1; e < NG; ++e) {
+                    const float* xm = reinterpret_cast<const float*>(S.xch[ia & 1][e - 1][0]);
+                    me[e] = xm[kk];
+                    le[e] = xm[kT + kk];
+                }
+                float mo = -INFINITY, lo = 0.f;
+                bool bad = false;
+#pragma unroll
+                for (int e = 0; e < NG; ++e) {
+                    bad |= isnan(le[e]);
+                    mo = fmaxf(mo, me[e]);
+                }
+#pragma unroll
+                for (int e = 0; e < NG; ++e) lo += (me[e] == -INFINITY) ? 0.f : le[e] * exp2f(me[e] - mo);
                 // an abandoned walk leaves NaN, which the column sums carry on
-                m2[(size_t)u * T + i] = dead ? __int_as_float(0x7fffffff) : m;
-                lout[(size_t)u * T + i] = dead ? __int_as_float(0x7fffffff) : l - lc;
+                m2[(size_t)u * T + i] = bad ? qnan : mo;
+                lout[(size_t)u * T + i] = bad ? qnan : lo;
             }
+            ++ia;
         }
     }
     tc_teardown_items(S, warp, w);
@@ -543,14 +656,15 @@ __global__ void __launch_bounds__(kThreads, 2)
 // BAND: also the band sums of the per-head policy profile (a separate
 // instantiation, so the plain pass carries none of their instructions).
 template <bool BAND>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreadsW, kScoreCtasPerSM)
     colsum_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK, int U,
                      int G, int T, int nb, int g, int nitems, float c2, const float* __restrict__ m2,
                      const float* __restrict__ lin, double* __restrict__ cout, double* __restrict__ bandB,
                      double* __restrict__ bandr, int wB, int wr, int* err)
 {
     extern __shared__ unsigned char smem_raw[];
-    TcSmem& S = tc_smem(smem_raw);
+    TcSmemW& S = tc_smem<TcSmemW>(smem_raw);
+    constexpr int NG = TcSmemW::kGrp;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     tc_setup(S, warp);
     const uint32_t tbase = S.tmem_base;
@@ -579,90 +693,112 @@ __global__ void __launch_bounds__(kThreads, 2)
                          err);
         __syncwarp();
     } else {
-        const int et = threadIdx.x - 64;          // epilogue thread 0..127
+        // Four epilogue groups as in pass 1: group e drains the tiles g of
+        // the walk with g % 4 == e; each keeps its own sums of the block's
+        // keys, and groups 1..3 hand theirs to group 0 at the end of an item.
         const int q = warp & 3;
+        const int grp = (warp - 2) >> 2;
+        const int kk = 32 * q + lane;             // key of the block (TMEM lane); also the query this thread stages
         const int wmax = max(wB, wr);
         const double nan = __longlong_as_double(0x7ff8000000000000LL);
-        int gt = 0;                               // tiles of the walk so far
+        const int P = (int)gridDim.x;
+        int gt = 0;                               // tiles of the walk so far (both groups)
+        int ia = 0;                               // items so far
         bool dead = false;                        // a wait ran out: the rest is NaN
-        // the next item of the walk after round r (nitems if none)
-        auto next_item = [&](int r) {
-            for (int r2 = r + 1; r2 * (int)gridDim.x < nitems; ++r2) {
-                const int x2 = walk_item(r2, nitems);
-                if (x2 < nitems) return x2;
+        // unit and query block of tile `target` of the walk, searching from
+        // round r, whose item starts at tile g0; false past the walk's end
+        auto locate = [&](int r, int g0, int target, int& uo, int& ibo) {
+            for (; r * P < nitems; ++r) {
+                const int x = walk_item(r, nitems);
+                if (x >= nitems) continue;
+                int u, jb;
+                group_order(x, U, nb, g, u, jb);
+                const int nt = nb - jb;
+                if (target < g0 + nt) {
+                    uo = u;
+                    ibo = jb + (target - g0);
+                    return true;
+                }
+                g0 += nt;
             }
-            return nitems;
+            return false;
         };
-        // stage the query statistics of a tile as one negated bias per
-        // query, -(m2 + log2(l)), so a weight is 2^(s c2 + nbias); -inf past
-        // T (weight 0)
-        auto nbias = [&](int uq, int iq) { return iq < T ? -(m2[(size_t)uq * T + iq] + log2f(lin[(size_t)uq * T + iq])) : -INFINITY; };
-        bool staged = false;                      // the item's first tile already staged by the previous item
-        for (int r = 0; r * (int)gridDim.x < nitems; ++r) {
+        // the query statistics of a tile as one negated bias per query,
+        // -(m2 + log2(l)), so a weight is 2^(s c2 + nbias); -inf past T
+        // (weight 0)
+        auto nbias = [&](float m, float l, int iq) { return iq < T ? -(m + log2f(l)) : -INFINITY; };
+        {
+            // the group's first tile: walk tile grp
+            int u0, ib0;
+            if (locate(0, 0, grp, u0, ib0)) {
+                const int iq = ib0 * kT + kk;
+                S.colstat[grp][0][kk] =
+                    iq < T ? nbias(m2[(size_t)u0 * T + iq], lin[(size_t)u0 * T + iq], iq) : -INFINITY;
+            }
+        }
+        for (int r = 0; r * P < nitems; ++r) {
             const int x = walk_item(r, nitems);
             if (x >= nitems) continue;
             int u, jb;
             group_order(x, U, nb, g, u, jb);
             const int ntiles = nb - jb;
-            const int j = jb * kT + 32 * q + lane;    // key within the unit
-            const float* m2u = m2 + (size_t)u * T;
-            const float* lu = lin + (size_t)u * T;
-            // the next item's first tile, staged during this item's last one
-            const int xn = next_item(r);
-            int un = 0, jbn = 0;
-            if (xn < nitems) group_order(xn, U, nb, g, un, jbn);
-            // (the buffer was last read two tiles ago, before the barrier
-            // that opened the last one)
-            if (!dead && !staged) S.colstat[gt & 1][et] = nbias(u, jb * kT + et);
+            const int j = jb * kT + kk;               // key within the unit
             float cs = 0.f, cc = 0.f;                 // Kahan-summed column sum
             double bsB = 0.0, bsr = 0.0;              // band sums (rows j .. j+w-1)
-            for (int t = 0; t < ntiles && !dead; ++t, ++gt) {
-                const int b = gt & 1;
+            for (int t = (grp - (gt & (NG - 1))) & (NG - 1); t < ntiles && !dead; t += NG) {
+                const int gg = gt + t;                // this tile of the walk: accumulator grp
                 const int ib = jb + t;
                 // some key of the block has rows of this tile in its band
                 const bool band = BAND && ib * kT < (jb + 1) * kT + wmax;
-                // the next tile's statistics (this item's, or the next item's
-                // first), stored after this tile
-                float nm = 0.f, nl = 0.f;
-                const bool last = t + 1 == ntiles;
-                const int inext = last ? jbn * kT + et : (ib + 1) * kT + et;
-                const float* m2n = last ? m2 + (size_t)un * T : m2u;
-                const float* ln = last ? lin + (size_t)un * T : lu;
-                const bool more = !last || xn < nitems;
+                // the group's next tile (gg + NG): its statistics are loaded
+                // now and staged after this tile
+                int un = u, ibn = ib + NG;
+                const bool more = t + NG < ntiles || locate(r, gt, gg + NG, un, ibn);
+                const int inext = ibn * kT + kk;
+                float nm = 0.f, nl = 1.f;
                 if (more && inext < T) {
-                    nm = m2n[inext];
-                    nl = ln[inext];
+                    nm = m2[(size_t)un * T + inext];
+                    nl = lin[(size_t)un * T + inext];
                 }
-                const bool ok = tc_wait(S, &S.acc_full[b], (uint32_t)(gt >> 1) & 1u, err);
-                // agreed by all epilogue threads; also publishes the statistics staged before
-                if (epilogue_any(!ok || aborted(S))) {
+                const bool ok = tc_wait(S, &S.acc_full[grp], (uint32_t)(gg / NG) & 1u, err);
+                // agreed by the group's threads; also publishes the statistics staged before
+                const bool stop = !ok || aborted(S);
+                const bool any = grp == 0 ? epilogue_any<1>(stop)
+                               : grp == 1 ? epilogue_any<2>(stop)
+                               : grp == 2 ? epilogue_any<3>(stop)
+                                          : epilogue_any<4>(stop);
+                if (any) {
                     dead = true;
                     break;
                 }
                 tc_fence_after();
                 const bool edge = (t == 0) || ((ib + 1) * kT > T);
-                const float* bs = S.colstat[b];
+                const float* bs = S.colstat[grp][(gg / NG) & 1];
                 const int dj = ib * kT - j;               // i - j of the tile's first row
                 float part = 0.f, partB = 0.f, partr = 0.f;
-                const uint32_t tcol = tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * kT);
-                uint32_t ra[32], rb[32];
-                tc_ld32_issue(tcol, ra);
-                tc_ld32_wait(ra);
-                // the tile's four 32-column chunks; the causal and past-T
-                // masks are compiled only into the edge tiles' copy
+                const uint32_t tcol = tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(grp * kT);
+                // chunks of CW columns, each load issued while the previous
+                // chunk is processed (16 with the band sums, whose registers
+                // would not leave room for two 32-column buffers)
+                constexpr int CW = BAND ? 16 : 32, NCH = kT / CW;
+                uint32_t ra[CW], rb[CW];
+                tc_ld_issue(tcol, ra);
+                tc_ld_wait(ra);
+                // the causal and past-T masks are compiled only into the edge
+                // tiles' copy of the chunk loop
                 auto chunks = [&](auto edge_tag) {
                     constexpr bool EDGE = decltype(edge_tag)::value;
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint32_t (&cur)[32] = (ch & 1) ? rb : ra;
-                        uint32_t (&nxt)[32] = (ch & 1) ? ra : rb;
-                        if (ch + 1 < 4) tc_ld32_issue(tcol + (uint32_t)((ch + 1) * 32), nxt);
-                        const int i0 = ib * kT + ch * 32;
+                    for (int ch = 0; ch < NCH; ++ch) {
+                        uint32_t (&cur)[CW] = (ch & 1) ? rb : ra;
+                        uint32_t (&nxt)[CW] = (ch & 1) ? ra : rb;
+                        if (ch + 1 < NCH) tc_ld_issue(tcol + (uint32_t)((ch + 1) * CW), nxt);
+                        const int i0 = ib * kT + ch * CW;
                         const float2 c22 = make_float2(c2, c2);
                         float2 pa = make_float2(0.f, 0.f), pb = make_float2(0.f, 0.f);
 #pragma unroll
-                        for (int e = 0; e < 32; e += 4) {
-                            const float4 b4 = *reinterpret_cast<const float4*>(bs + ch * 32 + e);
+                        for (int e = 0; e < CW; e += 4) {
+                            const float4 b4 = *reinterpret_cast<const float4*>(bs + ch * CW + e);
                             const float2 ta = __ffma2_rn(make_float2(__uint_as_float(cur[e]), __uint_as_float(cur[e + 1])),
                                                          c22, make_float2(b4.x, b4.y));
                             const float2 tb = __ffma2_rn(make_float2(__uint_as_float(cur[e + 2]), __uint_as_float(cur[e + 3])),
@@ -677,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                             pa = __fadd2_rn(pa, make_float2(w0, w1));
                             pb = __fadd2_rn(pb, make_float2(w2, w3));
                             if (band) {
-                                const int d0 = dj + ch * 32 + e;
+                                const int d0 = dj + ch * CW + e;
                                 partB += (d0 < wB ? w0 : 0.f) + (d0 + 1 < wB ? w1 : 0.f) + (d0 + 2 < wB ? w2 : 0.f) +
                                          (d0 + 3 < wB ? w3 : 0.f);
                                 partr += (d0 < wr ? w0 : 0.f) + (d0 + 1 < wr ? w1 : 0.f) + (d0 + 2 < wr ? w2 : 0.f) +
@@ -685,14 +821,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                             }
                         }
                         part += (pa.x + pa.y) + (pb.x + pb.y);
-                        if (ch + 1 < 4) tc_ld32_wait(nxt);
+                        if (ch + 1 < NCH) tc_ld_wait(nxt);
                     }
                 };
                 if (edge) chunks(std::true_type{});
                 else chunks(std::false_type{});
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&S.acc_empty[b]);
+                if (lane == 0) mbar_arrive(&S.acc_empty[grp]);
                 const float y = part - cc;
                 const float tsum = cs + y;
                 cc = (tsum - cs) - y;
@@ -701,18 +837,39 @@ __global__ void __launch_bounds__(kThreads, 2)
                     bsB += (double)partB;
                     bsr += (double)partr;
                 }
-                // publish the next tile's statistics into the other buffer
-                if (more) S.colstat[b ^ 1][et] = inext < T ? -(nm + log2f(nl)) : -INFINITY;
+                // stage the next tile's statistics into the group's other
+                // buffer (last read two of its tiles ago, before the barrier
+                // that opened this one)
+                if (more) S.colstat[grp][((gg / NG) + 1) & 1][kk] = nbias(nm, nl, inext);
             }
-            staged = !dead && xn < nitems;
-            // an abandoned walk leaves NaN in its columns
-            if (j < T) {
-                cout[(size_t)u * T + j] = dead ? nan : (double)cs - (double)cc;
+            gt += ntiles;
+            // groups 1..3 hand their sums to group 0, which adds and writes
+            if (grp > 0) {
+                S.xch[ia & 1][grp - 1][0][kk] = dead ? nan : (double)cs - (double)cc;
                 if constexpr (BAND) {
-                    bandB[(size_t)u * T + j] = dead ? nan : bsB;
-                    bandr[(size_t)u * T + j] = dead ? nan : bsr;
+                    S.xch[ia & 1][grp - 1][1][kk] = bsB;
+                    S.xch[ia & 1][grp - 1][2][kk] = bsr;
                 }
             }
+            groups_sync<NG>();
+            if (grp == 0 && j < T) {
+                double ct = dead ? nan : (double)cs - (double)cc, bt = bsB, rt = bsr;
+#pragma unroll
+                for (int e = 1; e < NG; ++e) {
+                    ct += S.xch[ia & 1][e - 1][0][kk];
+                    if constexpr (BAND) {
+                        bt += S.xch[ia & 1][e - 1][1][kk];
+                        rt += S.xch[ia & 1][e - 1][2][kk];
+                    }
+                }
+                // an abandoned walk leaves NaN in its columns (NaN propagates through the sum)
+                cout[(size_t)u * T + j] = ct;
+                if constexpr (BAND) {
+                    bandB[(size_t)u * T + j] = isnan(ct) ? nan : bt;
+                    bandr[(size_t)u * T + j] = isnan(ct) ? nan : rt;
+                }
+            }
+            ++ia;
         }
     }
     tc_teardown_items(S, warp, w);
@@ -735,7 +892,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                        uint32_t* __restrict__ ck, double* __restrict__ cout, int* err)
 {
     extern __shared__ unsigned char smem_raw[];
-    TcSmem& S = tc_smem(smem_raw);
+    static_assert(TcSmem::kGrp == 1, "the flags kernel drains with one group of four warps");
+    TcSmem& S = tc_smem<TcSmem>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int u = blockIdx.x % U;
     const int jb = (int)(blockIdx.x / U);
@@ -760,7 +918,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int et = threadIdx.x - 64;          // epilogue thread 0..127
         const int q = warp & 3;
         const int j = jb * kT + 32 * q + lane;    // key within the unit
-        S.colstat[0][et] = thr(first * kT + et);
+        S.colstat[0][0][et] = thr(first * kT + et);
         uint32_t hist = 0u;
         for (int t = 0; t < ntiles; ++t) {
             const int b = t & 1;
@@ -770,7 +928,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             // agreed by all epilogue threads; also publishes last iteration's thresholds
             if (epilogue_any(!ok || aborted(S))) break;
             tc_fence_after();
-            const float* th = S.colstat[b];
+            const float* th = S.colstat[0][b];
             const uint32_t tcol = tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * kT);
             uint32_t ra[32], rb[32];
             tc_ld32_issue(tcol, ra);
@@ -791,7 +949,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.acc_empty[b]);
-            if (t + 1 < ntiles) S.colstat[b ^ 1][et] = nthr;
+            if (t + 1 < ntiles) S.colstat[0][b ^ 1][et] = nthr;
         }
         if (j < T && !aborted(S)) {
             ck[(size_t)u * T + j] = hist;
@@ -862,7 +1020,7 @@ cudaError_t launch_prompt_stats_tc(const CacheView& c, const PromptArgs& p, cuda
     const int G = p.G > 1 ? p.G : 1;
     const long long rows = (long long)c.U * p.T;
     if (!make_map(&mq, p.Q, rows) || !make_map(&mk, p.K, rows / G)) return cudaErrorInvalidValue;
-    const size_t smem = sizeof(TcSmem) + 1024;
+    const size_t smem = sizeof(TcSmemW) + 1024;
     static bool configured[64] = {false};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -879,23 +1037,24 @@ cudaError_t launch_prompt_stats_tc(const CacheView& c, const PromptArgs& p, cuda
     }
     const int nb = (p.T + kT - 1) / kT;
     const int nitems = c.U * nb;
-    // Persistent grid of the resident CTAs (2 per SM) for prompts of up to
+    // Persistent grid of the resident CTAs for prompts of up to
     // 32 blocks (4096 tokens), where an item's 1..32 tiles leave the per-CTA
     // set-up a large share; longer prompts take one item per CTA, whose
     // hardware scheduling (heaviest first) balances items of up to nb tiles
-    // better than the fixed walk (measured: 32 768 tokens 2.5 % faster).
-    const unsigned grid = nb <= kPersistBlocks ? (unsigned)std::min(nitems, 2 * sm_count()) : (unsigned)nitems;
+    // better than the fixed walk.
+    const int resident = kScoreCtasPerSM * sm_count();
+    const unsigned grid = nb <= kPersistBlocks ? (unsigned)std::min(nitems, resident) : (unsigned)nitems;
     // units per schedule group: the resident CTAs over the blocks per unit
-    const int g = std::max(1, std::min(c.U, 2 * sm_count() / nb));
-    rowstats_tc_kernel<<<grid, kThreads, smem, st>>>(mq, mk, c.U, G, p.T, nb, g, nitems, c.qscale, p.m2, p.l,
+    const int g = std::max(1, std::min(c.U, resident / nb));
+    rowstats_tc_kernel<<<grid, kThreadsW, smem, st>>>(mq, mk, c.U, G, p.T, nb, g, nitems, c.qscale, p.m2, p.l,
                                                      c.err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (p.bandB)
-        colsum_tc_kernel<true><<<grid, kThreads, smem, st>>>(mq, mk, c.U, G, p.T, nb, g, nitems, c.qscale, p.m2, p.l,
+        colsum_tc_kernel<true><<<grid, kThreadsW, smem, st>>>(mq, mk, c.U, G, p.T, nb, g, nitems, c.qscale, p.m2, p.l,
                                                              p.c, p.bandB, p.bandr, p.wB, p.wr, c.err);
     else
-        colsum_tc_kernel<false><<<grid, kThreads, smem, st>>>(mq, mk, c.U, G, p.T, nb, g, nitems, c.qscale, p.m2,
+        colsum_tc_kernel<false><<<grid, kThreadsW, smem, st>>>(mq, mk, c.U, G, p.T, nb, g, nitems, c.qscale, p.m2,
                                                               p.l, p.c, nullptr, nullptr, 0, 0, c.err);
     return cudaGetLastError();
 }
@@ -909,14 +1068,14 @@ cudaError_t launch_sh_flags_tc(const CacheView& c, const PromptArgs& p, cudaStre
     CUtensorMap mq, mk;
     const long long rows = (long long)c.U * p.T;
     if (!make_map(&mq, p.Q, rows) || !make_map(&mk, p.K, rows)) return cudaErrorInvalidValue;
-    const size_t smem = sizeof(TcSmem) + 1024;
+    const size_t smem = sizeof(TcSmem) + 1024, smemW = sizeof(TcSmemW) + 1024;
     static bool configured[64] = {false};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(rowstats_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(rowstats_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smemW);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(sh_flags_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -926,7 +1085,7 @@ cudaError_t launch_sh_flags_tc(const CacheView& c, const PromptArgs& p, cudaStre
     const int w0 = p.T > 32 ? p.T - 32 : 0;
     const int qb0 = w0 / kT, nq = nb - qb0;
     const int nitems = c.U * nq;
-    rowstats_tc_kernel<<<(unsigned)std::min(nitems, 2 * sm_count()), kThreads, smem, st>>>(
+    rowstats_tc_kernel<<<(unsigned)std::min(nitems, kScoreCtasPerSM * sm_count()), kThreadsW, smemW, st>>>(
         mq, mk, c.U, 1, p.T, nb, c.U, nitems, c.qscale, p.m2, p.l, c.err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
