@@ -132,9 +132,7 @@ __device__ __forceinline__ void tc_ld16_wait(uint32_t (&r)[16])
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]) :: "memory");
 }
-__device__ __forceinline__ void tc_ld_issue(uint32_t taddr, uint32_t (&r)[32]) { tc_ld32_issue(taddr, r); }
 __device__ __forceinline__ void tc_ld_issue(uint32_t taddr, uint32_t (&r)[16]) { tc_ld16_issue(taddr, r); }
-__device__ __forceinline__ void tc_ld_wait(uint32_t (&r)[32]) { tc_ld32_wait(r); }
 __device__ __forceinline__ void tc_ld_wait(uint32_t (&r)[16]) { tc_ld16_wait(r); }
 
 // max(a, b, c) in one instruction
@@ -174,6 +172,18 @@ __device__ __forceinline__ void tile_mma(uint32_t d_tmem, const uint8_t* a, cons
     for (int k = 0; k < kD / 16; ++k) {
         const uint32_t off = (uint32_t)(k / 4) * kBox + (uint32_t)(k % 4) * 32u;
         tc_mma(d_tmem, sw128_desc(a + off), sw128_desc(b + off), k > 0 ? 1u : 0u);
+    }
+}
+
+// The same from the descriptors of the two tiles' starts: K slice k adds
+// the slice's byte offset >> 4 to the start-address field (bits 0-13; the
+// tiles lie below 256 KB, so the sum stays in the field).
+__device__ __forceinline__ void tile_mma_desc(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc)
+{
+#pragma unroll
+    for (int k = 0; k < kD / 16; ++k) {
+        const uint64_t off = (uint64_t)(((uint32_t)(k / 4) * kBox + (uint32_t)(k % 4) * 32u) >> 4);
+        tc_mma(d_tmem, adesc + off, bdesc + off, k > 0 ? 1u : 0u);
     }
 }
 
@@ -418,6 +428,7 @@ __device__ __forceinline__ void tc_mma_items(SM& S, uint32_t tbase, int nitems, 
         if (x >= nitems) continue;
         const int ntiles = tiles(x);
         const int ka = ia % NA;
+        const uint64_t adesc = sw128_desc(S.a[ka]);
         if (!tc_wait(S, &S.a_full[ka], (uint32_t)((ia / NA) & 1), err)) return;
         for (int t = 0; t < ntiles; ++t, ++g) {
             const int s = g % NS, b = g % NACC;
@@ -425,7 +436,7 @@ __device__ __forceinline__ void tc_mma_items(SM& S, uint32_t tbase, int nitems, 
             if (g >= NACC && !tc_wait(S, &S.acc_empty[b], ((uint32_t)(g / NACC) & 1u) ^ 1u, err)) return;
             if (aborted(S)) return;
             tc_fence_after();
-            tile_mma(tbase + (uint32_t)b * kT, S.a[ka], S.b[s]);
+            tile_mma_desc(tbase + (uint32_t)b * kT, adesc, sw128_desc(S.b[s]));
             tc_commit(&S.b_empty[s]);     // the stage is free once these MMAs have read it
             tc_commit(&S.acc_full[b]);    // and the accumulator is ready for the epilogue
         }
