@@ -378,7 +378,7 @@ class OracleSample:
 
     def __init__(self, w, rule, qb, target_s, units=None, steps=None):
         import oracle
-        self.w, self.rule = w, rule
+        self.w, self.rule, self.qb = w, rule, qb
         self.S = steps or w.steps
         self.Tp = w.prompt
         if w.prompt > ORACLE_MAX_PROMPT:
@@ -411,9 +411,23 @@ class OracleSample:
         return "%d of %d units of one layer (%s, %d decode steps, %s), %.1f s" % (
             self.n, w.units, pr, self.S, rule_name(self.rule, w), self.seconds())
 
-    def record(self):
-        return {"value": self.rate(), "unit": UNIT, "cores": self.threads, "kind": "oracle",
-                "sample": self.describe()}
+    def record(self, single_thread=False):
+        rec = {"value": self.rate(), "unit": UNIT, "cores": self.threads, "kind": "oracle",
+               "sample": self.describe()}
+        if single_thread and self.threads > 1:
+            # the same oracle on one thread, over the units one of the
+            # sample's threads took
+            import oracle
+            n1 = max(1, self.n // self.threads)
+            try:
+                oracle.set_threads(1)
+                tp, td, _ = oracle_job(self.w, self.rule, list(range(n1)), self.S, self.qb, self.Tp)
+            finally:
+                oracle.set_threads(self.threads)
+            rate = self.S / ((tp * self.pair_scale + td) * self.w.units / n1)
+            rec["single_thread"] = {"value": rate, "unit": UNIT, "cores": 1,
+                                    "sample": "%d units on one thread, %.1f s" % (n1, tp + td)}
+        return rec
 
 
 # -------------------------------------------------------------- reference
@@ -599,6 +613,48 @@ class Job:
         return max_over_ranks(elapsed, world, device="cuda"), phase
 
     # algorithmic work of one launch / phase
+    def l2_hot(self, n=64, reps=5):
+        """Decode launches on ONE layer cache, repeated: for caches that fit
+        in L2 (129 MB) the rows then come from L2, so this is labelled apart
+        from the HBM numbers.  Layer 0 is prompted, its first n decode steps
+        captured in a graph and replayed; the median replay per launch."""
+        torch = self.torch
+        n = min(n, self.S)
+        g = self.layers[0]
+        h, pp, op = self.hh[0], self.ptr[0], self.optr[0]
+        step = self.step_call
+
+        def steps():
+            for t in range(n):
+                step(h, pp["q"][t], pp["k"][t], pp["v"][t], op[0][t], op[1][t])
+        with torch.cuda.stream(self.stream):
+            self.prefill_call(self.hs[0], g["Q"], g["K"], g["V"], self.w.prompt)
+            steps()
+            gr = torch.cuda.CUDAGraph()
+            gr.capture_begin()
+            steps()
+            gr.capture_end()
+        torch.cuda.synchronize()
+        each = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(self.stream):
+                self.prefill_call(self.hs[0], g["Q"], g["K"], g["V"], self.w.prompt)
+                a.record(self.stream)
+                gr.replay()
+                b.record(self.stream)
+            torch.cuda.synchronize()
+            each.append(a.elapsed_time(b) * 1000.0 / (n * self.decode_launches()))
+        self.sync()
+        by = self.decode_launch_bytes() / self.decode_launches()
+        us = statistics.median(each)
+        fits = by < 129e6
+        return {"decode_us_per_launch": us, "launches": n * self.decode_launches(),
+                "bytes_per_launch": by, "gb_s": by / us / 1e3,
+                "note": ("one layer cache decoded %d steps in a row: %.0f MB %s L2 (129 MB), so the rows %s; not an HBM "
+                         "number" % (n, by / 1e6, "fits in" if fits else "exceeds",
+                                     "come from L2" if fits else "still stream from HBM"))}
+
     def decode_kernel(self):
         if self.rule == "lsh":
             return "lsh_decode"
@@ -724,9 +780,11 @@ def l2_note(job):
             "reused only after %d others" % (job.NL, job.NL * by / 1e6, prompts / 1e6, job.NL - 1))
 
 
-def measure(args, L, torch, cname, rule, NL, S, stream, world, rank, want_e2e, cpu_seconds, clocks=None):
+def measure(args, L, torch, cname, rule, NL, S, stream, world, rank, want_e2e, cpu_seconds, clocks=None,
+            main_record=False):
     """Build, time and describe one configuration's job (clocks sampled
-    during its timed region when a sampler is given)."""
+    during its timed region when a sampler is given; the main record's CPU
+    baseline adds the oracle's single-thread rate)."""
     from kv_cache_eviction_h2o_gb300 import workloads as wl
     wname, rule0, NL0, q0 = CONFIGS[cname]
     w = wl.WORKLOADS[wname]
@@ -741,6 +799,7 @@ def measure(args, L, torch, cname, rule, NL, S, stream, world, rank, want_e2e, c
         time.sleep(0.3)
     elapsed, phase = job.time(args.steps, args.warmup, world)
     clk = clocks.stop() if clocks is not None else None
+    hot = job.l2_hot()
     K = args.steps
     ms = elapsed / K
     rl = rooflines(job, phase, elapsed, K)
@@ -760,6 +819,7 @@ def measure(args, L, torch, cname, rule, NL, S, stream, world, rank, want_e2e, c
         "launch_us": {r["kernel"]: r["launch_us"] for r in rl},
         "phases_ms_per_step": {k: v / K for k, v in phase.items()},
         "gpu_launches": job.launches_per_step() * K,
+        "l2_hot": hot,
     }
     if want_e2e:
         rec["e2e"] = run_e2e(job, world)
@@ -768,7 +828,7 @@ def measure(args, L, torch, cname, rule, NL, S, stream, world, rank, want_e2e, c
     rec["clocks"] = clk
     rec["cpu_baseline"] = None
     if rank == 0 and world == 1 and cpu_seconds > 0:
-        rec["cpu_baseline"] = OracleSample(w, rule, qb, cpu_seconds, steps=S).record()
+        rec["cpu_baseline"] = OracleSample(w, rule, qb, cpu_seconds, steps=S).record(single_thread=main_record)
     if mix:
         rec["policies"] = {"local": mix[0], "frequency+local": mix[1], "full": mix[2]}
     return rec
@@ -877,7 +937,7 @@ def run_ours(args):
     L.lib()
     stream = torch.cuda.Stream()
     main = measure(args, L, torch, args.config, args.rule, args.layers, args.decode_steps, stream, world, rank,
-                   not args.no_e2e, 0 if args.no_cpu else args.oracle_seconds, Clocks(local))
+                   not args.no_e2e, 0 if args.no_cpu else args.oracle_seconds, Clocks(local), main_record=True)
     subs = {}
     if not args.no_sub:
         names = [s for s in (args.sub.split(",") if args.sub else SUB_CONFIGS) if s and s != args.config]
@@ -894,6 +954,7 @@ def run_ours(args):
         "phases_ms_per_step": main["phases_ms_per_step"], "head_steps_per_s": main["head_steps_per_s"],
         "cpu_baseline": main["cpu_baseline"], "clocks": main["clocks"], "e2e": main.get("e2e"),
         "gpu_launches": main["gpu_launches"],
+        "l2_hot": main["l2_hot"],
         "sub_records": subs,
     }
     if rank == 0:
