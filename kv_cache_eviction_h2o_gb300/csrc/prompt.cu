@@ -311,13 +311,22 @@ __device__ __forceinline__ void radix_digit(const unsigned* hist, int remaining,
     cum = __shfl_sync(kFull, c, L);
 }
 
-template <int NT>
+// Heavy set of each unit (one CTA per unit): an 8-bit radix select, from
+// the top byte down, of the H-th largest candidate's bit pattern (the
+// column sums are non-negative, so their fp64 bit patterns order as the
+// values).  The candidates' keys are held in registers across the rounds
+// (PER per thread, strided by NT) when they fit, and the rounds stop as
+// soon as the threshold's bucket is kept whole: every key sharing the
+// prefix found so far is then kept, and no tie needs breaking.  Otherwise
+// the keys equal to the full threshold are kept in ascending position up to
+// the count still needed.
+template <int NT, int PER>
 __global__ void __launch_bounds__(NT) select_kernel(CacheView cv, PromptArgs pa)
 {
     __shared__ unsigned hist[256];
     __shared__ int warp_tot[32];
     __shared__ unsigned long long s_prefix;
-    __shared__ int s_need;
+    __shared__ int s_need, s_done;
     const int unit = blockIdx.x;
     const int T_ = pa.T, B = pa.budget > 0 ? pa.budget : cv.B, r = cv.r;
     const double* cu = pa.c + (size_t)unit * T_;
@@ -330,26 +339,44 @@ __global__ void __launch_bounds__(NT) select_kernel(CacheView cv, PromptArgs pa)
     const int ncand = keep_all ? 0 : T_ - r;
     const int H = keep_all ? 0 : min(pa.H, ncand);
 
-    unsigned long long thr = 0ull;      // bit pattern of the H-th largest candidate
-    int need = 0;                       // how many candidates equal to thr are kept
+    unsigned long long thr = 0ull;      // the threshold's bits under `mask`
+    unsigned long long mask = 0ull;     // the bits the rounds have fixed
+    int need = 0;                       // how many candidates matching thr under mask are kept
     if (H > 0) {
-        unsigned long long prefix = 0ull, mask = 0ull;
+        unsigned long long prefix = 0ull;
         int remaining = H;
+        const bool in_regs = ncand <= NT * PER;
+        unsigned long long kr[PER];
+        if (in_regs) {
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int j = tid + i * NT;
+                kr[i] = j < ncand ? (unsigned long long)__double_as_longlong(cu[j]) : 0ull;
+            }
+        }
+        // one key's digit into the histogram, warp-aggregated: one
+        // shared-memory atomic per distinct digit per warp (many candidates
+        // can share a digit, e.g. the zero low bytes of integer-valued keys)
+        auto count = [&](bool valid, unsigned long long key, int shift) {
+            int dig = -1;
+            if (valid && (key & mask) == prefix) dig = (int)((key >> shift) & 255ull);
+            const unsigned peers = __match_any_sync(0xffffffffu, dig);
+            if (dig >= 0 && (tid & 31) == __ffs(peers) - 1) atomicAdd(&hist[dig], (unsigned)__popc(peers));
+        };
         for (int shift = 56; shift >= 0; shift -= 8) {
             for (int i = tid; i < 256; i += NT) hist[i] = 0u;
             __syncthreads();
-            // warp-aggregated: one shared-memory atomic per distinct digit
-            // per warp (many candidates can share a digit, e.g. the zero low
-            // bytes of integer-valued keys)
-            for (int jb = tid - (tid & 31); jb < ncand; jb += NT) {
-                const int j = jb + (tid & 31);
-                int dig = -1;
-                if (j < ncand) {
-                    const unsigned long long key = (unsigned long long)__double_as_longlong(cu[j]);
-                    if ((key & mask) == prefix) dig = (int)((key >> shift) & 255ull);
+            if (in_regs) {
+#pragma unroll
+                for (int i = 0; i < PER; ++i) {
+                    if (i * NT + (tid - (tid & 31)) >= ncand) break;      // warp-uniform
+                    count(tid + i * NT < ncand, kr[i], shift);
                 }
-                const unsigned peers = __match_any_sync(0xffffffffu, dig);
-                if (dig >= 0 && (tid & 31) == __ffs(peers) - 1) atomicAdd(&hist[dig], (unsigned)__popc(peers));
+            } else {
+                for (int jb = tid - (tid & 31); jb < ncand; jb += NT) {
+                    const int j = jb + (tid & 31);
+                    count(j < ncand, j < ncand ? (unsigned long long)__double_as_longlong(cu[j]) : 0ull, shift);
+                }
             }
             __syncthreads();
             if (tid < 32) {
@@ -358,13 +385,16 @@ __global__ void __launch_bounds__(NT) select_kernel(CacheView cv, PromptArgs pa)
                 if (tid == 0) {
                     s_prefix = prefix | ((unsigned long long)dig << shift);
                     s_need = remaining - cum;
+                    s_done = (remaining - cum) == (int)hist[dig];   // the bucket is kept whole
                 }
             }
             __syncthreads();
             prefix = s_prefix;
             remaining = s_need;
             mask |= 255ull << shift;
+            const bool done = s_done != 0;
             __syncthreads();
+            if (done) break;
         }
         thr = prefix;
         need = remaining;
@@ -374,7 +404,7 @@ __global__ void __launch_bounds__(NT) select_kernel(CacheView cv, PromptArgs pa)
     int my_eq = 0;
     if (H > 0) {
         for (int j = j0; j < j1; ++j)
-            if (j < ncand && (unsigned long long)__double_as_longlong(cu[j]) == thr) ++my_eq;
+            if (j < ncand && ((unsigned long long)__double_as_longlong(cu[j]) & mask) == thr) ++my_eq;
     }
     int tot;
     int eq_before = block_exclusive_scan(my_eq, warp_tot, &tot);
@@ -390,7 +420,7 @@ __global__ void __launch_bounds__(NT) select_kernel(CacheView cv, PromptArgs pa)
             } else if (H == 0) {
                 k = false;
             } else {
-                const unsigned long long key = (unsigned long long)__double_as_longlong(cu[j]);
+                const unsigned long long key = (unsigned long long)__double_as_longlong(cu[j]) & mask;
                 if (key > thr) k = true;
                 else if (key == thr) { k = eq < need; ++eq; }
                 else k = false;
@@ -409,7 +439,7 @@ __global__ void __launch_bounds__(NT) select_kernel(CacheView cv, PromptArgs pa)
             } else if (H == 0) {
                 k = false;
             } else {
-                const unsigned long long key = (unsigned long long)__double_as_longlong(cu[j]);
+                const unsigned long long key = (unsigned long long)__double_as_longlong(cu[j]) & mask;
                 if (key > thr) k = true;
                 else if (key == thr) { k = eq < need; ++eq; }
                 else k = false;
@@ -1326,8 +1356,10 @@ cudaError_t launch_select(const CacheView& c, const PromptArgs& p, cudaStream_t 
 {
     // a block of 256 threads for prompts up to 4096 tokens (more units per
     // SM), 1024 above
-    if (p.T <= 4096) select_kernel<256><<<(unsigned)c.U, 256, 0, st>>>(c, p);
-    else select_kernel<1024><<<(unsigned)c.U, 1024, 0, st>>>(c, p);
+    // keys in registers up to 4096 candidates (16 a thread); longer prompts
+    // read them from L2 each round
+    if (p.T <= 4096) select_kernel<256, 16><<<(unsigned)c.U, 256, 0, st>>>(c, p);
+    else select_kernel<1024, 1><<<(unsigned)c.U, 1024, 0, st>>>(c, p);
     return cudaGetLastError();
 }
 
