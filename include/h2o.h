@@ -380,9 +380,9 @@ void h2o_destroy(h2o_handle h);
  * allocations afterwards, and hosts whose allocation calls may synchronise
  * the device in the middle of their own streams' work.
  *
- * The scorer's scratch (row max and normaliser, 8 bytes per unit per token)
- * is a fixed device array inside the library of H2O_NOALLOC_MAX_TOKENS
- * unit-tokens (8 MiB), present on every device that loads the library until
+ * The scorer's scratch (row max, normaliser and bias, 12 bytes per unit per
+ * token) is a fixed device array inside the library of H2O_NOALLOC_MAX_TOKENS
+ * unit-tokens (12 MiB), present on every device that loads the library until
  * the process exits.  The call allocates nothing.
  *   Q, K:  device [batch*heads][T][head_dim] of dtype, 16-byte aligned;
  *   c:     device fp64 [batch*heads][T], written in full;

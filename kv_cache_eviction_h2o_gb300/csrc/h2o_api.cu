@@ -129,6 +129,7 @@ struct h2o_ctx {
     // prompt scratch
     int T_cap;
     float* m2;
+    float* nb;                 // row biases for the scorer's second pass: the second half of l's allocation
     float* l;
     double* c;                 // per query head
     double* ckv;               // per cache unit (G > 1): the sum over its heads
@@ -178,6 +179,7 @@ void free_prompt(h2o_ctx* h)
     cudaFree(h->m2); cudaFree(h->l); cudaFree(h->c); cudaFree(h->ckv); cudaFree(h->cq); cudaFree(h->ck);
     cudaFree(h->bandB); cudaFree(h->bandr);
     h->m2 = nullptr; h->l = nullptr; h->c = nullptr; h->ckv = nullptr; h->cq = nullptr; h->ck = nullptr;
+    h->nb = nullptr;
     h->bandB = nullptr; h->bandr = nullptr;
     h->T_cap = 0;
 }
@@ -342,7 +344,7 @@ int ensure_prompt_scratch(h2o_ctx* h, int T)
     int rc;
     if (h->kind == kFG) {
         if ((rc = dev_alloc((void**)&h->m2, n * sizeof(float), "row max")) ||
-            (rc = dev_alloc((void**)&h->l, n * sizeof(float), "row normaliser")) ||
+            (rc = dev_alloc((void**)&h->l, 2 * n * sizeof(float), "row normaliser and bias")) ||
             (rc = dev_alloc((void**)&h->c, n * sizeof(double), "column sums")) ||
             (rc = dev_alloc((void**)&h->bandB, n * sizeof(double), "band sums (budget)")) ||
             (rc = dev_alloc((void**)&h->bandr, n * sizeof(double), "band sums (window)"))) {
@@ -350,7 +352,7 @@ int ensure_prompt_scratch(h2o_ctx* h, int T)
         }
     } else if (h->kind == kH2O) {
         if ((rc = dev_alloc((void**)&h->m2, nq * sizeof(float), "row max")) ||
-            (rc = dev_alloc((void**)&h->l, nq * sizeof(float), "row normaliser")) ||
+            (rc = dev_alloc((void**)&h->l, 2 * nq * sizeof(float), "row normaliser and bias")) ||
             (rc = dev_alloc((void**)&h->c, nq * sizeof(double), "column sums"))) {
             free_prompt(h); return rc;
         }
@@ -370,6 +372,9 @@ int ensure_prompt_scratch(h2o_ctx* h, int T)
             free_prompt(h); return rc;
         }
     }
+    // the row biases follow the normalisers in the same allocation (the
+    // persistence-of-importance and hashing handles have no second pass)
+    h->nb = (h->kind == kFG) ? h->l + n : (h->kind == kH2O) ? h->l + nq : nullptr;
     h->T_cap = T;
     return H2O_OK;
 }
@@ -459,7 +464,7 @@ int h2o_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T
     CacheView cv = view(h);
     PromptArgs pa = {};
     pa.Q = Q; pa.K = K; pa.V = V; pa.T = T; pa.H = h->H;
-    pa.m2 = h->m2; pa.l = h->l; pa.c = h->c; pa.G = h->G;
+    pa.m2 = h->m2; pa.l = h->l; pa.nb = h->nb; pa.c = h->c; pa.G = h->G;
     note_cache_write(h->device, h->stream, h);
     cudaError_t e;
     if (h->G > 1) {
@@ -574,7 +579,7 @@ int fg_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T)
     CacheView cv = view(h);
     PromptArgs pa = {};
     pa.Q = Q; pa.K = K; pa.V = V; pa.T = T; pa.H = h->H; pa.G = 1;
-    pa.m2 = h->m2; pa.l = h->l; pa.c = h->c;
+    pa.m2 = h->m2; pa.l = h->l; pa.nb = h->nb; pa.c = h->c;
     pa.budget = h->B_sel;
     pa.bandB = h->bandB; pa.bandr = h->bandr; pa.wB = h->B_sel; pa.wr = h->r;
     FgArgs fa = {};

@@ -48,6 +48,7 @@ struct PromptArgs {
     int H;              // heavy-hitter slots (H2O)
     float* m2;          // [U][T] row max, base-2 logit units
     float* l;           // [U][T] row normaliser
+    float* nb;          // [U][T] row bias -(m2 + log2 l), written by the tensor-core pass 1 for its pass 2
     double* c;          // [U][T] column sums
     uint32_t* cq;       // [U][T] query codes (LSH)
     uint32_t* ck;       // [U][T] key codes (LSH)

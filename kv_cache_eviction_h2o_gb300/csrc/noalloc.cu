@@ -5,9 +5,9 @@
 // afterwards, and hosts whose allocation calls may synchronise the device in
 // the middle of their own streams' work.  This entry point computes the
 // same prompt column sums as h2o_prefill, with the scorer's scratch (per-row
-// max and normaliser, 8 bytes per unit per token) held in a fixed device
+// max, normaliser and bias, 12 bytes per unit per token) held in a fixed device
 // array inside the library instead of memory it allocates.  The array
-// occupies kNoallocTokens * 8 bytes (8 MiB) on every device that loads the
+// occupies kNoallocTokens * 12 bytes (12 MiB) on every device that loads the
 // library, until the process exits.  With no handle there is no error word
 // to sync on: a scorer CTA whose bounded wait runs out writes NaN into the
 // statistics it owns, so the failure shows in the column sums.
@@ -20,8 +20,9 @@ namespace {
 
 constexpr long long kNoallocTokens = H2O_NOALLOC_MAX_TOKENS;
 
-// row max (base-2 logits) in [0, kNoallocTokens), row normaliser after it
-static __device__ __align__(256) float g_noalloc_scratch[2 * kNoallocTokens];
+// row max (base-2 logits) in [0, kNoallocTokens), row normaliser after it,
+// then the row bias of the scorer's second pass
+static __device__ __align__(256) float g_noalloc_scratch[3 * kNoallocTokens];
 
 std::mutex g_mu;
 void* g_addr[64];   // device address of g_noalloc_scratch, per device
@@ -76,6 +77,7 @@ extern "C" int h2o_prompt_scores_noalloc(const void* Q, const void* K, int batch
     pa.T = T;
     pa.m2 = static_cast<float*>(base);
     pa.l = static_cast<float*>(base) + kNoallocTokens;
+    pa.nb = static_cast<float*>(base) + 2 * kNoallocTokens;
     pa.c = c;
     e = launch_prompt_stats(cv, pa, reinterpret_cast<cudaStream_t>(cuda_stream));
     if (e != cudaSuccess) return set_last_error(H2O_ERR_CUDA, "h2o_prompt_scores_noalloc launch: %s", cudaGetErrorString(e));

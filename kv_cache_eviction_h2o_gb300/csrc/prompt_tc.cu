@@ -197,7 +197,7 @@ struct alignas(1024) TcSmemT {
     static constexpr uint32_t kCols = (uint32_t)NACC * kT;   // TMEM columns (a power of 2)
     uint8_t a[NA][kTile];             // the item's own block (Q in pass 1, K in pass 2)
     uint8_t b[NS][kTile];             // ring of the swept blocks
-    alignas(16) float colstat[NGRP][2][kT];   // pass 2: per group, two buffers of the 128 queries' -(m2 + log2(l)) (read as float4)
+    alignas(16) float colstat[NGRP][4][kT];   // pass 2: per warp of each group, its tile's 128 query biases -(m2 + log2(l)) (read as float4)
     double xch[2][NGRP > 1 ? NGRP - 1 : 1][3][kT];   // groups 1.. hand their per-item results to group 0, two items deep
     uint64_t a_full[NA];
     uint64_t a_empty[NA];             // the MMAs have read the A buffer
@@ -492,7 +492,7 @@ __device__ __forceinline__ void group_order(int x, int U, int nb, int g, int& u,
 __global__ void __launch_bounds__(kThreadsW, kScoreCtasPerSM)
     rowstats_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK, int U,
                        int G, int T, int nb, int g, int nitems, float c2, float* __restrict__ m2,
-                       float* __restrict__ lout, int* err)
+                       float* __restrict__ lout, float* __restrict__ nbias, int* err)
 {
     extern __shared__ unsigned char smem_raw[];
     TcSmemW& S = tc_smem<TcSmemW>(smem_raw);
@@ -652,6 +652,8 @@ __global__ void __launch_bounds__(kThreadsW, kScoreCtasPerSM)
                 // an abandoned walk leaves NaN, which the column sums carry on
                 m2[(size_t)u * T + i] = bad ? qnan : mo;
                 lout[(size_t)u * T + i] = bad ? qnan : lo;
+                // the row's bias in the second pass: a weight is 2^(s c2 + bias)
+                if (nbias) nbias[(size_t)u * T + i] = bad ? qnan : -(mo + log2f(lo));
             }
             ++ia;
         }
@@ -669,9 +671,9 @@ __global__ void __launch_bounds__(kThreadsW, kScoreCtasPerSM)
 template <bool BAND>
 __global__ void __launch_bounds__(kThreadsW, kScoreCtasPerSM)
     colsum_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK, int U,
-                     int G, int T, int nb, int g, int nitems, float c2, const float* __restrict__ m2,
-                     const float* __restrict__ lin, double* __restrict__ cout, double* __restrict__ bandB,
-                     double* __restrict__ bandr, int wB, int wr, int* err)
+                     int G, int T, int nb, int g, int nitems, float c2, const float* __restrict__ nbias,
+                     double* __restrict__ cout, double* __restrict__ bandB, double* __restrict__ bandr, int wB,
+                     int wr, int* err)
 {
     extern __shared__ unsigned char smem_raw[];
     TcSmemW& S = tc_smem<TcSmemW>(smem_raw);
@@ -709,7 +711,7 @@ __global__ void __launch_bounds__(kThreadsW, kScoreCtasPerSM)
         // keys, and groups 1..3 hand theirs to group 0 at the end of an item.
         const int q = warp & 3;
         const int grp = (warp - 2) >> 2;
-        const int kk = 32 * q + lane;             // key of the block (TMEM lane); also the query this thread stages
+        const int kk = 32 * q + lane;             // key of the block (TMEM lane)
         const int wmax = max(wB, wr);
         const double nan = __longlong_as_double(0x7ff8000000000000LL);
         const int P = (int)gridDim.x;
@@ -734,17 +736,31 @@ __global__ void __launch_bounds__(kThreadsW, kScoreCtasPerSM)
             }
             return false;
         };
-        // the query statistics of a tile as one negated bias per query,
-        // -(m2 + log2(l)), so a weight is 2^(s c2 + nbias); -inf past T
-        // (weight 0)
-        auto nbias = [&](float m, float l, int iq) { return iq < T ? -(m + log2f(l)) : -INFINITY; };
+        // Each warp stages its own copy of a tile's 128 query biases
+        // (written by pass 1: a weight is 2^(s c2 + bias); -inf past T,
+        // weight 0), four per lane, so no barrier joins the group's warps:
+        // the next tile's four are loaded at the start of a tile and stored
+        // after it.
+        float* wbias = S.colstat[grp][q];
+        auto load_bias = [&](int uq, int ibq, float (&bq)[4]) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int iq = ibq * kT + 4 * lane + k;
+                bq[k] = iq < T ? nbias[(size_t)uq * T + iq] : -INFINITY;
+            }
+        };
+        auto store_bias = [&](const float (&bq)[4]) {
+            __syncwarp();                         // every lane is past its reads of the last tile's biases
+            *reinterpret_cast<float4*>(wbias + 4 * lane) = make_float4(bq[0], bq[1], bq[2], bq[3]);
+            __syncwarp();
+        };
         {
             // the group's first tile: walk tile grp
             int u0, ib0;
             if (locate(0, 0, grp, u0, ib0)) {
-                const int iq = ib0 * kT + kk;
-                S.colstat[grp][0][kk] =
-                    iq < T ? nbias(m2[(size_t)u0 * T + iq], lin[(size_t)u0 * T + iq], iq) : -INFINITY;
+                float b0[4];
+                load_bias(u0, ib0, b0);
+                store_bias(b0);
             }
         }
         for (int r = 0; r * P < nitems; ++r) {
@@ -761,30 +777,20 @@ __global__ void __launch_bounds__(kThreadsW, kScoreCtasPerSM)
                 const int ib = jb + t;
                 // some key of the block has rows of this tile in its band
                 const bool band = BAND && ib * kT < (jb + 1) * kT + wmax;
-                // the group's next tile (gg + NG): its statistics are loaded
-                // now and staged after this tile
+                // the group's next tile (gg + NG): its biases are loaded now
+                // and staged after this tile
                 int un = u, ibn = ib + NG;
                 const bool more = t + NG < ntiles || locate(r, gt, gg + NG, un, ibn);
-                const int inext = ibn * kT + kk;
-                float nm = 0.f, nl = 1.f;
-                if (more && inext < T) {
-                    nm = m2[(size_t)un * T + inext];
-                    nl = lin[(size_t)un * T + inext];
-                }
+                float bnext[4];
+                if (more) load_bias(un, ibn, bnext);
                 const bool ok = tc_wait(S, &S.acc_full[grp], (uint32_t)(gg / NG) & 1u, err);
-                // agreed by the group's threads; also publishes the statistics staged before
-                const bool stop = !ok || aborted(S);
-                const bool any = grp == 0 ? epilogue_any<1>(stop)
-                               : grp == 1 ? epilogue_any<2>(stop)
-                               : grp == 2 ? epilogue_any<3>(stop)
-                                          : epilogue_any<4>(stop);
-                if (any) {
+                if (__any_sync(0xffffffffu, !ok || aborted(S))) {
                     dead = true;
                     break;
                 }
                 tc_fence_after();
                 const bool edge = (t == 0) || ((ib + 1) * kT > T);
-                const float* bs = S.colstat[grp][(gg / NG) & 1];
+                const float* bs = wbias;
                 const int dj = ib * kT - j;               // i - j of the tile's first row
                 float part = 0.f, partB = 0.f, partr = 0.f;
                 const uint32_t tcol = tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(grp * kT);
@@ -849,10 +855,7 @@ __global__ void __launch_bounds__(kThreadsW, kScoreCtasPerSM)
                     bsB += (double)partB;
                     bsr += (double)partr;
                 }
-                // stage the next tile's statistics into the group's other
-                // buffer (last read two of its tiles ago, before the barrier
-                // that opened this one)
-                if (more) S.colstat[grp][((gg / NG) + 1) & 1][kk] = nbias(nm, nl, inext);
+                if (more) store_bias(bnext);
             }
             gt += ntiles;
             // groups 1..3 hand their sums to group 0, which adds and writes
@@ -1031,6 +1034,7 @@ cudaError_t launch_prompt_stats_tc(const CacheView& c, const PromptArgs& p, cuda
     CUtensorMap mq, mk;
     const int G = p.G > 1 ? p.G : 1;
     const long long rows = (long long)c.U * p.T;
+    if (!p.nb) return cudaErrorInvalidValue;      // pass 2 reads the row biases pass 1 writes there
     if (!make_map(&mq, p.Q, rows) || !make_map(&mk, p.K, rows / G)) return cudaErrorInvalidValue;
     const size_t smem = sizeof(TcSmemW) + 1024;
     static bool configured[64] = {false};
@@ -1059,15 +1063,15 @@ cudaError_t launch_prompt_stats_tc(const CacheView& c, const PromptArgs& p, cuda
     // units per schedule group: the resident CTAs over the blocks per unit
     const int g = std::max(1, std::min(c.U, resident / nb));
     rowstats_tc_kernel<<<grid, kThreadsW, smem, st>>>(mq, mk, c.U, G, p.T, nb, g, nitems, c.qscale, p.m2, p.l,
-                                                     c.err);
+                                                     p.nb, c.err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (p.bandB)
-        colsum_tc_kernel<true><<<grid, kThreadsW, smem, st>>>(mq, mk, c.U, G, p.T, nb, g, nitems, c.qscale, p.m2, p.l,
+        colsum_tc_kernel<true><<<grid, kThreadsW, smem, st>>>(mq, mk, c.U, G, p.T, nb, g, nitems, c.qscale, p.nb,
                                                              p.c, p.bandB, p.bandr, p.wB, p.wr, c.err);
     else
-        colsum_tc_kernel<false><<<grid, kThreadsW, smem, st>>>(mq, mk, c.U, G, p.T, nb, g, nitems, c.qscale, p.m2,
-                                                              p.l, p.c, nullptr, nullptr, 0, 0, c.err);
+        colsum_tc_kernel<false><<<grid, kThreadsW, smem, st>>>(mq, mk, c.U, G, p.T, nb, g, nitems, c.qscale, p.nb,
+                                                              p.c, nullptr, nullptr, 0, 0, c.err);
     return cudaGetLastError();
 }
 
@@ -1098,7 +1102,7 @@ cudaError_t launch_sh_flags_tc(const CacheView& c, const PromptArgs& p, cudaStre
     const int qb0 = w0 / kT, nq = nb - qb0;
     const int nitems = c.U * nq;
     rowstats_tc_kernel<<<(unsigned)std::min(nitems, kScoreCtasPerSM * sm_count()), kThreadsW, smemW, st>>>(
-        mq, mk, c.U, 1, p.T, nb, c.U, nitems, c.qscale, p.m2, p.l, c.err);
+        mq, mk, c.U, 1, p.T, nb, c.U, nitems, c.qscale, p.m2, p.l, nullptr, c.err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     sh_flags_tc_kernel<<<(unsigned)(c.U * nb), kThreads, smem, st>>>(mq, mk, c.U, p.T, nb, qb0, c.qscale, p.m2, p.l,
