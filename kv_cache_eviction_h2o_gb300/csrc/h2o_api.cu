@@ -477,8 +477,7 @@ int h2o_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T
     } else {
         e = launch_prompt_stats(cv, pa, h->stream);
     }
-    if (e == cudaSuccess) e = launch_select(cv, pa, h->stream);
-    if (e == cudaSuccess) e = launch_gather(cv, pa, false, h->stream);
+    if (e == cudaSuccess) e = launch_select_gather(cv, pa, h->stream);
     if (e != cudaSuccess) return cuda_fail(e, "h2o_prefill launch");
     h->last_T = T;
     h->ready = 1;

@@ -97,6 +97,8 @@ cudaError_t launch_sh_prompt(const CacheView& c, const PromptArgs& p, cudaStream
 // its tensor-core history pass (bf16, head_dim 128; needs p.m2, p.l scratch)
 cudaError_t launch_sh_flags_tc(const CacheView& c, const PromptArgs& p, cudaStream_t st);
 cudaError_t launch_gather(const CacheView& c, const PromptArgs& p, bool with_codes, cudaStream_t st);
+// the selection and the kept rows' copy in one kernel where the prompt allows (H2O)
+cudaError_t launch_select_gather(const CacheView& c, const PromptArgs& p, cudaStream_t st);
 // per-head policies: recoveries from the column and band sums and the H2O
 // selection already made, the policy, and the kept set of local and full
 // units rewritten (the gather follows)

@@ -23,6 +23,7 @@
 #include <climits>
 #include <cstdlib>
 #include <cstring>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -311,6 +312,105 @@ __device__ __forceinline__ void radix_digit(const unsigned* hist, int remaining,
     cum = __shfl_sync(kFull, c, L);
 }
 
+// Copy the prompt rows named by pos[] into slots s0 .. s0 + SW - 1 (those
+// below `end`; zero rows for empty slots): lanes 0..15 of the warp move K,
+// 16..31 move V (16 bytes each).  The warp requests all SW positions, then
+// all SW rows, before it stores any, so SW rows are in flight per lane.
+// Quantised slots take the half-warp's max magnitude as the row's scale.
+template <typename T, int D, int SW>
+__device__ __forceinline__ void gather_group(const CacheView& cv, const PromptArgs& pa, long long s0, long long end,
+                                             int lane, int with_codes)
+{
+    constexpr int NV = D * (int)sizeof(T) / 16;   // 16-byte vectors per row
+    constexpr int VE = 16 / (int)sizeof(T);       // elements per 16-byte vector
+    constexpr int VPL = (NV + 15) / 16;           // vectors per lane of a half-warp
+    const int half = lane >> 4, l16 = lane & 15;
+    int p[SW], unit[SW];
+#pragma unroll
+    for (int k = 0; k < SW; ++k) {
+        const long long slot = s0 + k;
+        unit[k] = (int)(slot / cv.B);
+        p[k] = slot < end ? cv.pos[slot] : -1;
+    }
+    uint4 w[SW][VPL];
+#pragma unroll
+    for (int k = 0; k < SW; ++k) {
+        const T* src = reinterpret_cast<const T*>(half ? pa.V : pa.K) + ((size_t)unit[k] * pa.T + (size_t)max(p[k], 0)) * D;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int v = l16 + 16 * i;
+            w[k][i] = make_uint4(0u, 0u, 0u, 0u);
+            if (p[k] >= 0 && v < NV) w[k][i] = reinterpret_cast<const uint4*>(src)[v];
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < SW; ++k) {
+        const long long slot = s0 + k;
+        if (slot >= end) break;
+        if (!cv.qbits) {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(half ? cv.V : cv.K) + (size_t)slot * D);
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) {
+                const int v = l16 + 16 * i;
+                if (v < NV) dst[v] = w[k][i];
+            }
+        } else {
+            float x[VPL][VE];
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) {
+                const uint32_t u[4] = {w[k][i].x, w[k][i].y, w[k][i].z, w[k][i].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if constexpr (sizeof(T) == 2) {
+                        x[i][2 * e] = __uint_as_float(u[e] << 16);
+                        x[i][2 * e + 1] = __uint_as_float(u[e] & 0xffff0000u);
+                    } else {
+                        x[i][e] = __uint_as_float(u[e]);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < VE; ++e) amax = fmaxf(amax, fabsf(x[i][e]));
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+            float* scale_out =
+                reinterpret_cast<float*>(cv.kvs + (size_t)unit[k] * cv.Bp + (slot - (long long)unit[k] * cv.B)) + half;
+            if (cv.qbits == 8) {
+                const float inv = q8_inv(amax);
+                uint8_t* dst = reinterpret_cast<uint8_t*>(half ? cv.V : cv.K) + (size_t)slot * D;
+#pragma unroll
+                for (int i = 0; i < VPL; ++i) {
+                    const int v = l16 + 16 * i;
+                    if (v < NV) {
+                        if constexpr (VE == 8) {
+                            *reinterpret_cast<uint2*>(dst + v * VE) =
+                                make_uint2(q8_pack4(&x[i][0], inv), q8_pack4(&x[i][4], inv));
+                        } else {
+                            *reinterpret_cast<uint32_t*>(dst + v * VE) = q8_pack4(&x[i][0], inv);
+                        }
+                    }
+                }
+                if (l16 == 0) *scale_out = q8_scale(amax);
+            } else {
+                // 4-bit row: D / 2 bytes, VE / 2 per 16-byte input vector
+                const float inv = q4_inv(amax);
+                uint8_t* dst = reinterpret_cast<uint8_t*>(half ? cv.V : cv.K) + (size_t)slot * (D / 2);
+#pragma unroll
+                for (int i = 0; i < VPL; ++i) {
+                    const int v = l16 + 16 * i;
+                    if (v < NV) {
+                        if constexpr (VE == 8) *reinterpret_cast<uint32_t*>(dst + v * 4) = q4_pack<4>(&x[i][0], inv);
+                        else *reinterpret_cast<uint16_t*>(dst + v * 2) = (uint16_t)q4_pack<2>(&x[i][0], inv);
+                    }
+                }
+                if (l16 == 0) *scale_out = q4_scale(amax);
+            }
+        }
+        if (with_codes && lane == 0) cv.code[slot] = p[k] >= 0 ? pa.ck[(size_t)unit[k] * pa.T + p[k]] : 0u;
+    }
+}
+
 // Heavy set of each unit (one CTA per unit): an 8-bit radix select, from
 // the top byte down, of the H-th largest candidate's bit pattern (the
 // column sums are non-negative, so their fp64 bit patterns order as the
@@ -319,8 +419,10 @@ __device__ __forceinline__ void radix_digit(const unsigned* hist, int remaining,
 // soon as the threshold's bucket is kept whole: every key sharing the
 // prefix found so far is then kept, and no tie needs breaking.  Otherwise
 // the keys equal to the full threshold are kept in ascending position up to
-// the count still needed.
-template <int NT, int PER>
+// the count still needed.  With a row type T (not void) the CTA then copies
+// its unit's kept rows into the slots itself (the H2O prompt phase): its
+// warps take 16 consecutive slots at a time, all their rows in flight.
+template <int NT, int PER, typename T = void, int D = 0>
 __global__ void __launch_bounds__(NT) select_kernel(CacheView cv, PromptArgs pa)
 {
     __shared__ unsigned hist[256];
@@ -459,6 +561,14 @@ __global__ void __launch_bounds__(NT) select_kernel(CacheView cv, PromptArgs pa)
         if (cv.score) cv.score[ub + s] = make_float2(0.f, 0.f);
     }
     if (tid == 0) cv.ustate[unit] = make_int2(nkept, T_);
+    if constexpr (!std::is_void<T>::value) {
+        constexpr int SW = 16;
+        __syncthreads();                          // every slot's position is written
+        const int warp = tid >> 5, lane = tid & 31;
+        const long long end = (long long)ub + cv.B;
+        for (long long s0 = (long long)ub + warp * SW; s0 < end; s0 += (NT / 32) * SW)
+            gather_group<T, D, SW>(cv, pa, s0, end, lane, 0);
+    }
 }
 
 // Per-head policy of every unit ["Model Tells You What to Discard" review
@@ -532,111 +642,21 @@ __global__ void __launch_bounds__(256) fg_policy_kernel(CacheView cv, PromptArgs
     if (tid == 0) cv.ustate[unit] = make_int2(nk, T_);
 }
 
-// Copy the prompt rows named by pos[] into the slots (zero for empty slots);
-// lanes 0..15 of a warp move K, 16..31 move V (16 bytes each).  A warp takes
-// kGatherSlots consecutive slots and requests all their positions, then all
-// their rows, before it stores any: four rows in flight per lane instead of
-// one, which the copy needs to reach HBM speed.
+// The rows of every unit's slots after a selection that pos[] records (the
+// per-head policies rewrite it after the selection; HashEvict's replay
+// writes it): a warp takes kGatherSlots consecutive slots per round of a
+// grid-stride loop.
 constexpr int kGatherSlots = 4;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(256) gather_kernel(CacheView cv, PromptArgs pa, int with_codes)
 {
-    constexpr int NV = D * (int)sizeof(T) / 16;   // 16-byte vectors per row
-    constexpr int VE = 16 / (int)sizeof(T);       // elements per 16-byte vector
-    constexpr int VPL = (NV + 15) / 16;           // vectors per lane of a half-warp
-    constexpr int SW = kGatherSlots;
-    const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
+    const int lane = threadIdx.x & 31;
     const long long total = (long long)cv.U * cv.B;
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
-    for (long long s0 = wid * SW; s0 < total; s0 += nw * SW) {
-        int p[SW], unit[SW];
-#pragma unroll
-        for (int k = 0; k < SW; ++k) {
-            const long long slot = s0 + k;
-            unit[k] = (int)(slot / cv.B);
-            p[k] = slot < total ? cv.pos[slot] : -1;
-        }
-        uint4 w[SW][VPL];
-#pragma unroll
-        for (int k = 0; k < SW; ++k) {
-            const T* src = reinterpret_cast<const T*>(half ? pa.V : pa.K) + ((size_t)unit[k] * pa.T + (size_t)max(p[k], 0)) * D;
-#pragma unroll
-            for (int i = 0; i < VPL; ++i) {
-                const int v = l16 + 16 * i;
-                w[k][i] = make_uint4(0u, 0u, 0u, 0u);
-                if (p[k] >= 0 && v < NV) w[k][i] = reinterpret_cast<const uint4*>(src)[v];
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < SW; ++k) {
-            const long long slot = s0 + k;
-            if (slot >= total) break;
-            if (!cv.qbits) {
-                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<T*>(half ? cv.V : cv.K) + (size_t)slot * D);
-#pragma unroll
-                for (int i = 0; i < VPL; ++i) {
-                    const int v = l16 + 16 * i;
-                    if (v < NV) dst[v] = w[k][i];
-                }
-            } else {
-                // quantised row: the half-warp's max magnitude gives the scale
-                float x[VPL][VE];
-                float amax = 0.f;
-#pragma unroll
-                for (int i = 0; i < VPL; ++i) {
-                    const uint32_t u[4] = {w[k][i].x, w[k][i].y, w[k][i].z, w[k][i].w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if constexpr (sizeof(T) == 2) {
-                            x[i][2 * e] = __uint_as_float(u[e] << 16);
-                            x[i][2 * e + 1] = __uint_as_float(u[e] & 0xffff0000u);
-                        } else {
-                            x[i][e] = __uint_as_float(u[e]);
-                        }
-                    }
-#pragma unroll
-                    for (int e = 0; e < VE; ++e) amax = fmaxf(amax, fabsf(x[i][e]));
-                }
-#pragma unroll
-                for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-                float* scale_out =
-                    reinterpret_cast<float*>(cv.kvs + (size_t)unit[k] * cv.Bp + (slot - (long long)unit[k] * cv.B)) + half;
-                if (cv.qbits == 8) {
-                    const float inv = q8_inv(amax);
-                    uint8_t* dst = reinterpret_cast<uint8_t*>(half ? cv.V : cv.K) + (size_t)slot * D;
-#pragma unroll
-                    for (int i = 0; i < VPL; ++i) {
-                        const int v = l16 + 16 * i;
-                        if (v < NV) {
-                            if constexpr (VE == 8) {
-                                *reinterpret_cast<uint2*>(dst + v * VE) =
-                                    make_uint2(q8_pack4(&x[i][0], inv), q8_pack4(&x[i][4], inv));
-                            } else {
-                                *reinterpret_cast<uint32_t*>(dst + v * VE) = q8_pack4(&x[i][0], inv);
-                            }
-                        }
-                    }
-                    if (l16 == 0) *scale_out = q8_scale(amax);
-                } else {
-                    // 4-bit row: D / 2 bytes, VE / 2 per 16-byte input vector
-                    const float inv = q4_inv(amax);
-                    uint8_t* dst = reinterpret_cast<uint8_t*>(half ? cv.V : cv.K) + (size_t)slot * (D / 2);
-#pragma unroll
-                    for (int i = 0; i < VPL; ++i) {
-                        const int v = l16 + 16 * i;
-                        if (v < NV) {
-                            if constexpr (VE == 8) *reinterpret_cast<uint32_t*>(dst + v * 4) = q4_pack<4>(&x[i][0], inv);
-                            else *reinterpret_cast<uint16_t*>(dst + v * 2) = (uint16_t)q4_pack<2>(&x[i][0], inv);
-                        }
-                    }
-                    if (l16 == 0) *scale_out = q4_scale(amax);
-                }
-            }
-            if (with_codes && lane == 0) cv.code[slot] = p[k] >= 0 ? pa.ck[(size_t)unit[k] * pa.T + p[k]] : 0u;
-        }
-    }
+    for (long long s0 = wid * kGatherSlots; s0 < total; s0 += nw * kGatherSlots)
+        gather_group<T, D, kGatherSlots>(cv, pa, s0, total, lane, with_codes);
 }
 
 // Sign codes of every prompt query and key, one row (a query or a key) per
@@ -1360,6 +1380,32 @@ cudaError_t launch_select(const CacheView& c, const PromptArgs& p, cudaStream_t 
     // read them from L2 each round
     if (p.T <= 4096) select_kernel<256, 16><<<(unsigned)c.U, 256, 0, st>>>(c, p);
     else select_kernel<1024, 1><<<(unsigned)c.U, 1024, 0, st>>>(c, p);
+    return cudaGetLastError();
+}
+
+// The selection with the kept rows' copy in the same kernel, for prompts up
+// to 4096 tokens (one CTA of 256 threads per unit: enough units to cover the
+// SMs) and rows kept as they are; longer prompts (few units would leave
+// most SMs out of the copy) and quantised rows (their copy is arithmetic:
+// measured 50 us slower per OPT-30B-shaped layer inside the selection's
+// CTAs) select, then gather in a kernel of their own.
+cudaError_t launch_select_gather(const CacheView& c, const PromptArgs& p, cudaStream_t st)
+{
+    if (p.T > 4096 || c.qbits) {
+        cudaError_t e = launch_select(c, p, st);
+        return e != cudaSuccess ? e : launch_gather(c, p, false, st);
+    }
+    const bool bf = c.dtype == 1;
+    const unsigned grid = (unsigned)c.U;
+    if (c.D == 128) {
+        if (bf) select_kernel<256, 16, __nv_bfloat16, 128><<<grid, 256, 0, st>>>(c, p);
+        else select_kernel<256, 16, float, 128><<<grid, 256, 0, st>>>(c, p);
+    } else if (c.D == 64) {
+        if (bf) select_kernel<256, 16, __nv_bfloat16, 64><<<grid, 256, 0, st>>>(c, p);
+        else select_kernel<256, 16, float, 64><<<grid, 256, 0, st>>>(c, p);
+    } else {
+        return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 
