@@ -155,7 +155,9 @@ int h2o_init_gqa(h2o_handle* out, int budget, int heavy, int recent, int batch, 
  * slots 0..n-1 in ascending position; each slot's score starts at c_j.
  *   Q, K, V: device [U][T][d] of the handle's dtype.
  * Resets the handle's decode position to T.  Allocates the prompt scratch
- * (16 bytes per unit per token) when T exceeds the largest T seen so far.
+ * (20 bytes per unit per token: row max, normaliser and bias, column sums;
+ * per query head on a grouped-query handle, plus 8 per cache unit per token)
+ * when T exceeds the largest T seen so far.
  */
 int h2o_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T);
 
@@ -205,7 +207,7 @@ int sh_init(h2o_handle* out, int budget, int heavy, int recent, int batch, int h
  * tokens among 0..T-r-1 with the most set bits (ties to the newer
  * position); slots 0..n-1 in ascending position with their histories.
  *   Q, K, V: device [U][T][d] of the handle's dtype.  Allocates prompt
- *   scratch (12 bytes per unit per token) when T exceeds the largest T seen.
+ *   scratch (20 bytes per unit per token) when T exceeds the largest T seen.
  */
 int sh_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T);
 
@@ -254,14 +256,16 @@ int fg_init(h2o_handle* out, int budget, int heavy, int recent, int full_budget,
  * with P_ij the causal softmax of the prompt (as h2o_prefill); then the
  * unit's cache is built by the H2O prompt rule with its policy's budget,
  * heavy count and window.  Q, K, V: device [U][T][d].  Allocates prompt
- * scratch (32 bytes per unit per token) when T exceeds the largest T seen.
+ * scratch (36 bytes per unit per token) when T exceeds the largest T seen.
  */
 int fg_prefill(h2o_handle h, const void* Q, const void* K, const void* V, int T);
 
 /*
  * fg_decode_step -- one decode step of every unit by the H2O rule
- * (h2o_decode_step) with its own policy's budget and recent window, all
- * units in one launch.  Arguments as h2o_decode_step.
+ * (h2o_decode_step) with its own policy's budget and recent window: two
+ * launches, one over the units on a compressed policy and one over the
+ * units on the full cache (lists built by fg_prefill).  Arguments as
+ * h2o_decode_step.
  */
 int fg_decode_step(h2o_handle h, const void* q, const void* k, const void* v, float* out, int* victim_out);
 
