@@ -10,7 +10,7 @@ if not torch.cuda.is_available():
 
 import oracle                                              # noqa: E402
 from kv_cache_eviction_h2o_gb300 import workloads as wl    # noqa: E402
-from parity import (record, Dev, align_prefill, check_out, check_scores, h2o_lockstep,  # noqa: E402
+from parity import (record, Dev, align_prefill, check_out, check_scores, h2o_lockstep, widen,  # noqa: E402
                     kept_lists, lsh_lockstep)
 
 pytestmark = pytest.mark.gpu
@@ -215,3 +215,42 @@ def test_state_roundtrip_and_errors():
     assert (v1 == v2).all()
     np.testing.assert_array_equal(o1, o2)
     dev.close(); dev2.close()
+
+
+@pytest.mark.parametrize("B", [16384, 9217])
+def test_largest_budgets_from_a_set_state(B):
+    """The largest budget the decode kernels take (16 CTAs of 1024 slots per
+    unit, a cluster of 16) and a ragged one (9 full CTAs and one slot more):
+    a full cache is written with h2o_set_state -- H heavy positions drawn
+    below the window, the recent window, scores and rows random -- and the
+    device and the oracle step from that same state."""
+    from kv_cache_eviction_h2o_gb300 import binding as L
+    U, d, S = 2, 128, 6
+    H = B // 2
+    r = B - H
+    T0 = 3 * B                                   # the position of the first decode step
+    rng = np.random.default_rng(B)
+    scale = 1.0 / np.sqrt(d)
+    st = oracle.H2OState(U, B, d)
+    bits = lambda x: (x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    Kb = bits(wl.round_bf16(rng.standard_normal((U, B, d), dtype=np.float32)))
+    Vb = bits(wl.round_bf16(rng.standard_normal((U, B, d), dtype=np.float32)))
+    for u in range(U):
+        heavy = np.sort(rng.choice(T0 - r, size=H, replace=False))
+        st.pos[u] = np.concatenate([heavy, np.arange(T0 - r, T0)]).astype(np.int32)
+        st.score[u] = np.where(st.pos[u] < T0 - r, rng.uniform(0.5, 3.0, B), rng.uniform(0.0, 1.0, B))
+        # scores exactly representable as the device's fp32 pair
+        st.score[u] = st.score[u].astype(np.float32).astype(np.float64)
+    st.K = widen(Kb, "bf16").astype(np.float64)
+    st.V = widen(Vb, "bf16").astype(np.float64)
+    st.occ[:] = B
+    dev = Dev("h2o", U, d, B, H, r, "bf16", scale)
+    try:
+        L.h2o_set_state(dev.h, Kb, Vb, st.score.copy(), st.pos.copy(), None, np.full(U, B, np.int32),
+                        np.full(U, T0, np.int32))
+        f = lambda *shape: wl.round_bf16(rng.standard_normal(shape, dtype=np.float32))
+        q, k, v = f(S, U, d), f(S, U, d), f(S, U, d)
+        near, _ = h2o_lockstep(dev, st, q, k, v, T0, r, scale)
+        record("largest budget %d" % B, near_ties=near)
+    finally:
+        dev.close()
