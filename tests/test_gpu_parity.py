@@ -254,3 +254,36 @@ def test_largest_budgets_from_a_set_state(B):
         record("largest budget %d" % B, near_ties=near)
     finally:
         dev.close()
+
+
+def test_largest_budget_hashevict_from_a_set_state():
+    """HashEvict at the largest budget (16384 slots, a cluster of 16 CTAs per
+    unit): a full cache with random rows, the codes of its keys (the
+    oracle's hash) and positions, set on the device; victims, codes,
+    positions and rows bit-exact and outputs within tolerance, step by step."""
+    from kv_cache_eviction_h2o_gb300 import binding as L
+    U, d, S, B = 2, 128, 6, 16384
+    r = B // 2
+    T0 = 3 * B
+    rng = np.random.default_rng(77)
+    scale = 1.0 / np.sqrt(d)
+    W = np.random.default_rng(5).standard_normal((d, 32), dtype=np.float32)
+    st = oracle.LSHState(U, B, d)
+    bits = lambda x: (x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    Kf = wl.round_bf16(rng.standard_normal((U, B, d), dtype=np.float32))
+    Vf = wl.round_bf16(rng.standard_normal((U, B, d), dtype=np.float32))
+    for u in range(U):
+        older = np.sort(rng.choice(T0 - r, size=B - r, replace=False))
+        st.pos[u] = np.concatenate([older, np.arange(T0 - r, T0)]).astype(np.int32)
+    st.K, st.V = Kf.astype(np.float64), Vf.astype(np.float64)
+    st.code = oracle.lsh_codes(Kf, W)
+    st.occ[:] = B
+    dev = Dev("lsh", U, d, B, 0, r, "bf16", scale, W=W)
+    try:
+        L.h2o_set_state(dev.h, bits(Kf), bits(Vf), np.zeros((U, B)), st.pos.copy(), st.code.copy(),
+                        np.full(U, B, np.int32), np.full(U, T0, np.int32))
+        f = lambda *shape: wl.round_bf16(rng.standard_normal(shape, dtype=np.float32))
+        q, k, v = f(S, U, d), f(S, U, d), f(S, U, d)
+        lsh_lockstep(dev, st, q, k, v, W, T0, r, scale)
+    finally:
+        dev.close()
