@@ -152,3 +152,39 @@ def test_kv4_and_kv8_together_rejected():
     with pytest.raises(L.H2OError) as e:
         L.h2o_init(8, 4, 4, 1, 2, 64, L.H2O_F32 | L.H2O_KV8 | L.H2O_KV4, 0.125, None)
     assert e.value.code == L.H2O_ERR_ARG
+
+
+@pytest.mark.parametrize("bits", BITS)
+def test_quant_largest_budget_from_a_set_state(bits):
+    """Quantised slots at the largest budget (16384 slots, a 16-CTA cluster
+    per unit): a full cache of random rows quantised by the oracle, its codes,
+    scales, positions and scores set on the device; the two step from that
+    same state."""
+    U, d, S, B = 2, 128, 6, 16384
+    H = B // 2
+    r = B - H
+    T0 = 3 * B
+    rng = np.random.default_rng(300 + bits)
+    scale = 1.0 / np.sqrt(d)
+    st = oracle.H2OState(U, B, d)
+    st.K = wl.round_bf16(rng.standard_normal((U, B, d), dtype=np.float32)).astype(np.float64)
+    st.V = wl.round_bf16(rng.standard_normal((U, B, d), dtype=np.float32)).astype(np.float64)
+    for u in range(U):
+        heavy = np.sort(rng.choice(T0 - r, size=H, replace=False))
+        st.pos[u] = np.concatenate([heavy, np.arange(T0 - r, T0)]).astype(np.int32)
+        st.score[u] = np.where(st.pos[u] < T0 - r, rng.uniform(0.5, 3.0, B), rng.uniform(0.0, 1.0, B))
+        st.score[u] = st.score[u].astype(np.float32).astype(np.float64)
+    st.occ[:] = B
+    st = _quant(st, bits)
+    kc, vc = (st.kq, st.vq) if bits == 8 else (oracle.pack4(st.kq), oracle.pack4(st.vq))
+    dev = Dev("h2o", U, d, B, H, r, "bf16", scale, kv8=bits == 8, kv4=bits == 4)
+    try:
+        L.h2o_set_state(dev.h, np.ascontiguousarray(kc), np.ascontiguousarray(vc), st.score.copy(), st.pos.copy(),
+                        None, np.full(U, B, np.int32), np.full(U, T0, np.int32))
+        L.h2o_set_kv_scales(dev.h, st.ks.copy(), st.vs.copy())
+        f = lambda *shape: wl.round_bf16(rng.standard_normal(shape, dtype=np.float32))
+        q, k, v = f(S, U, d), f(S, U, d), f(S, U, d)
+        near, _ = h2o_lockstep(dev, st, q, k, v, T0, r, scale)
+        record("quant%d largest budget" % bits, near_ties=near)
+    finally:
+        dev.close()
