@@ -1174,6 +1174,7 @@ cudaError_t launch_gqa_t(const DecodeArgs& a, cudaStream_t st)
     // CTAs per unit: enough to give every SM one while the exchange holds
     // their head states, never fewer than one per kMaxChunk slots
     int split = a.num_sms > 0 ? a.num_sms / max(1, a.c.U) : 1;
+    if (const char* ev = getenv("H2O_GQA_SPLIT")) split = atoi(ev);   // tuning override
     split = max(split, (a.c.B + kMaxChunk - 1) / kMaxChunk);
     split = max(1, min(split, GqaShape<G>::CMAX));
     cudaLaunchConfig_t cfg = {};
@@ -1198,16 +1199,18 @@ cudaError_t launch_gqa_t(const DecodeArgs& a, cudaStream_t st)
 }
 
 // the one-pass grouped-query kernel unless H2O_GQA_PATH=cluster (one CTA per
-// query head, kept for comparison)
-bool gqa_one_pass()
+// query head, kept for comparison); H2O_GQA_PATH=one takes it for every
+// shape it serves (for comparisons)
+int gqa_path()
 {
     static int v = -1;
     if (v < 0) {
         const char* e = getenv("H2O_GQA_PATH");
-        v = (e && strcmp(e, "cluster") == 0) ? 0 : 1;
+        v = (e && strcmp(e, "cluster") == 0) ? 0 : (e && strcmp(e, "one") == 0) ? 2 : 1;
     }
-    return v == 1;
+    return v;
 }
+bool gqa_one_pass() { return gqa_path() != 0; }
 
 // One row form QB over the dtypes and head sizes: tile TL, or TLF for bf16
 // rows of 128 with fewer units than SMs (one-head caches).
@@ -1244,7 +1247,7 @@ cudaError_t dispatch(const DecodeArgs& a, int split, cudaStream_t st)
             // 2, 4 or 8 heads per unit)
             // (4 heads on fewer units than half the SMs: the cluster path below
             // measured faster -- each of its CTAs walks fewer stages)
-            const bool small4 = a.G == 4 && a.num_sms > 0 && 2 * a.c.U < a.num_sms;
+            const bool small4 = a.G == 4 && a.num_sms > 0 && 2 * a.c.U < a.num_sms && gqa_path() != 2;
             if (a.c.D == 128 && bf && a.c.qbits == 0 && gqa_one_pass() && !small4) {
                 if (a.G == 2) return launch_gqa_t<__nv_bfloat16, 128, 2>(a, st);
                 if (a.G == 4) return launch_gqa_t<__nv_bfloat16, 128, 4>(a, st);
