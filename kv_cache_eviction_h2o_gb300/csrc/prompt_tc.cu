@@ -197,7 +197,9 @@ struct alignas(1024) TcSmemT {
     static constexpr uint32_t kCols = (uint32_t)NACC * kT;   // TMEM columns (a power of 2)
     uint8_t a[NA][kTile];             // the item's own block (Q in pass 1, K in pass 2)
     uint8_t b[NS][kTile];             // ring of the swept blocks
-    alignas(16) float colstat[NGRP][4][kT];   // pass 2: per warp of each group, its tile's 128 query biases -(m2 + log2(l)) (read as float4)
+    // pass 2: per warp of each group, its tile's 128 query biases -(m2 + log2(l)) (read as float4);
+    // the flags kernel: two buffers of the 128 queries' thresholds ([0][0], [0][1])
+    alignas(16) float colstat[NGRP][4][kT];
     double xch[2][NGRP > 1 ? NGRP - 1 : 1][3][kT];   // groups 1.. hand their per-item results to group 0, two items deep
     uint64_t a_full[NA];
     uint64_t a_empty[NA];             // the MMAs have read the A buffer
@@ -247,9 +249,9 @@ __device__ __forceinline__ bool tc_wait(SM& S, uint64_t* bar, uint32_t parity, i
 template <class SM>
 __device__ __forceinline__ bool aborted(SM& S) { return *(volatile int*)&S.abort != 0; }
 
-// OR of `pred` over the 128 threads of one epilogue group (named barrier
-// `id`: 1 + the group); also orders their earlier shared-memory writes
-// before the later reads
+// OR of `pred` over the 128 epilogue threads of the flags kernel (named
+// barrier ID); also orders their earlier shared-memory writes before the
+// later reads
 template <int ID = 1>
 __device__ __forceinline__ bool epilogue_any(bool pred)
 {
