@@ -667,7 +667,9 @@ __global__ void __launch_bounds__(256) gather_kernel(CacheView cv, PromptArgs pa
 // the warp, instead of through shared memory (where delivering one value to
 // 32 lanes costs a shared-memory cycle, a quarter of the SM's FMA rate; W
 // staged in shared memory and read four values per broadcast load measured
-// 1.5x slower than this: 331 against 220 us on the OPT-6.7B-shaped prompt).
+// 1.5x slower than this: 331 against 220 us on the OPT-6.7B-shaped prompt;
+// two rows per thread, each W value feeding both, 268 us: 128 registers
+// halve the warps per SM).
 constexpr int kCodeThreads = 256;
 
 template <int D>
