@@ -67,3 +67,14 @@ def test_bench_prompt_phase_byte_model():
     # budget 8 over four tokens: all four prompt rows read (two more, 16 B),
     # and all eight slots written (six more, 6 x 20 B)
     assert bench.prefill_bytes(1, 1, 4, 2, 8) - bench.prefill_bytes(1, 1, 4, 2, 2) == 16 + 6 * 20
+
+
+def test_bench_prompt_phase_flop_model():
+    """Both score passes take 2 d FLOPs per causal (i, j) pair: one unit of
+    two tokens (3 pairs: (0,0), (1,0), (1,1)) at d = 3 is 2 x 2 x 3 x 3 =
+    36 FLOPs; the OPT-6.7B-shaped layer (256 units, 2048 tokens, d = 128) is
+    275 GFLOP."""
+    import bench
+    assert bench.prefill_flops(1, 2, 3) == 36
+    assert bench.prefill_flops(256, 2048, 128) == 2 * 2 * 256 * 128 * 2048 * 2049 // 2
+    assert abs(bench.prefill_flops(256, 2048, 128) / 1e9 - 275.0) < 0.1
