@@ -597,7 +597,7 @@ __global__ void __launch_bounds__(kThreadsW, kScoreCtasPerSM)
                         // stays, 0 before the first finite column; a chunk of
                         // masked columns (-inf) leaves m, and adds nothing
                         const float mn = fmaxf(m, cm * c2);
-                        const float alpha = (mn == m) ? 1.f : ((m == -INFINITY) ? 0.f : exp2f(m - mn));
+                        const float alpha = (mn == m) ? 1.f : ex2_fast(m - mn);   // ex2(-inf) = 0
                         l *= alpha;
                         lc *= alpha;
                         m = mn;
