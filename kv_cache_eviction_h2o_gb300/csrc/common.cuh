@@ -249,6 +249,15 @@ __device__ __forceinline__ void prefetch_rows_l2(const void* q, const void* k, c
     }
 }
 
+// 2^x by the MUFU instruction (about 2 ulp; results below 2^-126 flush to
+// 0, ex2(-inf) = 0)
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void grid_dependency_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");

@@ -221,8 +221,8 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
         // this head's output, then its probabilities in place of its logits
         const float invL = 1.f / Lc;
         if (tid < D) a.out[qrow * D + tid] = Oc * invL;
-        for (int s = tid; s < n; s += TL::NT) S.z[s] = exp2f(S.z[s] - Mc) * invL;
-        if (tid == 0) S.P_new = exp2f(S.z_new - Mc) * invL;
+        for (int s = tid; s < n; s += TL::NT) S.z[s] = ex2_approx(S.z[s] - Mc) * invL;
+        if (tid == 0) S.P_new = ex2_approx(S.z_new - Mc) * invL;
         cluster_arrive();                    // every head's probabilities are in place
         cluster_wait();
         // scores of this CTA's share: add the heads' probabilities in head
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
     for (int i = 0; i < TL::SPT; ++i) {
         const int s = c0 + tid + i * TL::NT;
         if (s < c1) {
-            const float P = exp2f(S.z[s - c0] - M) * invL;
+            const float P = ex2_approx(S.z[s - c0] - M) * invL;
             ArgMin k;
             if constexpr (SH) {
                 const uint32_t h = (__float_as_uint(sc_old[i].x) << 1) | (P * (float)(n + 1) > 1.f ? 1u : 0u);
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(TL::NT, TL::MINB) h2o_decode_kernel(const Deco
         }
         a.out[qrow * D + tid] = acc * invL;
     }
-    if (rank == 0 && tid == 0) S.P_new = exp2f(S.z_new - M) * invL;
+    if (rank == 0 && tid == 0) S.P_new = ex2_approx(S.z_new - M) * invL;
     __syncthreads();
 
     if (C == 1) {
@@ -788,7 +788,7 @@ __global__ void __launch_bounds__(GqaShape<G>::NT, 1) gqa_decode_kernel(const De
         if (s < c1) {
             float2 ns = sc_old[i];
 #pragma unroll
-            for (int g = 0; g < G; ++g) ns = pair_add(ns, exp2f(S.z[g][s - f0] - S.M[g]) * S.invL[g]);
+            for (int g = 0; g < G; ++g) ns = pair_add(ns, ex2_approx(S.z[g][s - f0] - S.M[g]) * S.invL[g]);
             c.score[ub + s] = ns;
             const ArgMin k = ArgMin{ord_key(ns.x), ord_key(ns.y), (unsigned)s};
             if (full) {
@@ -808,7 +808,7 @@ __global__ void __launch_bounds__(GqaShape<G>::NT, 1) gqa_decode_kernel(const De
     if (rank == 0 && tid == 0) {
         float2 pn = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int g = 0; g < G; ++g) pn = pair_add(pn, exp2f(S.zn[g] - S.M[g]) * S.invL[g]);
+        for (int g = 0; g < G; ++g) pn = pair_add(pn, ex2_approx(S.zn[g] - S.M[g]) * S.invL[g]);
         S.P_new = pn;
     }
     __syncthreads();

@@ -117,7 +117,7 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
 
 __device__ __forceinline__ float safe_exp2_diff(float a, float m)
 {
-    return (a == -INFINITY) ? 0.f : exp2f(a - m);
+    return (a == -INFINITY) ? 0.f : ex2_approx(a - m);
 }
 
 // Lexicographic arg-min over (score hi, score lo, slot), each an unsigned

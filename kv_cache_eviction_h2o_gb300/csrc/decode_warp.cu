@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, MINB) h2o_warp_kernel(const
 #pragma unroll
             for (int e = 0; e < EPL; ++e) dst[e] = o[e] * invL;
         }
-        const float P_new = exp2f(zn - M) * invL;
+        const float P_new = ex2_approx(zn - M) * invL;
 
         // accumulate this step's probabilities; arg-min over candidates
         // (slots whose position is at most p - r)
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, MINB) h2o_warp_kernel(const
             for (int t = 0; t < 4; ++t) {
                 const int s = s0 + 32 * t + lane;
                 if (s < c1) {
-                    const float Pr = exp2f(z[s] - M) * invL;
+                    const float Pr = ex2_approx(z[s] - M) * invL;
                     const float2 ns = pair_add(so[t], Pr);
                     c.score[ub + s] = ns;
                     if (full && po[t] <= p - c.r) argmin_take(best, ArgMin{ord_key(ns.x), ord_key(ns.y), (unsigned)s});
