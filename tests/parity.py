@@ -21,8 +21,8 @@ NEAR_TIE = 1e-6
 OUT_ATOL, OUT_RTOL = 2e-3, 1e-2
 SCORE_RTOL, SCORE_ATOL = 1e-4, 1e-12
 
-# near ties and flag flips counted by the tests of this session, by test
-# name; tests/conftest.py writes them out at the end of the session
+# near ties and flag flips counted by the tests of this pytest run, by test
+# name; tests/conftest.py writes them out at the end of the run
 RECORD = {}
 
 
