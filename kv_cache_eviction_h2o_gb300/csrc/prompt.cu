@@ -411,7 +411,9 @@ __device__ __forceinline__ void gather_group(const CacheView& cv, const PromptAr
     }
 }
 
-// Heavy set of each unit (one CTA per unit): an 8-bit radix select, from
+// Heavy set of each unit [H2O review page, 提案手法: the H tokens of largest
+// accumulated attention outside the recent window] (one CTA per unit): an
+// 8-bit radix select, from
 // the top byte down, of the H-th largest candidate's bit pattern (the
 // column sums are non-negative, so their fp64 bit patterns order as the
 // values).  The candidates' keys are held in registers across the rounds
@@ -1417,9 +1419,12 @@ cudaError_t launch_fg_policy(const CacheView& c, const PromptArgs& p, const FgAr
     return cudaGetLastError();
 }
 
-// One CTA: the units of the compressed policies (0, 1) and of the full
-// cache (2), each list in unit order (a ballot and a running offset per
-// 1024 units).
+// The per-head policies' decode lists ["Model Tells You What to Discard"
+// review page, method section: each head keeps its own policy's cache]:
+// one CTA writes the units of the compressed policies (0, 1) and of the
+// full cache (2), each list in unit order (a ballot and a running offset
+// per 1024 units), so that each decode step can launch over each budget
+// class with a split of its own.
 __global__ void __launch_bounds__(1024) fg_lists_kernel(const int4* __restrict__ upol, int U, int* __restrict__ lists,
                                                         int* __restrict__ counts)
 {
