@@ -413,10 +413,9 @@ __device__ __forceinline__ void gather_group(const CacheView& cv, const PromptAr
 
 // Heavy set of each unit [H2O review page, 提案手法: the H tokens of largest
 // accumulated attention outside the recent window] (one CTA per unit): an
-// 8-bit radix select, from
-// the top byte down, of the H-th largest candidate's bit pattern (the
-// column sums are non-negative, so their fp64 bit patterns order as the
-// values).  The candidates' keys are held in registers across the rounds
+// 8-bit radix select, from the top byte down, of the H-th largest
+// candidate's bit pattern (the column sums are non-negative, so their fp64
+// bit patterns order as the values).  The candidates' keys are held in registers across the rounds
 // (PER per thread, strided by NT) when they fit, and the rounds stop as
 // soon as the threshold's bucket is kept whole: every key sharing the
 // prefix found so far is then kept, and no tie needs breaking.  Otherwise
