@@ -344,7 +344,7 @@ int ensure_prompt_scratch(h2o_ctx* h, int T)
     int rc;
     if (h->kind == kFG) {
         if ((rc = dev_alloc((void**)&h->m2, n * sizeof(float), "row max")) ||
-            (rc = dev_alloc((void**)&h->l, 2 * n * sizeof(float), "row normaliser and bias")) ||
+            (rc = dev_alloc((void**)&h->l, (2 * n + 4) * sizeof(float), "row normaliser and bias")) ||
             (rc = dev_alloc((void**)&h->c, n * sizeof(double), "column sums")) ||
             (rc = dev_alloc((void**)&h->bandB, n * sizeof(double), "band sums (budget)")) ||
             (rc = dev_alloc((void**)&h->bandr, n * sizeof(double), "band sums (window)"))) {
@@ -352,7 +352,7 @@ int ensure_prompt_scratch(h2o_ctx* h, int T)
         }
     } else if (h->kind == kH2O) {
         if ((rc = dev_alloc((void**)&h->m2, nq * sizeof(float), "row max")) ||
-            (rc = dev_alloc((void**)&h->l, 2 * nq * sizeof(float), "row normaliser and bias")) ||
+            (rc = dev_alloc((void**)&h->l, (2 * nq + 4) * sizeof(float), "row normaliser and bias")) ||
             (rc = dev_alloc((void**)&h->c, nq * sizeof(double), "column sums"))) {
             free_prompt(h); return rc;
         }
@@ -372,9 +372,11 @@ int ensure_prompt_scratch(h2o_ctx* h, int T)
             free_prompt(h); return rc;
         }
     }
-    // the row biases follow the normalisers in the same allocation (the
-    // persistence-of-importance and hashing handles have no second pass)
-    h->nb = (h->kind == kFG) ? h->l + n : (h->kind == kH2O) ? h->l + nq : nullptr;
+    // the row biases follow the normalisers in the same allocation, from a
+    // 16-byte boundary (the persistence-of-importance and hashing handles
+    // have no second pass)
+    const size_t nl = (h->kind == kFG) ? n : nq;
+    h->nb = (h->kind == kFG || h->kind == kH2O) ? h->l + ((nl + 3) & ~(size_t)3) : nullptr;
     h->T_cap = T;
     return H2O_OK;
 }

@@ -745,10 +745,15 @@ __global__ void __launch_bounds__(kThreadsW, kScoreCtasPerSM)
         // after it.
         float* wbias = S.colstat[grp][q];
         auto load_bias = [&](int uq, int ibq, float (&bq)[4]) {
+            const int iq0 = ibq * kT + 4 * lane;
+            const float* src = nbias + (size_t)uq * T + iq0;
+            if (iq0 + 3 < T && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+                // the four in one 16-byte load where the address allows
+                const float4 b4 = __ldg(reinterpret_cast<const float4*>(src));
+                bq[0] = b4.x; bq[1] = b4.y; bq[2] = b4.z; bq[3] = b4.w;
+            } else {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int iq = ibq * kT + 4 * lane + k;
-                bq[k] = iq < T ? nbias[(size_t)uq * T + iq] : -INFINITY;
+                for (int k = 0; k < 4; ++k) bq[k] = iq0 + k < T ? src[k] : -INFINITY;
             }
         };
         auto store_bias = [&](const float (&bq)[4]) {
